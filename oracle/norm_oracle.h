@@ -1,0 +1,45 @@
+/*
+ * norm_oracle.h -- declarations of the double-precision CPU oracle.
+ * TEST INFRASTRUCTURE ONLY; see norm_oracle.c.  Shares nothing with the CUDA
+ * library's headers.
+ */
+#ifndef NORM_ORACLE_H
+#define NORM_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_RELU = 1, ORACLE_ACT_GELU = 2 };
+
+void oracle_layernorm_fwd(int64_t rows, int64_t cols, const double *x,
+                          const double *w, const double *b, double eps,
+                          double *y, double *mean, double *rstd);
+void oracle_layernorm_bwd(int64_t rows, int64_t cols, const double *dy,
+                          const double *x, const double *w, double eps,
+                          double *dx, double *dw, double *db);
+void oracle_rmsnorm_fwd(int64_t rows, int64_t cols, const double *x,
+                        const double *w, double eps, double *y, double *rstd);
+void oracle_rmsnorm_bwd(int64_t rows, int64_t cols, const double *dy,
+                        const double *x, const double *w, double eps,
+                        double *dx, double *dw);
+void oracle_batchnorm_fwd(int64_t n, int64_t c, int64_t l, const double *x,
+                          const double *res, const double *w, const double *b,
+                          double eps, double momentum, int training, int act,
+                          double *running_mean, double *running_var,
+                          double *y, double *save_mean, double *save_rstd,
+                          uint32_t *act_mask, double *z_out);
+void oracle_batchnorm_bwd(int64_t n, int64_t c, int64_t l, const double *dy,
+                          const double *x, const double *res, const double *w,
+                          const double *b, const double *running_mean,
+                          const double *running_var, double eps, int training,
+                          int act, const uint32_t *act_mask, double *dx,
+                          double *dres, double *dw, double *db);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NORM_ORACLE_H */

@@ -1,0 +1,449 @@
+"""Pins that tie the CPU oracle to something other than itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError on failure.
+They are run against the committed oracle (test_oracle_pins.py) and against
+copies with a planted mistake (test_oracle_mutations.py), which every pin set
+must catch.
+
+What pins what:
+  * hand-worked fixtures in tests/golden/ (exact values derived on paper);
+  * closed forms and invariants: standardised rows/channels have mean 0 and
+    mean square var/(var+eps); LayerNorm and BatchNorm input gradients sum
+    to 0 and sum(dx*xhat) = rstd*sum(g*xhat)*eps/(var+eps); the RMSNorm gradient satisfies
+    sum(x*dx) = inv_rms*sum(g*x)*eps/(ms+eps); the running statistics follow
+    the EMA with the unbiased batch variance (numpy var with ddof=1);
+  * central finite differences of L = sum(dy * y) for every backward output;
+  * independent library routines: torch.nn.functional layer_norm / rms_norm /
+    batch_norm / gelu and torch autograd, all in float64 on the CPU.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+ACT = {"none": 0, "relu": 1, "gelu": 2}
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _close(a, b, rtol, atol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    err = np.abs(a - b)
+    bad = err > atol + rtol * np.abs(b)
+    assert not bad.any(), (f"{what}: max err {err.max():.3e} at {np.argmax(err)}; "
+                           f"got {a.ravel()[np.argmax(err)]}, want {b.ravel()[np.argmax(err)]}")
+
+
+def _central_diff(f, v, h):
+    """Gradient of scalar f at array v by central differences."""
+    g = np.zeros_like(v)
+    it = np.nditer(v, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        keep = v[i]
+        v[i] = keep + h
+        fp = f()
+        v[i] = keep - h
+        fm = f()
+        v[i] = keep
+        g[i] = (fp - fm) / (2 * h)
+    return g
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm
+# ---------------------------------------------------------------------------
+
+def pin_layernorm_golden(o):
+    d = json.load(open(os.path.join(GOLDEN, "layernorm_rmsnorm_hand_worked.json")))
+    for case in d["layernorm"]:
+        x = np.array([case["x"]])
+        w = None if case["w"] is None else np.array(case["w"])
+        b = None if case["b"] is None else np.array(case["b"])
+        y, mean, rstd = o.layernorm_fwd(x, w, b, eps=case["eps"])
+        _close(y[0], case["y"], 1e-15, 1e-15, "layernorm golden y")
+        _close(mean[0], case["mean"], 1e-15, 0, "layernorm golden mean")
+        _close(rstd[0], case["rstd"], 1e-15, 0, "layernorm golden rstd")
+
+
+def pin_layernorm_standardizes(o):
+    r = _rng(1)
+    x = r.normal(size=(6, 37)) * r.uniform(0.1, 5, size=(6, 1)) + r.uniform(-3, 3, size=(6, 1))
+    eps = 1e-3
+    y, mean, rstd = o.layernorm_fwd(x, None, None, eps=eps)
+    var = np.var(x, axis=1)
+    _close(y.mean(axis=1), np.zeros(6), 0, 1e-13, "row mean of standardised y")
+    _close((y * y).mean(axis=1), var / (var + eps), 1e-12, 0, "row mean square of y")
+    _close(mean, np.mean(x, axis=1), 1e-13, 1e-13, "saved mean")
+
+
+def pin_layernorm_vs_torch(o):
+    import torch
+    r = _rng(2)
+    x = r.normal(size=(7, 33)) * 2 + 0.5
+    w = 1 + 0.3 * r.normal(size=33)
+    b = 0.2 * r.normal(size=33)
+    y, _, rstd = o.layernorm_fwd(x, w, b, eps=1e-5)
+    yt = torch.nn.functional.layer_norm(torch.from_numpy(x), (33,), torch.from_numpy(w),
+                                        torch.from_numpy(b), eps=1e-5).numpy()
+    _close(y, yt, 1e-12, 1e-12, "layernorm vs torch")
+
+
+def pin_layernorm_bwd_fd(o):
+    r = _rng(3)
+    for rows, cols in ((3, 5), (2, 17)):
+        x = r.normal(size=(rows, cols))
+        w = 1 + 0.5 * r.normal(size=cols)
+        b = 0.5 * r.normal(size=cols)
+        dy = r.normal(size=(rows, cols))
+        eps = 1e-3
+        dx, dw, db = o.layernorm_bwd(dy, x, w, eps=eps)
+        loss = lambda: float((dy * o.layernorm_fwd(x, w, b, eps=eps)[0]).sum())
+        h = 1e-6
+        _close(dx, _central_diff(loss, x, h), 1e-6, 1e-7, "layernorm dx vs finite differences")
+        _close(dw, _central_diff(loss, w, h), 1e-6, 1e-7, "layernorm dw vs finite differences")
+        _close(db, _central_diff(loss, b, h), 1e-6, 1e-7, "layernorm db vs finite differences")
+
+
+def pin_layernorm_bwd_invariants(o):
+    # sum_j dx_j = 0 and sum_j dx_j*xhat_j = rstd * sum(g*xhat) * eps/(var+eps)
+    r = _rng(4)
+    x = r.normal(size=(5, 64)) * 3 + 1
+    w = 1 + 0.5 * r.normal(size=64)
+    dy = r.normal(size=(5, 64))
+    eps = 0.5
+    dx, _, _ = o.layernorm_bwd(dy, x, w, eps=eps)
+    var = x.var(1, keepdims=True)
+    rstd = 1 / np.sqrt(var + eps)
+    xhat = (x - x.mean(1, keepdims=True)) * rstd
+    scale = np.abs(dx).sum(1)
+    _close(dx.sum(1) / scale, np.zeros(5), 0, 1e-13, "sum of dx per row")
+    want = (rstd * ((dy * w) * xhat).sum(1, keepdims=True) * eps / (var + eps)).ravel()
+    _close((dx * xhat).sum(1), want, 1e-10, 1e-13, "sum of dx*xhat per row")
+
+
+def pin_layernorm_bwd_vs_torch(o):
+    import torch
+    r = _rng(5)
+    x = torch.tensor(r.normal(size=(4, 19)), requires_grad=True)
+    w = torch.tensor(1 + 0.4 * r.normal(size=19), requires_grad=True)
+    b = torch.tensor(0.3 * r.normal(size=19), requires_grad=True)
+    dy = r.normal(size=(4, 19))
+    y = torch.nn.functional.layer_norm(x, (19,), w, b, eps=1e-4)
+    y.backward(torch.from_numpy(dy))
+    dx, dw, db = o.layernorm_bwd(dy, x.detach().numpy(), w.detach().numpy(), eps=1e-4)
+    _close(dx, x.grad.numpy(), 1e-11, 1e-12, "layernorm dx vs torch autograd")
+    _close(dw, w.grad.numpy(), 1e-11, 1e-12, "layernorm dw vs torch autograd")
+    _close(db, b.grad.numpy(), 1e-11, 1e-12, "layernorm db vs torch autograd")
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm
+# ---------------------------------------------------------------------------
+
+def pin_rmsnorm_golden(o):
+    d = json.load(open(os.path.join(GOLDEN, "layernorm_rmsnorm_hand_worked.json")))
+    for case in d["rmsnorm"]:
+        y, rstd = o.rmsnorm_fwd(np.array([case["x"]]), np.array(case["w"]), eps=case["eps"])
+        _close(y[0], case["y"], 1e-15, 1e-15, "rmsnorm golden y")
+        _close(rstd[0], case["rstd"], 1e-15, 0, "rmsnorm golden rstd")
+
+
+def pin_rmsnorm_unit_rms(o):
+    r = _rng(6)
+    x = r.normal(size=(6, 41)) * r.uniform(0.1, 4, size=(6, 1)) + 0.3
+    eps = 1e-2
+    y, rstd = o.rmsnorm_fwd(x, None, eps=eps)
+    ms = np.mean(x * x, axis=1)
+    _close((y * y).mean(1), ms / (ms + eps), 1e-12, 0, "row mean square of RMS-normalised y")
+    # direction is preserved: y is a positive multiple of x
+    _close(y / x, np.broadcast_to((y / x)[:, :1], y.shape), 1e-12, 0, "y parallel to x")
+
+
+def pin_rmsnorm_vs_torch(o):
+    import torch
+    r = _rng(7)
+    x = r.normal(size=(5, 24)) * 1.5
+    w = 1 + 0.2 * r.normal(size=24)
+    y, _ = o.rmsnorm_fwd(x, w, eps=1e-6)
+    yt = torch.nn.functional.rms_norm(torch.from_numpy(x), (24,), torch.from_numpy(w),
+                                      eps=1e-6).numpy()
+    _close(y, yt, 1e-12, 1e-12, "rmsnorm vs torch")
+
+
+def pin_rmsnorm_bwd_fd(o):
+    r = _rng(8)
+    for rows, cols in ((3, 5), (2, 17)):
+        x = r.normal(size=(rows, cols))
+        w = 1 + 0.5 * r.normal(size=cols)
+        dy = r.normal(size=(rows, cols))
+        eps = 1e-3
+        dx, dw = o.rmsnorm_bwd(dy, x, w, eps=eps)
+        loss = lambda: float((dy * o.rmsnorm_fwd(x, w, eps=eps)[0]).sum())
+        _close(dx, _central_diff(loss, x, 1e-6), 1e-6, 1e-7, "rmsnorm dx vs finite differences")
+        _close(dw, _central_diff(loss, w, 1e-6), 1e-6, 1e-7, "rmsnorm dw vs finite differences")
+
+
+def pin_rmsnorm_bwd_invariant(o):
+    r = _rng(9)
+    x = r.normal(size=(4, 50))
+    w = 1 + 0.5 * r.normal(size=50)
+    dy = r.normal(size=(4, 50))
+    eps = 0.05
+    dx, _ = o.rmsnorm_bwd(dy, x, w, eps=eps)
+    ms = (x * x).mean(1)
+    rr = 1 / np.sqrt(ms + eps)
+    want = rr * ((dy * w) * x).sum(1) * eps / (ms + eps)
+    _close((x * dx).sum(1), want, 1e-11, 1e-13, "sum(x*dx) closed form")
+
+
+def pin_rmsnorm_bwd_vs_torch(o):
+    import torch
+    r = _rng(10)
+    x = torch.tensor(r.normal(size=(3, 21)), requires_grad=True)
+    w = torch.tensor(1 + 0.4 * r.normal(size=21), requires_grad=True)
+    dy = r.normal(size=(3, 21))
+    y = torch.nn.functional.rms_norm(x, (21,), w, eps=1e-5)
+    y.backward(torch.from_numpy(dy))
+    dx, dw = o.rmsnorm_bwd(dy, x.detach().numpy(), w.detach().numpy(), eps=1e-5)
+    _close(dx, x.grad.numpy(), 1e-11, 1e-12, "rmsnorm dx vs torch autograd")
+    _close(dw, w.grad.numpy(), 1e-11, 1e-12, "rmsnorm dw vs torch autograd")
+
+
+# ---------------------------------------------------------------------------
+# BatchNorm
+# ---------------------------------------------------------------------------
+
+def pin_batchnorm_golden(o):
+    d = json.load(open(os.path.join(GOLDEN, "batchnorm_hand_worked.json")))
+    for case in d["cases"]:
+        shape = tuple(case["shape"])
+        x = np.array(case["x"]).reshape(shape)
+        res = np.array(case["res"]).reshape(shape) if "res" in case else None
+        out = o.batchnorm_fwd(x, res, np.array(case["w"]), np.array(case["b"]),
+                              eps=case["eps"], momentum=case["momentum"],
+                              training=case.get("training", True), act=ACT[case["act"]],
+                              running_mean=np.array(case["running_mean_in"]),
+                              running_var=np.array(case["running_var_in"]),
+                              want_mask=case["act"] == "relu")
+        _close(out["y"].ravel(), case["y"], 1e-15, 1e-15, "batchnorm golden y")
+        _close(out["save_mean"], case["save_mean"], 1e-15, 0, "batchnorm golden mean")
+        _close(out["save_rstd"], case["save_rstd"], 1e-15, 0, "batchnorm golden rstd")
+        if "running_mean" in case:
+            _close(out["running_mean"], case["running_mean"], 1e-15, 0, "golden running_mean")
+            _close(out["running_var"], case["running_var"], 1e-15, 0, "golden running_var")
+        if "mask_words" in case:
+            assert list(out["mask"]) == case["mask_words"], f"mask {list(out['mask'])}"
+        if "dres_for_unit_dy" in case:
+            # dz = dy * ReLU'(z) with ReLU'(0) = 0, recomputed (no mask) and from the mask
+            for mask in (None, out["mask"]):
+                _, dres, _, _ = o.batchnorm_bwd(np.ones(shape), x, res, np.array(case["w"]),
+                                                np.array(case["b"]), eps=case["eps"],
+                                                training=case.get("training", True),
+                                                act=ACT[case["act"]], mask=mask)
+                _close(dres.ravel(), case["dres_for_unit_dy"], 0, 0, "golden ReLU gradient")
+
+
+def pin_batchnorm_standardizes_and_ema(o):
+    r = _rng(11)
+    n, c, l = 4, 3, 10
+    x = r.normal(size=(n, c, l)) * np.array([0.5, 2, 4])[None, :, None] + np.array([-1, 0, 3])[None, :, None]
+    eps = 1e-2
+    out = o.batchnorm_fwd(x, eps=eps, momentum=0.1, training=True,
+                          running_mean=np.zeros(c), running_var=np.ones(c))
+    y = out["y"]
+    xc = x.transpose(1, 0, 2).reshape(c, -1)
+    yc = y.transpose(1, 0, 2).reshape(c, -1)
+    var_b = np.var(xc, axis=1)
+    _close(yc.mean(1), np.zeros(c), 0, 1e-13, "channel mean of y")
+    _close((yc * yc).mean(1), var_b / (var_b + eps), 1e-12, 0, "channel mean square of y")
+    _close(out["running_mean"], 0.1 * np.mean(xc, axis=1), 1e-13, 1e-15, "running_mean EMA")
+    _close(out["running_var"], 0.9 + 0.1 * np.var(xc, axis=1, ddof=1), 1e-13, 0, "running_var EMA")
+
+
+def _torch_bn_forward(x, res, w, b, rm, rv, eps, momentum, training, act):
+    import torch
+    F = torch.nn.functional
+    xt = torch.from_numpy(x)
+    z = F.batch_norm(xt, rm, rv, torch.from_numpy(w), torch.from_numpy(b),
+                     training=training, momentum=momentum, eps=eps)
+    if res is not None:
+        z = z + torch.from_numpy(res)
+    if act == "relu":
+        return F.relu(z)
+    if act == "gelu":
+        return F.gelu(z, approximate="none")
+    return z
+
+
+def pin_batchnorm_vs_torch(o):
+    import torch
+    r = _rng(12)
+    n, c, l = 3, 4, 7
+    for training in (True, False):
+        for act in ("none", "relu", "gelu"):
+            for with_res in (False, True):
+                x = r.normal(size=(n, c, l)) * 1.7 + 0.4
+                res = r.normal(size=(n, c, l)) if with_res else None
+                w = 1 + 0.3 * r.normal(size=c)
+                b = 0.3 * r.normal(size=c)
+                rm0 = 0.2 * r.normal(size=c)
+                rv0 = 1 + 0.5 * r.uniform(size=c)
+                rm_t = torch.from_numpy(rm0.copy())
+                rv_t = torch.from_numpy(rv0.copy())
+                yt = _torch_bn_forward(x, res, w, b, rm_t, rv_t, 1e-5, 0.1, training, act).numpy()
+                out = o.batchnorm_fwd(x, res, w, b, eps=1e-5, momentum=0.1, training=training,
+                                      act=ACT[act], running_mean=rm0, running_var=rv0)
+                tag = f"batchnorm training={training} act={act} res={with_res}"
+                _close(out["y"], yt, 1e-12, 1e-12, tag + " y vs torch")
+                _close(out["running_mean"], rm_t.numpy(), 1e-13, 1e-15, tag + " running_mean")
+                _close(out["running_var"], rv_t.numpy(), 1e-13, 1e-15, tag + " running_var")
+
+
+def pin_gelu_values(o):
+    # eval mode with running_mean 0 and running_var + eps = 1 makes z = x exactly
+    z = np.array([-3.0, -1.0, 0.0, 0.5, 1.0, 2.0]).reshape(1, 1, 6)
+    out = o.batchnorm_fwd(z, eps=0.25, training=False, act=ACT["gelu"],
+                          running_mean=np.zeros(1), running_var=np.array([0.75]))
+    phi = np.array([0.5 * (1 + math.erf(v / math.sqrt(2))) for v in z.ravel()])
+    _close(out["y"].ravel(), z.ravel() * phi, 1e-15, 1e-16, "gelu = z * Phi(z)")
+    # Phi(1) = 0.8413447460685429 (standard normal table)
+    _close(out["y"].ravel()[4], 0.8413447460685429, 1e-15, 0, "gelu(1)")
+
+
+def pin_batchnorm_mask_layout(o):
+    # eval mode, z = x: mask bit (i, ch, j) must be x > 0 with the documented layout
+    n, c, l = 2, 3, 70
+    words = (l + 31) // 32
+    r = _rng(13)
+    x = r.choice([-1.0, 2.0], size=(n, c, l))
+    out = o.batchnorm_fwd(x, eps=0.25, training=False, act=ACT["relu"],
+                          running_mean=np.zeros(c), running_var=np.full(c, 0.75),
+                          want_mask=True)
+    want = np.zeros(n * c * words, dtype=np.uint32)
+    for i in range(n):
+        for ch in range(c):
+            for j in range(l):
+                if x[i, ch, j] > 0:
+                    want[(i * c + ch) * words + j // 32] |= np.uint32(1 << (j % 32))
+    assert (out["mask"] == want).all(), "ReLU mask layout"
+
+
+def _bn_inputs_away_from_kinks(r, n, c, l, act, with_res):
+    """Tiny BatchNorm inputs whose pre-activation stays 1e-3 away from 0 for
+    ReLU, so finite differences do not cross the kink."""
+    for _ in range(1000):
+        x = r.normal(size=(n, c, l)) * 1.3 + 0.2
+        res = r.normal(size=(n, c, l)) if with_res else None
+        w = 1 + 0.3 * r.normal(size=c)
+        b = 0.3 * r.normal(size=c)
+        if act != "relu":
+            return x, res, w, b
+        xc = x.transpose(1, 0, 2).reshape(c, -1)
+        mu = xc.mean(1)[None, :, None]
+        rs = (1 / np.sqrt(xc.var(1) + 1e-3))[None, :, None]
+        z = (x - mu) * rs * w[None, :, None] + b[None, :, None] + (res if with_res else 0)
+        if np.abs(z).min() > 1e-3:
+            return x, res, w, b
+    raise RuntimeError("no input away from the ReLU kink")
+
+
+def pin_batchnorm_bwd_fd(o):
+    r = _rng(14)
+    eps = 1e-3
+    for (n, c, l) in ((2, 3, 4), (3, 2, 5)):
+        for training in (True, False):
+            for act in ("none", "relu", "gelu"):
+                for with_res in (False, True):
+                    x, res, w, b = _bn_inputs_away_from_kinks(r, n, c, l, act, with_res)
+                    dy = r.normal(size=(n, c, l))
+                    rm = 0.1 * r.normal(size=c)
+                    rv = 1 + 0.2 * r.uniform(size=c)
+
+                    def loss():
+                        y = o.batchnorm_fwd(x, res, w, b, eps=eps, momentum=0.1,
+                                            training=training, act=ACT[act],
+                                            running_mean=rm, running_var=rv)["y"]
+                        return float((dy * y).sum())
+                    dx, dres, dw, db = o.batchnorm_bwd(dy, x, res, w, b, rm, rv, eps=eps,
+                                                       training=training, act=ACT[act])
+                    tag = f"batchnorm bwd training={training} act={act} res={with_res}"
+                    h = 1e-6
+                    _close(dx, _central_diff(loss, x, h), 1e-6, 1e-7, tag + " dx vs FD")
+                    _close(dw, _central_diff(loss, w, h), 1e-6, 1e-7, tag + " dw vs FD")
+                    _close(db, _central_diff(loss, b, h), 1e-6, 1e-7, tag + " db vs FD")
+                    if with_res:
+                        _close(dres, _central_diff(loss, res, h), 1e-6, 1e-7, tag + " dres vs FD")
+
+
+def pin_batchnorm_bwd_invariants(o):
+    # per channel: sum dx = 0 and sum dx*xhat = w*rstd*sum(dy*xhat)*eps/(var+eps)
+    r = _rng(15)
+    n, c, l = 5, 3, 9
+    x = r.normal(size=(n, c, l)) * 2 + 1
+    w = 1 + 0.3 * r.normal(size=c)
+    dy = r.normal(size=(n, c, l))
+    eps = 0.3
+    dx, _, _, _ = o.batchnorm_bwd(dy, x, None, w, None, eps=eps, training=True)
+    xc = x.transpose(1, 0, 2).reshape(c, -1)
+    var = xc.var(1, keepdims=True)
+    rstd = 1 / np.sqrt(var + eps)
+    xhat = (xc - xc.mean(1, keepdims=True)) * rstd
+    dyc = dy.transpose(1, 0, 2).reshape(c, -1)
+    dxc = dx.transpose(1, 0, 2).reshape(c, -1)
+    scale = np.abs(dxc).sum(1)
+    _close(dxc.sum(1) / scale, np.zeros(c), 0, 1e-13, "channel sum of dx")
+    want = (w[:, None] * rstd * (dyc * xhat).sum(1, keepdims=True) * eps / (var + eps)).ravel()
+    _close((dxc * xhat).sum(1), want, 1e-10, 1e-13, "channel sum of dx*xhat")
+
+
+def pin_batchnorm_bwd_vs_torch(o):
+    import torch
+    F = torch.nn.functional
+    r = _rng(16)
+    n, c, l = 3, 4, 6
+    for training in (True, False):
+        for act in ("none", "gelu"):
+            x = torch.tensor(r.normal(size=(n, c, l)) * 1.5, requires_grad=True)
+            res = torch.tensor(r.normal(size=(n, c, l)), requires_grad=True)
+            w = torch.tensor(1 + 0.3 * r.normal(size=c), requires_grad=True)
+            b = torch.tensor(0.3 * r.normal(size=c), requires_grad=True)
+            rm = 0.1 * r.normal(size=c)
+            rv = 1 + 0.2 * r.uniform(size=c)
+            z = F.batch_norm(x, torch.from_numpy(rm.copy()), torch.from_numpy(rv.copy()), w, b,
+                             training=training, momentum=0.1, eps=1e-5) + res
+            y = F.gelu(z, approximate="none") if act == "gelu" else z
+            dy = r.normal(size=(n, c, l))
+            y.backward(torch.from_numpy(dy))
+            dx, dres, dw, db = o.batchnorm_bwd(dy, x.detach().numpy(), res.detach().numpy(),
+                                               w.detach().numpy(), b.detach().numpy(), rm, rv,
+                                               eps=1e-5, training=training, act=ACT[act])
+            tag = f"batchnorm bwd vs torch training={training} act={act}"
+            _close(dx, x.grad.numpy(), 1e-10, 1e-12, tag + " dx")
+            _close(dres, res.grad.numpy(), 1e-10, 1e-12, tag + " dres")
+            _close(dw, w.grad.numpy(), 1e-10, 1e-12, tag + " dw")
+            _close(db, b.grad.numpy(), 1e-10, 1e-12, tag + " db")
+
+
+def pin_batchnorm_bwd_mask_matches_recompute(o):
+    r = _rng(17)
+    n, c, l = 3, 2, 45
+    x, res, w, b = _bn_inputs_away_from_kinks(r, n, c, l, "relu", True)
+    dy = r.normal(size=(n, c, l))
+    out = o.batchnorm_fwd(x, res, w, b, eps=1e-3, training=True, act=ACT["relu"], want_mask=True)
+    a = o.batchnorm_bwd(dy, x, res, w, b, eps=1e-3, training=True, act=ACT["relu"],
+                        mask=out["mask"])
+    bb = o.batchnorm_bwd(dy, x, res, w, b, eps=1e-3, training=True, act=ACT["relu"])
+    for u, v, name in zip(a, bb, ("dx", "dres", "dw", "db")):
+        _close(u, v, 1e-14, 1e-15, "mask-driven vs recomputed ReLU' " + name)
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,64 @@
+"""Plant a plausible mistake in a copy of the oracle's C source, build it, and
+check that at least one pin fails.  This shows the pins constrain every part
+of the oracle: a dropped term, a wrong sign, divisor or index, a swapped
+operand.  CPU only; the committed oracle is never modified."""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "norm_oracle.c")
+
+MUTATIONS = {
+    "ln_unbiased_variance": ("double var = ssd / (double)cols;",
+                             "double var = ssd / (double)(cols - 1);"),
+    "ln_eps_outside_root": ("double rs = 1.0 / sqrt(var + eps);",
+                            "double rs = 1.0 / (sqrt(var) + eps);"),
+    "ln_bwd_drops_xhat_term": ("- xhat * sum_gxhat / (double)cols);", ");"),
+    "ln_bwd_mean_term_divisor": ("rs * (g - sum_g / (double)cols",
+                                 "rs * (g - sum_g / (double)(cols - 1)"),
+    "ln_dw_uses_x_not_xhat": ("if (dw) dw[j] += dyr[j] * xhat;",
+                              "if (dw) dw[j] += dyr[j] * xr[j];"),
+    "ln_db_sign": ("if (db) db[j] += dyr[j];", "if (db) db[j] -= dyr[j];"),
+    "rms_fwd_drops_weight": ("y[r * cols + j] = xr[j] * rr * (w ? w[j] : 1.0);",
+                             "y[r * cols + j] = xr[j] * rr;"),
+    "rms_bwd_rstd_squared": ("xr[j] * rr * rr * rr * s", "xr[j] * rr * rr * s"),
+    "rms_bwd_term_sign": ("dx[r * cols + j] = rr * g - xr[j]",
+                          "dx[r * cols + j] = rr * g + xr[j]"),
+    "bn_normalise_unbiased": ("double var_biased = ssd / (double)m;",
+                              "double var_biased = ssd / (double)(m - 1);"),
+    "bn_running_var_biased": ("momentum * var_unbiased", "momentum * var_biased"),
+    "bn_momentum_swapped": ("(1.0 - momentum) * running_mean[ch] + momentum * mu",
+                            "momentum * running_mean[ch] + (1.0 - momentum) * mu"),
+    "bn_residual_after_activation": (
+        "y[e] = act_forward(act, z);",
+        "y[e] = act_forward(act, z - (res ? res[e] : 0.0)) + (res ? res[e] : 0.0);"),
+    "bn_gelu_grad_drops_pdf_term": ("return cdf + z * pdf;", "return cdf;"),
+    "bn_relu_grad_at_zero": ("case ORACLE_ACT_RELU: return z > 0.0 ? 1.0 : 0.0;",
+                             "case ORACLE_ACT_RELU: return z >= 0.0 ? 1.0 : 0.0;"),
+    "bn_mask_bit_order": ("|= (uint32_t)1u << (j % 32);", "|= (uint32_t)1u << (31 - j % 32);"),
+    "bn_dx_drops_mean_term": ("(dz - sum_dz / (double)m - xhat", "(dz - xhat"),
+    "bn_dw_not_xhat": ("sum_dz_xhat += dz * xhat;", "sum_dz_xhat += dz * x[e];"),
+    "bn_eval_dx_drops_weight": ("dx[e] = wc * rs * dz;", "dx[e] = rs * dz;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor must occur once: {old!r}"
+    mutated = tmp_path / "norm_oracle.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.build(src=str(mutated), out=str(tmp_path / "libmutant.so"), force=True)
+    o = oracle.Oracle(lib)
+    for pin in PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            return
+        except FloatingPointError:
+            return
+    pytest.fail(f"no pin caught the planted mistake {name}")
