@@ -1,0 +1,451 @@
+#!/usr/bin/env python
+"""Benchmark of libnorm's normalization hot path on GB300.
+
+One step = every row of the hot path, forward then backward, through the C ABI,
+on the full-size synthetic workloads:
+  * RMSNorm   bf16 [16384, 4096] (LLaMA-style, 8 outlier columns x20)
+  * LayerNorm fp16 [25216, 768]  (ViT-B tokens)
+  * BatchNorm2d fp32 [256, 64, 56, 56] + residual + ReLU, training (ResNet)
+  * BatchNorm2d fp16 [128, 512, 7, 7] + GELU(erf), training
+  * BatchNorm2d fp32 [256, 64, 56, 56] + residual + ReLU, eval (running statistics)
+L2 is flushed (a 512 MB write) before every call; each call is timed with CUDA
+events on the stream it is launched on.  value = algorithmic bytes of the step
+(every input read once, every output written once, saved statistics, ReLU mask
+bits) / summed device time, in GB/s.  Per-call times, GB/s and fraction of the
+measured HBM copy bandwidth are reported per workload.
+
+--impl reference times the CPU oracle (plain double-precision C, one core) on a
+bounded sample of the same workloads (a quarter of the rows or channels of each).
+
+Multi-GPU: one process per GPU (torchrun); each rank runs the same step on its
+own GPU (independent replicas, no collective on the data path); value sums
+the bytes of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd achieved HBM GB/s and % of GB300 peak per norm config; µs per call"
+UNIT = "GB/s"
+WORKLOAD = ("norm suite fwd+bwd: RMSNorm bf16 [16384,4096] + LayerNorm f16 [25216,768] + "
+            "BatchNorm2d f32 [256,64,56,56]+res+ReLU train + BatchNorm2d f16 [128,512,7,7]+GELU "
+            "train + BatchNorm2d f32 [256,64,56,56]+res+ReLU eval")
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20
+SAMPLE_FRACTION = 4   # the CPU oracle runs on 1/4 of the rows / channels of each workload
+
+
+# ---------------------------------------------------------------------------
+# multi-process plumbing (also exercised by the CPU tests with gloo)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(value: float) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate(local_ms: float, local_bytes: float, world: int) -> tuple[float, float]:
+    """(slowest rank's time in ms, whole-job GB/s) for weak scaling: every rank
+    moved local_bytes in its own time."""
+    slowest = reduce_max(local_ms)
+    return slowest, world * local_bytes / (slowest * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, ncu traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines: list[str] = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sms, maxs, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxs.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def ncu_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
+    kernel sources are unchanged since the capture (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    from normalization_layernorm_rmsnorm_gb300.build import source_digest
+    e = d.get(kernel)
+    if not e or e.get("source_digest") != source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# the GPU workload
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, world, rank, local):
+    import torch
+
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import workloads
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    nrm.load()
+    calls = workloads.build_calls(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one_step(record):
+        for c in calls:
+            flush.fill_(1.0)
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            c.fn()
+            e.record(stream)
+            if record is not None:
+                record.append((c, s, e))
+
+    for _ in range(args.warmup):
+        one_step(None)
+    nrm.nrm_sync_status()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    recs = []
+    for _ in range(args.steps):
+        one_step(recs)
+    torch.cuda.synchronize()
+    barrier()
+    clock_info = clocks.stop()
+    nrm.nrm_sync_status()
+    for c, s, e in recs:
+        c.times_ms.append(s.elapsed_time(e))
+
+    step_ms_local = sum(statistics.mean(c.times_ms) for c in calls)
+    step_bytes = sum(c.bytes for c in calls)
+    step_ms, value = aggregate(step_ms_local, step_bytes, world)
+
+    peak, peak_src = hbm_peak()
+    per = {}
+    for c in calls:
+        t = statistics.mean(c.times_ms)
+        gbs = c.bytes / (t * 1e-3) / 1e9
+        d = per.setdefault(c.workload, {})
+        d[f"{c.phase}_us"] = round(t * 1e3, 2)
+        d[f"{c.phase}_us_median"] = round(statistics.median(c.times_ms) * 1e3, 2)
+        d[f"{c.phase}_bytes"] = c.bytes
+        d[f"{c.phase}_gbs"] = round(gbs, 1)
+        d[f"{c.phase}_frac"] = round(gbs / peak, 4)
+    for d in per.values():
+        if "fwd_us" in d and "bwd_us" in d:
+            t = (d["fwd_us"] + d["bwd_us"]) * 1e-6
+            d["fwd_bwd_us"] = round(d["fwd_us"] + d["bwd_us"], 2)
+            d["fwd_bwd_gbs"] = round((d["fwd_bytes"] + d["bwd_bytes"]) / t / 1e9, 1)
+            d["fwd_bwd_frac"] = round((d["fwd_bytes"] + d["bwd_bytes"]) / t / 1e9 / peak, 4)
+
+    dom = max(calls, key=lambda c: statistics.mean(c.times_ms) / c.launches)
+    dom_t = statistics.mean(dom.times_ms)
+    achieved = dom.bytes / (dom_t * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dom.kernel),
+                "kernel": dom.kernel, "workload": dom.workload + " " + dom.phase,
+                "bytes_per_launch": dom.bytes, "launch_us": round(dom_t * 1e3, 2),
+                "peak_source": peak_src}
+
+    e2e = run_e2e(calls, args, stream, step_bytes, world)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator; shapes of the articles' models)",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                   "l2": "flushed (512 MB write) before every call",
+                   "timing": "CUDA events around each call on its stream; step = sum of calls"},
+        "roofline": roofline,
+        "gpu_launches": sum(c.launches for c in calls) * args.steps,
+        "e2e": e2e,
+        "clocks": clock_info,
+        "per_config": per,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(reps=24)
+    return line
+
+
+def run_e2e(calls, args, stream, step_bytes, world):
+    """Same step through host buffers: pinned inputs uploaded, every call, all
+    outputs downloaded, inside the timed region."""
+    import torch
+    ins, outs = [], []
+    seen = set()
+    for c in calls:
+        for t in c.inputs:
+            if id(t) not in seen:
+                seen.add(id(t))
+                ins.append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())))
+    seen = set()
+    for c in calls:
+        for t in c.outputs:
+            if id(t) not in seen:
+                seen.add(id(t))
+                outs.append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)))
+    h2d = sum(t.numel() * t.element_size() for t, _ in ins)
+    d2h = sum(t.numel() * t.element_size() for t, _ in outs)
+    steps = max(1, min(args.steps, 5))
+
+    def step():
+        for d, h in ins:
+            d.copy_(h, non_blocking=True)
+        for c in calls:
+            c.fn()
+        for d, h in outs:
+            h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    barrier()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    ms, gbs = aggregate(ms, step_bytes, world)
+    return {"value": round(gbs, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample():
+    """A bounded sample of each workload: the first 1/SAMPLE_FRACTION of the
+    rows (row norms) or channels (BatchNorm), as float64 arrays, with the
+    algorithmic bytes the same calls would move at the workload's dtypes."""
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    items = []
+    for name in ("rms_bf16_16384x4096", "ln_f16_25216x768"):
+        cfg = synth.CONFIGS[name]
+        rows = cfg.rows // SAMPLE_FRACTION
+        inp = synth.row_inputs(cfg, rows=rows)
+        es = 2 if cfg.dtype != "f32" else 4
+        a = {k: v.f64() for k, v in inp.items()}
+        if cfg.kind == "rmsnorm":
+            b = (2 * rows * cfg.cols * es + cfg.cols * es + rows * 4
+                 + 3 * rows * cfg.cols * es + rows * 4 + 2 * cfg.cols * es)
+        else:
+            b = (2 * rows * cfg.cols * es + 2 * cfg.cols * es + 2 * rows * 4
+                 + 3 * rows * cfg.cols * es + 2 * rows * 4 + 3 * cfg.cols * es)
+        items.append((name, cfg, a, b, f"first {rows} of {cfg.rows} rows"))
+    for name, training in (("bn_f32_256x64x56x56_res_relu", True), ("bn_f16_128x512x7x7_gelu", True),
+                           ("bn_f32_256x64x56x56_res_relu", False)):
+        cfg = synth.CONFIGS[name]
+        ch = cfg.c // SAMPLE_FRACTION
+        inp = synth.bn_inputs(cfg, channels=ch)
+        a = {k: v.f64() for k, v in inp.items()}
+        es = 2 if cfg.dtype != "f32" else 4
+        m = cfg.n * ch * cfg.l
+        words = cfg.n * ch * ((cfg.l + 31) // 32) * 4 if cfg.act == "relu" else 0
+        acts = 3 if cfg.residual else 2          # fwd: x, (res), y
+        bacts = 5 if cfg.residual else 3         # bwd: dy, x, dx, (dres)
+        if not cfg.residual:
+            bacts = 3
+        b = (acts * m * es + words + 8 * ch * 4) + (bacts * m * es + words + 6 * ch * 4)
+        tag = name + ("" if training else "_eval")
+        items.append((tag, cfg, a, b, f"first {ch} of {cfg.c} channels"))
+    return items
+
+
+def oracle_step(orc, items):
+    import oracle
+    acts = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "gelu": oracle.ACT_GELU}
+    for tag, cfg, a, _, _ in items:
+        if hasattr(cfg, "kind"):
+            if cfg.kind == "rmsnorm":
+                orc.rmsnorm_fwd(a["x"], a["w"], cfg.eps)
+                orc.rmsnorm_bwd(a["dy"], a["x"], a["w"], cfg.eps)
+            else:
+                orc.layernorm_fwd(a["x"], a["w"], a["b"], cfg.eps)
+                orc.layernorm_bwd(a["dy"], a["x"], a["w"], cfg.eps)
+        else:
+            training = not tag.endswith("_eval")
+            res = a.get("res")
+            f = orc.batchnorm_fwd(a["x"], res, a["w"], a["b"], cfg.eps, cfg.momentum, training,
+                                  acts[cfg.act], a["running_mean"], a["running_var"],
+                                  want_mask=cfg.act == "relu")
+            orc.batchnorm_bwd(a["dy"], a["x"], res, a["w"], a["b"], a["running_mean"],
+                              a["running_var"], cfg.eps, training, acts[cfg.act], mask=f["mask"])
+
+
+def cpu_baseline(reps=1):
+    import oracle
+    orc = oracle.get()
+    items = oracle_sample()
+    total = sum(i[3] for i in items)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(orc, items)
+    dt = time.perf_counter() - t0
+    return {"value": round(total * reps / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": "; ".join(f"{i[0]}: {i[4]}" for i in items) + " (fwd+bwd each, single-threaded C, fp64)"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    import oracle
+    orc = oracle.get()
+    items = oracle_sample()
+    total = sum(i[3] for i in items)
+    for _ in range(args.warmup):
+        oracle_step(orc, items)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(orc, items)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    value = total / (ms * 1e-3) / 1e9
+    sample = "; ".join(f"{i[0]}: {i[4]}" for i in items) + " (fwd+bwd each, single-threaded C, fp64)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded counter-based generator; shapes of the articles' models)",
+        "config": {"workload": WORKLOAD, "sample": f"1/{SAMPLE_FRACTION} of each workload"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("libnorm", "reference"), default="libnorm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        line = run_gpu(args, world, rank, local)
+    finally:
+        if world > 1 and dist.is_initialized():
+            dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

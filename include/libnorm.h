@@ -1,0 +1,243 @@
+/*
+ * libnorm.h -- C ABI of libnorm: forward and backward passes of LayerNorm,
+ * RMSNorm and BatchNorm (with fused residual add and activation) on one NVIDIA
+ * GB300 GPU (sm_103a), computed by hand-written CUDA kernels.
+ *
+ * Sources for what each call computes (web articles on the attorch
+ * normalization kernels):
+ *   [NK] "attorch如何实现LayerNorm、BatchNorm与RMSNorm？3种归一化Triton核代码全解析"
+ *   [AM] "如何用attorch.math快速开发自定义GPU算子：面向进阶开发者的算子融合实战指南"
+ *   [AF] "算子融合实战：attorch激活函数与Dropout融合核的完整实现原理"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.   Every pointer is a device pointer owned by the caller (cudaMalloc,
+ *           PyTorch, a pool...).  The library allocates nothing; it keeps only
+ *           per-device caches of device properties and kernel attributes.
+ *           Tensors are dense and row-major (C order).  Pointers must be aligned
+ *           to their element size; 16-byte alignment of every tensor (and a row
+ *           or segment length that is a multiple of 16 bytes) selects the
+ *           128-bit vector path, anything else a scalar path inside the same
+ *           kernels.  In-place use (y == x, dx == dy) is not supported.
+ * Streams.  Every call only enqueues work on `stream` (0 = legacy default
+ *           stream) and returns without synchronising.  Argument errors are
+ *           found on the host and returned before anything is enqueued.
+ * Dtypes.   `dt` is the storage type of the activations (x, y, dy, dx, residual,
+ *           dres).  Row-norm weight, bias and their gradients use the same `dt`;
+ *           BatchNorm weight, bias, running statistics and their gradients are
+ *           always float32.  Saved statistics are always float32.  All
+ *           arithmetic is float32; stores round to nearest even.
+ * Results.  For a fixed device, shape and set of pointers' alignment, every
+ *           output is bitwise reproducible from run to run (no atomics in any
+ *           reduction; all partial sums are combined in a fixed order).
+ * Errors.   NRM_ERR_INVALID_ARG for a bad pointer, size, flag or dtype;
+ *           NRM_ERR_UNSUPPORTED for a size beyond the limits below;
+ *           NRM_ERR_WORKSPACE when workspace_bytes is too small;
+ *           NRM_ERR_CUDA when a CUDA runtime call or launch fails;
+ *           NRM_ERR_TIMEOUT (from nrm_sync_status) when a kernel's bounded wait
+ *           on its own asynchronous copies gave up.  nrm_last_error_message()
+ *           gives a human-readable reason for the last failure on this thread.
+ * Limits.   rows, n*c*l < 2^40; cols < 2^31; a BatchNorm channel holds fewer
+ *           than 2^31 elements (n*l).
+ */
+#ifndef LIBNORM_H
+#define LIBNORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NRM_API __attribute__((visibility("default")))
+#else
+#define NRM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so callers need no CUDA header. */
+typedef struct CUstream_st *nrm_stream_t;
+
+typedef enum nrm_status {
+    NRM_OK = 0,
+    NRM_ERR_INVALID_ARG = 1,
+    NRM_ERR_UNSUPPORTED = 2,
+    NRM_ERR_WORKSPACE = 3,
+    NRM_ERR_CUDA = 4,
+    NRM_ERR_TIMEOUT = 5
+} nrm_status;
+
+typedef enum nrm_dtype { NRM_F32 = 0, NRM_F16 = 1, NRM_BF16 = 2 } nrm_dtype;
+
+/* Activation fused after BatchNorm ([NK] BatchNorm section, act_func; [AF]
+ * section "五、反向传播融合同样成立" for the derivative taken from the
+ * pre-activation input).  ReLU'(0) = 0.  GELU is the exact erf form
+ * z * Phi(z). */
+typedef enum nrm_act { NRM_ACT_NONE = 0, NRM_ACT_RELU = 1, NRM_ACT_GELU = 2 } nrm_act;
+
+/* Operations that need a workspace (for nrm_workspace_bytes). */
+typedef enum nrm_op { NRM_OP_LAYERNORM_BWD = 1, NRM_OP_RMSNORM_BWD = 2 } nrm_op;
+
+/* ------------------------------------------------------------------------ */
+/* LayerNorm over the last dimension                                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * nrm_layernorm_fwd -- [NK] section "LayerNorm：一个程序归一化一批行", forward
+ * steps 1-4; [AM] function table, calc_mean_and_inv_std and standardize.
+ * For each row r of x[rows, cols]:
+ *   mean = sum_j x_j / cols;  var = sum_j (x_j - mean)^2 / cols  (biased)
+ *   rstd = (var + eps)^(-1/2);  y_j = (x_j - mean) * rstd * w_j + b_j
+ * x, y: [rows, cols] in dt.  w, b: [cols] in dt, each may be NULL (1 and 0).
+ * mean, rstd: float32 [rows], each may be NULL (the "save_stats" option).
+ * rows >= 0 (0 is a no-op), cols >= 1, eps > 0.
+ */
+NRM_API nrm_status nrm_layernorm_fwd(const void *x, const void *w, const void *b, void *y,
+                             float *mean, float *rstd, int64_t rows, int64_t cols,
+                             float eps, nrm_dtype dt, nrm_stream_t stream);
+
+/*
+ * nrm_layernorm_bwd -- [NK] section "LayerNorm：一个程序归一化一批行", backward
+ * paragraph (the two per-row sums "term1" and "term2" in one launch), and
+ * section "三种核共享的工程技巧" (weight/bias gradients written per row block
+ * into an intermediate buffer, then summed).  With g = dy*w and
+ * xhat = (x - mean)*rstd:
+ *   dx = rstd * (g - sum(g)/cols - xhat * sum(g*xhat)/cols)
+ *   dw = sum over rows of dy*xhat;  db = sum over rows of dy
+ * dy, x, dx: [rows, cols] in dt.  w: [cols] in dt or NULL (1).  mean, rstd:
+ * float32 [rows] as written by nrm_layernorm_fwd.  dw, db: [cols] in dt, each
+ * may be NULL.  workspace: device memory of at least
+ * nrm_workspace_bytes(NRM_OP_LAYERNORM_BWD, rows, cols, dt) bytes, 16-byte
+ * aligned, used as scratch for the per-block dw/db partial sums (its contents
+ * on entry do not matter and are clobbered); may be NULL when dw and db are
+ * both NULL.  The call enqueues two kernels when dw or db is requested.
+ */
+NRM_API nrm_status nrm_layernorm_bwd(const void *dy, const void *x, const void *w,
+                             const float *mean, const float *rstd, void *dx,
+                             void *dw, void *db, int64_t rows, int64_t cols,
+                             nrm_dtype dt, void *workspace, size_t workspace_bytes,
+                             nrm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm over the last dimension                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * nrm_rmsnorm_fwd -- [NK] section "RMSNorm：去掉均值的极简版 LayerNorm": no mean
+ * is subtracted; output = input * inv_rms * weight with
+ *   inv_rms = (sum_j x_j^2 / cols + eps)^(-1/2).
+ * x, y: [rows, cols] in dt.  w: [cols] in dt or NULL (1).  There is no bias.
+ * rstd: float32 [rows] receives inv_rms, may be NULL.
+ */
+NRM_API nrm_status nrm_rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd,
+                           int64_t rows, int64_t cols, float eps, nrm_dtype dt,
+                           nrm_stream_t stream);
+
+/*
+ * nrm_rmsnorm_bwd -- [NK] RMSNorm section, backward sentence (the LayerNorm
+ * reduction reused with the row sum of input * output_grad * weight).  With
+ * g = dy*w and s = sum(g*x):
+ *   dx = inv_rms * g - x * inv_rms^3 * s / cols;  dw = sum over rows of dy*x*inv_rms
+ * Arguments as nrm_layernorm_bwd, with rstd = inv_rms from nrm_rmsnorm_fwd and
+ * NRM_OP_RMSNORM_BWD for the workspace size.
+ */
+NRM_API nrm_status nrm_rmsnorm_bwd(const void *dy, const void *x, const void *w,
+                           const float *rstd, void *dx, void *dw, int64_t rows,
+                           int64_t cols, nrm_dtype dt, void *workspace,
+                           size_t workspace_bytes, nrm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* BatchNorm over (batch, spatial) per channel, NCHW                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * nrm_batchnorm_fwd -- [NK] section "BatchNorm：按特征并行 + 激活融合" (statistics
+ * per channel over batch and spatial positions, accumulated block by block with
+ * an online mean/variance update; running statistics updated with momentum in
+ * training and read directly in inference; residual add and activation fused in
+ * the same kernel); [AM] section "实战二 Welford EMA 组合手写 BatchNorm 融合统计"
+ * (Welford update, EMA (1-momentum)*old + momentum*new).
+ * Per channel ch, over the M = n*l elements of x[:, ch, :]:
+ *   training:  mean = batch mean;  var = biased batch variance;
+ *              running_mean = (1-momentum)*running_mean + momentum*mean
+ *              running_var  = (1-momentum)*running_var  + momentum*var*M/(M-1)
+ *   eval:      mean = running_mean;  var = running_var (no update)
+ *   rstd = (var + eps)^(-1/2);  z = (x - mean)*rstd*w + b (+ residual);  y = act(z)
+ * x, residual, y: [n, c, l] in dt (NCHW with l = H*W; residual may be NULL).
+ * w, b: float32 [c] or NULL (1, 0).  running_mean, running_var: float32 [c],
+ * both NULL or both set in training (updated in place), both required in eval.
+ * save_mean, save_rstd: float32 [c] or NULL; training writes the batch mean and
+ * rstd, eval writes running_mean and (running_var+eps)^(-1/2); the backward
+ * reads them.
+ * act_mask: NULL or, for act == NRM_ACT_RELU, nrm_act_mask_words(n, c, l)
+ * uint32 words receiving bit (z > 0) per element: segment (i, ch) owns
+ * ceil(l/32) words starting at word (i*c + ch)*ceil(l/32) and element j of the
+ * segment is bit j%32 of word j/32 (unused high bits are 0).  It must be NULL
+ * for other activations.
+ * training requires M >= 2.  eps > 0, 0 <= momentum <= 1.
+ */
+NRM_API nrm_status nrm_batchnorm_fwd(const void *x, const void *residual, const float *w,
+                             const float *b, void *y, float *running_mean,
+                             float *running_var, float *save_mean, float *save_rstd,
+                             uint32_t *act_mask, int64_t n, int64_t c, int64_t l,
+                             float eps, float momentum, int training, nrm_act act,
+                             nrm_dtype dt, nrm_stream_t stream);
+
+/*
+ * nrm_batchnorm_bwd -- [NK] BatchNorm section, last sentences: with a fused
+ * activation the backward first recovers the pre-activation gradient, then
+ * computes the BatchNorm gradient.  With xhat = (x - save_mean)*save_rstd and
+ * z = xhat*w + b (+ residual):
+ *   dz   = dy * act'(z)   (ReLU: the act_mask bit when act_mask != NULL,
+ *                          otherwise z is recomputed from x and residual)
+ *   dres = dz;  db = sum dz;  dw = sum dz*xhat          (per channel)
+ *   training: dx = w*rstd*(dz - db/M - xhat*dw/M)
+ *   eval:     dx = w*rstd*dz
+ * dy, x, residual, dx, dres: [n, c, l] in dt.  residual is needed only to
+ * recompute z (GELU, or ReLU without a mask) when the forward used one.
+ * w, b: float32 [c] or NULL (1, 0), as in the forward.  save_mean, save_rstd:
+ * float32 [c] from nrm_batchnorm_fwd with the same `training` flag.
+ * act_mask: NULL, or the mask the forward wrote (ReLU only).  dres, dw, db may
+ * be NULL.
+ */
+NRM_API nrm_status nrm_batchnorm_bwd(const void *dy, const void *x, const void *residual,
+                             const float *w, const float *b, const float *save_mean,
+                             const float *save_rstd, const uint32_t *act_mask,
+                             void *dx, void *dres, float *dw, float *db, int64_t n,
+                             int64_t c, int64_t l, int training, nrm_act act,
+                             nrm_dtype dt, nrm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Helpers                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes the row-norm backward needs on the current device for
+ * [rows, cols] (it depends on the device's SM count).  Returns 0 for bad
+ * arguments or when no CUDA device is usable. */
+NRM_API size_t nrm_workspace_bytes(nrm_op op, int64_t rows, int64_t cols, nrm_dtype dt);
+
+/* Number of uint32 words of a BatchNorm ReLU mask for [n, c, l]. */
+NRM_API int64_t nrm_act_mask_words(int64_t n, int64_t c, int64_t l);
+
+/* Synchronises `stream`, then returns NRM_ERR_TIMEOUT if a kernel of this
+ * library on the current device reported a timed-out wait since the last call
+ * (and clears that report), NRM_ERR_CUDA if the stream reported an error, and
+ * NRM_OK otherwise. */
+NRM_API nrm_status nrm_sync_status(nrm_stream_t stream);
+
+/* Static string naming a status code. */
+NRM_API const char *nrm_status_str(nrm_status status);
+
+/* Human-readable reason for the last non-OK status returned on this thread
+ * ("" if none). */
+NRM_API const char *nrm_last_error_message(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+NRM_API int nrm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBNORM_H */

@@ -1,0 +1,458 @@
+// api.cu -- the C ABI of libnorm (declared in include/libnorm.h): argument
+// checks, dispatch by storage dtype and alignment, per-device caches and status
+// reporting.  The kernels live in rownorm_<dtype>.cu and batchnorm_<dtype>.cu.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+// Set by a kernel whose bounded wait gave up; read and cleared by nrm_sync_status.
+__device__ unsigned int g_nrm_error_word = 0;
+
+namespace nrm {
+
+namespace {
+
+thread_local char t_msg[512] = "";
+std::mutex g_mu;
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+bool g_dev_ok[kMaxDevices] = {};
+std::map<std::tuple<int, const void*, int, size_t>, int> g_occ;
+std::map<std::tuple<int, const void*, int, int, size_t>, int> g_clusters;
+std::map<std::tuple<int, const void*>, std::pair<size_t, bool>> g_prepared;
+
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+}  // namespace
+
+nrm_status fail(nrm_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+nrm_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return NRM_OK;
+    (void)cudaGetLastError();  // clear the launch error this call reports
+    return fail(NRM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+const DevInfo* dev_info() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_dev_ok[dev]) {
+        DevInfo d{};
+        d.device = dev;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        g_dev[dev] = d;
+        g_dev_ok[dev] = true;
+    }
+    return &g_dev[dev];
+}
+
+int cached_occupancy(const void* fn, int block, size_t smem) {
+    const DevInfo* d = dev_info();
+    if (!d) return 0;
+    const auto key = std::make_tuple(d->device, fn, block, smem);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, block, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_occ[key] = n;
+    return n;
+}
+
+nrm_status prepare_kernel(const void* fn, size_t dyn_smem, bool nonportable_cluster) {
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    const auto key = std::make_tuple(d->device, fn);
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto& st = g_prepared[key];
+    if (dyn_smem > st.first) {
+        // dynamic + static shared memory of a CTA may not exceed the opt-in limit
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+        if (e != cudaSuccess) return cuda_status(e, "cudaFuncGetAttributes");
+        const size_t cap = size_t(d->max_smem_optin) - fa.sharedSizeBytes;
+        if (dyn_smem > cap)
+            return fail(NRM_ERR_UNSUPPORTED, "kernel needs %zu bytes of shared memory, %zu available",
+                        dyn_smem, cap);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(cap));
+        if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(max dynamic smem)");
+        st.first = cap;
+    }
+    if (nonportable_cluster && !st.second) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(non-portable cluster)");
+        st.second = true;
+    }
+    return NRM_OK;
+}
+
+int max_active_clusters(const void* fn, int cs, int block, size_t smem) {
+    const DevInfo* d = dev_info();
+    if (!d) return 0;
+    const auto key = std::make_tuple(d->device, fn, cs, block, smem);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_clusters.find(key);
+        if (it != g_clusters.end()) return it->second;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(cs));
+    cfg.blockDim = dim3(unsigned(block));
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_clusters[key] = n;
+    return n;
+}
+
+nrm_status launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelExC(&cfg, fn, args), "dependent launch");
+}
+
+int row_bwd_max_partials(const DevInfo& d) { return 4 * d.sms; }
+
+}  // namespace nrm
+
+using namespace nrm;
+
+namespace {
+
+bool dtype_ok(nrm_dtype dt) { return dt == NRM_F32 || dt == NRM_F16 || dt == NRM_BF16; }
+size_t dsize(nrm_dtype dt) { return dt == NRM_F32 ? 4 : 2; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool all_aligned(std::initializer_list<const void*> ptrs, size_t a) {
+    for (const void* p : ptrs)
+        if (p && !aligned(p, a)) return false;
+    return true;
+}
+
+// rows*cols and friends: non-negative and below 2^40 elements, without overflow.
+bool size_ok(int64_t a, int64_t b, int64_t c = 1) {
+    if (a < 0 || b < 0 || c < 0) return false;
+    if (a == 0 || b == 0 || c == 0) return true;
+    if (a > kMaxElems / b) return false;
+    return a * b <= kMaxElems / c;
+}
+
+nrm_status check_eps(float eps) {
+    if (!(eps > 0.f) || !std::isfinite(eps)) return fail(NRM_ERR_INVALID_ARG, "eps must be finite and > 0");
+    return NRM_OK;
+}
+
+nrm_status check_rows(int64_t rows, int64_t cols, nrm_dtype dt) {
+    if (!dtype_ok(dt)) return fail(NRM_ERR_INVALID_ARG, "unknown dtype %d", int(dt));
+    if (rows < 0) return fail(NRM_ERR_INVALID_ARG, "rows must be >= 0");
+    if (cols < 1) return fail(NRM_ERR_INVALID_ARG, "cols must be >= 1");
+    if (cols >= (int64_t(1) << 31)) return fail(NRM_ERR_UNSUPPORTED, "cols must be < 2^31");
+    if (!size_ok(rows, cols)) return fail(NRM_ERR_UNSUPPORTED, "rows*cols must be < 2^40");
+    return NRM_OK;
+}
+
+template <typename F>
+nrm_status by_dtype(nrm_dtype dt, F&& f) {
+    switch (dt) {
+    case NRM_F32: return f(float{});
+    case NRM_F16: return f(__half{});
+    case NRM_BF16: return f(__nv_bfloat16{});
+    }
+    return fail(NRM_ERR_INVALID_ARG, "unknown dtype");
+}
+
+size_t row_ws_bytes(bool layernorm, int64_t cols) {
+    const DevInfo* d = dev_info();
+    if (!d) return 0;
+    return size_t(row_bwd_max_partials(*d)) * size_t(cols) * sizeof(float) * (layernorm ? 2 : 1);
+}
+
+nrm_status row_fwd_common(bool ln, const void* x, const void* w, const void* b, void* y, float* mean,
+                          float* rstd, int64_t rows, int64_t cols, float eps, nrm_dtype dt,
+                          nrm_stream_t stream) {
+    t_msg[0] = 0;
+    nrm_status st = check_rows(rows, cols, dt);
+    if (st != NRM_OK) return st;
+    if ((st = check_eps(eps)) != NRM_OK) return st;
+    if (rows > 0 && (!x || !y)) return fail(NRM_ERR_INVALID_ARG, "x and y must not be NULL");
+    const size_t es = dsize(dt);
+    if (!all_aligned({x, y, w, b}, es) || !all_aligned({mean, rstd}, 4))
+        return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    if (rows > 0 && x == y) return fail(NRM_ERR_INVALID_ARG, "in-place (y == x) is not supported");
+    const bool vec = (size_t(cols) * es) % 16 == 0 && all_aligned({x, y, w, b}, 16);
+    RowArgs a{};
+    a.x = x;
+    a.w = w;
+    a.b = ln ? b : nullptr;
+    a.y = y;
+    a.mean = ln ? mean : nullptr;
+    a.rstd = rstd;
+    a.rows = rows;
+    a.cols = int(cols);
+    a.eps = eps;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return by_dtype(dt, [&](auto tag) { return row_fwd<decltype(tag)>(a, ln, vec, s); });
+}
+
+nrm_status row_bwd_common(bool ln, const void* dy, const void* x, const void* w, const float* mean,
+                          const float* rstd, void* dx, void* dw, void* db, int64_t rows, int64_t cols,
+                          nrm_dtype dt, void* ws, size_t ws_bytes, nrm_stream_t stream) {
+    t_msg[0] = 0;
+    nrm_status st = check_rows(rows, cols, dt);
+    if (st != NRM_OK) return st;
+    if (rows > 0 && (!dy || !x || !dx || !rstd || (ln && !mean)))
+        return fail(NRM_ERR_INVALID_ARG, "dy, x, dx and the saved statistics must not be NULL");
+    const size_t es = dsize(dt);
+    if (!all_aligned({dy, x, dx, w, dw, db}, es) || !all_aligned({mean, rstd}, 4))
+        return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    if (rows > 0 && (dx == dy || dx == x))
+        return fail(NRM_ERR_INVALID_ARG, "in-place (dx == dy or x) is not supported");
+    const bool want = dw || (ln && db);
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    RowArgs a{};
+    if (want && rows > 0) {
+        const size_t need = row_ws_bytes(ln, cols);
+        if (!ws || !aligned(ws, 16)) return fail(NRM_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned");
+        if (ws_bytes < need)
+            return fail(NRM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
+        a.ws_dw = reinterpret_cast<float*>(ws);
+        a.ws_db = ln ? a.ws_dw + size_t(row_bwd_max_partials(*d)) * size_t(cols) : nullptr;
+    }
+    const bool vec = (size_t(cols) * es) % 16 == 0 && all_aligned({dy, x, dx, w}, 16);
+    a.x = x;
+    a.w = w;
+    a.dy = dy;
+    a.dx = dx;
+    a.mean_in = mean;
+    a.rstd_in = rstd;
+    a.dw = dw;
+    a.db = ln ? db : nullptr;
+    a.rows = rows;
+    a.cols = int(cols);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return by_dtype(dt, [&](auto tag) { return row_bwd<decltype(tag)>(a, ln, vec, s); });
+}
+
+nrm_status check_bn_shape(int64_t n, int64_t c, int64_t l, nrm_dtype dt, int training, nrm_act act) {
+    if (!dtype_ok(dt)) return fail(NRM_ERR_INVALID_ARG, "unknown dtype %d", int(dt));
+    if (n < 0 || c < 0 || l < 0) return fail(NRM_ERR_INVALID_ARG, "n, c, l must be >= 0");
+    if (!size_ok(n, c, l)) return fail(NRM_ERR_UNSUPPORTED, "n*c*l must be < 2^40");
+    if (!size_ok(n, l) || (n > 0 && l > 0 && n * l >= (int64_t(1) << 31)))
+        return fail(NRM_ERR_UNSUPPORTED, "a channel must hold fewer than 2^31 elements");
+    if (c * 16 >= (int64_t(1) << 31)) return fail(NRM_ERR_UNSUPPORTED, "c must be < 2^27");
+    if (act != NRM_ACT_NONE && act != NRM_ACT_RELU && act != NRM_ACT_GELU)
+        return fail(NRM_ERR_INVALID_ARG, "unknown activation %d", int(act));
+    if (training && c > 0 && n * l < 2)
+        return fail(NRM_ERR_INVALID_ARG, "training needs more than one value per channel (n*l >= 2)");
+    return NRM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+nrm_status nrm_layernorm_fwd(const void* x, const void* w, const void* b, void* y, float* mean,
+                             float* rstd, int64_t rows, int64_t cols, float eps, nrm_dtype dt,
+                             nrm_stream_t stream) {
+    return row_fwd_common(true, x, w, b, y, mean, rstd, rows, cols, eps, dt, stream);
+}
+
+nrm_status nrm_layernorm_bwd(const void* dy, const void* x, const void* w, const float* mean,
+                             const float* rstd, void* dx, void* dw, void* db, int64_t rows,
+                             int64_t cols, nrm_dtype dt, void* workspace, size_t workspace_bytes,
+                             nrm_stream_t stream) {
+    return row_bwd_common(true, dy, x, w, mean, rstd, dx, dw, db, rows, cols, dt, workspace,
+                          workspace_bytes, stream);
+}
+
+nrm_status nrm_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows,
+                           int64_t cols, float eps, nrm_dtype dt, nrm_stream_t stream) {
+    return row_fwd_common(false, x, w, nullptr, y, nullptr, rstd, rows, cols, eps, dt, stream);
+}
+
+nrm_status nrm_rmsnorm_bwd(const void* dy, const void* x, const void* w, const float* rstd, void* dx,
+                           void* dw, int64_t rows, int64_t cols, nrm_dtype dt, void* workspace,
+                           size_t workspace_bytes, nrm_stream_t stream) {
+    return row_bwd_common(false, dy, x, w, nullptr, rstd, dx, dw, nullptr, rows, cols, dt, workspace,
+                          workspace_bytes, stream);
+}
+
+nrm_status nrm_batchnorm_fwd(const void* x, const void* residual, const float* w, const float* b,
+                             void* y, float* running_mean, float* running_var, float* save_mean,
+                             float* save_rstd, uint32_t* act_mask, int64_t n, int64_t c, int64_t l,
+                             float eps, float momentum, int training, nrm_act act, nrm_dtype dt,
+                             nrm_stream_t stream) {
+    t_msg[0] = 0;
+    nrm_status st = check_bn_shape(n, c, l, dt, training, act);
+    if (st != NRM_OK) return st;
+    if ((st = check_eps(eps)) != NRM_OK) return st;
+    if (!(momentum >= 0.f && momentum <= 1.f)) return fail(NRM_ERR_INVALID_ARG, "momentum must be in [0, 1]");
+    const bool has_data = n > 0 && c > 0 && l > 0;
+    if (has_data && (!x || !y)) return fail(NRM_ERR_INVALID_ARG, "x and y must not be NULL");
+    if ((running_mean == nullptr) != (running_var == nullptr))
+        return fail(NRM_ERR_INVALID_ARG, "running_mean and running_var must be both NULL or both set");
+    if (!training && c > 0 && !running_mean)
+        return fail(NRM_ERR_INVALID_ARG, "eval mode needs running_mean and running_var");
+    if (act_mask && act != NRM_ACT_RELU) return fail(NRM_ERR_INVALID_ARG, "act_mask is only written for ReLU");
+    const size_t es = dsize(dt);
+    if (!all_aligned({x, residual, y}, es) ||
+        !all_aligned({w, b, running_mean, running_var, save_mean, save_rstd, act_mask}, 4))
+        return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    if (has_data && (x == y || (residual && residual == y)))
+        return fail(NRM_ERR_INVALID_ARG, "in-place is not supported");
+    if (c == 0) return NRM_OK;
+    const bool vec = (size_t(l) * es) % 16 == 0 && all_aligned({x, residual, y}, 16);
+    BnArgs a{};
+    a.x = x;
+    a.res = residual;
+    a.w = w;
+    a.b = b;
+    a.y = y;
+    a.rm = running_mean;
+    a.rv = running_var;
+    a.save_mean = save_mean;
+    a.save_rstd = save_rstd;
+    a.mask = act_mask;
+    a.n = n;
+    a.c = c;
+    a.l = l;
+    a.eps = eps;
+    a.momentum = momentum;
+    a.act = int(act);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return by_dtype(dt, [&](auto tag) { return bn_fwd<decltype(tag)>(a, training != 0, vec, s); });
+}
+
+nrm_status nrm_batchnorm_bwd(const void* dy, const void* x, const void* residual, const float* w,
+                             const float* b, const float* save_mean, const float* save_rstd,
+                             const uint32_t* act_mask, void* dx, void* dres, float* dw, float* db,
+                             int64_t n, int64_t c, int64_t l, int training, nrm_act act, nrm_dtype dt,
+                             nrm_stream_t stream) {
+    t_msg[0] = 0;
+    nrm_status st = check_bn_shape(n, c, l, dt, training, act);
+    if (st != NRM_OK) return st;
+    const bool has_data = n > 0 && c > 0 && l > 0;
+    if ((has_data && (!dy || !x || !dx)) || (c > 0 && (!save_mean || !save_rstd)))
+        return fail(NRM_ERR_INVALID_ARG, "dy, x, dx, save_mean and save_rstd must not be NULL");
+    if (act_mask && act != NRM_ACT_RELU) return fail(NRM_ERR_INVALID_ARG, "act_mask is only read for ReLU");
+    const size_t es = dsize(dt);
+    if (!all_aligned({dy, x, residual, dx, dres}, es) ||
+        !all_aligned({w, b, save_mean, save_rstd, act_mask, dw, db}, 4))
+        return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    if (has_data && (dx == dy || dx == x || (dres && (dres == dy || dres == x || dres == dx))))
+        return fail(NRM_ERR_INVALID_ARG, "in-place is not supported");
+    if (c == 0) return NRM_OK;
+    const bool vec = (size_t(l) * es) % 16 == 0 && all_aligned({dy, x, residual, dx, dres}, 16);
+    BnArgs a{};
+    a.x = x;
+    a.res = residual;
+    a.w = w;
+    a.b = b;
+    a.dy = dy;
+    a.dx = dx;
+    a.dres = dres;
+    a.dw = dw;
+    a.db = db;
+    a.mean_in = save_mean;
+    a.rstd_in = save_rstd;
+    a.mask_in = act_mask;
+    a.n = n;
+    a.c = c;
+    a.l = l;
+    a.act = int(act);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return by_dtype(dt, [&](auto tag) { return bn_bwd<decltype(tag)>(a, training != 0, vec, s); });
+}
+
+size_t nrm_workspace_bytes(nrm_op op, int64_t rows, int64_t cols, nrm_dtype dt) {
+    if (op != NRM_OP_LAYERNORM_BWD && op != NRM_OP_RMSNORM_BWD) return 0;
+    if (check_rows(rows, cols, dt) != NRM_OK) return 0;
+    return row_ws_bytes(op == NRM_OP_LAYERNORM_BWD, cols);
+}
+
+int64_t nrm_act_mask_words(int64_t n, int64_t c, int64_t l) {
+    if (n < 0 || c < 0 || l < 0) return 0;
+    return n * c * ((l + 31) / 32);
+}
+
+nrm_status nrm_sync_status(nrm_stream_t stream) {
+    t_msg[0] = 0;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e, "stream synchronize");
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_nrm_error_word, sizeof(word));
+    if (e != cudaSuccess) return cuda_status(e, "reading the device error word");
+    if (word != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_nrm_error_word, &zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_status(e, "clearing the device error word");
+        return fail(NRM_ERR_TIMEOUT, "a kernel's bounded wait gave up (code %u)", word);
+    }
+    return NRM_OK;
+}
+
+const char* nrm_status_str(nrm_status status) {
+    switch (status) {
+    case NRM_OK: return "NRM_OK";
+    case NRM_ERR_INVALID_ARG: return "NRM_ERR_INVALID_ARG";
+    case NRM_ERR_UNSUPPORTED: return "NRM_ERR_UNSUPPORTED";
+    case NRM_ERR_WORKSPACE: return "NRM_ERR_WORKSPACE";
+    case NRM_ERR_CUDA: return "NRM_ERR_CUDA";
+    case NRM_ERR_TIMEOUT: return "NRM_ERR_TIMEOUT";
+    }
+    return "NRM_ERR_UNKNOWN";
+}
+
+const char* nrm_last_error_message(void) { return t_msg; }
+
+int nrm_version(void) { return 100; }
+
+}  // extern "C"

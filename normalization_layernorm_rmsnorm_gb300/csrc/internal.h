@@ -1,0 +1,111 @@
+// internal.h -- host-side declarations shared by the C ABI (api.cu) and the
+// per-dtype kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "libnorm.h"
+
+namespace nrm {
+
+// Properties of the current device, read once per device.
+struct DevInfo {
+    int device;
+    int sms;
+    int max_smem_optin;   // bytes of dynamic shared memory a CTA may opt into
+};
+const DevInfo* dev_info();  // nullptr if no usable device
+
+// Records a human-readable reason for the status returned to the caller.
+nrm_status fail(nrm_status s, const char* fmt, ...);
+// Maps a CUDA error to NRM_ERR_CUDA with its message (NRM_OK for cudaSuccess).
+nrm_status cuda_status(cudaError_t e, const char* what);
+
+// Resident CTAs per SM of kernel `fn` (cached per device and kernel).
+int cached_occupancy(const void* fn, int block, size_t smem);
+// Opts `fn` into `dyn_smem` bytes of dynamic shared memory and, if asked, into
+// non-portable cluster sizes (once per device and kernel).
+nrm_status prepare_kernel(const void* fn, size_t dyn_smem, bool nonportable_cluster);
+// Clusters of `cs` CTAs of `fn` (kBnThreads threads, `smem` bytes) that fit at once.
+int max_active_clusters(const void* fn, int cs, int block, size_t smem);
+// Launch with programmatic stream serialisation (the kernel waits on its
+// predecessor with griddepcontrol.wait, so its launch overlaps the predecessor).
+nrm_status launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, cudaStream_t s);
+
+// Host copy of the device-side FastDiv.
+struct FastDivHost {
+    uint32_t d;
+    uint64_t m;
+};
+inline FastDivHost make_fast_div(uint32_t d) {
+    FastDivHost f;
+    f.d = d;
+    f.m = d <= 1 ? 0 : (~uint64_t(0)) / d + 1;
+    return f;
+}
+
+// ---------------------------------------------------------------------------
+// row norms (LayerNorm, RMSNorm)
+// ---------------------------------------------------------------------------
+struct RowArgs {
+    const void* x;
+    const void* w;
+    const void* b;
+    const void* dy;
+    void* y;
+    void* dx;
+    float* mean;          // forward outputs (nullable)
+    float* rstd;
+    const float* mean_in; // backward inputs
+    const float* rstd_in;
+    float* ws_dw;         // backward: per-CTA partial rows [P][cols] (nullable)
+    float* ws_db;
+    void* dw;             // backward outputs in the storage dtype (nullable)
+    void* db;
+    int64_t rows;
+    int cols;
+    float eps;
+};
+
+// Upper bound of per-CTA partial rows of the row-norm backward (P).
+int row_bwd_max_partials(const DevInfo& d);
+
+// One entry per storage dtype (defined in rownorm_<dtype>.cu).
+template <typename T> nrm_status row_fwd(const RowArgs& a, bool layernorm, bool vec,
+                                         cudaStream_t s);
+template <typename T> nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// BatchNorm
+// ---------------------------------------------------------------------------
+struct BnArgs {
+    const void* x;
+    const void* res;
+    const float* w;
+    const float* b;
+    void* y;
+    float* rm;
+    float* rv;
+    float* save_mean;
+    float* save_rstd;
+    uint32_t* mask;
+    const void* dy;
+    void* dx;
+    void* dres;
+    float* dw;
+    float* db;
+    const float* mean_in;
+    const float* rstd_in;
+    const uint32_t* mask_in;
+    int64_t n, c, l;
+    float eps;
+    float momentum;
+    int act;
+};
+
+template <typename T> nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, cudaStream_t s);
+template <typename T> nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, cudaStream_t s);
+
+}  // namespace nrm

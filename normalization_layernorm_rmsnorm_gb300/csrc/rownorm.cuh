@@ -1,0 +1,668 @@
+// rownorm.cuh -- LayerNorm and RMSNorm over the last dimension, forward and
+// backward, for one storage dtype T (included by rownorm_<dtype>.cu).
+//
+// What is computed follows the attorch normalization article
+// ("attorch如何实现LayerNorm、BatchNorm与RMSNorm？3种归一化Triton核代码全解析"):
+//   section "LayerNorm：一个程序归一化一批行" -- a program normalises a block of
+//     rows held whole in registers: row mean, variance from squared deviations
+//     of that mean, a reciprocal square root, optional stats, weight and bias;
+//     the backward needs two row sums and finishes a row in one launch;
+//   section "RMSNorm：去掉均值的极简版 LayerNorm" -- the same without the mean,
+//     backward with one row sum of input * output_grad * weight;
+//   section "三种核共享的工程技巧" -- fp32 accumulation, masks for ragged sizes,
+//     weight/bias gradients written per row block and then summed.
+//
+// GB300 design:
+//   * A row is held in registers by a group of TPR threads (a power of two from
+//     32 to 1024), each thread holding up to 4 (forward) or 2 (backward) raw
+//     16-byte vectors, unpacked to fp32 where used, so x is read from HBM once.
+//     Vector j of thread t is vector j*TPR + t of the row: a warp's accesses
+//     for one j are 512 contiguous bytes.
+//   * Group sums are warp butterflies, plus a named barrier and a fixed-order
+//     pass over shared memory when a group spans several warps.  The mean is
+//     subtracted from the registers before the variance sum (exact two-pass).
+//   * Grids are persistent: at most (resident CTAs per SM) x (SMs) CTAs, each
+//     looping over row groups with a stride, so each CTA's dw/db partials cover
+//     a fixed set of rows.
+//   * dw/db: each thread accumulates its columns over its rows in fp32
+//     registers; the CTA reduces its row groups in a fixed order and writes one
+//     partial row to the workspace; a second kernel (launched with programmatic
+//     dependent launch) sums the partial rows column-wise in a fixed order.  No
+//     atomics, so the result is bitwise reproducible.
+//   * The backward prefetches the next row of its group into registers while
+//     the current row is being reduced, so two rows per group are in flight.
+//   * Rows too wide for registers (more than 4096 vectors forward or 1024
+//     backward; elements on the unaligned path) take a two-pass "wide" kernel: Welford/Chan
+//     statistics in one pass over global memory, then a normalising pass.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace nrm {
+
+constexpr int kRowFwdVpt = 4;         // 16-byte vectors per thread, forward
+constexpr int kRowBwdVpt = 2;         // 16-byte vectors per thread, backward
+constexpr int kRowBwdBlock = 512;     // threads per backward CTA
+constexpr int kRowWideBlock = 1024;   // threads per CTA of the wide-row kernels
+constexpr int kRowMaxFwdTpr = 1024;
+constexpr int kRowMaxBwdTpr = 512;
+
+__host__ __device__ constexpr int row_fwd_block(int tpr) { return tpr > 256 ? tpr : 256; }
+
+// Sum of NV values over the TPR threads of row group `group`.  For TPR > 32
+// the per-warp sums meet in shared memory `buf` ([2][TPR/32][NV] floats for
+// this group), double-buffered by `phase`, behind named barrier 1 + group.
+template <int TPR, int NV>
+__device__ __forceinline__ void group_sum(float (&v)[NV], float* buf, int& phase, int group) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) v[k] = warp_sum(v[k]);
+    if constexpr (TPR > 32) {
+        constexpr int NW = TPR / 32;
+        const int lane = threadIdx.x & 31;
+        const int wig = (threadIdx.x % TPR) >> 5;
+        float* b = buf + phase * NW * NV;
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < NV; ++k) b[wig * NV + k] = v[k];
+        }
+        named_barrier(1 + group, TPR);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) s += b[w * NV + k];
+            v[k] = s;
+        }
+        phase ^= 1;
+    }
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ void load_raw(const T* p, Pack<T, VE>& pk, bool stream) {
+    if constexpr (VE > 1) {
+        pk.u = stream ? ld_stream_v4(p) : ld_cached_v4(p);
+    } else {
+        const typename Io<T>::bits_t* q = reinterpret_cast<const typename Io<T>::bits_t*>(p);
+        pk.b[0] = stream ? q[0] : __ldg(q);
+    }
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ float elem(const Pack<T, VE>& pk, int k) {
+    return Io<T>::load(pk.b[k]);
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ void load_param(const void* p, int vi, float (&out)[VE], float dflt) {
+    if (p) {
+        load_vec<T, VE, false>(reinterpret_cast<const T*>(p) + int64_t(vi) * VE, out);
+    } else {
+#pragma unroll
+        for (int k = 0; k < VE; ++k) out[k] = dflt;
+    }
+}
+
+// Row `row` of a [rows, cols] tensor as this thread's VPT packs (zero where
+// the vector lies past the end of the row).
+template <typename T, int TPR, int VPT, int VE>
+__device__ __forceinline__ void load_row(const T* base, int64_t row, int cols, int t,
+                                         Pack<T, VE> (&pk)[VPT]) {
+    const int nvec = cols / VE;
+    const T* r = base + row * cols;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int vi = j * TPR + t;
+        if (vi < nvec) {
+            load_raw<T, VE>(r + int64_t(vi) * VE, pk[j], true);
+        } else {
+            pk[j].u = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// forward, rows held in registers
+// ---------------------------------------------------------------------------
+template <typename T, bool LN, int TPR, int VE>
+__global__ void __launch_bounds__(row_fwd_block(TPR))
+row_fwd_kernel(const RowArgs a) {
+    constexpr int VPT = kRowFwdVpt;
+    constexpr int BLOCK = row_fwd_block(TPR);
+    constexpr int RPC = BLOCK / TPR;
+    constexpr int NW = TPR / 32;
+    __shared__ float red[RPC][2 * NW];
+
+    const int group = threadIdx.x / TPR;
+    const int t = threadIdx.x % TPR;
+    const int cols = a.cols;
+    const int nvec = cols / VE;
+    const float fcols = float(cols);
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    T* __restrict__ y = reinterpret_cast<T*>(a.y);
+    int phase = 0;
+
+    for (int64_t row = int64_t(blockIdx.x) * RPC + group; row < a.rows;
+         row += int64_t(gridDim.x) * RPC) {
+        Pack<T, VE> xp[VPT];
+        load_row<T, TPR, VPT, VE>(x, row, cols, t, xp);
+
+        float mu = 0.f;
+        float q[1] = {0.f};
+        if constexpr (LN) {
+            float s[1] = {0.f};
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+#pragma unroll
+                for (int k = 0; k < VE; ++k) s[0] += elem(xp[j], k);
+            group_sum<TPR, 1>(s, &red[group][0], phase, group);
+            mu = s[0] / fcols;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                if (j * TPR + t < nvec) {
+#pragma unroll
+                    for (int k = 0; k < VE; ++k) {
+                        const float d = elem(xp[j], k) - mu;
+                        q[0] = fmaf(d, d, q[0]);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+#pragma unroll
+                for (int k = 0; k < VE; ++k) q[0] = fmaf(elem(xp[j], k), elem(xp[j], k), q[0]);
+        }
+        group_sum<TPR, 1>(q, &red[group][0], phase, group);
+        const float rs = rsqrtf(q[0] / fcols + a.eps);
+
+        if (t == 0) {
+            if (LN && a.mean) a.mean[row] = mu;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+
+        T* yr = y + row * cols;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int vi = j * TPR + t;
+            if (vi < nvec) {
+                float wv[VE], bv[VE], o[VE];
+                load_param<T, VE>(a.w, vi, wv, 1.f);
+                if constexpr (LN) load_param<T, VE>(a.b, vi, bv, 0.f);
+#pragma unroll
+                for (int k = 0; k < VE; ++k) {
+                    const float xh = (elem(xp[j], k) - mu) * rs;
+                    o[k] = LN ? fmaf(xh, wv[k], bv[k]) : xh * wv[k];
+                }
+                store_vec<T, VE>(yr + int64_t(vi) * VE, o);
+            }
+        }
+    }
+}
+
+// Writes the CTA's partial row: the sum over its RPC row groups (in group
+// order) of each thread's per-column accumulators.  `part` holds
+// [RPC][TPR*VE] floats when RPC > 1.  Called by all threads of the CTA.
+template <int TPR, int VPT, int VE, int RPC>
+__device__ __forceinline__ void write_partial_row(const float (&acc)[VPT][VE], float* ws,
+                                                  float* part, int group, int t, int cols) {
+    const int nvec = cols / VE;
+    if constexpr (RPC == 1) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int vi = j * TPR + t;
+            if (vi < nvec) {
+#pragma unroll
+                for (int k = 0; k < VE; ++k) ws[vi * VE + k] = acc[j][k];
+            }
+        }
+    } else {
+        constexpr int BLOCK = TPR * RPC;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            if (j * TPR * VE >= cols) break;
+#pragma unroll
+            for (int k = 0; k < VE; ++k) part[group * TPR * VE + t * VE + k] = acc[j][k];
+            __syncthreads();
+            for (int i = threadIdx.x; i < TPR * VE; i += BLOCK) {
+                const int col = j * TPR * VE + i;
+                if (col < cols) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int g = 0; g < RPC; ++g) sum += part[g * TPR * VE + i];
+                    ws[col] = sum;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// backward, rows held in registers, next row prefetched; dw/db partials per CTA
+// ---------------------------------------------------------------------------
+template <typename T, bool LN, int TPR, int VE>
+__global__ void __launch_bounds__(kRowBwdBlock)
+row_bwd_kernel(const RowArgs a) {
+    constexpr int VPT = kRowBwdVpt;
+    constexpr int BLOCK = kRowBwdBlock;
+    constexpr int RPC = BLOCK / TPR;
+    constexpr int NW = TPR / 32;
+    constexpr int NV = LN ? 2 : 1;
+    __shared__ float red[RPC][2 * NW * NV];
+    __shared__ float part[RPC > 1 ? RPC : 1][RPC > 1 ? TPR * VE : 1];
+
+    const int group = threadIdx.x / TPR;
+    const int t = threadIdx.x % TPR;
+    const int cols = a.cols;
+    const int nvec = cols / VE;
+    const float fcols = float(cols);
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    const T* __restrict__ dy = reinterpret_cast<const T*>(a.dy);
+    T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
+    int phase = 0;
+
+    float accw[VPT][VE];
+    float accb[VPT][VE];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+        for (int k = 0; k < VE; ++k) accw[j][k] = accb[j][k] = 0.f;
+
+    // weight for this thread's columns, read once
+    float wv[VPT][VE];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int vi = j * TPR + t;
+        if (vi < nvec) {
+            load_param<T, VE>(a.w, vi, wv[j], 1.f);
+        } else {
+#pragma unroll
+            for (int k = 0; k < VE; ++k) wv[j][k] = 0.f;
+        }
+    }
+
+    const int64_t stride = int64_t(gridDim.x) * RPC;
+    int64_t row = int64_t(blockIdx.x) * RPC + group;
+    Pack<T, VE> xp[VPT], dp[VPT];
+    if (row < a.rows) {
+        load_row<T, TPR, VPT, VE>(x, row, cols, t, xp);
+        load_row<T, TPR, VPT, VE>(dy, row, cols, t, dp);
+    }
+    for (; row < a.rows; row += stride) {
+        // prefetch the next row of this group while this one is reduced
+        Pack<T, VE> xn[VPT], dn[VPT];
+        const int64_t nrow = row + stride;
+        if (nrow < a.rows) {
+            load_row<T, TPR, VPT, VE>(x, nrow, cols, t, xn);
+            load_row<T, TPR, VPT, VE>(dy, nrow, cols, t, dn);
+        }
+        const float rs = a.rstd_in[row];
+        const float mu = LN ? a.mean_in[row] : 0.f;
+
+        float s[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) s[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+#pragma unroll
+            for (int k = 0; k < VE; ++k) {
+                const float g = elem(dp[j], k) * wv[j][k];
+                if constexpr (LN) {
+                    const float xh = (elem(xp[j], k) - mu) * rs;
+                    s[0] += g;
+                    s[NV - 1] = fmaf(g, xh, s[NV - 1]);
+                } else {
+                    s[0] = fmaf(g, elem(xp[j], k), s[0]);
+                }
+            }
+        }
+        group_sum<TPR, NV>(s, &red[group][0], phase, group);
+
+        T* dxr = dx + row * cols;
+        const float c1 = s[0] / fcols;
+        const float c2 = LN ? s[NV - 1] / fcols : c1 * rs * rs;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int vi = j * TPR + t;
+            if (vi < nvec) {
+                float o[VE];
+#pragma unroll
+                for (int k = 0; k < VE; ++k) {
+                    const float xv = elem(xp[j], k);
+                    const float dv = elem(dp[j], k);
+                    const float g = dv * wv[j][k];
+                    if constexpr (LN) {
+                        const float xh = (xv - mu) * rs;
+                        o[k] = rs * (g - c1 - xh * c2);
+                        accw[j][k] = fmaf(dv, xh, accw[j][k]);
+                        accb[j][k] += dv;
+                    } else {
+                        o[k] = rs * (g - xv * c2);
+                        accw[j][k] = fmaf(dv, xv * rs, accw[j][k]);
+                    }
+                }
+                store_vec<T, VE>(dxr + int64_t(vi) * VE, o);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            xp[j] = xn[j];
+            dp[j] = dn[j];
+        }
+    }
+
+    // the column-sum kernel may be scheduled now; it waits for this grid
+    pdl_trigger();
+
+    // one partial row per CTA: fixed-order sum over the CTA's row groups
+    if (a.ws_dw)
+        write_partial_row<TPR, VPT, VE, RPC>(accw, a.ws_dw + int64_t(blockIdx.x) * cols, &part[0][0],
+                                             group, t, cols);
+    if constexpr (LN) {
+        if (a.ws_db)
+            write_partial_row<TPR, VPT, VE, RPC>(accb, a.ws_db + int64_t(blockIdx.x) * cols,
+                                                 &part[0][0], group, t, cols);
+    }
+}
+
+// dw/db[col] = sum over the P partial rows, in row order, rounded to T.
+template <typename T>
+__global__ void __launch_bounds__(256)
+row_colsum_kernel(const float* __restrict__ ws_dw, const float* __restrict__ ws_db, int P,
+                  int cols, T* dw, T* db) {
+    pdl_wait();
+    const float* ws = blockIdx.y == 0 ? ws_dw : ws_db;
+    T* out = blockIdx.y == 0 ? dw : db;
+    if (out == nullptr) return;
+    __shared__ float part[8][33];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int col = blockIdx.x * 32 + lane;
+    float s = 0.f;
+    if (col < cols) {
+#pragma unroll 8
+        for (int p = warp; p < P; p += 8) s += ws[int64_t(p) * cols + col];
+    }
+    part[warp][lane] = s;
+    __syncthreads();
+    if (warp == 0 && col < cols) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) tot += part[w][lane];
+        reinterpret_cast<typename Io<T>::bits_t*>(out)[col] = Io<T>::store(tot);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// wide rows: one CTA per row, two passes over global memory
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ Moments block_merge(Moments m, Moments* sm /* [33] */) {
+    warp_merge(m);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    if (lane == 0) sm[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Moments tot = sm[0];
+        for (int w = 1; w < int(blockDim.x >> 5); ++w) chan_merge(tot, sm[w].n, sm[w].mean, sm[w].m2);
+        sm[32] = tot;
+    }
+    __syncthreads();
+    const Moments r = sm[32];
+    __syncthreads();
+    return r;
+}
+
+template <int NV>
+__device__ __forceinline__ void block_sum(float (&v)[NV], float* sm /* [32*NV] */) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) v[k] = warp_sum(v[k]);
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k) sm[warp * NV + k] = v[k];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        float s = 0.f;
+        for (int w = 0; w < int(blockDim.x >> 5); ++w) s += sm[w * NV + k];
+        v[k] = s;
+    }
+    __syncthreads();
+}
+
+template <typename T, bool LN, int VE>
+__global__ void __launch_bounds__(kRowWideBlock)
+row_fwd_wide_kernel(const RowArgs a) {
+    __shared__ Moments msm[33];
+    __shared__ float ssm[32];
+    const int cols = a.cols;
+    const int nvec = cols / VE;
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    T* __restrict__ y = reinterpret_cast<T*>(a.y);
+    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+        const T* xr = x + row * cols;
+        float mu = 0.f, var;
+        if constexpr (LN) {
+            Moments m{0.f, 0.f, 0.f};
+            for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+                float v[VE];
+                load_vec<T, VE, false>(xr + int64_t(vi) * VE, v);
+                float s = 0.f;
+#pragma unroll
+                for (int k = 0; k < VE; ++k) s += v[k];
+                const float vm = s * (1.f / VE);
+                float q = 0.f;
+#pragma unroll
+                for (int k = 0; k < VE; ++k) q = fmaf(v[k] - vm, v[k] - vm, q);
+                chan_merge(m, float(VE), vm, q);
+            }
+            const Moments tot = block_merge(m, msm);
+            mu = tot.mean;
+            var = tot.m2 / float(cols);
+        } else {
+            float s[1] = {0.f};
+            for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+                float v[VE];
+                load_vec<T, VE, false>(xr + int64_t(vi) * VE, v);
+#pragma unroll
+                for (int k = 0; k < VE; ++k) s[0] = fmaf(v[k], v[k], s[0]);
+            }
+            block_sum<1>(s, ssm);
+            var = s[0] / float(cols);
+        }
+        const float rs = rsqrtf(var + a.eps);
+        if (threadIdx.x == 0) {
+            if (LN && a.mean) a.mean[row] = mu;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+        T* yr = y + row * cols;
+        for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+            float v[VE], wv[VE], bv[VE], o[VE];
+            load_vec<T, VE>(xr + int64_t(vi) * VE, v);
+            load_param<T, VE>(a.w, vi, wv, 1.f);
+            if constexpr (LN) load_param<T, VE>(a.b, vi, bv, 0.f);
+#pragma unroll
+            for (int k = 0; k < VE; ++k) {
+                const float xh = (v[k] - mu) * rs;
+                o[k] = LN ? fmaf(xh, wv[k], bv[k]) : xh * wv[k];
+            }
+            store_vec<T, VE>(yr + int64_t(vi) * VE, o);
+        }
+    }
+}
+
+template <typename T, bool LN, int VE>
+__global__ void __launch_bounds__(kRowWideBlock)
+row_bwd_wide_kernel(const RowArgs a) {
+    __shared__ float ssm[32 * 2];
+    const int cols = a.cols;
+    const int nvec = cols / VE;
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    const T* __restrict__ dy = reinterpret_cast<const T*>(a.dy);
+    T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
+    float* wsw = a.ws_dw ? a.ws_dw + int64_t(blockIdx.x) * cols : nullptr;
+    float* wsb = (LN && a.ws_db) ? a.ws_db + int64_t(blockIdx.x) * cols : nullptr;
+    // this CTA's partial rows; each column is always updated by the same thread
+    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+#pragma unroll
+        for (int k = 0; k < VE; ++k) {
+            if (wsw) wsw[vi * VE + k] = 0.f;
+            if (wsb) wsb[vi * VE + k] = 0.f;
+        }
+    }
+    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+        const T* xr = x + row * cols;
+        const T* dyr = dy + row * cols;
+        const float rs = a.rstd_in[row];
+        const float mu = LN ? a.mean_in[row] : 0.f;
+        constexpr int NV = LN ? 2 : 1;
+        float s[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) s[i] = 0.f;
+        for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+            float xv[VE], dv[VE], wv[VE];
+            load_vec<T, VE, false>(xr + int64_t(vi) * VE, xv);
+            load_vec<T, VE, false>(dyr + int64_t(vi) * VE, dv);
+            load_param<T, VE>(a.w, vi, wv, 1.f);
+#pragma unroll
+            for (int k = 0; k < VE; ++k) {
+                const float g = dv[k] * wv[k];
+                if constexpr (LN) {
+                    s[0] += g;
+                    s[NV - 1] = fmaf(g, (xv[k] - mu) * rs, s[NV - 1]);
+                } else {
+                    s[0] = fmaf(g, xv[k], s[0]);
+                }
+            }
+        }
+        block_sum<NV>(s, ssm);
+        const float c1 = s[0] / float(cols);
+        const float c2 = s[NV - 1] / float(cols);
+        T* dxr = dx + row * cols;
+        for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+            float xv[VE], dv[VE], wv[VE], o[VE];
+            load_vec<T, VE>(xr + int64_t(vi) * VE, xv);
+            load_vec<T, VE>(dyr + int64_t(vi) * VE, dv);
+            load_param<T, VE>(a.w, vi, wv, 1.f);
+#pragma unroll
+            for (int k = 0; k < VE; ++k) {
+                const float g = dv[k] * wv[k];
+                if constexpr (LN) {
+                    const float xh = (xv[k] - mu) * rs;
+                    o[k] = rs * (g - c1 - xh * c2);
+                    if (wsw) wsw[vi * VE + k] = fmaf(dv[k], xh, wsw[vi * VE + k]);
+                    if (wsb) wsb[vi * VE + k] += dv[k];
+                } else {
+                    o[k] = rs * (g - xv[k] * (c1 * rs * rs));
+                    if (wsw) wsw[vi * VE + k] = fmaf(dv[k], xv[k] * rs, wsw[vi * VE + k]);
+                }
+            }
+            store_vec<T, VE>(dxr + int64_t(vi) * VE, o);
+        }
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+template <typename T, bool LN, int VE>
+const void* row_fwd_fn(int tpr) {
+    switch (tpr) {
+    case 32: return (const void*)&row_fwd_kernel<T, LN, 32, VE>;
+    case 64: return (const void*)&row_fwd_kernel<T, LN, 64, VE>;
+    case 128: return (const void*)&row_fwd_kernel<T, LN, 128, VE>;
+    case 256: return (const void*)&row_fwd_kernel<T, LN, 256, VE>;
+    case 512: return (const void*)&row_fwd_kernel<T, LN, 512, VE>;
+    case 1024: return (const void*)&row_fwd_kernel<T, LN, 1024, VE>;
+    default: return (const void*)&row_fwd_wide_kernel<T, LN, VE>;
+    }
+}
+
+template <typename T, bool LN, int VE>
+const void* row_bwd_fn(int tpr) {
+    switch (tpr) {
+    case 32: return (const void*)&row_bwd_kernel<T, LN, 32, VE>;
+    case 64: return (const void*)&row_bwd_kernel<T, LN, 64, VE>;
+    case 128: return (const void*)&row_bwd_kernel<T, LN, 128, VE>;
+    case 256: return (const void*)&row_bwd_kernel<T, LN, 256, VE>;
+    case 512: return (const void*)&row_bwd_kernel<T, LN, 512, VE>;
+    default: return (const void*)&row_bwd_wide_kernel<T, LN, VE>;
+    }
+}
+
+// Threads per row group: the smallest power of two >= 32 holding the row in
+// `vpt` vectors per thread, or 0 for the wide-row kernel.
+inline int row_tpr(int nvec, int vpt, int max_tpr) {
+    int tpr = 32;
+    while (tpr * vpt < nvec && tpr < max_tpr) tpr *= 2;
+    return tpr * vpt < nvec ? 0 : tpr;
+}
+
+template <typename T>
+nrm_status row_fwd(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s) {
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    if (a.rows == 0) return NRM_OK;
+    const int ve = vec ? kVec<T> : 1;
+    const int tpr = row_tpr(a.cols / ve, kRowFwdVpt, kRowMaxFwdTpr);
+    const void* fn = layernorm ? (vec ? row_fwd_fn<T, true, kVec<T>>(tpr) : row_fwd_fn<T, true, 1>(tpr))
+                               : (vec ? row_fwd_fn<T, false, kVec<T>>(tpr) : row_fwd_fn<T, false, 1>(tpr));
+    const int block = tpr ? row_fwd_block(tpr) : kRowWideBlock;
+    const int rpc = tpr ? block / tpr : 1;
+    const int occ = cached_occupancy(fn, block, 0);
+    if (occ <= 0) return fail(NRM_ERR_CUDA, "row forward kernel cannot be resident");
+    const int64_t groups = (a.rows + rpc - 1) / rpc;
+    const int grid = int(groups < int64_t(occ) * d->sms ? groups : int64_t(occ) * d->sms);
+    RowArgs args = a;
+    void* kargs[] = {&args};
+    return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(block), kargs, 0, s), "row forward launch");
+}
+
+template <typename T>
+nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    const int ve = vec ? kVec<T> : 1;
+    const int tpr = row_tpr(a.cols / ve, kRowBwdVpt, kRowMaxBwdTpr);
+    const void* fn = layernorm ? (vec ? row_bwd_fn<T, true, kVec<T>>(tpr) : row_bwd_fn<T, true, 1>(tpr))
+                               : (vec ? row_bwd_fn<T, false, kVec<T>>(tpr) : row_bwd_fn<T, false, 1>(tpr));
+    const int block = tpr ? kRowBwdBlock : kRowWideBlock;
+    const int rpc = tpr ? block / tpr : 1;
+    const int occ = cached_occupancy(fn, block, 0);
+    if (occ <= 0) return fail(NRM_ERR_CUDA, "row backward kernel cannot be resident");
+    const int64_t groups = (a.rows + rpc - 1) / rpc;
+    int64_t p = int64_t(occ) * d->sms;
+    if (p > row_bwd_max_partials(*d)) p = row_bwd_max_partials(*d);
+    if (groups < p) p = groups;
+    const int P = int(p);
+    const bool want = a.dw || (layernorm && a.db);
+    if (!want) a.ws_dw = a.ws_db = nullptr;
+    if (P > 0) {
+        RowArgs args = a;
+        void* kargs[] = {&args};
+        nrm_status st = cuda_status(cudaLaunchKernel(fn, dim3(P), dim3(block), kargs, 0, s),
+                                    "row backward launch");
+        if (st != NRM_OK) return st;
+    }
+    if (!want) return NRM_OK;
+    const float* wsw = a.ws_dw;
+    const float* wsb = a.ws_db;
+    int P_ = P;
+    int cols = a.cols;
+    T* dw = reinterpret_cast<T*>(a.dw);
+    T* db = layernorm ? reinterpret_cast<T*>(a.db) : nullptr;
+    void* cargs[] = {&wsw, &wsb, &P_, &cols, &dw, &db};
+    return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((a.cols + 31) / 32, 2), dim3(256),
+                      cargs, s);
+}
+
+}  // namespace nrm
+
+#define NRM_INSTANTIATE_ROWNORM(T)                                                      \
+    template nrm_status nrm::row_fwd<T>(const nrm::RowArgs&, bool, bool, cudaStream_t); \
+    template nrm_status nrm::row_bwd<T>(nrm::RowArgs, bool, bool, cudaStream_t);

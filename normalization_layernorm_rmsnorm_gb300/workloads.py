@@ -1,0 +1,164 @@
+"""The bench's workloads as a list of C-ABI calls on device-resident inputs.
+
+Each Call wraps one libnorm entry point with its tensors, its algorithmic bytes
+(every input read once, every output written once, saved statistics, ReLU mask
+bits: the bytes that must cross HBM) and the kernels it launches.  Used by
+bench.py and by profile_case (the driver of the ncu captures).
+"""
+from __future__ import annotations
+
+
+def nbytes(*ts):
+    return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+class Call:
+    def __init__(self, workload, phase, kernel, fn, nbytes_, launches, inputs, outputs):
+        self.workload = workload
+        self.phase = phase
+        self.kernel = kernel
+        self.fn = fn
+        self.bytes = nbytes_
+        self.launches = launches
+        self.inputs = inputs      # device tensors a user would upload
+        self.outputs = outputs    # device tensors a user would download
+        self.times_ms: list[float] = []
+
+
+def build_calls(dev, names=None):
+    """The calls of one bench step (or only those of the workloads in `names`)."""
+    import torch
+
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+
+    calls = []
+
+    def f32(n):
+        return torch.empty(n, dtype=torch.float32, device=dev)
+
+    def want(name):
+        return names is None or name in names
+
+    # ---- RMSNorm bf16 [16384, 4096] ----
+    cfg = synth.CONFIGS["rms_bf16_16384x4096"]
+    if want(cfg.name):
+        calls += _rms(cfg, dev, f32)
+    cfg = synth.CONFIGS["ln_f16_25216x768"]
+    if want(cfg.name):
+        calls += _ln(cfg, dev, f32)
+    cfg = synth.CONFIGS["bn_f32_256x64x56x56_res_relu"]
+    if want(cfg.name) or want(cfg.name + "_eval"):
+        calls += [c for c in _bn_res_relu(cfg, dev, f32) if want(c.workload)]
+    cfg = synth.CONFIGS["bn_f16_128x512x7x7_gelu"]
+    if want(cfg.name):
+        calls += _bn_gelu(cfg, dev, f32)
+    return calls
+
+
+def _rms(cfg, dev, f32):
+    import torch
+
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    calls = []
+    inp = synth.row_inputs(cfg)
+    x, w, dy = (inp[k].torch(dev) for k in ("x", "w", "dy"))
+    y, dx, dw = torch.empty_like(x), torch.empty_like(x), torch.empty_like(w)
+    rstd = f32(cfg.rows)
+    ws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_RMSNORM_BWD, cfg.rows, cfg.cols, nrm.NRM_BF16) // 4)
+    calls.append(Call(cfg.name, "fwd", "row_fwd_kernel<bf16,rms>",
+                      lambda x=x, w=w, y=y, r=rstd, e=cfg.eps: nrm.nrm_rmsnorm_fwd(x, w, y, r, e),
+                      nbytes(x, y, w, rstd), 1, [x, w], [y, rstd]))
+    calls.append(Call(cfg.name, "bwd", "row_bwd_kernel<bf16,rms>+colsum",
+                      lambda: nrm.nrm_rmsnorm_bwd(dy, x, w, rstd, dx, dw, ws),
+                      nbytes(dy, x, w, rstd, dx, dw), 2, [dy], [dx, dw]))
+
+    return calls
+
+
+def _ln(cfg, dev, f32):
+    import torch
+
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    calls = []
+    inp = synth.row_inputs(cfg)
+    lx, lw, lb, ldy = (inp[k].torch(dev) for k in ("x", "w", "b", "dy"))
+    ly, ldx, ldw, ldb = torch.empty_like(lx), torch.empty_like(lx), torch.empty_like(lw), torch.empty_like(lb)
+    lmean, lrstd = f32(cfg.rows), f32(cfg.rows)
+    lws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_BWD, cfg.rows, cfg.cols, nrm.NRM_F16) // 4)
+    calls.append(Call(cfg.name, "fwd", "row_fwd_kernel<f16,ln>",
+                      lambda e=cfg.eps: nrm.nrm_layernorm_fwd(lx, lw, lb, ly, lmean, lrstd, e),
+                      nbytes(lx, lw, lb, ly, lmean, lrstd), 1, [lx, lw, lb], [ly, lmean, lrstd]))
+    calls.append(Call(cfg.name, "bwd", "row_bwd_kernel<f16,ln>+colsum",
+                      lambda: nrm.nrm_layernorm_bwd(ldy, lx, lw, lmean, lrstd, ldx, ldw, ldb, lws),
+                      nbytes(ldy, lx, lw, lmean, lrstd, ldx, ldw, ldb), 2, [ldy], [ldx, ldw, ldb]))
+
+    return calls
+
+
+def _bn_res_relu(cfg, dev, f32):
+    import torch
+
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    calls = []
+    inp = synth.bn_inputs(cfg)
+    bx, bres, bw, bb, bdy = (inp[k].torch(dev) for k in ("x", "res", "w", "b", "dy"))
+    brm, brv = inp["running_mean"].torch(dev), inp["running_var"].torch(dev)
+    n, c, l = cfg.n, cfg.c, cfg.l
+    by, bdx, bdres = torch.empty_like(bx), torch.empty_like(bx), torch.empty_like(bx)
+    bsm, bsr, bdw, bdb = f32(c), f32(c), f32(c), f32(c)
+    bmask = torch.empty(nrm.nrm_act_mask_words(n, c, l), dtype=torch.int32, device=dev)
+    calls.append(Call(cfg.name, "fwd", "bn_fwd_kernel<f32,train>",
+                      lambda: nrm.nrm_batchnorm_fwd(bx, bres, bw, bb, by, brm, brv, bsm, bsr, bmask,
+                                                    cfg.eps, cfg.momentum, True, "relu"),
+                      nbytes(bx, bres, by, bmask, bw, bb, bsm, bsr) + 2 * nbytes(brm, brv), 1,
+                      [bx, bres, bw, bb, brm, brv], [by, bmask, bsm, bsr, brm, brv]))
+    calls.append(Call(cfg.name, "bwd", "bn_bwd_kernel<f32,train>",
+                      lambda: nrm.nrm_batchnorm_bwd(bdy, bx, bres, bw, bb, bsm, bsr, bmask, bdx, bdres,
+                                                    bdw, bdb, True, "relu"),
+                      nbytes(bdy, bx, bmask, bw, bb, bsm, bsr, bdx, bdres, bdw, bdb), 1,
+                      [bdy], [bdx, bdres, bdw, bdb]))
+    erm = synth.store(0.3 * synth.normal(cfg.seed, 20, c), "f32", (c,)).torch(dev)
+    erv = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,)).torch(dev)
+    esm, esr = f32(c), f32(c)
+    eval_name = cfg.name + "_eval"
+    calls.append(Call(eval_name, "fwd", "bn_fwd_kernel<f32,eval>",
+                      lambda: nrm.nrm_batchnorm_fwd(bx, bres, bw, bb, by, erm, erv, esm, esr, bmask,
+                                                    cfg.eps, cfg.momentum, False, "relu"),
+                      nbytes(bx, bres, by, bmask, bw, bb, erm, erv, esm, esr), 1,
+                      [erm, erv], [by, bmask]))
+    calls.append(Call(eval_name, "bwd", "bn_bwd_kernel<f32,eval>",
+                      lambda: nrm.nrm_batchnorm_bwd(bdy, bx, bres, bw, bb, esm, esr, bmask, bdx, bdres,
+                                                    bdw, bdb, False, "relu"),
+                      nbytes(bdy, bx, bmask, bw, bb, esm, esr, bdx, bdres, bdw, bdb), 1,
+                      [], [bdx, bdres, bdw, bdb]))
+
+    return calls
+
+
+def _bn_gelu(cfg, dev, f32):
+    import torch
+
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    calls = []
+    inp = synth.bn_inputs(cfg)
+    gx, gw, gb, gdy = (inp[k].torch(dev) for k in ("x", "w", "b", "dy"))
+    grm, grv = inp["running_mean"].torch(dev), inp["running_var"].torch(dev)
+    c = cfg.c
+    gy, gdx = torch.empty_like(gx), torch.empty_like(gx)
+    gsm, gsr, gdw, gdb = f32(c), f32(c), f32(c), f32(c)
+    calls.append(Call(cfg.name, "fwd", "bn_fwd_kernel<f16,train>",
+                      lambda: nrm.nrm_batchnorm_fwd(gx, None, gw, gb, gy, grm, grv, gsm, gsr, None,
+                                                    cfg.eps, cfg.momentum, True, "gelu"),
+                      nbytes(gx, gy, gw, gb, gsm, gsr) + 2 * nbytes(grm, grv), 1,
+                      [gx, gw, gb, grm, grv], [gy, gsm, gsr, grm, grv]))
+    calls.append(Call(cfg.name, "bwd", "bn_bwd_kernel<f16,train>",
+                      lambda: nrm.nrm_batchnorm_bwd(gdy, gx, None, gw, gb, gsm, gsr, None, gdx, None,
+                                                    gdw, gdb, True, "gelu"),
+                      nbytes(gdy, gx, gw, gb, gsm, gsr, gdx, gdw, gdb), 1,
+                      [gdy], [gdx, gdw, gdb]))
+    return calls

@@ -1,0 +1,117 @@
+"""BatchNorm (training and eval, with fused residual and ReLU / GELU) through
+libnorm's C ABI against the CPU oracle, element by element: the full-size
+workloads (ResNet BatchNorm2d fp32 [256,64,56,56] + residual + ReLU, fp16
+[128,512,7,7] + GELU) and odd shapes that exercise every path (vector and
+scalar, clusters of 1 to 16 CTAs, channels larger than the shared-memory
+staging budget, ragged mask words)."""
+import numpy as np
+import pytest
+import torch
+
+import normalization_layernorm_rmsnorm_gb300 as nrm
+from normalization_layernorm_rmsnorm_gb300 import synth
+from parity_util import compare_bn, oracle_bn, run_bn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    nrm.load()
+
+
+@pytest.mark.parametrize("training", [True, False], ids=["train", "eval"])
+@pytest.mark.parametrize("name", ["bn_f32_256x64x56x56_res_relu", "bn_f16_128x512x7x7_gelu"])
+def test_bn_workloads_full_size(orc, name, training):
+    cfg = synth.CONFIGS[name]
+    inp = synth.bn_inputs(cfg)
+    if not training:
+        # eval reads running statistics: use non-trivial ones
+        c = cfg.c
+        inp["running_mean"] = synth.store(0.3 * synth.normal(cfg.seed, 20, c), "f32", (c,))
+        inp["running_var"] = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,))
+    use_mask = cfg.act == "relu"
+    got = run_bn(inp, cfg.dtype, cfg.eps, cfg.momentum, training, cfg.act, cfg.residual, use_mask)
+    want = oracle_bn(orc, inp, cfg.eps, cfg.momentum, training, cfg.act, cfg.residual)
+    compare_bn(got, want, cfg.dtype, training, cfg.act, f"{name} training={training}")
+
+
+ODD = [
+    # (n, c, l)
+    (2, 3, 1),
+    (3, 5, 49),
+    (4, 2, 70),
+    (1, 3, 300),
+    (5, 7, 33),
+    (8, 4, 64),
+    (64, 3, 3136),      # vector path, several CTAs per channel
+    (128, 2, 12544),    # fp32 channel of 6.4 MB: larger than the staging budget
+    (3, 1, 100003),     # one channel, odd length
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("shape", ODD, ids=[f"{n}x{c}x{l}" for n, c, l in ODD])
+def test_bn_odd_shapes(orc, dtype, shape):
+    n, c, l = shape
+    idx = ODD.index(shape)
+    acts = ["none", "relu", "gelu"]
+    for training in (True, False):
+        act = acts[(idx + int(training)) % 3]
+        with_res = (idx % 2 == 0)
+        cfg = synth.BnConfig("odd", n, c, l, dtype, 1e-5, 0.1, seed=200 + idx, act=act,
+                             residual=with_res, x_kind="offset_scale", w_std=0.2, b_std=0.2)
+        inp = synth.bn_inputs(cfg)
+        if not training:
+            inp["running_mean"] = synth.store(0.2 * synth.normal(cfg.seed, 20, c), "f32", (c,))
+            inp["running_var"] = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,))
+        use_mask = act == "relu" and idx % 3 != 0
+        got = run_bn(inp, dtype, cfg.eps, cfg.momentum, training, act, with_res, use_mask)
+        want = oracle_bn(orc, inp, cfg.eps, cfg.momentum, training, act, with_res)
+        compare_bn(got, want, dtype, training, act,
+                   f"bn {dtype} {shape} training={training} act={act} res={with_res} mask={use_mask}")
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu"])
+def test_bn_without_affine_or_running_stats(orc, act):
+    n, c, l = 6, 5, 200
+    cfg = synth.BnConfig("noaff", n, c, l, "f32", 1e-5, 0.1, seed=300, act=act, residual=True,
+                         x_kind="offset_scale")
+    inp = synth.bn_inputs(cfg)
+    x = inp["x"].torch("cuda")
+    res = inp["res"].torch("cuda")
+    dy = inp["dy"].torch("cuda")
+    y = torch.empty_like(x)
+    sm = torch.empty(c, device="cuda")
+    sr = torch.empty(c, device="cuda")
+    nrm.nrm_batchnorm_fwd(x, res, None, None, y, None, None, sm, sr, None, 1e-5, 0.1, True, act)
+    dx = torch.empty_like(x)
+    nrm.nrm_batchnorm_bwd(dy, x, res, None, None, sm, sr, None, dx, None, None, None, True, act)
+    nrm.nrm_sync_status()
+    want = oracle_bn(orc, inp, 1e-5, 0.1, True, act, True, with_affine=False)
+    yo = want["fwd"]["y"]
+    ok = ~want["amb"] if "amb" in want else np.ones_like(yo, dtype=bool)
+    err = np.abs(y.double().cpu().numpy() - yo)
+    assert (err[ok] <= 1e-5 + 1e-5 * np.abs(yo[ok])).all()
+    dxo = want["bwd"][0]
+    err = np.abs(dx.double().cpu().numpy() - dxo)
+    assert (err[ok] <= 1e-5 + 1e-5 * np.abs(dxo[ok])).all()
+
+
+def test_bn_running_stats_closed_form():
+    # from running_mean 0, running_var 1 and momentum m: rm = m*mean, rv = (1-m) + m*var_unbiased
+    n, c, l = 16, 3, 500
+    cfg = synth.BnConfig("ema", n, c, l, "f32", 1e-5, 0.1, seed=400, act="none", residual=False,
+                         x_kind="offset_scale")
+    inp = synth.bn_inputs(cfg)
+    x = inp["x"].torch("cuda")
+    y = torch.empty_like(x)
+    rm = torch.zeros(c, device="cuda")
+    rv = torch.ones(c, device="cuda")
+    nrm.nrm_batchnorm_fwd(x, None, None, None, y, rm, rv, None, None, None, 1e-5, 0.1, True, "none")
+    nrm.nrm_sync_status()
+    xc = inp["x"].f64().transpose(1, 0, 2).reshape(c, -1)
+    np.testing.assert_allclose(rm.double().cpu().numpy(), 0.1 * xc.mean(1), rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(rv.double().cpu().numpy(), 0.9 + 0.1 * xc.var(1, ddof=1), rtol=1e-5)
