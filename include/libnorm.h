@@ -119,6 +119,31 @@ NRM_API nrm_status nrm_layernorm_bwd(const void *dy, const void *x, const void *
                              nrm_dtype dt, void *workspace, size_t workspace_bytes,
                              nrm_stream_t stream);
 
+/*
+ * nrm_layernorm_bwd_noalloc -- nrm_layernorm_bwd without a workspace argument,
+ * for callers that cannot allocate device memory when they run the backward:
+ * code running under another framework's allocator (a plugin or custom op
+ * whose host runtime forbids or accounts every allocation), loops that must
+ * never enter the allocator after start-up (cudaMalloc can synchronise the
+ * device and stall), and C callers that were handed device pointers and have no
+ * allocator of their own.  The articles have no counterpart of this call; it is
+ * a property of this library's interface, not of the method.
+ * The dw/db partial rows live in a library-owned static device array of 8 MiB
+ * (2^21 floats), which every GPU that loads libnorm holds until the process
+ * exits.  cols must be <= 65536 (else NRM_ERR_UNSUPPORTED); the call allocates
+ * nothing.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current: make that first call before
+ * any stream capture.  All calls share the one array, so calls that overlap on
+ * the GPU (unordered streams) race on it; calls ordered on one stream are safe.
+ * Its contents need no initialisation: every call writes each partial value it
+ * reads.  Arguments, results and errors are otherwise those of
+ * nrm_layernorm_bwd.
+ */
+NRM_API nrm_status nrm_layernorm_bwd_noalloc(const void *dy, const void *x, const void *w,
+                                     const float *mean, const float *rstd, void *dx,
+                                     void *dw, void *db, int64_t rows, int64_t cols,
+                                     nrm_dtype dt, nrm_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* RMSNorm over the last dimension                                           */
 /* ------------------------------------------------------------------------ */

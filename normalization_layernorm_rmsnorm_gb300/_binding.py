@@ -23,7 +23,8 @@ NRM_OP_LAYERNORM_BWD, NRM_OP_RMSNORM_BWD = 1, 2
 ACTS = {"none": NRM_ACT_NONE, "relu": NRM_ACT_RELU, "gelu": NRM_ACT_GELU}
 
 # Every symbol the header declares (checked by the CPU tests).
-EXPORTS = ("nrm_layernorm_fwd", "nrm_layernorm_bwd", "nrm_rmsnorm_fwd", "nrm_rmsnorm_bwd",
+EXPORTS = ("nrm_layernorm_fwd", "nrm_layernorm_bwd", "nrm_layernorm_bwd_noalloc",
+           "nrm_rmsnorm_fwd", "nrm_rmsnorm_bwd",
            "nrm_batchnorm_fwd", "nrm_batchnorm_bwd", "nrm_workspace_bytes",
            "nrm_act_mask_words", "nrm_sync_status", "nrm_status_str",
            "nrm_last_error_message", "nrm_version")
@@ -55,6 +56,7 @@ def load(path: str | None = None):
     sig = {
         "nrm_layernorm_fwd": [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P],
         "nrm_layernorm_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, ctypes.c_size_t, _P],
+        "nrm_layernorm_bwd_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P],
         "nrm_rmsnorm_fwd": [_P, _P, _P, _P, _I64, _I64, _F, _I, _P],
         "nrm_rmsnorm_bwd": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, ctypes.c_size_t, _P],
         "nrm_batchnorm_fwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, _I,
@@ -138,6 +140,16 @@ def nrm_layernorm_bwd(dy, x, w, mean, rstd, dx, dw, db, workspace, stream=None):
                                     _ptr(dw), _ptr(db), rows, cols, _dtype_code(x), _ptr(workspace),
                                     ws_bytes, _stream(stream)),
            "nrm_layernorm_bwd")
+
+
+def nrm_layernorm_bwd_noalloc(dy, x, w, mean, rstd, dx, dw, db, stream=None):
+    """LayerNorm backward for callers that cannot allocate: no workspace; the
+    library's static device scratch holds the dw/db partial rows."""
+    rows, cols = _rows_cols(x)
+    _check(load().nrm_layernorm_bwd_noalloc(_ptr(dy), _ptr(x), _ptr(w), _ptr(mean), _ptr(rstd),
+                                            _ptr(dx), _ptr(dw), _ptr(db), rows, cols,
+                                            _dtype_code(x), _stream(stream)),
+           "nrm_layernorm_bwd_noalloc")
 
 
 def nrm_rmsnorm_fwd(x, w, y, rstd, eps, stream=None):

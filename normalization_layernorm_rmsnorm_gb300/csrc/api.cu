@@ -34,6 +34,8 @@ constexpr int64_t kMaxElems = int64_t(1) << 40;
 
 }  // namespace
 
+void clear_error() { t_msg[0] = 0; }
+
 nrm_status fail(nrm_status s, const char* fmt, ...) {
     va_list ap;
     va_start(ap, fmt);

@@ -18,6 +18,8 @@ struct DevInfo {
 };
 const DevInfo* dev_info();  // nullptr if no usable device
 
+// Clears this thread's last error message (at the start of an entry point).
+void clear_error();
 // Records a human-readable reason for the status returned to the caller.
 nrm_status fail(nrm_status s, const char* fmt, ...);
 // Maps a CUDA error to NRM_ERR_CUDA with its message (NRM_OK for cudaSuccess).
@@ -67,6 +69,7 @@ struct RowArgs {
     int64_t rows;
     int cols;
     float eps;
+    int max_partials;     // backward: cap on the partial rows P (0 = no cap)
 };
 
 // Upper bound of per-CTA partial rows of the row-norm backward (P).

@@ -638,6 +638,7 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     const int64_t groups = (a.rows + rpc - 1) / rpc;
     int64_t p = int64_t(occ) * d->sms;
     if (p > row_bwd_max_partials(*d)) p = row_bwd_max_partials(*d);
+    if (a.max_partials > 0 && p > a.max_partials) p = a.max_partials;
     if (groups < p) p = groups;
     const int P = int(p);
     const bool want = a.dw || (layernorm && a.db);
