@@ -32,6 +32,7 @@ class Guarded:
     def __init__(self, shape, dtype, offset=0):
         numel = int(np.prod(shape)) if len(shape) else 1
         es = torch.empty(0, dtype=dtype).element_size()
+        offset -= offset % es  # a view must start on an element boundary
         self.buf = torch.full((GUARD * 2 + numel * es + offset,), 0x5A, dtype=torch.uint8, device="cuda")
         start = GUARD + offset
         self.t = self.buf[start:start + numel * es].view(dtype).view(shape)
