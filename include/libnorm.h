@@ -195,6 +195,13 @@ NRM_API nrm_status nrm_rmsnorm_bwd(const void *dy, const void *x, const void *w,
  * save_mean, save_rstd: float32 [c] or NULL; training writes the batch mean and
  * rstd, eval writes running_mean and (running_var+eps)^(-1/2); the backward
  * reads them.
+ * workspace: device memory, 16-byte aligned, of at least
+ * nrm_batchnorm_workspace_bytes(n, c, l, dt) bytes; the call splits large
+ * channels over several CTAs, which meet there (per-channel counters reset by
+ * the call with an enqueued memset, and per-slice partial statistics).  It may
+ * be NULL when every channel fits one CTA; otherwise a NULL or short workspace
+ * returns NRM_ERR_WORKSPACE.  Calls that overlap on the GPU need separate
+ * workspaces.
  * act_mask: NULL or, for act == NRM_ACT_RELU, nrm_act_mask_words(n, c, l)
  * uint32 words receiving bit (z > 0) per element: segment (i, ch) owns
  * ceil(l/32) words starting at word (i*c + ch)*ceil(l/32) and element j of the
@@ -207,7 +214,8 @@ NRM_API nrm_status nrm_batchnorm_fwd(const void *x, const void *residual, const 
                              float *running_var, float *save_mean, float *save_rstd,
                              uint32_t *act_mask, int64_t n, int64_t c, int64_t l,
                              float eps, float momentum, int training, nrm_act act,
-                             nrm_dtype dt, nrm_stream_t stream);
+                             nrm_dtype dt, void *workspace, size_t workspace_bytes,
+                             nrm_stream_t stream);
 
 /*
  * nrm_batchnorm_bwd -- [NK] BatchNorm section, last sentences: with a fused
@@ -224,14 +232,15 @@ NRM_API nrm_status nrm_batchnorm_fwd(const void *x, const void *residual, const 
  * w, b: float32 [c] or NULL (1, 0), as in the forward.  save_mean, save_rstd:
  * float32 [c] from nrm_batchnorm_fwd with the same `training` flag.
  * act_mask: NULL, or the mask the forward wrote (ReLU only).  dres, dw, db may
- * be NULL.
+ * be NULL.  workspace: as for nrm_batchnorm_fwd.
  */
 NRM_API nrm_status nrm_batchnorm_bwd(const void *dy, const void *x, const void *residual,
                              const float *w, const float *b, const float *save_mean,
                              const float *save_rstd, const uint32_t *act_mask,
                              void *dx, void *dres, float *dw, float *db, int64_t n,
                              int64_t c, int64_t l, int training, nrm_act act,
-                             nrm_dtype dt, nrm_stream_t stream);
+                             nrm_dtype dt, void *workspace, size_t workspace_bytes,
+                             nrm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Helpers                                                                   */
@@ -241,6 +250,11 @@ NRM_API nrm_status nrm_batchnorm_bwd(const void *dy, const void *x, const void *
  * [rows, cols] (it depends on the device's SM count).  Returns 0 for bad
  * arguments or when no CUDA device is usable. */
 NRM_API size_t nrm_workspace_bytes(nrm_op op, int64_t rows, int64_t cols, nrm_dtype dt);
+
+/* Workspace bytes that suffice for nrm_batchnorm_fwd/bwd on [n, c, l] on the
+ * current device (it depends on the device's SM count).  Returns 0 for bad
+ * arguments or when no CUDA device is usable. */
+NRM_API size_t nrm_batchnorm_workspace_bytes(int64_t n, int64_t c, int64_t l, nrm_dtype dt);
 
 /* Number of uint32 words of a BatchNorm ReLU mask for [n, c, l]. */
 NRM_API int64_t nrm_act_mask_words(int64_t n, int64_t c, int64_t l);

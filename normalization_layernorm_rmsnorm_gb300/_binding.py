@@ -26,6 +26,7 @@ ACTS = {"none": NRM_ACT_NONE, "relu": NRM_ACT_RELU, "gelu": NRM_ACT_GELU}
 EXPORTS = ("nrm_layernorm_fwd", "nrm_layernorm_bwd", "nrm_layernorm_bwd_noalloc",
            "nrm_rmsnorm_fwd", "nrm_rmsnorm_bwd",
            "nrm_batchnorm_fwd", "nrm_batchnorm_bwd", "nrm_workspace_bytes",
+           "nrm_batchnorm_workspace_bytes",
            "nrm_act_mask_words", "nrm_sync_status", "nrm_status_str",
            "nrm_last_error_message", "nrm_version")
 
@@ -60,10 +61,11 @@ def load(path: str | None = None):
         "nrm_rmsnorm_fwd": [_P, _P, _P, _P, _I64, _I64, _F, _I, _P],
         "nrm_rmsnorm_bwd": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, ctypes.c_size_t, _P],
         "nrm_batchnorm_fwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, _I,
-                              _I, _I, _P],
+                              _I, _I, _P, ctypes.c_size_t, _P],
         "nrm_batchnorm_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I,
-                              _I, _I, _P],
+                              _I, _I, _P, ctypes.c_size_t, _P],
         "nrm_workspace_bytes": [_I, _I64, _I64, _I],
+        "nrm_batchnorm_workspace_bytes": [_I64, _I64, _I64, _I],
         "nrm_act_mask_words": [_I64, _I64, _I64],
         "nrm_sync_status": [_P],
         "nrm_status_str": [_I],
@@ -75,6 +77,7 @@ def load(path: str | None = None):
         f.argtypes = args
         f.restype = _I
     lib.nrm_workspace_bytes.restype = ctypes.c_size_t
+    lib.nrm_batchnorm_workspace_bytes.restype = ctypes.c_size_t
     lib.nrm_act_mask_words.restype = ctypes.c_int64
     lib.nrm_status_str.restype = ctypes.c_char_p
     lib.nrm_last_error_message.restype = ctypes.c_char_p
@@ -178,26 +181,42 @@ def _ncl(x):
     return n, c, l
 
 
+def _ws(workspace):
+    return 0 if workspace is None else workspace.numel() * workspace.element_size()
+
+
 def nrm_batchnorm_fwd(x, residual, w, b, y, running_mean, running_var, save_mean, save_rstd,
-                      act_mask, eps, momentum, training, act, stream=None):
+                      act_mask, eps, momentum, training, act, workspace, stream=None):
     n, c, l = _ncl(x)
     _check(load().nrm_batchnorm_fwd(_ptr(x), _ptr(residual), _ptr(w), _ptr(b), _ptr(y),
                                     _ptr(running_mean), _ptr(running_var), _ptr(save_mean),
                                     _ptr(save_rstd), _ptr(act_mask), n, c, l, eps, momentum,
                                     int(bool(training)), _act(act), _dtype_code(x),
-                                    _stream(stream)),
+                                    _ptr(workspace), _ws(workspace), _stream(stream)),
            "nrm_batchnorm_fwd")
 
 
 def nrm_batchnorm_bwd(dy, x, residual, w, b, save_mean, save_rstd, act_mask, dx, dres, dw, db,
-                      training, act, stream=None):
+                      training, act, workspace, stream=None):
     n, c, l = _ncl(x)
     _check(load().nrm_batchnorm_bwd(_ptr(dy), _ptr(x), _ptr(residual), _ptr(w), _ptr(b),
                                     _ptr(save_mean), _ptr(save_rstd), _ptr(act_mask), _ptr(dx),
                                     _ptr(dres), _ptr(dw), _ptr(db), n, c, l,
                                     int(bool(training)), _act(act), _dtype_code(x),
-                                    _stream(stream)),
+                                    _ptr(workspace), _ws(workspace), _stream(stream)),
            "nrm_batchnorm_bwd")
+
+
+def nrm_batchnorm_workspace_bytes(n: int, c: int, l: int, dtype_code: int) -> int:
+    return int(load().nrm_batchnorm_workspace_bytes(n, c, l, dtype_code))
+
+
+def batchnorm_workspace(x):
+    """A device workspace large enough for BatchNorm calls on x ([n, c, ...])."""
+    import torch
+    n, c, l = _ncl(x)
+    nbytes = nrm_batchnorm_workspace_bytes(n, c, l, _dtype_code(x))
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
 
 
 def nrm_workspace_bytes(op: int, rows: int, cols: int, dtype_code: int) -> int:

@@ -66,6 +66,12 @@ const DevInfo* dev_info() {
             (void)cudaGetLastError();
             return nullptr;
         }
+        void* err = nullptr;
+        if (cudaGetSymbolAddress(&err, g_nrm_error_word) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        d.err = static_cast<unsigned int*>(err);
         g_dev[dev] = d;
         g_dev_ok[dev] = true;
     }
@@ -331,7 +337,7 @@ nrm_status nrm_batchnorm_fwd(const void* x, const void* residual, const float* w
                              void* y, float* running_mean, float* running_var, float* save_mean,
                              float* save_rstd, uint32_t* act_mask, int64_t n, int64_t c, int64_t l,
                              float eps, float momentum, int training, nrm_act act, nrm_dtype dt,
-                             nrm_stream_t stream) {
+                             void* workspace, size_t workspace_bytes, nrm_stream_t stream) {
     t_msg[0] = 0;
     nrm_status st = check_bn_shape(n, c, l, dt, training, act);
     if (st != NRM_OK) return st;
@@ -369,15 +375,21 @@ nrm_status nrm_batchnorm_fwd(const void* x, const void* residual, const float* w
     a.eps = eps;
     a.momentum = momentum;
     a.act = int(act);
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    a.err = d->err;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return by_dtype(dt, [&](auto tag) { return bn_fwd<decltype(tag)>(a, training != 0, vec, s); });
+    if (workspace && !aligned(workspace, 16)) return fail(NRM_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    return by_dtype(dt, [&](auto tag) {
+        return bn_fwd<decltype(tag)>(a, training != 0, vec, workspace, workspace_bytes, s);
+    });
 }
 
 nrm_status nrm_batchnorm_bwd(const void* dy, const void* x, const void* residual, const float* w,
                              const float* b, const float* save_mean, const float* save_rstd,
                              const uint32_t* act_mask, void* dx, void* dres, float* dw, float* db,
                              int64_t n, int64_t c, int64_t l, int training, nrm_act act, nrm_dtype dt,
-                             nrm_stream_t stream) {
+                             void* workspace, size_t workspace_bytes, nrm_stream_t stream) {
     t_msg[0] = 0;
     nrm_status st = check_bn_shape(n, c, l, dt, training, act);
     if (st != NRM_OK) return st;
@@ -410,14 +422,27 @@ nrm_status nrm_batchnorm_bwd(const void* dy, const void* x, const void* residual
     a.c = c;
     a.l = l;
     a.act = int(act);
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    a.err = d->err;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return by_dtype(dt, [&](auto tag) { return bn_bwd<decltype(tag)>(a, training != 0, vec, s); });
+    if (workspace && !aligned(workspace, 16)) return fail(NRM_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    return by_dtype(dt, [&](auto tag) {
+        return bn_bwd<decltype(tag)>(a, training != 0, vec, workspace, workspace_bytes, s);
+    });
 }
 
 size_t nrm_workspace_bytes(nrm_op op, int64_t rows, int64_t cols, nrm_dtype dt) {
     if (op != NRM_OP_LAYERNORM_BWD && op != NRM_OP_RMSNORM_BWD) return 0;
     if (check_rows(rows, cols, dt) != NRM_OK) return 0;
     return row_ws_bytes(op == NRM_OP_LAYERNORM_BWD, cols);
+}
+
+size_t nrm_batchnorm_workspace_bytes(int64_t n, int64_t c, int64_t l, nrm_dtype dt) {
+    if (!dtype_ok(dt) || n < 0 || c < 0 || l < 0 || !size_ok(n, c, l)) return 0;
+    const DevInfo* d = dev_info();
+    if (!d) return 0;
+    return batchnorm_workspace_bytes(*d, c);
 }
 
 int64_t nrm_act_mask_words(int64_t n, int64_t c, int64_t l) {

@@ -4,64 +4,72 @@
 //
 // What is computed follows the attorch normalization article
 // ("attorch如何实现LayerNorm、BatchNorm与RMSNorm？3种归一化Triton核代码全解析"),
-// section "BatchNorm：按特征并行 + 激活融合": one program per channel; the
-// batch x spatial elements are visited block by block with an online
-// mean/variance update (no second pass over the input for the statistics);
-// running statistics follow an EMA with momentum in training and are read
-// directly in eval; the residual (pre_act_add) and the activation are applied
-// in the same kernel; the backward first undoes the activation.  The Welford
-// update and the EMA form are those of the math-helper article
-// ("如何用attorch.math快速开发自定义GPU算子：面向进阶开发者的算子融合实战指南",
-// section "实战二 Welford EMA 组合手写 BatchNorm 融合统计").
+// section "BatchNorm：按特征并行 + 激活融合": statistics per channel over the
+// batch x spatial elements, gathered block by block with an online update (one
+// pass over the input for the statistics); running statistics follow an EMA
+// with momentum in training and are read directly in eval; the residual
+// (pre_act_add) and the activation are applied in the same kernel; the backward
+// first undoes the activation.  The Welford update and the EMA form are those
+// of the math-helper article ("如何用attorch.math快速开发自定义GPU算子：面向进阶
+// 开发者的算子融合实战指南", section "实战二 Welford EMA 组合手写 BatchNorm 融合统计").
 //
 // GB300 design:
-//   * A channel (M = n*l elements, up to a few MB) is split over a thread-block
-//     cluster of `cs` CTAs (up to 16, co-scheduled on one GPC).  The channel's
-//     elements are numbered in blocks of 32 vectors (one vector per lane) within
-//     each (sample, channel) segment; CTA rank r owns a contiguous range of
-//     those blocks, and its warps take the blocks round-robin, kBnUnroll at a
-//     time so several 16-byte loads per lane are in flight.
-//   * Forward: the CTA keeps its slice of x in shared memory (up to ~220 KB) as
-//     it streams it in, and folds every vector into per-thread (count, mean, M2)
-//     with Chan's merge.  Warp, CTA and cluster partials are merged in a fixed
-//     order, the cluster step over distributed shared memory, so every CTA gets
-//     bit-identical statistics.  The normalise/affine/residual/activation pass
-//     then reads x from shared memory: x crosses HBM once.
-//   * Backward: dz = dy * act'(z) is formed once, written as dres, kept in
-//     shared memory (fp32), and summed (sum dz, sum dz*(x-mean)) with Kahan
-//     compensation; the cluster merges the sums in rank order; the dx pass reads
-//     dz from shared memory and x again (an L2 hit: the cluster's slice was
-//     read microseconds before).
-//   * A slice larger than the shared-memory budget keeps what fits and reads
-//     the rest from global memory twice.  Eval-mode forward needs no statistics
-//     and runs without a cluster.
+//   * A persistent, cooperative grid (every CTA resident at once).  A channel
+//     is cut into S contiguous slices, one per CTA; the grid holds a whole
+//     number k of channels (gridDim = k*S), so CTA i handles item i + r*gridDim
+//     in round r and the S slices of a channel always run in the same round on
+//     different CTAs.  A 3.2 MB fp32 channel uses S = 38 on 152 SMs (thread-
+//     block clusters, capped at 16 CTAs of one GPC, would leave a quarter of
+//     the SMs idle on this part).
+//   * L2 is the staging buffer: the statistics pass streams the slice from HBM
+//     with an L2 evict-last policy and the apply pass re-reads it from L2 with
+//     evict-first, so x crosses HBM once.  k is sized so that two rounds of
+//     slices stay well inside L2.
+//   * Statistics: per-thread sums of (x - K) and (x - K)^2 about the thread's
+//     first value K, turned into (n, mean, M2) and merged with Chan's formula
+//     across warps and the CTA.  The S slices of a channel meet through the
+//     caller's workspace: each CTA publishes its partial and signals a
+//     per-channel counter (release); readers wait (acquire, bounded by a 2 s
+//     timer) for all S, then merge the S partials in one fixed order, so every
+//     CTA gets bit-identical statistics.
+//   * Latency hiding: a CTA streams and publishes round r+1's statistics
+//     before it waits for round r's channel, so the other slices' arrival is
+//     overlapped with HBM traffic.  Every CTA publishes round r+1 before it
+//     waits on round r, so the waits cannot form a cycle.
+//   * Backward: dz = dy * act'(z) (ReLU from the mask bits, GELU by recomputing
+//     z), dres, and the channel sums sum(dz) and sum(dz*x) accumulated without
+//     rounding loss (error-free products and Kahan sums in fp32, combined in
+//     double); sum(dz*(x - mean)) = sum(dz*x) - mean*sum(dz) in double.  The dx
+//     pass re-reads dy and x from L2.
+//   * Streams read once carry an L2 evict-first policy.
 #pragma once
-
-#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace nrm {
 
-namespace cg = cooperative_groups;
-
 constexpr int kBnThreads = 512;
 constexpr int kBnWarps = kBnThreads / 32;
-constexpr int kBnUnroll = 4;
+constexpr int kBnUnroll = 8;        // blocks per warp in flight when streaming one tensor from HBM
+constexpr int kBnUnroll2 = 6;       // ... two tensors
+constexpr int kBnUnrollL2 = 4;      // ... when re-reading data that sits in L2
+constexpr uint64_t kBnWaitLimitNs = 2000000000ull;  // 2 s
 
-// Geometry of one launch (device copy).
+// Geometry and schedule of one launch (device copy).
 struct BnGeom {
-    int64_t c;            // channels
-    int lv;               // vectors per (sample, channel) segment = l / VE
-    int nbs;              // blocks of 32 vectors per segment
-    int words;            // ReLU-mask words per segment = ceil(l / 32)
-    FastDiv div_nbs;      // division by nbs
-    uint32_t nb_chan;     // blocks per channel = n * nbs
-    int cs;               // CTAs per channel
-    uint32_t stage_blocks;// blocks a CTA keeps in shared memory
-    float inv_m;          // 1 / (n*l)
-    float inv_m1;         // 1 / (n*l - 1)
+    int64_t c;             // channels
+    int lv;                // vectors per (sample, channel) segment = l / VE
+    int nbs;               // blocks of 32 vectors per segment
+    int words;             // ReLU-mask words per segment = ceil(l / 32)
+    FastDiv div_nbs;       // division by nbs
+    uint32_t nb_chan;      // blocks per channel = n * nbs
+    int S;                 // slices (CTAs) per channel
+    int rounds;            // items per CTA: item = blockIdx.x + r * gridDim.x
+    float inv_m;           // 1 / (n*l)
+    float inv_m1;          // 1 / (n*l - 1)
+    uint32_t* counters;    // [c] arrivals per channel, zero at launch (S > 1)
+    void* partials;        // [c][S]: float4 (n, mean, m2, 0) forward; double2 backward
 };
 
 __device__ __forceinline__ float act_forward(int act, float z) {
@@ -99,12 +107,15 @@ __device__ __forceinline__ BlockPos block_pos(const BnGeom& g, uint32_t bi, int 
 }
 
 template <typename T, int VE>
-__device__ __forceinline__ void raw_load(const T* base, int64_t vec_index, Pack<T, VE>& pk) {
+__device__ __forceinline__ void raw_load_pol(const T* base, int64_t vec_index, Pack<T, VE>& pk,
+                                             uint64_t pol) {
     const T* p = base + vec_index * VE;
     if constexpr (VE > 1) {
-        pk.u = ld_stream_v4(p);
+        pk.u = ld_v4_policy(p, pol);
+    } else if constexpr (sizeof(T) == 4) {
+        pk.b[0] = ld_u32_policy(p, pol);
     } else {
-        pk.b[0] = *reinterpret_cast<const typename Io<T>::bits_t*>(p);
+        pk.b[0] = ld_u16_policy(p, pol);
     }
 }
 
@@ -115,22 +126,18 @@ __device__ __forceinline__ void unpack(const Pack<T, VE>& pk, float (&v)[VE]) {
 }
 
 template <typename T, int VE>
-__device__ __forceinline__ void stage_put(unsigned char* stage, uint32_t slot, const Pack<T, VE>& pk) {
+__device__ __forceinline__ void store_vec_pol(T* p, const float (&in)[VE], uint64_t pol) {
+    Pack<T, VE> pk;
+#pragma unroll
+    for (int k = 0; k < VE; ++k) pk.b[k] = Io<T>::store(in[k]);
     if constexpr (VE > 1) {
-        reinterpret_cast<uint4*>(stage)[slot] = pk.u;
+        st_v4_policy(p, pk.u, pol);
     } else {
-        reinterpret_cast<typename Io<T>::bits_t*>(stage)[slot] = pk.b[0];
+        *reinterpret_cast<typename Io<T>::bits_t*>(p) = pk.b[0];
     }
 }
 
-template <typename T, int VE>
-__device__ __forceinline__ void stage_get(const unsigned char* stage, uint32_t slot, Pack<T, VE>& pk) {
-    if constexpr (VE > 1) {
-        pk.u = reinterpret_cast<const uint4*>(stage)[slot];
-    } else {
-        pk.b[0] = reinterpret_cast<const typename Io<T>::bits_t*>(stage)[slot];
-    }
-}
+
 
 // Packs bit k of `nib` (element lane*VE + k of the block) into the segment's
 // mask words and stores them.  Called by the whole warp.
@@ -156,173 +163,264 @@ __device__ __forceinline__ void store_mask_bits(uint32_t* mask, const BnGeom& g,
 // The VE mask bits of this lane's vector.
 template <int VE>
 __device__ __forceinline__ uint32_t load_mask_bits(const uint32_t* mask, const BnGeom& g,
-                                                   const BlockPos& p, int lane) {
+                                                   const BlockPos& p, int lane, uint64_t pol) {
     const int e = lane * VE;  // element offset within the block's 32*VE elements
-    const uint32_t word = mask[p.seg * g.words + int64_t(p.bs) * VE + (e >> 5)];
+    const uint32_t word = ld_u32_policy(mask + p.seg * g.words + int64_t(p.bs) * VE + (e >> 5), pol);
     return (word >> (e & 31)) & ((1u << VE) - 1u);
 }
+
+__device__ __forceinline__ void slice_range(const BnGeom& g, int s, uint32_t& b0, uint32_t& b1) {
+    b0 = uint32_t(uint64_t(s) * g.nb_chan / uint32_t(g.S));
+    b1 = uint32_t(uint64_t(s + 1) * g.nb_chan / uint32_t(g.S));
+}
+
+
+
+// One value per lane of each of this thread's vectors, accumulated as sums of
+// (x - K) and (x - K)^2 about the thread's first value K.
+struct ShiftedSums {
+    float k = 0.f, s = 0.f, q = 0.f;
+    int n = 0;
+    template <int VE>
+    __device__ __forceinline__ void add(const float (&v)[VE]) {
+        if (n == 0) k = v[0];
+#pragma unroll
+        for (int i = 0; i < VE; ++i) {
+            const float d = v[i] - k;
+            s += d;
+            q = fmaf(d, d, q);
+        }
+        n += VE;
+    }
+    __device__ __forceinline__ Moments moments() const {
+        Moments m;
+        m.n = float(n);
+        m.mean = n ? k + s / float(n) : 0.f;
+        m.m2 = n ? fmaxf(q - s * (s / float(n)), 0.f) : 0.f;
+        return m;
+    }
+};
+
+// Bounded wait until `count` CTAs have signalled `counter`; false on timeout.
+__device__ __forceinline__ bool wait_count(const uint32_t* counter, uint32_t count) {
+    if (ld_acquire_u32(counter) >= count) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire_u32(counter) >= count) return true;
+        if (global_timer_ns() - t0 > kBnWaitLimitNs) return false;
+    }
+}
+
+// Rounds of one CTA: item = blockIdx.x + r * gridDim.x, channel item / S,
+// slice item % S.
+struct Rounds {
+    const BnGeom& g;
+    int64_t items;
+    __device__ explicit Rounds(const BnGeom& g_) : g(g_), items(g_.c * g_.S) {}
+    __device__ bool valid(int r) const {
+        return r < g.rounds && int64_t(blockIdx.x) + int64_t(r) * gridDim.x < items;
+    }
+    __device__ void range(int r, int64_t& ch, int& s, uint32_t& b0, uint32_t& b1) const {
+        const int64_t it = int64_t(blockIdx.x) + int64_t(r) * gridDim.x;
+        ch = it / g.S;
+        s = int(it % g.S);
+        slice_range(g, s, b0, b1);
+    }
+};
+
 
 // ---------------------------------------------------------------------------
 // forward
 // ---------------------------------------------------------------------------
+
+// Statistics of round r's slice, streamed from HBM (kept in L2 for the apply
+// pass) and published to the workspace when the channel has S > 1 slices, or
+// kept in `keep` (by round parity) when S == 1.
+template <typename T, int VE>
+__device__ void fwd_stats(const T* x, const Rounds& rd, int r, Moments* warp_m, Moments* keep, int warp,
+                          int lane, uint64_t pol) {
+    const BnGeom& g = rd.g;
+    int64_t ch;
+    int s;
+    uint32_t b0, b1;
+    rd.range(r, ch, s, b0, b1);
+    ShiftedSums acc;
+    for (uint32_t base = b0 + warp; base < b1; base += kBnWarps * kBnUnroll) {
+        Pack<T, VE> pk[kBnUnroll];
+        bool ok[kBnUnroll];
+#pragma unroll
+        for (int u = 0; u < kBnUnroll; ++u) {
+            const uint32_t bi = base + u * kBnWarps;
+            ok[u] = false;
+            if (bi < b1) {
+                const BlockPos p = block_pos(g, bi, lane, ch);
+                if (p.v < g.lv) {
+                    ok[u] = true;
+                    raw_load_pol<T, VE>(x, p.seg * g.lv + p.v, pk[u], pol);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBnUnroll; ++u) {
+            if (!ok[u]) continue;
+            float v[VE];
+            unpack<T, VE>(pk[u], v);
+            acc.add(v);
+        }
+    }
+    Moments m = acc.moments();
+    warp_merge(m);
+    if (lane == 0) warp_m[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Moments cta = warp_m[0];
+        for (int w = 1; w < kBnWarps; ++w) chan_merge(cta, warp_m[w].n, warp_m[w].mean, warp_m[w].m2);
+        if (g.S > 1) {
+            float4* part = reinterpret_cast<float4*>(g.partials) + ch * g.S;
+            part[s] = make_float4(cta.n, cta.mean, cta.m2, 0.f);
+            red_release_add_u32(g.counters + ch, 1u);
+        } else {
+            keep[r & 1] = cta;
+        }
+    }
+    __syncthreads();  // warp_m is reused
+}
+
 template <typename T, int VE, bool TRAIN>
 __global__ void __launch_bounds__(kBnThreads, 1)
 bn_fwd_kernel(const BnArgs a, const BnGeom g) {
-    extern __shared__ __align__(16) unsigned char stage[];
     __shared__ Moments warp_m[kBnWarps];
-    __shared__ Moments cta_m;
+    __shared__ Moments keep[2];
     __shared__ float s_scale, s_shift;
+    __shared__ int s_bad;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const uint32_t rank = blockIdx.x % uint32_t(g.cs);
-    const int64_t ch = blockIdx.x / uint32_t(g.cs);
-    const uint32_t b0 = uint32_t(uint64_t(rank) * g.nb_chan / uint32_t(g.cs));
-    const uint32_t b1 = uint32_t(uint64_t(rank + 1) * g.nb_chan / uint32_t(g.cs));
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
     const T* __restrict__ res = reinterpret_cast<const T*>(a.res);
     T* __restrict__ y = reinterpret_cast<T*>(a.y);
-    const float wc = a.w ? a.w[ch] : 1.f;
-    const float bc = a.b ? a.b[ch] : 0.f;
+    const uint64_t pol_stream = l2_evict_first();
+    const uint64_t pol_keep = TRAIN ? l2_evict_last() : pol_stream;
+    const Rounds rd(g);
+    bool bad = false;
 
-    if constexpr (TRAIN) {
-        // ---- pass over x: stage in shared memory, Welford/Chan per thread ----
-        Moments m{0.f, 0.f, 0.f};
-        for (uint32_t base = b0 + warp; base < b1; base += kBnWarps * kBnUnroll) {
-            Pack<T, VE> pk[kBnUnroll];
-            bool ok[kBnUnroll];
+    if (threadIdx.x == 0) s_bad = 0;
+    if (TRAIN && rd.valid(0)) fwd_stats<T, VE>(x, rd, 0, warp_m, keep, warp, lane, pol_keep);
+
+    for (int r = 0; rd.valid(r); ++r) {
+        int64_t ch;
+        int s;
+        uint32_t b0, b1;
+        rd.range(r, ch, s, b0, b1);
+        // the next round's statistics go out before this round's wait
+        if (TRAIN && rd.valid(r + 1)) fwd_stats<T, VE>(x, rd, r + 1, warp_m, keep, warp, lane, pol_keep);
+
+        const float wc = a.w ? a.w[ch] : 1.f;
+        const float bc = a.b ? a.b[ch] : 0.f;
+        if constexpr (TRAIN) {
+            if (warp == 0) {
+                Moments tot = keep[r & 1];
+                if (g.S > 1) {
+                    const float4* part = reinterpret_cast<const float4*>(g.partials) + ch * g.S;
+                    if (!wait_count(g.counters + ch, uint32_t(g.S))) bad = true;
+                    Moments lm{0.f, 0.f, 0.f};
+                    for (int i = lane; i < g.S; i += 32) {
+                        const float4 pv = ld_cg_f4(part + i);
+                        chan_merge(lm, pv.x, pv.y, pv.z);
+                    }
+                    warp_merge(lm);
+                    tot = lm;
+                }
+                if (lane == 0) {
+                    const float var = tot.m2 * g.inv_m;
+                    const float rs = rsqrtf(var + a.eps);
+                    s_scale = wc * rs;
+                    s_shift = bc - tot.mean * wc * rs;
+                    if (s == 0) {
+                        if (a.save_mean) a.save_mean[ch] = tot.mean;
+                        if (a.save_rstd) a.save_rstd[ch] = rs;
+                        if (a.rm) a.rm[ch] = fmaf(a.momentum, tot.mean, (1.f - a.momentum) * a.rm[ch]);
+                        if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * a.rv[ch]);
+                    }
+                }
+            }
+        } else {
+            if (threadIdx.x == 0) {
+                const float rs = rsqrtf(a.rv[ch] + a.eps);
+                const float mu = a.rm[ch];
+                s_scale = wc * rs;
+                s_shift = bc - mu * wc * rs;
+                if (s == 0) {
+                    if (a.save_mean) a.save_mean[ch] = mu;
+                    if (a.save_rstd) a.save_rstd[ch] = rs;
+                }
+            }
+        }
+        __syncthreads();
+        const float scale = s_scale;
+        const float shift = s_shift;
+
+        // ---- normalise, affine, residual, activation, store (+ ReLU mask) ----
+        for (uint32_t base = b0 + warp; base < b1; base += kBnWarps * kBnUnroll2) {
+            Pack<T, VE> px[kBnUnroll2], pr[kBnUnroll2];
 #pragma unroll
-            for (int u = 0; u < kBnUnroll; ++u) {
+            for (int u = 0; u < kBnUnroll2; ++u) {
                 const uint32_t bi = base + u * kBnWarps;
-                ok[u] = false;
                 if (bi < b1) {
                     const BlockPos p = block_pos(g, bi, lane, ch);
                     if (p.v < g.lv) {
-                        ok[u] = true;
-                        raw_load<T, VE>(x, p.seg * g.lv + p.v, pk[u]);
+                        raw_load_pol<T, VE>(x, p.seg * g.lv + p.v, px[u], pol_stream);
+                        if (res) raw_load_pol<T, VE>(res, p.seg * g.lv + p.v, pr[u], pol_stream);
                     }
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kBnUnroll; ++u) {
-                if (!ok[u]) continue;
+            for (int u = 0; u < kBnUnroll2; ++u) {
                 const uint32_t bi = base + u * kBnWarps;
-                if (bi - b0 < g.stage_blocks) stage_put<T, VE>(stage, (bi - b0) * 32 + lane, pk[u]);
-                float v[VE];
-                unpack<T, VE>(pk[u], v);
-                float s = 0.f;
-#pragma unroll
-                for (int k = 0; k < VE; ++k) s += v[k];
-                const float vm = s * (1.f / VE);
-                float q = 0.f;
-#pragma unroll
-                for (int k = 0; k < VE; ++k) q = fmaf(v[k] - vm, v[k] - vm, q);
-                chan_merge(m, float(VE), vm, q);
-            }
-        }
-        // ---- warp -> CTA -> cluster, fixed order ----
-        warp_merge(m);
-        if (lane == 0) warp_m[warp] = m;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            Moments t = warp_m[0];
-            for (int w = 1; w < kBnWarps; ++w) chan_merge(t, warp_m[w].n, warp_m[w].mean, warp_m[w].m2);
-            cta_m = t;
-        }
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        if (threadIdx.x == 0) {
-            Moments tot{0.f, 0.f, 0.f};
-            for (int r = 0; r < g.cs; ++r) {
-                const Moments* pm = cluster.map_shared_rank(&cta_m, r);
-                chan_merge(tot, pm->n, pm->mean, pm->m2);
-            }
-            const float var = tot.m2 * g.inv_m;
-            const float rs = rsqrtf(var + a.eps);
-            s_scale = wc * rs;
-            s_shift = bc - tot.mean * wc * rs;
-            if (rank == 0) {
-                if (a.save_mean) a.save_mean[ch] = tot.mean;
-                if (a.save_rstd) a.save_rstd[ch] = rs;
-                if (a.rm) a.rm[ch] = fmaf(a.momentum, tot.mean, (1.f - a.momentum) * a.rm[ch]);
-                if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * a.rv[ch]);
-            }
-        }
-        // peers have read cta_m; s_scale/s_shift are visible to the CTA
-        cluster.sync();
-    } else {
-        if (threadIdx.x == 0) {
-            const float rs = rsqrtf(a.rv[ch] + a.eps);
-            const float mu = a.rm[ch];
-            s_scale = wc * rs;
-            s_shift = bc - mu * wc * rs;
-            if (rank == 0) {
-                if (a.save_mean) a.save_mean[ch] = mu;
-                if (a.save_rstd) a.save_rstd[ch] = rs;
-            }
-        }
-        __syncthreads();
-    }
-    const float scale = s_scale;
-    const float shift = s_shift;
-
-    // ---- normalise, affine, residual, activation, store (+ ReLU mask) ----
-    for (uint32_t base = b0 + warp; base < b1; base += kBnWarps * kBnUnroll) {
-        Pack<T, VE> px[kBnUnroll], pr[kBnUnroll];
-#pragma unroll
-        for (int u = 0; u < kBnUnroll; ++u) {
-            const uint32_t bi = base + u * kBnWarps;
-            if (bi < b1) {
+                if (bi >= b1) break;  // uniform across the warp
                 const BlockPos p = block_pos(g, bi, lane, ch);
+                uint32_t nib = 0;
                 if (p.v < g.lv) {
-                    if (TRAIN && bi - b0 < g.stage_blocks)
-                        stage_get<T, VE>(stage, (bi - b0) * 32 + lane, px[u]);
-                    else
-                        raw_load<T, VE>(x, p.seg * g.lv + p.v, px[u]);
-                    if (res) raw_load<T, VE>(res, p.seg * g.lv + p.v, pr[u]);
+                    float v[VE], rr[VE], o[VE];
+                    unpack<T, VE>(px[u], v);
+                    if (res) unpack<T, VE>(pr[u], rr);
+#pragma unroll
+                    for (int k = 0; k < VE; ++k) {
+                        float z = fmaf(v[k], scale, shift);
+                        if (res) z += rr[k];
+                        o[k] = act_forward(a.act, z);
+                        nib |= uint32_t(z > 0.f) << k;
+                    }
+                    store_vec_pol<T, VE>(y + (p.seg * g.lv + p.v) * VE, o, pol_stream);
                 }
+                if (a.mask) store_mask_bits<VE>(a.mask, g, p, lane, nib);
             }
         }
-#pragma unroll
-        for (int u = 0; u < kBnUnroll; ++u) {
-            const uint32_t bi = base + u * kBnWarps;
-            if (bi >= b1) break;  // uniform across the warp
-            const BlockPos p = block_pos(g, bi, lane, ch);
-            uint32_t nib = 0;
-            if (p.v < g.lv) {
-                float v[VE], r[VE], o[VE];
-                unpack<T, VE>(px[u], v);
-                if (res) unpack<T, VE>(pr[u], r);
-#pragma unroll
-                for (int k = 0; k < VE; ++k) {
-                    float z = fmaf(v[k], scale, shift);
-                    if (res) z += r[k];
-                    o[k] = act_forward(a.act, z);
-                    nib |= uint32_t(z > 0.f) << k;
-                }
-                store_vec<T, VE>(y + (p.seg * g.lv + p.v) * VE, o);
-            }
-            if (a.mask) store_mask_bits<VE>(a.mask, g, p, lane, nib);
-        }
+        __syncthreads();  // s_scale / s_shift are rewritten next round
     }
+
+    if (bad) s_bad = 1;
+    __syncthreads();
+    if (threadIdx.x == 0 && s_bad) atomicOr(a.err, kErrTimeoutPeers);
 }
 
 // ---------------------------------------------------------------------------
 // backward
 // ---------------------------------------------------------------------------
 
-// dz for one lane's vector of block position p.
+// dz for one lane's vector at block position p.
 template <typename T, int VE>
 __device__ __forceinline__ void form_dz(const BnArgs& a, const BnGeom& g, const BlockPos& p, int lane,
                                         bool need_z, float scale, float shift, const float (&dyv)[VE],
-                                        const float (&xv)[VE], float (&dz)[VE]) {
+                                        const float (&xv)[VE], float (&dz)[VE], uint64_t pol) {
     if (a.act == NRM_ACT_NONE) {
 #pragma unroll
         for (int k = 0; k < VE; ++k) dz[k] = dyv[k];
         return;
     }
     if (a.act == NRM_ACT_RELU && !need_z) {
-        const uint32_t bits = load_mask_bits<VE>(a.mask_in, g, p, lane);
+        const uint32_t bits = load_mask_bits<VE>(a.mask_in, g, p, lane, pol);
 #pragma unroll
         for (int k = 0; k < VE; ++k) dz[k] = ((bits >> k) & 1u) ? dyv[k] : 0.f;
         return;
@@ -330,7 +428,7 @@ __device__ __forceinline__ void form_dz(const BnArgs& a, const BnGeom& g, const 
     float r[VE];
     if (a.res) {
         Pack<T, VE> pk;
-        raw_load<T, VE>(reinterpret_cast<const T*>(a.res), p.seg * g.lv + p.v, pk);
+        raw_load_pol<T, VE>(reinterpret_cast<const T*>(a.res), p.seg * g.lv + p.v, pk, pol);
         unpack<T, VE>(pk, r);
     } else {
 #pragma unroll
@@ -343,51 +441,69 @@ __device__ __forceinline__ void form_dz(const BnArgs& a, const BnGeom& g, const 
     }
 }
 
-template <typename T, int VE, bool TRAIN>
-__global__ void __launch_bounds__(kBnThreads, 1)
-bn_bwd_kernel(const BnArgs a, const BnGeom g) {
-    extern __shared__ __align__(16) unsigned char stage_raw[];
-    float* dz_stage = reinterpret_cast<float*>(stage_raw);
-    __shared__ double warp_s[kBnWarps][2];
-    __shared__ double cta_s[2];
-    __shared__ float s_c1, s_c2;
+// Sum of dz and of dz*x without rounding loss: each product's rounding error
+// is recovered exactly with an fma, the rounded products and dz are summed
+// with Kahan compensation, and the three parts are combined in double.
+struct GradSums {
+    Kahan dz, dzx;
+    float dzx_err = 0.f;
+    template <int VE>
+    __device__ __forceinline__ void add(const float (&dzv)[VE], const float (&xv)[VE]) {
+#pragma unroll
+        for (int k = 0; k < VE; ++k) {
+            const float p = dzv[k] * xv[k];
+            dzx_err += fmaf(dzv[k], xv[k], -p);
+            dzx.add(p);
+            dz.add(dzv[k]);
+        }
+    }
+    __device__ __forceinline__ double sum_dz() const { return double(dz.s) - double(dz.c); }
+    __device__ __forceinline__ double sum_dzx() const {
+        return double(dzx.s) - double(dzx.c) + double(dzx_err);
+    }
+};
 
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const uint32_t rank = blockIdx.x % uint32_t(g.cs);
-    const int64_t ch = blockIdx.x / uint32_t(g.cs);
-    const uint32_t b0 = uint32_t(uint64_t(rank) * g.nb_chan / uint32_t(g.cs));
-    const uint32_t b1 = uint32_t(uint64_t(rank + 1) * g.nb_chan / uint32_t(g.cs));
+// First pass of round r: dz from dy and x (both streamed from HBM and kept in
+// L2 for the dx pass in training), dres, the two channel sums (published when
+// S > 1, kept when S == 1); in eval mode dx as well.
+template <typename T, int VE, bool TRAIN>
+__device__ void bwd_pass1(const BnArgs& a, const Rounds& rd, int r, double (*warp_s)[2], double2* keep,
+                          int warp, int lane, uint64_t pol_stream, uint64_t pol_keep, bool need_z) {
+    const BnGeom& g = rd.g;
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
     const T* __restrict__ dy = reinterpret_cast<const T*>(a.dy);
     T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
     T* __restrict__ dres = reinterpret_cast<T*>(a.dres);
-
+    int64_t ch;
+    int s;
+    uint32_t b0, b1;
+    rd.range(r, ch, s, b0, b1);
     const float mu = a.mean_in[ch];
     const float rs = a.rstd_in[ch];
     const float wc = a.w ? a.w[ch] : 1.f;
     const float bc = a.b ? a.b[ch] : 0.f;
     const float scale = wc * rs;
     const float shift = bc - mu * scale;
-    const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
 
-    // ---- undo the activation; dres; stage dz; channel sums ----
-    Kahan s1, s2;
-    for (uint32_t base = b0 + warp; base < b1; base += kBnWarps * kBnUnroll) {
-        Pack<T, VE> pdy[kBnUnroll], px[kBnUnroll];
+    const bool use_mask = a.act == NRM_ACT_RELU && !need_z;
+    GradSums acc;
+    for (uint32_t base = b0 + warp; base < b1; base += kBnWarps * kBnUnroll2) {
+        Pack<T, VE> pdy[kBnUnroll2], px[kBnUnroll2];
+        uint32_t mbits[kBnUnroll2];
 #pragma unroll
-        for (int u = 0; u < kBnUnroll; ++u) {
+        for (int u = 0; u < kBnUnroll2; ++u) {
             const uint32_t bi = base + u * kBnWarps;
             if (bi < b1) {
                 const BlockPos p = block_pos(g, bi, lane, ch);
                 if (p.v < g.lv) {
-                    raw_load<T, VE>(dy, p.seg * g.lv + p.v, pdy[u]);
-                    raw_load<T, VE>(x, p.seg * g.lv + p.v, px[u]);
+                    raw_load_pol<T, VE>(dy, p.seg * g.lv + p.v, pdy[u], pol_keep);
+                    raw_load_pol<T, VE>(x, p.seg * g.lv + p.v, px[u], pol_keep);
+                    if (use_mask) mbits[u] = load_mask_bits<VE>(a.mask_in, g, p, lane, pol_keep);
                 }
             }
         }
 #pragma unroll
-        for (int u = 0; u < kBnUnroll; ++u) {
+        for (int u = 0; u < kBnUnroll2; ++u) {
             const uint32_t bi = base + u * kBnWarps;
             if (bi >= b1) break;
             const BlockPos p = block_pos(g, bi, lane, ch);
@@ -395,34 +511,24 @@ bn_bwd_kernel(const BnArgs a, const BnGeom g) {
             float dyv[VE], xv[VE], dz[VE];
             unpack<T, VE>(pdy[u], dyv);
             unpack<T, VE>(px[u], xv);
-            form_dz<T, VE>(a, g, p, lane, need_z, scale, shift, dyv, xv, dz);
-            const int64_t e = (p.seg * g.lv + p.v) * VE;
-            if (dres) store_vec<T, VE>(dres + e, dz);
-            float t1 = 0.f, t2 = 0.f;
+            if (use_mask) {
 #pragma unroll
-            for (int k = 0; k < VE; ++k) {
-                t1 += dz[k];
-                t2 = fmaf(dz[k], xv[k] - mu, t2);
-            }
-            s1.add(t1);
-            s2.add(t2);
-            if constexpr (TRAIN) {
-                if (bi - b0 < g.stage_blocks) {
-                    float* d = dz_stage + (size_t((bi - b0) * 32 + lane)) * VE;
-#pragma unroll
-                    for (int k = 0; k < VE; ++k) d[k] = dz[k];
-                }
+                for (int k = 0; k < VE; ++k) dz[k] = ((mbits[u] >> k) & 1u) ? dyv[k] : 0.f;
             } else {
+                form_dz<T, VE>(a, g, p, lane, need_z, scale, shift, dyv, xv, dz, pol_keep);
+            }
+            const int64_t e = (p.seg * g.lv + p.v) * VE;
+            if (dres) store_vec_pol<T, VE>(dres + e, dz, pol_stream);
+            acc.add(dz, xv);
+            if constexpr (!TRAIN) {
                 float o[VE];
 #pragma unroll
                 for (int k = 0; k < VE; ++k) o[k] = dz[k] * scale;
-                store_vec<T, VE>(dx + e, o);
+                store_vec_pol<T, VE>(dx + e, o, pol_stream);
             }
         }
     }
-
-    // ---- sums: thread -> warp -> CTA (double, fixed order) -> cluster ----
-    double d1 = double(s1.s), d2 = double(s2.s);
+    double d1 = acc.sum_dz(), d2 = acc.sum_dzx();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         d1 += __shfl_xor_sync(0xffffffffu, d1, o);
@@ -439,88 +545,157 @@ bn_bwd_kernel(const BnArgs a, const BnGeom g) {
             t1 += warp_s[w][0];
             t2 += warp_s[w][1];
         }
-        cta_s[0] = t1;
-        cta_s[1] = t2;
-    }
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    if (threadIdx.x == 0) {
-        double t1 = 0.0, t2 = 0.0;
-        for (int r = 0; r < g.cs; ++r) {
-            const double* ps = cluster.map_shared_rank(&cta_s[0], r);
-            t1 += ps[0];
-            t2 += ps[1];
+        if (g.S > 1) {
+            double2* part = reinterpret_cast<double2*>(g.partials) + ch * g.S;
+            part[s] = make_double2(t1, t2);
+            red_release_add_u32(g.counters + ch, 1u);
+        } else {
+            keep[r & 1] = make_double2(t1, t2);
         }
-        const float sum_dz = float(t1);
-        const float sum_dz_xhat = float(t2 * double(rs));
-        if (rank == 0) {
-            if (a.db) a.db[ch] = sum_dz;
-            if (a.dw) a.dw[ch] = sum_dz_xhat;
-        }
-        s_c1 = float(t1 * double(g.inv_m));
-        s_c2 = float(t2 * double(rs) * double(g.inv_m));
     }
-    cluster.sync();
+    __syncthreads();
+}
 
-    if constexpr (TRAIN) {
-        // ---- dx = w*rstd*(dz - sum(dz)/M - xhat*sum(dz*xhat)/M) ----
-        const float c1 = s_c1;
-        const float c2 = s_c2;
-        for (uint32_t base = b0 + warp; base < b1; base += kBnWarps * kBnUnroll) {
-            Pack<T, VE> px[kBnUnroll], pdy[kBnUnroll];
+template <typename T, int VE, bool TRAIN>
+__global__ void __launch_bounds__(kBnThreads, 1)
+bn_bwd_kernel(const BnArgs a, const BnGeom g) {
+    __shared__ double warp_s[kBnWarps][2];
+    __shared__ double2 keep[2];
+    __shared__ float s_c1, s_c2;
+    __shared__ int s_bad;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    const T* __restrict__ dy = reinterpret_cast<const T*>(a.dy);
+    T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
+    // training reads dy, x (and the mask / residual) twice: keep them in L2
+    // until the dx pass; everything else streams through once
+    const uint64_t pol_stream = l2_evict_first();
+    const uint64_t pol_keep = TRAIN ? l2_evict_last() : pol_stream;
+    const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
+    const Rounds rd(g);
+    bool bad = false;
+
+    if (threadIdx.x == 0) s_bad = 0;
+    if (rd.valid(0)) bwd_pass1<T, VE, TRAIN>(a, rd, 0, warp_s, keep, warp, lane, pol_stream, pol_keep, need_z);
+
+    for (int r = 0; rd.valid(r); ++r) {
+        int64_t ch;
+        int s;
+        uint32_t b0, b1;
+        rd.range(r, ch, s, b0, b1);
+        if (rd.valid(r + 1))
+            bwd_pass1<T, VE, TRAIN>(a, rd, r + 1, warp_s, keep, warp, lane, pol_stream, pol_keep, need_z);
+        const float mu = a.mean_in[ch];
+        const float rs = a.rstd_in[ch];
+        const float wc = a.w ? a.w[ch] : 1.f;
+        const float bc = a.b ? a.b[ch] : 0.f;
+        const float scale = wc * rs;
+        const float shift = bc - mu * scale;
+
+        // ---- this round's channel sums ----
+        if (warp == 0) {
+            double t1 = keep[r & 1].x, t2 = keep[r & 1].y;
+            if (g.S > 1) {
+                const double2* part = reinterpret_cast<const double2*>(g.partials) + ch * g.S;
+                if (!wait_count(g.counters + ch, uint32_t(g.S))) bad = true;
+                double l1 = 0.0, l2 = 0.0;
+                for (int i = lane; i < g.S; i += 32) {
+                    const double2 pv = ld_cg_d2(part + i);
+                    l1 += pv.x;
+                    l2 += pv.y;
+                }
 #pragma unroll
-            for (int u = 0; u < kBnUnroll; ++u) {
-                const uint32_t bi = base + u * kBnWarps;
-                if (bi < b1) {
-                    const BlockPos p = block_pos(g, bi, lane, ch);
-                    if (p.v < g.lv) {
-                        raw_load<T, VE>(x, p.seg * g.lv + p.v, px[u]);
-                        if (bi - b0 >= g.stage_blocks) raw_load<T, VE>(dy, p.seg * g.lv + p.v, pdy[u]);
+                for (int o = 16; o > 0; o >>= 1) {
+                    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+                    l2 += __shfl_xor_sync(0xffffffffu, l2, o);
+                }
+                t1 = l1;
+                t2 = l2;
+            }
+            if (lane == 0) {
+                // sum dz*(x - mean) = sum dz*x - mean*sum dz, in double
+                const double t2c = t2 - double(mu) * t1;
+                if (s == 0) {
+                    if (a.db) a.db[ch] = float(t1);
+                    if (a.dw) a.dw[ch] = float(t2c * double(rs));
+                }
+                s_c1 = float(t1 * double(g.inv_m));
+                s_c2 = float(t2c * double(rs) * double(g.inv_m));
+            }
+        }
+        __syncthreads();
+
+        if constexpr (TRAIN) {
+            // ---- dx = w*rstd*(dz - sum(dz)/M - xhat*sum(dz*xhat)/M) ----
+            const float c1 = s_c1;
+            const float c2 = s_c2;
+            const bool use_mask = a.act == NRM_ACT_RELU && !need_z;
+            for (uint32_t base = b0 + warp; base < b1; base += kBnWarps * kBnUnrollL2) {
+                Pack<T, VE> pdy[kBnUnrollL2], px[kBnUnrollL2];
+                uint32_t mbits[kBnUnrollL2];
+#pragma unroll
+                for (int u = 0; u < kBnUnrollL2; ++u) {
+                    const uint32_t bi = base + u * kBnWarps;
+                    if (bi < b1) {
+                        const BlockPos p = block_pos(g, bi, lane, ch);
+                        if (p.v < g.lv) {
+                            raw_load_pol<T, VE>(dy, p.seg * g.lv + p.v, pdy[u], pol_stream);
+                            raw_load_pol<T, VE>(x, p.seg * g.lv + p.v, px[u], pol_stream);
+                            if (use_mask) mbits[u] = load_mask_bits<VE>(a.mask_in, g, p, lane, pol_stream);
+                        }
                     }
                 }
-            }
 #pragma unroll
-            for (int u = 0; u < kBnUnroll; ++u) {
-                const uint32_t bi = base + u * kBnWarps;
-                if (bi >= b1) break;
-                const BlockPos p = block_pos(g, bi, lane, ch);
-                if (p.v >= g.lv) continue;
-                float xv[VE], dz[VE], o[VE];
-                unpack<T, VE>(px[u], xv);
-                if (bi - b0 < g.stage_blocks) {
-                    const float* d = dz_stage + (size_t((bi - b0) * 32 + lane)) * VE;
-#pragma unroll
-                    for (int k = 0; k < VE; ++k) dz[k] = d[k];
-                } else {
-                    float dyv[VE];
+                for (int u = 0; u < kBnUnrollL2; ++u) {
+                    const uint32_t bi = base + u * kBnWarps;
+                    if (bi >= b1) break;
+                    const BlockPos p = block_pos(g, bi, lane, ch);
+                    if (p.v >= g.lv) continue;
+                    float dyv[VE], xv[VE], dz[VE], o[VE];
                     unpack<T, VE>(pdy[u], dyv);
-                    form_dz<T, VE>(a, g, p, lane, need_z, scale, shift, dyv, xv, dz);
-                }
+                    unpack<T, VE>(px[u], xv);
+                    if (use_mask) {
 #pragma unroll
-                for (int k = 0; k < VE; ++k) {
-                    const float xh = (xv[k] - mu) * rs;
-                    o[k] = scale * (dz[k] - c1 - xh * c2);
+                        for (int k = 0; k < VE; ++k) dz[k] = ((mbits[u] >> k) & 1u) ? dyv[k] : 0.f;
+                    } else {
+                        form_dz<T, VE>(a, g, p, lane, need_z, scale, shift, dyv, xv, dz, pol_stream);
+                    }
+#pragma unroll
+                    for (int k = 0; k < VE; ++k) {
+                        const float xh = (xv[k] - mu) * rs;
+                        o[k] = scale * (dz[k] - c1 - xh * c2);
+                    }
+                    store_vec_pol<T, VE>(dx + (p.seg * g.lv + p.v) * VE, o, pol_stream);
                 }
-                store_vec<T, VE>(dx + (p.seg * g.lv + p.v) * VE, o);
             }
         }
+        __syncthreads();  // s_c1 / s_c2 are rewritten next round
     }
+
+    if (bad) s_bad = 1;
+    __syncthreads();
+    if (threadIdx.x == 0 && s_bad) atomicOr(a.err, kErrTimeoutPeers);
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// Shared-memory budget for staging, leaving room for the static arrays.
-inline size_t bn_stage_budget(const DevInfo& d) {
-    const size_t cap = size_t(d.max_smem_optin);
-    const size_t reserve = 2048;
-    return cap > reserve ? cap - reserve : 0;
+
+// Upper bound of slices per channel (sizes the workspace).
+inline int bn_max_slices(const DevInfo& d) { return 4 * d.sms; }
+
+// Workspace bytes: per-channel counters, then per-(channel, slice) partials.
+inline size_t bn_workspace_bytes(const DevInfo& d, int64_t c) {
+    const size_t counters = (size_t(c) * 4 + 255) / 256 * 256;
+    return counters + size_t(c) * size_t(bn_max_slices(d)) * 16;
 }
 
 struct BnPlan {
     BnGeom g;
     size_t smem;
-    int cluster;   // cluster size of the launch (1 = no cluster)
+    int grid;
 };
 
 inline void bn_geometry(BnGeom& g, const BnArgs& a, int ve) {
@@ -535,71 +710,98 @@ inline void bn_geometry(BnGeom& g, const BnArgs& a, int ve) {
     const double m = double(a.n) * double(a.l);
     g.inv_m = m > 0 ? float(1.0 / m) : 0.f;
     g.inv_m1 = m > 1 ? float(1.0 / (m - 1.0)) : 0.f;
+    g.counters = nullptr;
+    g.partials = nullptr;
 }
 
-// Picks the cluster size and the staged blocks.  `slot_bytes` is the shared
-// memory one block occupies when staged (0: nothing is staged).
-inline nrm_status bn_plan(BnPlan& pl, const BnArgs& a, int ve, size_t slot_bytes, bool use_cluster,
-                          const void* fn) {
+// L2 held by the slices of two rounds in flight (the statistics pass of
+// round r+1 overlaps the apply pass of round r).
+constexpr double kBnL2Budget = 48.0 * 1024 * 1024;
+// Fixed cost of a round (channel barrier, reductions), in blocks of work.
+constexpr double kBnRoundOverheadBlocks = 32.0;
+
+// Chooses k channels per round and S = G/k slices per channel (the grid is a
+// whole number of channels, every CTA resident).  `stage_bytes` is the bytes
+// per element the passes keep in L2 between the two passes of a round.
+inline nrm_status bn_plan(BnPlan& pl, const BnArgs& a, int ve, size_t stage_bytes, const void* fn) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     bn_geometry(pl.g, a, ve);
     BnGeom& g = pl.g;
-    const uint32_t nb = g.nb_chan;
-    const int64_t target_ctas = 2 * int64_t(d->sms);
-    const size_t budget = bn_stage_budget(*d);
-    const int max_cs = use_cluster ? 16 : 64;
-
-    auto per_cta = [&](int cs) -> uint64_t { return (uint64_t(nb) + cs - 1) / cs; };
-    int cs = 1;
-    if (slot_bytes > 0) {
-        while (cs < max_cs && per_cta(cs) * slot_bytes > budget) cs *= 2;
+    const int occ = cached_occupancy(fn, kBnThreads, 0);
+    if (occ < 1) return fail(NRM_ERR_CUDA, "batchnorm kernel cannot be resident");
+    const int64_t G = int64_t(occ) * d->sms;
+    const uint64_t nb = g.nb_chan;
+    const double chan_bytes = double(a.n) * double(a.l) * double(stage_bytes);
+    int64_t k_max = int64_t(kBnL2Budget / (2.0 * (chan_bytes > 1.0 ? chan_bytes : 1.0)));
+    if (k_max < 1) k_max = 1;
+    if (k_max > G) k_max = G;
+    if (k_max > a.c) k_max = a.c > 0 ? a.c : 1;
+    // a channel with few blocks gets few slices (each slice keeps its warps busy)
+    int64_t best_k = k_max;
+    double best = 1e300;
+    for (int64_t k = 1; k <= k_max; ++k) {
+        int64_t S = G / k;
+        const int64_t s_cap = int64_t(nb / (uint64_t(kBnWarps) * 2)) > 0 ? int64_t(nb / (uint64_t(kBnWarps) * 2)) : 1;
+        if (S > s_cap) S = s_cap;
+        if (S < 1) S = 1;
+        const int64_t kk = G / S;  // channels per round the grid holds at this S
+        const int64_t rounds = (a.c + kk - 1) / kk;
+        const double cost = double(rounds) * (double((nb + S - 1) / S) + kBnRoundOverheadBlocks);
+        if (cost < best) {
+            best = cost;
+            best_k = k;
+        }
     }
-    // more CTAs per channel while the GPU is not filled and each CTA keeps
-    // at least one block per warp
-    const int grow_limit = use_cluster ? 8 : 64;
-    while (cs < grow_limit && a.c * cs < target_ctas && per_cta(cs * 2) >= uint64_t(kBnWarps)) cs *= 2;
-    // every CTA owns at least one block when possible
-    while (cs > 1 && uint64_t(cs) > nb) cs /= 2;
-
-    for (;;) {
-        const uint64_t fit = slot_bytes ? budget / slot_bytes : 0;
-        const uint64_t want = per_cta(cs);
-        g.cs = cs;
-        g.stage_blocks = uint32_t(slot_bytes ? (want < fit ? want : fit) : 0);
-        pl.smem = size_t(g.stage_blocks) * slot_bytes;
-        pl.cluster = use_cluster ? cs : 1;
-        nrm_status st = prepare_kernel(fn, pl.smem, pl.cluster > 8);
-        if (st != NRM_OK) return st;
-        if (!use_cluster || cs == 1) break;
-        if (max_active_clusters(fn, cs, kBnThreads, pl.smem) > 0) break;
-        cs /= 2;  // this cluster shape cannot be scheduled here: smaller cluster
+    int64_t S = G / best_k;
+    {
+        const int64_t s_cap = int64_t(nb / (uint64_t(kBnWarps) * 2)) > 0 ? int64_t(nb / (uint64_t(kBnWarps) * 2)) : 1;
+        if (S > s_cap) S = s_cap;
+        if (S < 1) S = 1;
+        if (S > bn_max_slices(*d)) S = bn_max_slices(*d);
     }
+    g.S = int(S);
+    const int64_t k = G / S;
+    const int64_t items = a.c * S;
+    int64_t grid = k * S;
+    if (grid > items) grid = items;
+    pl.grid = int(grid > 0 ? grid : 1);
+    g.rounds = int((items + pl.grid - 1) / pl.grid);
+    pl.smem = 0;
     return NRM_OK;
 }
 
-inline nrm_status launch_bn(const void* fn, const BnArgs& a, const BnPlan& pl, cudaStream_t s) {
+inline nrm_status launch_bn(const void* fn, const BnArgs& a, BnPlan& pl, void* ws, size_t ws_bytes,
+                            cudaStream_t s) {
     if (a.c == 0) return NRM_OK;
+    const DevInfo* d = dev_info();
+    if (pl.g.S > 1) {
+        if (!ws || ws_bytes < bn_workspace_bytes(*d, a.c))
+            return fail(NRM_ERR_WORKSPACE, "batchnorm needs a workspace of %zu bytes for this shape",
+                        bn_workspace_bytes(*d, a.c));
+        pl.g.counters = reinterpret_cast<uint32_t*>(ws);
+        pl.g.partials = reinterpret_cast<unsigned char*>(ws) + (size_t(a.c) * 4 + 255) / 256 * 256;
+        nrm_status st = cuda_status(cudaMemsetAsync(ws, 0, size_t(a.c) * 4, s), "workspace counters reset");
+        if (st != NRM_OK) return st;
+    }
     BnArgs args = a;
     BnGeom geom = pl.g;
     void* kargs[] = {&args, &geom};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(a.c * pl.g.cs));
+    cfg.gridDim = dim3(unsigned(pl.grid));
     cfg.blockDim = dim3(kBnThreads);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(pl.cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cuda_status(cudaLaunchKernelExC(&cfg, fn, kargs), "batchnorm launch");
 }
 
 template <typename T>
-nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, cudaStream_t s) {
+nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_bytes, cudaStream_t s) {
     const int ve = vec ? kVec<T> : 1;
     const void* fn;
     if (training)
@@ -607,14 +809,13 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, cudaStream_t s) {
     else
         fn = vec ? (const void*)&bn_fwd_kernel<T, kVec<T>, false> : (const void*)&bn_fwd_kernel<T, 1, false>;
     BnPlan pl;
-    const size_t slot = training ? size_t(32) * ve * sizeof(T) : 0;
-    nrm_status st = bn_plan(pl, a, ve, slot, training, fn);
+    nrm_status st = bn_plan(pl, a, ve, sizeof(T), fn);
     if (st != NRM_OK) return st;
-    return launch_bn(fn, a, pl, s);
+    return launch_bn(fn, a, pl, ws, ws_bytes, s);
 }
 
 template <typename T>
-nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, cudaStream_t s) {
+nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_bytes, cudaStream_t s) {
     const int ve = vec ? kVec<T> : 1;
     const void* fn;
     if (training)
@@ -622,14 +823,13 @@ nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, cudaStream_t s) {
     else
         fn = vec ? (const void*)&bn_bwd_kernel<T, kVec<T>, false> : (const void*)&bn_bwd_kernel<T, 1, false>;
     BnPlan pl;
-    const size_t slot = training ? size_t(32) * ve * sizeof(float) : 0;
-    nrm_status st = bn_plan(pl, a, ve, slot, true, fn);
+    nrm_status st = bn_plan(pl, a, ve, 2 * sizeof(T), fn);
     if (st != NRM_OK) return st;
-    return launch_bn(fn, a, pl, s);
+    return launch_bn(fn, a, pl, ws, ws_bytes, s);
 }
 
 }  // namespace nrm
 
-#define NRM_INSTANTIATE_BATCHNORM(T)                                                    \
-    template nrm_status nrm::bn_fwd<T>(const nrm::BnArgs&, bool, bool, cudaStream_t);   \
-    template nrm_status nrm::bn_bwd<T>(const nrm::BnArgs&, bool, bool, cudaStream_t);
+#define NRM_INSTANTIATE_BATCHNORM(T)                                                                  \
+    template nrm_status nrm::bn_fwd<T>(const nrm::BnArgs&, bool, bool, void*, size_t, cudaStream_t); \
+    template nrm_status nrm::bn_bwd<T>(const nrm::BnArgs&, bool, bool, void*, size_t, cudaStream_t);

@@ -15,6 +15,7 @@ struct DevInfo {
     int device;
     int sms;
     int max_smem_optin;   // bytes of dynamic shared memory a CTA may opt into
+    unsigned int* err;    // device address of the library's error word
 };
 const DevInfo* dev_info();  // nullptr if no usable device
 
@@ -106,9 +107,14 @@ struct BnArgs {
     float eps;
     float momentum;
     int act;
+    unsigned int* err;    // device error word (bounded waits that gave up)
 };
 
-template <typename T> nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, cudaStream_t s);
-template <typename T> nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, cudaStream_t s);
+template <typename T> nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_bytes,
+                                        cudaStream_t s);
+template <typename T> nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_bytes,
+                                        cudaStream_t s);
+// Workspace bytes that suffice for any BatchNorm call with c channels.
+size_t batchnorm_workspace_bytes(const DevInfo& d, int64_t c);
 
 }  // namespace nrm

@@ -111,14 +111,15 @@ def _bn_res_relu(cfg, dev, f32):
     by, bdx, bdres = torch.empty_like(bx), torch.empty_like(bx), torch.empty_like(bx)
     bsm, bsr, bdw, bdb = f32(c), f32(c), f32(c), f32(c)
     bmask = torch.empty(nrm.nrm_act_mask_words(n, c, l), dtype=torch.int32, device=dev)
+    bws = nrm.batchnorm_workspace(bx)
     calls.append(Call(cfg.name, "fwd", "bn_fwd_kernel<f32,train>",
                       lambda: nrm.nrm_batchnorm_fwd(bx, bres, bw, bb, by, brm, brv, bsm, bsr, bmask,
-                                                    cfg.eps, cfg.momentum, True, "relu"),
+                                                    cfg.eps, cfg.momentum, True, "relu", bws),
                       nbytes(bx, bres, by, bmask, bw, bb, bsm, bsr) + 2 * nbytes(brm, brv), 1,
                       [bx, bres, bw, bb, brm, brv], [by, bmask, bsm, bsr, brm, brv]))
     calls.append(Call(cfg.name, "bwd", "bn_bwd_kernel<f32,train>",
                       lambda: nrm.nrm_batchnorm_bwd(bdy, bx, bres, bw, bb, bsm, bsr, bmask, bdx, bdres,
-                                                    bdw, bdb, True, "relu"),
+                                                    bdw, bdb, True, "relu", bws),
                       nbytes(bdy, bx, bmask, bw, bb, bsm, bsr, bdx, bdres, bdw, bdb), 1,
                       [bdy], [bdx, bdres, bdw, bdb]))
     erm = synth.store(0.3 * synth.normal(cfg.seed, 20, c), "f32", (c,)).torch(dev)
@@ -127,12 +128,12 @@ def _bn_res_relu(cfg, dev, f32):
     eval_name = cfg.name + "_eval"
     calls.append(Call(eval_name, "fwd", "bn_fwd_kernel<f32,eval>",
                       lambda: nrm.nrm_batchnorm_fwd(bx, bres, bw, bb, by, erm, erv, esm, esr, bmask,
-                                                    cfg.eps, cfg.momentum, False, "relu"),
+                                                    cfg.eps, cfg.momentum, False, "relu", bws),
                       nbytes(bx, bres, by, bmask, bw, bb, erm, erv, esm, esr), 1,
                       [erm, erv], [by, bmask]))
     calls.append(Call(eval_name, "bwd", "bn_bwd_kernel<f32,eval>",
                       lambda: nrm.nrm_batchnorm_bwd(bdy, bx, bres, bw, bb, esm, esr, bmask, bdx, bdres,
-                                                    bdw, bdb, False, "relu"),
+                                                    bdw, bdb, False, "relu", bws),
                       nbytes(bdy, bx, bmask, bw, bb, esm, esr, bdx, bdres, bdw, bdb), 1,
                       [], [bdx, bdres, bdw, bdb]))
 
@@ -151,14 +152,15 @@ def _bn_gelu(cfg, dev, f32):
     c = cfg.c
     gy, gdx = torch.empty_like(gx), torch.empty_like(gx)
     gsm, gsr, gdw, gdb = f32(c), f32(c), f32(c), f32(c)
+    gws = nrm.batchnorm_workspace(gx)
     calls.append(Call(cfg.name, "fwd", "bn_fwd_kernel<f16,train>",
                       lambda: nrm.nrm_batchnorm_fwd(gx, None, gw, gb, gy, grm, grv, gsm, gsr, None,
-                                                    cfg.eps, cfg.momentum, True, "gelu"),
+                                                    cfg.eps, cfg.momentum, True, "gelu", gws),
                       nbytes(gx, gy, gw, gb, gsm, gsr) + 2 * nbytes(grm, grv), 1,
                       [gx, gw, gb, grm, grv], [gy, gsm, gsr, grm, grv]))
     calls.append(Call(cfg.name, "bwd", "bn_bwd_kernel<f16,train>",
                       lambda: nrm.nrm_batchnorm_bwd(gdy, gx, None, gw, gb, gsm, gsr, None, gdx, None,
-                                                    gdw, gdb, True, "gelu"),
+                                                    gdw, gdb, True, "gelu", gws),
                       nbytes(gdy, gx, gw, gb, gsm, gsr, gdx, gdw, gdb), 1,
                       [gdy], [gdx, gdw, gdb]))
     return calls

@@ -86,9 +86,10 @@ def test_bn_without_affine_or_running_stats(orc, act):
     y = torch.empty_like(x)
     sm = torch.empty(c, device="cuda")
     sr = torch.empty(c, device="cuda")
-    nrm.nrm_batchnorm_fwd(x, res, None, None, y, None, None, sm, sr, None, 1e-5, 0.1, True, act)
+    ws = nrm.batchnorm_workspace(x)
+    nrm.nrm_batchnorm_fwd(x, res, None, None, y, None, None, sm, sr, None, 1e-5, 0.1, True, act, ws)
     dx = torch.empty_like(x)
-    nrm.nrm_batchnorm_bwd(dy, x, res, None, None, sm, sr, None, dx, None, None, None, True, act)
+    nrm.nrm_batchnorm_bwd(dy, x, res, None, None, sm, sr, None, dx, None, None, None, True, act, ws)
     nrm.nrm_sync_status()
     want = oracle_bn(orc, inp, 1e-5, 0.1, True, act, True, with_affine=False)
     yo = want["fwd"]["y"]
@@ -110,7 +111,8 @@ def test_bn_running_stats_closed_form():
     y = torch.empty_like(x)
     rm = torch.zeros(c, device="cuda")
     rv = torch.ones(c, device="cuda")
-    nrm.nrm_batchnorm_fwd(x, None, None, None, y, rm, rv, None, None, None, 1e-5, 0.1, True, "none")
+    nrm.nrm_batchnorm_fwd(x, None, None, None, y, rm, rv, None, None, None, 1e-5, 0.1, True, "none",
+                          nrm.batchnorm_workspace(x))
     nrm.nrm_sync_status()
     xc = inp["x"].f64().transpose(1, 0, 2).reshape(c, -1)
     np.testing.assert_allclose(rm.double().cpu().numpy(), 0.1 * xc.mean(1), rtol=1e-5, atol=1e-6)

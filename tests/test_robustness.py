@@ -105,12 +105,14 @@ def _bn_run(dtype, n, c, l, act, res, training, mask, offset):
         ("db", (c,), torch.float32))}
     mk = Guarded((nrm.nrm_act_mask_words(n, c, l),), torch.int32) if mask else None
     o = {k: g.t for k, g in outs.items()}
+    nws = nrm.nrm_batchnorm_workspace_bytes(n, c, l, DT_CODE[dtype])
+    ws = Guarded((nws,), torch.uint8)
     nrm.nrm_batchnorm_fwd(x, r, w, b_, o["y"], rm.t, rv.t, o["sm"], o["sr"], mk.t if mk else None,
-                          1e-5, 0.1, training, act)
+                          1e-5, 0.1, training, act, ws.t)
     nrm.nrm_batchnorm_bwd(dy, x, r, w, b_, o["sm"], o["sr"], mk.t if mk else None, o["dx"], o["dres"],
-                          o["dw"], o["db"], training, act)
+                          o["dw"], o["db"], training, act, ws.t)
     nrm.nrm_sync_status()
-    for k, g in list(outs.items()) + [("rm", rm), ("rv", rv)] + ([("mask", mk)] if mk else []):
+    for k, g in list(outs.items()) + [("rm", rm), ("rv", rv), ("ws", ws)] + ([("mask", mk)] if mk else []):
         g.check(f"bn {dtype} [{n},{c},{l}] {act} {k}")
     got = {k: g.t.clone() for k, g in outs.items()}
     got["rm"], got["rv"] = rm.t.clone(), rv.t.clone()
@@ -159,15 +161,16 @@ def test_errors_leave_the_context_usable():
 
 
 def test_streams_are_respected():
-    # work enqueued on a side stream completes in order with that stream
+    # work enqueued on a side stream is complete once that stream has synchronised
     s = torch.cuda.Stream()
     x = torch.randn(4096, 1024, device="cuda", dtype=torch.bfloat16)
-    y = torch.empty_like(x)
+    y = torch.zeros_like(x)
     rstd = torch.empty(4096, device="cuda")
+    s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         nrm.nrm_rmsnorm_fwd(x, None, y, rstd, 1e-6)
-        z = y.float().sum()
     s.synchronize()
     xf = x.float()
-    ref = (xf * torch.rsqrt((xf * xf).mean(1, keepdim=True) + 1e-6)).sum()
-    assert torch.allclose(z, ref, rtol=1e-3, atol=1.0)
+    ref = xf * torch.rsqrt((xf * xf).mean(1, keepdim=True) + 1e-6)
+    err = (y.float() - ref).abs()
+    assert bool((err <= 2e-2 + 1e-2 * ref.abs()).all())
