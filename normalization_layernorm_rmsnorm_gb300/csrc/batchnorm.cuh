@@ -406,6 +406,322 @@ bn_fwd_kernel(const BnArgs a, const BnGeom g) {
 }
 
 // ---------------------------------------------------------------------------
+// 16-byte vectors: a TMA producer warp and 16 consumer warps
+// ---------------------------------------------------------------------------
+// The producer warp streams a CTA's passes in chunks through a ring of 32 KB
+// shared-memory slots (the bulk copy engine moves the tensors, the warp's
+// lanes move ReLU-mask words with 4-byte async copies).  A chunk of a pass
+// over nt tensors holds 64/nt blocks of each.  The consumer warps compute
+// from the slots, release them, and synchronise only among themselves (named
+// barrier 1), so while they wait for a channel's slices the producer keeps
+// the ring full and HBM busy.  Both sides walk the same sequence of chunks.
+constexpr int kRingConsumerWarps = 16;
+constexpr int kRingConsumers = kRingConsumerWarps * 32;
+constexpr int kRingThreads = kRingConsumers + 32;
+constexpr int kSlotBlocks = 64;                    // 512-byte blocks per slot
+constexpr int kSlotBytes = kSlotBlocks * 512;
+constexpr int kSlotMaskWords = 32 * 8;             // mask words of a chunk of >= 2 tensors
+constexpr int kRingSlotsFwd = 7;
+constexpr int kRingSlotsBwd = 6;
+
+__device__ __forceinline__ uint32_t chunk_span(int nt) { return uint32_t(kSlotBlocks / nt); }
+
+// Calls f(sample n, first block lo, end block hi) for each (sample, channel)
+// segment that blocks [b0, b1) of a channel touch.
+template <typename F>
+__device__ __forceinline__ void for_segments(const BnGeom& g, uint32_t b0, uint32_t b1, F&& f) {
+    const uint32_t nbs = uint32_t(g.nbs);
+    const uint32_t n_first = fast_div(b0, g.div_nbs);
+    const uint32_t n_last = fast_div(b1 - 1, g.div_nbs);
+    for (uint32_t n = n_first; n <= n_last; ++n) {
+        const uint32_t lo = b0 > n * nbs ? b0 : n * nbs;
+        const uint32_t hi = b1 < (n + 1) * nbs ? b1 : (n + 1) * nbs;
+        f(n, lo, hi);
+    }
+}
+
+// One pass over a slice as the producer sees it: up to three tensors (each
+// with its L2 policy) and, optionally, the ReLU mask words.
+template <typename T>
+struct RingPass {
+    const T* t[3];
+    uint64_t pol[3];
+    int nt;
+    const uint32_t* mask;
+};
+
+template <int SLOTS>
+struct Ring {
+    unsigned char* data;   // SLOTS x kSlotBytes
+    uint32_t* mask;        // SLOTS x kSlotMaskWords, or null
+    uint64_t* full;
+    uint64_t* empty;
+    int seq = 0;
+    __device__ int slot() const { return seq % SLOTS; }
+    __device__ uint32_t use() const { return uint32_t(seq / SLOTS); }
+};
+
+// Producer (whole warp): the chunks of round r's slice for pass `ps`.
+template <typename T, int VE, int SLOTS>
+__device__ void ring_produce(Ring<SLOTS>& rg, const Rounds& rd, int r, const RingPass<T>& ps, int lane,
+                             bool& bad) {
+    const BnGeom& g = rd.g;
+    int64_t ch;
+    int s;
+    uint32_t b0, b1;
+    rd.range(r, ch, s, b0, b1);
+    const uint32_t span = chunk_span(ps.nt);
+    for (uint32_t cb = b0; cb < b1; cb += span) {
+        const uint32_t ce = b1 - cb < span ? b1 : cb + span;
+        const int slot = rg.slot();
+        const uint32_t use = rg.use();
+        if (use > 0 && !mbar_wait_bounded(&rg.empty[slot], (use - 1) & 1u, kBnWaitLimitNs)) bad = true;
+        unsigned char* base = rg.data + size_t(slot) * kSlotBytes;
+        if (lane == 0) {
+            uint32_t bytes = 0;
+            for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
+                const uint32_t v_lo = (lo - n * g.nbs) * 32;
+                const uint32_t v_hi = min((hi - n * g.nbs) * 32, uint32_t(g.lv));
+                bytes += (v_hi - v_lo) * 16;
+            });
+            mbar_arrive_expect_tx(&rg.full[slot], bytes * uint32_t(ps.nt));
+            for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
+                const uint32_t v_lo = (lo - n * g.nbs) * 32;
+                const uint32_t v_hi = min((hi - n * g.nbs) * 32, uint32_t(g.lv));
+                const int64_t e = ((int64_t(n) * g.c + ch) * g.lv + v_lo) * VE;
+                const size_t off = size_t(lo - cb) * 512;
+                for (int t = 0; t < ps.nt; ++t)
+                    bulk_g2s(base + size_t(t) * span * 512 + off, ps.t[t] + e, (v_hi - v_lo) * 16, &rg.full[slot],
+                             ps.pol[t]);
+            });
+        }
+        if (ps.mask) {
+            uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
+            for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
+                const uint32_t w_lo = (lo - n * g.nbs) * VE;
+                const uint32_t w_hi = min((hi - n * g.nbs) * VE, uint32_t(g.words));
+                const uint32_t* src = ps.mask + (int64_t(n) * g.c + ch) * g.words;
+                uint32_t* dst = mw + (lo - cb) * VE;
+                for (uint32_t w = w_lo + lane; w < w_hi; w += 32) cp_async_4(dst + (w - w_lo), src + w);
+            });
+            cp_async_mbar_arrive_noinc(&rg.full[slot]);
+        }
+        ++rg.seq;
+    }
+}
+
+// Consumer side of one chunk: wait until it has landed / hand the slot back.
+template <int SLOTS>
+__device__ __forceinline__ int ring_take(Ring<SLOTS>& rg, bool& bad) {
+    const int slot = rg.slot();
+    if (!mbar_wait_bounded(&rg.full[slot], rg.use() & 1u, kBnWaitLimitNs)) bad = true;
+    return slot;
+}
+template <int SLOTS>
+__device__ __forceinline__ void ring_give(Ring<SLOTS>& rg, int slot, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rg.empty[slot]);
+    ++rg.seq;
+}
+
+template <int SLOTS>
+__device__ __forceinline__ void ring_init(Ring<SLOTS>& rg, uint32_t full_count) {
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < SLOTS; ++i) {
+            mbar_init(&rg.full[i], full_count);
+            mbar_init(&rg.empty[i], kRingConsumerWarps);
+        }
+        mbar_init_fence();
+    }
+}
+
+// The VE mask bits of `lane`'s vector of chunk block i, from the slot's words.
+template <int VE>
+__device__ __forceinline__ uint32_t slot_mask_bits(const uint32_t* mw, uint32_t i, int lane) {
+    const int e = lane * VE;
+    return (mw[i * VE + (e >> 5)] >> (e & 31)) & ((1u << VE) - 1u);
+}
+
+// ---------------------------------------------------------------------------
+// forward on the ring
+// ---------------------------------------------------------------------------
+// Passes: statistics of round r+1 (x, kept in L2) ahead of the apply pass of
+// round r (x from L2 and the residual, both read for the last time).
+template <typename T, bool TRAIN>
+__global__ void __launch_bounds__(kRingThreads, 1)
+bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
+    constexpr int VE = kVec<T>;
+    constexpr int SLOTS = kRingSlotsFwd;
+    extern __shared__ __align__(128) unsigned char ring_data[];
+    __shared__ __align__(8) uint64_t full[SLOTS];
+    __shared__ __align__(8) uint64_t empty[SLOTS];
+    __shared__ Moments warp_m[kRingConsumerWarps];
+    __shared__ Moments keep[2];
+    __shared__ float s_scale[2], s_shift[2];  // by round parity: no barrier at the end of a round
+    __shared__ int s_bad;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    const T* __restrict__ res = reinterpret_cast<const T*>(a.res);
+    T* __restrict__ y = reinterpret_cast<T*>(a.y);
+    const Rounds rd(g);
+    Ring<SLOTS> rg{ring_data, nullptr, full, empty};
+    bool bad = false;
+
+    if (threadIdx.x == 0) s_bad = 0;
+    ring_init(rg, 1);
+    __syncthreads();
+
+    if (warp == kRingConsumerWarps) {
+        // ---------------- producer ----------------
+        const uint64_t pol_keep = TRAIN ? l2_evict_last() : l2_evict_first();
+        const uint64_t pol_stream = l2_evict_first();
+        const RingPass<T> stats{{x, nullptr, nullptr}, {pol_keep, 0, 0}, 1, nullptr};
+        const RingPass<T> apply{{x, res, nullptr}, {pol_stream, pol_stream, 0}, res ? 2 : 1, nullptr};
+        if (TRAIN && rd.valid(0)) ring_produce<T, VE>(rg, rd, 0, stats, lane, bad);
+        for (int r = 0; rd.valid(r); ++r) {
+            if (TRAIN && rd.valid(r + 1)) ring_produce<T, VE>(rg, rd, r + 1, stats, lane, bad);
+            ring_produce<T, VE>(rg, rd, r, apply, lane, bad);
+        }
+    } else {
+        // ---------------- consumers ----------------
+        const uint64_t pol_stream = l2_evict_first();
+        // statistics of round r's slice, published (S > 1) or kept (S == 1)
+        auto stats = [&](int r) {
+            int64_t ch;
+            int s;
+            uint32_t b0, b1;
+            rd.range(r, ch, s, b0, b1);
+            ShiftedSums acc;
+            const uint32_t span = chunk_span(1);
+            for (uint32_t cb = b0; cb < b1; cb += span) {
+                const uint32_t n = b1 - cb < span ? b1 - cb : span;
+                const int slot = ring_take(rg, bad);
+                const uint4* sx = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
+                for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
+                    const BlockPos p = block_pos(g, cb + i, lane, ch);
+                    if (p.v < g.lv) {
+                        Pack<T, VE> pk;
+                        pk.u = sx[i * 32 + lane];
+                        float v[VE];
+                        unpack<T, VE>(pk, v);
+                        acc.add(v);
+                    }
+                }
+                ring_give(rg, slot, lane);
+            }
+            Moments m = acc.moments();
+            warp_merge(m);
+            if (lane == 0) warp_m[warp] = m;
+            named_barrier(1, kRingConsumers);
+            if (threadIdx.x == 0) {
+                Moments cta = warp_m[0];
+                for (int w = 1; w < kRingConsumerWarps; ++w) chan_merge(cta, warp_m[w].n, warp_m[w].mean, warp_m[w].m2);
+                if (g.S > 1) {
+                    float4* part = reinterpret_cast<float4*>(g.partials) + ch * g.S;
+                    part[s] = make_float4(cta.n, cta.mean, cta.m2, 0.f);
+                    red_release_add_u32(g.counters + ch, 1u);
+                } else {
+                    keep[r & 1] = cta;
+                }
+            }
+            named_barrier(1, kRingConsumers);
+        };
+
+        if (TRAIN && rd.valid(0)) stats(0);
+        for (int r = 0; rd.valid(r); ++r) {
+            int64_t ch;
+            int s;
+            uint32_t b0, b1;
+            rd.range(r, ch, s, b0, b1);
+            if (TRAIN && rd.valid(r + 1)) stats(r + 1);
+            const float wc = a.w ? a.w[ch] : 1.f;
+            const float bc = a.b ? a.b[ch] : 0.f;
+            if constexpr (TRAIN) {
+                if (warp == 0) {
+                    Moments tot = keep[r & 1];
+                    if (g.S > 1) {
+                        const float4* part = reinterpret_cast<const float4*>(g.partials) + ch * g.S;
+                        if (!wait_count(g.counters + ch, uint32_t(g.S))) bad = true;
+                        Moments lm{0.f, 0.f, 0.f};
+                        for (int i = lane; i < g.S; i += 32) {
+                            const float4 pv = ld_cg_f4(part + i);
+                            chan_merge(lm, pv.x, pv.y, pv.z);
+                        }
+                        warp_merge(lm);
+                        tot = lm;
+                    }
+                    if (lane == 0) {
+                        const float var = tot.m2 * g.inv_m;
+                        const float rs = rsqrtf(var + a.eps);
+                        s_scale[r & 1] = wc * rs;
+                        s_shift[r & 1] = bc - tot.mean * wc * rs;
+                        if (s == 0) {
+                            if (a.save_mean) a.save_mean[ch] = tot.mean;
+                            if (a.save_rstd) a.save_rstd[ch] = rs;
+                            if (a.rm) a.rm[ch] = fmaf(a.momentum, tot.mean, (1.f - a.momentum) * a.rm[ch]);
+                            if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * a.rv[ch]);
+                        }
+                    }
+                }
+            } else {
+                if (threadIdx.x == 0) {
+                    const float rs = rsqrtf(a.rv[ch] + a.eps);
+                    const float mu = a.rm[ch];
+                    s_scale[r & 1] = wc * rs;
+                    s_shift[r & 1] = bc - mu * wc * rs;
+                    if (s == 0) {
+                        if (a.save_mean) a.save_mean[ch] = mu;
+                        if (a.save_rstd) a.save_rstd[ch] = rs;
+                    }
+                }
+            }
+            named_barrier(1, kRingConsumers);
+            const float scale = s_scale[r & 1];
+            const float shift = s_shift[r & 1];
+
+            // ---- y = act(x*scale + shift (+ residual)) (+ ReLU mask) ----
+            const uint32_t span = chunk_span(res ? 2 : 1);
+            for (uint32_t cb = b0; cb < b1; cb += span) {
+                const uint32_t n = b1 - cb < span ? b1 - cb : span;
+                const int slot = ring_take(rg, bad);
+                const uint4* sx = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
+                const uint4* sr = sx + span * 32;
+                for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
+                    const BlockPos p = block_pos(g, cb + i, lane, ch);
+                    uint32_t nib = 0;
+                    if (p.v < g.lv) {
+                        Pack<T, VE> px, pr;
+                        px.u = sx[i * 32 + lane];
+                        float v[VE], rr[VE], o[VE];
+                        unpack<T, VE>(px, v);
+                        if (res) {
+                            pr.u = sr[i * 32 + lane];
+                            unpack<T, VE>(pr, rr);
+                        }
+#pragma unroll
+                        for (int k = 0; k < VE; ++k) {
+                            float z = fmaf(v[k], scale, shift);
+                            if (res) z += rr[k];
+                            nib |= uint32_t(z > 0.f) << k;
+                            o[k] = act_forward(a.act, z);
+                        }
+                        store_vec_pol<T, VE>(y + (p.seg * g.lv + p.v) * VE, o, pol_stream);
+                    }
+                    if (a.mask) store_mask_bits<VE>(a.mask, g, p, lane, nib);
+                }
+                ring_give(rg, slot, lane);
+            }
+        }
+    }
+
+    if (bad) s_bad = 1;
+    __syncthreads();
+    if (threadIdx.x == 0 && s_bad) atomicOr(a.err, kErrTimeoutStage | kErrTimeoutPeers);
+}
+
+// ---------------------------------------------------------------------------
 // backward
 // ---------------------------------------------------------------------------
 
@@ -680,6 +996,280 @@ bn_bwd_kernel(const BnArgs a, const BnGeom g) {
 }
 
 // ---------------------------------------------------------------------------
+// backward on the ring
+// ---------------------------------------------------------------------------
+// Tensors of a pass: dy, x, and the residual when z must be recomputed with
+// it; the ReLU mask words ride along in the slot.  Training: pass 1 of round
+// r+1 (dz, dres, channel sums; dy and x kept in L2) ahead of pass 2 of round
+// r (dx, dy and x re-read from L2).  Eval: one pass per round (dx = dz*scale),
+// and the last slice of a channel to finish merges the sums into dw, db.
+
+// dz of one lane's vector from the slot: dy passed through the activation's
+// derivative at z (mask bits, or z recomputed from x and the residual).
+template <typename T, int VE>
+__device__ __forceinline__ void ring_dz(const BnArgs& a, bool use_mask, bool need_z, const uint32_t* mw,
+                                        const uint4* sr, uint32_t i, int lane, float scale, float shift,
+                                        const float (&dyv)[VE], const float (&xv)[VE], float (&dz)[VE]) {
+    if (use_mask) {
+        const uint32_t bits = slot_mask_bits<VE>(mw, i, lane);
+#pragma unroll
+        for (int k = 0; k < VE; ++k) dz[k] = ((bits >> k) & 1u) ? dyv[k] : 0.f;
+    } else if (need_z) {
+        float r[VE];
+        if (a.res) {
+            Pack<T, VE> pk;
+            pk.u = sr[i * 32 + lane];
+            unpack<T, VE>(pk, r);
+        } else {
+#pragma unroll
+            for (int k = 0; k < VE; ++k) r[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < VE; ++k) {
+            const float z = fmaf(xv[k], scale, shift) + r[k];
+            dz[k] = dyv[k] * act_derivative(a.act, z);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < VE; ++k) dz[k] = dyv[k];
+    }
+}
+
+template <typename T, bool TRAIN>
+__global__ void __launch_bounds__(kRingThreads, 1)
+bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
+    constexpr int VE = kVec<T>;
+    constexpr int SLOTS = kRingSlotsBwd;
+    extern __shared__ __align__(128) unsigned char ring_data[];
+    __shared__ __align__(8) uint64_t full[SLOTS];
+    __shared__ __align__(8) uint64_t empty[SLOTS];
+    __shared__ double warp_s[kRingConsumerWarps][2];
+    __shared__ double2 keep[2];
+    __shared__ float s_c1[2], s_c2[2];  // by round parity
+    __shared__ int s_bad;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    const T* __restrict__ dy = reinterpret_cast<const T*>(a.dy);
+    const T* __restrict__ res = reinterpret_cast<const T*>(a.res);
+    T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
+    T* __restrict__ dres = reinterpret_cast<T*>(a.dres);
+    const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
+    const bool use_mask = a.act == NRM_ACT_RELU && a.mask_in != nullptr;
+    const int nt = (need_z && res) ? 3 : 2;
+    const Rounds rd(g);
+    Ring<SLOTS> rg{ring_data, reinterpret_cast<uint32_t*>(ring_data + size_t(SLOTS) * kSlotBytes), full, empty};
+    bool bad = false;
+
+    if (threadIdx.x == 0) s_bad = 0;
+    ring_init(rg, use_mask ? 33u : 1u);
+    __syncthreads();
+
+    if (warp == kRingConsumerWarps) {
+        // ---------------- producer ----------------
+        const uint64_t pol_keep = TRAIN ? l2_evict_last() : l2_evict_first();
+        const uint64_t pol_stream = l2_evict_first();
+        const uint32_t* mk = use_mask ? a.mask_in : nullptr;
+        const RingPass<T> first{{dy, x, res}, {pol_keep, pol_keep, pol_keep}, nt, mk};
+        const RingPass<T> second{{dy, x, res}, {pol_stream, pol_stream, pol_stream}, nt, mk};
+        if (TRAIN && rd.valid(0)) ring_produce<T, VE>(rg, rd, 0, first, lane, bad);
+        for (int r = 0; rd.valid(r); ++r) {
+            if constexpr (TRAIN) {
+                if (rd.valid(r + 1)) ring_produce<T, VE>(rg, rd, r + 1, first, lane, bad);
+                ring_produce<T, VE>(rg, rd, r, second, lane, bad);
+            } else {
+                ring_produce<T, VE>(rg, rd, r, first, lane, bad);
+            }
+        }
+    } else {
+        // ---------------- consumers ----------------
+        const uint64_t pol_stream = l2_evict_first();
+        const uint32_t span = chunk_span(nt);
+
+        // channel sums of warp 0's lanes -> dw, db (slice 0, or the last slice
+        // in eval) and the dx coefficients of round r
+        auto finish = [&](int r, int64_t ch, int s, double t1, double t2, bool write_grads) {
+            const float mu = a.mean_in[ch];
+            const float rs = a.rstd_in[ch];
+            // sum dz*(x - mean) = sum dz*x - mean*sum dz, in double
+            const double t2c = t2 - double(mu) * t1;
+            if (write_grads) {
+                if (a.db) a.db[ch] = float(t1);
+                if (a.dw) a.dw[ch] = float(t2c * double(rs));
+            }
+            s_c1[r & 1] = float(t1 * double(g.inv_m));
+            s_c2[r & 1] = float(t2c * double(rs) * double(g.inv_m));
+            (void)s;
+        };
+        // sum of the S partials of channel ch by warp 0 in a fixed order
+        auto merge_partials = [&](int64_t ch, double& t1, double& t2) {
+            const double2* part = reinterpret_cast<const double2*>(g.partials) + ch * g.S;
+            double l1 = 0.0, l2 = 0.0;
+            for (int i = lane; i < g.S; i += 32) {
+                const double2 pv = ld_cg_d2(part + i);
+                l1 += pv.x;
+                l2 += pv.y;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+                l2 += __shfl_xor_sync(0xffffffffu, l2, o);
+            }
+            t1 = l1;
+            t2 = l2;
+        };
+
+        // pass 1 of round r: dz, dres (and dx in eval), the two channel sums
+        auto pass1 = [&](int r) {
+            int64_t ch;
+            int s;
+            uint32_t b0, b1;
+            rd.range(r, ch, s, b0, b1);
+            const float mu = a.mean_in[ch];
+            const float rs = a.rstd_in[ch];
+            const float wc = a.w ? a.w[ch] : 1.f;
+            const float bc = a.b ? a.b[ch] : 0.f;
+            const float scale = wc * rs;
+            const float shift = bc - mu * scale;
+            GradSums acc;
+            for (uint32_t cb = b0; cb < b1; cb += span) {
+                const uint32_t n = b1 - cb < span ? b1 - cb : span;
+                const int slot = ring_take(rg, bad);
+                const uint4* sd = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
+                const uint4* sx = sd + span * 32;
+                const uint4* sr = sx + span * 32;
+                const uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
+                for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
+                    const BlockPos p = block_pos(g, cb + i, lane, ch);
+                    if (p.v >= g.lv) continue;
+                    Pack<T, VE> pdy, px;
+                    pdy.u = sd[i * 32 + lane];
+                    px.u = sx[i * 32 + lane];
+                    float dyv[VE], xv[VE], dz[VE];
+                    unpack<T, VE>(pdy, dyv);
+                    unpack<T, VE>(px, xv);
+                    ring_dz<T, VE>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
+                    const int64_t e = (p.seg * g.lv + p.v) * VE;
+                    if (dres) store_vec_pol<T, VE>(dres + e, dz, pol_stream);
+                    acc.add(dz, xv);
+                    if constexpr (!TRAIN) {
+                        float o[VE];
+#pragma unroll
+                        for (int k = 0; k < VE; ++k) o[k] = dz[k] * scale;
+                        store_vec_pol<T, VE>(dx + e, o, pol_stream);
+                    }
+                }
+                ring_give(rg, slot, lane);
+            }
+            double d1 = acc.sum_dz(), d2 = acc.sum_dzx();
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+                d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+            }
+            if (lane == 0) {
+                warp_s[warp][0] = d1;
+                warp_s[warp][1] = d2;
+            }
+            named_barrier(1, kRingConsumers);
+            if (warp == 0) {
+                double t1 = 0.0, t2 = 0.0;
+                if (lane == 0) {
+                    for (int w = 0; w < kRingConsumerWarps; ++w) {
+                        t1 += warp_s[w][0];
+                        t2 += warp_s[w][1];
+                    }
+                }
+                if (g.S == 1) {
+                    if (lane == 0) {
+                        if (TRAIN) keep[r & 1] = make_double2(t1, t2);
+                        else finish(r, ch, s, t1, t2, true);
+                    }
+                } else {
+                    uint32_t last = 0;
+                    if (lane == 0) {
+                        double2* part = reinterpret_cast<double2*>(g.partials) + ch * g.S;
+                        part[s] = make_double2(t1, t2);
+                        if (TRAIN) red_release_add_u32(g.counters + ch, 1u);
+                        else last = atom_acq_rel_add_u32(g.counters + ch, 1u) == uint32_t(g.S - 1);
+                    }
+                    if (!TRAIN && __shfl_sync(0xffffffffu, last, 0)) {
+                        // the other slices have all published: acquire and merge
+                        if (ld_acquire_u32(g.counters + ch) < uint32_t(g.S)) bad = true;
+                        merge_partials(ch, t1, t2);
+                        if (lane == 0) finish(r, ch, s, t1, t2, true);
+                    }
+                }
+            }
+            named_barrier(1, kRingConsumers);
+        };
+
+        if (TRAIN && rd.valid(0)) pass1(0);
+        for (int r = 0; rd.valid(r); ++r) {
+            if constexpr (!TRAIN) {
+                pass1(r);
+                continue;
+            }
+            int64_t ch;
+            int s;
+            uint32_t b0, b1;
+            rd.range(r, ch, s, b0, b1);
+            if (rd.valid(r + 1)) pass1(r + 1);
+            if (warp == 0) {
+                double t1 = keep[r & 1].x, t2 = keep[r & 1].y;
+                if (g.S > 1) {
+                    if (!wait_count(g.counters + ch, uint32_t(g.S))) bad = true;
+                    merge_partials(ch, t1, t2);
+                }
+                if (lane == 0) finish(r, ch, s, t1, t2, s == 0);
+            }
+            named_barrier(1, kRingConsumers);
+
+            // ---- dx = w*rstd*(dz - sum(dz)/M - xhat*sum(dz*xhat)/M) ----
+            const float mu = a.mean_in[ch];
+            const float rs = a.rstd_in[ch];
+            const float wc = a.w ? a.w[ch] : 1.f;
+            const float bc = a.b ? a.b[ch] : 0.f;
+            const float scale = wc * rs;
+            const float shift = bc - mu * scale;
+            const float c1 = s_c1[r & 1];
+            const float c2 = s_c2[r & 1];
+            for (uint32_t cb = b0; cb < b1; cb += span) {
+                const uint32_t n = b1 - cb < span ? b1 - cb : span;
+                const int slot = ring_take(rg, bad);
+                const uint4* sd = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
+                const uint4* sx = sd + span * 32;
+                const uint4* sr = sx + span * 32;
+                const uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
+                for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
+                    const BlockPos p = block_pos(g, cb + i, lane, ch);
+                    if (p.v >= g.lv) continue;
+                    Pack<T, VE> pdy, px;
+                    pdy.u = sd[i * 32 + lane];
+                    px.u = sx[i * 32 + lane];
+                    float dyv[VE], xv[VE], dz[VE], o[VE];
+                    unpack<T, VE>(pdy, dyv);
+                    unpack<T, VE>(px, xv);
+                    ring_dz<T, VE>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
+#pragma unroll
+                    for (int k = 0; k < VE; ++k) {
+                        const float xh = (xv[k] - mu) * rs;
+                        o[k] = scale * (dz[k] - c1 - xh * c2);
+                    }
+                    store_vec_pol<T, VE>(dx + (p.seg * g.lv + p.v) * VE, o, pol_stream);
+                }
+                ring_give(rg, slot, lane);
+            }
+        }
+    }
+
+    if (bad) s_bad = 1;
+    __syncthreads();
+    if (threadIdx.x == 0 && s_bad) atomicOr(a.err, kErrTimeoutStage | kErrTimeoutPeers);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -771,8 +1361,56 @@ inline nrm_status bn_plan(BnPlan& pl, const BnArgs& a, int ve, size_t stage_byte
     return NRM_OK;
 }
 
+// Plan of a ring kernel: `smem` bytes of slots, `kept` tensors per element
+// held in L2 between the two passes of a round (0 in eval).  S and k trade
+// rounds (each with a fixed cost) against the L2 held by two rounds.
+inline nrm_status bn_plan_ring(BnPlan& pl, const BnArgs& a, const void* fn, size_t smem, int kept) {
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    BnGeom& g = pl.g;
+    pl.smem = smem;
+    nrm_status st = prepare_kernel(fn, pl.smem, false);
+    if (st != NRM_OK) return st;
+    const int occ = cached_occupancy(fn, kRingThreads, pl.smem);
+    if (occ < 1) return fail(NRM_ERR_CUDA, "batchnorm kernel cannot be resident");
+    const int64_t G = int64_t(occ) * d->sms;
+    const uint64_t nb = g.nb_chan;
+    int64_t k_max = G;
+    if (kept > 0) {
+        const double chan_bytes = double(nb) * 512.0 * kept;
+        k_max = int64_t(kBnL2Budget / (2.0 * chan_bytes));
+    }
+    if (k_max < 1) k_max = 1;
+    if (k_max > G) k_max = G;
+    if (k_max > a.c) k_max = a.c;
+    const int64_t s_cap = nb / uint64_t(kSlotBlocks) > 0 ? int64_t(nb / uint64_t(kSlotBlocks)) : 1;
+    int64_t best_S = 1;
+    double best = 1e300;
+    for (int64_t k = 1; k <= k_max; ++k) {
+        int64_t S = G / k;
+        if (S > s_cap) S = s_cap;
+        if (S > bn_max_slices(*d)) S = bn_max_slices(*d);
+        if (S < 1) S = 1;
+        const int64_t kk = G / S;
+        const int64_t rounds = (a.c + kk - 1) / kk;
+        const double cost = double(rounds) * (double((nb + S - 1) / S) + kBnRoundOverheadBlocks);
+        if (cost < best) {
+            best = cost;
+            best_S = S;
+        }
+    }
+    g.S = int(best_S);
+    const int64_t k = G / best_S;
+    const int64_t items = a.c * best_S;
+    int64_t grid = k * best_S;
+    if (grid > items) grid = items;
+    pl.grid = int(grid > 0 ? grid : 1);
+    g.rounds = int((items + pl.grid - 1) / pl.grid);
+    return NRM_OK;
+}
+
 inline nrm_status launch_bn(const void* fn, const BnArgs& a, BnPlan& pl, void* ws, size_t ws_bytes,
-                            cudaStream_t s) {
+                            cudaStream_t s, int threads = kBnThreads) {
     if (a.c == 0) return NRM_OK;
     const DevInfo* d = dev_info();
     if (pl.g.S > 1) {
@@ -789,7 +1427,7 @@ inline nrm_status launch_bn(const void* fn, const BnArgs& a, BnPlan& pl, void* w
     void* kargs[] = {&args, &geom};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(pl.grid));
-    cfg.blockDim = dim3(kBnThreads);
+    cfg.blockDim = dim3(unsigned(threads));
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -802,6 +1440,15 @@ inline nrm_status launch_bn(const void* fn, const BnArgs& a, BnPlan& pl, void* w
 
 template <typename T>
 nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_bytes, cudaStream_t s) {
+    if (vec && a.c > 0 && a.n * a.l > 0) {
+        const void* fn = training ? (const void*)&bn_fwd_ring_kernel<T, true>
+                                  : (const void*)&bn_fwd_ring_kernel<T, false>;
+        BnPlan pl;
+        bn_geometry(pl.g, a, kVec<T>);
+        nrm_status st = bn_plan_ring(pl, a, fn, size_t(kRingSlotsFwd) * kSlotBytes, training ? 1 : 0);
+        if (st != NRM_OK) return st;
+        return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads);
+    }
     const int ve = vec ? kVec<T> : 1;
     const void* fn;
     if (training)
@@ -816,6 +1463,18 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
 
 template <typename T>
 nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_bytes, cudaStream_t s) {
+    if (vec && a.c > 0 && a.n * a.l > 0) {
+        const void* fn = training ? (const void*)&bn_bwd_ring_kernel<T, true>
+                                  : (const void*)&bn_bwd_ring_kernel<T, false>;
+        BnPlan pl;
+        bn_geometry(pl.g, a, kVec<T>);
+        const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
+        const int nt = (need_z && a.res) ? 3 : 2;
+        const size_t smem = size_t(kRingSlotsBwd) * (kSlotBytes + kSlotMaskWords * sizeof(uint32_t));
+        nrm_status st = bn_plan_ring(pl, a, fn, smem, training ? nt : 0);
+        if (st != NRM_OK) return st;
+        return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads);
+    }
     const int ve = vec ? kVec<T> : 1;
     const void* fn;
     if (training)
