@@ -221,6 +221,12 @@ struct Rounds {
     __device__ bool valid(int r) const {
         return r < g.rounds && int64_t(blockIdx.x) + int64_t(r) * gridDim.x < items;
     }
+    // number of valid rounds of this CTA
+    __device__ int count() const {
+        if (int64_t(blockIdx.x) >= items) return 0;
+        const int64_t n = (items - int64_t(blockIdx.x) + gridDim.x - 1) / gridDim.x;
+        return n < g.rounds ? int(n) : g.rounds;
+    }
     __device__ void range(int r, int64_t& ch, int& s, uint32_t& b0, uint32_t& b1) const {
         const int64_t it = int64_t(blockIdx.x) + int64_t(r) * gridDim.x;
         ch = it / g.S;
@@ -406,25 +412,31 @@ bn_fwd_kernel(const BnArgs a, const BnGeom g) {
 }
 
 // ---------------------------------------------------------------------------
-// 16-byte vectors: a TMA producer warp and 16 consumer warps
+// 16-byte vectors: warp-specialised ring kernels
 // ---------------------------------------------------------------------------
-// The producer warp streams a CTA's passes in chunks through a ring of 32 KB
-// shared-memory slots (the bulk copy engine moves the tensors, the warp's
-// lanes move ReLU-mask words with 4-byte async copies).  A chunk of a pass
-// over nt tensors holds 64/nt blocks of each.  The consumer warps compute
-// from the slots, release them, and synchronise only among themselves (named
-// barrier 1), so while they wait for a channel's slices the producer keeps
-// the ring full and HBM busy.  Both sides walk the same sequence of chunks.
+// Three roles per CTA.  The producer warp streams the CTA's passes in chunks
+// through a ring of 32 KB shared-memory slots (the bulk copy engine moves the
+// tensors, the warp's lanes move ReLU-mask words with 4-byte async copies); a
+// chunk of a pass over nt tensors holds 64/nt blocks of each.  16 consumer
+// warps compute from the slots and release them.  The bookkeeper warp does
+// everything that waits on memory latency or on other CTAs -- per-round
+// channel parameters, publishing the CTA's partial sums, merging a channel's
+// slices -- and trades results with the consumers through mbarrier
+// handoffs in shared memory, so the consumers never stop for it unless the
+// channel itself is late.  Every handoff is a ready/free barrier pair, every
+// wait is bounded.
 constexpr int kRingConsumerWarps = 16;
-constexpr int kRingConsumers = kRingConsumerWarps * 32;
-constexpr int kRingThreads = kRingConsumers + 32;
+constexpr int kProducerWarp = kRingConsumerWarps;
+constexpr int kBookkeeperWarp = kRingConsumerWarps + 1;
+constexpr int kRingThreads = (kRingConsumerWarps + 2) * 32;
 constexpr int kSlotBlocks = 64;                    // 512-byte blocks per slot
 constexpr int kSlotBytes = kSlotBlocks * 512;
 constexpr int kSlotMaskWords = 32 * 8;             // mask words of a chunk of >= 2 tensors
 constexpr int kRingSlotsFwd = 7;
 constexpr int kRingSlotsBwd = 6;
+constexpr int kRingUnrollL2 = 3;                   // blocks per warp in flight when reading L2 directly
 
-__device__ __forceinline__ uint32_t chunk_span(int nt) { return uint32_t(kSlotBlocks / nt); }
+__host__ __device__ constexpr uint32_t chunk_span(int nt) { return uint32_t(kSlotBlocks / nt); }
 
 // Calls f(sample n, first block lo, end block hi) for each (sample, channel)
 // segment that blocks [b0, b1) of a channel touch.
@@ -461,53 +473,64 @@ struct Ring {
     __device__ uint32_t use() const { return uint32_t(seq / SLOTS); }
 };
 
-// Producer (whole warp): the chunks of round r's slice for pass `ps`.
+// Producer (whole warp): one chunk, blocks [cb, ce) of round r's slice, of
+// pass `ps`.
 template <typename T, int VE, int SLOTS>
-__device__ void ring_produce(Ring<SLOTS>& rg, const Rounds& rd, int r, const RingPass<T>& ps, int lane,
-                             bool& bad) {
+__device__ void ring_produce_chunk(Ring<SLOTS>& rg, const Rounds& rd, int r, const RingPass<T>& ps, uint32_t cb,
+                                   uint32_t ce, int lane, bool& bad) {
     const BnGeom& g = rd.g;
     int64_t ch;
     int s;
     uint32_t b0, b1;
     rd.range(r, ch, s, b0, b1);
     const uint32_t span = chunk_span(ps.nt);
-    for (uint32_t cb = b0; cb < b1; cb += span) {
-        const uint32_t ce = b1 - cb < span ? b1 : cb + span;
-        const int slot = rg.slot();
-        const uint32_t use = rg.use();
-        if (use > 0 && !mbar_wait_bounded(&rg.empty[slot], (use - 1) & 1u, kBnWaitLimitNs)) bad = true;
-        unsigned char* base = rg.data + size_t(slot) * kSlotBytes;
-        if (lane == 0) {
-            uint32_t bytes = 0;
-            for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
-                const uint32_t v_lo = (lo - n * g.nbs) * 32;
-                const uint32_t v_hi = min((hi - n * g.nbs) * 32, uint32_t(g.lv));
-                bytes += (v_hi - v_lo) * 16;
-            });
-            mbar_arrive_expect_tx(&rg.full[slot], bytes * uint32_t(ps.nt));
-            for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
-                const uint32_t v_lo = (lo - n * g.nbs) * 32;
-                const uint32_t v_hi = min((hi - n * g.nbs) * 32, uint32_t(g.lv));
-                const int64_t e = ((int64_t(n) * g.c + ch) * g.lv + v_lo) * VE;
-                const size_t off = size_t(lo - cb) * 512;
-                for (int t = 0; t < ps.nt; ++t)
-                    bulk_g2s(base + size_t(t) * span * 512 + off, ps.t[t] + e, (v_hi - v_lo) * 16, &rg.full[slot],
-                             ps.pol[t]);
-            });
-        }
-        if (ps.mask) {
-            uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
-            for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
-                const uint32_t w_lo = (lo - n * g.nbs) * VE;
-                const uint32_t w_hi = min((hi - n * g.nbs) * VE, uint32_t(g.words));
-                const uint32_t* src = ps.mask + (int64_t(n) * g.c + ch) * g.words;
-                uint32_t* dst = mw + (lo - cb) * VE;
-                for (uint32_t w = w_lo + lane; w < w_hi; w += 32) cp_async_4(dst + (w - w_lo), src + w);
-            });
-            cp_async_mbar_arrive_noinc(&rg.full[slot]);
-        }
-        ++rg.seq;
+    const int slot = rg.slot();
+    const uint32_t use = rg.use();
+    if (use > 0 && !mbar_wait_bounded(&rg.empty[slot], (use - 1) & 1u, kBnWaitLimitNs)) bad = true;
+    unsigned char* base = rg.data + size_t(slot) * kSlotBytes;
+    if (lane == 0) {
+        uint32_t bytes = 0;
+        for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
+            const uint32_t v_lo = (lo - n * g.nbs) * 32;
+            const uint32_t v_hi = min((hi - n * g.nbs) * 32, uint32_t(g.lv));
+            bytes += (v_hi - v_lo) * 16;
+        });
+        mbar_arrive_expect_tx(&rg.full[slot], bytes * uint32_t(ps.nt));
+        for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
+            const uint32_t v_lo = (lo - n * g.nbs) * 32;
+            const uint32_t v_hi = min((hi - n * g.nbs) * 32, uint32_t(g.lv));
+            const int64_t e = ((int64_t(n) * g.c + ch) * g.lv + v_lo) * VE;
+            const size_t off = size_t(lo - cb) * 512;
+            for (int t = 0; t < ps.nt; ++t)
+                bulk_g2s(base + size_t(t) * span * 512 + off, ps.t[t] + e, (v_hi - v_lo) * 16, &rg.full[slot],
+                         ps.pol[t]);
+        });
     }
+    if (ps.mask) {
+        uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
+        for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
+            const uint32_t w_lo = (lo - n * g.nbs) * VE;
+            const uint32_t w_hi = min((hi - n * g.nbs) * VE, uint32_t(g.words));
+            const uint32_t* src = ps.mask + (int64_t(n) * g.c + ch) * g.words;
+            uint32_t* dst = mw + (lo - cb) * VE;
+            for (uint32_t w = w_lo + lane; w < w_hi; w += 32) cp_async_4(dst + (w - w_lo), src + w);
+        });
+        cp_async_mbar_arrive_noinc(&rg.full[slot]);
+    }
+    ++rg.seq;
+}
+
+// Producer (whole warp): all chunks of round r's slice for pass `ps`.
+template <typename T, int VE, int SLOTS>
+__device__ void ring_produce(Ring<SLOTS>& rg, const Rounds& rd, int r, const RingPass<T>& ps, int lane,
+                             bool& bad) {
+    int64_t ch;
+    int s;
+    uint32_t b0, b1;
+    rd.range(r, ch, s, b0, b1);
+    const uint32_t span = chunk_span(ps.nt);
+    for (uint32_t cb = b0; cb < b1; cb += span)
+        ring_produce_chunk<T, VE>(rg, rd, r, ps, cb, b1 - cb < span ? b1 : cb + span, lane, bad);
 }
 
 // Consumer side of one chunk: wait until it has landed / hand the slot back.
@@ -535,6 +558,32 @@ __device__ __forceinline__ void ring_init(Ring<SLOTS>& rg, uint32_t full_count) 
     }
 }
 
+// Bookkeeper <-> consumer handoffs: per-warp partial sums (by pass parity),
+// a round's coefficients (by round parity), a round's channel parameters (by
+// round mod 4).  "ready" completes when the writer side has arrived, "free"
+// when the reader side has.
+struct Handoffs {
+    uint64_t sums_ready[2], sums_free[2];
+    uint64_t coef_ready[2], coef_free[2];
+    uint64_t par_ready[4], par_free[4];
+};
+
+__device__ __forceinline__ void handoffs_init(Handoffs& h) {
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&h.sums_ready[i], kRingConsumerWarps);
+            mbar_init(&h.sums_free[i], 1);
+            mbar_init(&h.coef_ready[i], 1);
+            mbar_init(&h.coef_free[i], kRingConsumerWarps);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&h.par_ready[i], 1);
+            mbar_init(&h.par_free[i], kRingConsumerWarps);
+        }
+        mbar_init_fence();
+    }
+}
+
 // The VE mask bits of `lane`'s vector of chunk block i, from the slot's words.
 template <int VE>
 __device__ __forceinline__ uint32_t slot_mask_bits(const uint32_t* mw, uint32_t i, int lane) {
@@ -545,8 +594,11 @@ __device__ __forceinline__ uint32_t slot_mask_bits(const uint32_t* mw, uint32_t 
 // ---------------------------------------------------------------------------
 // forward on the ring
 // ---------------------------------------------------------------------------
-// Passes: statistics of round r+1 (x, kept in L2) ahead of the apply pass of
-// round r (x from L2 and the residual, both read for the last time).
+// Consumers: statistics of round r+1 (x, kept in L2) ahead of the apply pass
+// of round r (x from L2 and the residual, both read for the last time).  The
+// bookkeeper merges each statistics pass over the 16 consumer warps and
+// publishes it, merges a channel's S slices once they have all arrived, and
+// hands the consumers the channel's scale and shift.
 template <typename T, bool TRAIN>
 __global__ void __launch_bounds__(kRingThreads, 1)
 bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
@@ -555,9 +607,9 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
     extern __shared__ __align__(128) unsigned char ring_data[];
     __shared__ __align__(8) uint64_t full[SLOTS];
     __shared__ __align__(8) uint64_t empty[SLOTS];
-    __shared__ Moments warp_m[kRingConsumerWarps];
-    __shared__ Moments keep[2];
-    __shared__ float s_scale[2], s_shift[2];  // by round parity: no barrier at the end of a round
+    __shared__ Handoffs hs;
+    __shared__ Moments warp_m[2][kRingConsumerWarps];
+    __shared__ float2 coef[2];  // (scale, shift) by round parity
     __shared__ int s_bad;
 
     const int lane = threadIdx.x & 31;
@@ -566,33 +618,138 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
     const T* __restrict__ res = reinterpret_cast<const T*>(a.res);
     T* __restrict__ y = reinterpret_cast<T*>(a.y);
     const Rounds rd(g);
+    const int nr = rd.count();
     Ring<SLOTS> rg{ring_data, nullptr, full, empty};
     bool bad = false;
 
     if (threadIdx.x == 0) s_bad = 0;
     ring_init(rg, 1);
+    handoffs_init(hs);
     __syncthreads();
 
-    if (warp == kRingConsumerWarps) {
+    if (warp == kProducerWarp) {
         // ---------------- producer ----------------
         const uint64_t pol_keep = TRAIN ? l2_evict_last() : l2_evict_first();
         const uint64_t pol_stream = l2_evict_first();
         const RingPass<T> stats{{x, nullptr, nullptr}, {pol_keep, 0, 0}, 1, nullptr};
         const RingPass<T> apply{{x, res, nullptr}, {pol_stream, pol_stream, 0}, res ? 2 : 1, nullptr};
-        if (TRAIN && rd.valid(0)) ring_produce<T, VE>(rg, rd, 0, stats, lane, bad);
-        for (int r = 0; rd.valid(r); ++r) {
-            if (TRAIN && rd.valid(r + 1)) ring_produce<T, VE>(rg, rd, r + 1, stats, lane, bad);
+        if (TRAIN && nr > 0) ring_produce<T, VE>(rg, rd, 0, stats, lane, bad);
+        for (int r = 0; r < nr; ++r) {
+            if (TRAIN && r + 1 < nr) ring_produce<T, VE>(rg, rd, r + 1, stats, lane, bad);
             ring_produce<T, VE>(rg, rd, r, apply, lane, bad);
+        }
+    } else if (warp == kBookkeeperWarp) {
+        // ---------------- bookkeeper ----------------
+        Moments keep0{0.f, 0.f, 0.f}, keep1{0.f, 0.f, 0.f};  // S == 1: statistics by round parity
+        int q_pub = TRAIN ? 0 : nr, r_mrg = 0;
+        int pre_r = -1;  // round whose weight and bias are in pre_w, pre_b
+        float pre_w = 1.f, pre_b = 0.f;
+        bool aborted = false;
+        uint64_t t_last = global_timer_ns();
+        while (q_pub < nr || r_mrg < nr) {
+            bool moved = false;
+            if (q_pub < nr && (aborted || mbar_test_wait(&hs.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
+                Moments m = lane < kRingConsumerWarps ? warp_m[q_pub & 1][lane] : Moments{0.f, 0.f, 0.f};
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hs.sums_free[q_pub & 1]);
+                warp_merge(m);
+                int64_t ch;
+                int s;
+                uint32_t b0, b1;
+                rd.range(q_pub, ch, s, b0, b1);
+                if (g.S > 1) {
+                    if (lane == 0) {
+                        float4* part = reinterpret_cast<float4*>(g.partials) + ch * g.S;
+                        part[s] = make_float4(m.n, m.mean, m.m2, 0.f);
+                        red_release_add_u32(g.counters + ch, 1u);
+                    }
+                } else if (q_pub & 1) {
+                    keep1 = m;
+                } else {
+                    keep0 = m;
+                }
+                ++q_pub;
+                moved = true;
+            }
+            if (r_mrg < nr && (!TRAIN || r_mrg < q_pub)) {
+                const uint32_t u = uint32_t(r_mrg) >> 1;
+                bool ok = u == 0 || aborted || mbar_test_wait(&hs.coef_free[r_mrg & 1], (u - 1) & 1);
+                int64_t ch;
+                int s;
+                uint32_t b0, b1;
+                rd.range(r_mrg, ch, s, b0, b1);
+                if (pre_r != r_mrg) {
+                    // issued now, used once the channel is complete
+                    pre_w = a.w ? a.w[ch] : 1.f;
+                    pre_b = a.b ? a.b[ch] : 0.f;
+                    pre_r = r_mrg;
+                }
+                if (TRAIN && ok && g.S > 1 && !aborted) {
+                    // every lane acquires: the partials may then be read directly
+                    ok = __all_sync(0xffffffffu, ld_acquire_u32(g.counters + ch) >= uint32_t(g.S));
+                }
+                if (ok) {
+                    const float wc = pre_w;
+                    const float bc = pre_b;
+                    if constexpr (TRAIN) {
+                        Moments tot = (r_mrg & 1) ? keep1 : keep0;
+                        if (g.S > 1) {
+                            const float4* part = reinterpret_cast<const float4*>(g.partials) + ch * g.S;
+                            Moments lm{0.f, 0.f, 0.f};
+                            for (int i = lane; i < g.S; i += 32) {
+                                const float4 pv = ld_cg_f4(part + i);
+                                chan_merge(lm, pv.x, pv.y, pv.z);
+                            }
+                            warp_merge(lm);
+                            tot = lm;
+                        }
+                        if (lane == 0) {
+                            const float var = tot.m2 * g.inv_m;
+                            const float rs = rsqrtf(var + a.eps);
+                            coef[r_mrg & 1] = make_float2(wc * rs, bc - tot.mean * wc * rs);
+                            mbar_arrive(&hs.coef_ready[r_mrg & 1]);
+                            if (s == 0) {
+                                if (a.save_mean) a.save_mean[ch] = tot.mean;
+                                if (a.save_rstd) a.save_rstd[ch] = rs;
+                                if (a.rm) a.rm[ch] = fmaf(a.momentum, tot.mean, (1.f - a.momentum) * a.rm[ch]);
+                                if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * a.rv[ch]);
+                            }
+                        }
+                    } else {
+                        if (lane == 0) {
+                            const float rs = rsqrtf(a.rv[ch] + a.eps);
+                            const float mu = a.rm[ch];
+                            coef[r_mrg & 1] = make_float2(wc * rs, bc - mu * wc * rs);
+                            mbar_arrive(&hs.coef_ready[r_mrg & 1]);
+                            if (s == 0) {
+                                if (a.save_mean) a.save_mean[ch] = mu;
+                                if (a.save_rstd) a.save_rstd[ch] = rs;
+                            }
+                        }
+                    }
+                    ++r_mrg;
+                    moved = true;
+                }
+            }
+            if (moved) {
+                t_last = global_timer_ns();
+            } else {
+                __nanosleep(32);
+                if (global_timer_ns() - t_last > kBnWaitLimitNs) {
+                    aborted = true;
+                    bad = true;
+                }
+            }
         }
     } else {
         // ---------------- consumers ----------------
         const uint64_t pol_stream = l2_evict_first();
-        // statistics of round r's slice, published (S > 1) or kept (S == 1)
-        auto stats = [&](int r) {
+        // statistics of round q's slice -> this warp's moments -> bookkeeper
+        auto stats = [&](int q) {
             int64_t ch;
             int s;
             uint32_t b0, b1;
-            rd.range(r, ch, s, b0, b1);
+            rd.range(q, ch, s, b0, b1);
             ShiftedSums acc;
             const uint32_t span = chunk_span(1);
             for (uint32_t cb = b0; cb < b1; cb += span) {
@@ -613,73 +770,26 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
             }
             Moments m = acc.moments();
             warp_merge(m);
-            if (lane == 0) warp_m[warp] = m;
-            named_barrier(1, kRingConsumers);
-            if (threadIdx.x == 0) {
-                Moments cta = warp_m[0];
-                for (int w = 1; w < kRingConsumerWarps; ++w) chan_merge(cta, warp_m[w].n, warp_m[w].mean, warp_m[w].m2);
-                if (g.S > 1) {
-                    float4* part = reinterpret_cast<float4*>(g.partials) + ch * g.S;
-                    part[s] = make_float4(cta.n, cta.mean, cta.m2, 0.f);
-                    red_release_add_u32(g.counters + ch, 1u);
-                } else {
-                    keep[r & 1] = cta;
-                }
+            if (lane == 0) {
+                if (q >= 2 && !mbar_wait_bounded(&hs.sums_free[q & 1], ((q >> 1) - 1) & 1, kBnWaitLimitNs)) bad = true;
+                warp_m[q & 1][warp] = m;
+                mbar_arrive(&hs.sums_ready[q & 1]);
             }
-            named_barrier(1, kRingConsumers);
         };
 
-        if (TRAIN && rd.valid(0)) stats(0);
-        for (int r = 0; rd.valid(r); ++r) {
+        if (TRAIN && nr > 0) stats(0);
+        for (int r = 0; r < nr; ++r) {
             int64_t ch;
             int s;
             uint32_t b0, b1;
             rd.range(r, ch, s, b0, b1);
-            if (TRAIN && rd.valid(r + 1)) stats(r + 1);
-            const float wc = a.w ? a.w[ch] : 1.f;
-            const float bc = a.b ? a.b[ch] : 0.f;
-            if constexpr (TRAIN) {
-                if (warp == 0) {
-                    Moments tot = keep[r & 1];
-                    if (g.S > 1) {
-                        const float4* part = reinterpret_cast<const float4*>(g.partials) + ch * g.S;
-                        if (!wait_count(g.counters + ch, uint32_t(g.S))) bad = true;
-                        Moments lm{0.f, 0.f, 0.f};
-                        for (int i = lane; i < g.S; i += 32) {
-                            const float4 pv = ld_cg_f4(part + i);
-                            chan_merge(lm, pv.x, pv.y, pv.z);
-                        }
-                        warp_merge(lm);
-                        tot = lm;
-                    }
-                    if (lane == 0) {
-                        const float var = tot.m2 * g.inv_m;
-                        const float rs = rsqrtf(var + a.eps);
-                        s_scale[r & 1] = wc * rs;
-                        s_shift[r & 1] = bc - tot.mean * wc * rs;
-                        if (s == 0) {
-                            if (a.save_mean) a.save_mean[ch] = tot.mean;
-                            if (a.save_rstd) a.save_rstd[ch] = rs;
-                            if (a.rm) a.rm[ch] = fmaf(a.momentum, tot.mean, (1.f - a.momentum) * a.rm[ch]);
-                            if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * a.rv[ch]);
-                        }
-                    }
-                }
-            } else {
-                if (threadIdx.x == 0) {
-                    const float rs = rsqrtf(a.rv[ch] + a.eps);
-                    const float mu = a.rm[ch];
-                    s_scale[r & 1] = wc * rs;
-                    s_shift[r & 1] = bc - mu * wc * rs;
-                    if (s == 0) {
-                        if (a.save_mean) a.save_mean[ch] = mu;
-                        if (a.save_rstd) a.save_rstd[ch] = rs;
-                    }
-                }
-            }
-            named_barrier(1, kRingConsumers);
-            const float scale = s_scale[r & 1];
-            const float shift = s_shift[r & 1];
+            if (TRAIN && r + 1 < nr) stats(r + 1);
+            if (!mbar_wait_bounded(&hs.coef_ready[r & 1], (r >> 1) & 1, kBnWaitLimitNs)) bad = true;
+            const float2 sc = coef[r & 1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&hs.coef_free[r & 1]);
+            const float scale = sc.x;
+            const float shift = sc.y;
 
             // ---- y = act(x*scale + shift (+ residual)) (+ ReLU mask) ----
             const uint32_t span = chunk_span(res ? 2 : 1);
@@ -1001,8 +1111,13 @@ bn_bwd_kernel(const BnArgs a, const BnGeom g) {
 // Tensors of a pass: dy, x, and the residual when z must be recomputed with
 // it; the ReLU mask words ride along in the slot.  Training: pass 1 of round
 // r+1 (dz, dres, channel sums; dy and x kept in L2) ahead of pass 2 of round
-// r (dx, dy and x re-read from L2).  Eval: one pass per round (dx = dz*scale),
-// and the last slice of a channel to finish merges the sums into dw, db.
+// r (dx), which the consumers read straight from L2 with vector loads: only
+// HBM-sourced passes use the ring, so it keeps prefetching pass 1 of the next
+// rounds while pass 2 and the channel waits run.  Eval: one pass per round
+// (dx = dz*scale).
+// The bookkeeper stages each round's channel parameters, publishes the sums,
+// merges a channel's S slices (training: into the dx coefficients; eval: in
+// the last slice to finish, into dw and db) and writes dw, db.
 
 // dz of one lane's vector from the slot: dy passed through the activation's
 // derivative at z (mask bits, or z recomputed from x and the residual).
@@ -1035,6 +1150,37 @@ __device__ __forceinline__ void ring_dz(const BnArgs& a, bool use_mask, bool nee
     }
 }
 
+// Sum by one warp of the S published (sum dz, sum dz*x) of channel ch, in a
+// fixed order.  Every lane must have acquired the complete counter first.
+__device__ __forceinline__ void merge_grad_partials(const BnGeom& g, int64_t ch, int lane, double& t1, double& t2) {
+    const double2* part = reinterpret_cast<const double2*>(g.partials) + ch * g.S;
+    double l1 = 0.0, l2 = 0.0;
+    for (int i = lane; i < g.S; i += 32) {
+        const double2 pv = ld_cg_d2(part + i);
+        l1 += pv.x;
+        l2 += pv.y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        l2 += __shfl_xor_sync(0xffffffffu, l2, o);
+    }
+    t1 = l1;
+    t2 = l2;
+}
+
+// dw, db of channel ch from its two sums: sum dz*(x - mean) = sum dz*x -
+// mean*sum dz, in double.  Returns sum dz*xhat.
+__device__ __forceinline__ double grad_center(const BnArgs& a, int64_t ch, float mu, float rs, double t1, double t2,
+                                              bool write_grads) {
+    const double t2c = t2 - double(mu) * t1;
+    if (write_grads) {
+        if (a.db) a.db[ch] = float(t1);
+        if (a.dw) a.dw[ch] = float(t2c * double(rs));
+    }
+    return t2c * double(rs);
+}
+
 template <typename T, bool TRAIN>
 __global__ void __launch_bounds__(kRingThreads, 1)
 bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
@@ -1043,9 +1189,10 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
     extern __shared__ __align__(128) unsigned char ring_data[];
     __shared__ __align__(8) uint64_t full[SLOTS];
     __shared__ __align__(8) uint64_t empty[SLOTS];
-    __shared__ double warp_s[kRingConsumerWarps][2];
-    __shared__ double2 keep[2];
-    __shared__ float s_c1[2], s_c2[2];  // by round parity
+    __shared__ Handoffs hs;
+    __shared__ double2 warp_s[2][kRingConsumerWarps];
+    __shared__ float4 par[4];   // (mean, rstd, scale, shift) by round mod 4
+    __shared__ float2 coef[2];  // dx coefficients (c1, c2) by round parity
     __shared__ int s_bad;
 
     const int lane = threadIdx.x & 31;
@@ -1059,27 +1206,132 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
     const bool use_mask = a.act == NRM_ACT_RELU && a.mask_in != nullptr;
     const int nt = (need_z && res) ? 3 : 2;
     const Rounds rd(g);
+    const int nr = rd.count();
     Ring<SLOTS> rg{ring_data, reinterpret_cast<uint32_t*>(ring_data + size_t(SLOTS) * kSlotBytes), full, empty};
     bool bad = false;
 
     if (threadIdx.x == 0) s_bad = 0;
     ring_init(rg, use_mask ? 33u : 1u);
+    handoffs_init(hs);
     __syncthreads();
 
-    if (warp == kRingConsumerWarps) {
+    if (warp == kProducerWarp) {
         // ---------------- producer ----------------
         const uint64_t pol_keep = TRAIN ? l2_evict_last() : l2_evict_first();
-        const uint64_t pol_stream = l2_evict_first();
         const uint32_t* mk = use_mask ? a.mask_in : nullptr;
         const RingPass<T> first{{dy, x, res}, {pol_keep, pol_keep, pol_keep}, nt, mk};
-        const RingPass<T> second{{dy, x, res}, {pol_stream, pol_stream, pol_stream}, nt, mk};
-        if (TRAIN && rd.valid(0)) ring_produce<T, VE>(rg, rd, 0, first, lane, bad);
-        for (int r = 0; rd.valid(r); ++r) {
-            if constexpr (TRAIN) {
-                if (rd.valid(r + 1)) ring_produce<T, VE>(rg, rd, r + 1, first, lane, bad);
-                ring_produce<T, VE>(rg, rd, r, second, lane, bad);
+        // only pass 1 streams through the ring: pass 2 reads L2 directly,
+        // so the ring keeps fetching the next rounds from HBM meanwhile
+        for (int q = 0; q < nr; ++q) ring_produce<T, VE>(rg, rd, q, first, lane, bad);
+    } else if (warp == kBookkeeperWarp) {
+        // ---------------- bookkeeper ----------------
+        double2 keep0 = make_double2(0.0, 0.0), keep1 = make_double2(0.0, 0.0);  // S == 1 (training)
+        int q_par = 0, q_pub = 0, r_mrg = TRAIN ? 0 : nr;
+        bool aborted = false;
+        uint64_t t_last = global_timer_ns();
+        while (q_par < nr || q_pub < nr || r_mrg < nr) {
+            bool moved = false;
+            // channel parameters of round q_par
+            if (q_par < nr) {
+                const uint32_t u = uint32_t(q_par) >> 2;
+                if (u == 0 || aborted || mbar_test_wait(&hs.par_free[q_par & 3], (u - 1) & 1)) {
+                    if (lane == 0) {
+                        int64_t ch;
+                        int s;
+                        uint32_t b0, b1;
+                        rd.range(q_par, ch, s, b0, b1);
+                        const float mu = a.mean_in[ch];
+                        const float rs = a.rstd_in[ch];
+                        const float wc = a.w ? a.w[ch] : 1.f;
+                        const float bc = a.b ? a.b[ch] : 0.f;
+                        const float scale = wc * rs;
+                        par[q_par & 3] = make_float4(mu, rs, scale, bc - mu * scale);
+                        mbar_arrive(&hs.par_ready[q_par & 3]);
+                    }
+                    ++q_par;
+                    moved = true;
+                }
+            }
+            // pass-1 sums of round q_pub
+            if (q_pub < nr && (aborted || mbar_test_wait(&hs.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
+                double2 v = lane < kRingConsumerWarps ? warp_s[q_pub & 1][lane] : make_double2(0.0, 0.0);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hs.sums_free[q_pub & 1]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+                    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+                }
+                int64_t ch;
+                int s;
+                uint32_t b0, b1;
+                rd.range(q_pub, ch, s, b0, b1);
+                if (g.S == 1) {
+                    if (TRAIN) {
+                        if (q_pub & 1) keep1 = v;
+                        else keep0 = v;
+                    } else if (lane == 0) {
+                        grad_center(a, ch, a.mean_in[ch], a.rstd_in[ch], v.x, v.y, true);
+                    }
+                } else {
+                    uint32_t last = 0;
+                    if (lane == 0) {
+                        double2* part = reinterpret_cast<double2*>(g.partials) + ch * g.S;
+                        part[s] = v;
+                        if (TRAIN) red_release_add_u32(g.counters + ch, 1u);
+                        else last = atom_acq_rel_add_u32(g.counters + ch, 1u) == uint32_t(g.S - 1);
+                    }
+                    if (!TRAIN && __shfl_sync(0xffffffffu, last, 0)) {
+                        // every other slice has published: merge into dw, db
+                        if (ld_acquire_u32(g.counters + ch) < uint32_t(g.S)) bad = true;
+                        double t1, t2;
+                        merge_grad_partials(g, ch, lane, t1, t2);
+                        if (lane == 0) grad_center(a, ch, a.mean_in[ch], a.rstd_in[ch], t1, t2, true);
+                    }
+                }
+                ++q_pub;
+                moved = true;
+            }
+            // training: the dx coefficients of round r_mrg once its channel is complete
+            if (TRAIN && r_mrg < nr && r_mrg < q_pub) {
+                const uint32_t u = uint32_t(r_mrg) >> 1;
+                bool ok = u == 0 || aborted || mbar_test_wait(&hs.coef_free[r_mrg & 1], (u - 1) & 1);
+                int64_t ch;
+                int s;
+                uint32_t b0, b1;
+                rd.range(r_mrg, ch, s, b0, b1);
+                if (ok && g.S > 1 && !aborted) {
+                    // every lane acquires: the partials may then be read directly
+                    ok = __all_sync(0xffffffffu, ld_acquire_u32(g.counters + ch) >= uint32_t(g.S));
+                }
+                if (ok) {
+                    double t1, t2;
+                    if (g.S > 1) {
+                        merge_grad_partials(g, ch, lane, t1, t2);
+                    } else {
+                        const double2 k = (r_mrg & 1) ? keep1 : keep0;
+                        t1 = k.x;
+                        t2 = k.y;
+                    }
+                    if (lane == 0) {
+                        // this round's parameters are still staged: its consumers free them after pass 2
+                        const float4 pr = par[r_mrg & 3];
+                        const double t2r = grad_center(a, ch, pr.x, pr.y, t1, t2, s == 0);
+                        coef[r_mrg & 1] = make_float2(float(t1 * double(g.inv_m)), float(t2r * double(g.inv_m)));
+                        mbar_arrive(&hs.coef_ready[r_mrg & 1]);
+                    }
+                    ++r_mrg;
+                    moved = true;
+                }
+            }
+            if (moved) {
+                t_last = global_timer_ns();
             } else {
-                ring_produce<T, VE>(rg, rd, r, first, lane, bad);
+                __nanosleep(32);
+                if (global_timer_ns() - t_last > kBnWaitLimitNs) {
+                    aborted = true;
+                    bad = true;
+                }
             }
         }
     } else {
@@ -1087,81 +1339,37 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
         const uint64_t pol_stream = l2_evict_first();
         const uint32_t span = chunk_span(nt);
 
-        // channel sums of warp 0's lanes -> dw, db (slice 0, or the last slice
-        // in eval) and the dx coefficients of round r
-        auto finish = [&](int r, int64_t ch, int s, double t1, double t2, bool write_grads) {
-            const float mu = a.mean_in[ch];
-            const float rs = a.rstd_in[ch];
-            // sum dz*(x - mean) = sum dz*x - mean*sum dz, in double
-            const double t2c = t2 - double(mu) * t1;
-            if (write_grads) {
-                if (a.db) a.db[ch] = float(t1);
-                if (a.dw) a.dw[ch] = float(t2c * double(rs));
-            }
-            s_c1[r & 1] = float(t1 * double(g.inv_m));
-            s_c2[r & 1] = float(t2c * double(rs) * double(g.inv_m));
-            (void)s;
-        };
-        // sum of the S partials of channel ch by warp 0 in a fixed order
-        auto merge_partials = [&](int64_t ch, double& t1, double& t2) {
-            const double2* part = reinterpret_cast<const double2*>(g.partials) + ch * g.S;
-            double l1 = 0.0, l2 = 0.0;
-            for (int i = lane; i < g.S; i += 32) {
-                const double2 pv = ld_cg_d2(part + i);
-                l1 += pv.x;
-                l2 += pv.y;
-            }
+        // one chunk of pass 1: dz, dres (and dx in eval), the two channel sums
+        auto chunk1 = [&](int64_t ch, float scale, float shift, uint32_t cb, uint32_t n, GradSums& acc) {
+            const int slot = ring_take(rg, bad);
+            const uint4* sd = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
+            const uint4* sx = sd + span * 32;
+            const uint4* sr = sx + span * 32;
+            const uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
+            for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
+                const BlockPos p = block_pos(g, cb + i, lane, ch);
+                if (p.v >= g.lv) continue;
+                Pack<T, VE> pdy, px;
+                pdy.u = sd[i * 32 + lane];
+                px.u = sx[i * 32 + lane];
+                float dyv[VE], xv[VE], dz[VE];
+                unpack<T, VE>(pdy, dyv);
+                unpack<T, VE>(px, xv);
+                ring_dz<T, VE>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
+                const int64_t e = (p.seg * g.lv + p.v) * VE;
+                if (dres) store_vec_pol<T, VE>(dres + e, dz, pol_stream);
+                acc.add(dz, xv);
+                if constexpr (!TRAIN) {
+                    float o[VE];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-                l2 += __shfl_xor_sync(0xffffffffu, l2, o);
-            }
-            t1 = l1;
-            t2 = l2;
-        };
-
-        // pass 1 of round r: dz, dres (and dx in eval), the two channel sums
-        auto pass1 = [&](int r) {
-            int64_t ch;
-            int s;
-            uint32_t b0, b1;
-            rd.range(r, ch, s, b0, b1);
-            const float mu = a.mean_in[ch];
-            const float rs = a.rstd_in[ch];
-            const float wc = a.w ? a.w[ch] : 1.f;
-            const float bc = a.b ? a.b[ch] : 0.f;
-            const float scale = wc * rs;
-            const float shift = bc - mu * scale;
-            GradSums acc;
-            for (uint32_t cb = b0; cb < b1; cb += span) {
-                const uint32_t n = b1 - cb < span ? b1 - cb : span;
-                const int slot = ring_take(rg, bad);
-                const uint4* sd = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
-                const uint4* sx = sd + span * 32;
-                const uint4* sr = sx + span * 32;
-                const uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
-                for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
-                    const BlockPos p = block_pos(g, cb + i, lane, ch);
-                    if (p.v >= g.lv) continue;
-                    Pack<T, VE> pdy, px;
-                    pdy.u = sd[i * 32 + lane];
-                    px.u = sx[i * 32 + lane];
-                    float dyv[VE], xv[VE], dz[VE];
-                    unpack<T, VE>(pdy, dyv);
-                    unpack<T, VE>(px, xv);
-                    ring_dz<T, VE>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
-                    const int64_t e = (p.seg * g.lv + p.v) * VE;
-                    if (dres) store_vec_pol<T, VE>(dres + e, dz, pol_stream);
-                    acc.add(dz, xv);
-                    if constexpr (!TRAIN) {
-                        float o[VE];
-#pragma unroll
-                        for (int k = 0; k < VE; ++k) o[k] = dz[k] * scale;
-                        store_vec_pol<T, VE>(dx + e, o, pol_stream);
-                    }
+                    for (int k = 0; k < VE; ++k) o[k] = dz[k] * scale;
+                    store_vec_pol<T, VE>(dx + e, o, pol_stream);
                 }
-                ring_give(rg, slot, lane);
             }
+            ring_give(rg, slot, lane);
+        };
+        // this warp's pass-1 sums of round q -> bookkeeper
+        auto publish = [&](int q, const GradSums& acc) {
             double d1 = acc.sum_dz(), d2 = acc.sum_dzx();
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -1169,97 +1377,86 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
                 d2 += __shfl_xor_sync(0xffffffffu, d2, o);
             }
             if (lane == 0) {
-                warp_s[warp][0] = d1;
-                warp_s[warp][1] = d2;
+                if (q >= 2 && !mbar_wait_bounded(&hs.sums_free[q & 1], ((q >> 1) - 1) & 1, kBnWaitLimitNs)) bad = true;
+                warp_s[q & 1][warp] = make_double2(d1, d2);
+                mbar_arrive(&hs.sums_ready[q & 1]);
+                if (!TRAIN) mbar_arrive(&hs.par_free[q & 3]);
             }
-            named_barrier(1, kRingConsumers);
-            if (warp == 0) {
-                double t1 = 0.0, t2 = 0.0;
-                if (lane == 0) {
-                    for (int w = 0; w < kRingConsumerWarps; ++w) {
-                        t1 += warp_s[w][0];
-                        t2 += warp_s[w][1];
-                    }
-                }
-                if (g.S == 1) {
-                    if (lane == 0) {
-                        if (TRAIN) keep[r & 1] = make_double2(t1, t2);
-                        else finish(r, ch, s, t1, t2, true);
-                    }
-                } else {
-                    uint32_t last = 0;
-                    if (lane == 0) {
-                        double2* part = reinterpret_cast<double2*>(g.partials) + ch * g.S;
-                        part[s] = make_double2(t1, t2);
-                        if (TRAIN) red_release_add_u32(g.counters + ch, 1u);
-                        else last = atom_acq_rel_add_u32(g.counters + ch, 1u) == uint32_t(g.S - 1);
-                    }
-                    if (!TRAIN && __shfl_sync(0xffffffffu, last, 0)) {
-                        // the other slices have all published: acquire and merge
-                        if (ld_acquire_u32(g.counters + ch) < uint32_t(g.S)) bad = true;
-                        merge_partials(ch, t1, t2);
-                        if (lane == 0) finish(r, ch, s, t1, t2, true);
-                    }
-                }
-            }
-            named_barrier(1, kRingConsumers);
         };
-
-        if (TRAIN && rd.valid(0)) pass1(0);
-        for (int r = 0; rd.valid(r); ++r) {
-            if constexpr (!TRAIN) {
-                pass1(r);
-                continue;
-            }
+        // channel parameters (mean, rstd, scale, shift) of round q
+        auto params = [&](int q) {
+            if (!mbar_wait_bounded(&hs.par_ready[q & 3], (q >> 2) & 1, kBnWaitLimitNs)) bad = true;
+            return par[q & 3];
+        };
+        auto pass1 = [&](int q) {
             int64_t ch;
             int s;
             uint32_t b0, b1;
-            rd.range(r, ch, s, b0, b1);
-            if (rd.valid(r + 1)) pass1(r + 1);
-            if (warp == 0) {
-                double t1 = keep[r & 1].x, t2 = keep[r & 1].y;
-                if (g.S > 1) {
-                    if (!wait_count(g.counters + ch, uint32_t(g.S))) bad = true;
-                    merge_partials(ch, t1, t2);
-                }
-                if (lane == 0) finish(r, ch, s, t1, t2, s == 0);
-            }
-            named_barrier(1, kRingConsumers);
+            rd.range(q, ch, s, b0, b1);
+            const float4 pr = params(q);
+            GradSums acc;
+            for (uint32_t cb = b0; cb < b1; cb += span) chunk1(ch, pr.z, pr.w, cb, min(span, b1 - cb), acc);
+            publish(q, acc);
+        };
 
-            // ---- dx = w*rstd*(dz - sum(dz)/M - xhat*sum(dz*xhat)/M) ----
-            const float mu = a.mean_in[ch];
-            const float rs = a.rstd_in[ch];
-            const float wc = a.w ? a.w[ch] : 1.f;
-            const float bc = a.b ? a.b[ch] : 0.f;
-            const float scale = wc * rs;
-            const float shift = bc - mu * scale;
-            const float c1 = s_c1[r & 1];
-            const float c2 = s_c2[r & 1];
-            for (uint32_t cb = b0; cb < b1; cb += span) {
-                const uint32_t n = b1 - cb < span ? b1 - cb : span;
-                const int slot = ring_take(rg, bad);
-                const uint4* sd = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
-                const uint4* sx = sd + span * 32;
-                const uint4* sr = sx + span * 32;
-                const uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
-                for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
-                    const BlockPos p = block_pos(g, cb + i, lane, ch);
-                    if (p.v >= g.lv) continue;
-                    Pack<T, VE> pdy, px;
-                    pdy.u = sd[i * 32 + lane];
-                    px.u = sx[i * 32 + lane];
-                    float dyv[VE], xv[VE], dz[VE], o[VE];
-                    unpack<T, VE>(pdy, dyv);
-                    unpack<T, VE>(px, xv);
-                    ring_dz<T, VE>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
+        if constexpr (!TRAIN) {
+            for (int q = 0; q < nr; ++q) pass1(q);
+        } else {
+            if (nr > 0) pass1(0);
+            for (int r = 0; r < nr; ++r) {
+                int64_t ch;
+                int s;
+                uint32_t b0, b1;
+                rd.range(r, ch, s, b0, b1);
+                if (r + 1 < nr) pass1(r + 1);
+                const float4 pr = par[r & 3];  // waited for in pass 1 of round r; freed below
+                const float mu = pr.x, rs = pr.y, scale = pr.z, shift = pr.w;
+                if (!mbar_wait_bounded(&hs.coef_ready[r & 1], (r >> 1) & 1, kBnWaitLimitNs)) bad = true;
+                const float2 cc = coef[r & 1];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hs.coef_free[r & 1]);
+                const float c1 = cc.x, c2 = cc.y;
+                // ---- pass 2: dx = w*rstd*(dz - sum(dz)/M - xhat*sum(dz*xhat)/M), from L2 ----
+                for (uint32_t base = b0 + warp; base < b1; base += kRingConsumerWarps * kRingUnrollL2) {
+                    Pack<T, VE> pdy[kRingUnrollL2], px[kRingUnrollL2];
+                    uint32_t mbits[kRingUnrollL2];
 #pragma unroll
-                    for (int k = 0; k < VE; ++k) {
-                        const float xh = (xv[k] - mu) * rs;
-                        o[k] = scale * (dz[k] - c1 - xh * c2);
+                    for (int u = 0; u < kRingUnrollL2; ++u) {
+                        const uint32_t bi = base + u * kRingConsumerWarps;
+                        if (bi < b1) {
+                            const BlockPos p = block_pos(g, bi, lane, ch);
+                            if (p.v < g.lv) {
+                                raw_load_pol<T, VE>(dy, p.seg * g.lv + p.v, pdy[u], pol_stream);
+                                raw_load_pol<T, VE>(x, p.seg * g.lv + p.v, px[u], pol_stream);
+                                if (use_mask) mbits[u] = load_mask_bits<VE>(a.mask_in, g, p, lane, pol_stream);
+                            }
+                        }
                     }
-                    store_vec_pol<T, VE>(dx + (p.seg * g.lv + p.v) * VE, o, pol_stream);
+#pragma unroll
+                    for (int u = 0; u < kRingUnrollL2; ++u) {
+                        const uint32_t bi = base + u * kRingConsumerWarps;
+                        if (bi >= b1) break;
+                        const BlockPos p = block_pos(g, bi, lane, ch);
+                        if (p.v >= g.lv) continue;
+                        float dyv[VE], xv[VE], dz[VE], o[VE];
+                        unpack<T, VE>(pdy[u], dyv);
+                        unpack<T, VE>(px[u], xv);
+                        if (use_mask) {
+#pragma unroll
+                            for (int k = 0; k < VE; ++k) dz[k] = ((mbits[u] >> k) & 1u) ? dyv[k] : 0.f;
+                        } else {
+                            form_dz<T, VE>(a, g, p, lane, need_z, scale, shift, dyv, xv, dz, pol_stream);
+                        }
+#pragma unroll
+                        for (int k = 0; k < VE; ++k) {
+                            const float xh = (xv[k] - mu) * rs;
+                            o[k] = scale * (dz[k] - c1 - xh * c2);
+                        }
+                        store_vec_pol<T, VE>(dx + (p.seg * g.lv + p.v) * VE, o, pol_stream);
+                    }
                 }
-                ring_give(rg, slot, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hs.par_free[r & 3]);
             }
         }
     }
@@ -1306,9 +1503,15 @@ inline void bn_geometry(BnGeom& g, const BnArgs& a, int ve) {
 
 // L2 held by the slices of two rounds in flight (the statistics pass of
 // round r+1 overlaps the apply pass of round r).
-constexpr double kBnL2Budget = 48.0 * 1024 * 1024;
+#ifndef NRM_BN_L2_BUDGET_MB
+#define NRM_BN_L2_BUDGET_MB 48
+#endif
+#ifndef NRM_BN_ROUND_OVERHEAD
+#define NRM_BN_ROUND_OVERHEAD 32
+#endif
+constexpr double kBnL2Budget = double(NRM_BN_L2_BUDGET_MB) * 1024 * 1024;
 // Fixed cost of a round (channel barrier, reductions), in blocks of work.
-constexpr double kBnRoundOverheadBlocks = 32.0;
+constexpr double kBnRoundOverheadBlocks = double(NRM_BN_ROUND_OVERHEAD);
 
 // Chooses k channels per round and S = G/k slices per channel (the grid is a
 // whole number of channels, every CTA resident).  `stage_bytes` is the bytes
@@ -1362,9 +1565,9 @@ inline nrm_status bn_plan(BnPlan& pl, const BnArgs& a, int ve, size_t stage_byte
 }
 
 // Plan of a ring kernel: `smem` bytes of slots, `kept` tensors per element
-// held in L2 between the two passes of a round (0 in eval).  S and k trade
-// rounds (each with a fixed cost) against the L2 held by two rounds.
-inline nrm_status bn_plan_ring(BnPlan& pl, const BnArgs& a, const void* fn, size_t smem, int kept) {
+// held in L2 between the two passes of a round (0 in eval) for `held` rounds
+// at a time.  S and k trade rounds (each with a fixed cost) against L2.
+inline nrm_status bn_plan_ring(BnPlan& pl, const BnArgs& a, const void* fn, size_t smem, int kept, int held) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     BnGeom& g = pl.g;
@@ -1378,12 +1581,13 @@ inline nrm_status bn_plan_ring(BnPlan& pl, const BnArgs& a, const void* fn, size
     int64_t k_max = G;
     if (kept > 0) {
         const double chan_bytes = double(nb) * 512.0 * kept;
-        k_max = int64_t(kBnL2Budget / (2.0 * chan_bytes));
+        k_max = int64_t(kBnL2Budget / (double(held) * chan_bytes));
     }
     if (k_max < 1) k_max = 1;
     if (k_max > G) k_max = G;
     if (k_max > a.c) k_max = a.c;
-    const int64_t s_cap = nb / uint64_t(kSlotBlocks) > 0 ? int64_t(nb / uint64_t(kSlotBlocks)) : 1;
+    // a slice of at least one two-tensor chunk
+    const int64_t s_cap = nb / uint64_t(chunk_span(2)) > 0 ? int64_t(nb / uint64_t(chunk_span(2))) : 1;
     int64_t best_S = 1;
     double best = 1e300;
     for (int64_t k = 1; k <= k_max; ++k) {
@@ -1406,6 +1610,8 @@ inline nrm_status bn_plan_ring(BnPlan& pl, const BnArgs& a, const void* fn, size
     if (grid > items) grid = items;
     pl.grid = int(grid > 0 ? grid : 1);
     g.rounds = int((items + pl.grid - 1) / pl.grid);
+    // the kernels rely on a CTA keeping the same slice in every round
+    if (g.rounds > 1 && pl.grid % g.S != 0) return fail(NRM_ERR_CUDA, "batchnorm plan: grid not a multiple of S");
     return NRM_OK;
 }
 
@@ -1445,7 +1651,7 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
                                   : (const void*)&bn_fwd_ring_kernel<T, false>;
         BnPlan pl;
         bn_geometry(pl.g, a, kVec<T>);
-        nrm_status st = bn_plan_ring(pl, a, fn, size_t(kRingSlotsFwd) * kSlotBytes, training ? 1 : 0);
+        nrm_status st = bn_plan_ring(pl, a, fn, size_t(kRingSlotsFwd) * kSlotBytes, training ? 1 : 0, 2);
         if (st != NRM_OK) return st;
         return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads);
     }
@@ -1471,7 +1677,7 @@ nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
         const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
         const int nt = (need_z && a.res) ? 3 : 2;
         const size_t smem = size_t(kRingSlotsBwd) * (kSlotBytes + kSlotMaskWords * sizeof(uint32_t));
-        nrm_status st = bn_plan_ring(pl, a, fn, smem, training ? nt : 0);
+        nrm_status st = bn_plan_ring(pl, a, fn, smem, training ? nt : 0, 2);
         if (st != NRM_OK) return st;
         return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads);
     }
