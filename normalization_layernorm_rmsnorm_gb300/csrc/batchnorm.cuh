@@ -434,7 +434,12 @@ constexpr int kSlotBytes = kSlotBlocks * 512;
 constexpr int kSlotMaskWords = 32 * 8;             // mask words of a chunk of >= 2 tensors
 constexpr int kRingSlotsFwd = 7;
 constexpr int kRingSlotsBwd = 6;
-constexpr int kRingUnrollL2 = 3;                   // blocks per warp in flight when reading L2 directly
+// training backward: pass 1 (HBM) and pass 2 (L2 re-reads) on separate rings
+// with one producer each, so pass 2 never holds up the HBM stream
+constexpr int kRingSlotsBwdHbm = 4;
+constexpr int kRingSlotsBwdL2 = 2;
+constexpr int kProducer2Warp = kRingConsumerWarps + 2;
+constexpr int kRingThreadsBwdTrain = kRingThreads + 32;
 
 __host__ __device__ constexpr uint32_t chunk_span(int nt) { return uint32_t(kSlotBlocks / nt); }
 
@@ -584,11 +589,135 @@ __device__ __forceinline__ void handoffs_init(Handoffs& h) {
     }
 }
 
+// Shared state of the consumer warps and the bookkeeper.
+struct BnFwdShared {
+    Handoffs hs;
+    Moments warp_m[2][kRingConsumerWarps];  // per-warp statistics by pass parity
+    float2 coef[2];                         // (scale, shift) by round parity
+    Moments keep[4];                        // S == 1: a round's statistics by round mod 4
+};
+struct BnBwdShared {
+    Handoffs hs;
+    double2 warp_s[2][kRingConsumerWarps];  // per-warp (sum dz, sum dz*x) by pass parity
+    float4 par[4];                          // (mean, rstd, scale, shift) by round mod 4
+    float2 coef[2];                         // dx coefficients (c1, c2) by round parity
+    double2 keep[4];                        // S == 1: a round's sums by round mod 4
+};
+
 // The VE mask bits of `lane`'s vector of chunk block i, from the slot's words.
 template <int VE>
 __device__ __forceinline__ uint32_t slot_mask_bits(const uint32_t* mw, uint32_t i, int lane) {
     const int e = lane * VE;
     return (mw[i * VE + (e >> 5)] >> (e & 31)) & ((1u << VE) - 1u);
+}
+
+// Bookkeeper of a forward kernel (one warp): merges each statistics pass
+// over the consumer warps and publishes it, merges a complete channel into
+// (scale, shift) for the consumers (training; eval reads the running
+// statistics), and writes the saved and running statistics from slice 0.
+// Polls every handoff without blocking; gives up (sets `bad`) after 2 s
+// without progress.
+template <bool TRAIN>
+__device__ void fwd_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& rd, int nr, BnFwdShared& sh,
+                               int lane, bool& bad) {
+    int q_pub = TRAIN ? 0 : nr, r_mrg = 0;
+    int pre_r = -1;  // round whose weight and bias are in pre_w, pre_b
+    float pre_w = 1.f, pre_b = 0.f;
+    bool aborted = false;
+    uint64_t t_last = global_timer_ns();
+    while (q_pub < nr || r_mrg < nr) {
+        bool moved = false;
+        if (q_pub < nr && (aborted || mbar_test_wait(&sh.hs.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
+            Moments m = lane < kRingConsumerWarps ? sh.warp_m[q_pub & 1][lane] : Moments{0.f, 0.f, 0.f};
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.hs.sums_free[q_pub & 1]);
+            warp_merge(m);
+            int64_t ch;
+            int s;
+            uint32_t b0, b1;
+            rd.range(q_pub, ch, s, b0, b1);
+            if (g.S > 1) {
+                if (lane == 0) {
+                    float4* part = reinterpret_cast<float4*>(g.partials) + ch * g.S;
+                    part[s] = make_float4(m.n, m.mean, m.m2, 0.f);
+                    red_release_add_u32(g.counters + ch, 1u);
+                }
+            } else if (lane == 0) {
+                sh.keep[q_pub & 3] = m;
+            }
+            ++q_pub;
+            moved = true;
+        }
+        if (r_mrg < nr && (!TRAIN || r_mrg < q_pub)) {
+            const uint32_t u = uint32_t(r_mrg) >> 1;
+            bool ok = u == 0 || aborted || mbar_test_wait(&sh.hs.coef_free[r_mrg & 1], (u - 1) & 1);
+            int64_t ch;
+            int s;
+            uint32_t b0, b1;
+            rd.range(r_mrg, ch, s, b0, b1);
+            if (pre_r != r_mrg) {
+                // issued now, used once the channel is complete
+                pre_w = a.w ? a.w[ch] : 1.f;
+                pre_b = a.b ? a.b[ch] : 0.f;
+                pre_r = r_mrg;
+            }
+            if (TRAIN && ok && g.S > 1 && !aborted) {
+                // every lane acquires: the partials may then be read directly
+                ok = __all_sync(0xffffffffu, ld_acquire_u32(g.counters + ch) >= uint32_t(g.S));
+            }
+            if (ok) {
+                const float wc = pre_w;
+                const float bc = pre_b;
+                if constexpr (TRAIN) {
+                    Moments tot = sh.keep[r_mrg & 3];  // lane 0's copy is the one used when S == 1
+                    if (g.S > 1) {
+                        const float4* part = reinterpret_cast<const float4*>(g.partials) + ch * g.S;
+                        Moments lm{0.f, 0.f, 0.f};
+                        for (int i = lane; i < g.S; i += 32) {
+                            const float4 pv = ld_cg_f4(part + i);
+                            chan_merge(lm, pv.x, pv.y, pv.z);
+                        }
+                        warp_merge(lm);
+                        tot = lm;
+                    }
+                    if (lane == 0) {
+                        const float var = tot.m2 * g.inv_m;
+                        const float rs = rsqrtf(var + a.eps);
+                        sh.coef[r_mrg & 1] = make_float2(wc * rs, bc - tot.mean * wc * rs);
+                        mbar_arrive(&sh.hs.coef_ready[r_mrg & 1]);
+                        if (s == 0) {
+                            if (a.save_mean) a.save_mean[ch] = tot.mean;
+                            if (a.save_rstd) a.save_rstd[ch] = rs;
+                            if (a.rm) a.rm[ch] = fmaf(a.momentum, tot.mean, (1.f - a.momentum) * a.rm[ch]);
+                            if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * a.rv[ch]);
+                        }
+                    }
+                } else {
+                    if (lane == 0) {
+                        const float rs = rsqrtf(a.rv[ch] + a.eps);
+                        const float mu = a.rm[ch];
+                        sh.coef[r_mrg & 1] = make_float2(wc * rs, bc - mu * wc * rs);
+                        mbar_arrive(&sh.hs.coef_ready[r_mrg & 1]);
+                        if (s == 0) {
+                            if (a.save_mean) a.save_mean[ch] = mu;
+                            if (a.save_rstd) a.save_rstd[ch] = rs;
+                        }
+                    }
+                }
+                ++r_mrg;
+                moved = true;
+            }
+        }
+        if (moved) {
+            t_last = global_timer_ns();
+        } else {
+            __nanosleep(32);
+            if (global_timer_ns() - t_last > kBnWaitLimitNs) {
+                aborted = true;
+                bad = true;
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -607,9 +736,7 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
     extern __shared__ __align__(128) unsigned char ring_data[];
     __shared__ __align__(8) uint64_t full[SLOTS];
     __shared__ __align__(8) uint64_t empty[SLOTS];
-    __shared__ Handoffs hs;
-    __shared__ Moments warp_m[2][kRingConsumerWarps];
-    __shared__ float2 coef[2];  // (scale, shift) by round parity
+    __shared__ BnFwdShared sh;
     __shared__ int s_bad;
 
     const int lane = threadIdx.x & 31;
@@ -624,7 +751,7 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
 
     if (threadIdx.x == 0) s_bad = 0;
     ring_init(rg, 1);
-    handoffs_init(hs);
+    handoffs_init(sh.hs);
     __syncthreads();
 
     if (warp == kProducerWarp) {
@@ -640,107 +767,7 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
         }
     } else if (warp == kBookkeeperWarp) {
         // ---------------- bookkeeper ----------------
-        Moments keep0{0.f, 0.f, 0.f}, keep1{0.f, 0.f, 0.f};  // S == 1: statistics by round parity
-        int q_pub = TRAIN ? 0 : nr, r_mrg = 0;
-        int pre_r = -1;  // round whose weight and bias are in pre_w, pre_b
-        float pre_w = 1.f, pre_b = 0.f;
-        bool aborted = false;
-        uint64_t t_last = global_timer_ns();
-        while (q_pub < nr || r_mrg < nr) {
-            bool moved = false;
-            if (q_pub < nr && (aborted || mbar_test_wait(&hs.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
-                Moments m = lane < kRingConsumerWarps ? warp_m[q_pub & 1][lane] : Moments{0.f, 0.f, 0.f};
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&hs.sums_free[q_pub & 1]);
-                warp_merge(m);
-                int64_t ch;
-                int s;
-                uint32_t b0, b1;
-                rd.range(q_pub, ch, s, b0, b1);
-                if (g.S > 1) {
-                    if (lane == 0) {
-                        float4* part = reinterpret_cast<float4*>(g.partials) + ch * g.S;
-                        part[s] = make_float4(m.n, m.mean, m.m2, 0.f);
-                        red_release_add_u32(g.counters + ch, 1u);
-                    }
-                } else if (q_pub & 1) {
-                    keep1 = m;
-                } else {
-                    keep0 = m;
-                }
-                ++q_pub;
-                moved = true;
-            }
-            if (r_mrg < nr && (!TRAIN || r_mrg < q_pub)) {
-                const uint32_t u = uint32_t(r_mrg) >> 1;
-                bool ok = u == 0 || aborted || mbar_test_wait(&hs.coef_free[r_mrg & 1], (u - 1) & 1);
-                int64_t ch;
-                int s;
-                uint32_t b0, b1;
-                rd.range(r_mrg, ch, s, b0, b1);
-                if (pre_r != r_mrg) {
-                    // issued now, used once the channel is complete
-                    pre_w = a.w ? a.w[ch] : 1.f;
-                    pre_b = a.b ? a.b[ch] : 0.f;
-                    pre_r = r_mrg;
-                }
-                if (TRAIN && ok && g.S > 1 && !aborted) {
-                    // every lane acquires: the partials may then be read directly
-                    ok = __all_sync(0xffffffffu, ld_acquire_u32(g.counters + ch) >= uint32_t(g.S));
-                }
-                if (ok) {
-                    const float wc = pre_w;
-                    const float bc = pre_b;
-                    if constexpr (TRAIN) {
-                        Moments tot = (r_mrg & 1) ? keep1 : keep0;
-                        if (g.S > 1) {
-                            const float4* part = reinterpret_cast<const float4*>(g.partials) + ch * g.S;
-                            Moments lm{0.f, 0.f, 0.f};
-                            for (int i = lane; i < g.S; i += 32) {
-                                const float4 pv = ld_cg_f4(part + i);
-                                chan_merge(lm, pv.x, pv.y, pv.z);
-                            }
-                            warp_merge(lm);
-                            tot = lm;
-                        }
-                        if (lane == 0) {
-                            const float var = tot.m2 * g.inv_m;
-                            const float rs = rsqrtf(var + a.eps);
-                            coef[r_mrg & 1] = make_float2(wc * rs, bc - tot.mean * wc * rs);
-                            mbar_arrive(&hs.coef_ready[r_mrg & 1]);
-                            if (s == 0) {
-                                if (a.save_mean) a.save_mean[ch] = tot.mean;
-                                if (a.save_rstd) a.save_rstd[ch] = rs;
-                                if (a.rm) a.rm[ch] = fmaf(a.momentum, tot.mean, (1.f - a.momentum) * a.rm[ch]);
-                                if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * a.rv[ch]);
-                            }
-                        }
-                    } else {
-                        if (lane == 0) {
-                            const float rs = rsqrtf(a.rv[ch] + a.eps);
-                            const float mu = a.rm[ch];
-                            coef[r_mrg & 1] = make_float2(wc * rs, bc - mu * wc * rs);
-                            mbar_arrive(&hs.coef_ready[r_mrg & 1]);
-                            if (s == 0) {
-                                if (a.save_mean) a.save_mean[ch] = mu;
-                                if (a.save_rstd) a.save_rstd[ch] = rs;
-                            }
-                        }
-                    }
-                    ++r_mrg;
-                    moved = true;
-                }
-            }
-            if (moved) {
-                t_last = global_timer_ns();
-            } else {
-                __nanosleep(32);
-                if (global_timer_ns() - t_last > kBnWaitLimitNs) {
-                    aborted = true;
-                    bad = true;
-                }
-            }
-        }
+        fwd_bookkeeper<TRAIN>(a, g, rd, nr, sh, lane, bad);
     } else {
         // ---------------- consumers ----------------
         const uint64_t pol_stream = l2_evict_first();
@@ -771,9 +798,9 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
             Moments m = acc.moments();
             warp_merge(m);
             if (lane == 0) {
-                if (q >= 2 && !mbar_wait_bounded(&hs.sums_free[q & 1], ((q >> 1) - 1) & 1, kBnWaitLimitNs)) bad = true;
-                warp_m[q & 1][warp] = m;
-                mbar_arrive(&hs.sums_ready[q & 1]);
+                if (q >= 2 && !mbar_wait_bounded(&sh.hs.sums_free[q & 1], ((q >> 1) - 1) & 1, kBnWaitLimitNs)) bad = true;
+                sh.warp_m[q & 1][warp] = m;
+                mbar_arrive(&sh.hs.sums_ready[q & 1]);
             }
         };
 
@@ -784,10 +811,10 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
             uint32_t b0, b1;
             rd.range(r, ch, s, b0, b1);
             if (TRAIN && r + 1 < nr) stats(r + 1);
-            if (!mbar_wait_bounded(&hs.coef_ready[r & 1], (r >> 1) & 1, kBnWaitLimitNs)) bad = true;
-            const float2 sc = coef[r & 1];
+            if (!mbar_wait_bounded(&sh.hs.coef_ready[r & 1], (r >> 1) & 1, kBnWaitLimitNs)) bad = true;
+            const float2 sc = sh.coef[r & 1];
             __syncwarp();
-            if (lane == 0) mbar_arrive(&hs.coef_free[r & 1]);
+            if (lane == 0) mbar_arrive(&sh.hs.coef_free[r & 1]);
             const float scale = sc.x;
             const float shift = sc.y;
 
@@ -1111,10 +1138,10 @@ bn_bwd_kernel(const BnArgs a, const BnGeom g) {
 // Tensors of a pass: dy, x, and the residual when z must be recomputed with
 // it; the ReLU mask words ride along in the slot.  Training: pass 1 of round
 // r+1 (dz, dres, channel sums; dy and x kept in L2) ahead of pass 2 of round
-// r (dx), which the consumers read straight from L2 with vector loads: only
-// HBM-sourced passes use the ring, so it keeps prefetching pass 1 of the next
-// rounds while pass 2 and the channel waits run.  Eval: one pass per round
-// (dx = dz*scale).
+// r (dx).  Pass 1 streams from HBM through one ring, pass 2 re-reads L2
+// through a second ring with its own producer warp, so the HBM ring keeps
+// prefetching the next rounds while pass 2 and the channel waits run.  Eval:
+// one pass per round (dx = dz*scale).
 // The bookkeeper stages each round's channel parameters, publishes the sums,
 // merges a channel's S slices (training: into the dx coefficients; eval: in
 // the last slice to finish, into dw and db) and writes dw, db.
@@ -1181,18 +1208,135 @@ __device__ __forceinline__ double grad_center(const BnArgs& a, int64_t ch, float
     return t2c * double(rs);
 }
 
+// Bookkeeper of a backward kernel (one warp): stages each round's channel
+// parameters, publishes the CTA's pass-1 sums, and (training) turns a
+// complete channel into the dx coefficients; dw, db come from slice 0
+// (training) or from the last slice to publish (eval).  Polls every handoff
+// without blocking; gives up (sets `bad`) after 2 s without progress.
+template <bool TRAIN>
+__device__ void bwd_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& rd, int nr, BnBwdShared& sh,
+                               int lane, bool& bad) {
+    int q_par = 0, q_pub = 0, r_mrg = TRAIN ? 0 : nr;
+    bool aborted = false;
+    uint64_t t_last = global_timer_ns();
+    while (q_par < nr || q_pub < nr || r_mrg < nr) {
+        bool moved = false;
+        // channel parameters of round q_par
+        if (q_par < nr) {
+            const uint32_t u = uint32_t(q_par) >> 2;
+            if (u == 0 || aborted || mbar_test_wait(&sh.hs.par_free[q_par & 3], (u - 1) & 1)) {
+                if (lane == 0) {
+                    int64_t ch;
+                    int s;
+                    uint32_t b0, b1;
+                    rd.range(q_par, ch, s, b0, b1);
+                    const float mu = a.mean_in[ch];
+                    const float rs = a.rstd_in[ch];
+                    const float wc = a.w ? a.w[ch] : 1.f;
+                    const float bc = a.b ? a.b[ch] : 0.f;
+                    const float scale = wc * rs;
+                    sh.par[q_par & 3] = make_float4(mu, rs, scale, bc - mu * scale);
+                    mbar_arrive(&sh.hs.par_ready[q_par & 3]);
+                }
+                ++q_par;
+                moved = true;
+            }
+        }
+        // pass-1 sums of round q_pub
+        if (q_pub < nr && (aborted || mbar_test_wait(&sh.hs.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
+            double2 v = lane < kRingConsumerWarps ? sh.warp_s[q_pub & 1][lane] : make_double2(0.0, 0.0);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.hs.sums_free[q_pub & 1]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+                v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+            }
+            int64_t ch;
+            int s;
+            uint32_t b0, b1;
+            rd.range(q_pub, ch, s, b0, b1);
+            if (g.S == 1) {
+                if (TRAIN) {
+                    if (lane == 0) sh.keep[q_pub & 3] = v;
+                } else if (lane == 0) {
+                    grad_center(a, ch, a.mean_in[ch], a.rstd_in[ch], v.x, v.y, true);
+                }
+            } else {
+                uint32_t last = 0;
+                if (lane == 0) {
+                    double2* part = reinterpret_cast<double2*>(g.partials) + ch * g.S;
+                    part[s] = v;
+                    if (TRAIN) red_release_add_u32(g.counters + ch, 1u);
+                    else last = atom_acq_rel_add_u32(g.counters + ch, 1u) == uint32_t(g.S - 1);
+                }
+                if (!TRAIN && __shfl_sync(0xffffffffu, last, 0)) {
+                    // every other slice has published: merge into dw, db
+                    if (ld_acquire_u32(g.counters + ch) < uint32_t(g.S)) bad = true;
+                    double t1, t2;
+                    merge_grad_partials(g, ch, lane, t1, t2);
+                    if (lane == 0) grad_center(a, ch, a.mean_in[ch], a.rstd_in[ch], t1, t2, true);
+                }
+            }
+            ++q_pub;
+            moved = true;
+        }
+        // training: the dx coefficients of round r_mrg once its channel is complete
+        if (TRAIN && r_mrg < nr && r_mrg < q_pub) {
+            const uint32_t u = uint32_t(r_mrg) >> 1;
+            bool ok = u == 0 || aborted || mbar_test_wait(&sh.hs.coef_free[r_mrg & 1], (u - 1) & 1);
+            int64_t ch;
+            int s;
+            uint32_t b0, b1;
+            rd.range(r_mrg, ch, s, b0, b1);
+            if (ok && g.S > 1 && !aborted) {
+                // every lane acquires: the partials may then be read directly
+                ok = __all_sync(0xffffffffu, ld_acquire_u32(g.counters + ch) >= uint32_t(g.S));
+            }
+            if (ok) {
+                double t1, t2;
+                if (g.S > 1) {
+                    merge_grad_partials(g, ch, lane, t1, t2);
+                } else {
+                    const double2 k = sh.keep[r_mrg & 3];  // used by lane 0 only
+                    t1 = k.x;
+                    t2 = k.y;
+                }
+                if (lane == 0) {
+                    // this round's parameters are still staged: its consumers free them after pass 2
+                    const float4 pr = sh.par[r_mrg & 3];
+                    const double t2r = grad_center(a, ch, pr.x, pr.y, t1, t2, s == 0);
+                    sh.coef[r_mrg & 1] = make_float2(float(t1 * double(g.inv_m)), float(t2r * double(g.inv_m)));
+                    mbar_arrive(&sh.hs.coef_ready[r_mrg & 1]);
+                }
+                ++r_mrg;
+                moved = true;
+            }
+        }
+        if (moved) {
+            t_last = global_timer_ns();
+        } else {
+            __nanosleep(32);
+            if (global_timer_ns() - t_last > kBnWaitLimitNs) {
+                aborted = true;
+                bad = true;
+            }
+        }
+    }
+}
+
 template <typename T, bool TRAIN>
-__global__ void __launch_bounds__(kRingThreads, 1)
+__global__ void __launch_bounds__(TRAIN ? kRingThreadsBwdTrain : kRingThreads, 1)
 bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
     constexpr int VE = kVec<T>;
-    constexpr int SLOTS = kRingSlotsBwd;
+    constexpr int SLOTS = TRAIN ? kRingSlotsBwdHbm : kRingSlotsBwd;
+    constexpr int SLOTS2 = TRAIN ? kRingSlotsBwdL2 : 1;
     extern __shared__ __align__(128) unsigned char ring_data[];
     __shared__ __align__(8) uint64_t full[SLOTS];
     __shared__ __align__(8) uint64_t empty[SLOTS];
-    __shared__ Handoffs hs;
-    __shared__ double2 warp_s[2][kRingConsumerWarps];
-    __shared__ float4 par[4];   // (mean, rstd, scale, shift) by round mod 4
-    __shared__ float2 coef[2];  // dx coefficients (c1, c2) by round parity
+    __shared__ __align__(8) uint64_t full2[SLOTS2];
+    __shared__ __align__(8) uint64_t empty2[SLOTS2];
+    __shared__ BnBwdShared sh;
     __shared__ int s_bad;
 
     const int lane = threadIdx.x & 31;
@@ -1207,12 +1351,17 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
     const int nt = (need_z && res) ? 3 : 2;
     const Rounds rd(g);
     const int nr = rd.count();
+    // [ring: SLOTS data | SLOTS mask words][ring 2 (training): SLOTS2 data | SLOTS2 mask words]
+    constexpr size_t kRingBytes = size_t(SLOTS) * (kSlotBytes + kSlotMaskWords * 4);
     Ring<SLOTS> rg{ring_data, reinterpret_cast<uint32_t*>(ring_data + size_t(SLOTS) * kSlotBytes), full, empty};
+    Ring<SLOTS2> rg2{ring_data + kRingBytes,
+                     reinterpret_cast<uint32_t*>(ring_data + kRingBytes + size_t(SLOTS2) * kSlotBytes), full2, empty2};
     bool bad = false;
 
     if (threadIdx.x == 0) s_bad = 0;
     ring_init(rg, use_mask ? 33u : 1u);
-    handoffs_init(hs);
+    if (TRAIN) ring_init(rg2, use_mask ? 33u : 1u);
+    handoffs_init(sh.hs);
     __syncthreads();
 
     if (warp == kProducerWarp) {
@@ -1220,120 +1369,16 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
         const uint64_t pol_keep = TRAIN ? l2_evict_last() : l2_evict_first();
         const uint32_t* mk = use_mask ? a.mask_in : nullptr;
         const RingPass<T> first{{dy, x, res}, {pol_keep, pol_keep, pol_keep}, nt, mk};
-        // only pass 1 streams through the ring: pass 2 reads L2 directly,
-        // so the ring keeps fetching the next rounds from HBM meanwhile
         for (int q = 0; q < nr; ++q) ring_produce<T, VE>(rg, rd, q, first, lane, bad);
+    } else if (warp == kProducer2Warp) {
+        // ---------------- producer of pass 2 (training): L2 re-reads ----------------
+        const uint64_t pol_stream = l2_evict_first();
+        const RingPass<T> second{{dy, x, res}, {pol_stream, pol_stream, pol_stream}, nt,
+                                 use_mask ? a.mask_in : nullptr};
+        for (int r = 0; r < nr; ++r) ring_produce<T, VE>(rg2, rd, r, second, lane, bad);
     } else if (warp == kBookkeeperWarp) {
         // ---------------- bookkeeper ----------------
-        double2 keep0 = make_double2(0.0, 0.0), keep1 = make_double2(0.0, 0.0);  // S == 1 (training)
-        int q_par = 0, q_pub = 0, r_mrg = TRAIN ? 0 : nr;
-        bool aborted = false;
-        uint64_t t_last = global_timer_ns();
-        while (q_par < nr || q_pub < nr || r_mrg < nr) {
-            bool moved = false;
-            // channel parameters of round q_par
-            if (q_par < nr) {
-                const uint32_t u = uint32_t(q_par) >> 2;
-                if (u == 0 || aborted || mbar_test_wait(&hs.par_free[q_par & 3], (u - 1) & 1)) {
-                    if (lane == 0) {
-                        int64_t ch;
-                        int s;
-                        uint32_t b0, b1;
-                        rd.range(q_par, ch, s, b0, b1);
-                        const float mu = a.mean_in[ch];
-                        const float rs = a.rstd_in[ch];
-                        const float wc = a.w ? a.w[ch] : 1.f;
-                        const float bc = a.b ? a.b[ch] : 0.f;
-                        const float scale = wc * rs;
-                        par[q_par & 3] = make_float4(mu, rs, scale, bc - mu * scale);
-                        mbar_arrive(&hs.par_ready[q_par & 3]);
-                    }
-                    ++q_par;
-                    moved = true;
-                }
-            }
-            // pass-1 sums of round q_pub
-            if (q_pub < nr && (aborted || mbar_test_wait(&hs.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
-                double2 v = lane < kRingConsumerWarps ? warp_s[q_pub & 1][lane] : make_double2(0.0, 0.0);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&hs.sums_free[q_pub & 1]);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-                    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-                }
-                int64_t ch;
-                int s;
-                uint32_t b0, b1;
-                rd.range(q_pub, ch, s, b0, b1);
-                if (g.S == 1) {
-                    if (TRAIN) {
-                        if (q_pub & 1) keep1 = v;
-                        else keep0 = v;
-                    } else if (lane == 0) {
-                        grad_center(a, ch, a.mean_in[ch], a.rstd_in[ch], v.x, v.y, true);
-                    }
-                } else {
-                    uint32_t last = 0;
-                    if (lane == 0) {
-                        double2* part = reinterpret_cast<double2*>(g.partials) + ch * g.S;
-                        part[s] = v;
-                        if (TRAIN) red_release_add_u32(g.counters + ch, 1u);
-                        else last = atom_acq_rel_add_u32(g.counters + ch, 1u) == uint32_t(g.S - 1);
-                    }
-                    if (!TRAIN && __shfl_sync(0xffffffffu, last, 0)) {
-                        // every other slice has published: merge into dw, db
-                        if (ld_acquire_u32(g.counters + ch) < uint32_t(g.S)) bad = true;
-                        double t1, t2;
-                        merge_grad_partials(g, ch, lane, t1, t2);
-                        if (lane == 0) grad_center(a, ch, a.mean_in[ch], a.rstd_in[ch], t1, t2, true);
-                    }
-                }
-                ++q_pub;
-                moved = true;
-            }
-            // training: the dx coefficients of round r_mrg once its channel is complete
-            if (TRAIN && r_mrg < nr && r_mrg < q_pub) {
-                const uint32_t u = uint32_t(r_mrg) >> 1;
-                bool ok = u == 0 || aborted || mbar_test_wait(&hs.coef_free[r_mrg & 1], (u - 1) & 1);
-                int64_t ch;
-                int s;
-                uint32_t b0, b1;
-                rd.range(r_mrg, ch, s, b0, b1);
-                if (ok && g.S > 1 && !aborted) {
-                    // every lane acquires: the partials may then be read directly
-                    ok = __all_sync(0xffffffffu, ld_acquire_u32(g.counters + ch) >= uint32_t(g.S));
-                }
-                if (ok) {
-                    double t1, t2;
-                    if (g.S > 1) {
-                        merge_grad_partials(g, ch, lane, t1, t2);
-                    } else {
-                        const double2 k = (r_mrg & 1) ? keep1 : keep0;
-                        t1 = k.x;
-                        t2 = k.y;
-                    }
-                    if (lane == 0) {
-                        // this round's parameters are still staged: its consumers free them after pass 2
-                        const float4 pr = par[r_mrg & 3];
-                        const double t2r = grad_center(a, ch, pr.x, pr.y, t1, t2, s == 0);
-                        coef[r_mrg & 1] = make_float2(float(t1 * double(g.inv_m)), float(t2r * double(g.inv_m)));
-                        mbar_arrive(&hs.coef_ready[r_mrg & 1]);
-                    }
-                    ++r_mrg;
-                    moved = true;
-                }
-            }
-            if (moved) {
-                t_last = global_timer_ns();
-            } else {
-                __nanosleep(32);
-                if (global_timer_ns() - t_last > kBnWaitLimitNs) {
-                    aborted = true;
-                    bad = true;
-                }
-            }
-        }
+        bwd_bookkeeper<TRAIN>(a, g, rd, nr, sh, lane, bad);
     } else {
         // ---------------- consumers ----------------
         const uint64_t pol_stream = l2_evict_first();
@@ -1377,16 +1422,16 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
                 d2 += __shfl_xor_sync(0xffffffffu, d2, o);
             }
             if (lane == 0) {
-                if (q >= 2 && !mbar_wait_bounded(&hs.sums_free[q & 1], ((q >> 1) - 1) & 1, kBnWaitLimitNs)) bad = true;
-                warp_s[q & 1][warp] = make_double2(d1, d2);
-                mbar_arrive(&hs.sums_ready[q & 1]);
-                if (!TRAIN) mbar_arrive(&hs.par_free[q & 3]);
+                if (q >= 2 && !mbar_wait_bounded(&sh.hs.sums_free[q & 1], ((q >> 1) - 1) & 1, kBnWaitLimitNs)) bad = true;
+                sh.warp_s[q & 1][warp] = make_double2(d1, d2);
+                mbar_arrive(&sh.hs.sums_ready[q & 1]);
+                if (!TRAIN) mbar_arrive(&sh.hs.par_free[q & 3]);
             }
         };
         // channel parameters (mean, rstd, scale, shift) of round q
         auto params = [&](int q) {
-            if (!mbar_wait_bounded(&hs.par_ready[q & 3], (q >> 2) & 1, kBnWaitLimitNs)) bad = true;
-            return par[q & 3];
+            if (!mbar_wait_bounded(&sh.hs.par_ready[q & 3], (q >> 2) & 1, kBnWaitLimitNs)) bad = true;
+            return sh.par[q & 3];
         };
         auto pass1 = [&](int q) {
             int64_t ch;
@@ -1409,44 +1454,31 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
                 uint32_t b0, b1;
                 rd.range(r, ch, s, b0, b1);
                 if (r + 1 < nr) pass1(r + 1);
-                const float4 pr = par[r & 3];  // waited for in pass 1 of round r; freed below
+                const float4 pr = sh.par[r & 3];  // waited for in pass 1 of round r; freed below
                 const float mu = pr.x, rs = pr.y, scale = pr.z, shift = pr.w;
-                if (!mbar_wait_bounded(&hs.coef_ready[r & 1], (r >> 1) & 1, kBnWaitLimitNs)) bad = true;
-                const float2 cc = coef[r & 1];
+                if (!mbar_wait_bounded(&sh.hs.coef_ready[r & 1], (r >> 1) & 1, kBnWaitLimitNs)) bad = true;
+                const float2 cc = sh.coef[r & 1];
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&hs.coef_free[r & 1]);
+                if (lane == 0) mbar_arrive(&sh.hs.coef_free[r & 1]);
                 const float c1 = cc.x, c2 = cc.y;
-                // ---- pass 2: dx = w*rstd*(dz - sum(dz)/M - xhat*sum(dz*xhat)/M), from L2 ----
-                for (uint32_t base = b0 + warp; base < b1; base += kRingConsumerWarps * kRingUnrollL2) {
-                    Pack<T, VE> pdy[kRingUnrollL2], px[kRingUnrollL2];
-                    uint32_t mbits[kRingUnrollL2];
-#pragma unroll
-                    for (int u = 0; u < kRingUnrollL2; ++u) {
-                        const uint32_t bi = base + u * kRingConsumerWarps;
-                        if (bi < b1) {
-                            const BlockPos p = block_pos(g, bi, lane, ch);
-                            if (p.v < g.lv) {
-                                raw_load_pol<T, VE>(dy, p.seg * g.lv + p.v, pdy[u], pol_stream);
-                                raw_load_pol<T, VE>(x, p.seg * g.lv + p.v, px[u], pol_stream);
-                                if (use_mask) mbits[u] = load_mask_bits<VE>(a.mask_in, g, p, lane, pol_stream);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < kRingUnrollL2; ++u) {
-                        const uint32_t bi = base + u * kRingConsumerWarps;
-                        if (bi >= b1) break;
-                        const BlockPos p = block_pos(g, bi, lane, ch);
+                // ---- pass 2: dx = w*rstd*(dz - sum(dz)/M - xhat*sum(dz*xhat)/M), from ring 2 ----
+                for (uint32_t cb = b0; cb < b1; cb += span) {
+                    const uint32_t n = min(span, b1 - cb);
+                    const int slot = ring_take(rg2, bad);
+                    const uint4* sd = reinterpret_cast<const uint4*>(rg2.data + size_t(slot) * kSlotBytes);
+                    const uint4* sx = sd + span * 32;
+                    const uint4* sr = sx + span * 32;
+                    const uint32_t* mw = rg2.mask + size_t(slot) * kSlotMaskWords;
+                    for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
+                        const BlockPos p = block_pos(g, cb + i, lane, ch);
                         if (p.v >= g.lv) continue;
+                        Pack<T, VE> pdy, px;
+                        pdy.u = sd[i * 32 + lane];
+                        px.u = sx[i * 32 + lane];
                         float dyv[VE], xv[VE], dz[VE], o[VE];
-                        unpack<T, VE>(pdy[u], dyv);
-                        unpack<T, VE>(px[u], xv);
-                        if (use_mask) {
-#pragma unroll
-                            for (int k = 0; k < VE; ++k) dz[k] = ((mbits[u] >> k) & 1u) ? dyv[k] : 0.f;
-                        } else {
-                            form_dz<T, VE>(a, g, p, lane, need_z, scale, shift, dyv, xv, dz, pol_stream);
-                        }
+                        unpack<T, VE>(pdy, dyv);
+                        unpack<T, VE>(px, xv);
+                        ring_dz<T, VE>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
 #pragma unroll
                         for (int k = 0; k < VE; ++k) {
                             const float xh = (xv[k] - mu) * rs;
@@ -1454,9 +1486,10 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
                         }
                         store_vec_pol<T, VE>(dx + (p.seg * g.lv + p.v) * VE, o, pol_stream);
                     }
+                    ring_give(rg2, slot, lane);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&hs.par_free[r & 3]);
+                if (lane == 0) mbar_arrive(&sh.hs.par_free[r & 3]);
             }
         }
     }
@@ -1567,14 +1600,15 @@ inline nrm_status bn_plan(BnPlan& pl, const BnArgs& a, int ve, size_t stage_byte
 // Plan of a ring kernel: `smem` bytes of slots, `kept` tensors per element
 // held in L2 between the two passes of a round (0 in eval) for `held` rounds
 // at a time.  S and k trade rounds (each with a fixed cost) against L2.
-inline nrm_status bn_plan_ring(BnPlan& pl, const BnArgs& a, const void* fn, size_t smem, int kept, int held) {
+inline nrm_status bn_plan_ring(BnPlan& pl, const BnArgs& a, const void* fn, size_t smem, int kept, int held,
+                               int threads = kRingThreads) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     BnGeom& g = pl.g;
     pl.smem = smem;
     nrm_status st = prepare_kernel(fn, pl.smem, false);
     if (st != NRM_OK) return st;
-    const int occ = cached_occupancy(fn, kRingThreads, pl.smem);
+    const int occ = cached_occupancy(fn, threads, pl.smem);
     if (occ < 1) return fail(NRM_ERR_CUDA, "batchnorm kernel cannot be resident");
     const int64_t G = int64_t(occ) * d->sms;
     const uint64_t nb = g.nb_chan;
@@ -1676,10 +1710,12 @@ nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
         bn_geometry(pl.g, a, kVec<T>);
         const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
         const int nt = (need_z && a.res) ? 3 : 2;
-        const size_t smem = size_t(kRingSlotsBwd) * (kSlotBytes + kSlotMaskWords * sizeof(uint32_t));
-        nrm_status st = bn_plan_ring(pl, a, fn, smem, training ? nt : 0, 2);
+        const int slots = training ? kRingSlotsBwdHbm + kRingSlotsBwdL2 : kRingSlotsBwd;
+        const int threads = training ? kRingThreadsBwdTrain : kRingThreads;
+        const size_t smem = size_t(slots) * (kSlotBytes + kSlotMaskWords * sizeof(uint32_t));
+        nrm_status st = bn_plan_ring(pl, a, fn, smem, training ? nt : 0, 2, threads);
         if (st != NRM_OK) return st;
-        return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads);
+        return launch_bn(fn, a, pl, ws, ws_bytes, s, threads);
     }
     const int ve = vec ? kVec<T> : 1;
     const void* fn;
