@@ -1499,6 +1499,12 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
     if (threadIdx.x == 0 && s_bad) atomicOr(a.err, kErrTimeoutStage | kErrTimeoutPeers);
 }
 
+}  // namespace nrm
+
+#include "batchnorm_group.cuh"
+
+namespace nrm {
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1680,6 +1686,11 @@ inline nrm_status launch_bn(const void* fn, const BnArgs& a, BnPlan& pl, void* w
 
 template <typename T>
 nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_bytes, cudaStream_t s) {
+    if (!vec) {
+        // short segments: channel groups staged whole in shared memory
+        nrm_status st = NRM_OK;
+        if (bn_fwd_group<T>(a, training, s, st)) return st;
+    }
     if (vec && a.c > 0 && a.n * a.l > 0) {
         const void* fn = training ? (const void*)&bn_fwd_ring_kernel<T, true>
                                   : (const void*)&bn_fwd_ring_kernel<T, false>;
@@ -1703,6 +1714,10 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
 
 template <typename T>
 nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_bytes, cudaStream_t s) {
+    if (!vec) {
+        nrm_status st = NRM_OK;
+        if (bn_bwd_group<T>(a, training, s, st)) return st;
+    }
     if (vec && a.c > 0 && a.n * a.l > 0) {
         const void* fn = training ? (const void*)&bn_bwd_ring_kernel<T, true>
                                   : (const void*)&bn_bwd_ring_kernel<T, false>;

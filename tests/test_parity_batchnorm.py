@@ -117,3 +117,34 @@ def test_bn_running_stats_closed_form():
     xc = inp["x"].f64().transpose(1, 0, 2).reshape(c, -1)
     np.testing.assert_allclose(rm.double().cpu().numpy(), 0.1 * xc.mean(1), rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(rv.double().cpu().numpy(), 0.9 + 0.1 * xc.var(1, ddof=1), rtol=1e-5)
+
+
+GROUPS = [
+    # (dtype, n, c, l): segments too short for 16-byte access; G channels of a
+    # sample form an aligned span (G = 16 / gcd(l*size, 16))
+    ("f16", 16, 16, 49),     # G = 8, two groups
+    ("bf16", 9, 8, 7),       # a 16-byte vector spans up to three channels
+    ("f32", 33, 12, 9),      # G = 4; a cluster of 8 where the last CTA has no samples
+    ("f32", 4, 2, 70),       # G = 2
+    ("f16", 300, 8, 25),     # one group, many samples per CTA
+    ("bf16", 2048, 8, 49),   # forward fits the group path, backward falls back
+]
+
+
+@pytest.mark.parametrize("case", GROUPS, ids=[f"{d}-{n}x{c}x{l}" for d, n, c, l in GROUPS])
+def test_bn_channel_groups(orc, case):
+    dtype, n, c, l = case
+    idx = GROUPS.index(case)
+    for training in (True, False):
+        for act, with_res, use_mask in (("relu", True, True), ("gelu", False, False), ("none", True, False),
+                                        ("relu", False, False)):
+            cfg = synth.BnConfig("grp", n, c, l, dtype, 1e-5, 0.1, seed=500 + idx, act=act,
+                                 residual=with_res, x_kind="offset_scale", w_std=0.2, b_std=0.2)
+            inp = synth.bn_inputs(cfg)
+            if not training:
+                inp["running_mean"] = synth.store(0.2 * synth.normal(cfg.seed, 20, c), "f32", (c,))
+                inp["running_var"] = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,))
+            got = run_bn(inp, dtype, cfg.eps, cfg.momentum, training, act, with_res, use_mask)
+            want = oracle_bn(orc, inp, cfg.eps, cfg.momentum, training, act, with_res)
+            compare_bn(got, want, dtype, training, act,
+                       f"bn {dtype} {case} training={training} act={act} res={with_res} mask={use_mask}")

@@ -128,6 +128,8 @@ def _bn_run(dtype, n, c, l, act, res, training, mask, offset):
     ("bf16", 2, 3, 70, "relu", False, False, True, 2),
     ("f32", 128, 2, 12544, "none", True, True, False, 0),
     ("f16", 7, 3, 33, "relu", True, False, False, 0),
+    ("bf16", 9, 8, 7, "relu", True, True, True, 0),     # channel groups, cluster of 8
+    ("f32", 33, 12, 9, "gelu", True, False, False, 0),  # channel groups, an empty CTA
 ])
 def test_bn_guards_and_determinism(dtype, n, c, l, act, res, training, mask, offset):
     a = _bn_run(dtype, n, c, l, act, res, training, mask, offset)
