@@ -13,35 +13,30 @@
 // of the math-helper article ("如何用attorch.math快速开发自定义GPU算子：面向进阶
 // 开发者的算子融合实战指南", section "实战二 Welford EMA 组合手写 BatchNorm 融合统计").
 //
-// GB300 design:
-//   * A persistent, cooperative grid (every CTA resident at once).  A channel
-//     is cut into S contiguous slices, one per CTA; the grid holds a whole
-//     number k of channels (gridDim = k*S), so CTA i handles item i + r*gridDim
-//     in round r and the S slices of a channel always run in the same round on
-//     different CTAs.  A 3.2 MB fp32 channel uses S = 38 on 152 SMs (thread-
-//     block clusters, capped at 16 CTAs of one GPC, would leave a quarter of
-//     the SMs idle on this part).
-//   * L2 is the staging buffer: the statistics pass streams the slice from HBM
-//     with an L2 evict-last policy and the apply pass re-reads it from L2 with
-//     evict-first, so x crosses HBM once.  k is sized so that two rounds of
-//     slices stay well inside L2.
+// GB300 design (three kernel families, chosen per call):
+//   * Ring kernels (16-byte vectors): a persistent cooperative grid, one CTA
+//     per SM.  A channel is cut into S slices, one per CTA; the grid holds a
+//     whole number k of channels, so the S slices of a channel run in the same
+//     round on different CTAs.  Inside a CTA, warps specialise: a producer
+//     warp streams the passes through a ring of shared-memory slots with bulk
+//     copies, 16 consumer warps compute, and a bookkeeper warp publishes the
+//     CTA's partial sums to the caller's workspace (release counter per
+//     channel), merges the channel's S partials in one fixed order once they
+//     have all arrived (acquire, bounded by 2 s) and hands the consumers the
+//     channel's coefficients.  The statistics pass of round r+1 runs ahead of
+//     the apply pass of round r; every CTA publishes round r+1 before it needs
+//     round r, so the waits cannot form a cycle.  L2 holds x (dy and x in the
+//     backward) between the two passes of a round: loads carry evict-last on
+//     the first pass and evict-first on the second.
+//   * Channel-group kernels (batchnorm_group.cuh): short segments, staged
+//     whole in shared memory by a thread-block cluster per channel group.
+//   * Scalar kernels (bn_fwd_kernel / bn_bwd_kernel with VE = 1): tensors not
+//     aligned to 16 bytes, with the same cooperative schedule and L2 staging.
 //   * Statistics: per-thread sums of (x - K) and (x - K)^2 about the thread's
-//     first value K, turned into (n, mean, M2) and merged with Chan's formula
-//     across warps and the CTA.  The S slices of a channel meet through the
-//     caller's workspace: each CTA publishes its partial and signals a
-//     per-channel counter (release); readers wait (acquire, bounded by a 2 s
-//     timer) for all S, then merge the S partials in one fixed order, so every
-//     CTA gets bit-identical statistics.
-//   * Latency hiding: a CTA streams and publishes round r+1's statistics
-//     before it waits for round r's channel, so the other slices' arrival is
-//     overlapped with HBM traffic.  Every CTA publishes round r+1 before it
-//     waits on round r, so the waits cannot form a cycle.
-//   * Backward: dz = dy * act'(z) (ReLU from the mask bits, GELU by recomputing
-//     z), dres, and the channel sums sum(dz) and sum(dz*x) accumulated without
-//     rounding loss (error-free products and Kahan sums in fp32, combined in
-//     double); sum(dz*(x - mean)) = sum(dz*x) - mean*sum(dz) in double.  The dx
-//     pass re-reads dy and x from L2.
-//   * Streams read once carry an L2 evict-first policy.
+//     first value K, turned into (n, mean, M2) and merged with Chan's formula.
+//     Backward sums: sum(dz) and sum(dz*x) accumulated without rounding loss
+//     (error-free products and Kahan sums in fp32, combined in double);
+//     sum(dz*(x - mean)) = sum(dz*x) - mean*sum(dz) in double.
 #pragma once
 
 #include "common.cuh"
@@ -1700,14 +1695,10 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
         if (st != NRM_OK) return st;
         return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads);
     }
-    const int ve = vec ? kVec<T> : 1;
-    const void* fn;
-    if (training)
-        fn = vec ? (const void*)&bn_fwd_kernel<T, kVec<T>, true> : (const void*)&bn_fwd_kernel<T, 1, true>;
-    else
-        fn = vec ? (const void*)&bn_fwd_kernel<T, kVec<T>, false> : (const void*)&bn_fwd_kernel<T, 1, false>;
+    // unaligned tensors, channel counts the group path cannot tile, empty channels
+    const void* fn = training ? (const void*)&bn_fwd_kernel<T, 1, true> : (const void*)&bn_fwd_kernel<T, 1, false>;
     BnPlan pl;
-    nrm_status st = bn_plan(pl, a, ve, sizeof(T), fn);
+    nrm_status st = bn_plan(pl, a, 1, sizeof(T), fn);
     if (st != NRM_OK) return st;
     return launch_bn(fn, a, pl, ws, ws_bytes, s);
 }
@@ -1732,14 +1723,9 @@ nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
         if (st != NRM_OK) return st;
         return launch_bn(fn, a, pl, ws, ws_bytes, s, threads);
     }
-    const int ve = vec ? kVec<T> : 1;
-    const void* fn;
-    if (training)
-        fn = vec ? (const void*)&bn_bwd_kernel<T, kVec<T>, true> : (const void*)&bn_bwd_kernel<T, 1, true>;
-    else
-        fn = vec ? (const void*)&bn_bwd_kernel<T, kVec<T>, false> : (const void*)&bn_bwd_kernel<T, 1, false>;
+    const void* fn = training ? (const void*)&bn_bwd_kernel<T, 1, true> : (const void*)&bn_bwd_kernel<T, 1, false>;
     BnPlan pl;
-    nrm_status st = bn_plan(pl, a, ve, 2 * sizeof(T), fn);
+    nrm_status st = bn_plan(pl, a, 1, 2 * sizeof(T), fn);
     if (st != NRM_OK) return st;
     return launch_bn(fn, a, pl, ws, ws_bytes, s);
 }

@@ -71,6 +71,7 @@ struct RowArgs {
     int cols;
     float eps;
     int max_partials;     // backward: cap on the partial rows P (0 = no cap)
+    unsigned int* err;    // device error word (set by the launcher; bounded waits that gave up)
 };
 
 // Upper bound of per-CTA partial rows of the row-norm backward (P).

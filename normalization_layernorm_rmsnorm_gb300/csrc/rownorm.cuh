@@ -29,8 +29,11 @@
 //     partial row to the workspace; a second kernel (launched with programmatic
 //     dependent launch) sums the partial rows column-wise in a fixed order.  No
 //     atomics, so the result is bitwise reproducible.
-//   * The backward prefetches the next row of its group into registers while
-//     the current row is being reduced, so two rows per group are in flight.
+//   * The backward of 16-byte-aligned rows up to 2048 vectors streams rows
+//     through shared memory with bulk copies (rowring.cuh).  The register
+//     backward (other rows) prefetches the next row of its group into
+//     registers while the current row is being reduced, so two rows per group
+//     are in flight.
 //   * Rows too wide for registers (more than 4096 vectors forward or 1024
 //     backward; elements on the unaligned path) take a two-pass "wide" kernel: Welford/Chan
 //     statistics in one pass over global memory, then a normalising pass.
@@ -366,7 +369,21 @@ row_bwd_kernel(const RowArgs a) {
     }
 }
 
-// dw/db[col] = sum over the P partial rows, in row order, rounded to T.
+// Compensated fp32 sum (Neumaier's variant of Kahan's): exact to about two
+// ulps of the result even when the terms are much larger than their sum.
+struct NeumaierSum {
+    float s = 0.f, c = 0.f;
+    __device__ __forceinline__ void add(float v) {
+        const float t = s + v;
+        c += fabsf(s) >= fabsf(v) ? (s - t) + v : (v - t) + s;
+        s = t;
+    }
+    __device__ __forceinline__ float value() const { return s + c; }
+};
+
+// dw/db[col] = sum over the P partial rows, in a fixed order, rounded to T.
+// The partial rows can be much larger than their sum (dw of a column whose
+// per-row terms cancel), so the sum is compensated.
 template <typename T>
 __global__ void __launch_bounds__(256)
 row_colsum_kernel(const float* __restrict__ ws_dw, const float* __restrict__ ws_db, int P,
@@ -375,22 +392,26 @@ row_colsum_kernel(const float* __restrict__ ws_dw, const float* __restrict__ ws_
     const float* ws = blockIdx.y == 0 ? ws_dw : ws_db;
     T* out = blockIdx.y == 0 ? dw : db;
     if (out == nullptr) return;
-    __shared__ float part[8][33];
+    __shared__ float part[8][2][33];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
-    float s = 0.f;
+    NeumaierSum s;
     if (col < cols) {
 #pragma unroll 8
-        for (int p = warp; p < P; p += 8) s += ws[int64_t(p) * cols + col];
+        for (int p = warp; p < P; p += 8) s.add(ws[int64_t(p) * cols + col]);
     }
-    part[warp][lane] = s;
+    part[warp][0][lane] = s.s;
+    part[warp][1][lane] = s.c;
     __syncthreads();
     if (warp == 0 && col < cols) {
-        float tot = 0.f;
+        NeumaierSum tot;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) tot += part[w][lane];
-        reinterpret_cast<typename Io<T>::bits_t*>(out)[col] = Io<T>::store(tot);
+        for (int w = 0; w < 8; ++w) {
+            tot.add(part[w][0][lane]);
+            tot.add(part[w][1][lane]);
+        }
+        reinterpret_cast<typename Io<T>::bits_t*>(out)[col] = Io<T>::store(tot.value());
     }
 }
 
@@ -567,9 +588,78 @@ row_bwd_wide_kernel(const RowArgs a) {
     pdl_trigger();
 }
 
+constexpr uint64_t kRowWaitLimitNs = 2000000000ull;  // 2 s
+
+}  // namespace nrm
+
+#include "rowring.cuh"
+
+namespace nrm {
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+
+// Plan of a backward ring kernel: TPR (rows of at most kRrVpt*512 vectors), R rows per
+// chunk (a multiple of the row groups per CTA, about 48 KB per slot) and at
+// least three slots where they fit.  False when the row does not suit.
+inline bool rr_plan(RrGeom& g, int& tpr, size_t& smem, const RowArgs& a, size_t es, bool ln) {
+    const DevInfo* d = dev_info();
+    if (!d || a.rows <= 0) return false;
+    const int nvec = int(size_t(a.cols) * es / 16);
+    tpr = 32;
+    while (tpr * kRrVpt < nvec && tpr < kRrConsumers) tpr *= 2;
+    if (tpr * kRrVpt < nvec) return false;
+    const int rpc = kRrConsumers / tpr;
+    const size_t row_bytes = size_t(a.cols) * es;
+    const int nt = 2;  // dy, x
+    const size_t param = (size_t(a.cols) * 4 + 127) / 128 * 128;
+    const size_t cap = size_t(d->max_smem_optin) - 4096;  // room for the static shared memory
+    if (param >= cap) return false;
+    const size_t avail = cap - param;
+    int m = int(49152 / (size_t(nt) * rpc * row_bytes));
+    if (m < 1) m = 1;
+    size_t slot = 0;
+    int slots = 0;
+    for (;; --m) {
+        const size_t R = size_t(m) * rpc;
+        slot = (size_t(nt) * R * row_bytes + R * 4 * (ln ? 2 : 1) + 127) / 128 * 128;
+        slots = int(avail / slot < size_t(kRrMaxSlots) ? avail / slot : size_t(kRrMaxSlots));
+        if (slots >= 3 || m == 1) break;
+    }
+    if (slots < 2) return false;
+    g.R = m * rpc;
+    g.slots = slots;
+    g.slot_bytes = uint32_t(slot);
+    g.param_bytes = uint32_t(param);
+    g.chunks = (a.rows + g.R - 1) / g.R;
+    smem = param + size_t(slots) * slot;
+    return true;
+}
+
+template <typename T, bool LN>
+const void* rr_fn(int tpr) {
+    switch (tpr) {
+    case 32: return (const void*)&row_bwd_ring_kernel<T, LN, 32>;
+    case 64: return (const void*)&row_bwd_ring_kernel<T, LN, 64>;
+    case 128: return (const void*)&row_bwd_ring_kernel<T, LN, 128>;
+    case 256: return (const void*)&row_bwd_ring_kernel<T, LN, 256>;
+    default: return (const void*)&row_bwd_ring_kernel<T, LN, 512>;
+    }
+}
+
+// Launches a ring kernel on `grid` CTAs (one per SM at most).
+inline nrm_status rr_launch(const void* fn, const RowArgs& a, const RrGeom& g, size_t smem, int grid,
+                            cudaStream_t s) {
+    nrm_status st = prepare_kernel(fn, smem, false);
+    if (st != NRM_OK) return st;
+    RowArgs args = a;
+    args.err = dev_info()->err;
+    RrGeom geom = g;
+    void* kargs[] = {&args, &geom};
+    return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(kRrThreads), kargs, smem, s), "row ring launch");
+}
+
 template <typename T, bool LN, int VE>
 const void* row_fwd_fn(int tpr) {
     switch (tpr) {
@@ -627,23 +717,39 @@ template <typename T>
 nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    const bool want = a.dw || (layernorm && a.db);
+    if (!want) a.ws_dw = a.ws_db = nullptr;
     const int ve = vec ? kVec<T> : 1;
-    const int tpr = row_tpr(a.cols / ve, kRowBwdVpt, kRowMaxBwdTpr);
-    const void* fn = layernorm ? (vec ? row_bwd_fn<T, true, kVec<T>>(tpr) : row_bwd_fn<T, true, 1>(tpr))
-                               : (vec ? row_bwd_fn<T, false, kVec<T>>(tpr) : row_bwd_fn<T, false, 1>(tpr));
-    const int block = tpr ? kRowBwdBlock : kRowWideBlock;
-    const int rpc = tpr ? block / tpr : 1;
-    const int occ = cached_occupancy(fn, block, 0);
-    if (occ <= 0) return fail(NRM_ERR_CUDA, "row backward kernel cannot be resident");
-    const int64_t groups = (a.rows + rpc - 1) / rpc;
-    int64_t p = int64_t(occ) * d->sms;
+    RrGeom rg;
+    int rtpr = 0;
+    size_t rsmem = 0;
+    const bool ring = vec && rr_plan(rg, rtpr, rsmem, a, sizeof(T), layernorm);
+    const int tpr = ring ? 0 : row_tpr(a.cols / ve, kRowBwdVpt, kRowMaxBwdTpr);
+    const void* fn;
+    int64_t groups, p;
+    int block = kRrThreads;
+    if (ring) {
+        fn = layernorm ? rr_fn<T, true>(rtpr) : rr_fn<T, false>(rtpr);
+        groups = rg.chunks;
+        p = d->sms;
+    } else {
+        fn = layernorm ? (vec ? row_bwd_fn<T, true, kVec<T>>(tpr) : row_bwd_fn<T, true, 1>(tpr))
+                       : (vec ? row_bwd_fn<T, false, kVec<T>>(tpr) : row_bwd_fn<T, false, 1>(tpr));
+        block = tpr ? kRowBwdBlock : kRowWideBlock;
+        const int rpc = tpr ? block / tpr : 1;
+        const int occ = cached_occupancy(fn, block, 0);
+        if (occ <= 0) return fail(NRM_ERR_CUDA, "row backward kernel cannot be resident");
+        groups = (a.rows + rpc - 1) / rpc;
+        p = int64_t(occ) * d->sms;
+    }
     if (p > row_bwd_max_partials(*d)) p = row_bwd_max_partials(*d);
     if (a.max_partials > 0 && p > a.max_partials) p = a.max_partials;
     if (groups < p) p = groups;
     const int P = int(p);
-    const bool want = a.dw || (layernorm && a.db);
-    if (!want) a.ws_dw = a.ws_db = nullptr;
-    if (P > 0) {
+    if (ring && P > 0) {
+        nrm_status st = rr_launch(fn, a, rg, rsmem, P, s);
+        if (st != NRM_OK) return st;
+    } else if (P > 0) {
         RowArgs args = a;
         void* kargs[] = {&args};
         nrm_status st = cuda_status(cudaLaunchKernel(fn, dim3(P), dim3(block), kargs, 0, s),

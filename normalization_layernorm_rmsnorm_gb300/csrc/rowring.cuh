@@ -1,0 +1,270 @@
+// rowring.cuh -- LayerNorm and RMSNorm backward for rows that are 16-byte
+// aligned and at most 2048 vectors long, with the rows streamed through shared
+// memory (included by rownorm.cuh; computes what that file states).
+//
+// Rows of a [rows, cols] tensor are contiguous, so a chunk of R rows is one
+// bulk copy per tensor.  A producer warp streams the CTA's chunks of dy and x
+// (CTA b takes chunks b, b + grid, ...) through a ring of shared-memory slots;
+// the rows' rstd and mean ride along as 4-byte async copies.  16 consumer
+// warps process the rows in groups of TPR threads (vector j*TPR + t of a row
+// belongs to thread t of its group): the row sums from the slot, then dx from
+// a second read of the slot, stored with 16-byte stores, and dw/db
+// accumulated per thread in fp32.  The weight is converted to fp32 once per
+// CTA and kept in shared memory.  Memory parallelism comes from the ring
+// (several chunks in flight per SM), not from registers.  (The forward keeps
+// the register kernel: its rows need one read, and many resident CTAs hide
+// its reduction latency better than one ring CTA per SM.)
+#pragma once
+
+namespace nrm {
+
+constexpr int kRrConsumerWarps = 16;
+constexpr int kRrConsumers = kRrConsumerWarps * 32;
+constexpr int kRrThreads = kRrConsumers + 32;  // + the producer warp
+constexpr int kRrVpt = 4;                      // 16-byte vectors per thread and row, at most
+constexpr int kRrMaxSlots = 8;
+constexpr int kRrBarConsumers = 15;            // named barrier over the consumer warps
+
+struct RrGeom {
+    int R;                 // rows per chunk
+    int slots;             // ring slots
+    uint32_t slot_bytes;   // bytes of a slot: nt*R rows (+ R floats of rstd and of mean, backward)
+    uint32_t param_bytes;  // fp32 weight (and bias) at the front of dynamic shared memory
+    int64_t chunks;        // ceil(rows / R)
+};
+
+// Producer (whole warp): the CTA's chunks of dy and x (and the rows' rstd,
+// mean) into the ring, in order.
+template <typename T, bool LN>
+__device__ void rr_produce(const RowArgs& a, const RrGeom& g, unsigned char* ring, uint64_t* full,
+                           uint64_t* empty, int lane, bool& bad) {
+    const size_t row_bytes = size_t(a.cols) * sizeof(T);
+    const uint64_t pol = l2_evict_first();
+    int q = 0;
+    for (int64_t c = blockIdx.x; c < g.chunks; c += gridDim.x, ++q) {
+        const int slot = q % g.slots;
+        const uint32_t use = uint32_t(q / g.slots);
+        if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u, kRowWaitLimitNs)) bad = true;
+        const int64_t r0 = c * g.R;
+        const int ra = int(a.rows - r0 < g.R ? a.rows - r0 : g.R);
+        unsigned char* base = ring + size_t(slot) * g.slot_bytes;
+        const uint32_t bytes = uint32_t(size_t(ra) * row_bytes);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[slot], 2 * bytes);
+            bulk_g2s(base, reinterpret_cast<const T*>(a.dy) + r0 * a.cols, bytes, &full[slot], pol);
+            bulk_g2s(base + size_t(g.R) * row_bytes, reinterpret_cast<const T*>(a.x) + r0 * a.cols, bytes,
+                     &full[slot], pol);
+        }
+        float* st = reinterpret_cast<float*>(base + 2 * size_t(g.R) * row_bytes);
+        for (int i = lane; i < ra; i += 32) {
+            cp_async_4(st + i, a.rstd_in + r0 + i);
+            if (LN) cp_async_4(st + g.R + i, a.mean_in + r0 + i);
+        }
+        cp_async_mbar_arrive_noinc(&full[slot]);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void rr_unpack(const unsigned char* p, float (&v)[kVec<T>]) {
+    Pack<T, kVec<T>> pk;
+    pk.u = *reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int k = 0; k < kVec<T>; ++k) v[k] = Io<T>::load(pk.b[k]);
+}
+
+// VE consecutive fp32 values from shared memory (16-byte aligned), as float4s.
+template <int VE>
+__device__ __forceinline__ void rr_params(const float* p, float (&v)[VE]) {
+#pragma unroll
+    for (int h = 0; h < VE / 4; ++h) {
+        const float4 f = reinterpret_cast<const float4*>(p)[h];
+        v[4 * h] = f.x;
+        v[4 * h + 1] = f.y;
+        v[4 * h + 2] = f.z;
+        v[4 * h + 3] = f.w;
+    }
+}
+
+// The weight of the row as fp32 in shared memory (consumer threads).
+template <typename T>
+__device__ __forceinline__ void rr_stage_weight(const RowArgs& a, float* wsm) {
+    using bits = typename Io<T>::bits_t;
+    for (int i = threadIdx.x; i < a.cols; i += kRrConsumers)
+        wsm[i] = a.w ? Io<T>::load(reinterpret_cast<const bits*>(a.w)[i]) : 1.f;
+}
+
+// The CTA's dw (or db) partial row: each thread's per-column sums, summed over
+// the row groups in group order.  Consumer threads only; `part` is scratch
+// shared memory of RPC*TPR*VE floats (the drained ring).
+template <int TPR, int VPT, int VE, int RPC>
+__device__ __forceinline__ void rr_partial_row(const float (&acc)[VPT][VE], float* ws, float* part, int group,
+                                               int t, int cols) {
+    const int nvec = cols / VE;
+    if constexpr (RPC == 1) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int vi = j * TPR + t;
+            if (vi < nvec) {
+#pragma unroll
+                for (int k = 0; k < VE; ++k) ws[vi * VE + k] = acc[j][k];
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            if (j * TPR * VE >= cols) break;
+#pragma unroll
+            for (int k = 0; k < VE; ++k) part[group * TPR * VE + t * VE + k] = acc[j][k];
+            named_barrier(kRrBarConsumers, kRrConsumers);
+            for (int i = threadIdx.x; i < TPR * VE; i += kRrConsumers) {
+                const int col = j * TPR * VE + i;
+                if (col < cols) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int gg = 0; gg < RPC; ++gg) sum += part[gg * TPR * VE + i];
+                    ws[col] = sum;
+                }
+            }
+            named_barrier(kRrBarConsumers, kRrConsumers);
+        }
+    }
+}
+
+template <typename T, bool LN, int TPR>
+__global__ void __launch_bounds__(kRrThreads, 1)
+row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
+    constexpr int VE = kVec<T>;
+    constexpr int VPT = kRrVpt;
+    constexpr int RPC = kRrConsumers / TPR;
+    constexpr int NW = TPR / 32;
+    constexpr int NV = LN ? 2 : 1;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[kRrMaxSlots];
+    __shared__ __align__(8) uint64_t empty[kRrMaxSlots];
+    __shared__ float red[RPC][2 * NW * NV];
+    __shared__ int s_bad;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    float* wsm = reinterpret_cast<float*>(smem);
+    unsigned char* ring = smem + g.param_bytes;
+    bool bad = false;
+
+    if (threadIdx.x == 0) {
+        s_bad = 0;
+        for (int i = 0; i < g.slots; ++i) {
+            mbar_init(&full[i], 33);  // the bulk copies' arrival + one per producer lane (mean/rstd)
+            mbar_init(&empty[i], kRrConsumerWarps);
+        }
+        mbar_init_fence();
+    }
+    if (warp < kRrConsumerWarps) rr_stage_weight<T>(a, wsm);
+    __syncthreads();
+
+    if (warp == kRrConsumerWarps) {
+        rr_produce<T, LN>(a, g, ring, full, empty, lane, bad);
+    } else {
+        const int group = threadIdx.x / TPR;
+        const int t = threadIdx.x % TPR;
+        const int cols = a.cols;
+        const int nvec = cols / VE;
+        const float fcols = float(cols);
+        const size_t row_bytes = size_t(cols) * sizeof(T);
+        T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
+        int phase = 0;
+        float accw[VPT][VE];
+        float accb[VPT][VE];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+#pragma unroll
+            for (int k = 0; k < VE; ++k) accw[j][k] = accb[j][k] = 0.f;
+
+        int q = 0;
+        for (int64_t c = blockIdx.x; c < g.chunks; c += gridDim.x, ++q) {
+            const int slot = q % g.slots;
+            if (!mbar_wait_bounded(&full[slot], uint32_t(q / g.slots) & 1u, kRowWaitLimitNs)) bad = true;
+            const int64_t r0 = c * g.R;
+            const int ra = int(a.rows - r0 < g.R ? a.rows - r0 : g.R);
+            const unsigned char* base = ring + size_t(slot) * g.slot_bytes;
+            const float* st = reinterpret_cast<const float*>(base + 2 * size_t(g.R) * row_bytes);
+            for (int r = group; r < ra; r += RPC) {
+                const unsigned char* dr = base + size_t(r) * row_bytes;
+                const unsigned char* xr = base + size_t(g.R + r) * row_bytes;
+                const float rs = st[r];
+                const float mu = LN ? st[g.R + r] : 0.f;
+                // the row sums: sum(dy*w) and sum(dy*w*xhat) (LN) / sum(dy*w*x) (RMS)
+                float s[NV];
+#pragma unroll
+                for (int i = 0; i < NV; ++i) s[i] = 0.f;
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    const int vi = j * TPR + t;
+                    if (vi < nvec) {
+                        float dv[VE], xv[VE], wv[VE];
+                        rr_unpack<T>(dr + size_t(vi) * 16, dv);
+                        rr_unpack<T>(xr + size_t(vi) * 16, xv);
+                        rr_params<VE>(wsm + vi * VE, wv);
+#pragma unroll
+                        for (int k = 0; k < VE; ++k) {
+                            const float gw = dv[k] * wv[k];
+                            if constexpr (LN) {
+                                const float xh = (xv[k] - mu) * rs;
+                                s[0] += gw;
+                                s[NV - 1] = fmaf(gw, xh, s[NV - 1]);
+                            } else {
+                                s[0] = fmaf(gw, xv[k], s[0]);
+                            }
+                        }
+                    }
+                }
+                group_sum<TPR, NV>(s, &red[group][0], phase, group);
+                const float c1 = s[0] / fcols;
+                const float c2 = LN ? s[NV - 1] / fcols : c1 * rs * rs;
+                T* dxr = dx + (r0 + r) * cols;
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    const int vi = j * TPR + t;
+                    if (vi < nvec) {
+                        float dv[VE], xv[VE], wv[VE], o[VE];
+                        rr_unpack<T>(dr + size_t(vi) * 16, dv);
+                        rr_unpack<T>(xr + size_t(vi) * 16, xv);
+                        rr_params<VE>(wsm + vi * VE, wv);
+#pragma unroll
+                        for (int k = 0; k < VE; ++k) {
+                            const float gw = dv[k] * wv[k];
+                            if constexpr (LN) {
+                                const float xh = (xv[k] - mu) * rs;
+                                o[k] = rs * (gw - c1 - xh * c2);
+                                accw[j][k] = fmaf(dv[k], xh, accw[j][k]);
+                                accb[j][k] += dv[k];
+                            } else {
+                                o[k] = rs * (gw - xv[k] * c2);
+                                accw[j][k] = fmaf(dv[k], xv[k] * rs, accw[j][k]);
+                            }
+                        }
+                        store_vec<T, VE>(dxr + int64_t(vi) * VE, o);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+
+        // the column-sum kernel may be scheduled now; it waits for this grid
+        pdl_trigger();
+        // every chunk has been consumed (and its copies have landed): the ring is scratch now
+        named_barrier(kRrBarConsumers, kRrConsumers);
+        float* part = reinterpret_cast<float*>(ring);
+        if (a.ws_dw)
+            rr_partial_row<TPR, VPT, VE, RPC>(accw, a.ws_dw + int64_t(blockIdx.x) * cols, part, group, t, cols);
+        if constexpr (LN) {
+            if (a.ws_db)
+                rr_partial_row<TPR, VPT, VE, RPC>(accb, a.ws_db + int64_t(blockIdx.x) * cols, part, group, t, cols);
+        }
+    }
+    if (bad) s_bad = 1;
+    __syncthreads();
+    if (threadIdx.x == 0 && s_bad) atomicOr(a.err, kErrTimeoutStage);
+}
+
+}  // namespace nrm

@@ -131,3 +131,15 @@ def test_constant_rows(orc):
     want_y, want_mean, want_rstd = orc.layernorm_fwd(host(x), host(w), host(b), 1e-4)
     np.testing.assert_allclose(host(y), want_y, atol=1e-5, rtol=1e-5)
     np.testing.assert_allclose(host(rstd), want_rstd, rtol=1e-5)
+
+
+@pytest.mark.parametrize("kind", ["layernorm", "rmsnorm"])
+@pytest.mark.parametrize("dtype,rows,cols", [("f16", 20011, 256), ("f32", 3001, 1024), ("bf16", 613, 8192)])
+def test_row_backward_ring_many_chunks(orc, kind, dtype, rows, cols):
+    # aligned rows the backward streams through shared memory: several chunks
+    # per CTA and a ragged last chunk
+    cfg = synth.RowConfig("ring", kind, rows, cols, dtype, 1e-5, seed=rows + cols, x_mean=-0.3, x_std=1.7)
+    inp = synth.row_inputs(cfg)
+    got = run_row(kind, inp, dtype, cfg.eps)
+    want = oracle_row(orc, kind, inp, cfg.eps)
+    compare_row(got, want, dtype, f"{kind} {dtype} [{rows},{cols}]")
