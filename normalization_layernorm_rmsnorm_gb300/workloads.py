@@ -70,7 +70,7 @@ def _rms(cfg, dev, f32):
     calls.append(Call(cfg.name, "fwd", "row_fwd_kernel<bf16,rms>",
                       lambda x=x, w=w, y=y, r=rstd, e=cfg.eps: nrm.nrm_rmsnorm_fwd(x, w, y, r, e),
                       nbytes(x, y, w, rstd), 1, [x, w], [y, rstd]))
-    calls.append(Call(cfg.name, "bwd", "row_bwd_kernel<bf16,rms>+colsum",
+    calls.append(Call(cfg.name, "bwd", "row_bwd_ring_kernel<bf16,rms>+colsum",
                       lambda: nrm.nrm_rmsnorm_bwd(dy, x, w, rstd, dx, dw, ws),
                       nbytes(dy, x, w, rstd, dx, dw), 2, [dy], [dx, dw]))
 
@@ -91,7 +91,7 @@ def _ln(cfg, dev, f32):
     calls.append(Call(cfg.name, "fwd", "row_fwd_kernel<f16,ln>",
                       lambda e=cfg.eps: nrm.nrm_layernorm_fwd(lx, lw, lb, ly, lmean, lrstd, e),
                       nbytes(lx, lw, lb, ly, lmean, lrstd), 1, [lx, lw, lb], [ly, lmean, lrstd]))
-    calls.append(Call(cfg.name, "bwd", "row_bwd_kernel<f16,ln>+colsum",
+    calls.append(Call(cfg.name, "bwd", "row_bwd_ring_kernel<f16,ln>+colsum",
                       lambda: nrm.nrm_layernorm_bwd(ldy, lx, lw, lmean, lrstd, ldx, ldw, ldb, lws),
                       nbytes(ldy, lx, lw, lmean, lrstd, ldx, ldw, ldb), 2, [ldy], [ldx, ldw, ldb]))
 
@@ -112,12 +112,12 @@ def _bn_res_relu(cfg, dev, f32):
     bsm, bsr, bdw, bdb = f32(c), f32(c), f32(c), f32(c)
     bmask = torch.empty(nrm.nrm_act_mask_words(n, c, l), dtype=torch.int32, device=dev)
     bws = nrm.batchnorm_workspace(bx)
-    calls.append(Call(cfg.name, "fwd", "bn_fwd_kernel<f32,train>",
+    calls.append(Call(cfg.name, "fwd", "bn_fwd_ring_kernel<f32,train>",
                       lambda: nrm.nrm_batchnorm_fwd(bx, bres, bw, bb, by, brm, brv, bsm, bsr, bmask,
                                                     cfg.eps, cfg.momentum, True, "relu", bws),
                       nbytes(bx, bres, by, bmask, bw, bb, bsm, bsr) + 2 * nbytes(brm, brv), 1,
                       [bx, bres, bw, bb, brm, brv], [by, bmask, bsm, bsr, brm, brv]))
-    calls.append(Call(cfg.name, "bwd", "bn_bwd_kernel<f32,train>",
+    calls.append(Call(cfg.name, "bwd", "bn_bwd_ring_kernel<f32,train>",
                       lambda: nrm.nrm_batchnorm_bwd(bdy, bx, bres, bw, bb, bsm, bsr, bmask, bdx, bdres,
                                                     bdw, bdb, True, "relu", bws),
                       nbytes(bdy, bx, bmask, bw, bb, bsm, bsr, bdx, bdres, bdw, bdb), 1,
@@ -126,12 +126,12 @@ def _bn_res_relu(cfg, dev, f32):
     erv = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,)).torch(dev)
     esm, esr = f32(c), f32(c)
     eval_name = cfg.name + "_eval"
-    calls.append(Call(eval_name, "fwd", "bn_fwd_kernel<f32,eval>",
+    calls.append(Call(eval_name, "fwd", "bn_fwd_ring_kernel<f32,eval>",
                       lambda: nrm.nrm_batchnorm_fwd(bx, bres, bw, bb, by, erm, erv, esm, esr, bmask,
                                                     cfg.eps, cfg.momentum, False, "relu", bws),
                       nbytes(bx, bres, by, bmask, bw, bb, erm, erv, esm, esr), 1,
                       [erm, erv], [by, bmask]))
-    calls.append(Call(eval_name, "bwd", "bn_bwd_kernel<f32,eval>",
+    calls.append(Call(eval_name, "bwd", "bn_bwd_ring_kernel<f32,eval>",
                       lambda: nrm.nrm_batchnorm_bwd(bdy, bx, bres, bw, bb, esm, esr, bmask, bdx, bdres,
                                                     bdw, bdb, False, "relu", bws),
                       nbytes(bdy, bx, bmask, bw, bb, esm, esr, bdx, bdres, bdw, bdb), 1,
@@ -153,12 +153,12 @@ def _bn_gelu(cfg, dev, f32):
     gy, gdx = torch.empty_like(gx), torch.empty_like(gx)
     gsm, gsr, gdw, gdb = f32(c), f32(c), f32(c), f32(c)
     gws = nrm.batchnorm_workspace(gx)
-    calls.append(Call(cfg.name, "fwd", "bn_fwd_kernel<f16,train>",
+    calls.append(Call(cfg.name, "fwd", "bn_fwd_group_kernel<f16,train>",
                       lambda: nrm.nrm_batchnorm_fwd(gx, None, gw, gb, gy, grm, grv, gsm, gsr, None,
                                                     cfg.eps, cfg.momentum, True, "gelu", gws),
                       nbytes(gx, gy, gw, gb, gsm, gsr) + 2 * nbytes(grm, grv), 1,
                       [gx, gw, gb, grm, grv], [gy, gsm, gsr, grm, grv]))
-    calls.append(Call(cfg.name, "bwd", "bn_bwd_kernel<f16,train>",
+    calls.append(Call(cfg.name, "bwd", "bn_bwd_group_kernel<f16,train>",
                       lambda: nrm.nrm_batchnorm_bwd(gdy, gx, None, gw, gb, gsm, gsr, None, gdx, None,
                                                     gdw, gdb, True, "gelu", gws),
                       nbytes(gdy, gx, gw, gb, gsm, gsr, gdx, gdw, gdb), 1,
