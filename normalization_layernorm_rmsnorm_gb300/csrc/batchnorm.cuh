@@ -593,7 +593,7 @@ struct BnFwdShared {
 };
 struct BnBwdShared {
     Handoffs hs;
-    double2 warp_s[2][kRingConsumerWarps];  // per-warp (sum dz, sum dz*x) by pass parity
+    float4 warp_s[2][kRingConsumerWarps];   // per-warp (sum dz, sum dz*x) as float-float pairs, by pass parity
     float4 par[4];                          // (mean, rstd, scale, shift) by round mod 4
     float2 coef[2];                         // dx coefficients (c1, c2) by round parity
     double2 keep[4];                        // S == 1: a round's sums by round mod 4
@@ -909,6 +909,9 @@ struct GradSums {
     __device__ __forceinline__ double sum_dzx() const {
         return double(dzx.s) - double(dzx.c) + double(dzx_err);
     }
+    // the same sums as float-float pairs (Kahan's s - c; plus the products' error term)
+    __device__ __forceinline__ FF ff_dz() const { return FF{dz.s, -dz.c}; }
+    __device__ __forceinline__ FF ff_dzx() const { return ff_add(FF{dzx.s, -dzx.c}, FF{dzx_err, 0.f}); }
 };
 
 // First pass of round r: dz from dy and x (both streamed from HBM and kept in
@@ -1239,7 +1242,11 @@ __device__ void bwd_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& r
         }
         // pass-1 sums of round q_pub
         if (q_pub < nr && (aborted || mbar_test_wait(&sh.hs.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
-            double2 v = lane < kRingConsumerWarps ? sh.warp_s[q_pub & 1][lane] : make_double2(0.0, 0.0);
+            double2 v = make_double2(0.0, 0.0);
+            if (lane < kRingConsumerWarps) {
+                const float4 f = sh.warp_s[q_pub & 1][lane];
+                v = make_double2(ff_to_double(FF{f.x, f.y}), ff_to_double(FF{f.z, f.w}));
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.hs.sums_free[q_pub & 1]);
 #pragma unroll
@@ -1410,15 +1417,12 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
         };
         // this warp's pass-1 sums of round q -> bookkeeper
         auto publish = [&](int q, const GradSums& acc) {
-            double d1 = acc.sum_dz(), d2 = acc.sum_dzx();
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                d1 += __shfl_xor_sync(0xffffffffu, d1, o);
-                d2 += __shfl_xor_sync(0xffffffffu, d2, o);
-            }
+            // float-float warp sums: no double-precision arithmetic on the consumers' path
+            const FF d1 = ff_warp_sum(acc.ff_dz());
+            const FF d2 = ff_warp_sum(acc.ff_dzx());
             if (lane == 0) {
                 if (q >= 2 && !mbar_wait_bounded(&sh.hs.sums_free[q & 1], ((q >> 1) - 1) & 1, kBnWaitLimitNs)) bad = true;
-                sh.warp_s[q & 1][warp] = make_double2(d1, d2);
+                sh.warp_s[q & 1][warp] = make_float4(d1.hi, d1.lo, d2.hi, d2.lo);
                 mbar_arrive(&sh.hs.sums_ready[q & 1]);
                 if (!TRAIN) mbar_arrive(&sh.hs.par_free[q & 3]);
             }

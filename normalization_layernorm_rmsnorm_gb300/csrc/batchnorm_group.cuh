@@ -284,13 +284,9 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
                 tz[idx] = dz[0];
                 acc.add(dz, xv);
             }
-        double d1 = acc.sum_dz(), d2 = acc.sum_dzx();
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            d1 += __shfl_xor_sync(0xffffffffu, d1, o);
-            d2 += __shfl_xor_sync(0xffffffffu, d2, o);
-        }
-        if (lane == 0) ws[warp] = make_double2(d1, d2);
+        const FF d1 = ff_warp_sum(acc.ff_dz());
+        const FF d2 = ff_warp_sum(acc.ff_dzx());
+        if (lane == 0) ws[warp] = make_double2(ff_to_double(d1), ff_to_double(d2));
     }
     __syncthreads();
     if (threadIdx.x < g.G) {

@@ -141,6 +141,32 @@ __device__ __forceinline__ void warp_merge(Moments& m) {
     }
 }
 
+// An unevaluated sum hi + lo of two floats (about 48 significant bits), added
+// with Knuth's TwoSum and renormalised: sums that need more than fp32 stay on
+// the fp32 pipe (double-precision throughput on this part is a small fraction
+// of fp32).
+struct FF {
+    float hi, lo;
+};
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    const float s = a.hi + b.hi;
+    const float bb = s - a.hi;
+    const float e = (a.hi - (s - bb)) + (b.hi - bb);
+    const float t = e + (a.lo + b.lo);
+    const float hi = s + t;
+    return FF{hi, t - (hi - s)};
+}
+// Sum over the warp (every lane gets it; the tree is fixed, so it is bitwise reproducible).
+__device__ __forceinline__ FF ff_warp_sum(FF v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const FF w{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+        v = ff_add(v, w);
+    }
+    return v;
+}
+__device__ __forceinline__ double ff_to_double(FF v) { return double(v.hi) + double(v.lo); }
+
 // Compensated (Kahan) float accumulation.
 struct Kahan {
     float s = 0.f;
