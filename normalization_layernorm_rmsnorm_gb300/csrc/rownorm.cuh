@@ -384,30 +384,32 @@ struct NeumaierSum {
 // dw/db[col] = sum over the P partial rows, in a fixed order, rounded to T.
 // The partial rows can be much larger than their sum (dw of a column whose
 // per-row terms cancel), so the sum is compensated.
+constexpr int kColsumWarps = 32;  // partial rows are split over the warps: short dependent chains
+
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kColsumWarps * 32)
 row_colsum_kernel(const float* __restrict__ ws_dw, const float* __restrict__ ws_db, int P,
                   int cols, T* dw, T* db) {
     pdl_wait();
     const float* ws = blockIdx.y == 0 ? ws_dw : ws_db;
     T* out = blockIdx.y == 0 ? dw : db;
     if (out == nullptr) return;
-    __shared__ float part[8][2][33];
+    __shared__ float part[kColsumWarps][2][33];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
     NeumaierSum s;
     if (col < cols) {
-#pragma unroll 8
-        for (int p = warp; p < P; p += 8) s.add(ws[int64_t(p) * cols + col]);
+#pragma unroll 4
+        for (int p = warp; p < P; p += kColsumWarps) s.add(ws[int64_t(p) * cols + col]);
     }
     part[warp][0][lane] = s.s;
     part[warp][1][lane] = s.c;
     __syncthreads();
     if (warp == 0 && col < cols) {
         NeumaierSum tot;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
+#pragma unroll 8
+        for (int w = 0; w < kColsumWarps; ++w) {
             tot.add(part[w][0][lane]);
             tot.add(part[w][1][lane]);
         }
@@ -764,7 +766,7 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     T* dw = reinterpret_cast<T*>(a.dw);
     T* db = layernorm ? reinterpret_cast<T*>(a.db) : nullptr;
     void* cargs[] = {&wsw, &wsb, &P_, &cols, &dw, &db};
-    return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((a.cols + 31) / 32, 2), dim3(256),
+    return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((a.cols + 31) / 32, 2), dim3(kColsumWarps * 32),
                       cargs, s);
 }
 
