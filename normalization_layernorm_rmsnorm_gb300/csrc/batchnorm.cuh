@@ -1539,15 +1539,15 @@ inline void bn_geometry(BnGeom& g, const BnArgs& a, int ve) {
     g.partials = nullptr;
 }
 
-// L2 held by the slices of two rounds in flight (the statistics pass of
-// round r+1 overlaps the apply pass of round r).
-#ifndef NRM_BN_L2_BUDGET_MB
-#define NRM_BN_L2_BUDGET_MB 48
-#endif
+// L2 held by the kept data of the rounds in flight (the first pass of round
+// r+1 overlaps the second pass of round r).  The ring forward keeps one tensor
+// and prefers fewer, longer rounds (measured on the ResNet shape), so it gets
+// a larger share.
+constexpr double kBnL2Budget = 48.0 * 1024 * 1024;
+constexpr double kBnL2BudgetRingFwd = 64.0 * 1024 * 1024;
 #ifndef NRM_BN_ROUND_OVERHEAD
 #define NRM_BN_ROUND_OVERHEAD 32
 #endif
-constexpr double kBnL2Budget = double(NRM_BN_L2_BUDGET_MB) * 1024 * 1024;
 // Fixed cost of a round (channel barrier, reductions), in blocks of work.
 constexpr double kBnRoundOverheadBlocks = double(NRM_BN_ROUND_OVERHEAD);
 
@@ -1606,7 +1606,7 @@ inline nrm_status bn_plan(BnPlan& pl, const BnArgs& a, int ve, size_t stage_byte
 // held in L2 between the two passes of a round (0 in eval) for `held` rounds
 // at a time.  S and k trade rounds (each with a fixed cost) against L2.
 inline nrm_status bn_plan_ring(BnPlan& pl, const BnArgs& a, const void* fn, size_t smem, int kept, int held,
-                               int threads = kRingThreads) {
+                               int threads, double l2_budget) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     BnGeom& g = pl.g;
@@ -1620,7 +1620,7 @@ inline nrm_status bn_plan_ring(BnPlan& pl, const BnArgs& a, const void* fn, size
     int64_t k_max = G;
     if (kept > 0) {
         const double chan_bytes = double(nb) * 512.0 * kept;
-        k_max = int64_t(kBnL2Budget / (double(held) * chan_bytes));
+        k_max = int64_t(l2_budget / (double(held) * chan_bytes));
     }
     if (k_max < 1) k_max = 1;
     if (k_max > G) k_max = G;
@@ -1695,7 +1695,8 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
                                   : (const void*)&bn_fwd_ring_kernel<T, false>;
         BnPlan pl;
         bn_geometry(pl.g, a, kVec<T>);
-        nrm_status st = bn_plan_ring(pl, a, fn, size_t(kRingSlotsFwd) * kSlotBytes, training ? 1 : 0, 2);
+        nrm_status st = bn_plan_ring(pl, a, fn, size_t(kRingSlotsFwd) * kSlotBytes, training ? 1 : 0, 2,
+                                      kRingThreads, kBnL2BudgetRingFwd);
         if (st != NRM_OK) return st;
         return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads);
     }
@@ -1723,7 +1724,7 @@ nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
         const int slots = training ? kRingSlotsBwdHbm + kRingSlotsBwdL2 : kRingSlotsBwd;
         const int threads = training ? kRingThreadsBwdTrain : kRingThreads;
         const size_t smem = size_t(slots) * (kSlotBytes + kSlotMaskWords * sizeof(uint32_t));
-        nrm_status st = bn_plan_ring(pl, a, fn, smem, training ? nt : 0, 2, threads);
+        nrm_status st = bn_plan_ring(pl, a, fn, smem, training ? nt : 0, 2, threads, kBnL2Budget);
         if (st != NRM_OK) return st;
         return launch_bn(fn, a, pl, ws, ws_bytes, s, threads);
     }
