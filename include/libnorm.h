@@ -70,11 +70,20 @@ typedef enum nrm_status {
 
 typedef enum nrm_dtype { NRM_F32 = 0, NRM_F16 = 1, NRM_BF16 = 2 } nrm_dtype;
 
-/* Activation fused after BatchNorm ([NK] BatchNorm section, act_func; [AF]
- * section "五、反向传播融合同样成立" for the derivative taken from the
- * pre-activation input).  ReLU'(0) = 0.  GELU is the exact erf form
- * z * Phi(z). */
-typedef enum nrm_act { NRM_ACT_NONE = 0, NRM_ACT_RELU = 1, NRM_ACT_GELU = 2 } nrm_act;
+/* Activation fused after BatchNorm ([NK] BatchNorm section, act_func, which
+ * lists relu, gelu, silu and mish among the fusable activations; [AF] section
+ * "六、一个内核通吃 21 种激活" for the set and section "五、反向传播融合同样成立"
+ * for the derivative taken from the pre-activation input).  ReLU'(0) = 0.
+ * GELU is the exact erf form z * Phi(z).  SiLU is z * sigmoid(z); Mish is
+ * z * tanh(softplus(z)), softplus(z) = log(1 + e^z) (PyTorch's definitions:
+ * the articles name the activations without formulas). */
+typedef enum nrm_act {
+    NRM_ACT_NONE = 0,
+    NRM_ACT_RELU = 1,
+    NRM_ACT_GELU = 2,
+    NRM_ACT_SILU = 3,
+    NRM_ACT_MISH = 4
+} nrm_act;
 
 /* Operations that need a workspace (for nrm_workspace_bytes). */
 typedef enum nrm_op { NRM_OP_LAYERNORM_BWD = 1, NRM_OP_RMSNORM_BWD = 2 } nrm_op;

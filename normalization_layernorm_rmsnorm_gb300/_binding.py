@@ -17,10 +17,11 @@ LIB_PATH = os.path.join(_PKG, "_build", "libnorm.so")
 
 NRM_OK, NRM_ERR_INVALID_ARG, NRM_ERR_UNSUPPORTED, NRM_ERR_WORKSPACE, NRM_ERR_CUDA, NRM_ERR_TIMEOUT = range(6)
 NRM_F32, NRM_F16, NRM_BF16 = 0, 1, 2
-NRM_ACT_NONE, NRM_ACT_RELU, NRM_ACT_GELU = 0, 1, 2
+NRM_ACT_NONE, NRM_ACT_RELU, NRM_ACT_GELU, NRM_ACT_SILU, NRM_ACT_MISH = 0, 1, 2, 3, 4
 NRM_OP_LAYERNORM_BWD, NRM_OP_RMSNORM_BWD = 1, 2
 
-ACTS = {"none": NRM_ACT_NONE, "relu": NRM_ACT_RELU, "gelu": NRM_ACT_GELU}
+ACTS = {"none": NRM_ACT_NONE, "relu": NRM_ACT_RELU, "gelu": NRM_ACT_GELU, "silu": NRM_ACT_SILU,
+        "mish": NRM_ACT_MISH}
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("nrm_layernorm_fwd", "nrm_layernorm_bwd", "nrm_layernorm_bwd_noalloc",

@@ -296,7 +296,8 @@ nrm_status check_bn_shape(int64_t n, int64_t c, int64_t l, nrm_dtype dt, int tra
     if (!size_ok(n, l) || (n > 0 && l > 0 && n * l >= (int64_t(1) << 31)))
         return fail(NRM_ERR_UNSUPPORTED, "a channel must hold fewer than 2^31 elements");
     if (c * 16 >= (int64_t(1) << 31)) return fail(NRM_ERR_UNSUPPORTED, "c must be < 2^27");
-    if (act != NRM_ACT_NONE && act != NRM_ACT_RELU && act != NRM_ACT_GELU)
+    if (act != NRM_ACT_NONE && act != NRM_ACT_RELU && act != NRM_ACT_GELU && act != NRM_ACT_SILU &&
+        act != NRM_ACT_MISH)
         return fail(NRM_ERR_INVALID_ARG, "unknown activation %d", int(act));
     if (training && c > 0 && n * l < 2)
         return fail(NRM_ERR_INVALID_ARG, "training needs more than one value per channel (n*l >= 2)");

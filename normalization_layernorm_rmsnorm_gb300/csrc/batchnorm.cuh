@@ -67,9 +67,16 @@ struct BnGeom {
     void* partials;        // [c][S]: float4 (n, mean, m2, 0) forward; double2 backward
 };
 
+// softplus(z) = log(1 + e^z), without overflow for large z
+__device__ __forceinline__ float softplus_f(float z) {
+    return z > 0.f ? z + log1pf(expf(-z)) : log1pf(expf(z));
+}
+
 __device__ __forceinline__ float act_forward(int act, float z) {
     if (act == NRM_ACT_RELU) return z > 0.f ? z : 0.f;
     if (act == NRM_ACT_GELU) return 0.5f * z * (1.f + erff(z * 0.70710678118654752f));
+    if (act == NRM_ACT_SILU) return z / (1.f + expf(-z));
+    if (act == NRM_ACT_MISH) return z * tanhf(softplus_f(z));
     return z;
 }
 
@@ -81,7 +88,53 @@ __device__ __forceinline__ float act_derivative(int act, float z) {
         const float pdf = expf(-0.5f * z * z) * 0.39894228040143268f;
         return fmaf(z, pdf, cdf);
     }
+    if (act == NRM_ACT_SILU) {
+        const float sg = 1.f / (1.f + expf(-z));
+        return sg * fmaf(z, 1.f - sg, 1.f);
+    }
+    if (act == NRM_ACT_MISH) {
+        const float t = tanhf(softplus_f(z));
+        const float sg = 1.f / (1.f + expf(-z));
+        return fmaf(z * sg, 1.f - t * t, t);
+    }
     return 1.f;
+}
+
+// Whether the backward recomputes z = x*scale + shift (+ residual) to take the
+// activation's derivative (every activation but none, and ReLU with a mask).
+__host__ __device__ __forceinline__ bool bn_need_z(int act, const void* mask_in) {
+    return act != NRM_ACT_NONE && !(act == NRM_ACT_RELU && mask_in != nullptr);
+}
+
+// The same for an activation fixed at compile time (the ring and group
+// kernels are instantiated per activation, so the hot loops carry one).
+template <int ACT>
+__device__ __forceinline__ float act_forward_c(float z) {
+    if constexpr (ACT == NRM_ACT_RELU) return z > 0.f ? z : 0.f;
+    else if constexpr (ACT == NRM_ACT_NONE) return z;
+    else return act_forward(ACT, z);
+}
+template <int ACT>
+__device__ __forceinline__ float act_derivative_c(float z) {
+    if constexpr (ACT == NRM_ACT_RELU) return z > 0.f ? 1.f : 0.f;
+    else if constexpr (ACT == NRM_ACT_NONE) return 1.f;
+    else return act_derivative(ACT, z);
+}
+
+// Calls f(std::integral_constant-like tag) with the activation as a compile-time value.
+template <int A>
+struct ActTag {
+    static constexpr int value = A;
+};
+template <typename F>
+auto with_act(int act, F&& f) {
+    switch (act) {
+    case NRM_ACT_RELU: return f(ActTag<NRM_ACT_RELU>{});
+    case NRM_ACT_GELU: return f(ActTag<NRM_ACT_GELU>{});
+    case NRM_ACT_SILU: return f(ActTag<NRM_ACT_SILU>{});
+    case NRM_ACT_MISH: return f(ActTag<NRM_ACT_MISH>{});
+    default: return f(ActTag<NRM_ACT_NONE>{});
+    }
 }
 
 // Location of lane `lane` of block `bi` of channel `ch`.
@@ -723,7 +776,7 @@ __device__ void fwd_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& r
 // bookkeeper merges each statistics pass over the 16 consumer warps and
 // publishes it, merges a channel's S slices once they have all arrived, and
 // hands the consumers the channel's scale and shift.
-template <typename T, bool TRAIN>
+template <typename T, bool TRAIN, int ACT>
 __global__ void __launch_bounds__(kRingThreads, 1)
 bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
     constexpr int VE = kVec<T>;
@@ -837,7 +890,7 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
                             float z = fmaf(v[k], scale, shift);
                             if (res) z += rr[k];
                             nib |= uint32_t(z > 0.f) << k;
-                            o[k] = act_forward(a.act, z);
+                            o[k] = act_forward_c<ACT>(z);
                         }
                         store_vec_pol<T, VE>(y + (p.seg * g.lv + p.v) * VE, o, pol_stream);
                     }
@@ -1024,7 +1077,7 @@ bn_bwd_kernel(const BnArgs a, const BnGeom g) {
     // until the dx pass; everything else streams through once
     const uint64_t pol_stream = l2_evict_first();
     const uint64_t pol_keep = TRAIN ? l2_evict_last() : pol_stream;
-    const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
+    const bool need_z = bn_need_z(a.act, a.mask_in);
     const Rounds rd(g);
     bool bad = false;
 
@@ -1146,7 +1199,7 @@ bn_bwd_kernel(const BnArgs a, const BnGeom g) {
 
 // dz of one lane's vector from the slot: dy passed through the activation's
 // derivative at z (mask bits, or z recomputed from x and the residual).
-template <typename T, int VE>
+template <typename T, int VE, int ACT>
 __device__ __forceinline__ void ring_dz(const BnArgs& a, bool use_mask, bool need_z, const uint32_t* mw,
                                         const uint4* sr, uint32_t i, int lane, float scale, float shift,
                                         const float (&dyv)[VE], const float (&xv)[VE], float (&dz)[VE]) {
@@ -1167,7 +1220,7 @@ __device__ __forceinline__ void ring_dz(const BnArgs& a, bool use_mask, bool nee
 #pragma unroll
         for (int k = 0; k < VE; ++k) {
             const float z = fmaf(xv[k], scale, shift) + r[k];
-            dz[k] = dyv[k] * act_derivative(a.act, z);
+            dz[k] = dyv[k] * act_derivative_c<ACT>(z);
         }
     } else {
 #pragma unroll
@@ -1327,7 +1380,7 @@ __device__ void bwd_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& r
     }
 }
 
-template <typename T, bool TRAIN>
+template <typename T, bool TRAIN, int ACT>
 __global__ void __launch_bounds__(TRAIN ? kRingThreadsBwdTrain : kRingThreads, 1)
 bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
     constexpr int VE = kVec<T>;
@@ -1348,8 +1401,8 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
     const T* __restrict__ res = reinterpret_cast<const T*>(a.res);
     T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
     T* __restrict__ dres = reinterpret_cast<T*>(a.dres);
-    const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
-    const bool use_mask = a.act == NRM_ACT_RELU && a.mask_in != nullptr;
+    const bool need_z = bn_need_z(ACT, a.mask_in);
+    const bool use_mask = ACT == NRM_ACT_RELU && a.mask_in != nullptr;
     const int nt = (need_z && res) ? 3 : 2;
     const Rounds rd(g);
     const int nr = rd.count();
@@ -1402,7 +1455,7 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
                 float dyv[VE], xv[VE], dz[VE];
                 unpack<T, VE>(pdy, dyv);
                 unpack<T, VE>(px, xv);
-                ring_dz<T, VE>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
+                ring_dz<T, VE, ACT>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
                 const int64_t e = (p.seg * g.lv + p.v) * VE;
                 if (dres) store_vec_pol<T, VE>(dres + e, dz, pol_stream);
                 acc.add(dz, xv);
@@ -1477,7 +1530,7 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
                         float dyv[VE], xv[VE], dz[VE], o[VE];
                         unpack<T, VE>(pdy, dyv);
                         unpack<T, VE>(px, xv);
-                        ring_dz<T, VE>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
+                        ring_dz<T, VE, ACT>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
 #pragma unroll
                         for (int k = 0; k < VE; ++k) {
                             const float xh = (xv[k] - mu) * rs;
@@ -1691,8 +1744,10 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
         if (bn_fwd_group<T>(a, training, s, st)) return st;
     }
     if (vec && a.c > 0 && a.n * a.l > 0) {
-        const void* fn = training ? (const void*)&bn_fwd_ring_kernel<T, true>
-                                  : (const void*)&bn_fwd_ring_kernel<T, false>;
+        const void* fn = with_act(a.act, [&](auto act) {
+            return training ? (const void*)&bn_fwd_ring_kernel<T, true, decltype(act)::value>
+                            : (const void*)&bn_fwd_ring_kernel<T, false, decltype(act)::value>;
+        });
         BnPlan pl;
         bn_geometry(pl.g, a, kVec<T>);
         nrm_status st = bn_plan_ring(pl, a, fn, size_t(kRingSlotsFwd) * kSlotBytes, training ? 1 : 0, 2,
@@ -1715,11 +1770,13 @@ nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
         if (bn_bwd_group<T>(a, training, s, st)) return st;
     }
     if (vec && a.c > 0 && a.n * a.l > 0) {
-        const void* fn = training ? (const void*)&bn_bwd_ring_kernel<T, true>
-                                  : (const void*)&bn_bwd_ring_kernel<T, false>;
+        const void* fn = with_act(a.act, [&](auto act) {
+            return training ? (const void*)&bn_bwd_ring_kernel<T, true, decltype(act)::value>
+                            : (const void*)&bn_bwd_ring_kernel<T, false, decltype(act)::value>;
+        });
         BnPlan pl;
         bn_geometry(pl.g, a, kVec<T>);
-        const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
+        const bool need_z = bn_need_z(a.act, a.mask_in);
         const int nt = (need_z && a.res) ? 3 : 2;
         const int slots = training ? kRingSlotsBwdHbm + kRingSlotsBwdL2 : kRingSlotsBwd;
         const int threads = training ? kRingThreadsBwdTrain : kRingThreads;

@@ -85,7 +85,7 @@ __device__ __forceinline__ void grp_vec(const unsigned char* tile, int e, float 
     unpack<T, kVec<T>>(pk, v);
 }
 
-template <typename T, bool TRAIN>
+template <typename T, bool TRAIN, int ACT>
 __global__ void __launch_bounds__(kGrpThreads)
 bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
     constexpr int VE = kVec<T>;
@@ -185,7 +185,7 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
             }
             float z = fmaf(xv[k], coef[j].x, coef[j].y);
             if (res) z += rv[k];
-            ov[k] = act_forward(a.act, z);
+            ov[k] = act_forward_c<ACT>(z);
         }
         store_vec_pol<T, VE>(y + (int64_t(p.n0 + s) * g.c + p.ch0) * g.l + o, ov, pol);
     }
@@ -211,7 +211,7 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
     if (bad) atomicOr(a.err, kErrTimeoutStage);
 }
 
-template <typename T, bool TRAIN>
+template <typename T, bool TRAIN, int ACT>
 __global__ void __launch_bounds__(kGrpThreads)
 bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     constexpr int VE = kVec<T>;
@@ -228,8 +228,8 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     const T* __restrict__ res = reinterpret_cast<const T*>(a.res);
     T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
     T* __restrict__ dres = reinterpret_cast<T*>(a.dres);
-    const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
-    const bool use_mask = a.act == NRM_ACT_RELU && a.mask_in != nullptr;
+    const bool need_z = bn_need_z(ACT, a.mask_in);
+    const bool use_mask = ACT == NRM_ACT_RELU && a.mask_in != nullptr;
     const bool with_res = need_z && res != nullptr;
     const GrpPos p = grp_pos(g);
     const unsigned char* tdy = smem;
@@ -267,7 +267,7 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     // dz of element e of segment (s, j)
     auto dz_of = [&](int s, int j, int e, float dyv, float xv, float rv) {
         if (use_mask) return ((tm[(s * g.G + j) * g.words + (e >> 5)] >> (e & 31)) & 1u) ? dyv : 0.f;
-        if (need_z) return dyv * act_derivative(a.act, fmaf(xv, prm[j].z, prm[j].w) + rv);
+        if (need_z) return dyv * act_derivative_c<ACT>(fmaf(xv, prm[j].z, prm[j].w) + rv);
         return dyv;
     };
 
@@ -459,7 +459,10 @@ bool bn_fwd_group(const BnArgs& a, bool training, cudaStream_t s, nrm_status& st
     if (!aligned16(a.x) || !aligned16(a.res) || !aligned16(a.y)) return false;
     GrpPlan pl;
     if (!bn_plan_group(pl, a, sizeof(T), a.res ? 2 : 1, false, false)) return false;
-    const void* fn = training ? (const void*)&bn_fwd_group_kernel<T, true> : (const void*)&bn_fwd_group_kernel<T, false>;
+    const void* fn = with_act(a.act, [&](auto act) {
+        return training ? (const void*)&bn_fwd_group_kernel<T, true, decltype(act)::value>
+                        : (const void*)&bn_fwd_group_kernel<T, false, decltype(act)::value>;
+    });
     st = launch_group(fn, a, pl, s);
     return true;
 }
@@ -468,11 +471,14 @@ template <typename T>
 bool bn_bwd_group(const BnArgs& a, bool training, cudaStream_t s, nrm_status& st) {
     if (!aligned16(a.x) || !aligned16(a.res) || !aligned16(a.dy) || !aligned16(a.dx) || !aligned16(a.dres))
         return false;
-    const bool need_z = a.act == NRM_ACT_GELU || (a.act == NRM_ACT_RELU && a.mask_in == nullptr);
+    const bool need_z = bn_need_z(a.act, a.mask_in);
     const bool use_mask = a.act == NRM_ACT_RELU && a.mask_in != nullptr;
     GrpPlan pl;
     if (!bn_plan_group(pl, a, sizeof(T), (need_z && a.res) ? 3 : 2, true, use_mask)) return false;
-    const void* fn = training ? (const void*)&bn_bwd_group_kernel<T, true> : (const void*)&bn_bwd_group_kernel<T, false>;
+    const void* fn = with_act(a.act, [&](auto act) {
+        return training ? (const void*)&bn_bwd_group_kernel<T, true, decltype(act)::value>
+                        : (const void*)&bn_bwd_group_kernel<T, false, decltype(act)::value>;
+    });
     st = launch_group(fn, a, pl, s);
     return true;
 }

@@ -24,7 +24,7 @@ _SRC = os.path.join(_HERE, "norm_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
-ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU, ACT_MISH = 0, 1, 2, 3, 4
 
 # -ffp-contract=off keeps a*b+c as two roundings on every host (gcc fuses them by
 # default on aarch64), so the oracle gives the same bits here and on the GPU machine.

@@ -183,12 +183,20 @@ void oracle_rmsnorm_bwd(int64_t rows, int64_t cols, const double *dy,
 /* ------------------------------------------------------------------------ */
 
 /* [AF] section "五、反向传播融合同样成立": the activation derivative is taken from
- * the pre-activation input; GELU is the error-function form. */
+ * the pre-activation input; GELU is the error-function form.  [NK] BatchNorm
+ * section names silu and mish among the fused activations; their formulas are
+ * the standard ones (the articles give none): silu(z) = z * sigmoid(z),
+ * mish(z) = z * tanh(softplus(z)), softplus(z) = log(1 + e^z). */
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+static double softplus(double z) { return z > 0.0 ? z + log1p(exp(-z)) : log1p(exp(z)); }
+
 static double act_forward(int act, double z)
 {
     switch (act) {
     case ORACLE_ACT_RELU: return z > 0.0 ? z : 0.0;
     case ORACLE_ACT_GELU: return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
+    case ORACLE_ACT_SILU: return z * sigmoid(z);
+    case ORACLE_ACT_MISH: return z * tanh(softplus(z));
     default:              return z;
     }
 }
@@ -201,6 +209,16 @@ static double act_derivative(int act, double z)
         double cdf = 0.5 * (1.0 + erf(z / sqrt(2.0)));
         double pdf = exp(-0.5 * z * z) / sqrt(2.0 * M_PI);
         return cdf + z * pdf;
+    }
+    case ORACLE_ACT_SILU: {
+        /* d/dz z*s(z) = s + z*s*(1 - s) */
+        double s = sigmoid(z);
+        return s + z * s * (1.0 - s);
+    }
+    case ORACLE_ACT_MISH: {
+        /* d/dz z*tanh(sp(z)) = tanh(sp) + z*(1 - tanh(sp)^2)*sp'(z), sp' = sigmoid */
+        double t = tanh(softplus(z));
+        return t + z * (1.0 - t * t) * sigmoid(z);
     }
     default: return 1.0;
     }

@@ -25,7 +25,7 @@ import os
 import numpy as np
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-ACT = {"none": 0, "relu": 1, "gelu": 2}
+ACT = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "mish": 4}
 
 
 def _rng(seed):
@@ -281,6 +281,10 @@ def _torch_bn_forward(x, res, w, b, rm, rv, eps, momentum, training, act):
         return F.relu(z)
     if act == "gelu":
         return F.gelu(z, approximate="none")
+    if act == "silu":
+        return F.silu(z)
+    if act == "mish":
+        return F.mish(z)
     return z
 
 
@@ -289,7 +293,7 @@ def pin_batchnorm_vs_torch(o):
     r = _rng(12)
     n, c, l = 3, 4, 7
     for training in (True, False):
-        for act in ("none", "relu", "gelu"):
+        for act in ("none", "relu", "gelu", "silu", "mish"):
             for with_res in (False, True):
                 x = r.normal(size=(n, c, l)) * 1.7 + 0.4
                 res = r.normal(size=(n, c, l)) if with_res else None
@@ -317,6 +321,31 @@ def pin_gelu_values(o):
     _close(out["y"].ravel(), z.ravel() * phi, 1e-15, 1e-16, "gelu = z * Phi(z)")
     # Phi(1) = 0.8413447460685429 (standard normal table)
     _close(out["y"].ravel()[4], 0.8413447460685429, 1e-15, 0, "gelu(1)")
+
+
+def pin_silu_mish_values(o):
+    # eval mode with running_mean 0 and running_var + eps = 1 makes z = x exactly;
+    # then y = act(z) and, with w = 1 and dy = 1, dx = act'(z)
+    ln3 = math.log(3.0)
+    z = np.array([0.0, ln3, -ln3, math.log(math.e - 1.0), 2.0]).reshape(1, 1, 5)
+    rm, rv = np.zeros(1), np.array([0.75])
+    y_silu = o.batchnorm_fwd(z, eps=0.25, training=False, act=ACT["silu"], running_mean=rm,
+                             running_var=rv)["y"].ravel()
+    # sigmoid(ln 3) = 3/4, sigmoid(-ln 3) = 1/4
+    _close(y_silu[:3], [0.0, 0.75 * ln3, -0.25 * ln3], 1e-15, 1e-16, "silu(0), silu(+-ln 3)")
+    y_mish = o.batchnorm_fwd(z, eps=0.25, training=False, act=ACT["mish"], running_mean=rm,
+                             running_var=rv)["y"].ravel()
+    # softplus(log(e - 1)) = 1, so mish = log(e - 1) * tanh(1)
+    _close(y_mish[[0, 3]], [0.0, math.log(math.e - 1.0) * math.tanh(1.0)], 1e-15, 1e-16, "mish(0), mish(log(e-1))")
+    dy = np.ones_like(z)
+    dx_silu = o.batchnorm_bwd(dy, z, None, np.ones(1), np.zeros(1), rm, rv, eps=0.25, training=False,
+                              act=ACT["silu"])[0].ravel()
+    # silu'(0) = 1/2; silu'(ln 3) = 3/4 + ln3 * 3/16
+    _close(dx_silu[:2], [0.5, 0.75 + ln3 * 3.0 / 16.0], 1e-15, 1e-16, "silu'(0), silu'(ln 3)")
+    dx_mish = o.batchnorm_bwd(dy, z, None, np.ones(1), np.zeros(1), rm, rv, eps=0.25, training=False,
+                              act=ACT["mish"])[0].ravel()
+    # mish'(0) = tanh(ln 2) = 3/5
+    _close(dx_mish[0], 0.6, 1e-15, 1e-16, "mish'(0)")
 
 
 def pin_batchnorm_mask_layout(o):
@@ -361,7 +390,7 @@ def pin_batchnorm_bwd_fd(o):
     eps = 1e-3
     for (n, c, l) in ((2, 3, 4), (3, 2, 5)):
         for training in (True, False):
-            for act in ("none", "relu", "gelu"):
+            for act in ("none", "relu", "gelu", "silu", "mish"):
                 for with_res in (False, True):
                     x, res, w, b = _bn_inputs_away_from_kinks(r, n, c, l, act, with_res)
                     dy = r.normal(size=(n, c, l))
@@ -410,8 +439,10 @@ def pin_batchnorm_bwd_vs_torch(o):
     F = torch.nn.functional
     r = _rng(16)
     n, c, l = 3, 4, 6
+    acts = {"none": lambda z: z, "gelu": lambda z: F.gelu(z, approximate="none"), "silu": F.silu,
+            "mish": F.mish}
     for training in (True, False):
-        for act in ("none", "gelu"):
+        for act in acts:
             x = torch.tensor(r.normal(size=(n, c, l)) * 1.5, requires_grad=True)
             res = torch.tensor(r.normal(size=(n, c, l)), requires_grad=True)
             w = torch.tensor(1 + 0.3 * r.normal(size=c), requires_grad=True)
@@ -420,7 +451,7 @@ def pin_batchnorm_bwd_vs_torch(o):
             rv = 1 + 0.2 * r.uniform(size=c)
             z = F.batch_norm(x, torch.from_numpy(rm.copy()), torch.from_numpy(rv.copy()), w, b,
                              training=training, momentum=0.1, eps=1e-5) + res
-            y = F.gelu(z, approximate="none") if act == "gelu" else z
+            y = acts[act](z)
             dy = r.normal(size=(n, c, l))
             y.backward(torch.from_numpy(dy))
             dx, dres, dw, db = o.batchnorm_bwd(dy, x.detach().numpy(), res.detach().numpy(),

@@ -182,7 +182,8 @@ def run_bn(inp, dtype, eps, momentum, training, act, with_res, use_mask, with_af
 
 def oracle_bn(orc, inp, eps, momentum, training, act, with_res, with_affine=True):
     import oracle as oracle_mod
-    a = {"none": oracle_mod.ACT_NONE, "relu": oracle_mod.ACT_RELU, "gelu": oracle_mod.ACT_GELU}[act]
+    a = {"none": oracle_mod.ACT_NONE, "relu": oracle_mod.ACT_RELU, "gelu": oracle_mod.ACT_GELU,
+         "silu": oracle_mod.ACT_SILU, "mish": oracle_mod.ACT_MISH}[act]
     x = inp["x"].f64()
     res = inp["res"].f64() if with_res else None
     w = inp["w"].f64() if with_affine else None

@@ -42,6 +42,13 @@ MUTATIONS = {
     "bn_dx_drops_mean_term": ("(dz - sum_dz / (double)m - xhat", "(dz - xhat"),
     "bn_dw_not_xhat": ("sum_dz_xhat += dz * xhat;", "sum_dz_xhat += dz * x[e];"),
     "bn_eval_dx_drops_weight": ("dx[e] = wc * rs * dz;", "dx[e] = rs * dz;"),
+    "silu_uses_tanh": ("case ORACLE_ACT_SILU: return z * sigmoid(z);",
+                       "case ORACLE_ACT_SILU: return z * tanh(z);"),
+    "silu_grad_drops_product_term": ("return s + z * s * (1.0 - s);", "return s;"),
+    "mish_softplus_without_log": ("case ORACLE_ACT_MISH: return z * tanh(softplus(z));",
+                                  "case ORACLE_ACT_MISH: return z * tanh(exp(z));"),
+    "mish_grad_wrong_chain_factor": ("return t + z * (1.0 - t * t) * sigmoid(z);",
+                                     "return t + z * (1.0 - t * t);"),
 }
 
 

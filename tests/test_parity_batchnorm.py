@@ -57,9 +57,9 @@ ODD = [
 def test_bn_odd_shapes(orc, dtype, shape):
     n, c, l = shape
     idx = ODD.index(shape)
-    acts = ["none", "relu", "gelu"]
+    acts = ["none", "relu", "gelu", "silu", "mish"]
     for training in (True, False):
-        act = acts[(idx + int(training)) % 3]
+        act = acts[(idx + 2 * int(training)) % len(acts)]
         with_res = (idx % 2 == 0)
         cfg = synth.BnConfig("odd", n, c, l, dtype, 1e-5, 0.1, seed=200 + idx, act=act,
                              residual=with_res, x_kind="offset_scale", w_std=0.2, b_std=0.2)
@@ -137,7 +137,7 @@ def test_bn_channel_groups(orc, case):
     idx = GROUPS.index(case)
     for training in (True, False):
         for act, with_res, use_mask in (("relu", True, True), ("gelu", False, False), ("none", True, False),
-                                        ("relu", False, False)):
+                                        ("relu", False, False), ("silu", True, False), ("mish", False, False)):
             cfg = synth.BnConfig("grp", n, c, l, dtype, 1e-5, 0.1, seed=500 + idx, act=act,
                                  residual=with_res, x_kind="offset_scale", w_std=0.2, b_std=0.2)
             inp = synth.bn_inputs(cfg)
@@ -148,3 +148,21 @@ def test_bn_channel_groups(orc, case):
             want = oracle_bn(orc, inp, cfg.eps, cfg.momentum, training, act, with_res)
             compare_bn(got, want, dtype, training, act,
                        f"bn {dtype} {case} training={training} act={act} res={with_res} mask={use_mask}")
+
+
+@pytest.mark.parametrize("act", ["silu", "mish"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bn_silu_mish_vector_path(orc, act, dtype):
+    # the ring kernels with z recomputed in the backward, with and without a residual
+    n, c, l = 32, 6, 1568
+    for training in (True, False):
+        for with_res in (False, True):
+            cfg = synth.BnConfig("act", n, c, l, dtype, 1e-5, 0.1, seed=700 + int(with_res), act=act,
+                                 residual=with_res, x_kind="offset_scale", w_std=0.2, b_std=0.2)
+            inp = synth.bn_inputs(cfg)
+            if not training:
+                inp["running_mean"] = synth.store(0.2 * synth.normal(cfg.seed, 20, c), "f32", (c,))
+                inp["running_var"] = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,))
+            got = run_bn(inp, dtype, cfg.eps, cfg.momentum, training, act, with_res, False)
+            want = oracle_bn(orc, inp, cfg.eps, cfg.momentum, training, act, with_res)
+            compare_bn(got, want, dtype, training, act, f"bn {dtype} {act} training={training} res={with_res}")
