@@ -113,14 +113,17 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
     if (p.ns > 0 && !mbar_wait_bounded(&bar, 0, kBnWaitLimitNs)) bad = true;
 
     if constexpr (TRAIN) {
-        // warp w: channel w % G, every (kGrpWarps / G)-th sample from w / G
+        // the warps w with w % G == j share channel j: its ns*l elements
+        // (sample-major) are dealt to their lanes, so every lane's chain is
+        // short even when l is 1
         const int j = warp % g.G;
+        const int wpc = kGrpWarps / g.G;  // warps per channel
         ShiftedSums acc;
-        for (int s = warp / g.G; s < p.ns; s += kGrpWarps / g.G)
-            for (int e = lane; e < g.l; e += 32) {
-                const float v[1] = {grp_elem<T>(tx, s * g.span + j * g.l + e)};
-                acc.add(v);
-            }
+        for (int t = (warp / g.G) * 32 + lane; t < p.ns * g.l; t += wpc * 32) {
+            const int s = int(fast_div(uint32_t(t), g.div_l));
+            const float v[1] = {grp_elem<T>(tx, s * g.span + j * g.l + (t - s * g.l))};
+            acc.add(v);
+        }
         Moments m = acc.moments();
         warp_merge(m);
         if (lane == 0) wm[warp] = m;
@@ -274,16 +277,18 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     // ---- the two channel sums: warp w takes channel w % G ----
     {
         const int j = warp % g.G;
+        const int wpc = kGrpWarps / g.G;
         GradSums acc;
-        for (int s = warp / g.G; s < p.ns; s += kGrpWarps / g.G)
-            for (int e = lane; e < g.l; e += 32) {
-                const int idx = s * g.span + j * g.l + e;
-                const float xv[1] = {grp_elem<T>(tx, idx)};
-                const float rv = with_res ? grp_elem<T>(tr, idx) : 0.f;
-                const float dz[1] = {dz_of(s, j, e, grp_elem<T>(tdy, idx), xv[0], rv)};
-                tz[idx] = dz[0];
-                acc.add(dz, xv);
-            }
+        for (int t = (warp / g.G) * 32 + lane; t < p.ns * g.l; t += wpc * 32) {
+            const int s = int(fast_div(uint32_t(t), g.div_l));
+            const int e = t - s * g.l;
+            const int idx = s * g.span + j * g.l + e;
+            const float xv[1] = {grp_elem<T>(tx, idx)};
+            const float rv = with_res ? grp_elem<T>(tr, idx) : 0.f;
+            const float dz[1] = {dz_of(s, j, e, grp_elem<T>(tdy, idx), xv[0], rv)};
+            tz[idx] = dz[0];
+            acc.add(dz, xv);
+        }
         const FF d1 = ff_warp_sum(acc.ff_dz());
         const FF d2 = ff_warp_sum(acc.ff_dzx());
         if (lane == 0) ws[warp] = make_double2(ff_to_double(d1), ff_to_double(d2));

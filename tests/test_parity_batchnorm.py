@@ -166,3 +166,26 @@ def test_bn_silu_mish_vector_path(orc, act, dtype):
             got = run_bn(inp, dtype, cfg.eps, cfg.momentum, training, act, with_res, False)
             want = oracle_bn(orc, inp, cfg.eps, cfg.momentum, training, act, with_res)
             compare_bn(got, want, dtype, training, act, f"bn {dtype} {act} training={training} res={with_res}")
+
+
+BN1D = [("f32", 4096, 64), ("f16", 4096, 64), ("bf16", 300, 24), ("f32", 50000, 8)]
+
+
+@pytest.mark.parametrize("case", BN1D, ids=[f"{d}-{n}x{c}" for d, n, c in BN1D])
+def test_bn1d(orc, case):
+    # BatchNorm1d on [N, C] is [n, c, l] with l = 1: a sample's channels are
+    # contiguous, so G channels form one 16-byte span (the channel-group path,
+    # or the scalar path when a group does not fit in shared memory)
+    dtype, n, c = case
+    for training in (True, False):
+        for act, with_res, use_mask in (("relu", True, True), ("none", False, False), ("silu", True, False)):
+            cfg = synth.BnConfig("bn1d", n, c, 1, dtype, 1e-5, 0.1, seed=900 + n + c, act=act,
+                                 residual=with_res, x_kind="offset_scale", w_std=0.2, b_std=0.2)
+            inp = synth.bn_inputs(cfg)
+            if not training:
+                inp["running_mean"] = synth.store(0.2 * synth.normal(cfg.seed, 20, c), "f32", (c,))
+                inp["running_var"] = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,))
+            got = run_bn(inp, dtype, cfg.eps, cfg.momentum, training, act, with_res, use_mask)
+            want = oracle_bn(orc, inp, cfg.eps, cfg.momentum, training, act, with_res)
+            compare_bn(got, want, dtype, training, act,
+                       f"bn1d {dtype} [{n},{c}] training={training} act={act} res={with_res}")
