@@ -76,6 +76,8 @@ class Oracle:
         lib = ctypes.CDLL(self.lib_path)
         lib.oracle_layernorm_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D, _D]
         lib.oracle_layernorm_bwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D, _D]
+        lib.oracle_layernorm_cf_fwd.argtypes = [_I64, _I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D, _D]
+        lib.oracle_layernorm_cf_bwd.argtypes = [_I64, _I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D, _D]
         lib.oracle_rmsnorm_fwd.argtypes = [_I64, _I64, _D, _D, ctypes.c_double, _D, _D]
         lib.oracle_rmsnorm_bwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D]
         lib.oracle_batchnorm_fwd.argtypes = [_I64, _I64, _I64, _D, _D, _D, _D,
@@ -85,7 +87,8 @@ class Oracle:
         lib.oracle_batchnorm_bwd.argtypes = [_I64, _I64, _I64, _D, _D, _D, _D, _D,
                                              _D, _D, ctypes.c_double, ctypes.c_int,
                                              ctypes.c_int, _U32, _D, _D, _D, _D]
-        for f in ("oracle_layernorm_fwd", "oracle_layernorm_bwd", "oracle_rmsnorm_fwd",
+        for f in ("oracle_layernorm_fwd", "oracle_layernorm_bwd", "oracle_layernorm_cf_fwd",
+                  "oracle_layernorm_cf_bwd", "oracle_rmsnorm_fwd",
                   "oracle_rmsnorm_bwd", "oracle_batchnorm_fwd", "oracle_batchnorm_bwd"):
             getattr(lib, f).restype = None
         self.lib = lib
@@ -112,6 +115,30 @@ class Oracle:
         db = np.empty(cols)
         self.lib.oracle_layernorm_bwd(rows, cols, _ptr(dy), _ptr(x), _ptr(w), eps,
                                       _ptr(dx), _ptr(dw), _ptr(db))
+        return dx, dw, db
+
+    def layernorm_cf_fwd(self, x, w=None, b=None, eps=1e-6):
+        """Channels-first LayerNorm: x of shape [n, c, l]; returns (y, mean, rstd),
+        mean and rstd of shape [n, l]."""
+        x = _f64(x)
+        n, c, l = x.shape
+        w, b = _f64(w), _f64(b)
+        y = np.empty_like(x)
+        mean = np.empty((n, l))
+        rstd = np.empty((n, l))
+        self.lib.oracle_layernorm_cf_fwd(n, c, l, _ptr(x), _ptr(w), _ptr(b), eps, _ptr(y),
+                                         _ptr(mean), _ptr(rstd))
+        return y, mean, rstd
+
+    def layernorm_cf_bwd(self, dy, x, w=None, eps=1e-6):
+        """Returns (dx, dw, db) of the channels-first LayerNorm."""
+        dy, x, w = _f64(dy), _f64(x), _f64(w)
+        n, c, l = x.shape
+        dx = np.empty_like(x)
+        dw = np.empty(c)
+        db = np.empty(c)
+        self.lib.oracle_layernorm_cf_bwd(n, c, l, _ptr(dy), _ptr(x), _ptr(w), eps, _ptr(dx),
+                                         _ptr(dw), _ptr(db))
         return dx, dw, db
 
     def rmsnorm_fwd(self, x, w=None, eps=1e-6):

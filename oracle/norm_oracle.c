@@ -179,6 +179,84 @@ void oracle_rmsnorm_bwd(int64_t rows, int64_t cols, const double *dy,
 }
 
 /* ------------------------------------------------------------------------ */
+/* LayerNorm over the channels of an NCHW tensor                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The LayerNorm of [NK] section "LayerNorm：一个程序归一化一批行" (mean, biased
+ * variance, reciprocal square root, weight and bias), taken for every sample i
+ * and spatial position p over the c channels of x[i, :, p], x of shape
+ * [n, c, l] with l = H*W.  [NK] section "三种核共享的工程技巧" (application
+ * paragraph) has ConvNeXt use attorch.LayerNorm; ConvNeXt normalises over the
+ * channels of each position.  mean and rstd are [n, l].
+ */
+void oracle_layernorm_cf_fwd(int64_t n, int64_t c, int64_t l, const double *x,
+                             const double *w, const double *b, double eps,
+                             double *y, double *mean, double *rstd)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        for (int64_t p = 0; p < l; ++p) {
+            const double *xp = x + i * c * l + p;
+            double sum = 0.0;
+            for (int64_t ch = 0; ch < c; ++ch) sum += xp[ch * l];
+            double mu = sum / (double)c;
+            double ssd = 0.0;
+            for (int64_t ch = 0; ch < c; ++ch) {
+                double d = xp[ch * l] - mu;
+                ssd += d * d;
+            }
+            double var = ssd / (double)c;
+            double inv_std = 1.0 / sqrt(var + eps);
+            for (int64_t ch = 0; ch < c; ++ch) {
+                double xhat = (xp[ch * l] - mu) * inv_std;
+                y[i * c * l + ch * l + p] = xhat * (w ? w[ch] : 1.0) + (b ? b[ch] : 0.0);
+            }
+            if (mean) mean[i * l + p] = mu;
+            if (rstd) rstd[i * l + p] = inv_std;
+        }
+    }
+}
+
+/* Backward of the above: with g = dy*w over the channels of a position,
+ * dx = rstd*(g - sum(g)/c - xhat*sum(g*xhat)/c); dw = sum over (i, p) of
+ * dy*xhat, db = sum of dy (the row LayerNorm's backward, per position). */
+void oracle_layernorm_cf_bwd(int64_t n, int64_t c, int64_t l, const double *dy,
+                             const double *x, const double *w, double eps,
+                             double *dx, double *dw, double *db)
+{
+    if (dw) for (int64_t ch = 0; ch < c; ++ch) dw[ch] = 0.0;
+    if (db) for (int64_t ch = 0; ch < c; ++ch) db[ch] = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        for (int64_t p = 0; p < l; ++p) {
+            const int64_t base = i * c * l + p;
+            double sum = 0.0;
+            for (int64_t ch = 0; ch < c; ++ch) sum += x[base + ch * l];
+            double mu = sum / (double)c;
+            double ssd = 0.0;
+            for (int64_t ch = 0; ch < c; ++ch) {
+                double d = x[base + ch * l] - mu;
+                ssd += d * d;
+            }
+            double rs = 1.0 / sqrt(ssd / (double)c + eps);
+            double sum_g = 0.0, sum_gxhat = 0.0;
+            for (int64_t ch = 0; ch < c; ++ch) {
+                double g = dy[base + ch * l] * (w ? w[ch] : 1.0);
+                double xhat = (x[base + ch * l] - mu) * rs;
+                sum_g += g;
+                sum_gxhat += g * xhat;
+            }
+            for (int64_t ch = 0; ch < c; ++ch) {
+                double g = dy[base + ch * l] * (w ? w[ch] : 1.0);
+                double xhat = (x[base + ch * l] - mu) * rs;
+                dx[base + ch * l] = rs * (g - sum_g / (double)c - xhat * sum_gxhat / (double)c);
+                if (dw) dw[ch] += dy[base + ch * l] * xhat;
+                if (db) db[ch] += dy[base + ch * l];
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* BatchNorm with fused residual add and activation                          */
 /* ------------------------------------------------------------------------ */
 

@@ -477,4 +477,62 @@ def pin_batchnorm_bwd_mask_matches_recompute(o):
         _close(u, v, 1e-14, 1e-15, "mask-driven vs recomputed ReLU' " + name)
 
 
+def pin_layernorm_cf_is_row_layernorm_of_the_transpose(o):
+    # channels-first LayerNorm of x[n, c, l] = row LayerNorm of the [n*l, c] matrix
+    # whose row (i, p) is x[i, :, p]; both sum the channels in the same order, so
+    # the results agree to the last bit
+    r = _rng(30)
+    n, c, l = 3, 7, 11
+    x = r.normal(size=(n, c, l)) * 1.4 + 0.3
+    w = 1 + 0.2 * r.normal(size=c)
+    b = 0.2 * r.normal(size=c)
+    y, mean, rstd = o.layernorm_cf_fwd(x, w, b, eps=1e-5)
+    rows = x.transpose(0, 2, 1).reshape(n * l, c)
+    yr, mr, rr = o.layernorm_fwd(rows, w, b, eps=1e-5)
+    _close(y, yr.reshape(n, l, c).transpose(0, 2, 1), 0, 0, "cf y == row y of the transpose")
+    _close(mean.ravel(), mr, 0, 0, "cf mean")
+    _close(rstd.ravel(), rr, 0, 0, "cf rstd")
+    dy = r.normal(size=(n, c, l))
+    dx, dw, db = o.layernorm_cf_bwd(dy, x, w, eps=1e-5)
+    dxr, dwr, dbr = o.layernorm_bwd(dy.transpose(0, 2, 1).reshape(n * l, c), rows, w, eps=1e-5)
+    _close(dx, dxr.reshape(n, l, c).transpose(0, 2, 1), 0, 0, "cf dx")
+    _close(dw, dwr, 1e-15, 1e-15, "cf dw")
+    _close(db, dbr, 1e-15, 1e-15, "cf db")
+
+
+def pin_layernorm_cf_vs_torch(o):
+    import torch
+    F = torch.nn.functional
+    r = _rng(31)
+    n, c, l = 2, 5, 9
+    x = torch.tensor(r.normal(size=(n, c, l)) * 2 - 0.5, requires_grad=True)
+    w = torch.tensor(1 + 0.3 * r.normal(size=c), requires_grad=True)
+    b = torch.tensor(0.3 * r.normal(size=c), requires_grad=True)
+    y = F.layer_norm(x.permute(0, 2, 1), [c], w, b, eps=1e-6).permute(0, 2, 1)
+    dy = r.normal(size=(n, c, l))
+    y.backward(torch.from_numpy(dy))
+    yo, _, _ = o.layernorm_cf_fwd(x.detach().numpy(), w.detach().numpy(), b.detach().numpy(), eps=1e-6)
+    dx, dw, db = o.layernorm_cf_bwd(dy, x.detach().numpy(), w.detach().numpy(), eps=1e-6)
+    _close(yo, y.detach().numpy(), 1e-12, 1e-13, "cf y vs torch")
+    _close(dx, x.grad.numpy(), 1e-10, 1e-12, "cf dx vs torch")
+    _close(dw, w.grad.numpy(), 1e-10, 1e-12, "cf dw vs torch")
+    _close(db, b.grad.numpy(), 1e-10, 1e-12, "cf db vs torch")
+
+
+def pin_layernorm_cf_bwd_fd(o):
+    r = _rng(32)
+    n, c, l = 2, 4, 3
+    x = r.normal(size=(n, c, l)) + 0.2
+    w = 1 + 0.3 * r.normal(size=c)
+    b = 0.3 * r.normal(size=c)
+    dy = r.normal(size=(n, c, l))
+
+    def loss():
+        return float((dy * o.layernorm_cf_fwd(x, w, b, eps=1e-3)[0]).sum())
+    dx, dw, db = o.layernorm_cf_bwd(dy, x, w, eps=1e-3)
+    _close(dx, _central_diff(loss, x, 1e-6), 1e-6, 1e-7, "cf dx vs FD")
+    _close(dw, _central_diff(loss, w, 1e-6), 1e-6, 1e-7, "cf dw vs FD")
+    _close(db, _central_diff(loss, b, 1e-6), 1e-6, 1e-7, "cf db vs FD")
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

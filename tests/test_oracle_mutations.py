@@ -42,6 +42,9 @@ MUTATIONS = {
     "bn_dx_drops_mean_term": ("(dz - sum_dz / (double)m - xhat", "(dz - xhat"),
     "bn_dw_not_xhat": ("sum_dz_xhat += dz * xhat;", "sum_dz_xhat += dz * x[e];"),
     "bn_eval_dx_drops_weight": ("dx[e] = wc * rs * dz;", "dx[e] = rs * dz;"),
+    "ln_cf_divides_by_positions": ("double var = ssd / (double)c;", "double var = ssd / (double)l;"),
+    "ln_cf_dw_uses_x": ("if (dw) dw[ch] += dy[base + ch * l] * xhat;",
+                        "if (dw) dw[ch] += dy[base + ch * l] * x[base + ch * l];"),
     "silu_uses_tanh": ("case ORACLE_ACT_SILU: return z * sigmoid(z);",
                        "case ORACLE_ACT_SILU: return z * tanh(z);"),
     "silu_grad_drops_product_term": ("return s + z * s * (1.0 - s);", "return s;"),
