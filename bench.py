@@ -12,7 +12,9 @@ L2 is flushed (a 512 MB write) before every call; each call is timed with CUDA
 events on the stream it is launched on.  value = algorithmic bytes of the step
 (every input read once, every output written once, saved statistics, ReLU mask
 bits) / summed device time, in GB/s.  Per-call times, GB/s and fraction of the
-measured HBM copy bandwidth are reported per workload.
+measured HBM copy bandwidth are reported per workload.  Beside the step, and
+outside its value, extra_rows times the channels-first LayerNorm on fp16
+[128, 96, 56, 56] (ConvNeXt-T's 96 channels of 56x56) the same way.
 
 --impl reference times the CPU oracle (plain double-precision C, one core) on a
 bounded sample of the same workloads (a quarter of the rows or channels of each).
@@ -180,11 +182,12 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(dev)
     nrm.load()
     calls = workloads.build_calls(dev)
+    extra = workloads.build_extra_calls(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def one_step(record):
-        for c in calls:
+    def one_step(record, which=calls):
+        for c in which:
             flush.fill_(1.0)
             s = torch.cuda.Event(enable_timing=True)
             e = torch.cuda.Event(enable_timing=True)
@@ -212,28 +215,24 @@ def run_gpu(args, world, rank, local):
     nrm.nrm_sync_status()
     for c, s, e in recs:
         c.times_ms.append(s.elapsed_time(e))
+    # the operations built beyond the step, timed the same way after it
+    for _ in range(args.warmup):
+        one_step(None, extra)
+    recs = []
+    for _ in range(args.steps):
+        one_step(recs, extra)
+    torch.cuda.synchronize()
+    nrm.nrm_sync_status()
+    for c, s, e in recs:
+        c.times_ms.append(s.elapsed_time(e))
 
     step_ms_local = sum(statistics.mean(c.times_ms) for c in calls)
     step_bytes = sum(c.bytes for c in calls)
     step_ms, value = aggregate(step_ms_local, step_bytes, world)
 
     peak, peak_src = hbm_peak()
-    per = {}
-    for c in calls:
-        t = statistics.mean(c.times_ms)
-        gbs = c.bytes / (t * 1e-3) / 1e9
-        d = per.setdefault(c.workload, {})
-        d[f"{c.phase}_us"] = round(t * 1e3, 2)
-        d[f"{c.phase}_us_median"] = round(statistics.median(c.times_ms) * 1e3, 2)
-        d[f"{c.phase}_bytes"] = c.bytes
-        d[f"{c.phase}_gbs"] = round(gbs, 1)
-        d[f"{c.phase}_frac"] = round(gbs / peak, 4)
-    for d in per.values():
-        if "fwd_us" in d and "bwd_us" in d:
-            t = (d["fwd_us"] + d["bwd_us"]) * 1e-6
-            d["fwd_bwd_us"] = round(d["fwd_us"] + d["bwd_us"], 2)
-            d["fwd_bwd_gbs"] = round((d["fwd_bytes"] + d["bwd_bytes"]) / t / 1e9, 1)
-            d["fwd_bwd_frac"] = round((d["fwd_bytes"] + d["bwd_bytes"]) / t / 1e9 / peak, 4)
+    per = per_workload(calls, peak)
+    extra_rows = per_workload(extra, peak)
 
     dom = max(calls, key=lambda c: statistics.mean(c.times_ms) / c.launches)
     dom_t = statistics.mean(dom.times_ms)
@@ -258,10 +257,33 @@ def run_gpu(args, world, rank, local):
         "e2e": e2e,
         "clocks": clock_info,
         "per_config": per,
+        "extra_rows": extra_rows,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(reps=24)
     return line
+
+
+def per_workload(calls, peak):
+    """Per workload and phase: mean and median device time, bytes, GB/s and
+    fraction of the measured HBM bandwidth."""
+    per = {}
+    for c in calls:
+        t = statistics.mean(c.times_ms)
+        gbs = c.bytes / (t * 1e-3) / 1e9
+        d = per.setdefault(c.workload, {})
+        d[f"{c.phase}_us"] = round(t * 1e3, 2)
+        d[f"{c.phase}_us_median"] = round(statistics.median(c.times_ms) * 1e3, 2)
+        d[f"{c.phase}_bytes"] = c.bytes
+        d[f"{c.phase}_gbs"] = round(gbs, 1)
+        d[f"{c.phase}_frac"] = round(gbs / peak, 4)
+    for d in per.values():
+        if "fwd_us" in d and "bwd_us" in d:
+            t = (d["fwd_us"] + d["bwd_us"]) * 1e-6
+            d["fwd_bwd_us"] = round(d["fwd_us"] + d["bwd_us"], 2)
+            d["fwd_bwd_gbs"] = round((d["fwd_bytes"] + d["bwd_bytes"]) / t / 1e9, 1)
+            d["fwd_bwd_frac"] = round((d["fwd_bytes"] + d["bwd_bytes"]) / t / 1e9 / peak, 4)
+    return per
 
 
 def run_e2e(calls, args, stream, step_bytes, world):

@@ -86,7 +86,11 @@ typedef enum nrm_act {
 } nrm_act;
 
 /* Operations that need a workspace (for nrm_workspace_bytes). */
-typedef enum nrm_op { NRM_OP_LAYERNORM_BWD = 1, NRM_OP_RMSNORM_BWD = 2 } nrm_op;
+typedef enum nrm_op {
+    NRM_OP_LAYERNORM_BWD = 1,
+    NRM_OP_RMSNORM_BWD = 2,
+    NRM_OP_LAYERNORM_CF_BWD = 3 /* rows: n*l (unused), cols: c */
+} nrm_op;
 
 /* ------------------------------------------------------------------------ */
 /* LayerNorm over the last dimension                                         */
@@ -152,6 +156,45 @@ NRM_API nrm_status nrm_layernorm_bwd_noalloc(const void *dy, const void *x, cons
                                      const float *mean, const float *rstd, void *dx,
                                      void *dw, void *db, int64_t rows, int64_t cols,
                                      nrm_dtype dt, nrm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* LayerNorm over the channels of an NCHW tensor (channels first)            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * nrm_layernorm_cf_fwd -- the LayerNorm of nrm_layernorm_fwd ([NK] section
+ * "LayerNorm：一个程序归一化一批行", forward steps 1-4) taken over the channels:
+ * for x of shape [n, c, l] (NCHW, l = H*W), for every sample i and spatial
+ * position p,
+ *   mean = sum_ch x[i,ch,p] / c;  var = sum_ch (x[i,ch,p] - mean)^2 / c
+ *   rstd = (var + eps)^(-1/2);  y[i,ch,p] = (x[i,ch,p] - mean)*rstd*w[ch] + b[ch]
+ * (the layout of ConvNeXt, which [NK] section "三种核共享的工程技巧" lists as a
+ * LayerNorm user; it normalises the channels of each position).  x, y:
+ * [n, c, l] in dt.  w, b: [c] in dt, each may be NULL (1 and 0).  mean,
+ * rstd: float32 [n, l], each may be NULL.  n, l >= 0 (an empty tensor is a
+ * no-op), 1 <= c <= 16384, eps > 0.
+ */
+NRM_API nrm_status nrm_layernorm_cf_fwd(const void *x, const void *w, const void *b, void *y,
+                                float *mean, float *rstd, int64_t n, int64_t c, int64_t l,
+                                float eps, nrm_dtype dt, nrm_stream_t stream);
+
+/*
+ * nrm_layernorm_cf_bwd -- backward of nrm_layernorm_cf_fwd: per (sample,
+ * position), with g = dy*w and xhat = (x - mean)*rstd over its channels,
+ *   dx = rstd * (g - sum(g)/c - xhat * sum(g*xhat)/c)
+ *   dw[ch] = sum over (i, p) of dy*xhat;  db[ch] = sum over (i, p) of dy
+ * dy, x, dx: [n, c, l] in dt.  w: [c] in dt or NULL (1).  mean, rstd:
+ * float32 [n, l] as written by nrm_layernorm_cf_fwd.  dw, db: [c] in dt, each
+ * may be NULL.  workspace: at least
+ * nrm_workspace_bytes(NRM_OP_LAYERNORM_CF_BWD, n*l, c, dt) bytes, 16-byte
+ * aligned, scratch for the per-block dw/db partial sums (clobbered); may be
+ * NULL when dw and db are both NULL.  Two kernels are enqueued when dw or db
+ * is requested.  Errors as nrm_layernorm_bwd.
+ */
+NRM_API nrm_status nrm_layernorm_cf_bwd(const void *dy, const void *x, const void *w,
+                                const float *mean, const float *rstd, void *dx, void *dw,
+                                void *db, int64_t n, int64_t c, int64_t l, nrm_dtype dt,
+                                void *workspace, size_t workspace_bytes, nrm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* RMSNorm over the last dimension                                           */

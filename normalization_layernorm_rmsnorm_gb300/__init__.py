@@ -10,8 +10,8 @@ from ._binding import (  # noqa: F401
     ACTS, EXPORTS, LIB_PATH, NRM_ACT_GELU, NRM_ACT_MISH, NRM_ACT_NONE, NRM_ACT_RELU, NRM_ACT_SILU,
     NRM_BF16, NRM_ERR_CUDA,
     NRM_ERR_INVALID_ARG, NRM_ERR_TIMEOUT, NRM_ERR_UNSUPPORTED, NRM_ERR_WORKSPACE, NRM_F16,
-    NRM_F32, NRM_OK, NRM_OP_LAYERNORM_BWD, NRM_OP_RMSNORM_BWD, NrmError, batchnorm_workspace, load,
+    NRM_F32, NRM_OK, NRM_OP_LAYERNORM_BWD, NRM_OP_LAYERNORM_CF_BWD, NRM_OP_RMSNORM_BWD, NrmError, batchnorm_workspace, load,
     nrm_act_mask_words, nrm_batchnorm_bwd, nrm_batchnorm_fwd, nrm_batchnorm_workspace_bytes, nrm_last_error_message,
-    nrm_layernorm_bwd, nrm_layernorm_bwd_noalloc, nrm_layernorm_fwd, nrm_rmsnorm_bwd, nrm_rmsnorm_fwd, nrm_status_str,
+    nrm_layernorm_bwd, nrm_layernorm_bwd_noalloc, nrm_layernorm_cf_bwd, nrm_layernorm_cf_fwd, nrm_layernorm_fwd, nrm_rmsnorm_bwd, nrm_rmsnorm_fwd, nrm_status_str,
     nrm_sync_status, nrm_version, nrm_workspace_bytes,
 )

@@ -18,13 +18,14 @@ LIB_PATH = os.path.join(_PKG, "_build", "libnorm.so")
 NRM_OK, NRM_ERR_INVALID_ARG, NRM_ERR_UNSUPPORTED, NRM_ERR_WORKSPACE, NRM_ERR_CUDA, NRM_ERR_TIMEOUT = range(6)
 NRM_F32, NRM_F16, NRM_BF16 = 0, 1, 2
 NRM_ACT_NONE, NRM_ACT_RELU, NRM_ACT_GELU, NRM_ACT_SILU, NRM_ACT_MISH = 0, 1, 2, 3, 4
-NRM_OP_LAYERNORM_BWD, NRM_OP_RMSNORM_BWD = 1, 2
+NRM_OP_LAYERNORM_BWD, NRM_OP_RMSNORM_BWD, NRM_OP_LAYERNORM_CF_BWD = 1, 2, 3
 
 ACTS = {"none": NRM_ACT_NONE, "relu": NRM_ACT_RELU, "gelu": NRM_ACT_GELU, "silu": NRM_ACT_SILU,
         "mish": NRM_ACT_MISH}
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("nrm_layernorm_fwd", "nrm_layernorm_bwd", "nrm_layernorm_bwd_noalloc",
+           "nrm_layernorm_cf_fwd", "nrm_layernorm_cf_bwd",
            "nrm_rmsnorm_fwd", "nrm_rmsnorm_bwd",
            "nrm_batchnorm_fwd", "nrm_batchnorm_bwd", "nrm_workspace_bytes",
            "nrm_batchnorm_workspace_bytes",
@@ -59,6 +60,9 @@ def load(path: str | None = None):
         "nrm_layernorm_fwd": [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P],
         "nrm_layernorm_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, ctypes.c_size_t, _P],
         "nrm_layernorm_bwd_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P],
+        "nrm_layernorm_cf_fwd": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _I, _P],
+        "nrm_layernorm_cf_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _P, ctypes.c_size_t,
+                                 _P],
         "nrm_rmsnorm_fwd": [_P, _P, _P, _P, _I64, _I64, _F, _I, _P],
         "nrm_rmsnorm_bwd": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, ctypes.c_size_t, _P],
         "nrm_batchnorm_fwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, _I,
@@ -146,6 +150,24 @@ def nrm_layernorm_bwd(dy, x, w, mean, rstd, dx, dw, db, workspace, stream=None):
            "nrm_layernorm_bwd")
 
 
+def nrm_layernorm_cf_fwd(x, w, b, y, mean, rstd, eps, stream=None):
+    """LayerNorm over the channels of x[n, c, *spatial]; mean, rstd hold n * prod(spatial)
+    floats (or are None)."""
+    n, c, l = _ncl(x)
+    _check(load().nrm_layernorm_cf_fwd(_ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(mean), _ptr(rstd),
+                                       n, c, l, eps, _dtype_code(x), _stream(stream)),
+           "nrm_layernorm_cf_fwd")
+
+
+def nrm_layernorm_cf_bwd(dy, x, w, mean, rstd, dx, dw, db, workspace, stream=None):
+    n, c, l = _ncl(x)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().nrm_layernorm_cf_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(mean), _ptr(rstd), _ptr(dx),
+                                       _ptr(dw), _ptr(db), n, c, l, _dtype_code(x), _ptr(workspace),
+                                       ws_bytes, _stream(stream)),
+           "nrm_layernorm_cf_bwd")
+
+
 def nrm_layernorm_bwd_noalloc(dy, x, w, mean, rstd, dx, dw, db, stream=None):
     """LayerNorm backward for callers that cannot allocate: no workspace; the
     library's static device scratch holds the dw/db partial rows."""
@@ -174,7 +196,7 @@ def nrm_rmsnorm_bwd(dy, x, w, rstd, dx, dw, workspace, stream=None):
 
 def _ncl(x):
     if x.dim() < 2:
-        raise ValueError("BatchNorm input needs at least [n, c]")
+        raise ValueError("input needs at least [n, c] (NCHW-like, channels second)")
     n, c = x.shape[0], x.shape[1]
     l = 1
     for s in x.shape[2:]:

@@ -289,6 +289,15 @@ nrm_status row_bwd_common(bool ln, const void* dy, const void* x, const void* w,
     return by_dtype(dt, [&](auto tag) { return row_bwd<decltype(tag)>(a, ln, vec, s); });
 }
 
+nrm_status check_cf_shape(int64_t n, int64_t c, int64_t l, nrm_dtype dt) {
+    if (!dtype_ok(dt)) return fail(NRM_ERR_INVALID_ARG, "unknown dtype %d", int(dt));
+    if (n < 0 || l < 0) return fail(NRM_ERR_INVALID_ARG, "n and l must be >= 0");
+    if (c < 1) return fail(NRM_ERR_INVALID_ARG, "c must be >= 1");
+    if (c > kCfMaxChannels) return fail(NRM_ERR_UNSUPPORTED, "c must be <= %d", kCfMaxChannels);
+    if (!size_ok(n, c, l)) return fail(NRM_ERR_UNSUPPORTED, "n*c*l must be < 2^40");
+    return NRM_OK;
+}
+
 nrm_status check_bn_shape(int64_t n, int64_t c, int64_t l, nrm_dtype dt, int training, nrm_act act) {
     if (!dtype_ok(dt)) return fail(NRM_ERR_INVALID_ARG, "unknown dtype %d", int(dt));
     if (n < 0 || c < 0 || l < 0) return fail(NRM_ERR_INVALID_ARG, "n, c, l must be >= 0");
@@ -320,6 +329,79 @@ nrm_status nrm_layernorm_bwd(const void* dy, const void* x, const void* w, const
                              nrm_stream_t stream) {
     return row_bwd_common(true, dy, x, w, mean, rstd, dx, dw, db, rows, cols, dt, workspace,
                           workspace_bytes, stream);
+}
+
+nrm_status nrm_layernorm_cf_fwd(const void* x, const void* w, const void* b, void* y, float* mean,
+                                float* rstd, int64_t n, int64_t c, int64_t l, float eps, nrm_dtype dt,
+                                nrm_stream_t stream) {
+    t_msg[0] = 0;
+    nrm_status st = check_cf_shape(n, c, l, dt);
+    if (st != NRM_OK) return st;
+    if ((st = check_eps(eps)) != NRM_OK) return st;
+    const bool has_data = n > 0 && l > 0;
+    if (has_data && (!x || !y)) return fail(NRM_ERR_INVALID_ARG, "x and y must not be NULL");
+    const size_t es = dsize(dt);
+    if (!all_aligned({x, y, w, b}, es) || !all_aligned({mean, rstd}, 4))
+        return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    if (has_data && x == y) return fail(NRM_ERR_INVALID_ARG, "in-place (y == x) is not supported");
+    CfArgs a{};
+    a.x = x;
+    a.w = w;
+    a.b = b;
+    a.y = y;
+    a.mean = mean;
+    a.rstd = rstd;
+    a.n = n;
+    a.c = c;
+    a.l = l;
+    a.eps = eps;
+    const bool vec = (size_t(l) * es) % 16 == 0 && all_aligned({x, y}, 16);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return by_dtype(dt, [&](auto tag) { return cf_fwd<decltype(tag)>(a, vec, s); });
+}
+
+nrm_status nrm_layernorm_cf_bwd(const void* dy, const void* x, const void* w, const float* mean,
+                                const float* rstd, void* dx, void* dw, void* db, int64_t n, int64_t c,
+                                int64_t l, nrm_dtype dt, void* workspace, size_t workspace_bytes,
+                                nrm_stream_t stream) {
+    t_msg[0] = 0;
+    nrm_status st = check_cf_shape(n, c, l, dt);
+    if (st != NRM_OK) return st;
+    const bool has_data = n > 0 && l > 0;
+    if (has_data && (!dy || !x || !dx || !mean || !rstd))
+        return fail(NRM_ERR_INVALID_ARG, "dy, x, dx and the saved statistics must not be NULL");
+    const size_t es = dsize(dt);
+    if (!all_aligned({dy, x, dx, w, dw, db}, es) || !all_aligned({mean, rstd}, 4))
+        return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    if (has_data && (dx == dy || dx == x))
+        return fail(NRM_ERR_INVALID_ARG, "in-place (dx == dy or x) is not supported");
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    CfArgs a{};
+    if ((dw || db) && has_data) {
+        const size_t need = row_ws_bytes(true, c);
+        if (!workspace || !aligned(workspace, 16))
+            return fail(NRM_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned");
+        if (workspace_bytes < need)
+            return fail(NRM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                        workspace_bytes, need);
+        a.ws_dw = reinterpret_cast<float*>(workspace);
+        a.ws_db = a.ws_dw + size_t(row_bwd_max_partials(*d)) * size_t(c);
+    }
+    a.x = x;
+    a.w = w;
+    a.dy = dy;
+    a.dx = dx;
+    a.mean_in = mean;
+    a.rstd_in = rstd;
+    a.dw = dw;
+    a.db = db;
+    a.n = n;
+    a.c = c;
+    a.l = l;
+    const bool vec = (size_t(l) * es) % 16 == 0 && all_aligned({dy, x, dx}, 16);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return by_dtype(dt, [&](auto tag) { return cf_bwd<decltype(tag)>(a, vec, s); });
 }
 
 nrm_status nrm_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows,
@@ -434,9 +516,10 @@ nrm_status nrm_batchnorm_bwd(const void* dy, const void* x, const void* residual
 }
 
 size_t nrm_workspace_bytes(nrm_op op, int64_t rows, int64_t cols, nrm_dtype dt) {
-    if (op != NRM_OP_LAYERNORM_BWD && op != NRM_OP_RMSNORM_BWD) return 0;
+    if (op != NRM_OP_LAYERNORM_BWD && op != NRM_OP_RMSNORM_BWD && op != NRM_OP_LAYERNORM_CF_BWD) return 0;
     if (check_rows(rows, cols, dt) != NRM_OK) return 0;
-    return row_ws_bytes(op == NRM_OP_LAYERNORM_BWD, cols);
+    if (op == NRM_OP_LAYERNORM_CF_BWD && cols > kCfMaxChannels) return 0;
+    return row_ws_bytes(op != NRM_OP_RMSNORM_BWD, cols);
 }
 
 size_t nrm_batchnorm_workspace_bytes(int64_t n, int64_t c, int64_t l, nrm_dtype dt) {

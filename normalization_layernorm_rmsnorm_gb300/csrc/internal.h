@@ -74,6 +74,31 @@ struct RowArgs {
     unsigned int* err;    // device error word (set by the launcher; bounded waits that gave up)
 };
 
+// LayerNorm over the channels of x[n, c, l] (channels first, l = H*W).
+// The backward keeps a CTA's dw/db partial row (2*c floats) in shared memory.
+constexpr int64_t kCfMaxChannels = 16384;
+struct CfArgs {
+    const void* x;
+    const void* w;        // [c] in the storage dtype (nullable)
+    const void* b;
+    const void* dy;
+    void* y;
+    void* dx;
+    float* mean;          // forward outputs [n*l] (nullable)
+    float* rstd;
+    const float* mean_in; // backward inputs [n*l]
+    const float* rstd_in;
+    float* ws_dw;         // backward: per-CTA partial rows [P][c] (nullable)
+    float* ws_db;
+    void* dw;             // backward outputs [c] in the storage dtype (nullable)
+    void* db;
+    int64_t n, c, l;
+    float eps;
+};
+
+template <typename T> nrm_status cf_fwd(const CfArgs& a, bool vec, cudaStream_t s);
+template <typename T> nrm_status cf_bwd(CfArgs a, bool vec, cudaStream_t s);
+
 // Upper bound of per-CTA partial rows of the row-norm backward (P).
 int row_bwd_max_partials(const DevInfo& d);
 

@@ -595,6 +595,7 @@ constexpr uint64_t kRowWaitLimitNs = 2000000000ull;  // 2 s
 }  // namespace nrm
 
 #include "rowring.cuh"
+#include "layernorm_cf.cuh"
 
 namespace nrm {
 
@@ -770,8 +771,75 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
                       cargs, s);
 }
 
+template <typename T>
+nrm_status cf_fwd(const CfArgs& a, bool vec, cudaStream_t s) {
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    if (a.n == 0 || a.l == 0) return NRM_OK;
+    const void* fn = vec ? (const void*)&lncf_fwd_kernel<T, kVec<T>> : (const void*)&lncf_fwd_kernel<T, 1>;
+    const int pw = 32 * (vec ? kVec<T> : 1);
+    const int64_t tiles = a.n * ((a.l + pw - 1) / pw);
+    const int occ = cached_occupancy(fn, kCfThreads, 0);
+    if (occ <= 0) return fail(NRM_ERR_CUDA, "channels-first LayerNorm forward cannot be resident");
+    const int64_t cap = int64_t(occ) * d->sms;
+    const int grid = int(tiles < cap ? tiles : cap);
+    CfArgs args = a;
+    void* kargs[] = {&args};
+    return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(kCfThreads), kargs, 0, s),
+                       "channels-first LayerNorm forward launch");
+}
+
+template <typename T>
+nrm_status cf_bwd(CfArgs a, bool vec, cudaStream_t s) {
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    const bool want = a.dw || a.db;
+    if (!want) a.ws_dw = a.ws_db = nullptr;
+    if (a.n == 0 || a.l == 0) {
+        if (!want) return NRM_OK;
+        // no positions: dw = db = 0 (the column sum over zero partial rows)
+        const float* none = nullptr;
+        int P0 = 0;
+        int cols = int(a.c);
+        T* dw = reinterpret_cast<T*>(a.dw);
+        T* db = reinterpret_cast<T*>(a.db);
+        void* cargs[] = {&none, &none, &P0, &cols, &dw, &db};
+        return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((cols + 31) / 32, 2),
+                          dim3(kColsumWarps * 32), cargs, s);
+    }
+    const void* fn = vec ? (const void*)&lncf_bwd_kernel<T, kVec<T>> : (const void*)&lncf_bwd_kernel<T, 1>;
+    const int pw = 32 * (vec ? kVec<T> : 1);
+    const int64_t tiles = a.n * ((a.l + pw - 1) / pw);
+    // the CTA's dw, db partial row
+    const size_t smem = size_t(a.c) * 2 * sizeof(float);
+    nrm_status st = prepare_kernel(fn, smem, false);
+    if (st != NRM_OK) return st;
+    const int occ = cached_occupancy(fn, kCfThreads, smem);
+    if (occ <= 0) return fail(NRM_ERR_CUDA, "channels-first LayerNorm backward cannot be resident");
+    int64_t p = int64_t(occ) * d->sms;
+    if (p > row_bwd_max_partials(*d)) p = row_bwd_max_partials(*d);
+    if (tiles < p) p = tiles;
+    const int P = int(p);
+    CfArgs args = a;
+    void* kargs[] = {&args};
+    st = cuda_status(cudaLaunchKernel(fn, dim3(P), dim3(kCfThreads), kargs, smem, s),
+                     "channels-first LayerNorm backward launch");
+    if (st != NRM_OK || !want) return st;
+    const float* wsw = a.ws_dw;
+    const float* wsb = a.ws_db;
+    int P_ = P;
+    int cols = int(a.c);
+    T* dw = reinterpret_cast<T*>(a.dw);
+    T* db = reinterpret_cast<T*>(a.db);
+    void* cargs[] = {&wsw, &wsb, &P_, &cols, &dw, &db};
+    return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((cols + 31) / 32, 2), dim3(kColsumWarps * 32),
+                      cargs, s);
+}
+
 }  // namespace nrm
 
 #define NRM_INSTANTIATE_ROWNORM(T)                                                      \
     template nrm_status nrm::row_fwd<T>(const nrm::RowArgs&, bool, bool, cudaStream_t); \
-    template nrm_status nrm::row_bwd<T>(nrm::RowArgs, bool, bool, cudaStream_t);
+    template nrm_status nrm::row_bwd<T>(nrm::RowArgs, bool, bool, cudaStream_t);        \
+    template nrm_status nrm::cf_fwd<T>(const nrm::CfArgs&, bool, cudaStream_t);         \
+    template nrm_status nrm::cf_bwd<T>(nrm::CfArgs, bool, cudaStream_t);

@@ -56,6 +56,25 @@ def build_calls(dev, names=None):
     return calls
 
 
+# Workloads of the operations built beyond the step, timed beside it (not part
+# of the step's bytes or time): LayerNorm over the channels of an NCHW tensor,
+# as in ConvNeXt-T's stem and first downsampling layer (96 channels of 56x56).
+EXTRA = ("ln_cf_f16_128x96x56x56",)
+
+
+def build_extra_calls(dev, names=None):
+    import torch
+
+    calls = []
+
+    def f32(n):
+        return torch.empty(n, dtype=torch.float32, device=dev)
+
+    if names is None or EXTRA[0] in names:
+        calls += _ln_cf(EXTRA[0], 128, 96, 56 * 56, dev, f32)
+    return calls
+
+
 def _rms(cfg, dev, f32):
     import torch
 
@@ -164,3 +183,25 @@ def _bn_gelu(cfg, dev, f32):
                       nbytes(gdy, gx, gw, gb, gsm, gsr, gdx, gdw, gdb), 1,
                       [gdy], [gdx, gdw, gdb]))
     return calls
+
+
+def _ln_cf(name, n, c, l, dev, f32):
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    seed = 31
+    x = synth.random_tensor(seed, 1, (n, c, l), "f16", mean=0.3, std=1.5).torch(dev)
+    dy = synth.random_tensor(seed, 2, (n, c, l), "f16").torch(dev)
+    w = synth.store(1 + 0.1 * synth.normal(seed, 3, c), "f16", (c,)).torch(dev)
+    b = synth.store(0.1 * synth.normal(seed, 4, c), "f16", (c,)).torch(dev)
+    y, dx = x.new_empty(x.shape), x.new_empty(x.shape)
+    dw, db = w.new_empty(c), w.new_empty(c)
+    mean, rstd = f32(n * l), f32(n * l)
+    ws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_CF_BWD, n * l, c, nrm.NRM_F16) // 4)
+    return [
+        Call(name, "fwd", "lncf_fwd_kernel<f16>",
+             lambda: nrm.nrm_layernorm_cf_fwd(x, w, b, y, mean, rstd, 1e-6),
+             nbytes(x, w, b, y, mean, rstd), 1, [x, w, b], [y, mean, rstd]),
+        Call(name, "bwd", "lncf_bwd_kernel<f16>+colsum",
+             lambda: nrm.nrm_layernorm_cf_bwd(dy, x, w, mean, rstd, dx, dw, db, ws),
+             nbytes(dy, x, w, mean, rstd, dx, dw, db), 2, [dy], [dx, dw, db]),
+    ]
