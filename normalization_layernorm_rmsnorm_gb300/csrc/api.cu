@@ -169,6 +169,41 @@ nrm_status launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, cudaSt
 
 int row_bwd_max_partials(const DevInfo& d) { return 4 * d.sms; }
 
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+}  // namespace
+
+nrm_status encode_ncl_map(CUtensorMap* map, const void* base, size_t es, int64_t n, int64_t c, int64_t l,
+                          int box_l, int box_c) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return fail(NRM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[3] = {cuuint64_t(l), cuuint64_t(c), cuuint64_t(n)};
+    const cuuint64_t strides[2] = {cuuint64_t(l) * es, cuuint64_t(c) * cuuint64_t(l) * es};
+    const cuuint32_t box[3] = {cuuint32_t(box_l), cuuint32_t(box_c), 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUtensorMapDataType dt = es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    const CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(NRM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+    return NRM_OK;
+}
+
 }  // namespace nrm
 
 using namespace nrm;

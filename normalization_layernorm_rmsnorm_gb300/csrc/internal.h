@@ -2,6 +2,7 @@
 // per-dtype kernel translation units.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap and its enums (types only; the driver is reached through the runtime)
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -94,7 +95,14 @@ struct CfArgs {
     void* db;
     int64_t n, c, l;
     float eps;
+    unsigned int* err;    // device error word (bounded waits that gave up)
 };
+
+// A 3-D tiled TMA map of a [n, c, l] tensor of es-byte elements (dims {l, c, n},
+// box {box_l, box_c, 1}, out-of-range elements read as zero).  The base must be
+// 16-byte aligned and l*es a multiple of 16.
+nrm_status encode_ncl_map(CUtensorMap* map, const void* base, size_t es, int64_t n, int64_t c, int64_t l,
+                          int box_l, int box_c);
 
 template <typename T> nrm_status cf_fwd(const CfArgs& a, bool vec, cudaStream_t s);
 template <typename T> nrm_status cf_bwd(CfArgs a, bool vec, cudaStream_t s);

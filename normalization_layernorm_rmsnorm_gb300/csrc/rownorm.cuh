@@ -596,6 +596,7 @@ constexpr uint64_t kRowWaitLimitNs = 2000000000ull;  // 2 s
 
 #include "rowring.cuh"
 #include "layernorm_cf.cuh"
+#include "layernorm_cf_ring.cuh"
 
 namespace nrm {
 
@@ -771,11 +772,75 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
                       cargs, s);
 }
 
+// Plan of a channels-first ring kernel: positions per tile (the widest of 32,
+// 16, 8 vectors per channel row that the plane needs and that leaves at least
+// four slots, else three, else two), channel boxes of at most 256 rows, and
+// the shared-memory layout.  False when a tile does not fit (the register kernel runs instead).
+inline bool cfr_plan(CfrGeom& g, size_t& smem, const CfArgs& a, size_t es, bool bwd) {
+    const DevInfo* d = dev_info();
+    if (!d || a.n <= 0 || a.l <= 0 || a.c > 4096) return false;
+    if (a.l >= (int64_t(1) << 31) || a.n >= (int64_t(1) << 31)) return false;
+    const int V = int(16 / es);
+    const auto r128 = [](size_t b) { return (b + 127) / 128 * 128; };
+    const size_t param = r128(size_t(a.c) * 4 * (bwd ? 1 : 2));
+    const size_t acc = bwd ? r128(size_t(a.c) * 4 * 2 * kCfrTeams) : 0;
+    const size_t cap = size_t(d->max_smem_optin) - 1024;  // room for the static shared memory
+    const int nb = int((a.c + 255) / 256);
+    const int cb = int((a.c + nb - 1) / nb);
+    int pv = 8;
+    while (pv < 32 && int64_t(pv) * V < a.l) pv *= 2;
+    bool found = false;
+    // two tiles are being consumed at a time (one per team): four slots keep two loading
+    for (int want = 4; want >= 2 && !found; --want) {
+        for (int p = pv; p >= 8; p /= 2) {
+            const int P = p * V;
+            const size_t part = r128((size_t(kCfrTeams) * kCfrTeamFloatsPerPos * P + 2 * kCfrTeamWarps) * 4);
+            const size_t tensor = size_t(nb) * cb * P * es;
+            const size_t slot = r128(tensor * (bwd ? 2 : 1) + (bwd ? size_t(2) * P * 4 : 0));
+            if (param + part + acc >= cap) continue;
+            const size_t n_slots = (cap - param - part - acc) / slot;
+            if (n_slots < size_t(want)) continue;
+            g.pv = p;
+            g.P = P;
+            g.cb = cb;
+            g.nb = nb;
+            g.slots = int(n_slots < size_t(kCfrMaxSlots) ? n_slots : size_t(kCfrMaxSlots));
+            g.slot_bytes = uint32_t(slot);
+            g.tx_tensor = uint32_t(tensor);
+            g.param_bytes = uint32_t(param);
+            g.part_bytes = uint32_t(part);
+            g.acc_bytes = uint32_t(acc);
+            smem = param + part + acc + size_t(g.slots) * slot;
+            found = true;
+            break;
+        }
+    }
+    if (!found) return false;
+    g.tps = (a.l + g.P - 1) / g.P;
+    g.tiles = a.n * g.tps;
+    return true;
+}
+
 template <typename T>
 nrm_status cf_fwd(const CfArgs& a, bool vec, cudaStream_t s) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     if (a.n == 0 || a.l == 0) return NRM_OK;
+    CfrGeom g{};
+    size_t smem = 0;
+    if (vec && cfr_plan(g, smem, a, sizeof(T), false)) {
+        alignas(64) CUtensorMap map_x;
+        nrm_status st = encode_ncl_map(&map_x, a.x, sizeof(T), a.n, a.c, a.l, g.P, g.cb);
+        if (st != NRM_OK) return st;
+        const void* fn = (const void*)&lncf_fwd_ring_kernel<T>;
+        if ((st = prepare_kernel(fn, smem, false)) != NRM_OK) return st;
+        CfArgs args = a;
+        args.err = d->err;
+        const int grid = int(g.tiles < d->sms ? g.tiles : d->sms);
+        void* kargs[] = {&args, &g, &map_x};
+        return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(kCfrThreads), kargs, smem, s),
+                           "channels-first LayerNorm forward launch");
+    }
     const void* fn = vec ? (const void*)&lncf_fwd_kernel<T, kVec<T>> : (const void*)&lncf_fwd_kernel<T, 1>;
     const int pw = 32 * (vec ? kVec<T> : 1);
     const int64_t tiles = a.n * ((a.l + pw - 1) / pw);
@@ -804,6 +869,34 @@ nrm_status cf_bwd(CfArgs a, bool vec, cudaStream_t s) {
         T* dw = reinterpret_cast<T*>(a.dw);
         T* db = reinterpret_cast<T*>(a.db);
         void* cargs[] = {&none, &none, &P0, &cols, &dw, &db};
+        return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((cols + 31) / 32, 2),
+                          dim3(kColsumWarps * 32), cargs, s);
+    }
+    CfrGeom g{};
+    size_t rsmem = 0;
+    const bool stats16 = ((reinterpret_cast<uintptr_t>(a.mean_in) | reinterpret_cast<uintptr_t>(a.rstd_in)) & 15) == 0;
+    if (vec && stats16 && cfr_plan(g, rsmem, a, sizeof(T), true)) {
+        alignas(64) CUtensorMap map_dy;
+        alignas(64) CUtensorMap map_x;
+        nrm_status st = encode_ncl_map(&map_dy, a.dy, sizeof(T), a.n, a.c, a.l, g.P, g.cb);
+        if (st == NRM_OK) st = encode_ncl_map(&map_x, a.x, sizeof(T), a.n, a.c, a.l, g.P, g.cb);
+        if (st != NRM_OK) return st;
+        const void* fn = (const void*)&lncf_bwd_ring_kernel<T>;
+        if ((st = prepare_kernel(fn, rsmem, false)) != NRM_OK) return st;
+        CfArgs args = a;
+        args.err = d->err;
+        const int grid = int(g.tiles < d->sms ? g.tiles : d->sms);
+        void* kargs[] = {&args, &g, &map_dy, &map_x};
+        st = cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(kCfrThreads), kargs, rsmem, s),
+                         "channels-first LayerNorm backward launch");
+        if (st != NRM_OK || !want) return st;
+        const float* wsw = a.ws_dw;
+        const float* wsb = a.ws_db;
+        int P_ = grid;
+        int cols = int(a.c);
+        T* dw = reinterpret_cast<T*>(a.dw);
+        T* db = reinterpret_cast<T*>(a.db);
+        void* cargs[] = {&wsw, &wsb, &P_, &cols, &dw, &db};
         return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((cols + 31) / 32, 2),
                           dim3(kColsumWarps * 32), cargs, s);
     }

@@ -25,7 +25,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     nrm.load()
     dev = torch.device("cuda", 0)
-    calls = workloads.build_calls(dev, set(args.workload))
+    names = set(args.workload)
+    calls = workloads.build_calls(dev, names) + workloads.build_extra_calls(dev, names)
     if not calls:
         ap.error(f"no such workload: {args.workload}")
     for _ in range(args.repeat):

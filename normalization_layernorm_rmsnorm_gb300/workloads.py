@@ -198,10 +198,10 @@ def _ln_cf(name, n, c, l, dev, f32):
     mean, rstd = f32(n * l), f32(n * l)
     ws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_CF_BWD, n * l, c, nrm.NRM_F16) // 4)
     return [
-        Call(name, "fwd", "lncf_fwd_kernel<f16>",
+        Call(name, "fwd", "lncf_fwd_ring_kernel<f16>",
              lambda: nrm.nrm_layernorm_cf_fwd(x, w, b, y, mean, rstd, 1e-6),
              nbytes(x, w, b, y, mean, rstd), 1, [x, w, b], [y, mean, rstd]),
-        Call(name, "bwd", "lncf_bwd_kernel<f16>+colsum",
+        Call(name, "bwd", "lncf_bwd_ring_kernel<f16>+colsum",
              lambda: nrm.nrm_layernorm_cf_bwd(dy, x, w, mean, rstd, dx, dw, db, ws),
              nbytes(dy, x, w, mean, rstd, dx, dw, db), 2, [dy], [dx, dw, db]),
     ]

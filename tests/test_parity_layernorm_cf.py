@@ -29,14 +29,15 @@ def _inputs(n, c, l, dtype, seed, affine=True):
     return x, dy, w, b
 
 
-def _run(x, dy, w, b, dtype, eps):
+def _run(x, dy, w, b, dtype, eps, stat_offset=0):
     n, c, l = x.shape
     xt, dyt = x.torch("cuda"), dy.torch("cuda")
     wt = w.torch("cuda") if w is not None else None
     bt = b.torch("cuda") if b is not None else None
     y = empty((n, c, l), dtype)
-    mean = torch.empty((n, l), device="cuda")
-    rstd = torch.empty((n, l), device="cuda")
+    # stat_offset floats in: saved statistics that are not 16-byte aligned
+    mean = torch.empty(n * l + stat_offset, device="cuda")[stat_offset:].view(n, l)
+    rstd = torch.empty(n * l + stat_offset, device="cuda")[stat_offset:].view(n, l)
     nrm.nrm_layernorm_cf_fwd(xt, wt, bt, y, mean, rstd, eps)
     dx = empty((n, c, l), dtype)
     dw = empty((c,), dtype)
@@ -47,8 +48,8 @@ def _run(x, dy, w, b, dtype, eps):
     return {k: host(v) for k, v in dict(y=y, mean=mean, rstd=rstd, dx=dx, dw=dw, db=db).items()}
 
 
-def _check(orc, x, dy, w, b, dtype, eps, tag):
-    got = _run(x, dy, w, b, dtype, eps)
+def _check(orc, x, dy, w, b, dtype, eps, tag, stat_offset=0):
+    got = _run(x, dy, w, b, dtype, eps, stat_offset)
     wf = w.f64() if w is not None else None
     bf = b.f64() if b is not None else None
     y, mean, rstd = orc.layernorm_cf_fwd(x.f64(), wf, bf, eps=eps)
@@ -70,6 +71,9 @@ CASES = [
     ("f32", 3, 5, 33),       # scalar, few channels, ragged tile
     ("bf16", 2, 384, 196),   # 392-byte planes (not a multiple of 16): the scalar path
     ("f16", 1, 3, 8),        # one tile, three channels
+    ("f16", 3, 257, 200),    # two channel boxes (the second one past c), positions past l
+    ("bf16", 2, 1024, 64),   # too many channels for a shared-memory tile: the register kernel
+    ("f32", 5, 300, 36),     # 144-byte planes, two boxes of 150 channels
 ]
 
 
@@ -83,6 +87,12 @@ def test_layernorm_cf(orc, case):
 def test_layernorm_cf_without_affine(orc):
     x, dy, _, _ = _inputs(2, 64, 1024, "f32", seed=11, affine=False)
     _check(orc, x, dy, None, None, "f32", 1e-5, "cf no affine")
+
+
+def test_layernorm_cf_unaligned_saved_statistics(orc):
+    # saved mean/rstd 4-byte but not 16-byte aligned: the backward cannot bulk-copy them
+    x, dy, w, b = _inputs(4, 96, 784, "f16", seed=13)
+    _check(orc, x, dy, w, b, "f16", 1e-6, "cf unaligned stats", stat_offset=1)
 
 
 def test_layernorm_cf_many_tiles_per_cta(orc):
