@@ -27,7 +27,7 @@ constexpr int kCfrTeamThreads = kCfrTeamWarps * 32;
 constexpr int kCfrConsumerWarps = kCfrTeams * kCfrTeamWarps;
 constexpr int kCfrConsumers = kCfrConsumerWarps * 32;
 constexpr int kCfrThreads = kCfrConsumers + 32;  // + the producer warp
-constexpr int kCfrMaxSlots = 8;
+constexpr int kCfrMaxSlots = 8;                   // the slot count is even (see cfr_plan)
 constexpr int kCfrBarTeam = 1;                    // named barriers 1, 2: one per team
 constexpr int kCfrBarAll = 3;                     // named barrier over all consumer warps
 // floats of a team's shared scratch per tile position: per-warp partials
@@ -62,13 +62,58 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-template <typename T>
-__device__ __forceinline__ void cfr_unpack(const unsigned char* p, float (&v)[kVec<T>]) {
-    Pack<T, kVec<T>> pk;
-    pk.u = *reinterpret_cast<const uint4*>(p);
-#pragma unroll
-    for (int k = 0; k < kVec<T>; ++k) v[k] = Io<T>::load(pk.b[k]);
+// The element loops work on pairs of fp32 values with Blackwell's packed FP32
+// instructions (add/mul/fma.rn.f32x2): two elements per instruction, each
+// rounded as the scalar instruction would.
+template <typename T> constexpr int kPairs = kVec<T> / 2;
+
+template <typename T> __device__ __forceinline__ float2 cfr_cvt2(uint32_t w);
+template <> __device__ __forceinline__ float2 cfr_cvt2<__half>(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
+template <> __device__ __forceinline__ float2 cfr_cvt2<__nv_bfloat16>(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+template <typename T> __device__ __forceinline__ uint32_t cfr_pack2(float2 v);
+template <> __device__ __forceinline__ uint32_t cfr_pack2<__half>(float2 v) {
+    const __half2 h = __float22half2_rn(v);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <> __device__ __forceinline__ uint32_t cfr_pack2<__nv_bfloat16>(float2 v) {
+    const __nv_bfloat162 h = __float22bfloat162_rn(v);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 16 bytes of shared memory as fp32 pairs.
+template <typename T>
+__device__ __forceinline__ void cfr_load2(const unsigned char* p, float2 (&v)[kPairs<T>]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    if constexpr (sizeof(T) == 4) {
+        v[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+        v[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+    } else {
+        v[0] = cfr_cvt2<T>(u.x);
+        v[1] = cfr_cvt2<T>(u.y);
+        v[2] = cfr_cvt2<T>(u.z);
+        v[3] = cfr_cvt2<T>(u.w);
+    }
+}
+
+// fp32 pairs rounded to T and stored as one 16-byte global store.
+template <typename T>
+__device__ __forceinline__ void cfr_store2(T* p, const float2 (&o)[kPairs<T>]) {
+    uint4 u;
+    if constexpr (sizeof(T) == 4) {
+        u = make_uint4(__float_as_uint(o[0].x), __float_as_uint(o[0].y), __float_as_uint(o[1].x),
+                       __float_as_uint(o[1].y));
+    } else {
+        u = make_uint4(cfr_pack2<T>(o[0]), cfr_pack2<T>(o[1]), cfr_pack2<T>(o[2]), cfr_pack2<T>(o[3]));
+    }
+    st_v4(p, u);
+}
+
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 f2neg(float2 v) { return make_float2(-v.x, -v.y); }
 
 // Producer (whole warp, lane 0 issues): the CTA's tiles into the ring, in
 // order.  `map_a` is x (forward) or dy (backward); `map_b` is x (backward).
@@ -192,7 +237,7 @@ lncf_fwd_ring_kernel(const CfArgs a, const CfrGeom g, const __grid_constant__ CU
         for (int q = team; q < nq; q += kCfrTeams) {
             const int64_t tt = blockIdx.x + int64_t(q) * gridDim.x;
             const int slot = q % g.slots;
-            if (!mbar_wait_bounded(&full[slot], uint32_t(q / g.slots) & 1u, kRowWaitLimitNs)) bad = true;
+            if (!mbar_wait_bounded_sleep(&full[slot], uint32_t(q / g.slots) & 1u, kRowWaitLimitNs)) bad = true;
             const int64_t i = tt / g.tps;
             const int p0 = int((tt - i * g.tps) * P);
             const bool on = p0 + pv * V < a.l;  // V divides l: a vector is all in or all out
@@ -200,29 +245,37 @@ lncf_fwd_ring_kernel(const CfArgs a, const CfrGeom g, const __grid_constant__ CU
             float* st = stat + ((q / kCfrTeams) & 1) * 2 * P;
             // ---- pass 1: (count, mean, M2) of the group's channels per position,
             // from sums shifted by the group's first channel ----
+            constexpr int H = kPairs<T>;
             float mean[V], m2[V];
 #pragma unroll
             for (int k = 0; k < V; ++k) mean[k] = m2[k] = 0.f;
             if (on && my_ch > 0) {
-                float kk[V], s[V], sq[V];
-                cfr_unpack<T>(base + size_t(grp) * row, kk);
+                float2 kk[H], nk[H], s[H], sq[H];
+                cfr_load2<T>(base + size_t(grp) * row, kk);
 #pragma unroll
-                for (int k = 0; k < V; ++k) s[k] = sq[k] = 0.f;
-                for (int j = 1; j < my_ch; ++j) {
-                    float v[V];
-                    cfr_unpack<T>(base + size_t(grp + j * CG) * row, v);
+                for (int h = 0; h < H; ++h) {
+                    nk[h] = f2neg(kk[h]);
+                    s[h] = sq[h] = f2(0.f);
+                }
+                const unsigned char* pch = base + size_t(grp + CG) * row;
+                const size_t step = size_t(CG) * row;
+                for (int j = 1; j < my_ch; ++j, pch += step) {
+                    float2 v[H];
+                    cfr_load2<T>(pch, v);
 #pragma unroll
-                    for (int k = 0; k < V; ++k) {
-                        const float d = v[k] - kk[k];
-                        s[k] += d;
-                        sq[k] = fmaf(d, d, sq[k]);
+                    for (int h = 0; h < H; ++h) {
+                        const float2 d = __fadd2_rn(v[h], nk[h]);
+                        s[h] = __fadd2_rn(s[h], d);
+                        sq[h] = __ffma2_rn(d, d, sq[h]);
                     }
                 }
                 const float rc = 1.f / float(my_ch);
 #pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    mean[k] = fmaf(s[k], rc, kk[k]);
-                    m2[k] = fmaxf(fmaf(-s[k], s[k] * rc, sq[k]), 0.f);
+                for (int h = 0; h < H; ++h) {
+                    mean[2 * h] = fmaf(s[h].x, rc, kk[h].x);
+                    mean[2 * h + 1] = fmaf(s[h].y, rc, kk[h].y);
+                    m2[2 * h] = fmaxf(fmaf(-s[h].x, s[h].x * rc, sq[h].x), 0.f);
+                    m2[2 * h + 1] = fmaxf(fmaf(-s[h].y, s[h].y * rc, sq[h].y), 0.f);
                 }
             }
             // groups that share a warp (PV < 32) hold the same positions: merge them
@@ -270,21 +323,25 @@ lncf_fwd_ring_kernel(const CfArgs a, const CfrGeom g, const __grid_constant__ CU
             named_barrier(kCfrBarTeam + team, kCfrTeamThreads);
             // ---- pass 2: y = (x - mean) * rstd * w + b ----
             if (on) {
-                float mu[V], rs[V];
+                float2 nmu[H], rs[H];
 #pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    mu[k] = st[k * PV + pv];
-                    rs[k] = st[P + k * PV + pv];
+                for (int h = 0; h < H; ++h) {
+                    nmu[h] = make_float2(-st[(2 * h) * PV + pv], -st[(2 * h + 1) * PV + pv]);
+                    rs[h] = make_float2(st[P + (2 * h) * PV + pv], st[P + (2 * h + 1) * PV + pv]);
                 }
-                T* yb = y + i * a.c * a.l + p0 + pv * V;
-                for (int j = 0; j < my_ch; ++j) {
+                T* yb = y + i * a.c * a.l + p0 + pv * V + int64_t(grp) * a.l;
+                const int64_t ystep = int64_t(CG) * a.l;
+                const unsigned char* pch = base + size_t(grp) * row;
+                const size_t step = size_t(CG) * row;
+                for (int j = 0; j < my_ch; ++j, pch += step, yb += ystep) {
                     const int ch = grp + j * CG;
-                    float v[V], o[V];
-                    cfr_unpack<T>(base + size_t(ch) * row, v);
-                    const float wc = wsm[ch], bc = bsm[ch];
+                    float2 v[H], o[H];
+                    cfr_load2<T>(pch, v);
+                    const float2 wc = f2(wsm[ch]), bc = f2(bsm[ch]);
 #pragma unroll
-                    for (int k = 0; k < V; ++k) o[k] = fmaf((v[k] - mu[k]) * rs[k], wc, bc);
-                    store_vec<T, V>(yb + int64_t(ch) * a.l, o);
+                    for (int h = 0; h < H; ++h)
+                        o[h] = __ffma2_rn(__fmul2_rn(__fadd2_rn(v[h], nmu[h]), rs[h]), wc, bc);
+                    cfr_store2<T>(yb, o);
                 }
             }
             __syncwarp();
@@ -361,51 +418,61 @@ lncf_bwd_ring_kernel(const CfArgs a, const CfrGeom g, const __grid_constant__ CU
         for (int q = team; q < nq; q += kCfrTeams) {
             const int64_t tt = blockIdx.x + int64_t(q) * gridDim.x;
             const int slot = q % g.slots;
-            if (!mbar_wait_bounded(&full[slot], uint32_t(q / g.slots) & 1u, kRowWaitLimitNs)) bad = true;
+            if (!mbar_wait_bounded_sleep(&full[slot], uint32_t(q / g.slots) & 1u, kRowWaitLimitNs)) bad = true;
             const int64_t i = tt / g.tps;
             const int p0 = int((tt - i * g.tps) * P);
             const bool on = p0 + pv * V < a.l;
             const unsigned char* sbase = ring + size_t(slot) * g.slot_bytes;
             const unsigned char* dyb = sbase + size_t(pv) * 16;
-            const unsigned char* xb = dyb + tensor_bytes;
             const float* sst = reinterpret_cast<const float*>(sbase + 2 * tensor_bytes);  // mean [P], rstd [P]
             float* cf = coef + ((q / kCfrTeams) & 1) * 2 * P;
-            float mu[V], rs[V];
+            constexpr int H = kPairs<T>;
+            float2 nmu[H], rs[H];
             if (on) {
-                rr_params<V>(sst + pv * V, mu);
-                rr_params<V>(sst + P + pv * V, rs);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float2 m = *reinterpret_cast<const float2*>(sst + pv * V + 2 * h);
+                    nmu[h] = f2neg(m);
+                    rs[h] = *reinterpret_cast<const float2*>(sst + P + pv * V + 2 * h);
+                }
             }
+            const size_t step = size_t(CG) * row;
             // ---- pass 1: sum g and sum g*xhat over the group's channels, g = dy*w ----
-            float s1[V], s2[V];
+            float2 s1[H], s2[H];
 #pragma unroll
-            for (int k = 0; k < V; ++k) s1[k] = s2[k] = 0.f;
+            for (int h = 0; h < H; ++h) s1[h] = s2[h] = f2(0.f);
             if (on) {
-                for (int j = 0; j < my_ch; ++j) {
+                const unsigned char* pd = dyb + size_t(grp) * row;
+                for (int j = 0; j < my_ch; ++j, pd += step) {
                     const int ch = grp + j * CG;
-                    float dv[V], xv[V];
-                    cfr_unpack<T>(dyb + size_t(ch) * row, dv);
-                    cfr_unpack<T>(xb + size_t(ch) * row, xv);
-                    const float wc = wsm[ch];
+                    float2 dv[H], xv[H];
+                    cfr_load2<T>(pd, dv);
+                    cfr_load2<T>(pd + tensor_bytes, xv);
+                    const float2 wc = f2(wsm[ch]);
 #pragma unroll
-                    for (int k = 0; k < V; ++k) {
-                        const float gg = dv[k] * wc;
-                        s1[k] += gg;
-                        s2[k] = fmaf(gg, (xv[k] - mu[k]) * rs[k], s2[k]);
+                    for (int h = 0; h < H; ++h) {
+                        const float2 gg = __fmul2_rn(dv[h], wc);
+                        s1[h] = __fadd2_rn(s1[h], gg);
+                        s2[h] = __ffma2_rn(gg, __fmul2_rn(__fadd2_rn(xv[h], nmu[h]), rs[h]), s2[h]);
                     }
                 }
             }
             for (int o = PV; o < 32; o <<= 1) {
 #pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    s1[k] += __shfl_xor_sync(0xffffffffu, s1[k], o);
-                    s2[k] += __shfl_xor_sync(0xffffffffu, s2[k], o);
+                for (int h = 0; h < H; ++h) {
+                    s1[h].x += __shfl_xor_sync(0xffffffffu, s1[h].x, o);
+                    s1[h].y += __shfl_xor_sync(0xffffffffu, s1[h].y, o);
+                    s2[h].x += __shfl_xor_sync(0xffffffffu, s2[h].x, o);
+                    s2[h].y += __shfl_xor_sync(0xffffffffu, s2[h].y, o);
                 }
             }
             if (lane < PV) {
 #pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    part[(tw * 2 + 0) * P + k * PV + pv] = s1[k];
-                    part[(tw * 2 + 1) * P + k * PV + pv] = s2[k];
+                for (int h = 0; h < H; ++h) {
+                    part[(tw * 2 + 0) * P + (2 * h) * PV + pv] = s1[h].x;
+                    part[(tw * 2 + 0) * P + (2 * h + 1) * PV + pv] = s1[h].y;
+                    part[(tw * 2 + 1) * P + (2 * h) * PV + pv] = s2[h].x;
+                    part[(tw * 2 + 1) * P + (2 * h + 1) * PV + pv] = s2[h].y;
                 }
             }
             named_barrier(kCfrBarTeam + team, kCfrTeamThreads);
@@ -421,29 +488,36 @@ lncf_bwd_ring_kernel(const CfArgs a, const CfrGeom g, const __grid_constant__ CU
             }
             named_barrier(kCfrBarTeam + team, kCfrTeamThreads);
             // ---- pass 2: dx; this tile's dw, db per channel ----
-            float c1[V], c2[V];
+            float2 nc1[H], nc2[H];
 #pragma unroll
-            for (int k = 0; k < V; ++k) {
-                c1[k] = cf[k * PV + pv];
-                c2[k] = cf[P + k * PV + pv];
+            for (int h = 0; h < H; ++h) {
+                nc1[h] = make_float2(-cf[(2 * h) * PV + pv], -cf[(2 * h + 1) * PV + pv]);
+                nc2[h] = make_float2(-cf[P + (2 * h) * PV + pv], -cf[P + (2 * h + 1) * PV + pv]);
             }
-            T* dxb = dx + i * a.c * a.l + p0 + pv * V;
-            for (int j = 0; j < nch; ++j) {
+            T* dxb = dx + i * a.c * a.l + p0 + pv * V + int64_t(grp) * a.l;
+            const int64_t dstep = int64_t(CG) * a.l;
+            const unsigned char* pd = dyb + size_t(grp) * row;
+            for (int j = 0; j < nch; ++j, pd += step, dxb += dstep) {
                 const int ch = grp + j * CG;
                 float pw = 0.f, pb = 0.f;
                 if (on && j < my_ch) {
-                    float dv[V], xv[V], o[V];
-                    cfr_unpack<T>(dyb + size_t(ch) * row, dv);
-                    cfr_unpack<T>(xb + size_t(ch) * row, xv);
-                    const float wc = wsm[ch];
+                    float2 dv[H], xv[H], o[H];
+                    cfr_load2<T>(pd, dv);
+                    cfr_load2<T>(pd + tensor_bytes, xv);
+                    const float2 wc = f2(wsm[ch]);
+                    float2 pw2 = f2(0.f), pb2 = f2(0.f);
 #pragma unroll
-                    for (int k = 0; k < V; ++k) {
-                        const float xh = (xv[k] - mu[k]) * rs[k];
-                        o[k] = rs[k] * (dv[k] * wc - c1[k] - xh * c2[k]);
-                        pw = fmaf(dv[k], xh, pw);
-                        pb += dv[k];
+                    for (int h = 0; h < H; ++h) {
+                        const float2 xh = __fmul2_rn(__fadd2_rn(xv[h], nmu[h]), rs[h]);
+                        // rstd * (dy*w - c1 - xhat*c2)
+                        const float2 u = __ffma2_rn(xh, nc2[h], __fadd2_rn(__fmul2_rn(dv[h], wc), nc1[h]));
+                        o[h] = __fmul2_rn(rs[h], u);
+                        pw2 = __ffma2_rn(dv[h], xh, pw2);
+                        pb2 = __fadd2_rn(pb2, dv[h]);
                     }
-                    store_vec<T, V>(dxb + int64_t(ch) * a.l, o);
+                    cfr_store2<T>(dxb, o);
+                    pw = pw2.x + pw2.y;
+                    pb = pb2.x + pb2.y;
                 }
                 if (grads) {
                     // the PV threads of this channel are PV consecutive lanes

@@ -791,20 +791,27 @@ inline bool cfr_plan(CfrGeom& g, size_t& smem, const CfArgs& a, size_t es, bool 
     while (pv < 32 && int64_t(pv) * V < a.l) pv *= 2;
     bool found = false;
     // two tiles are being consumed at a time (one per team): four slots keep two loading
-    for (int want = 4; want >= 2 && !found; --want) {
+    for (int want = 4; want >= 2 && !found; want -= 2) {
         for (int p = pv; p >= 8; p /= 2) {
             const int P = p * V;
             const size_t part = r128((size_t(kCfrTeams) * kCfrTeamFloatsPerPos * P + 2 * kCfrTeamWarps) * 4);
             const size_t tensor = size_t(nb) * cb * P * es;
             const size_t slot = r128(tensor * (bwd ? 2 : 1) + (bwd ? size_t(2) * P * 4 : 0));
             if (param + part + acc >= cap) continue;
-            const size_t n_slots = (cap - param - part - acc) / slot;
+            // an even number of slots: the tile that used a slot before tile q is then
+            // q - slots, which the same team consumed (so it has landed).  With an odd
+            // count it belongs to the other team and may still be in flight, and a wait
+            // on the slot's barrier for tile q (parity of phase q / slots) would see the
+            // phase before it pending and return at once.
+            size_t n_slots = (cap - param - part - acc) / slot;
+            if (n_slots > size_t(kCfrMaxSlots)) n_slots = kCfrMaxSlots;
+            n_slots &= ~size_t(1);
             if (n_slots < size_t(want)) continue;
             g.pv = p;
             g.P = P;
             g.cb = cb;
             g.nb = nb;
-            g.slots = int(n_slots < size_t(kCfrMaxSlots) ? n_slots : size_t(kCfrMaxSlots));
+            g.slots = int(n_slots);
             g.slot_bytes = uint32_t(slot);
             g.tx_tensor = uint32_t(tensor);
             g.param_bytes = uint32_t(param);
