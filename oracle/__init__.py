@@ -1,4 +1,5 @@
-"""Double-precision CPU oracle for LayerNorm, RMSNorm and BatchNorm.
+"""Double-precision CPU oracle for LayerNorm, RMSNorm and BatchNorm, and for the
+activation with fused dropout.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library and
@@ -87,9 +88,17 @@ class Oracle:
         lib.oracle_batchnorm_bwd.argtypes = [_I64, _I64, _I64, _D, _D, _D, _D, _D,
                                              _D, _D, ctypes.c_double, ctypes.c_int,
                                              ctypes.c_int, _U32, _D, _D, _D, _D]
+        _U8 = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_philox4x32_10.argtypes = [_U32, _U32, _U32]
+        lib.oracle_dropout_mask.argtypes = [_I64, ctypes.c_double, ctypes.c_uint32, _U8]
+        lib.oracle_act_dropout_fwd.argtypes = [_I64, _D, ctypes.c_int, ctypes.c_double, ctypes.c_uint32, _D]
+        lib.oracle_act_dropout_bwd.argtypes = [_I64, _D, _D, ctypes.c_int, ctypes.c_double,
+                                               ctypes.c_uint32, _D]
         for f in ("oracle_layernorm_fwd", "oracle_layernorm_bwd", "oracle_layernorm_cf_fwd",
                   "oracle_layernorm_cf_bwd", "oracle_rmsnorm_fwd",
-                  "oracle_rmsnorm_bwd", "oracle_batchnorm_fwd", "oracle_batchnorm_bwd"):
+                  "oracle_rmsnorm_bwd", "oracle_batchnorm_fwd", "oracle_batchnorm_bwd",
+                  "oracle_philox4x32_10", "oracle_dropout_mask", "oracle_act_dropout_fwd",
+                  "oracle_act_dropout_bwd"):
             getattr(lib, f).restype = None
         self.lib = lib
 
@@ -206,6 +215,40 @@ class Oracle:
                                       int(bool(training)), int(act), _ptr(mask, _U32),
                                       _ptr(dx), _ptr(dres), _ptr(dw), _ptr(db))
         return dx, dres, dw, db
+
+
+    # -- activation with fused dropout ---------------------------------------
+    def philox4x32_10(self, ctr, key):
+        """The four 32-bit output words of Philox4x32-10 for a counter of four
+        words and a key of two."""
+        c = np.ascontiguousarray(ctr, dtype=np.uint32)
+        k = np.ascontiguousarray(key, dtype=np.uint32)
+        out = np.empty(4, dtype=np.uint32)
+        self.lib.oracle_philox4x32_10(_ptr(c, _U32), _ptr(k, _U32), _ptr(out, _U32))
+        return out
+
+    def dropout_mask(self, count, drop_p, seed):
+        """uint8 keep flags of elements 0 .. count-1."""
+        keep = np.empty(int(count), dtype=np.uint8)
+        self.lib.oracle_dropout_mask(int(count), float(drop_p), int(seed) & 0xFFFFFFFF,
+                                     keep.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
+        return keep
+
+    def act_dropout_fwd(self, x, act, drop_p, seed):
+        """y = act(x) / (1 - p) where kept, 0 where dropped (x flattened)."""
+        x = _f64(x)
+        y = np.empty_like(x)
+        self.lib.oracle_act_dropout_fwd(x.size, _ptr(x), int(act), float(drop_p),
+                                        int(seed) & 0xFFFFFFFF, _ptr(y))
+        return y
+
+    def act_dropout_bwd(self, dy, x, act, drop_p, seed):
+        """dx = dy / (1 - p) * act'(x) where kept, 0 where dropped."""
+        dy, x = _f64(dy), _f64(x)
+        dx = np.empty_like(x)
+        self.lib.oracle_act_dropout_bwd(x.size, _ptr(dy), _ptr(x), int(act), float(drop_p),
+                                        int(seed) & 0xFFFFFFFF, _ptr(dx))
+        return dx
 
 
 _default: Oracle | None = None

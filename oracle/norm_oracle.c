@@ -1,6 +1,6 @@
 /*
  * norm_oracle.c -- plain double-precision CPU oracle for LayerNorm, RMSNorm and
- * BatchNorm, forward and backward.
+ * BatchNorm, forward and backward, and for the activation with fused dropout.
  *
  * TEST INFRASTRUCTURE ONLY.  The parity tests, the smoke check and the bench's
  * CPU-baseline leg call it; the CUDA library never does, and this file shares no
@@ -27,6 +27,9 @@
  *   - The residual is added after the affine step and before the activation; its
  *     gradient is the pre-activation gradient itself.
  *   - ReLU'(z) = 1 for z > 0 and 0 otherwise; GELU is the exact erf form.
+ *   - Dropout draws Philox4x32-10 with key (seed, 0) and counter (e / 4, 0, 0) for
+ *     element e, which takes output word e % 4 as the uniform (word >> 8) * 2^-24;
+ *     the element is dropped when that value is below drop_p (single precision).
  *
  * Parity status: every function here is pinned by the CPU tests (closed forms,
  * invariants, finite differences, independent library routines, hand-worked
@@ -457,5 +460,91 @@ void oracle_batchnorm_bwd(int64_t n, int64_t c, int64_t l, const double *dy,
                 else
                     dx[e] = wc * rs * dz;
             }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Activation with fused dropout                                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The counter-based generator, Philox4x32 with 10 rounds, from its published
+ * definition (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as
+ * 1, 2, 3", SC 2011).  A round forms the 64-bit products of counter words 0 and 2
+ * with the multipliers 0xD2511F53 and 0xCD9E8D57 and replaces the counter by
+ *   (hi(M1*c2) ^ c1 ^ k0, lo(M1*c2), hi(M0*c0) ^ c3 ^ k1, lo(M0*c0));
+ * between rounds the key is advanced by the Weyl increments 0x9E3779B9 and
+ * 0xBB67AE85.  The output is the counter after the tenth round.
+ */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        uint32_t n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        uint32_t n3 = (uint32_t)p0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/*
+ * [AF] section "四、Dropout 融合的关键：可复现的随机掩码": an element's random value is
+ * a function of the seed and the element's offset alone, so the backward rebuilds
+ * the forward's mask from the seed; an element is dropped when its value is below
+ * drop_p and kept elements are divided by (1 - drop_p) (inverted dropout).  The
+ * generator and the offset-to-counter mapping are this library's reading (header).
+ */
+static int dropout_keep(uint32_t seed, int64_t e, double drop_p)
+{
+    uint32_t ctr[4] = {(uint32_t)((uint64_t)e >> 2), (uint32_t)((uint64_t)e >> 34), 0u, 0u};
+    uint32_t key[2] = {seed, 0u};
+    uint32_t out[4];
+    oracle_philox4x32_10(ctr, key, out);
+    float u = (float)(out[e & 3] >> 8) * (1.0f / 16777216.0f);
+    return !(u < (float)drop_p);
+}
+
+void oracle_dropout_mask(int64_t count, double drop_p, uint32_t seed, uint8_t *keep)
+{
+    for (int64_t e = 0; e < count; ++e) keep[e] = (uint8_t)dropout_keep(seed, e, drop_p);
+}
+
+/* [AF] sections "三、融合内核的骨架" and "四": the activation is applied first and its
+ * result goes through dropout in the same pass: y = act(x) / (1 - p) where kept,
+ * 0 where dropped. */
+void oracle_act_dropout_fwd(int64_t count, const double *x, int act, double drop_p,
+                            uint32_t seed, double *y)
+{
+    for (int64_t e = 0; e < count; ++e) {
+        double a = act_forward(act, x[e]);
+        y[e] = dropout_keep(seed, e, drop_p) ? a / (1.0 - drop_p) : 0.0;
+    }
+}
+
+/* [AF] section "五、反向传播融合同样成立": the output gradient goes through the
+ * dropout gradient (the same mask rebuilt from the seed, the same 1/(1 - p)
+ * scale) and is multiplied by the activation's derivative at the saved input:
+ * dx = dy / (1 - p) * act'(x) where kept, 0 where dropped. */
+void oracle_act_dropout_bwd(int64_t count, const double *dy, const double *x, int act,
+                            double drop_p, uint32_t seed, double *dx)
+{
+    for (int64_t e = 0; e < count; ++e) {
+        if (dropout_keep(seed, e, drop_p))
+            dx[e] = dy[e] / (1.0 - drop_p) * act_derivative(act, x[e]);
+        else
+            dx[e] = 0.0;
     }
 }

@@ -14,7 +14,10 @@ What pins what:
     the EMA with the unbiased batch variance (numpy var with ddof=1);
   * central finite differences of L = sum(dy * y) for every backward output;
   * independent library routines: torch.nn.functional layer_norm / rms_norm /
-    batch_norm / gelu and torch autograd, all in float64 on the CPU.
+    batch_norm / gelu / silu / mish and torch autograd, all in float64 on the CPU;
+  * the dropout generator: the published Philox4x32-10 known-answer vectors
+    (tests/golden/), and binomial bounds on keep rates and on the agreement of
+    masks that must be independent.
 """
 from __future__ import annotations
 
@@ -533,6 +536,111 @@ def pin_layernorm_cf_bwd_fd(o):
     _close(dx, _central_diff(loss, x, 1e-6), 1e-6, 1e-7, "cf dx vs FD")
     _close(dw, _central_diff(loss, w, 1e-6), 1e-6, 1e-7, "cf dw vs FD")
     _close(db, _central_diff(loss, b, 1e-6), 1e-6, 1e-7, "cf db vs FD")
+
+
+# ---------------------------------------------------------------------------
+# activation with fused dropout
+# ---------------------------------------------------------------------------
+
+def pin_philox_known_answers(o):
+    """The generator against the published Philox4x32-10 known-answer vectors."""
+    with open(os.path.join(GOLDEN, "philox4x32_10_known_answers.json")) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        ctr = [int(v, 16) for v in case["ctr"]]
+        key = [int(v, 16) for v in case["key"]]
+        want = [int(v, 16) for v in case["out"]]
+        got = [int(v) for v in o.philox4x32_10(ctr, key)]
+        assert got == want, f"philox4x32-10 {case['ctr']} {case['key']}: {[hex(v) for v in got]}"
+
+
+def pin_dropout_keep_rate(o):
+    """Each element is kept with probability 1 - p (binomial bound, 6 sigma);
+    p = 0 keeps everything and p = 1 nothing."""
+    n = 200_000
+    for p in (0.1, 0.5, 0.9):
+        for seed in (0, 12345, 65535):
+            kept = o.dropout_mask(n, p, seed).mean()
+            sigma = (p * (1 - p) / n) ** 0.5
+            assert abs(kept - (1 - p)) < 6 * sigma, f"keep rate {kept} for p={p}, seed={seed}"
+    assert o.dropout_mask(1000, 0.0, 3).all()
+    assert not o.dropout_mask(1000, 1.0, 3).any()
+
+
+def pin_dropout_independence(o):
+    """Neighbouring elements (the same generator call), elements four apart (the
+    next counter) and two seeds agree as often as independent fair coins do."""
+    n = 200_000
+    a = o.dropout_mask(n + 4, 0.5, 77).astype(bool)
+    b = o.dropout_mask(n, 0.5, 78).astype(bool)
+    sigma = (0.25 / n) ** 0.5
+    for what, u, v in (("adjacent", a[:n], a[1:n + 1]), ("four apart", a[:n], a[4:n + 4]),
+                       ("seeds", a[:n], b)):
+        agree = float((u == v).mean())
+        assert abs(agree - 0.5) < 6 * sigma, f"dropout masks {what}: agreement {agree}"
+
+
+def _act_torch():
+    import torch
+    import torch.nn.functional as F
+    return {0: lambda t: t, 1: torch.relu, 2: F.gelu, 3: F.silu, 4: F.mish}
+
+
+def pin_act_dropout_no_drop_is_activation(o):
+    """p = 0: the kernel is the plain activation (torch's reference functions)."""
+    import torch
+    x = _rng(40).normal(size=4096) * 3
+    for act, fn in _act_torch().items():
+        y = o.act_dropout_fwd(x, act, 0.0, 9)
+        _close(y, fn(torch.from_numpy(x)).numpy(), 1e-15, 1e-14, f"act {act} without dropout")
+
+
+def pin_act_dropout_inverted_scale(o):
+    """Kept elements are act(x) / (1 - p); dropped ones are 0; the mask is the
+    generator's."""
+    import torch
+    x = _rng(41).normal(size=20000) * 2
+    p = 0.25
+    keep = o.dropout_mask(x.size, p, 4321).astype(bool)
+    for act, fn in _act_torch().items():
+        y = o.act_dropout_fwd(x, act, p, 4321)
+        a = fn(torch.from_numpy(x)).numpy()
+        _close(y[keep], a[keep] / (1 - p), 1e-15, 1e-14, f"act {act} kept elements")
+        assert not y[~keep].any(), f"act {act}: dropped elements must be 0"
+    # the mean is preserved in expectation (inverted dropout)
+    xs = np.abs(_rng(42).normal(size=200_000)) + 1.0
+    y = o.act_dropout_fwd(xs, 0, p, 5)
+    assert abs(y.mean() - xs.mean()) < 6 * xs.std() * (p / (1 - p) / xs.size) ** 0.5 + 6 * xs.std() / xs.size ** 0.5
+
+
+def pin_act_dropout_bwd_fd(o):
+    """Backward = derivative of sum(dy * forward) with the seed held fixed."""
+    r = _rng(43)
+    x = r.normal(size=64) * 2
+    x = np.where(np.abs(x) < 0.05, 0.3, x)  # keep ReLU's kink out of the stencil
+    dy = r.normal(size=64)
+    for act in (0, 1, 2, 3, 4):
+        for p in (0.0, 0.3):
+            def loss():
+                return float((dy * o.act_dropout_fwd(x, act, p, 11)).sum())
+            dx = o.act_dropout_bwd(dy, x, act, p, 11)
+            _close(dx, _central_diff(loss, x, 1e-6), 1e-7, 1e-7, f"act {act} p {p} dx vs FD")
+
+
+def pin_act_dropout_bwd_vs_torch(o):
+    """Backward against torch autograd of act(x) * keep / (1 - p)."""
+    import torch
+    r = _rng(44)
+    x = torch.tensor(r.normal(size=5000) * 2, requires_grad=True)
+    dy = r.normal(size=5000)
+    p = 0.4
+    keep = torch.from_numpy(o.dropout_mask(5000, p, 999).astype(np.float64))
+    for act, fn in _act_torch().items():
+        if x.grad is not None:
+            x.grad = None
+        (fn(x) * keep / (1 - p)).backward(torch.from_numpy(dy))
+        dx = o.act_dropout_bwd(dy, x.detach().numpy(), act, p, 999)
+        _close(dx, x.grad.numpy(), 1e-14, 1e-13, f"act {act} dx vs torch")
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
