@@ -295,6 +295,42 @@ NRM_API nrm_status nrm_batchnorm_bwd(const void *dy, const void *x, const void *
                              nrm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Activation with fused dropout                                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * nrm_act_dropout_fwd -- "算子融合实战：attorch激活函数与Dropout融合核的完整实现原理",
+ * sections "三、融合内核的骨架" and "四、Dropout 融合的关键：可复现的随机掩码": the
+ * activation's result goes through inverted dropout in the same pass,
+ *   y[e] = act(x[e]) / (1 - drop_p)  if element e is kept,  else 0.
+ * The mask is not stored: element e's random value is a function of (seed, e)
+ * alone.  Generator (this library's reading of the article's tl.rand(seed,
+ * offset)): Philox4x32-10 (Salmon et al., SC 2011) with key (seed, 0) and
+ * counter (e / 4 as two 32-bit words, 0, 0); element e takes output word e % 4,
+ * u = (word >> 8) * 2^-24, and is dropped when u < drop_p (compared in single
+ * precision).  x, y: count elements in dt (contiguous; y may equal x).
+ * act: NRM_ACT_NONE (plain dropout), RELU, GELU, SILU or MISH.  drop_p in
+ * [0, 1]: 0 keeps every element, 1 drops every one.  Any seed; the article
+ * draws a 16-bit one.  One kernel is enqueued (none for count == 0).
+ * Errors: NRM_ERR_INVALID_ARG for a negative count, drop_p outside [0, 1] or
+ * NaN, an unknown act or dtype, NULL or misaligned pointers with count > 0.
+ */
+NRM_API nrm_status nrm_act_dropout_fwd(const void *x, void *y, int64_t count, nrm_act act,
+                               float drop_p, uint32_t seed, nrm_dtype dt, nrm_stream_t stream);
+
+/*
+ * nrm_act_dropout_bwd -- same article, section "五、反向传播融合同样成立": the mask
+ * is rebuilt from the same seed and offsets and the derivative is taken at the
+ * saved input,
+ *   dx[e] = dy[e] / (1 - drop_p) * act'(x[e])  if kept,  else 0   (ReLU'(0) = 0).
+ * dy, x, dx: count elements in dt (dx may equal dy or x).  act, drop_p, seed:
+ * those of the forward.  Errors as nrm_act_dropout_fwd.
+ */
+NRM_API nrm_status nrm_act_dropout_bwd(const void *dy, const void *x, void *dx, int64_t count,
+                               nrm_act act, float drop_p, uint32_t seed, nrm_dtype dt,
+                               nrm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Helpers                                                                   */
 /* ------------------------------------------------------------------------ */
 

@@ -27,7 +27,8 @@ ACTS = {"none": NRM_ACT_NONE, "relu": NRM_ACT_RELU, "gelu": NRM_ACT_GELU, "silu"
 EXPORTS = ("nrm_layernorm_fwd", "nrm_layernorm_bwd", "nrm_layernorm_bwd_noalloc",
            "nrm_layernorm_cf_fwd", "nrm_layernorm_cf_bwd",
            "nrm_rmsnorm_fwd", "nrm_rmsnorm_bwd",
-           "nrm_batchnorm_fwd", "nrm_batchnorm_bwd", "nrm_workspace_bytes",
+           "nrm_batchnorm_fwd", "nrm_batchnorm_bwd", "nrm_act_dropout_fwd", "nrm_act_dropout_bwd",
+           "nrm_workspace_bytes",
            "nrm_batchnorm_workspace_bytes",
            "nrm_act_mask_words", "nrm_sync_status", "nrm_status_str",
            "nrm_last_error_message", "nrm_version")
@@ -69,6 +70,8 @@ def load(path: str | None = None):
                               _I, _I, _P, ctypes.c_size_t, _P],
         "nrm_batchnorm_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I,
                               _I, _I, _P, ctypes.c_size_t, _P],
+        "nrm_act_dropout_fwd": [_P, _P, _I64, _I, _F, ctypes.c_uint32, _I, _P],
+        "nrm_act_dropout_bwd": [_P, _P, _P, _I64, _I, _F, ctypes.c_uint32, _I, _P],
         "nrm_workspace_bytes": [_I, _I64, _I64, _I],
         "nrm_batchnorm_workspace_bytes": [_I64, _I64, _I64, _I],
         "nrm_act_mask_words": [_I64, _I64, _I64],
@@ -244,6 +247,20 @@ def batchnorm_workspace(x):
 
 def nrm_workspace_bytes(op: int, rows: int, cols: int, dtype_code: int) -> int:
     return int(load().nrm_workspace_bytes(op, rows, cols, dtype_code))
+
+
+def nrm_act_dropout_fwd(x, y, act, drop_p, seed, stream=None):
+    """y = act(x) / (1 - drop_p) where kept, else 0 (mask rebuilt from seed and offset)."""
+    _check(load().nrm_act_dropout_fwd(_ptr(x), _ptr(y), x.numel(), _act(act), float(drop_p),
+                                      int(seed) & 0xFFFFFFFF, _dtype_code(x), _stream(stream)),
+           "nrm_act_dropout_fwd")
+
+
+def nrm_act_dropout_bwd(dy, x, dx, act, drop_p, seed, stream=None):
+    """dx = dy / (1 - drop_p) * act'(x) where kept, else 0."""
+    _check(load().nrm_act_dropout_bwd(_ptr(dy), _ptr(x), _ptr(dx), x.numel(), _act(act), float(drop_p),
+                                      int(seed) & 0xFFFFFFFF, _dtype_code(x), _stream(stream)),
+           "nrm_act_dropout_bwd")
 
 
 def nrm_act_mask_words(n: int, c: int, l: int) -> int:

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libnorm.so")
 
-SOURCES = ["api.cu", "noalloc.cu",
+SOURCES = ["api.cu", "noalloc.cu", "dropout.cu",
            "rownorm_f32.cu", "rownorm_f16.cu", "rownorm_bf16.cu",
            "batchnorm_f32.cu", "batchnorm_f16.cu", "batchnorm_bf16.cu"]
 

@@ -564,6 +564,46 @@ size_t nrm_batchnorm_workspace_bytes(int64_t n, int64_t c, int64_t l, nrm_dtype 
     return batchnorm_workspace_bytes(*d, c);
 }
 
+namespace {
+nrm_status check_act_dropout(int64_t count, nrm_act act, float p, nrm_dtype dt) {
+    if (!dtype_ok(dt)) return fail(NRM_ERR_INVALID_ARG, "unknown dtype %d", int(dt));
+    if (count < 0) return fail(NRM_ERR_INVALID_ARG, "count must be >= 0");
+    if (count >= (int64_t(1) << 40)) return fail(NRM_ERR_UNSUPPORTED, "count must be < 2^40");
+    if (act != NRM_ACT_NONE && act != NRM_ACT_RELU && act != NRM_ACT_GELU && act != NRM_ACT_SILU &&
+        act != NRM_ACT_MISH)
+        return fail(NRM_ERR_INVALID_ARG, "unknown activation %d", int(act));
+    if (!(p >= 0.f && p <= 1.f)) return fail(NRM_ERR_INVALID_ARG, "drop_p must be in [0, 1]");
+    return NRM_OK;
+}
+}  // namespace
+
+nrm_status nrm_act_dropout_fwd(const void* x, void* y, int64_t count, nrm_act act, float drop_p, uint32_t seed,
+                               nrm_dtype dt, nrm_stream_t stream) {
+    t_msg[0] = 0;
+    nrm_status st = check_act_dropout(count, act, drop_p, dt);
+    if (st != NRM_OK) return st;
+    if (count > 0 && (!x || !y)) return fail(NRM_ERR_INVALID_ARG, "x and y must not be NULL");
+    const size_t es = dsize(dt);
+    if (!all_aligned({x, y}, es)) return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    const bool vec = all_aligned({x, y}, 16);
+    return act_dropout(x, nullptr, y, count, int(act), drop_p, seed, dt, false, vec,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+nrm_status nrm_act_dropout_bwd(const void* dy, const void* x, void* dx, int64_t count, nrm_act act, float drop_p,
+                               uint32_t seed, nrm_dtype dt, nrm_stream_t stream) {
+    t_msg[0] = 0;
+    nrm_status st = check_act_dropout(count, act, drop_p, dt);
+    if (st != NRM_OK) return st;
+    if (count > 0 && (!dy || !x || !dx)) return fail(NRM_ERR_INVALID_ARG, "dy, x and dx must not be NULL");
+    const size_t es = dsize(dt);
+    if (!all_aligned({dy, x, dx}, es))
+        return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    const bool vec = all_aligned({dy, x, dx}, 16);
+    return act_dropout(x, dy, dx, count, int(act), drop_p, seed, dt, true, vec,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
 int64_t nrm_act_mask_words(int64_t n, int64_t c, int64_t l) {
     if (n < 0 || c < 0 || l < 0) return 0;
     return n * c * ((l + 31) / 32);

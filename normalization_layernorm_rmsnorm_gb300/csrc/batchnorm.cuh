@@ -39,6 +39,7 @@
 //     sum(dz*(x - mean)) = sum(dz*x) - mean*sum(dz) in double.
 #pragma once
 
+#include "activation.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -67,74 +68,10 @@ struct BnGeom {
     void* partials;        // [c][S]: float4 (n, mean, m2, 0) forward; double2 backward
 };
 
-// softplus(z) = log(1 + e^z), without overflow for large z
-__device__ __forceinline__ float softplus_f(float z) {
-    return z > 0.f ? z + log1pf(expf(-z)) : log1pf(expf(z));
-}
-
-__device__ __forceinline__ float act_forward(int act, float z) {
-    if (act == NRM_ACT_RELU) return z > 0.f ? z : 0.f;
-    if (act == NRM_ACT_GELU) return 0.5f * z * (1.f + erff(z * 0.70710678118654752f));
-    if (act == NRM_ACT_SILU) return z / (1.f + expf(-z));
-    if (act == NRM_ACT_MISH) return z * tanhf(softplus_f(z));
-    return z;
-}
-
-// Derivative at the pre-activation value z (ReLU'(0) = 0).
-__device__ __forceinline__ float act_derivative(int act, float z) {
-    if (act == NRM_ACT_RELU) return z > 0.f ? 1.f : 0.f;
-    if (act == NRM_ACT_GELU) {
-        const float cdf = 0.5f * (1.f + erff(z * 0.70710678118654752f));
-        const float pdf = expf(-0.5f * z * z) * 0.39894228040143268f;
-        return fmaf(z, pdf, cdf);
-    }
-    if (act == NRM_ACT_SILU) {
-        const float sg = 1.f / (1.f + expf(-z));
-        return sg * fmaf(z, 1.f - sg, 1.f);
-    }
-    if (act == NRM_ACT_MISH) {
-        const float t = tanhf(softplus_f(z));
-        const float sg = 1.f / (1.f + expf(-z));
-        return fmaf(z * sg, 1.f - t * t, t);
-    }
-    return 1.f;
-}
-
 // Whether the backward recomputes z = x*scale + shift (+ residual) to take the
 // activation's derivative (every activation but none, and ReLU with a mask).
 __host__ __device__ __forceinline__ bool bn_need_z(int act, const void* mask_in) {
     return act != NRM_ACT_NONE && !(act == NRM_ACT_RELU && mask_in != nullptr);
-}
-
-// The same for an activation fixed at compile time (the ring and group
-// kernels are instantiated per activation, so the hot loops carry one).
-template <int ACT>
-__device__ __forceinline__ float act_forward_c(float z) {
-    if constexpr (ACT == NRM_ACT_RELU) return z > 0.f ? z : 0.f;
-    else if constexpr (ACT == NRM_ACT_NONE) return z;
-    else return act_forward(ACT, z);
-}
-template <int ACT>
-__device__ __forceinline__ float act_derivative_c(float z) {
-    if constexpr (ACT == NRM_ACT_RELU) return z > 0.f ? 1.f : 0.f;
-    else if constexpr (ACT == NRM_ACT_NONE) return 1.f;
-    else return act_derivative(ACT, z);
-}
-
-// Calls f(std::integral_constant-like tag) with the activation as a compile-time value.
-template <int A>
-struct ActTag {
-    static constexpr int value = A;
-};
-template <typename F>
-auto with_act(int act, F&& f) {
-    switch (act) {
-    case NRM_ACT_RELU: return f(ActTag<NRM_ACT_RELU>{});
-    case NRM_ACT_GELU: return f(ActTag<NRM_ACT_GELU>{});
-    case NRM_ACT_SILU: return f(ActTag<NRM_ACT_SILU>{});
-    case NRM_ACT_MISH: return f(ActTag<NRM_ACT_MISH>{});
-    default: return f(ActTag<NRM_ACT_NONE>{});
-    }
 }
 
 // Location of lane `lane` of block `bi` of channel `ch`.

@@ -1,0 +1,188 @@
+// dropout.cu -- an activation with fused dropout, forward and backward, for
+// every storage dtype (the activation-dropout article, "算子融合实战：attorch激活
+// 函数与Dropout融合核的完整实现原理"):
+//   y  = act(x) / (1 - p)         where element e is kept, else 0   (sections 三, 四)
+//   dx = dy / (1 - p) * act'(x)   where element e is kept, else 0   (section 五)
+// The mask is never stored: both passes rebuild it from the seed and the
+// element's offset with a counter-based generator, Philox4x32-10 (Salmon,
+// Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+// SC 2011), keyed by (seed, 0) with counter (e / 4, 0, 0); element e takes
+// output word e % 4 and is dropped when (word >> 8) * 2^-24 < p, tested here as
+// the integer comparison (word >> 8) < ceil(p * 2^24), which decides the same.
+//
+// GB300 design: an HBM-streaming elementwise kernel.  A persistent grid of
+// 256-thread CTAs walks the tensor in 16-byte vectors, two per thread per
+// iteration so that two loads are in flight before any arithmetic; one
+// generator call covers four elements (its four output words).  Tensors that
+// are not 16-byte aligned take a scalar kernel over groups of four elements.
+#include <cmath>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "activation.cuh"
+#include "common.cuh"
+#include "internal.h"
+
+namespace nrm {
+
+constexpr int kDropThreads = 256;
+constexpr int kDropUnroll = 2;  // 16-byte vectors per thread and iteration
+
+struct DropArgs {
+    const void* x;
+    const void* dy;
+    void* y;
+    void* dx;
+    int64_t count;
+    uint32_t seed;
+    uint32_t thresh;  // ceil(p * 2^24): element kept when (word >> 8) >= thresh
+    float scale;      // 1 / (1 - p) (0 when p = 1)
+};
+
+// Philox4x32 with 10 rounds on counter c and key (k0, k1).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = uint64_t(0xD2511F53u) * c.x;
+        const uint64_t p1 = uint64_t(0xCD9E8D57u) * c.z;
+        c = make_uint4(uint32_t(p1 >> 32) ^ c.y ^ k0, uint32_t(p1), uint32_t(p0 >> 32) ^ c.w ^ k1, uint32_t(p0));
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// The four random words of elements 4g .. 4g+3.
+__device__ __forceinline__ uint4 drop_words(uint64_t g, uint32_t seed) {
+    return philox4x32_10(make_uint4(uint32_t(g), uint32_t(g >> 32), 0u, 0u), seed, 0u);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& r, int k) {
+    return k == 0 ? r.x : (k == 1 ? r.y : (k == 2 ? r.z : r.w));
+}
+
+template <int ACT, bool BWD>
+__device__ __forceinline__ float drop_elem(float xv, float dyv, uint32_t word, const DropArgs& a) {
+    if ((word >> 8) < a.thresh) return 0.f;
+    if constexpr (BWD) return dyv * a.scale * act_derivative_c<ACT>(xv);
+    else return act_forward_c<ACT>(xv) * a.scale;
+}
+
+// One element by scalar accesses (tails and unaligned tensors).
+template <typename T, int ACT, bool BWD>
+__device__ __forceinline__ void drop_scalar(const DropArgs& a, int64_t e, uint32_t word) {
+    using bits = typename Io<T>::bits_t;
+    const float xv = Io<T>::load(reinterpret_cast<const bits*>(a.x)[e]);
+    const float dyv = BWD ? Io<T>::load(reinterpret_cast<const bits*>(a.dy)[e]) : 0.f;
+    const float o = drop_elem<ACT, BWD>(xv, dyv, word, a);
+    reinterpret_cast<bits*>(BWD ? a.dx : a.y)[e] = Io<T>::store(o);
+}
+
+// 16-byte vectors (every pointer 16-byte aligned); the count % V tail elements
+// by scalar accesses.
+template <typename T, int ACT, bool BWD>
+__global__ void __launch_bounds__(kDropThreads)
+act_dropout_vec_kernel(const DropArgs a) {
+    constexpr int V = kVec<T>;  // elements per vector: 4 (fp32) or 8 (16-bit)
+    const int64_t nvec = a.count / V;
+    const int64_t stride = int64_t(gridDim.x) * kDropThreads;
+    const int64_t t0 = int64_t(blockIdx.x) * kDropThreads + threadIdx.x;
+    const T* x = reinterpret_cast<const T*>(a.x);
+    const T* dy = reinterpret_cast<const T*>(a.dy);
+    T* out = reinterpret_cast<T*>(BWD ? a.dx : a.y);
+    for (int64_t v0 = t0; v0 < nvec; v0 += kDropUnroll * stride) {
+        float xv[kDropUnroll][V], dv[kDropUnroll][V];
+#pragma unroll
+        for (int u = 0; u < kDropUnroll; ++u) {
+            const int64_t v = v0 + u * stride;
+            if (v < nvec) {
+                load_vec<T, V>(x + v * V, xv[u]);
+                if (BWD) load_vec<T, V>(dy + v * V, dv[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kDropUnroll; ++u) {
+            const int64_t v = v0 + u * stride;
+            if (v < nvec) {
+                float o[V];
+#pragma unroll
+                for (int q = 0; q < V / 4; ++q) {
+                    const uint4 r = drop_words(uint64_t(v) * (V / 4) + q, a.seed);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        o[4 * q + k] = drop_elem<ACT, BWD>(xv[u][4 * q + k], BWD ? dv[u][4 * q + k] : 0.f,
+                                                           word_of(r, k), a);
+                }
+                store_vec<T, V>(out + v * V, o);
+            }
+        }
+    }
+    // the tail: fewer than V elements after the last whole vector
+    const int64_t e = nvec * V + t0;
+    if (e < a.count) drop_scalar<T, ACT, BWD>(a, e, word_of(drop_words(uint64_t(e) >> 2, a.seed), int(e & 3)));
+}
+
+// Any alignment: groups of four elements (one generator call), scalar accesses.
+template <typename T, int ACT, bool BWD>
+__global__ void __launch_bounds__(kDropThreads)
+act_dropout_scalar_kernel(const DropArgs a) {
+    const int64_t groups = (a.count + 3) / 4;
+    const int64_t stride = int64_t(gridDim.x) * kDropThreads;
+    for (int64_t g = int64_t(blockIdx.x) * kDropThreads + threadIdx.x; g < groups; g += stride) {
+        const uint4 r = drop_words(uint64_t(g), a.seed);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t e = 4 * g + k;
+            if (e < a.count) drop_scalar<T, ACT, BWD>(a, e, word_of(r, k));
+        }
+    }
+}
+
+template <typename T, bool BWD>
+nrm_status act_dropout_launch(const DropArgs& a, int act, bool vec, cudaStream_t s) {
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    if (a.count == 0) return NRM_OK;
+    const void* fn = with_act(act, [&](auto tag) {
+        constexpr int A = decltype(tag)::value;
+        return vec ? (const void*)&act_dropout_vec_kernel<T, A, BWD>
+                   : (const void*)&act_dropout_scalar_kernel<T, A, BWD>;
+    });
+    const int64_t items = vec ? (a.count / kVec<T> + kDropUnroll - 1) / kDropUnroll : (a.count + 3) / 4;
+    int64_t blocks = (items + kDropThreads - 1) / kDropThreads;
+    const int occ = cached_occupancy(fn, kDropThreads, 0);
+    if (occ <= 0) return fail(NRM_ERR_CUDA, "activation-dropout kernel cannot be resident");
+    const int64_t cap = int64_t(occ) * d->sms;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;  // the vector kernel's tail needs a thread even with no whole vector
+    DropArgs args = a;
+    void* kargs[] = {&args};
+    return cuda_status(cudaLaunchKernel(fn, dim3(unsigned(blocks)), dim3(kDropThreads), kargs, 0, s),
+                       "activation-dropout launch");
+}
+
+nrm_status act_dropout(const void* x, const void* dy, void* out, int64_t count, int act, float p, uint32_t seed,
+                       nrm_dtype dt, bool bwd, bool vec, cudaStream_t s) {
+    DropArgs a{};
+    a.x = x;
+    a.dy = dy;
+    a.y = bwd ? nullptr : out;
+    a.dx = bwd ? out : nullptr;
+    a.count = count;
+    a.seed = seed;
+    // p * 2^24 is exact in double; its ceiling is the smallest 24-bit value kept
+    a.thresh = uint32_t(std::ceil(double(p) * 16777216.0));
+    a.scale = p < 1.f ? float(1.0 / (1.0 - double(p))) : 0.f;
+    switch (dt) {
+    case NRM_F32:
+        return bwd ? act_dropout_launch<float, true>(a, act, vec, s) : act_dropout_launch<float, false>(a, act, vec, s);
+    case NRM_F16:
+        return bwd ? act_dropout_launch<__half, true>(a, act, vec, s) : act_dropout_launch<__half, false>(a, act, vec, s);
+    default:
+        return bwd ? act_dropout_launch<__nv_bfloat16, true>(a, act, vec, s)
+                   : act_dropout_launch<__nv_bfloat16, false>(a, act, vec, s);
+    }
+}
+
+}  // namespace nrm

@@ -104,6 +104,10 @@ struct CfArgs {
 nrm_status encode_ncl_map(CUtensorMap* map, const void* base, size_t es, int64_t n, int64_t c, int64_t l,
                           int box_l, int box_c);
 
+// Activation with fused dropout (dropout.cu): out = y (forward) or dx (backward).
+nrm_status act_dropout(const void* x, const void* dy, void* out, int64_t count, int act, float p, uint32_t seed,
+                       nrm_dtype dt, bool bwd, bool vec, cudaStream_t s);
+
 template <typename T> nrm_status cf_fwd(const CfArgs& a, bool vec, cudaStream_t s);
 template <typename T> nrm_status cf_bwd(CfArgs a, bool vec, cudaStream_t s);
 

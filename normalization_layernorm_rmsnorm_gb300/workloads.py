@@ -58,8 +58,13 @@ def build_calls(dev, names=None):
 
 # Workloads of the operations built beyond the step, timed beside it (not part
 # of the step's bytes or time): LayerNorm over the channels of an NCHW tensor,
-# as in ConvNeXt-T's stem and first downsampling layer (96 channels of 56x56).
-EXTRA = ("ln_cf_f16_128x96x56x56",)
+# as in ConvNeXt-T's stem and first downsampling layer (96 channels of 56x56),
+# and GELU with fused dropout on a ViT-B MLP hidden activation (128 images x 197
+# tokens x 3072 features).
+DROPOUT_WORKLOAD = "act_dropout_gelu_f16_25216x3072"
+DROPOUT_P = 0.1
+DROPOUT_SEED = 2024
+EXTRA = ("ln_cf_f16_128x96x56x56", DROPOUT_WORKLOAD)
 
 
 def build_extra_calls(dev, names=None):
@@ -72,6 +77,8 @@ def build_extra_calls(dev, names=None):
 
     if names is None or EXTRA[0] in names:
         calls += _ln_cf(EXTRA[0], 128, 96, 56 * 56, dev, f32)
+    if names is None or DROPOUT_WORKLOAD in names:
+        calls += _act_dropout(DROPOUT_WORKLOAD, 25216, 3072, dev)
     return calls
 
 
@@ -204,4 +211,20 @@ def _ln_cf(name, n, c, l, dev, f32):
         Call(name, "bwd", "lncf_bwd_ring_kernel<f16>+colsum",
              lambda: nrm.nrm_layernorm_cf_bwd(dy, x, w, mean, rstd, dx, dw, db, ws),
              nbytes(dy, x, w, mean, rstd, dx, dw, db), 2, [dy], [dx, dw, db]),
+    ]
+
+
+def _act_dropout(name, rows, cols, dev):
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    seed = 37
+    x = synth.random_tensor(seed, 1, (rows, cols), "f16").torch(dev)
+    dy = synth.random_tensor(seed, 2, (rows, cols), "f16").torch(dev)
+    y, dx = x.new_empty(x.shape), x.new_empty(x.shape)
+    p, s = DROPOUT_P, DROPOUT_SEED
+    return [
+        Call(name, "fwd", "act_dropout_vec_kernel<f16,gelu>",
+             lambda: nrm.nrm_act_dropout_fwd(x, y, "gelu", p, s), nbytes(x, y), 1, [x], [y]),
+        Call(name, "bwd", "act_dropout_vec_kernel<f16,gelu,bwd>",
+             lambda: nrm.nrm_act_dropout_bwd(dy, x, dx, "gelu", p, s), nbytes(dy, x, dx), 1, [dy], [dx]),
     ]

@@ -90,9 +90,10 @@ class Oracle:
                                              ctypes.c_int, _U32, _D, _D, _D, _D]
         _U8 = ctypes.POINTER(ctypes.c_uint8)
         lib.oracle_philox4x32_10.argtypes = [_U32, _U32, _U32]
-        lib.oracle_dropout_mask.argtypes = [_I64, ctypes.c_double, ctypes.c_uint32, _U8]
-        lib.oracle_act_dropout_fwd.argtypes = [_I64, _D, ctypes.c_int, ctypes.c_double, ctypes.c_uint32, _D]
-        lib.oracle_act_dropout_bwd.argtypes = [_I64, _D, _D, ctypes.c_int, ctypes.c_double,
+        lib.oracle_dropout_mask.argtypes = [_I64, _I64, ctypes.c_double, ctypes.c_uint32, _U8]
+        lib.oracle_act_dropout_fwd.argtypes = [_I64, _I64, _D, ctypes.c_int, ctypes.c_double,
+                                               ctypes.c_uint32, _D]
+        lib.oracle_act_dropout_bwd.argtypes = [_I64, _I64, _D, _D, ctypes.c_int, ctypes.c_double,
                                                ctypes.c_uint32, _D]
         for f in ("oracle_layernorm_fwd", "oracle_layernorm_bwd", "oracle_layernorm_cf_fwd",
                   "oracle_layernorm_cf_bwd", "oracle_rmsnorm_fwd",
@@ -227,26 +228,27 @@ class Oracle:
         self.lib.oracle_philox4x32_10(_ptr(c, _U32), _ptr(k, _U32), _ptr(out, _U32))
         return out
 
-    def dropout_mask(self, count, drop_p, seed):
-        """uint8 keep flags of elements 0 .. count-1."""
+    def dropout_mask(self, count, drop_p, seed, first=0):
+        """uint8 keep flags of elements first .. first+count-1."""
         keep = np.empty(int(count), dtype=np.uint8)
-        self.lib.oracle_dropout_mask(int(count), float(drop_p), int(seed) & 0xFFFFFFFF,
+        self.lib.oracle_dropout_mask(int(count), int(first), float(drop_p), int(seed) & 0xFFFFFFFF,
                                      keep.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
         return keep
 
-    def act_dropout_fwd(self, x, act, drop_p, seed):
-        """y = act(x) / (1 - p) where kept, 0 where dropped (x flattened)."""
+    def act_dropout_fwd(self, x, act, drop_p, seed, first=0):
+        """y = act(x) / (1 - p) where kept, 0 where dropped; x (flattened) holds
+        the tensor's elements first, first+1, ..."""
         x = _f64(x)
         y = np.empty_like(x)
-        self.lib.oracle_act_dropout_fwd(x.size, _ptr(x), int(act), float(drop_p),
+        self.lib.oracle_act_dropout_fwd(x.size, int(first), _ptr(x), int(act), float(drop_p),
                                         int(seed) & 0xFFFFFFFF, _ptr(y))
         return y
 
-    def act_dropout_bwd(self, dy, x, act, drop_p, seed):
+    def act_dropout_bwd(self, dy, x, act, drop_p, seed, first=0):
         """dx = dy / (1 - p) * act'(x) where kept, 0 where dropped."""
         dy, x = _f64(dy), _f64(x)
         dx = np.empty_like(x)
-        self.lib.oracle_act_dropout_bwd(x.size, _ptr(dy), _ptr(x), int(act), float(drop_p),
+        self.lib.oracle_act_dropout_bwd(x.size, int(first), _ptr(dy), _ptr(x), int(act), float(drop_p),
                                         int(seed) & 0xFFFFFFFF, _ptr(dx))
         return dx
 

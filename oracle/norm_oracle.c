@@ -517,20 +517,22 @@ static int dropout_keep(uint32_t seed, int64_t e, double drop_p)
     return !(u < (float)drop_p);
 }
 
-void oracle_dropout_mask(int64_t count, double drop_p, uint32_t seed, uint8_t *keep)
+/* Arrays hold elements first .. first + count - 1 of the tensor: the random
+ * value belongs to the element's offset in the whole tensor. */
+void oracle_dropout_mask(int64_t count, int64_t first, double drop_p, uint32_t seed, uint8_t *keep)
 {
-    for (int64_t e = 0; e < count; ++e) keep[e] = (uint8_t)dropout_keep(seed, e, drop_p);
+    for (int64_t i = 0; i < count; ++i) keep[i] = (uint8_t)dropout_keep(seed, first + i, drop_p);
 }
 
 /* [AF] sections "三、融合内核的骨架" and "四": the activation is applied first and its
  * result goes through dropout in the same pass: y = act(x) / (1 - p) where kept,
  * 0 where dropped. */
-void oracle_act_dropout_fwd(int64_t count, const double *x, int act, double drop_p,
-                            uint32_t seed, double *y)
+void oracle_act_dropout_fwd(int64_t count, int64_t first, const double *x, int act,
+                            double drop_p, uint32_t seed, double *y)
 {
-    for (int64_t e = 0; e < count; ++e) {
-        double a = act_forward(act, x[e]);
-        y[e] = dropout_keep(seed, e, drop_p) ? a / (1.0 - drop_p) : 0.0;
+    for (int64_t i = 0; i < count; ++i) {
+        double a = act_forward(act, x[i]);
+        y[i] = dropout_keep(seed, first + i, drop_p) ? a / (1.0 - drop_p) : 0.0;
     }
 }
 
@@ -538,13 +540,13 @@ void oracle_act_dropout_fwd(int64_t count, const double *x, int act, double drop
  * dropout gradient (the same mask rebuilt from the seed, the same 1/(1 - p)
  * scale) and is multiplied by the activation's derivative at the saved input:
  * dx = dy / (1 - p) * act'(x) where kept, 0 where dropped. */
-void oracle_act_dropout_bwd(int64_t count, const double *dy, const double *x, int act,
-                            double drop_p, uint32_t seed, double *dx)
+void oracle_act_dropout_bwd(int64_t count, int64_t first, const double *dy, const double *x,
+                            int act, double drop_p, uint32_t seed, double *dx)
 {
-    for (int64_t e = 0; e < count; ++e) {
-        if (dropout_keep(seed, e, drop_p))
-            dx[e] = dy[e] / (1.0 - drop_p) * act_derivative(act, x[e]);
+    for (int64_t i = 0; i < count; ++i) {
+        if (dropout_keep(seed, first + i, drop_p))
+            dx[i] = dy[i] / (1.0 - drop_p) * act_derivative(act, x[i]);
         else
-            dx[e] = 0.0;
+            dx[i] = 0.0;
     }
 }

@@ -45,11 +45,12 @@ void oracle_batchnorm_bwd(int64_t n, int64_t c, int64_t l, const double *dy,
                           double *dres, double *dw, double *db);
 
 void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
-void oracle_dropout_mask(int64_t count, double drop_p, uint32_t seed, uint8_t *keep);
-void oracle_act_dropout_fwd(int64_t count, const double *x, int act, double drop_p,
-                            uint32_t seed, double *y);
-void oracle_act_dropout_bwd(int64_t count, const double *dy, const double *x, int act,
-                            double drop_p, uint32_t seed, double *dx);
+void oracle_dropout_mask(int64_t count, int64_t first, double drop_p, uint32_t seed,
+                         uint8_t *keep);
+void oracle_act_dropout_fwd(int64_t count, int64_t first, const double *x, int act,
+                            double drop_p, uint32_t seed, double *y);
+void oracle_act_dropout_bwd(int64_t count, int64_t first, const double *dy, const double *x,
+                            int act, double drop_p, uint32_t seed, double *dx);
 
 #ifdef __cplusplus
 }

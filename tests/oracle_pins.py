@@ -567,6 +567,21 @@ def pin_dropout_keep_rate(o):
     assert not o.dropout_mask(1000, 1.0, 3).any()
 
 
+def pin_dropout_window_is_slice(o):
+    """A window of elements starting at `first` gets the flags and values of
+    that slice of the whole tensor (the random value belongs to the element's
+    offset in the tensor)."""
+    x = _rng(45).normal(size=1000)
+    full_mask = o.dropout_mask(1000, 0.3, 21)
+    full_y = o.act_dropout_fwd(x, 2, 0.3, 21)
+    full_dx = o.act_dropout_bwd(np.ones(1000), x, 2, 0.3, 21)
+    for first in (0, 1, 3, 4, 517):
+        assert (o.dropout_mask(1000 - first, 0.3, 21, first=first) == full_mask[first:]).all()
+        assert (o.act_dropout_fwd(x[first:], 2, 0.3, 21, first=first) == full_y[first:]).all()
+        assert (o.act_dropout_bwd(np.ones(1000 - first), x[first:], 2, 0.3, 21, first=first)
+                == full_dx[first:]).all()
+
+
 def pin_dropout_independence(o):
     """Neighbouring elements (the same generator call), elements four apart (the
     next counter) and two seeds agree as often as independent fair coins do."""

@@ -102,6 +102,16 @@ P = 1 << 20  # a fake, aligned, non-null address: never dereferenced (validation
     # a channel with 2^31 elements
     (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, None, None, None, None, None,
                                    1 << 16, 1, 1 << 15, 1e-5, 0.1, 1, 0, 0, None, 0, None), 2),
+    # channels-first LayerNorm with no channels
+    (lambda L: L.nrm_layernorm_cf_fwd(P, None, None, P * 2, None, None, 2, 0, 5, 1e-5, 0, None), 1),
+    # dropout probability above 1, NaN, negative count, unknown activation, null y
+    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 2, 1.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 2, float("nan"), 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, -1, 2, 0.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, 16, 9, 0.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_fwd(P, None, 16, 2, 0.5, 7, 1, None), 1),
+    # element-misaligned fp16 pointer
+    (lambda L: L.nrm_act_dropout_fwd(P + 1, P * 2, 16, 2, 0.5, 7, 1, None), 1),
 ])
 def test_bad_arguments_are_rejected_on_the_host(lib, call, expect):
     assert call(lib) == expect

@@ -55,12 +55,13 @@ MUTATIONS = {
     "philox_no_key_schedule": ("        k0 += 0x9E3779B9u;\n", ""),
     "philox_hi_lo_swapped": ("uint32_t n1 = (uint32_t)p1;", "uint32_t n1 = (uint32_t)(p1 >> 32);"),
     "dropout_scale_not_inverted": ("? a / (1.0 - drop_p) : 0.0;", "? a * (1.0 - drop_p) : 0.0;"),
+    "dropout_window_ignores_first": ("y[i] = dropout_keep(seed, first + i, drop_p)", "y[i] = dropout_keep(seed, i, drop_p)"),
     "dropout_keep_flipped": ("return !(u < (float)drop_p);", "return u < (float)drop_p;"),
     "dropout_one_word_per_call": ("out[e & 3] >> 8", "out[0] >> 8"),
-    "dropout_bwd_drops_scale": ("dx[e] = dy[e] / (1.0 - drop_p) * act_derivative(act, x[e]);",
-                                "dx[e] = dy[e] * act_derivative(act, x[e]);"),
-    "dropout_bwd_mask_ignored": ("        if (dropout_keep(seed, e, drop_p))\n            dx[e]",
-                                 "        if (1)\n            dx[e]"),
+    "dropout_bwd_drops_scale": ("dx[i] = dy[i] / (1.0 - drop_p) * act_derivative(act, x[i]);",
+                                "dx[i] = dy[i] * act_derivative(act, x[i]);"),
+    "dropout_bwd_mask_ignored": ("        if (dropout_keep(seed, first + i, drop_p))\n            dx[i]",
+                                 "        if (1)\n            dx[i]"),
 }
 
 
