@@ -8,13 +8,15 @@
 // Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3",
 // SC 2011), keyed by (seed, 0) with counter (e / 4, 0, 0); element e takes
 // output word e % 4 and is dropped when (word >> 8) * 2^-24 < p, tested here as
-// the integer comparison (word >> 8) < ceil(p * 2^24), which decides the same.
+// the integer comparison word < ceil(p * 2^24) * 2^8, which decides the same
+// (p = 1 drops everything and is a zero fill).
 //
-// GB300 design: an HBM-streaming elementwise kernel.  A persistent grid of
-// 256-thread CTAs walks the tensor in 16-byte vectors, two per thread per
-// iteration so that two loads are in flight before any arithmetic; one
-// generator call covers four elements (its four output words).  Tensors that
-// are not 16-byte aligned take a scalar kernel over groups of four elements.
+// GB300 design: an elementwise kernel over 16-byte vectors; a persistent grid
+// of 256-thread CTAs walks the tensor, one vector per thread per iteration.
+// One generator call covers four elements (its four output words).  With
+// GELU, SiLU or Mish the kernel is bound by instruction issue (ten Philox
+// rounds per four elements plus the activation), not by HBM.  Tensors that are
+// not 16-byte aligned take a scalar kernel over groups of four elements.
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -27,7 +29,9 @@
 namespace nrm {
 
 constexpr int kDropThreads = 256;
-constexpr int kDropUnroll = 2;  // 16-byte vectors per thread and iteration
+constexpr int kDropUnroll = 1;  // 16-byte vectors per thread and iteration (2 and 4 measured slower)
+
+constexpr int kPhiloxRounds = 10;
 
 struct DropArgs {
     const void* x;
@@ -35,36 +39,40 @@ struct DropArgs {
     void* y;
     void* dx;
     int64_t count;
-    uint32_t seed;
-    uint32_t thresh;  // ceil(p * 2^24): element kept when (word >> 8) >= thresh
-    float scale;      // 1 / (1 - p) (0 when p = 1)
+    // the key of each round: (seed, 0) advanced by the Weyl increments, computed
+    // on the host (the key depends on the seed alone), read from the constant bank
+    uint32_t rk0[kPhiloxRounds];
+    uint32_t rk1[kPhiloxRounds];
+    uint32_t thresh_w;  // ceil(p * 2^24) << 8: element kept when its word >= thresh_w (p < 1)
+    int drop_all;       // p == 1: every element dropped
+    float scale;        // 1 / (1 - p)
 };
 
-// Philox4x32 with 10 rounds on counter c and key (k0, k1).
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// Philox4x32 with 10 rounds on counter c, with the round keys of `a`.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const DropArgs& a) {
 #pragma unroll
-    for (int r = 0; r < 10; ++r) {
+    for (int r = 0; r < kPhiloxRounds; ++r) {
         const uint64_t p0 = uint64_t(0xD2511F53u) * c.x;
         const uint64_t p1 = uint64_t(0xCD9E8D57u) * c.z;
-        c = make_uint4(uint32_t(p1 >> 32) ^ c.y ^ k0, uint32_t(p1), uint32_t(p0 >> 32) ^ c.w ^ k1, uint32_t(p0));
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
+        c = make_uint4(uint32_t(p1 >> 32) ^ c.y ^ a.rk0[r], uint32_t(p1), uint32_t(p0 >> 32) ^ c.w ^ a.rk1[r],
+                       uint32_t(p0));
     }
     return c;
 }
 
 // The four random words of elements 4g .. 4g+3.
-__device__ __forceinline__ uint4 drop_words(uint64_t g, uint32_t seed) {
-    return philox4x32_10(make_uint4(uint32_t(g), uint32_t(g >> 32), 0u, 0u), seed, 0u);
+__device__ __forceinline__ uint4 drop_words(uint64_t g, const DropArgs& a) {
+    return philox4x32_10(make_uint4(uint32_t(g), uint32_t(g >> 32), 0u, 0u), a);
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& r, int k) {
     return k == 0 ? r.x : (k == 1 ? r.y : (k == 2 ? r.z : r.w));
 }
 
+// (word >> 8) < ceil(p * 2^24)  <=>  word < ceil(p * 2^24) * 2^8, for p < 1
 template <int ACT, bool BWD>
 __device__ __forceinline__ float drop_elem(float xv, float dyv, uint32_t word, const DropArgs& a) {
-    if ((word >> 8) < a.thresh) return 0.f;
+    if (word < a.thresh_w) return 0.f;
     if constexpr (BWD) return dyv * a.scale * act_derivative_c<ACT>(xv);
     else return act_forward_c<ACT>(xv) * a.scale;
 }
@@ -108,7 +116,7 @@ act_dropout_vec_kernel(const DropArgs a) {
                 float o[V];
 #pragma unroll
                 for (int q = 0; q < V / 4; ++q) {
-                    const uint4 r = drop_words(uint64_t(v) * (V / 4) + q, a.seed);
+                    const uint4 r = drop_words(uint64_t(v) * (V / 4) + q, a);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         o[4 * q + k] = drop_elem<ACT, BWD>(xv[u][4 * q + k], BWD ? dv[u][4 * q + k] : 0.f,
@@ -120,7 +128,7 @@ act_dropout_vec_kernel(const DropArgs a) {
     }
     // the tail: fewer than V elements after the last whole vector
     const int64_t e = nvec * V + t0;
-    if (e < a.count) drop_scalar<T, ACT, BWD>(a, e, word_of(drop_words(uint64_t(e) >> 2, a.seed), int(e & 3)));
+    if (e < a.count) drop_scalar<T, ACT, BWD>(a, e, word_of(drop_words(uint64_t(e) >> 2, a), int(e & 3)));
 }
 
 // Any alignment: groups of four elements (one generator call), scalar accesses.
@@ -130,7 +138,7 @@ act_dropout_scalar_kernel(const DropArgs a) {
     const int64_t groups = (a.count + 3) / 4;
     const int64_t stride = int64_t(gridDim.x) * kDropThreads;
     for (int64_t g = int64_t(blockIdx.x) * kDropThreads + threadIdx.x; g < groups; g += stride) {
-        const uint4 r = drop_words(uint64_t(g), a.seed);
+        const uint4 r = drop_words(uint64_t(g), a);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int64_t e = 4 * g + k;
@@ -144,6 +152,9 @@ nrm_status act_dropout_launch(const DropArgs& a, int act, bool vec, cudaStream_t
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     if (a.count == 0) return NRM_OK;
+    if (a.drop_all)  // p = 1: every output is 0 (the oracle's y = 0, dx = 0)
+        return cuda_status(cudaMemsetAsync(BWD ? a.dx : a.y, 0, size_t(a.count) * sizeof(T), s),
+                           "activation-dropout zero fill");
     const void* fn = with_act(act, [&](auto tag) {
         constexpr int A = decltype(tag)::value;
         return vec ? (const void*)&act_dropout_vec_kernel<T, A, BWD>
@@ -170,10 +181,18 @@ nrm_status act_dropout(const void* x, const void* dy, void* out, int64_t count, 
     a.y = bwd ? nullptr : out;
     a.dx = bwd ? out : nullptr;
     a.count = count;
-    a.seed = seed;
+    uint32_t k0 = seed, k1 = 0u;
+    for (int r = 0; r < kPhiloxRounds; ++r) {
+        a.rk0[r] = k0;
+        a.rk1[r] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
     // p * 2^24 is exact in double; its ceiling is the smallest 24-bit value kept
-    a.thresh = uint32_t(std::ceil(double(p) * 16777216.0));
-    a.scale = p < 1.f ? float(1.0 / (1.0 - double(p))) : 0.f;
+    const uint32_t thresh = uint32_t(std::ceil(double(p) * 16777216.0));
+    a.drop_all = thresh >= (1u << 24);
+    a.thresh_w = a.drop_all ? 0u : thresh << 8;
+    a.scale = a.drop_all ? 0.f : float(1.0 / (1.0 - double(p)));
     switch (dt) {
     case NRM_F32:
         return bwd ? act_dropout_launch<float, true>(a, act, vec, s) : act_dropout_launch<float, false>(a, act, vec, s);
