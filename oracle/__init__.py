@@ -25,7 +25,7 @@ _SRC = os.path.join(_HERE, "norm_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
-ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU, ACT_MISH = 0, 1, 2, 3, 4
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU, ACT_MISH, ACT_LEAKY_RELU, ACT_ELU = 0, 1, 2, 3, 4, 5, 6
 
 # -ffp-contract=off keeps a*b+c as two roundings on every host (gcc fuses them by
 # default on aarch64), so the oracle gives the same bits here and on the GPU machine.
@@ -83,18 +83,18 @@ class Oracle:
         lib.oracle_rmsnorm_bwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D]
         lib.oracle_batchnorm_fwd.argtypes = [_I64, _I64, _I64, _D, _D, _D, _D,
                                              ctypes.c_double, ctypes.c_double,
-                                             ctypes.c_int, ctypes.c_int, _D, _D,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_double, _D, _D,
                                              _D, _D, _D, _U32, _D]
         lib.oracle_batchnorm_bwd.argtypes = [_I64, _I64, _I64, _D, _D, _D, _D, _D,
                                              _D, _D, ctypes.c_double, ctypes.c_int,
-                                             ctypes.c_int, _U32, _D, _D, _D, _D]
+                                             ctypes.c_int, ctypes.c_double, _U32, _D, _D, _D, _D]
         _U8 = ctypes.POINTER(ctypes.c_uint8)
         lib.oracle_philox4x32_10.argtypes = [_U32, _U32, _U32]
         lib.oracle_dropout_mask.argtypes = [_I64, _I64, ctypes.c_double, ctypes.c_uint32, _U8]
         lib.oracle_act_dropout_fwd.argtypes = [_I64, _I64, _D, ctypes.c_int, ctypes.c_double,
-                                               ctypes.c_uint32, _D]
+                                               ctypes.c_double, ctypes.c_uint32, _D]
         lib.oracle_act_dropout_bwd.argtypes = [_I64, _I64, _D, _D, ctypes.c_int, ctypes.c_double,
-                                               ctypes.c_uint32, _D]
+                                               ctypes.c_double, ctypes.c_uint32, _D]
         for f in ("oracle_layernorm_fwd", "oracle_layernorm_bwd", "oracle_layernorm_cf_fwd",
                   "oracle_layernorm_cf_bwd", "oracle_rmsnorm_fwd",
                   "oracle_rmsnorm_bwd", "oracle_batchnorm_fwd", "oracle_batchnorm_bwd",
@@ -177,7 +177,7 @@ class Oracle:
 
     def batchnorm_fwd(self, x, res=None, w=None, b=None, eps=1e-5, momentum=0.1,
                       training=True, act=ACT_NONE, running_mean=None,
-                      running_var=None, want_mask=False, want_z=False):
+                      running_var=None, want_mask=False, want_z=False, act_param=0.0):
         """x: [n, c, l].  Returns a dict with y, save_mean, save_rstd,
         running_mean, running_var (updated copies, or None), mask (uint32 or
         None) and z (pre-activation, or None)."""
@@ -192,7 +192,7 @@ class Oracle:
         mask = np.zeros(self.mask_words(n, c, l), dtype=np.uint32) if want_mask else None
         z = np.empty_like(x) if want_z else None
         self.lib.oracle_batchnorm_fwd(n, c, l, _ptr(x), _ptr(res), _ptr(w), _ptr(b),
-                                      eps, momentum, int(bool(training)), int(act),
+                                      eps, momentum, int(bool(training)), int(act), float(act_param),
                                       _ptr(rm), _ptr(rv), _ptr(y), _ptr(sm), _ptr(sr),
                                       _ptr(mask, _U32), _ptr(z))
         return dict(y=y, save_mean=sm, save_rstd=sr, running_mean=rm,
@@ -200,7 +200,7 @@ class Oracle:
 
     def batchnorm_bwd(self, dy, x, res=None, w=None, b=None, running_mean=None,
                       running_var=None, eps=1e-5, training=True, act=ACT_NONE,
-                      mask=None):
+                      mask=None, act_param=0.0):
         """Returns (dx, dres, dw, db)."""
         dy, x = _f64(dy), _f64(x)
         n, c, l = x.shape
@@ -213,7 +213,7 @@ class Oracle:
         db = np.empty(c)
         self.lib.oracle_batchnorm_bwd(n, c, l, _ptr(dy), _ptr(x), _ptr(res), _ptr(w),
                                       _ptr(b), _ptr(rm), _ptr(rv), eps,
-                                      int(bool(training)), int(act), _ptr(mask, _U32),
+                                      int(bool(training)), int(act), float(act_param), _ptr(mask, _U32),
                                       _ptr(dx), _ptr(dres), _ptr(dw), _ptr(db))
         return dx, dres, dw, db
 
@@ -235,20 +235,22 @@ class Oracle:
                                      keep.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
         return keep
 
-    def act_dropout_fwd(self, x, act, drop_p, seed, first=0):
+    def act_dropout_fwd(self, x, act, drop_p, seed, first=0, act_param=0.0):
         """y = act(x) / (1 - p) where kept, 0 where dropped; x (flattened) holds
         the tensor's elements first, first+1, ..."""
         x = _f64(x)
         y = np.empty_like(x)
-        self.lib.oracle_act_dropout_fwd(x.size, int(first), _ptr(x), int(act), float(drop_p),
+        self.lib.oracle_act_dropout_fwd(x.size, int(first), _ptr(x), int(act), float(act_param),
+                                        float(drop_p),
                                         int(seed) & 0xFFFFFFFF, _ptr(y))
         return y
 
-    def act_dropout_bwd(self, dy, x, act, drop_p, seed, first=0):
+    def act_dropout_bwd(self, dy, x, act, drop_p, seed, first=0, act_param=0.0):
         """dx = dy / (1 - p) * act'(x) where kept, 0 where dropped."""
         dy, x = _f64(dy), _f64(x)
         dx = np.empty_like(x)
-        self.lib.oracle_act_dropout_bwd(x.size, int(first), _ptr(dy), _ptr(x), int(act), float(drop_p),
+        self.lib.oracle_act_dropout_bwd(x.size, int(first), _ptr(dy), _ptr(x), int(act),
+                                        float(act_param), float(drop_p),
                                         int(seed) & 0xFFFFFFFF, _ptr(dx))
         return dx
 

@@ -27,6 +27,9 @@
  *   - The residual is added after the affine step and before the activation; its
  *     gradient is the pre-activation gradient itself.
  *   - ReLU'(z) = 1 for z > 0 and 0 otherwise; GELU is the exact erf form.
+ *   - The activations with a parameter a (the article encodes it in the name):
+ *     leaky_relu(z) = z for z > 0, else a*z (derivative 1, else a);
+ *     elu(z) = z for z > 0, else a*(e^z - 1) (derivative 1, else a*e^z).
  *   - Dropout draws Philox4x32-10 with key (seed, 0) and counter (e / 4, 0, 0) for
  *     element e, which takes output word e % 4 as the uniform (word >> 8) * 2^-24;
  *     the element is dropped when that value is below drop_p (single precision).
@@ -271,10 +274,12 @@ void oracle_layernorm_cf_bwd(int64_t n, int64_t c, int64_t l, const double *dy,
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
 static double softplus(double z) { return z > 0.0 ? z + log1p(exp(-z)) : log1p(exp(z)); }
 
-static double act_forward(int act, double z)
+static double act_forward(int act, double param, double z)
 {
     switch (act) {
     case ORACLE_ACT_RELU: return z > 0.0 ? z : 0.0;
+    case ORACLE_ACT_LEAKY_RELU: return z > 0.0 ? z : param * z;
+    case ORACLE_ACT_ELU: return z > 0.0 ? z : param * expm1(z);
     case ORACLE_ACT_GELU: return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
     case ORACLE_ACT_SILU: return z * sigmoid(z);
     case ORACLE_ACT_MISH: return z * tanh(softplus(z));
@@ -282,10 +287,12 @@ static double act_forward(int act, double z)
     }
 }
 
-static double act_derivative(int act, double z)
+static double act_derivative(int act, double param, double z)
 {
     switch (act) {
     case ORACLE_ACT_RELU: return z > 0.0 ? 1.0 : 0.0;
+    case ORACLE_ACT_LEAKY_RELU: return z > 0.0 ? 1.0 : param;
+    case ORACLE_ACT_ELU: return z > 0.0 ? 1.0 : param * exp(z);
     case ORACLE_ACT_GELU: {
         double cdf = 0.5 * (1.0 + erf(z / sqrt(2.0)));
         double pdf = exp(-0.5 * z * z) / sqrt(2.0 * M_PI);
@@ -328,7 +335,7 @@ static int64_t mask_words_per_segment(int64_t l) { return (l + 31) / 32; }
 void oracle_batchnorm_fwd(int64_t n, int64_t c, int64_t l, const double *x,
                           const double *res, const double *w, const double *b,
                           double eps, double momentum, int training, int act,
-                          double *running_mean, double *running_var,
+                          double act_param, double *running_mean, double *running_var,
                           double *y, double *save_mean, double *save_rstd,
                           uint32_t *act_mask, double *z_out)
 {
@@ -373,7 +380,7 @@ void oracle_batchnorm_fwd(int64_t n, int64_t c, int64_t l, const double *x,
                 double z = (x[e] - mu) * rs * wc + bc;
                 if (res) z += res[e];
                 if (z_out) z_out[e] = z;
-                y[e] = act_forward(act, z);
+                y[e] = act_forward(act, act_param, z);
                 if (act_mask && act == ORACLE_ACT_RELU && z > 0.0)
                     act_mask[(i * c + ch) * words + j / 32] |= (uint32_t)1u << (j % 32);
             }
@@ -395,7 +402,7 @@ void oracle_batchnorm_bwd(int64_t n, int64_t c, int64_t l, const double *dy,
                           const double *x, const double *res, const double *w,
                           const double *b, const double *running_mean,
                           const double *running_var, double eps, int training,
-                          int act, const uint32_t *act_mask, double *dx,
+                          int act, double act_param, const uint32_t *act_mask, double *dx,
                           double *dres, double *dw, double *db)
 {
     const int64_t m = n * l;
@@ -434,7 +441,7 @@ void oracle_batchnorm_bwd(int64_t n, int64_t c, int64_t l, const double *dy,
                 if (act == ORACLE_ACT_RELU && act_mask)
                     d = (act_mask[(i * c + ch) * words + j / 32] >> (j % 32)) & 1u ? 1.0 : 0.0;
                 else
-                    d = act_derivative(act, z);
+                    d = act_derivative(act, act_param, z);
                 double dz = dy[e] * d;
                 if (dres) dres[e] = dz;
                 sum_dz += dz;
@@ -453,7 +460,7 @@ void oracle_batchnorm_bwd(int64_t n, int64_t c, int64_t l, const double *dy,
                 if (act == ORACLE_ACT_RELU && act_mask)
                     d = (act_mask[(i * c + ch) * words + j / 32] >> (j % 32)) & 1u ? 1.0 : 0.0;
                 else
-                    d = act_derivative(act, z);
+                    d = act_derivative(act, act_param, z);
                 double dz = dy[e] * d;
                 if (training)
                     dx[e] = wc * rs * (dz - sum_dz / (double)m - xhat * sum_dz_xhat / (double)m);
@@ -528,10 +535,10 @@ void oracle_dropout_mask(int64_t count, int64_t first, double drop_p, uint32_t s
  * result goes through dropout in the same pass: y = act(x) / (1 - p) where kept,
  * 0 where dropped. */
 void oracle_act_dropout_fwd(int64_t count, int64_t first, const double *x, int act,
-                            double drop_p, uint32_t seed, double *y)
+                            double act_param, double drop_p, uint32_t seed, double *y)
 {
     for (int64_t i = 0; i < count; ++i) {
-        double a = act_forward(act, x[i]);
+        double a = act_forward(act, act_param, x[i]);
         y[i] = dropout_keep(seed, first + i, drop_p) ? a / (1.0 - drop_p) : 0.0;
     }
 }
@@ -541,11 +548,12 @@ void oracle_act_dropout_fwd(int64_t count, int64_t first, const double *x, int a
  * scale) and is multiplied by the activation's derivative at the saved input:
  * dx = dy / (1 - p) * act'(x) where kept, 0 where dropped. */
 void oracle_act_dropout_bwd(int64_t count, int64_t first, const double *dy, const double *x,
-                            int act, double drop_p, uint32_t seed, double *dx)
+                            int act, double act_param, double drop_p, uint32_t seed,
+                            double *dx)
 {
     for (int64_t i = 0; i < count; ++i) {
         if (dropout_keep(seed, first + i, drop_p))
-            dx[i] = dy[i] / (1.0 - drop_p) * act_derivative(act, x[i]);
+            dx[i] = dy[i] / (1.0 - drop_p) * act_derivative(act, act_param, x[i]);
         else
             dx[i] = 0.0;
     }

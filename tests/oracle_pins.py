@@ -28,7 +28,10 @@ import os
 import numpy as np
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-ACT = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "mish": 4}
+ACT = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "mish": 4, "leaky_relu": 5, "elu": 6}
+# the parameter the activations that take one are exercised with (slope, alpha)
+ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3}
+ALL_ACTS = tuple(ACT)
 
 
 def _rng(seed):
@@ -288,6 +291,10 @@ def _torch_bn_forward(x, res, w, b, rm, rv, eps, momentum, training, act):
         return F.silu(z)
     if act == "mish":
         return F.mish(z)
+    if act == "leaky_relu":
+        return F.leaky_relu(z, ACT_PARAM[act])
+    if act == "elu":
+        return F.elu(z, ACT_PARAM[act])
     return z
 
 
@@ -296,7 +303,7 @@ def pin_batchnorm_vs_torch(o):
     r = _rng(12)
     n, c, l = 3, 4, 7
     for training in (True, False):
-        for act in ("none", "relu", "gelu", "silu", "mish"):
+        for act in ALL_ACTS:
             for with_res in (False, True):
                 x = r.normal(size=(n, c, l)) * 1.7 + 0.4
                 res = r.normal(size=(n, c, l)) if with_res else None
@@ -308,7 +315,8 @@ def pin_batchnorm_vs_torch(o):
                 rv_t = torch.from_numpy(rv0.copy())
                 yt = _torch_bn_forward(x, res, w, b, rm_t, rv_t, 1e-5, 0.1, training, act).numpy()
                 out = o.batchnorm_fwd(x, res, w, b, eps=1e-5, momentum=0.1, training=training,
-                                      act=ACT[act], running_mean=rm0, running_var=rv0)
+                                      act=ACT[act], running_mean=rm0, running_var=rv0,
+                                      act_param=ACT_PARAM.get(act, 0.0))
                 tag = f"batchnorm training={training} act={act} res={with_res}"
                 _close(out["y"], yt, 1e-12, 1e-12, tag + " y vs torch")
                 _close(out["running_mean"], rm_t.numpy(), 1e-13, 1e-15, tag + " running_mean")
@@ -351,6 +359,24 @@ def pin_silu_mish_values(o):
     _close(dx_mish[0], 0.6, 1e-15, 1e-16, "mish'(0)")
 
 
+def pin_leaky_relu_elu_values(o):
+    # z = x as above; closed forms: leaky(-2) = -2a, elu(-ln 2) = -a/2,
+    # elu'(-ln 2) = a/2, leaky'(z < 0) = a, both derivatives 1 for z > 0
+    z = np.array([-2.0, -math.log(2.0), 0.5]).reshape(1, 1, 3)
+    rm, rv = np.zeros(1), np.array([0.75])
+    for act, a in (("leaky_relu", 0.2), ("elu", 1.7)):
+        y = o.batchnorm_fwd(z, eps=0.25, training=False, act=ACT[act], running_mean=rm,
+                            running_var=rv, act_param=a)["y"].ravel()
+        dx = o.batchnorm_bwd(np.ones_like(z), z, None, np.ones(1), np.zeros(1), rm, rv, eps=0.25,
+                             training=False, act=ACT[act], act_param=a)[0].ravel()
+        if act == "leaky_relu":
+            _close(y, [-2.0 * a, -math.log(2.0) * a, 0.5], 1e-15, 0, "leaky_relu values")
+            _close(dx, [a, a, 1.0], 1e-15, 0, "leaky_relu derivative")
+        else:
+            _close(y[1:], [-a / 2.0, 0.5], 1e-15, 1e-16, "elu values")
+            _close(dx[1:], [a / 2.0, 1.0], 1e-15, 1e-16, "elu derivative")
+
+
 def pin_batchnorm_mask_layout(o):
     # eval mode, z = x: mask bit (i, ch, j) must be x > 0 with the documented layout
     n, c, l = 2, 3, 70
@@ -377,7 +403,7 @@ def _bn_inputs_away_from_kinks(r, n, c, l, act, with_res):
         res = r.normal(size=(n, c, l)) if with_res else None
         w = 1 + 0.3 * r.normal(size=c)
         b = 0.3 * r.normal(size=c)
-        if act != "relu":
+        if act not in ("relu", "leaky_relu"):
             return x, res, w, b
         xc = x.transpose(1, 0, 2).reshape(c, -1)
         mu = xc.mean(1)[None, :, None]
@@ -393,7 +419,7 @@ def pin_batchnorm_bwd_fd(o):
     eps = 1e-3
     for (n, c, l) in ((2, 3, 4), (3, 2, 5)):
         for training in (True, False):
-            for act in ("none", "relu", "gelu", "silu", "mish"):
+            for act in ALL_ACTS:
                 for with_res in (False, True):
                     x, res, w, b = _bn_inputs_away_from_kinks(r, n, c, l, act, with_res)
                     dy = r.normal(size=(n, c, l))
@@ -403,10 +429,12 @@ def pin_batchnorm_bwd_fd(o):
                     def loss():
                         y = o.batchnorm_fwd(x, res, w, b, eps=eps, momentum=0.1,
                                             training=training, act=ACT[act],
-                                            running_mean=rm, running_var=rv)["y"]
+                                            running_mean=rm, running_var=rv,
+                                            act_param=ACT_PARAM.get(act, 0.0))["y"]
                         return float((dy * y).sum())
                     dx, dres, dw, db = o.batchnorm_bwd(dy, x, res, w, b, rm, rv, eps=eps,
-                                                       training=training, act=ACT[act])
+                                                       training=training, act=ACT[act],
+                                                       act_param=ACT_PARAM.get(act, 0.0))
                     tag = f"batchnorm bwd training={training} act={act} res={with_res}"
                     h = 1e-6
                     _close(dx, _central_diff(loss, x, h), 1e-6, 1e-7, tag + " dx vs FD")
@@ -443,7 +471,7 @@ def pin_batchnorm_bwd_vs_torch(o):
     r = _rng(16)
     n, c, l = 3, 4, 6
     acts = {"none": lambda z: z, "gelu": lambda z: F.gelu(z, approximate="none"), "silu": F.silu,
-            "mish": F.mish}
+            "mish": F.mish, "elu": lambda z: F.elu(z, ACT_PARAM["elu"])}
     for training in (True, False):
         for act in acts:
             x = torch.tensor(r.normal(size=(n, c, l)) * 1.5, requires_grad=True)
@@ -459,7 +487,8 @@ def pin_batchnorm_bwd_vs_torch(o):
             y.backward(torch.from_numpy(dy))
             dx, dres, dw, db = o.batchnorm_bwd(dy, x.detach().numpy(), res.detach().numpy(),
                                                w.detach().numpy(), b.detach().numpy(), rm, rv,
-                                               eps=1e-5, training=training, act=ACT[act])
+                                               eps=1e-5, training=training, act=ACT[act],
+                                               act_param=ACT_PARAM.get(act, 0.0))
             tag = f"batchnorm bwd vs torch training={training} act={act}"
             _close(dx, x.grad.numpy(), 1e-10, 1e-12, tag + " dx")
             _close(dres, res.grad.numpy(), 1e-10, 1e-12, tag + " dres")
@@ -596,17 +625,20 @@ def pin_dropout_independence(o):
 
 
 def _act_torch():
+    """act code -> (torch function, the parameter passed to the oracle)."""
     import torch
     import torch.nn.functional as F
-    return {0: lambda t: t, 1: torch.relu, 2: F.gelu, 3: F.silu, 4: F.mish}
+    lk, al = ACT_PARAM["leaky_relu"], ACT_PARAM["elu"]
+    return {0: (lambda t: t, 0.0), 1: (torch.relu, 0.0), 2: (F.gelu, 0.0), 3: (F.silu, 0.0),
+            4: (F.mish, 0.0), 5: (lambda t: F.leaky_relu(t, lk), lk), 6: (lambda t: F.elu(t, al), al)}
 
 
 def pin_act_dropout_no_drop_is_activation(o):
     """p = 0: the kernel is the plain activation (torch's reference functions)."""
     import torch
     x = _rng(40).normal(size=4096) * 3
-    for act, fn in _act_torch().items():
-        y = o.act_dropout_fwd(x, act, 0.0, 9)
+    for act, (fn, prm) in _act_torch().items():
+        y = o.act_dropout_fwd(x, act, 0.0, 9, act_param=prm)
         _close(y, fn(torch.from_numpy(x)).numpy(), 1e-15, 1e-14, f"act {act} without dropout")
 
 
@@ -617,8 +649,8 @@ def pin_act_dropout_inverted_scale(o):
     x = _rng(41).normal(size=20000) * 2
     p = 0.25
     keep = o.dropout_mask(x.size, p, 4321).astype(bool)
-    for act, fn in _act_torch().items():
-        y = o.act_dropout_fwd(x, act, p, 4321)
+    for act, (fn, prm) in _act_torch().items():
+        y = o.act_dropout_fwd(x, act, p, 4321, act_param=prm)
         a = fn(torch.from_numpy(x)).numpy()
         _close(y[keep], a[keep] / (1 - p), 1e-15, 1e-14, f"act {act} kept elements")
         assert not y[~keep].any(), f"act {act}: dropped elements must be 0"
@@ -634,11 +666,11 @@ def pin_act_dropout_bwd_fd(o):
     x = r.normal(size=64) * 2
     x = np.where(np.abs(x) < 0.05, 0.3, x)  # keep ReLU's kink out of the stencil
     dy = r.normal(size=64)
-    for act in (0, 1, 2, 3, 4):
+    for act, (_, prm) in _act_torch().items():
         for p in (0.0, 0.3):
             def loss():
-                return float((dy * o.act_dropout_fwd(x, act, p, 11)).sum())
-            dx = o.act_dropout_bwd(dy, x, act, p, 11)
+                return float((dy * o.act_dropout_fwd(x, act, p, 11, act_param=prm)).sum())
+            dx = o.act_dropout_bwd(dy, x, act, p, 11, act_param=prm)
             _close(dx, _central_diff(loss, x, 1e-6), 1e-7, 1e-7, f"act {act} p {p} dx vs FD")
 
 
@@ -650,11 +682,11 @@ def pin_act_dropout_bwd_vs_torch(o):
     dy = r.normal(size=5000)
     p = 0.4
     keep = torch.from_numpy(o.dropout_mask(5000, p, 999).astype(np.float64))
-    for act, fn in _act_torch().items():
+    for act, (fn, prm) in _act_torch().items():
         if x.grad is not None:
             x.grad = None
         (fn(x) * keep / (1 - p)).backward(torch.from_numpy(dy))
-        dx = o.act_dropout_bwd(dy, x.detach().numpy(), act, p, 999)
+        dx = o.act_dropout_bwd(dy, x.detach().numpy(), act, p, 999, act_param=prm)
         _close(dx, x.grad.numpy(), 1e-14, 1e-13, f"act {act} dx vs torch")
 
 

@@ -33,8 +33,16 @@ MUTATIONS = {
     "bn_momentum_swapped": ("(1.0 - momentum) * running_mean[ch] + momentum * mu",
                             "momentum * running_mean[ch] + (1.0 - momentum) * mu"),
     "bn_residual_after_activation": (
-        "y[e] = act_forward(act, z);",
-        "y[e] = act_forward(act, z - (res ? res[e] : 0.0)) + (res ? res[e] : 0.0);"),
+        "y[e] = act_forward(act, act_param, z);",
+        "y[e] = act_forward(act, act_param, z - (res ? res[e] : 0.0)) + (res ? res[e] : 0.0);"),
+    "leaky_relu_slope_on_positive_side": ("case ORACLE_ACT_LEAKY_RELU: return z > 0.0 ? z : param * z;",
+                                          "case ORACLE_ACT_LEAKY_RELU: return z > 0.0 ? param * z : z;"),
+    "leaky_relu_grad_ignores_slope": ("case ORACLE_ACT_LEAKY_RELU: return z > 0.0 ? 1.0 : param;",
+                                      "case ORACLE_ACT_LEAKY_RELU: return z > 0.0 ? 1.0 : 0.0;"),
+    "elu_without_minus_one": ("case ORACLE_ACT_ELU: return z > 0.0 ? z : param * expm1(z);",
+                              "case ORACLE_ACT_ELU: return z > 0.0 ? z : param * exp(z);"),
+    "elu_grad_drops_exp": ("case ORACLE_ACT_ELU: return z > 0.0 ? 1.0 : param * exp(z);",
+                           "case ORACLE_ACT_ELU: return z > 0.0 ? 1.0 : param;"),
     "bn_gelu_grad_drops_pdf_term": ("return cdf + z * pdf;", "return cdf;"),
     "bn_relu_grad_at_zero": ("case ORACLE_ACT_RELU: return z > 0.0 ? 1.0 : 0.0;",
                              "case ORACLE_ACT_RELU: return z >= 0.0 ? 1.0 : 0.0;"),
@@ -58,8 +66,8 @@ MUTATIONS = {
     "dropout_window_ignores_first": ("y[i] = dropout_keep(seed, first + i, drop_p)", "y[i] = dropout_keep(seed, i, drop_p)"),
     "dropout_keep_flipped": ("return !(u < (float)drop_p);", "return u < (float)drop_p;"),
     "dropout_one_word_per_call": ("out[e & 3] >> 8", "out[0] >> 8"),
-    "dropout_bwd_drops_scale": ("dx[i] = dy[i] / (1.0 - drop_p) * act_derivative(act, x[i]);",
-                                "dx[i] = dy[i] * act_derivative(act, x[i]);"),
+    "dropout_bwd_drops_scale": ("dx[i] = dy[i] / (1.0 - drop_p) * act_derivative(act, act_param, x[i]);",
+                                "dx[i] = dy[i] * act_derivative(act, act_param, x[i]);"),
     "dropout_bwd_mask_ignored": ("        if (dropout_keep(seed, first + i, drop_p))\n            dx[i]",
                                  "        if (1)\n            dx[i]"),
 }
