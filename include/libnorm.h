@@ -76,13 +76,19 @@ typedef enum nrm_dtype { NRM_F32 = 0, NRM_F16 = 1, NRM_BF16 = 2 } nrm_dtype;
  * for the derivative taken from the pre-activation input).  ReLU'(0) = 0.
  * GELU is the exact erf form z * Phi(z).  SiLU is z * sigmoid(z); Mish is
  * z * tanh(softplus(z)), softplus(z) = log(1 + e^z) (PyTorch's definitions:
- * the articles name the activations without formulas). */
+ * the articles name the activations without formulas).  Two take a parameter,
+ * passed as act_param (the [AF] article encodes it in the name, e.g.
+ * "leaky_relu_0.01"): LEAKY_RELU is z for z > 0, else act_param*z (derivative
+ * 1, else act_param); ELU is z for z > 0, else act_param*(e^z - 1) (derivative
+ * 1, else act_param*e^z).  act_param is ignored by the others. */
 typedef enum nrm_act {
     NRM_ACT_NONE = 0,
     NRM_ACT_RELU = 1,
     NRM_ACT_GELU = 2,
     NRM_ACT_SILU = 3,
-    NRM_ACT_MISH = 4
+    NRM_ACT_MISH = 4,
+    NRM_ACT_LEAKY_RELU = 5,
+    NRM_ACT_ELU = 6
 } nrm_act;
 
 /* Operations that need a workspace (for nrm_workspace_bytes). */
@@ -258,7 +264,8 @@ NRM_API nrm_status nrm_rmsnorm_bwd(const void *dy, const void *x, const void *w,
  * uint32 words receiving bit (z > 0) per element: segment (i, ch) owns
  * ceil(l/32) words starting at word (i*c + ch)*ceil(l/32) and element j of the
  * segment is bit j%32 of word j/32 (unused high bits are 0).  It must be NULL
- * for other activations.
+ * for other activations.  act_param: the slope or alpha of LEAKY_RELU / ELU
+ * (finite; ignored otherwise).
  * training requires M >= 2.  eps > 0, 0 <= momentum <= 1.
  */
 NRM_API nrm_status nrm_batchnorm_fwd(const void *x, const void *residual, const float *w,
@@ -266,8 +273,8 @@ NRM_API nrm_status nrm_batchnorm_fwd(const void *x, const void *residual, const 
                              float *running_var, float *save_mean, float *save_rstd,
                              uint32_t *act_mask, int64_t n, int64_t c, int64_t l,
                              float eps, float momentum, int training, nrm_act act,
-                             nrm_dtype dt, void *workspace, size_t workspace_bytes,
-                             nrm_stream_t stream);
+                             float act_param, nrm_dtype dt, void *workspace,
+                             size_t workspace_bytes, nrm_stream_t stream);
 
 /*
  * nrm_batchnorm_bwd -- [NK] BatchNorm section, last sentences: with a fused
@@ -283,16 +290,17 @@ NRM_API nrm_status nrm_batchnorm_fwd(const void *x, const void *residual, const 
  * recompute z (GELU, or ReLU without a mask) when the forward used one.
  * w, b: float32 [c] or NULL (1, 0), as in the forward.  save_mean, save_rstd:
  * float32 [c] from nrm_batchnorm_fwd with the same `training` flag.
- * act_mask: NULL, or the mask the forward wrote (ReLU only).  dres, dw, db may
- * be NULL.  workspace: as for nrm_batchnorm_fwd.
+ * act_mask: NULL, or the mask the forward wrote (ReLU only).  act, act_param:
+ * those of the forward.  dres, dw, db may be NULL.  workspace: as for
+ * nrm_batchnorm_fwd.
  */
 NRM_API nrm_status nrm_batchnorm_bwd(const void *dy, const void *x, const void *residual,
                              const float *w, const float *b, const float *save_mean,
                              const float *save_rstd, const uint32_t *act_mask,
                              void *dx, void *dres, float *dw, float *db, int64_t n,
                              int64_t c, int64_t l, int training, nrm_act act,
-                             nrm_dtype dt, void *workspace, size_t workspace_bytes,
-                             nrm_stream_t stream);
+                             float act_param, nrm_dtype dt, void *workspace,
+                             size_t workspace_bytes, nrm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Activation with fused dropout                                             */
@@ -309,26 +317,29 @@ NRM_API nrm_status nrm_batchnorm_bwd(const void *dy, const void *x, const void *
  * counter (e / 4 as two 32-bit words, 0, 0); element e takes output word e % 4,
  * u = (word >> 8) * 2^-24, and is dropped when u < drop_p (compared in single
  * precision).  x, y: count elements in dt (contiguous; y may equal x).
- * act: NRM_ACT_NONE (plain dropout), RELU, GELU, SILU or MISH.  drop_p in
+ * act: NRM_ACT_NONE (plain dropout) or any activation of nrm_act, with
+ * act_param for LEAKY_RELU and ELU.  drop_p in
  * [0, 1]: 0 keeps every element, 1 drops every one.  Any seed; the article
  * draws a 16-bit one.  One kernel is enqueued (none for count == 0).
  * Errors: NRM_ERR_INVALID_ARG for a negative count, drop_p outside [0, 1] or
- * NaN, an unknown act or dtype, NULL or misaligned pointers with count > 0.
+ * NaN, an unknown act or dtype, a non-finite act_param, NULL or misaligned
+ * pointers with count > 0.
  */
 NRM_API nrm_status nrm_act_dropout_fwd(const void *x, void *y, int64_t count, nrm_act act,
-                               float drop_p, uint32_t seed, nrm_dtype dt, nrm_stream_t stream);
+                               float act_param, float drop_p, uint32_t seed, nrm_dtype dt,
+                               nrm_stream_t stream);
 
 /*
  * nrm_act_dropout_bwd -- same article, section "五、反向传播融合同样成立": the mask
  * is rebuilt from the same seed and offsets and the derivative is taken at the
  * saved input,
  *   dx[e] = dy[e] / (1 - drop_p) * act'(x[e])  if kept,  else 0   (ReLU'(0) = 0).
- * dy, x, dx: count elements in dt (dx may equal dy or x).  act, drop_p, seed:
- * those of the forward.  Errors as nrm_act_dropout_fwd.
+ * dy, x, dx: count elements in dt (dx may equal dy or x).  act, act_param,
+ * drop_p, seed: those of the forward.  Errors as nrm_act_dropout_fwd.
  */
 NRM_API nrm_status nrm_act_dropout_bwd(const void *dy, const void *x, void *dx, int64_t count,
-                               nrm_act act, float drop_p, uint32_t seed, nrm_dtype dt,
-                               nrm_stream_t stream);
+                               nrm_act act, float act_param, float drop_p, uint32_t seed,
+                               nrm_dtype dt, nrm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Helpers                                                                   */

@@ -8,7 +8,8 @@ the ctypes binding of the C ABI (``_binding``, re-exported here under the C
 names) and the seeded synthetic input generator (``synth``).
 """
 from ._binding import (  # noqa: F401
-    ACTS, EXPORTS, LIB_PATH, NRM_ACT_GELU, NRM_ACT_MISH, NRM_ACT_NONE, NRM_ACT_RELU, NRM_ACT_SILU,
+    ACTS, EXPORTS, LIB_PATH, NRM_ACT_ELU, NRM_ACT_GELU, NRM_ACT_LEAKY_RELU, NRM_ACT_MISH, NRM_ACT_NONE,
+    NRM_ACT_RELU, NRM_ACT_SILU,
     NRM_BF16, NRM_ERR_CUDA,
     NRM_ERR_INVALID_ARG, NRM_ERR_TIMEOUT, NRM_ERR_UNSUPPORTED, NRM_ERR_WORKSPACE, NRM_F16,
     NRM_F32, NRM_OK, NRM_OP_LAYERNORM_BWD, NRM_OP_LAYERNORM_CF_BWD, NRM_OP_RMSNORM_BWD, NrmError, batchnorm_workspace, load,

@@ -18,10 +18,11 @@ LIB_PATH = os.path.join(_PKG, "_build", "libnorm.so")
 NRM_OK, NRM_ERR_INVALID_ARG, NRM_ERR_UNSUPPORTED, NRM_ERR_WORKSPACE, NRM_ERR_CUDA, NRM_ERR_TIMEOUT = range(6)
 NRM_F32, NRM_F16, NRM_BF16 = 0, 1, 2
 NRM_ACT_NONE, NRM_ACT_RELU, NRM_ACT_GELU, NRM_ACT_SILU, NRM_ACT_MISH = 0, 1, 2, 3, 4
+NRM_ACT_LEAKY_RELU, NRM_ACT_ELU = 5, 6
 NRM_OP_LAYERNORM_BWD, NRM_OP_RMSNORM_BWD, NRM_OP_LAYERNORM_CF_BWD = 1, 2, 3
 
 ACTS = {"none": NRM_ACT_NONE, "relu": NRM_ACT_RELU, "gelu": NRM_ACT_GELU, "silu": NRM_ACT_SILU,
-        "mish": NRM_ACT_MISH}
+        "mish": NRM_ACT_MISH, "leaky_relu": NRM_ACT_LEAKY_RELU, "elu": NRM_ACT_ELU}
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("nrm_layernorm_fwd", "nrm_layernorm_bwd", "nrm_layernorm_bwd_noalloc",
@@ -67,11 +68,11 @@ def load(path: str | None = None):
         "nrm_rmsnorm_fwd": [_P, _P, _P, _P, _I64, _I64, _F, _I, _P],
         "nrm_rmsnorm_bwd": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, ctypes.c_size_t, _P],
         "nrm_batchnorm_fwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, _I,
-                              _I, _I, _P, ctypes.c_size_t, _P],
+                              _I, _F, _I, _P, ctypes.c_size_t, _P],
         "nrm_batchnorm_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I,
-                              _I, _I, _P, ctypes.c_size_t, _P],
-        "nrm_act_dropout_fwd": [_P, _P, _I64, _I, _F, ctypes.c_uint32, _I, _P],
-        "nrm_act_dropout_bwd": [_P, _P, _P, _I64, _I, _F, ctypes.c_uint32, _I, _P],
+                              _I, _F, _I, _P, ctypes.c_size_t, _P],
+        "nrm_act_dropout_fwd": [_P, _P, _I64, _I, _F, _F, ctypes.c_uint32, _I, _P],
+        "nrm_act_dropout_bwd": [_P, _P, _P, _I64, _I, _F, _F, ctypes.c_uint32, _I, _P],
         "nrm_workspace_bytes": [_I, _I64, _I64, _I],
         "nrm_batchnorm_workspace_bytes": [_I64, _I64, _I64, _I],
         "nrm_act_mask_words": [_I64, _I64, _I64],
@@ -212,23 +213,23 @@ def _ws(workspace):
 
 
 def nrm_batchnorm_fwd(x, residual, w, b, y, running_mean, running_var, save_mean, save_rstd,
-                      act_mask, eps, momentum, training, act, workspace, stream=None):
+                      act_mask, eps, momentum, training, act, workspace, stream=None, act_param=0.0):
     n, c, l = _ncl(x)
     _check(load().nrm_batchnorm_fwd(_ptr(x), _ptr(residual), _ptr(w), _ptr(b), _ptr(y),
                                     _ptr(running_mean), _ptr(running_var), _ptr(save_mean),
                                     _ptr(save_rstd), _ptr(act_mask), n, c, l, eps, momentum,
-                                    int(bool(training)), _act(act), _dtype_code(x),
+                                    int(bool(training)), _act(act), float(act_param), _dtype_code(x),
                                     _ptr(workspace), _ws(workspace), _stream(stream)),
            "nrm_batchnorm_fwd")
 
 
 def nrm_batchnorm_bwd(dy, x, residual, w, b, save_mean, save_rstd, act_mask, dx, dres, dw, db,
-                      training, act, workspace, stream=None):
+                      training, act, workspace, stream=None, act_param=0.0):
     n, c, l = _ncl(x)
     _check(load().nrm_batchnorm_bwd(_ptr(dy), _ptr(x), _ptr(residual), _ptr(w), _ptr(b),
                                     _ptr(save_mean), _ptr(save_rstd), _ptr(act_mask), _ptr(dx),
                                     _ptr(dres), _ptr(dw), _ptr(db), n, c, l,
-                                    int(bool(training)), _act(act), _dtype_code(x),
+                                    int(bool(training)), _act(act), float(act_param), _dtype_code(x),
                                     _ptr(workspace), _ws(workspace), _stream(stream)),
            "nrm_batchnorm_bwd")
 
@@ -249,16 +250,17 @@ def nrm_workspace_bytes(op: int, rows: int, cols: int, dtype_code: int) -> int:
     return int(load().nrm_workspace_bytes(op, rows, cols, dtype_code))
 
 
-def nrm_act_dropout_fwd(x, y, act, drop_p, seed, stream=None):
+def nrm_act_dropout_fwd(x, y, act, drop_p, seed, stream=None, act_param=0.0):
     """y = act(x) / (1 - drop_p) where kept, else 0 (mask rebuilt from seed and offset)."""
-    _check(load().nrm_act_dropout_fwd(_ptr(x), _ptr(y), x.numel(), _act(act), float(drop_p),
+    _check(load().nrm_act_dropout_fwd(_ptr(x), _ptr(y), x.numel(), _act(act), float(act_param), float(drop_p),
                                       int(seed) & 0xFFFFFFFF, _dtype_code(x), _stream(stream)),
            "nrm_act_dropout_fwd")
 
 
-def nrm_act_dropout_bwd(dy, x, dx, act, drop_p, seed, stream=None):
+def nrm_act_dropout_bwd(dy, x, dx, act, drop_p, seed, stream=None, act_param=0.0):
     """dx = dy / (1 - drop_p) * act'(x) where kept, else 0."""
-    _check(load().nrm_act_dropout_bwd(_ptr(dy), _ptr(x), _ptr(dx), x.numel(), _act(act), float(drop_p),
+    _check(load().nrm_act_dropout_bwd(_ptr(dy), _ptr(x), _ptr(dx), x.numel(), _act(act), float(act_param),
+                                      float(drop_p),
                                       int(seed) & 0xFFFFFFFF, _dtype_code(x), _stream(stream)),
            "nrm_act_dropout_bwd")
 

@@ -6,7 +6,10 @@
 // 实现原理", section "五、反向传播融合同样成立") takes the derivative at the saved
 // input and uses the error-function GELU; the normalization article's BatchNorm
 // section lists SiLU and Mish among the fusable activations (their formulas
-// are the standard ones: silu(z) = z*sigmoid(z), mish(z) = z*tanh(softplus(z))).
+// are the standard ones: silu(z) = z*sigmoid(z), mish(z) = z*tanh(softplus(z))),
+// and the activation article's list (section 六) has leaky_relu and elu, whose
+// parameter prm (slope, alpha) the article encodes in the name:
+// leaky_relu(z) = z > 0 ? z : prm*z, elu(z) = z > 0 ? z : prm*(e^z - 1).
 #pragma once
 
 #include "libnorm.h"
@@ -18,8 +21,10 @@ __device__ __forceinline__ float softplus_f(float z) {
     return z > 0.f ? z + log1pf(expf(-z)) : log1pf(expf(z));
 }
 
-__device__ __forceinline__ float act_forward(int act, float z) {
+__device__ __forceinline__ float act_forward(int act, float z, float prm) {
     if (act == NRM_ACT_RELU) return z > 0.f ? z : 0.f;
+    if (act == NRM_ACT_LEAKY_RELU) return z > 0.f ? z : prm * z;
+    if (act == NRM_ACT_ELU) return z > 0.f ? z : prm * expm1f(z);
     if (act == NRM_ACT_GELU) return 0.5f * z * (1.f + erff(z * 0.70710678118654752f));
     if (act == NRM_ACT_SILU) return z / (1.f + expf(-z));
     if (act == NRM_ACT_MISH) return z * tanhf(softplus_f(z));
@@ -27,8 +32,10 @@ __device__ __forceinline__ float act_forward(int act, float z) {
 }
 
 // Derivative at the pre-activation value z (ReLU'(0) = 0).
-__device__ __forceinline__ float act_derivative(int act, float z) {
+__device__ __forceinline__ float act_derivative(int act, float z, float prm) {
     if (act == NRM_ACT_RELU) return z > 0.f ? 1.f : 0.f;
+    if (act == NRM_ACT_LEAKY_RELU) return z > 0.f ? 1.f : prm;
+    if (act == NRM_ACT_ELU) return z > 0.f ? 1.f : prm * expf(z);
     if (act == NRM_ACT_GELU) {
         const float cdf = 0.5f * (1.f + erff(z * 0.70710678118654752f));
         const float pdf = expf(-0.5f * z * z) * 0.39894228040143268f;
@@ -49,16 +56,16 @@ __device__ __forceinline__ float act_derivative(int act, float z) {
 // The same for an activation fixed at compile time (the ring and group
 // kernels are instantiated per activation, so the hot loops carry one).
 template <int ACT>
-__device__ __forceinline__ float act_forward_c(float z) {
+__device__ __forceinline__ float act_forward_c(float z, float prm) {
     if constexpr (ACT == NRM_ACT_RELU) return z > 0.f ? z : 0.f;
     else if constexpr (ACT == NRM_ACT_NONE) return z;
-    else return act_forward(ACT, z);
+    else return act_forward(ACT, z, prm);
 }
 template <int ACT>
-__device__ __forceinline__ float act_derivative_c(float z) {
+__device__ __forceinline__ float act_derivative_c(float z, float prm) {
     if constexpr (ACT == NRM_ACT_RELU) return z > 0.f ? 1.f : 0.f;
     else if constexpr (ACT == NRM_ACT_NONE) return 1.f;
-    else return act_derivative(ACT, z);
+    else return act_derivative(ACT, z, prm);
 }
 
 // Calls f(std::integral_constant-like tag) with the activation as a compile-time value.
@@ -73,6 +80,8 @@ auto with_act(int act, F&& f) {
     case NRM_ACT_GELU: return f(ActTag<NRM_ACT_GELU>{});
     case NRM_ACT_SILU: return f(ActTag<NRM_ACT_SILU>{});
     case NRM_ACT_MISH: return f(ActTag<NRM_ACT_MISH>{});
+    case NRM_ACT_LEAKY_RELU: return f(ActTag<NRM_ACT_LEAKY_RELU>{});
+    case NRM_ACT_ELU: return f(ActTag<NRM_ACT_ELU>{});
     default: return f(ActTag<NRM_ACT_NONE>{});
     }
 }

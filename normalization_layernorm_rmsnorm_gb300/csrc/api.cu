@@ -333,16 +333,23 @@ nrm_status check_cf_shape(int64_t n, int64_t c, int64_t l, nrm_dtype dt) {
     return NRM_OK;
 }
 
-nrm_status check_bn_shape(int64_t n, int64_t c, int64_t l, nrm_dtype dt, int training, nrm_act act) {
+nrm_status check_act(nrm_act act, float act_param) {
+    if (act != NRM_ACT_NONE && act != NRM_ACT_RELU && act != NRM_ACT_GELU && act != NRM_ACT_SILU &&
+        act != NRM_ACT_MISH && act != NRM_ACT_LEAKY_RELU && act != NRM_ACT_ELU)
+        return fail(NRM_ERR_INVALID_ARG, "unknown activation %d", int(act));
+    if (!std::isfinite(act_param)) return fail(NRM_ERR_INVALID_ARG, "act_param must be finite");
+    return NRM_OK;
+}
+
+nrm_status check_bn_shape(int64_t n, int64_t c, int64_t l, nrm_dtype dt, int training, nrm_act act,
+                          float act_param) {
     if (!dtype_ok(dt)) return fail(NRM_ERR_INVALID_ARG, "unknown dtype %d", int(dt));
     if (n < 0 || c < 0 || l < 0) return fail(NRM_ERR_INVALID_ARG, "n, c, l must be >= 0");
     if (!size_ok(n, c, l)) return fail(NRM_ERR_UNSUPPORTED, "n*c*l must be < 2^40");
     if (!size_ok(n, l) || (n > 0 && l > 0 && n * l >= (int64_t(1) << 31)))
         return fail(NRM_ERR_UNSUPPORTED, "a channel must hold fewer than 2^31 elements");
     if (c * 16 >= (int64_t(1) << 31)) return fail(NRM_ERR_UNSUPPORTED, "c must be < 2^27");
-    if (act != NRM_ACT_NONE && act != NRM_ACT_RELU && act != NRM_ACT_GELU && act != NRM_ACT_SILU &&
-        act != NRM_ACT_MISH)
-        return fail(NRM_ERR_INVALID_ARG, "unknown activation %d", int(act));
+    if (nrm_status st = check_act(act, act_param); st != NRM_OK) return st;
     if (training && c > 0 && n * l < 2)
         return fail(NRM_ERR_INVALID_ARG, "training needs more than one value per channel (n*l >= 2)");
     return NRM_OK;
@@ -454,10 +461,10 @@ nrm_status nrm_rmsnorm_bwd(const void* dy, const void* x, const void* w, const f
 nrm_status nrm_batchnorm_fwd(const void* x, const void* residual, const float* w, const float* b,
                              void* y, float* running_mean, float* running_var, float* save_mean,
                              float* save_rstd, uint32_t* act_mask, int64_t n, int64_t c, int64_t l,
-                             float eps, float momentum, int training, nrm_act act, nrm_dtype dt,
-                             void* workspace, size_t workspace_bytes, nrm_stream_t stream) {
+                             float eps, float momentum, int training, nrm_act act, float act_param,
+                             nrm_dtype dt, void* workspace, size_t workspace_bytes, nrm_stream_t stream) {
     t_msg[0] = 0;
-    nrm_status st = check_bn_shape(n, c, l, dt, training, act);
+    nrm_status st = check_bn_shape(n, c, l, dt, training, act, act_param);
     if (st != NRM_OK) return st;
     if ((st = check_eps(eps)) != NRM_OK) return st;
     if (!(momentum >= 0.f && momentum <= 1.f)) return fail(NRM_ERR_INVALID_ARG, "momentum must be in [0, 1]");
@@ -493,6 +500,7 @@ nrm_status nrm_batchnorm_fwd(const void* x, const void* residual, const float* w
     a.eps = eps;
     a.momentum = momentum;
     a.act = int(act);
+    a.act_param = act_param;
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     a.err = d->err;
@@ -506,10 +514,10 @@ nrm_status nrm_batchnorm_fwd(const void* x, const void* residual, const float* w
 nrm_status nrm_batchnorm_bwd(const void* dy, const void* x, const void* residual, const float* w,
                              const float* b, const float* save_mean, const float* save_rstd,
                              const uint32_t* act_mask, void* dx, void* dres, float* dw, float* db,
-                             int64_t n, int64_t c, int64_t l, int training, nrm_act act, nrm_dtype dt,
-                             void* workspace, size_t workspace_bytes, nrm_stream_t stream) {
+                             int64_t n, int64_t c, int64_t l, int training, nrm_act act, float act_param,
+                             nrm_dtype dt, void* workspace, size_t workspace_bytes, nrm_stream_t stream) {
     t_msg[0] = 0;
-    nrm_status st = check_bn_shape(n, c, l, dt, training, act);
+    nrm_status st = check_bn_shape(n, c, l, dt, training, act, act_param);
     if (st != NRM_OK) return st;
     const bool has_data = n > 0 && c > 0 && l > 0;
     if ((has_data && (!dy || !x || !dx)) || (c > 0 && (!save_mean || !save_rstd)))
@@ -540,6 +548,7 @@ nrm_status nrm_batchnorm_bwd(const void* dy, const void* x, const void* residual
     a.c = c;
     a.l = l;
     a.act = int(act);
+    a.act_param = act_param;
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     a.err = d->err;
@@ -565,42 +574,40 @@ size_t nrm_batchnorm_workspace_bytes(int64_t n, int64_t c, int64_t l, nrm_dtype 
 }
 
 namespace {
-nrm_status check_act_dropout(int64_t count, nrm_act act, float p, nrm_dtype dt) {
+nrm_status check_act_dropout(int64_t count, nrm_act act, float act_param, float p, nrm_dtype dt) {
     if (!dtype_ok(dt)) return fail(NRM_ERR_INVALID_ARG, "unknown dtype %d", int(dt));
     if (count < 0) return fail(NRM_ERR_INVALID_ARG, "count must be >= 0");
     if (count >= (int64_t(1) << 40)) return fail(NRM_ERR_UNSUPPORTED, "count must be < 2^40");
-    if (act != NRM_ACT_NONE && act != NRM_ACT_RELU && act != NRM_ACT_GELU && act != NRM_ACT_SILU &&
-        act != NRM_ACT_MISH)
-        return fail(NRM_ERR_INVALID_ARG, "unknown activation %d", int(act));
+    if (nrm_status st = check_act(act, act_param); st != NRM_OK) return st;
     if (!(p >= 0.f && p <= 1.f)) return fail(NRM_ERR_INVALID_ARG, "drop_p must be in [0, 1]");
     return NRM_OK;
 }
 }  // namespace
 
-nrm_status nrm_act_dropout_fwd(const void* x, void* y, int64_t count, nrm_act act, float drop_p, uint32_t seed,
-                               nrm_dtype dt, nrm_stream_t stream) {
+nrm_status nrm_act_dropout_fwd(const void* x, void* y, int64_t count, nrm_act act, float act_param, float drop_p,
+                               uint32_t seed, nrm_dtype dt, nrm_stream_t stream) {
     t_msg[0] = 0;
-    nrm_status st = check_act_dropout(count, act, drop_p, dt);
+    nrm_status st = check_act_dropout(count, act, act_param, drop_p, dt);
     if (st != NRM_OK) return st;
     if (count > 0 && (!x || !y)) return fail(NRM_ERR_INVALID_ARG, "x and y must not be NULL");
     const size_t es = dsize(dt);
     if (!all_aligned({x, y}, es)) return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
     const bool vec = all_aligned({x, y}, 16);
-    return act_dropout(x, nullptr, y, count, int(act), drop_p, seed, dt, false, vec,
+    return act_dropout(x, nullptr, y, count, int(act), act_param, drop_p, seed, dt, false, vec,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
-nrm_status nrm_act_dropout_bwd(const void* dy, const void* x, void* dx, int64_t count, nrm_act act, float drop_p,
-                               uint32_t seed, nrm_dtype dt, nrm_stream_t stream) {
+nrm_status nrm_act_dropout_bwd(const void* dy, const void* x, void* dx, int64_t count, nrm_act act,
+                               float act_param, float drop_p, uint32_t seed, nrm_dtype dt, nrm_stream_t stream) {
     t_msg[0] = 0;
-    nrm_status st = check_act_dropout(count, act, drop_p, dt);
+    nrm_status st = check_act_dropout(count, act, act_param, drop_p, dt);
     if (st != NRM_OK) return st;
     if (count > 0 && (!dy || !x || !dx)) return fail(NRM_ERR_INVALID_ARG, "dy, x and dx must not be NULL");
     const size_t es = dsize(dt);
     if (!all_aligned({dy, x, dx}, es))
         return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
     const bool vec = all_aligned({dy, x, dx}, 16);
-    return act_dropout(x, dy, dx, count, int(act), drop_p, seed, dt, true, vec,
+    return act_dropout(x, dy, dx, count, int(act), act_param, drop_p, seed, dt, true, vec,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 

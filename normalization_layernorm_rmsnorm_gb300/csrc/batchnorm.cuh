@@ -380,7 +380,7 @@ bn_fwd_kernel(const BnArgs a, const BnGeom g) {
                     for (int k = 0; k < VE; ++k) {
                         float z = fmaf(v[k], scale, shift);
                         if (res) z += rr[k];
-                        o[k] = act_forward(a.act, z);
+                        o[k] = act_forward(a.act, z, a.act_param);
                         nib |= uint32_t(z > 0.f) << k;
                     }
                     store_vec_pol<T, VE>(y + (p.seg * g.lv + p.v) * VE, o, pol_stream);
@@ -827,7 +827,7 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
                             float z = fmaf(v[k], scale, shift);
                             if (res) z += rr[k];
                             nib |= uint32_t(z > 0.f) << k;
-                            o[k] = act_forward_c<ACT>(z);
+                            o[k] = act_forward_c<ACT>(z, a.act_param);
                         }
                         store_vec_pol<T, VE>(y + (p.seg * g.lv + p.v) * VE, o, pol_stream);
                     }
@@ -875,7 +875,7 @@ __device__ __forceinline__ void form_dz(const BnArgs& a, const BnGeom& g, const 
 #pragma unroll
     for (int k = 0; k < VE; ++k) {
         const float z = fmaf(xv[k], scale, shift) + r[k];
-        dz[k] = dyv[k] * act_derivative(a.act, z);
+        dz[k] = dyv[k] * act_derivative(a.act, z, a.act_param);
     }
 }
 
@@ -1157,7 +1157,7 @@ __device__ __forceinline__ void ring_dz(const BnArgs& a, bool use_mask, bool nee
 #pragma unroll
         for (int k = 0; k < VE; ++k) {
             const float z = fmaf(xv[k], scale, shift) + r[k];
-            dz[k] = dyv[k] * act_derivative_c<ACT>(z);
+            dz[k] = dyv[k] * act_derivative_c<ACT>(z, a.act_param);
         }
     } else {
 #pragma unroll

@@ -46,6 +46,7 @@ struct DropArgs {
     uint32_t thresh_w;  // ceil(p * 2^24) << 8: element kept when its word >= thresh_w (p < 1)
     int drop_all;       // p == 1: every element dropped
     float scale;        // 1 / (1 - p)
+    float act_param;    // slope (leaky_relu) or alpha (elu)
 };
 
 // Philox4x32 with 10 rounds on counter c, with the round keys of `a`.
@@ -73,8 +74,8 @@ __device__ __forceinline__ uint32_t word_of(const uint4& r, int k) {
 template <int ACT, bool BWD>
 __device__ __forceinline__ float drop_elem(float xv, float dyv, uint32_t word, const DropArgs& a) {
     if (word < a.thresh_w) return 0.f;
-    if constexpr (BWD) return dyv * a.scale * act_derivative_c<ACT>(xv);
-    else return act_forward_c<ACT>(xv) * a.scale;
+    if constexpr (BWD) return dyv * a.scale * act_derivative_c<ACT>(xv, a.act_param);
+    else return act_forward_c<ACT>(xv, a.act_param) * a.scale;
 }
 
 // One element by scalar accesses (tails and unaligned tensors).
@@ -173,9 +174,10 @@ nrm_status act_dropout_launch(const DropArgs& a, int act, bool vec, cudaStream_t
                        "activation-dropout launch");
 }
 
-nrm_status act_dropout(const void* x, const void* dy, void* out, int64_t count, int act, float p, uint32_t seed,
-                       nrm_dtype dt, bool bwd, bool vec, cudaStream_t s) {
+nrm_status act_dropout(const void* x, const void* dy, void* out, int64_t count, int act, float act_param, float p,
+                       uint32_t seed, nrm_dtype dt, bool bwd, bool vec, cudaStream_t s) {
     DropArgs a{};
+    a.act_param = act_param;
     a.x = x;
     a.dy = dy;
     a.y = bwd ? nullptr : out;

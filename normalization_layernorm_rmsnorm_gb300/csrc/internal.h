@@ -105,8 +105,8 @@ nrm_status encode_ncl_map(CUtensorMap* map, const void* base, size_t es, int64_t
                           int box_l, int box_c);
 
 // Activation with fused dropout (dropout.cu): out = y (forward) or dx (backward).
-nrm_status act_dropout(const void* x, const void* dy, void* out, int64_t count, int act, float p, uint32_t seed,
-                       nrm_dtype dt, bool bwd, bool vec, cudaStream_t s);
+nrm_status act_dropout(const void* x, const void* dy, void* out, int64_t count, int act, float act_param, float p,
+                       uint32_t seed, nrm_dtype dt, bool bwd, bool vec, cudaStream_t s);
 
 template <typename T> nrm_status cf_fwd(const CfArgs& a, bool vec, cudaStream_t s);
 template <typename T> nrm_status cf_bwd(CfArgs a, bool vec, cudaStream_t s);
@@ -145,6 +145,7 @@ struct BnArgs {
     float eps;
     float momentum;
     int act;
+    float act_param;      // slope (leaky_relu) or alpha (elu)
     unsigned int* err;    // device error word (bounded waits that gave up)
 };
 

@@ -27,6 +27,11 @@ import normalization_layernorm_rmsnorm_gb300 as nrm
 from normalization_layernorm_rmsnorm_gb300 import synth
 
 TOL = {"f32": (1e-5, 1e-5), "f16": (2e-2, 1e-2), "bf16": (2e-2, 1e-2)}
+# the parameter the parameterised activations are tested with (slope, alpha)
+ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3}
+# activations with a kink at 0 whose branch the kernel (fp32) and the oracle
+# (double) may decide differently within RELU_BAND
+KINKED = ("relu", "leaky_relu", "elu")
 STAT_TOL = (1e-5, 1e-5)
 RELU_BAND = 1e-4
 TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
@@ -166,12 +171,13 @@ def run_bn(inp, dtype, eps, momentum, training, act, with_res, use_mask, with_af
         mask = torch.full((nrm.nrm_act_mask_words(n, c, l),), 0xA5A5A5A5 - 2**32, dtype=torch.int32,
                           device="cuda")
     ws = nrm.batchnorm_workspace(x)
-    nrm.nrm_batchnorm_fwd(x, res, w, b, y, rm, rv, sm, sr, mask, eps, momentum, training, act, ws)
+    prm = ACT_PARAM.get(act, 0.0)
+    nrm.nrm_batchnorm_fwd(x, res, w, b, y, rm, rv, sm, sr, mask, eps, momentum, training, act, ws, act_param=prm)
     dx = empty(x.shape, dtype)
     dres = empty(x.shape, dtype)
     dw = torch.empty(c, dtype=torch.float32, device="cuda")
     db = torch.empty(c, dtype=torch.float32, device="cuda")
-    nrm.nrm_batchnorm_bwd(dy, x, res, w, b, sm, sr, mask, dx, dres, dw, db, training, act, ws)
+    nrm.nrm_batchnorm_bwd(dy, x, res, w, b, sm, sr, mask, dx, dres, dw, db, training, act, ws, act_param=prm)
     nrm.nrm_sync_status()
     out = dict(y=host(y), save_mean=host(sm), save_rstd=host(sr), running_mean=host(rm),
                running_var=host(rv), dx=host(dx), dres=host(dres), dw=host(dw), db=host(db))
@@ -183,7 +189,9 @@ def run_bn(inp, dtype, eps, momentum, training, act, with_res, use_mask, with_af
 def oracle_bn(orc, inp, eps, momentum, training, act, with_res, with_affine=True):
     import oracle as oracle_mod
     a = {"none": oracle_mod.ACT_NONE, "relu": oracle_mod.ACT_RELU, "gelu": oracle_mod.ACT_GELU,
-         "silu": oracle_mod.ACT_SILU, "mish": oracle_mod.ACT_MISH}[act]
+         "silu": oracle_mod.ACT_SILU, "mish": oracle_mod.ACT_MISH, "leaky_relu": oracle_mod.ACT_LEAKY_RELU,
+         "elu": oracle_mod.ACT_ELU}[act]
+    prm = ACT_PARAM.get(act, 0.0)
     x = inp["x"].f64()
     res = inp["res"].f64() if with_res else None
     w = inp["w"].f64() if with_affine else None
@@ -192,14 +200,17 @@ def oracle_bn(orc, inp, eps, momentum, training, act, with_res, with_affine=True
     rv0 = inp["running_var"].f64()
     dy = inp["dy"].f64()
     f = orc.batchnorm_fwd(x, res, w, b, eps, momentum, training, a, rm0, rv0,
-                          want_mask=(act == "relu"), want_z=True)
-    bw = orc.batchnorm_bwd(dy, x, res, w, b, rm0, rv0, eps, training, a, mask=f["mask"])
+                          want_mask=(act == "relu"), want_z=True, act_param=prm)
+    bw = orc.batchnorm_bwd(dy, x, res, w, b, rm0, rv0, eps, training, a, mask=f["mask"], act_param=prm)
     out = dict(fwd=f, bwd=bw, act=a, x=x, dy=dy)
-    if act == "relu":
+    if act in KINKED:
         z = f["z"]
         amb = np.abs(z) < RELU_BAND
         out["amb"] = amb
-        if amb.any():
+        # the other branch's output at the kink: relu 0 | z, leaky a*z | z, elu a*(e^z - 1) | z
+        neg = {"relu": 0.0 * z, "leaky_relu": prm * z, "elu": prm * np.expm1(z)}[act]
+        out["y_alt"] = np.where(z > 0, neg, z)
+        if act == "relu" and amb.any():
             bits = unpack_mask(f["mask"], *x.shape)
             out["bwd_flipped"] = orc.batchnorm_bwd(dy, x, res, w, b, rm0, rv0, eps, training, a,
                                                    mask=pack_mask(bits ^ amb))
@@ -214,11 +225,12 @@ def compare_bn(got, want, dtype, training, act, tag):
     ok = None if amb is None else ~amb
     assert_close(got["y"], f["y"], tol, f"{tag} y", mask=ok)
     if amb is not None and amb.any():
-        # either branch of the ReLU decision, within tolerance
+        # either branch of the kink decision, within tolerance
         y_amb = got["y"][amb]
-        z_amb = f["z"][amb]
-        lim = tol[0] + tol[1] * np.abs(z_amb)
-        assert (np.minimum(np.abs(y_amb), np.abs(y_amb - z_amb)) <= lim).all(), f"{tag} y at ReLU ties"
+        lim = tol[0] + tol[1] * np.abs(f["z"][amb])
+        e1 = np.abs(y_amb - f["y"][amb])
+        e2 = np.abs(y_amb - want["y_alt"][amb])
+        assert (np.minimum(e1, e2) <= lim).all(), f"{tag} y at kink ties"
     assert_close(got["save_mean"], f["save_mean"], STAT_TOL, f"{tag} save_mean")
     assert_close(got["save_rstd"], f["save_rstd"], STAT_TOL, f"{tag} save_rstd")
     if training:
@@ -243,6 +255,10 @@ def compare_bn(got, want, dtype, training, act, tag):
             eb = np.abs(g - b_) <= atol + rtol * np.abs(b_)
             good = np.where(amb, ea | eb, ea)
             assert good.all(), f"{tag} {name}: {int((~good).sum())} elements out of tolerance"
+        elif amb is not None and amb.any():
+            # a tie decided the other way changes that element's derivative (1 vs
+            # the slope or alpha); the per-channel sums below bound its effect
+            assert_close(g, a_, tol, f"{tag} {name}", mask=~amb)
         else:
             assert_close(g, a_, tol, f"{tag} {name}")
     # per-channel sums.  Outside ReLU ties they are unique.  A tie element the

@@ -83,35 +83,39 @@ P = 1 << 20  # a fake, aligned, non-null address: never dereferenced (validation
                                    None), 1),
     # training BatchNorm with one value per channel
     (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, None, None, None, None, None, 1, 3,
-                                   1, 1e-5, 0.1, 1, 0, 0, None, 0, None), 1),
+                                   1, 1e-5, 0.1, 1, 0, 0.0, 0, None, 0, None), 1),
     # running_mean without running_var
     (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, P * 3, None, None, None, None, 2, 3,
-                                   4, 1e-5, 0.1, 1, 0, 0, None, 0, None), 1),
+                                   4, 1e-5, 0.1, 1, 0, 0.0, 0, None, 0, None), 1),
     # eval without running statistics
     (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, None, None, None, None, None, 2, 3,
-                                   4, 1e-5, 0.1, 0, 0, 0, None, 0, None), 1),
+                                   4, 1e-5, 0.1, 0, 0, 0.0, 0, None, 0, None), 1),
     # momentum out of range
     (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, None, None, None, None, None, 2, 3,
-                                   4, 1e-5, 1.5, 1, 0, 0, None, 0, None), 1),
+                                   4, 1e-5, 1.5, 1, 0, 0.0, 0, None, 0, None), 1),
     # a mask for GELU
     (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, None, None, None, None, P * 3, 2, 3,
-                                   4, 1e-5, 0.1, 1, 2, 0, None, 0, None), 1),
+                                   4, 1e-5, 0.1, 1, 2, 0.0, 0, None, 0, None), 1),
     # unknown activation
     (lambda L: L.nrm_batchnorm_bwd(P, P * 2, None, None, None, P * 3, P * 4, None, P * 5, None, None,
-                                   None, 2, 3, 4, 1, 9, 0, None, 0, None), 1),
+                                   None, 2, 3, 4, 1, 9, 0.0, 0, None, 0, None), 1),
     # a channel with 2^31 elements
     (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, None, None, None, None, None,
-                                   1 << 16, 1, 1 << 15, 1e-5, 0.1, 1, 0, 0, None, 0, None), 2),
+                                   1 << 16, 1, 1 << 15, 1e-5, 0.1, 1, 0, 0.0, 0, None, 0, None), 2),
     # channels-first LayerNorm with no channels
     (lambda L: L.nrm_layernorm_cf_fwd(P, None, None, P * 2, None, None, 2, 0, 5, 1e-5, 0, None), 1),
     # dropout probability above 1, NaN, negative count, unknown activation, null y
-    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 2, 1.5, 7, 1, None), 1),
-    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 2, float("nan"), 7, 1, None), 1),
-    (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, -1, 2, 0.5, 7, 1, None), 1),
-    (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, 16, 9, 0.5, 7, 1, None), 1),
-    (lambda L: L.nrm_act_dropout_fwd(P, None, 16, 2, 0.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 2, 0.0, 1.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 2, 0.0, float("nan"), 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, -1, 2, 0.0, 0.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, 16, 9, 0.0, 0.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_fwd(P, None, 16, 2, 0.0, 0.5, 7, 1, None), 1),
+    # a non-finite activation parameter (BatchNorm and dropout)
+    (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, None, None, None, None, None, 2, 3,
+                                   4, 1e-5, 0.1, 1, 5, float("inf"), 0, None, 0, None), 1),
+    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 6, float("nan"), 0.5, 7, 1, None), 1),
     # element-misaligned fp16 pointer
-    (lambda L: L.nrm_act_dropout_fwd(P + 1, P * 2, 16, 2, 0.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_fwd(P + 1, P * 2, 16, 2, 0.0, 0.5, 7, 1, None), 1),
 ])
 def test_bad_arguments_are_rejected_on_the_host(lib, call, expect):
     assert call(lib) == expect

@@ -168,6 +168,34 @@ def test_bn_silu_mish_vector_path(orc, act, dtype):
             compare_bn(got, want, dtype, training, act, f"bn {dtype} {act} training={training} res={with_res}")
 
 
+LEAKY_ELU = [
+    # (dtype, n, c, l): the ring kernels, the channel-group kernels (7x7 maps), the scalar path
+    ("f32", 32, 6, 1568),
+    ("bf16", 32, 6, 1568),
+    ("f16", 16, 24, 49),
+    ("f32", 5, 7, 33),
+]
+
+
+@pytest.mark.parametrize("act", ["leaky_relu", "elu"])
+@pytest.mark.parametrize("case", LEAKY_ELU, ids=[f"{d}-{n}x{c}x{l}" for d, n, c, l in LEAKY_ELU])
+def test_bn_leaky_relu_elu(orc, act, case):
+    # the activations with a parameter (slope 0.05, alpha 1.3), z recomputed in the backward
+    dtype, n, c, l = case
+    for training in (True, False):
+        for with_res in (False, True):
+            cfg = synth.BnConfig("actp", n, c, l, dtype, 1e-5, 0.1, seed=750 + int(with_res), act=act,
+                                 residual=with_res, x_kind="offset_scale", w_std=0.2, b_std=0.2)
+            inp = synth.bn_inputs(cfg)
+            if not training:
+                inp["running_mean"] = synth.store(0.2 * synth.normal(cfg.seed, 20, c), "f32", (c,))
+                inp["running_var"] = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,))
+            got = run_bn(inp, dtype, cfg.eps, cfg.momentum, training, act, with_res, False)
+            want = oracle_bn(orc, inp, cfg.eps, cfg.momentum, training, act, with_res)
+            compare_bn(got, want, dtype, training, act,
+                       f"bn {dtype} [{n},{c},{l}] {act} training={training} res={with_res}")
+
+
 BN1D = [("f32", 4096, 64), ("f16", 4096, 64), ("bf16", 300, 24), ("f32", 50000, 8)]
 
 

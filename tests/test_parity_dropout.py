@@ -13,8 +13,9 @@ from parity_util import TOL, assert_close, host
 
 pytestmark = pytest.mark.gpu
 
-ACTS = ["none", "relu", "gelu", "silu", "mish"]
-ACT_CODE = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "mish": 4}
+ACTS = ["none", "relu", "gelu", "silu", "mish", "leaky_relu", "elu"]
+ACT_CODE = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "mish": 4, "leaky_relu": 5, "elu": 6}
+ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,16 +36,18 @@ def _run(x, dy, act, p, seed, offset=0):
     xt, dyt = xb[offset:], dyb[offset:]
     y = torch.empty_like(xb)[offset:]
     dx = torch.empty_like(xb)[offset:]
-    nrm.nrm_act_dropout_fwd(xt, y, act, p, seed)
-    nrm.nrm_act_dropout_bwd(dyt, xt, dx, act, p, seed)
+    prm = ACT_PARAM.get(act, 0.0)
+    nrm.nrm_act_dropout_fwd(xt, y, act, p, seed, act_param=prm)
+    nrm.nrm_act_dropout_bwd(dyt, xt, dx, act, p, seed, act_param=prm)
     nrm.nrm_sync_status()
     return host(y), host(dx)
 
 
 def _check(orc, x, dy, act, p, seed, dtype, tag, offset=0):
     y, dx = _run(x, dy, act, p, seed, offset)
-    yo = orc.act_dropout_fwd(x.f64(), ACT_CODE[act], p, seed)
-    dxo = orc.act_dropout_bwd(dy.f64(), x.f64(), ACT_CODE[act], p, seed)
+    prm = ACT_PARAM.get(act, 0.0)
+    yo = orc.act_dropout_fwd(x.f64(), ACT_CODE[act], p, seed, act_param=prm)
+    dxo = orc.act_dropout_bwd(dy.f64(), x.f64(), ACT_CODE[act], p, seed, act_param=prm)
     keep = orc.dropout_mask(x.shape[0], p, seed).astype(bool)
     # dropped elements are exactly zero on both passes
     assert not y[~keep].any(), f"{tag}: nonzero y at dropped elements"
