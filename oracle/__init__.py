@@ -79,8 +79,8 @@ class Oracle:
         lib.oracle_layernorm_bwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D, _D]
         lib.oracle_layernorm_cf_fwd.argtypes = [_I64, _I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D, _D]
         lib.oracle_layernorm_cf_bwd.argtypes = [_I64, _I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D, _D]
-        lib.oracle_rmsnorm_fwd.argtypes = [_I64, _I64, _D, _D, ctypes.c_double, _D, _D]
-        lib.oracle_rmsnorm_bwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D]
+        lib.oracle_rmsnorm_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D]
+        lib.oracle_rmsnorm_bwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _D, _D, _D]
         lib.oracle_batchnorm_fwd.argtypes = [_I64, _I64, _I64, _D, _D, _D, _D,
                                              ctypes.c_double, ctypes.c_double,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_double, _D, _D,
@@ -151,24 +151,25 @@ class Oracle:
                                          _ptr(dw), _ptr(db))
         return dx, dw, db
 
-    def rmsnorm_fwd(self, x, w=None, eps=1e-6):
-        """Returns (y, rstd)."""
-        x, w = _f64(x), _f64(w)
+    def rmsnorm_fwd(self, x, w=None, eps=1e-6, b=None):
+        """Returns (y, rstd); b is the optional bias."""
+        x, w, b = _f64(x), _f64(w), _f64(b)
         rows, cols = x.shape
         y = np.empty_like(x)
         rstd = np.empty(rows)
-        self.lib.oracle_rmsnorm_fwd(rows, cols, _ptr(x), _ptr(w), eps, _ptr(y), _ptr(rstd))
+        self.lib.oracle_rmsnorm_fwd(rows, cols, _ptr(x), _ptr(w), _ptr(b), eps, _ptr(y), _ptr(rstd))
         return y, rstd
 
-    def rmsnorm_bwd(self, dy, x, w=None, eps=1e-6):
-        """Returns (dx, dw)."""
+    def rmsnorm_bwd(self, dy, x, w=None, eps=1e-6, with_db=False):
+        """Returns (dx, dw), or (dx, dw, db) with with_db (the bias gradient)."""
         dy, x, w = _f64(dy), _f64(x), _f64(w)
         rows, cols = x.shape
         dx = np.empty_like(x)
         dw = np.empty(cols)
+        db = np.empty(cols) if with_db else None
         self.lib.oracle_rmsnorm_bwd(rows, cols, _ptr(dy), _ptr(x), _ptr(w), eps,
-                                    _ptr(dx), _ptr(dw))
-        return dx, dw
+                                    _ptr(dx), _ptr(dw), _ptr(db))
+        return (dx, dw, db) if with_db else (dx, dw)
 
     # -- BatchNorm -----------------------------------------------------------
     @staticmethod

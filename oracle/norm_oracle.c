@@ -20,7 +20,8 @@
  * design notes):
  *   - LayerNorm variance divides by N (biased), as a drop-in nn.LayerNorm does.
  *   - eps sits inside the root: (var + eps)^(-1/2), (ms + eps)^(-1/2).
- *   - RMSNorm has a weight and no bias.
+ *   - RMSNorm has a weight; its bias (NULL in the articles' formula) is added
+ *     after the weight, as LayerNorm's is, and its gradient is db = sum dy.
  *   - BatchNorm normalises with the biased batch variance and feeds the unbiased
  *     one, M/(M-1) times larger, to running_var.
  *   - EMA: new = (1 - momentum) * old + momentum * batch value.
@@ -136,10 +137,12 @@ void oracle_layernorm_bwd(int64_t rows, int64_t cols, const double *dy,
 
 /*
  * [NK] section "RMSNorm：去掉均值的极简版 LayerNorm": no mean is taken; the output
- * is input * inv_rms * weight, inv_rms = (mean(x^2) + eps)^(-1/2).
+ * is input * inv_rms * weight, inv_rms = (mean(x^2) + eps)^(-1/2).  An optional
+ * bias b (the formula has none) is added last.
  */
 void oracle_rmsnorm_fwd(int64_t rows, int64_t cols, const double *x,
-                        const double *w, double eps, double *y, double *rstd)
+                        const double *w, const double *b, double eps, double *y,
+                        double *rstd)
 {
     for (int64_t r = 0; r < rows; ++r) {
         const double *xr = x + r * cols;
@@ -148,7 +151,7 @@ void oracle_rmsnorm_fwd(int64_t rows, int64_t cols, const double *x,
             ss += xr[j] * xr[j];
         double rr = 1.0 / sqrt(ss / (double)cols + eps);
         for (int64_t j = 0; j < cols; ++j)
-            y[r * cols + j] = xr[j] * rr * (w ? w[j] : 1.0);
+            y[r * cols + j] = xr[j] * rr * (w ? w[j] : 1.0) + (b ? b[j] : 0.0);
         if (rstd) rstd[r] = rr;
     }
 }
@@ -157,13 +160,15 @@ void oracle_rmsnorm_fwd(int64_t rows, int64_t cols, const double *x,
  * [NK] section "RMSNorm：去掉均值的极简版 LayerNorm", backward sentence: the
  * LayerNorm reduction is reused with the row sum of input * output_grad * weight.
  * With g = dy * w and s = sum(g * x):
- *   dx = inv_rms * g - x * inv_rms^3 * s / N,    dw = sum over rows of dy * x * inv_rms.
+ *   dx = inv_rms * g - x * inv_rms^3 * s / N,    dw = sum over rows of dy * x * inv_rms,
+ *   db = sum over rows of dy (the optional bias).
  */
 void oracle_rmsnorm_bwd(int64_t rows, int64_t cols, const double *dy,
                         const double *x, const double *w, double eps,
-                        double *dx, double *dw)
+                        double *dx, double *dw, double *db)
 {
     if (dw) for (int64_t j = 0; j < cols; ++j) dw[j] = 0.0;
+    if (db) for (int64_t j = 0; j < cols; ++j) db[j] = 0.0;
 
     for (int64_t r = 0; r < rows; ++r) {
         const double *xr = x + r * cols;
@@ -180,6 +185,7 @@ void oracle_rmsnorm_bwd(int64_t rows, int64_t cols, const double *dy,
             double g = dyr[j] * (w ? w[j] : 1.0);
             dx[r * cols + j] = rr * g - xr[j] * rr * rr * rr * s / (double)cols;
             if (dw) dw[j] += dyr[j] * xr[j] * rr;
+            if (db) db[j] = db[j] + dyr[j];
         }
     }
 }

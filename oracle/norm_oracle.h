@@ -28,10 +28,11 @@ void oracle_layernorm_cf_bwd(int64_t n, int64_t c, int64_t l, const double *dy,
                              const double *x, const double *w, double eps,
                              double *dx, double *dw, double *db);
 void oracle_rmsnorm_fwd(int64_t rows, int64_t cols, const double *x,
-                        const double *w, double eps, double *y, double *rstd);
+                        const double *w, const double *b, double eps, double *y,
+                        double *rstd);
 void oracle_rmsnorm_bwd(int64_t rows, int64_t cols, const double *dy,
                         const double *x, const double *w, double eps,
-                        double *dx, double *dw);
+                        double *dx, double *dw, double *db);
 void oracle_batchnorm_fwd(int64_t n, int64_t c, int64_t l, const double *x,
                           const double *res, const double *w, const double *b,
                           double eps, double momentum, int training, int act,

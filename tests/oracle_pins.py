@@ -198,6 +198,27 @@ def pin_rmsnorm_bwd_fd(o):
         _close(dw, _central_diff(loss, w, 1e-6), 1e-6, 1e-7, "rmsnorm dw vs finite differences")
 
 
+def pin_rmsnorm_bias(o):
+    """With a bias: y is torch's rms_norm plus b; db = sum of dy over rows and
+    dx, dw are those without the bias; all three against finite differences."""
+    import torch
+    r = _rng(33)
+    x = r.normal(size=(4, 19)) * 1.2
+    w = 1 + 0.2 * r.normal(size=19)
+    b = 0.3 * r.normal(size=19)
+    y, _ = o.rmsnorm_fwd(x, w, eps=1e-5, b=b)
+    yt = torch.nn.functional.rms_norm(torch.from_numpy(x), (19,), torch.from_numpy(w), eps=1e-5).numpy()
+    _close(y, yt + b, 1e-12, 1e-12, "rmsnorm with bias vs torch")
+    dy = r.normal(size=(4, 19))
+    dx, dw, db = o.rmsnorm_bwd(dy, x, w, eps=1e-5, with_db=True)
+    dx0, dw0 = o.rmsnorm_bwd(dy, x, w, eps=1e-5)
+    _close(db, dy.sum(0), 1e-15, 1e-15, "rmsnorm db = sum dy")
+    assert (dx == dx0).all() and (dw == dw0).all(), "the bias must not change dx, dw"
+    loss = lambda: float((dy * o.rmsnorm_fwd(x, w, eps=1e-5, b=b)[0]).sum())
+    _close(db, _central_diff(loss, b, 1e-6), 1e-7, 1e-7, "rmsnorm db vs finite differences")
+    _close(dx, _central_diff(loss, x, 1e-6), 1e-6, 1e-7, "rmsnorm (bias) dx vs finite differences")
+
+
 def pin_rmsnorm_bwd_invariant(o):
     r = _rng(9)
     x = r.normal(size=(4, 50))

@@ -22,8 +22,11 @@ MUTATIONS = {
     "ln_dw_uses_x_not_xhat": ("if (dw) dw[j] += dyr[j] * xhat;",
                               "if (dw) dw[j] += dyr[j] * xr[j];"),
     "ln_db_sign": ("if (db) db[j] += dyr[j];", "if (db) db[j] -= dyr[j];"),
-    "rms_fwd_drops_weight": ("y[r * cols + j] = xr[j] * rr * (w ? w[j] : 1.0);",
-                             "y[r * cols + j] = xr[j] * rr;"),
+    "rms_fwd_drops_weight": ("y[r * cols + j] = xr[j] * rr * (w ? w[j] : 1.0) + (b ? b[j] : 0.0);",
+                             "y[r * cols + j] = xr[j] * rr + (b ? b[j] : 0.0);"),
+    "rms_fwd_drops_bias": ("y[r * cols + j] = xr[j] * rr * (w ? w[j] : 1.0) + (b ? b[j] : 0.0);",
+                           "y[r * cols + j] = xr[j] * rr * (w ? w[j] : 1.0);"),
+    "rms_db_scaled_by_x": ("if (db) db[j] = db[j] + dyr[j];", "if (db) db[j] = db[j] + dyr[j] * xr[j];"),
     "rms_bwd_rstd_squared": ("xr[j] * rr * rr * rr * s", "xr[j] * rr * rr * s"),
     "rms_bwd_term_sign": ("dx[r * cols + j] = rr * g - xr[j]",
                           "dx[r * cols + j] = rr * g + xr[j]"),
