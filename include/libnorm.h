@@ -208,13 +208,14 @@ NRM_API nrm_status nrm_layernorm_cf_bwd(const void *dy, const void *x, const voi
 
 /*
  * nrm_rmsnorm_fwd -- [NK] section "RMSNorm：去掉均值的极简版 LayerNorm": no mean
- * is subtracted; output = input * inv_rms * weight with
+ * is subtracted; output = input * inv_rms * weight (+ bias) with
  *   inv_rms = (sum_j x_j^2 / cols + eps)^(-1/2).
- * x, y: [rows, cols] in dt.  w: [cols] in dt or NULL (1).  There is no bias.
- * rstd: float32 [rows] receives inv_rms, may be NULL.
+ * x, y: [rows, cols] in dt.  w: [cols] in dt or NULL (1).  b: [cols] in dt or
+ * NULL: the article's formula has no bias; a bias is added after the weight,
+ * as LayerNorm's is.  rstd: float32 [rows] receives inv_rms, may be NULL.
  */
-NRM_API nrm_status nrm_rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd,
-                           int64_t rows, int64_t cols, float eps, nrm_dtype dt,
+NRM_API nrm_status nrm_rmsnorm_fwd(const void *x, const void *w, const void *b, void *y,
+                           float *rstd, int64_t rows, int64_t cols, float eps, nrm_dtype dt,
                            nrm_stream_t stream);
 
 /*
@@ -222,11 +223,12 @@ NRM_API nrm_status nrm_rmsnorm_fwd(const void *x, const void *w, void *y, float 
  * reduction reused with the row sum of input * output_grad * weight).  With
  * g = dy*w and s = sum(g*x):
  *   dx = inv_rms * g - x * inv_rms^3 * s / cols;  dw = sum over rows of dy*x*inv_rms
+ *   db = sum over rows of dy (the bias, when the forward had one)
  * Arguments as nrm_layernorm_bwd, with rstd = inv_rms from nrm_rmsnorm_fwd and
- * NRM_OP_RMSNORM_BWD for the workspace size.
+ * NRM_OP_RMSNORM_BWD for the workspace size.  dw, db may be NULL.
  */
 NRM_API nrm_status nrm_rmsnorm_bwd(const void *dy, const void *x, const void *w,
-                           const float *rstd, void *dx, void *dw, int64_t rows,
+                           const float *rstd, void *dx, void *dw, void *db, int64_t rows,
                            int64_t cols, nrm_dtype dt, void *workspace,
                            size_t workspace_bytes, nrm_stream_t stream);
 

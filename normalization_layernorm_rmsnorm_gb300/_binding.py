@@ -65,8 +65,8 @@ def load(path: str | None = None):
         "nrm_layernorm_cf_fwd": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _I, _P],
         "nrm_layernorm_cf_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _P, ctypes.c_size_t,
                                  _P],
-        "nrm_rmsnorm_fwd": [_P, _P, _P, _P, _I64, _I64, _F, _I, _P],
-        "nrm_rmsnorm_bwd": [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, ctypes.c_size_t, _P],
+        "nrm_rmsnorm_fwd": [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P],
+        "nrm_rmsnorm_bwd": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, ctypes.c_size_t, _P],
         "nrm_batchnorm_fwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, _I,
                               _I, _F, _I, _P, ctypes.c_size_t, _P],
         "nrm_batchnorm_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I,
@@ -182,17 +182,19 @@ def nrm_layernorm_bwd_noalloc(dy, x, w, mean, rstd, dx, dw, db, stream=None):
            "nrm_layernorm_bwd_noalloc")
 
 
-def nrm_rmsnorm_fwd(x, w, y, rstd, eps, stream=None):
+def nrm_rmsnorm_fwd(x, w, y, rstd, eps, stream=None, b=None):
+    """RMSNorm of the rows of x; b is the optional bias."""
     rows, cols = _rows_cols(x)
-    _check(load().nrm_rmsnorm_fwd(_ptr(x), _ptr(w), _ptr(y), _ptr(rstd), rows, cols, eps,
+    _check(load().nrm_rmsnorm_fwd(_ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(rstd), rows, cols, eps,
                                   _dtype_code(x), _stream(stream)),
            "nrm_rmsnorm_fwd")
 
 
-def nrm_rmsnorm_bwd(dy, x, w, rstd, dx, dw, workspace, stream=None):
+def nrm_rmsnorm_bwd(dy, x, w, rstd, dx, dw, workspace, stream=None, db=None):
+    """RMSNorm backward; db receives the bias gradient when given."""
     rows, cols = _rows_cols(x)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load().nrm_rmsnorm_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw),
+    _check(load().nrm_rmsnorm_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw), _ptr(db),
                                   rows, cols, _dtype_code(x), _ptr(workspace), ws_bytes,
                                   _stream(stream)),
            "nrm_rmsnorm_bwd")

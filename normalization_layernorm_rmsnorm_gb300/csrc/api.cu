@@ -273,7 +273,7 @@ nrm_status row_fwd_common(bool ln, const void* x, const void* w, const void* b, 
     RowArgs a{};
     a.x = x;
     a.w = w;
-    a.b = ln ? b : nullptr;
+    a.b = b;  // RMSNorm's is optional
     a.y = y;
     a.mean = ln ? mean : nullptr;
     a.rstd = rstd;
@@ -297,17 +297,17 @@ nrm_status row_bwd_common(bool ln, const void* dy, const void* x, const void* w,
         return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
     if (rows > 0 && (dx == dy || dx == x))
         return fail(NRM_ERR_INVALID_ARG, "in-place (dx == dy or x) is not supported");
-    const bool want = dw || (ln && db);
+    const bool want = dw || db;
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     RowArgs a{};
     if (want && rows > 0) {
-        const size_t need = row_ws_bytes(ln, cols);
+        const size_t need = row_ws_bytes(ln || db, cols);
         if (!ws || !aligned(ws, 16)) return fail(NRM_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned");
         if (ws_bytes < need)
             return fail(NRM_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
         a.ws_dw = reinterpret_cast<float*>(ws);
-        a.ws_db = ln ? a.ws_dw + size_t(row_bwd_max_partials(*d)) * size_t(cols) : nullptr;
+        a.ws_db = (ln || db) ? a.ws_dw + size_t(row_bwd_max_partials(*d)) * size_t(cols) : nullptr;
     }
     const bool vec = (size_t(cols) * es) % 16 == 0 && all_aligned({dy, x, dx, w}, 16);
     a.x = x;
@@ -317,7 +317,7 @@ nrm_status row_bwd_common(bool ln, const void* dy, const void* x, const void* w,
     a.mean_in = mean;
     a.rstd_in = rstd;
     a.dw = dw;
-    a.db = ln ? db : nullptr;
+    a.db = db;
     a.rows = rows;
     a.cols = int(cols);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -446,15 +446,15 @@ nrm_status nrm_layernorm_cf_bwd(const void* dy, const void* x, const void* w, co
     return by_dtype(dt, [&](auto tag) { return cf_bwd<decltype(tag)>(a, vec, s); });
 }
 
-nrm_status nrm_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows,
+nrm_status nrm_rmsnorm_fwd(const void* x, const void* w, const void* b, void* y, float* rstd, int64_t rows,
                            int64_t cols, float eps, nrm_dtype dt, nrm_stream_t stream) {
-    return row_fwd_common(false, x, w, nullptr, y, nullptr, rstd, rows, cols, eps, dt, stream);
+    return row_fwd_common(false, x, w, b, y, nullptr, rstd, rows, cols, eps, dt, stream);
 }
 
 nrm_status nrm_rmsnorm_bwd(const void* dy, const void* x, const void* w, const float* rstd, void* dx,
-                           void* dw, int64_t rows, int64_t cols, nrm_dtype dt, void* workspace,
+                           void* dw, void* db, int64_t rows, int64_t cols, nrm_dtype dt, void* workspace,
                            size_t workspace_bytes, nrm_stream_t stream) {
-    return row_bwd_common(false, dy, x, w, nullptr, rstd, dx, dw, nullptr, rows, cols, dt, workspace,
+    return row_bwd_common(false, dy, x, w, nullptr, rstd, dx, dw, db, rows, cols, dt, workspace,
                           workspace_bytes, stream);
 }
 
@@ -563,7 +563,7 @@ size_t nrm_workspace_bytes(nrm_op op, int64_t rows, int64_t cols, nrm_dtype dt) 
     if (op != NRM_OP_LAYERNORM_BWD && op != NRM_OP_RMSNORM_BWD && op != NRM_OP_LAYERNORM_CF_BWD) return 0;
     if (check_rows(rows, cols, dt) != NRM_OK) return 0;
     if (op == NRM_OP_LAYERNORM_CF_BWD && cols > kCfMaxChannels) return 0;
-    return row_ws_bytes(op != NRM_OP_RMSNORM_BWD, cols);
+    return row_ws_bytes(true, cols);  // dw and db partial rows (RMSNorm's db: the optional bias)
 }
 
 size_t nrm_batchnorm_workspace_bytes(int64_t n, int64_t c, int64_t l, nrm_dtype dt) {

@@ -191,11 +191,11 @@ row_fwd_kernel(const RowArgs a) {
             if (vi < nvec) {
                 float wv[VE], bv[VE], o[VE];
                 load_param<T, VE>(a.w, vi, wv, 1.f);
-                if constexpr (LN) load_param<T, VE>(a.b, vi, bv, 0.f);
+                load_param<T, VE>(a.b, vi, bv, 0.f);  // LayerNorm's bias, or RMSNorm's optional one
 #pragma unroll
                 for (int k = 0; k < VE; ++k) {
                     const float xh = (elem(xp[j], k) - mu) * rs;
-                    o[k] = LN ? fmaf(xh, wv[k], bv[k]) : xh * wv[k];
+                    o[k] = fmaf(xh, wv[k], bv[k]);
                 }
                 store_vec<T, VE>(yr + int64_t(vi) * VE, o);
             }
@@ -263,6 +263,7 @@ row_bwd_kernel(const RowArgs a) {
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
     const T* __restrict__ dy = reinterpret_cast<const T*>(a.dy);
     T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
+    const bool want_db = LN || a.ws_db != nullptr;  // RMSNorm: the optional bias
     int phase = 0;
 
     float accw[VPT][VE];
@@ -343,6 +344,7 @@ row_bwd_kernel(const RowArgs a) {
                     } else {
                         o[k] = rs * (g - xv * c2);
                         accw[j][k] = fmaf(dv, xv * rs, accw[j][k]);
+                        if (want_db) accb[j][k] += dv;
                     }
                 }
                 store_vec<T, VE>(dxr + int64_t(vi) * VE, o);
@@ -362,11 +364,9 @@ row_bwd_kernel(const RowArgs a) {
     if (a.ws_dw)
         write_partial_row<TPR, VPT, VE, RPC>(accw, a.ws_dw + int64_t(blockIdx.x) * cols, &part[0][0],
                                              group, t, cols);
-    if constexpr (LN) {
-        if (a.ws_db)
-            write_partial_row<TPR, VPT, VE, RPC>(accb, a.ws_db + int64_t(blockIdx.x) * cols,
-                                                 &part[0][0], group, t, cols);
-    }
+    if (a.ws_db)
+        write_partial_row<TPR, VPT, VE, RPC>(accb, a.ws_db + int64_t(blockIdx.x) * cols, &part[0][0],
+                                             group, t, cols);
 }
 
 // Compensated fp32 sum (Neumaier's variant of Kahan's): exact to about two
@@ -507,11 +507,11 @@ row_fwd_wide_kernel(const RowArgs a) {
             float v[VE], wv[VE], bv[VE], o[VE];
             load_vec<T, VE>(xr + int64_t(vi) * VE, v);
             load_param<T, VE>(a.w, vi, wv, 1.f);
-            if constexpr (LN) load_param<T, VE>(a.b, vi, bv, 0.f);
+            load_param<T, VE>(a.b, vi, bv, 0.f);
 #pragma unroll
             for (int k = 0; k < VE; ++k) {
                 const float xh = (v[k] - mu) * rs;
-                o[k] = LN ? fmaf(xh, wv[k], bv[k]) : xh * wv[k];
+                o[k] = fmaf(xh, wv[k], bv[k]);
             }
             store_vec<T, VE>(yr + int64_t(vi) * VE, o);
         }
@@ -528,7 +528,7 @@ row_bwd_wide_kernel(const RowArgs a) {
     const T* __restrict__ dy = reinterpret_cast<const T*>(a.dy);
     T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
     float* wsw = a.ws_dw ? a.ws_dw + int64_t(blockIdx.x) * cols : nullptr;
-    float* wsb = (LN && a.ws_db) ? a.ws_db + int64_t(blockIdx.x) * cols : nullptr;
+    float* wsb = a.ws_db ? a.ws_db + int64_t(blockIdx.x) * cols : nullptr;
     // this CTA's partial rows; each column is always updated by the same thread
     for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
 #pragma unroll
@@ -582,6 +582,7 @@ row_bwd_wide_kernel(const RowArgs a) {
                 } else {
                     o[k] = rs * (g - xv[k] * (c1 * rs * rs));
                     if (wsw) wsw[vi * VE + k] = fmaf(dv[k], xv[k] * rs, wsw[vi * VE + k]);
+                    if (wsb) wsb[vi * VE + k] += dv[k];
                 }
             }
             store_vec<T, VE>(dxr + int64_t(vi) * VE, o);
@@ -641,14 +642,14 @@ inline bool rr_plan(RrGeom& g, int& tpr, size_t& smem, const RowArgs& a, size_t 
     return true;
 }
 
-template <typename T, bool LN>
+template <typename T, bool LN, bool DB>
 const void* rr_fn(int tpr) {
     switch (tpr) {
-    case 32: return (const void*)&row_bwd_ring_kernel<T, LN, 32>;
-    case 64: return (const void*)&row_bwd_ring_kernel<T, LN, 64>;
-    case 128: return (const void*)&row_bwd_ring_kernel<T, LN, 128>;
-    case 256: return (const void*)&row_bwd_ring_kernel<T, LN, 256>;
-    default: return (const void*)&row_bwd_ring_kernel<T, LN, 512>;
+    case 32: return (const void*)&row_bwd_ring_kernel<T, LN, 32, DB>;
+    case 64: return (const void*)&row_bwd_ring_kernel<T, LN, 64, DB>;
+    case 128: return (const void*)&row_bwd_ring_kernel<T, LN, 128, DB>;
+    case 256: return (const void*)&row_bwd_ring_kernel<T, LN, 256, DB>;
+    default: return (const void*)&row_bwd_ring_kernel<T, LN, 512, DB>;
     }
 }
 
@@ -721,7 +722,7 @@ template <typename T>
 nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
-    const bool want = a.dw || (layernorm && a.db);
+    const bool want = a.dw || a.db;
     if (!want) a.ws_dw = a.ws_db = nullptr;
     const int ve = vec ? kVec<T> : 1;
     RrGeom rg;
@@ -733,7 +734,8 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     int64_t groups, p;
     int block = kRrThreads;
     if (ring) {
-        fn = layernorm ? rr_fn<T, true>(rtpr) : rr_fn<T, false>(rtpr);
+        fn = layernorm ? rr_fn<T, true, true>(rtpr)
+                       : (a.ws_db ? rr_fn<T, false, true>(rtpr) : rr_fn<T, false, false>(rtpr));
         groups = rg.chunks;
         p = d->sms;
     } else {
@@ -766,7 +768,7 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     int P_ = P;
     int cols = a.cols;
     T* dw = reinterpret_cast<T*>(a.dw);
-    T* db = layernorm ? reinterpret_cast<T*>(a.db) : nullptr;
+    T* db = reinterpret_cast<T*>(a.db);
     void* cargs[] = {&wsw, &wsb, &P_, &cols, &dw, &db};
     return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((a.cols + 31) / 32, 2), dim3(kColsumWarps * 32),
                       cargs, s);

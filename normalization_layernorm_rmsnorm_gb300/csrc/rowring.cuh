@@ -130,7 +130,9 @@ __device__ __forceinline__ void rr_partial_row(const float (&acc)[VPT][VE], floa
     }
 }
 
-template <typename T, bool LN, int TPR>
+// DB: accumulate db = sum dy (LayerNorm, or RMSNorm with a bias); a template
+// parameter so that RMSNorm without one keeps those registers free.
+template <typename T, bool LN, int TPR, bool DB>
 __global__ void __launch_bounds__(kRrThreads, 1)
 row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
     constexpr int VE = kVec<T>;
@@ -240,6 +242,7 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
                             } else {
                                 o[k] = rs * (gw - xv[k] * c2);
                                 accw[j][k] = fmaf(dv[k], xv[k] * rs, accw[j][k]);
+                                if constexpr (DB) accb[j][k] += dv[k];
                             }
                         }
                         store_vec<T, VE>(dxr + int64_t(vi) * VE, o);
@@ -257,7 +260,7 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
         float* part = reinterpret_cast<float*>(ring);
         if (a.ws_dw)
             rr_partial_row<TPR, VPT, VE, RPC>(accw, a.ws_dw + int64_t(blockIdx.x) * cols, part, group, t, cols);
-        if constexpr (LN) {
+        if constexpr (DB) {
             if (a.ws_db)
                 rr_partial_row<TPR, VPT, VE, RPC>(accb, a.ws_db + int64_t(blockIdx.x) * cols, part, group, t, cols);
         }

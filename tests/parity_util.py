@@ -83,28 +83,29 @@ def run_row(kind, inp, dtype, eps, with_w=True, with_b=True, want_dw=True, want_
     x = dev(inp["x"])
     dy = dev(inp["dy"])
     w = dev(inp.get("w")) if with_w else None
-    b = dev(inp.get("b")) if (with_b and kind == "layernorm") else None
+    # RMSNorm takes its optional bias when the inputs carry one
+    b = dev(inp.get("b")) if (with_b and (kind == "layernorm" or "b" in inp)) else None
     rows, cols = x.shape
     y = empty(x.shape, dtype)
     dx = empty(x.shape, dtype)
     rstd = torch.empty(rows, dtype=torch.float32, device="cuda")
     mean = torch.empty(rows, dtype=torch.float32, device="cuda")
     dw = empty((cols,), dtype) if want_dw else None
-    db = empty((cols,), dtype) if (want_db and kind == "layernorm") else None
+    db = empty((cols,), dtype) if (want_db and (kind == "layernorm" or b is not None)) else None
     if kind == "layernorm":
         nrm.nrm_layernorm_fwd(x, w, b, y, mean, rstd, eps)
         ws = workspace(nrm.NRM_OP_LAYERNORM_BWD, rows, cols, DT_CODE[dtype])
         nrm.nrm_layernorm_bwd(dy, x, w, mean, rstd, dx, dw, db, ws)
     else:
-        nrm.nrm_rmsnorm_fwd(x, w, y, rstd, eps)
+        nrm.nrm_rmsnorm_fwd(x, w, y, rstd, eps, b=b)
         ws = workspace(nrm.NRM_OP_RMSNORM_BWD, rows, cols, DT_CODE[dtype])
-        nrm.nrm_rmsnorm_bwd(dy, x, w, rstd, dx, dw, ws)
+        nrm.nrm_rmsnorm_bwd(dy, x, w, rstd, dx, dw, ws, db=db)
     nrm.nrm_sync_status()
     out = dict(y=host(y), dx=host(dx), rstd=host(rstd))
     if kind == "layernorm":
         out["mean"] = host(mean)
-        if db is not None:
-            out["db"] = host(db)
+    if db is not None:
+        out["db"] = host(db)
     if dw is not None:
         out["dw"] = host(dw)
     return out
@@ -119,9 +120,9 @@ def oracle_row(orc, kind, inp, eps, with_w=True, with_b=True):
         y, mean, rstd = orc.layernorm_fwd(x, w, b, eps)
         dx, dw, db = orc.layernorm_bwd(dy, x, w, eps)
         return dict(y=y, mean=mean, rstd=rstd, dx=dx, dw=dw, db=db)
-    y, rstd = orc.rmsnorm_fwd(x, w, eps)
-    dx, dw = orc.rmsnorm_bwd(dy, x, w, eps)
-    return dict(y=y, rstd=rstd, dx=dx, dw=dw)
+    y, rstd = orc.rmsnorm_fwd(x, w, eps, b=b)
+    dx, dw, db = orc.rmsnorm_bwd(dy, x, w, eps, with_db=True)
+    return dict(y=y, rstd=rstd, dx=dx, dw=dw, db=db)
 
 
 def compare_row(got, want, dtype, tag):

@@ -67,11 +67,11 @@ P = 1 << 20  # a fake, aligned, non-null address: never dereferenced (validation
     # cols = 0
     (lambda L: L.nrm_layernorm_fwd(P, None, None, P * 2, None, None, 4, 0, 1e-5, 0, None), 1),
     # negative rows
-    (lambda L: L.nrm_rmsnorm_fwd(P, None, P * 2, None, -1, 8, 1e-5, 0, None), 1),
+    (lambda L: L.nrm_rmsnorm_fwd(P, None, None, P * 2, None, -1, 8, 1e-5, 0, None), 1),
     # eps <= 0
-    (lambda L: L.nrm_rmsnorm_fwd(P, None, P * 2, None, 4, 8, 0.0, 0, None), 1),
+    (lambda L: L.nrm_rmsnorm_fwd(P, None, None, P * 2, None, 4, 8, 0.0, 0, None), 1),
     # unknown dtype
-    (lambda L: L.nrm_rmsnorm_fwd(P, None, P * 2, None, 4, 8, 1e-5, 7, None), 1),
+    (lambda L: L.nrm_rmsnorm_fwd(P, None, None, P * 2, None, 4, 8, 1e-5, 7, None), 1),
     # element-misaligned fp32 pointer
     (lambda L: L.nrm_layernorm_fwd(P + 2, None, None, P * 2, None, None, 4, 8, 1e-5, 0, None), 1),
     # in place

@@ -143,3 +143,25 @@ def test_row_backward_ring_many_chunks(orc, kind, dtype, rows, cols):
     got = run_row(kind, inp, dtype, cfg.eps)
     want = oracle_row(orc, kind, inp, cfg.eps)
     compare_row(got, want, dtype, f"{kind} {dtype} [{rows},{cols}]")
+
+
+RMS_BIAS = [(300, 256), (300, 768), (97, 1023), (5, 40000), (2000, 4096)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("shape", RMS_BIAS, ids=[f"{r}x{c}" for r, c in RMS_BIAS])
+def test_rmsnorm_with_bias(orc, dtype, shape):
+    # the ring backward (aligned rows), the register kernels (1023 columns are
+    # not 16-byte rows), the wide-row kernels (40000 columns)
+    rows, cols = shape
+    seed = 60 + cols % 97
+    inp = {
+        "x": synth.random_tensor(seed, 1, (rows, cols), dtype, std=1.3),
+        "w": synth.store(1 + 0.1 * synth.normal(seed, 2, cols), dtype, (cols,)),
+        "b": synth.store(0.2 * synth.normal(seed, 3, cols), dtype, (cols,)),
+        "dy": synth.random_tensor(seed, 4, (rows, cols), dtype),
+    }
+    got = run_row("rmsnorm", inp, dtype, 1e-6)
+    want = oracle_row(orc, "rmsnorm", inp, 1e-6)
+    assert "db" in got
+    compare_row(got, want, dtype, f"rms+bias {dtype} [{rows},{cols}]")
