@@ -30,7 +30,11 @@
  *   - ReLU'(z) = 1 for z > 0 and 0 otherwise; GELU is the exact erf form.
  *   - The activations with a parameter a (the article encodes it in the name):
  *     leaky_relu(z) = z for z > 0, else a*z (derivative 1, else a);
- *     elu(z) = z for z > 0, else a*(e^z - 1) (derivative 1, else a*e^z).
+ *     elu(z) = z for z > 0, else a*(e^z - 1) (derivative 1, else a*e^z);
+ *     celu(z) = z for z > 0, else a*(e^(z/a) - 1) (derivative 1, else e^(z/a)).
+ *   - sigmoid(z) = 1/(1 + e^-z); selu(z) = L*z for z > 0, else L*A*(e^z - 1),
+ *     with the constants L, A of Klambauer et al., "Self-Normalizing Neural
+ *     Networks" (2017).
  *   - Dropout draws Philox4x32-10 with key (seed, 0) and counter (e / 4, 0, 0) for
  *     element e, which takes output word e % 4 as the uniform (word >> 8) * 2^-24;
  *     the element is dropped when that value is below drop_p (single precision).
@@ -278,6 +282,10 @@ void oracle_layernorm_cf_bwd(int64_t n, int64_t c, int64_t l, const double *dy,
  * the standard ones (the articles give none): silu(z) = z * sigmoid(z),
  * mish(z) = z * tanh(softplus(z)), softplus(z) = log(1 + e^z). */
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+/* SELU's scale and alpha (Klambauer et al. 2017, the fixed point of their
+ * self-normalising mapping) */
+#define SELU_LAMBDA 1.0507009873554804934193349852946
+#define SELU_ALPHA 1.6732632423543772848170429916717
 static double softplus(double z) { return z > 0.0 ? z + log1p(exp(-z)) : log1p(exp(z)); }
 
 static double act_forward(int act, double param, double z)
@@ -286,6 +294,9 @@ static double act_forward(int act, double param, double z)
     case ORACLE_ACT_RELU: return z > 0.0 ? z : 0.0;
     case ORACLE_ACT_LEAKY_RELU: return z > 0.0 ? z : param * z;
     case ORACLE_ACT_ELU: return z > 0.0 ? z : param * expm1(z);
+    case ORACLE_ACT_SIGMOID: return sigmoid(z);
+    case ORACLE_ACT_CELU: return z > 0.0 ? z : param * expm1(z / param);
+    case ORACLE_ACT_SELU: return z > 0.0 ? SELU_LAMBDA * z : SELU_LAMBDA * SELU_ALPHA * expm1(z);
     case ORACLE_ACT_GELU: return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
     case ORACLE_ACT_SILU: return z * sigmoid(z);
     case ORACLE_ACT_MISH: return z * tanh(softplus(z));
@@ -299,6 +310,12 @@ static double act_derivative(int act, double param, double z)
     case ORACLE_ACT_RELU: return z > 0.0 ? 1.0 : 0.0;
     case ORACLE_ACT_LEAKY_RELU: return z > 0.0 ? 1.0 : param;
     case ORACLE_ACT_ELU: return z > 0.0 ? 1.0 : param * exp(z);
+    case ORACLE_ACT_SIGMOID: {
+        double s = sigmoid(z);
+        return s * (1.0 - s);
+    }
+    case ORACLE_ACT_CELU: return z > 0.0 ? 1.0 : exp(z / param);
+    case ORACLE_ACT_SELU: return z > 0.0 ? SELU_LAMBDA : SELU_LAMBDA * SELU_ALPHA * exp(z);
     case ORACLE_ACT_GELU: {
         double cdf = 0.5 * (1.0 + erf(z / sqrt(2.0)));
         double pdf = exp(-0.5 * z * z) / sqrt(2.0 * M_PI);

@@ -28,9 +28,10 @@ import os
 import numpy as np
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-ACT = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "mish": 4, "leaky_relu": 5, "elu": 6}
+ACT = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "mish": 4, "leaky_relu": 5, "elu": 6,
+       "sigmoid": 7, "celu": 8, "selu": 9}
 # the parameter the activations that take one are exercised with (slope, alpha)
-ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3}
+ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3, "celu": 0.7}
 ALL_ACTS = tuple(ACT)
 
 
@@ -316,6 +317,12 @@ def _torch_bn_forward(x, res, w, b, rm, rv, eps, momentum, training, act):
         return F.leaky_relu(z, ACT_PARAM[act])
     if act == "elu":
         return F.elu(z, ACT_PARAM[act])
+    if act == "sigmoid":
+        return torch.sigmoid(z)
+    if act == "celu":
+        return F.celu(z, ACT_PARAM[act])
+    if act == "selu":
+        return F.selu(z)
     return z
 
 
@@ -339,7 +346,7 @@ def pin_batchnorm_vs_torch(o):
                                       act=ACT[act], running_mean=rm0, running_var=rv0,
                                       act_param=ACT_PARAM.get(act, 0.0))
                 tag = f"batchnorm training={training} act={act} res={with_res}"
-                _close(out["y"], yt, 1e-12, 1e-12, tag + " y vs torch")
+                _close(out["y"], yt, _torch_rtol(act, 1e-12), 1e-12, tag + " y vs torch")
                 _close(out["running_mean"], rm_t.numpy(), 1e-13, 1e-15, tag + " running_mean")
                 _close(out["running_var"], rv_t.numpy(), 1e-13, 1e-15, tag + " running_var")
 
@@ -396,6 +403,31 @@ def pin_leaky_relu_elu_values(o):
         else:
             _close(y[1:], [-a / 2.0, 0.5], 1e-15, 1e-16, "elu values")
             _close(dx[1:], [a / 2.0, 1.0], 1e-15, 1e-16, "elu derivative")
+
+
+def pin_sigmoid_celu_selu_values(o):
+    # z = x as above; closed forms: sigmoid(ln 3) = 3/4, sigmoid'(ln 3) = 3/16;
+    # celu(-a ln 2) = -a/2, celu'(-a ln 2) = 1/2; selu(1) = L, selu'(-ln 2) = L*A/2
+    rm, rv = np.zeros(1), np.array([0.75])
+    lam, alp = 1.0507009873554805, 1.6732632423543772
+
+    def run(act, zs, a=0.0):
+        z = np.array(zs).reshape(1, 1, len(zs))
+        y = o.batchnorm_fwd(z, eps=0.25, training=False, act=ACT[act], running_mean=rm,
+                            running_var=rv, act_param=a)["y"].ravel()
+        dx = o.batchnorm_bwd(np.ones_like(z), z, None, np.ones(1), np.zeros(1), rm, rv, eps=0.25,
+                             training=False, act=ACT[act], act_param=a)[0].ravel()
+        return y, dx
+    y, dx = run("sigmoid", [math.log(3.0)])
+    _close(y, [0.75], 1e-15, 0, "sigmoid(ln 3)")
+    _close(dx, [3.0 / 16.0], 1e-15, 0, "sigmoid'(ln 3)")
+    a = 0.8
+    y, dx = run("celu", [-a * math.log(2.0), 1.5], a)
+    _close(y, [-a / 2.0, 1.5], 1e-15, 1e-16, "celu values")
+    _close(dx, [0.5, 1.0], 1e-15, 1e-16, "celu derivative")
+    y, dx = run("selu", [1.0, -math.log(2.0)])
+    _close(y, [lam, -lam * alp / 2.0], 1e-15, 1e-16, "selu values")
+    _close(dx, [lam, lam * alp / 2.0], 1e-15, 1e-16, "selu derivative")
 
 
 def pin_batchnorm_mask_layout(o):
@@ -492,7 +524,8 @@ def pin_batchnorm_bwd_vs_torch(o):
     r = _rng(16)
     n, c, l = 3, 4, 6
     acts = {"none": lambda z: z, "gelu": lambda z: F.gelu(z, approximate="none"), "silu": F.silu,
-            "mish": F.mish, "elu": lambda z: F.elu(z, ACT_PARAM["elu"])}
+            "mish": F.mish, "elu": lambda z: F.elu(z, ACT_PARAM["elu"]), "sigmoid": torch.sigmoid,
+            "celu": lambda z: F.celu(z, ACT_PARAM["celu"]), "selu": F.selu}
     for training in (True, False):
         for act in acts:
             x = torch.tensor(r.normal(size=(n, c, l)) * 1.5, requires_grad=True)
@@ -511,10 +544,11 @@ def pin_batchnorm_bwd_vs_torch(o):
                                                eps=1e-5, training=training, act=ACT[act],
                                                act_param=ACT_PARAM.get(act, 0.0))
             tag = f"batchnorm bwd vs torch training={training} act={act}"
-            _close(dx, x.grad.numpy(), 1e-10, 1e-12, tag + " dx")
-            _close(dres, res.grad.numpy(), 1e-10, 1e-12, tag + " dres")
-            _close(dw, w.grad.numpy(), 1e-10, 1e-12, tag + " dw")
-            _close(db, b.grad.numpy(), 1e-10, 1e-12, tag + " db")
+            rt = _torch_rtol(act, 1e-10)
+            _close(dx, x.grad.numpy(), rt, 1e-12, tag + " dx")
+            _close(dres, res.grad.numpy(), rt, 1e-12, tag + " dres")
+            _close(dw, w.grad.numpy(), rt, 1e-12, tag + " dw")
+            _close(db, b.grad.numpy(), rt, 1e-12, tag + " db")
 
 
 def pin_batchnorm_bwd_mask_matches_recompute(o):
@@ -645,13 +679,22 @@ def pin_dropout_independence(o):
         assert abs(agree - 0.5) < 6 * sigma, f"dropout masks {what}: agreement {agree}"
 
 
+# torch evaluates CELU with 1/alpha held in single precision (its elu kernel's
+# input scale: a relative error of about 3e-8 * |z/alpha| in e^(z/alpha)), so
+# CELU is compared with torch to 1e-6 relative; the finite differences and the
+# closed forms pin it exactly
+def _torch_rtol(act, rtol):
+    return max(rtol, 1e-6) if act in (8, "celu") else rtol
+
+
 def _act_torch():
     """act code -> (torch function, the parameter passed to the oracle)."""
     import torch
     import torch.nn.functional as F
-    lk, al = ACT_PARAM["leaky_relu"], ACT_PARAM["elu"]
+    lk, al, ca = ACT_PARAM["leaky_relu"], ACT_PARAM["elu"], ACT_PARAM["celu"]
     return {0: (lambda t: t, 0.0), 1: (torch.relu, 0.0), 2: (F.gelu, 0.0), 3: (F.silu, 0.0),
-            4: (F.mish, 0.0), 5: (lambda t: F.leaky_relu(t, lk), lk), 6: (lambda t: F.elu(t, al), al)}
+            4: (F.mish, 0.0), 5: (lambda t: F.leaky_relu(t, lk), lk), 6: (lambda t: F.elu(t, al), al),
+            7: (torch.sigmoid, 0.0), 8: (lambda t: F.celu(t, ca), ca), 9: (F.selu, 0.0)}
 
 
 def pin_act_dropout_no_drop_is_activation(o):
@@ -660,7 +703,7 @@ def pin_act_dropout_no_drop_is_activation(o):
     x = _rng(40).normal(size=4096) * 3
     for act, (fn, prm) in _act_torch().items():
         y = o.act_dropout_fwd(x, act, 0.0, 9, act_param=prm)
-        _close(y, fn(torch.from_numpy(x)).numpy(), 1e-15, 1e-14, f"act {act} without dropout")
+        _close(y, fn(torch.from_numpy(x)).numpy(), _torch_rtol(act, 1e-15), 1e-14, f"act {act} without dropout")
 
 
 def pin_act_dropout_inverted_scale(o):
@@ -673,7 +716,7 @@ def pin_act_dropout_inverted_scale(o):
     for act, (fn, prm) in _act_torch().items():
         y = o.act_dropout_fwd(x, act, p, 4321, act_param=prm)
         a = fn(torch.from_numpy(x)).numpy()
-        _close(y[keep], a[keep] / (1 - p), 1e-15, 1e-14, f"act {act} kept elements")
+        _close(y[keep], a[keep] / (1 - p), _torch_rtol(act, 1e-15), 1e-14, f"act {act} kept elements")
         assert not y[~keep].any(), f"act {act}: dropped elements must be 0"
     # the mean is preserved in expectation (inverted dropout)
     xs = np.abs(_rng(42).normal(size=200_000)) + 1.0
@@ -708,7 +751,7 @@ def pin_act_dropout_bwd_vs_torch(o):
             x.grad = None
         (fn(x) * keep / (1 - p)).backward(torch.from_numpy(dy))
         dx = o.act_dropout_bwd(dy, x.detach().numpy(), act, p, 999, act_param=prm)
-        _close(dx, x.grad.numpy(), 1e-14, 1e-13, f"act {act} dx vs torch")
+        _close(dx, x.grad.numpy(), _torch_rtol(act, 1e-14), 1e-13, f"act {act} dx vs torch")
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

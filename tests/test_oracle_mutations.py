@@ -44,6 +44,12 @@ MUTATIONS = {
                                       "case ORACLE_ACT_LEAKY_RELU: return z > 0.0 ? 1.0 : 0.0;"),
     "elu_without_minus_one": ("case ORACLE_ACT_ELU: return z > 0.0 ? z : param * expm1(z);",
                               "case ORACLE_ACT_ELU: return z > 0.0 ? z : param * exp(z);"),
+    "sigmoid_grad_missing_one_minus": ("        return s * (1.0 - s);\n    }\n    case ORACLE_ACT_CELU",
+                                       "        return s;\n    }\n    case ORACLE_ACT_CELU"),
+    "celu_without_scaled_exponent": ("case ORACLE_ACT_CELU: return z > 0.0 ? z : param * expm1(z / param);",
+                                     "case ORACLE_ACT_CELU: return z > 0.0 ? z : param * expm1(z);"),
+    "selu_positive_side_unscaled": ("case ORACLE_ACT_SELU: return z > 0.0 ? SELU_LAMBDA * z :",
+                                    "case ORACLE_ACT_SELU: return z > 0.0 ? z :"),
     "elu_grad_drops_exp": ("case ORACLE_ACT_ELU: return z > 0.0 ? 1.0 : param * exp(z);",
                            "case ORACLE_ACT_ELU: return z > 0.0 ? 1.0 : param;"),
     "bn_gelu_grad_drops_pdf_term": ("return cdf + z * pdf;", "return cdf;"),
