@@ -80,7 +80,10 @@ typedef enum nrm_dtype { NRM_F32 = 0, NRM_F16 = 1, NRM_BF16 = 2 } nrm_dtype;
  * passed as act_param (the [AF] article encodes it in the name, e.g.
  * "leaky_relu_0.01"): LEAKY_RELU is z for z > 0, else act_param*z (derivative
  * 1, else act_param); ELU is z for z > 0, else act_param*(e^z - 1) (derivative
- * 1, else act_param*e^z).  act_param is ignored by the others. */
+ * 1, else act_param*e^z); CELU is z for z > 0, else act_param*(e^(z/act_param)
+ * - 1) (derivative 1, else e^(z/act_param); act_param != 0).  SIGMOID is
+ * 1/(1 + e^-z).  SELU is L*z for z > 0, else L*A*(e^z - 1), L and A the
+ * constants of Klambauer et al. (2017).  act_param is ignored by the others. */
 typedef enum nrm_act {
     NRM_ACT_NONE = 0,
     NRM_ACT_RELU = 1,
@@ -88,7 +91,10 @@ typedef enum nrm_act {
     NRM_ACT_SILU = 3,
     NRM_ACT_MISH = 4,
     NRM_ACT_LEAKY_RELU = 5,
-    NRM_ACT_ELU = 6
+    NRM_ACT_ELU = 6,
+    NRM_ACT_SIGMOID = 7,
+    NRM_ACT_CELU = 8,
+    NRM_ACT_SELU = 9
 } nrm_act;
 
 /* Operations that need a workspace (for nrm_workspace_bytes). */

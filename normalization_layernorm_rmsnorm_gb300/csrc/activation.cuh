@@ -7,14 +7,24 @@
 // input and uses the error-function GELU; the normalization article's BatchNorm
 // section lists SiLU and Mish among the fusable activations (their formulas
 // are the standard ones: silu(z) = z*sigmoid(z), mish(z) = z*tanh(softplus(z))),
-// and the activation article's list (section 六) has leaky_relu and elu, whose
-// parameter prm (slope, alpha) the article encodes in the name:
-// leaky_relu(z) = z > 0 ? z : prm*z, elu(z) = z > 0 ? z : prm*(e^z - 1).
+// and the activation article's list (section 六) has leaky_relu, elu and celu,
+// whose parameter prm (slope, alpha) the article encodes in the name:
+// leaky_relu(z) = z > 0 ? z : prm*z, elu(z) = z > 0 ? z : prm*(e^z - 1),
+// celu(z) = z > 0 ? z : prm*(e^(z/prm) - 1); it also names sigmoid and SELU
+// (section 七), selu(z) = L*z for z > 0, else L*A*(e^z - 1), with the constants
+// of Klambauer et al., "Self-Normalizing Neural Networks" (2017).
 #pragma once
 
 #include "libnorm.h"
 
 namespace nrm {
+
+constexpr float kSeluLambda = 1.0507009873554805f;
+constexpr float kSeluAlpha = 1.6732632423543772f;
+// The template value of the kernels that dispatch the less common activations
+// (sigmoid, CELU, SELU) at run time, so that each does not cost a set of
+// instantiations.
+constexpr int kActGeneric = 100;
 
 // softplus(z) = log(1 + e^z), without overflow for large z
 __device__ __forceinline__ float softplus_f(float z) {
@@ -25,6 +35,9 @@ __device__ __forceinline__ float act_forward(int act, float z, float prm) {
     if (act == NRM_ACT_RELU) return z > 0.f ? z : 0.f;
     if (act == NRM_ACT_LEAKY_RELU) return z > 0.f ? z : prm * z;
     if (act == NRM_ACT_ELU) return z > 0.f ? z : prm * expm1f(z);
+    if (act == NRM_ACT_SIGMOID) return 1.f / (1.f + expf(-z));
+    if (act == NRM_ACT_CELU) return z > 0.f ? z : prm * expm1f(z / prm);
+    if (act == NRM_ACT_SELU) return z > 0.f ? kSeluLambda * z : (kSeluLambda * kSeluAlpha) * expm1f(z);
     if (act == NRM_ACT_GELU) return 0.5f * z * (1.f + erff(z * 0.70710678118654752f));
     if (act == NRM_ACT_SILU) return z / (1.f + expf(-z));
     if (act == NRM_ACT_MISH) return z * tanhf(softplus_f(z));
@@ -36,6 +49,12 @@ __device__ __forceinline__ float act_derivative(int act, float z, float prm) {
     if (act == NRM_ACT_RELU) return z > 0.f ? 1.f : 0.f;
     if (act == NRM_ACT_LEAKY_RELU) return z > 0.f ? 1.f : prm;
     if (act == NRM_ACT_ELU) return z > 0.f ? 1.f : prm * expf(z);
+    if (act == NRM_ACT_SIGMOID) {
+        const float sg = 1.f / (1.f + expf(-z));
+        return sg * (1.f - sg);
+    }
+    if (act == NRM_ACT_CELU) return z > 0.f ? 1.f : expf(z / prm);
+    if (act == NRM_ACT_SELU) return z > 0.f ? kSeluLambda : (kSeluLambda * kSeluAlpha) * expf(z);
     if (act == NRM_ACT_GELU) {
         const float cdf = 0.5f * (1.f + erff(z * 0.70710678118654752f));
         const float pdf = expf(-0.5f * z * z) * 0.39894228040143268f;
@@ -56,15 +75,17 @@ __device__ __forceinline__ float act_derivative(int act, float z, float prm) {
 // The same for an activation fixed at compile time (the ring and group
 // kernels are instantiated per activation, so the hot loops carry one).
 template <int ACT>
-__device__ __forceinline__ float act_forward_c(float z, float prm) {
+__device__ __forceinline__ float act_forward_c(float z, float prm, int act_rt) {
     if constexpr (ACT == NRM_ACT_RELU) return z > 0.f ? z : 0.f;
     else if constexpr (ACT == NRM_ACT_NONE) return z;
+    else if constexpr (ACT == kActGeneric) return act_forward(act_rt, z, prm);
     else return act_forward(ACT, z, prm);
 }
 template <int ACT>
-__device__ __forceinline__ float act_derivative_c(float z, float prm) {
+__device__ __forceinline__ float act_derivative_c(float z, float prm, int act_rt) {
     if constexpr (ACT == NRM_ACT_RELU) return z > 0.f ? 1.f : 0.f;
     else if constexpr (ACT == NRM_ACT_NONE) return 1.f;
+    else if constexpr (ACT == kActGeneric) return act_derivative(act_rt, z, prm);
     else return act_derivative(ACT, z, prm);
 }
 
@@ -82,6 +103,9 @@ auto with_act(int act, F&& f) {
     case NRM_ACT_MISH: return f(ActTag<NRM_ACT_MISH>{});
     case NRM_ACT_LEAKY_RELU: return f(ActTag<NRM_ACT_LEAKY_RELU>{});
     case NRM_ACT_ELU: return f(ActTag<NRM_ACT_ELU>{});
+    case NRM_ACT_SIGMOID:
+    case NRM_ACT_CELU:
+    case NRM_ACT_SELU: return f(ActTag<kActGeneric>{});
     default: return f(ActTag<NRM_ACT_NONE>{});
     }
 }

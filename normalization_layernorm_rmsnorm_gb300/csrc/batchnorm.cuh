@@ -827,7 +827,7 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
                             float z = fmaf(v[k], scale, shift);
                             if (res) z += rr[k];
                             nib |= uint32_t(z > 0.f) << k;
-                            o[k] = act_forward_c<ACT>(z, a.act_param);
+                            o[k] = act_forward_c<ACT>(z, a.act_param, a.act);
                         }
                         store_vec_pol<T, VE>(y + (p.seg * g.lv + p.v) * VE, o, pol_stream);
                     }
@@ -1157,7 +1157,7 @@ __device__ __forceinline__ void ring_dz(const BnArgs& a, bool use_mask, bool nee
 #pragma unroll
         for (int k = 0; k < VE; ++k) {
             const float z = fmaf(xv[k], scale, shift) + r[k];
-            dz[k] = dyv[k] * act_derivative_c<ACT>(z, a.act_param);
+            dz[k] = dyv[k] * act_derivative_c<ACT>(z, a.act_param, a.act);
         }
     } else {
 #pragma unroll

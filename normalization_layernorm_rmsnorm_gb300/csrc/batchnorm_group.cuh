@@ -188,7 +188,7 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
             }
             float z = fmaf(xv[k], coef[j].x, coef[j].y);
             if (res) z += rv[k];
-            ov[k] = act_forward_c<ACT>(z, a.act_param);
+            ov[k] = act_forward_c<ACT>(z, a.act_param, a.act);
         }
         store_vec_pol<T, VE>(y + (int64_t(p.n0 + s) * g.c + p.ch0) * g.l + o, ov, pol);
     }
@@ -270,7 +270,7 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     // dz of element e of segment (s, j)
     auto dz_of = [&](int s, int j, int e, float dyv, float xv, float rv) {
         if (use_mask) return ((tm[(s * g.G + j) * g.words + (e >> 5)] >> (e & 31)) & 1u) ? dyv : 0.f;
-        if (need_z) return dyv * act_derivative_c<ACT>(fmaf(xv, prm[j].z, prm[j].w) + rv, a.act_param);
+        if (need_z) return dyv * act_derivative_c<ACT>(fmaf(xv, prm[j].z, prm[j].w) + rv, a.act_param, a.act);
         return dyv;
     };
 

@@ -46,7 +46,8 @@ struct DropArgs {
     uint32_t thresh_w;  // ceil(p * 2^24) << 8: element kept when its word >= thresh_w (p < 1)
     int drop_all;       // p == 1: every element dropped
     float scale;        // 1 / (1 - p)
-    float act_param;    // slope (leaky_relu) or alpha (elu)
+    float act_param;    // slope (leaky_relu) or alpha (elu, celu)
+    int act;            // the activation (read by the run-time dispatched instantiation)
 };
 
 // Philox4x32 with 10 rounds on counter c, with the round keys of `a`.
@@ -74,8 +75,8 @@ __device__ __forceinline__ uint32_t word_of(const uint4& r, int k) {
 template <int ACT, bool BWD>
 __device__ __forceinline__ float drop_elem(float xv, float dyv, uint32_t word, const DropArgs& a) {
     if (word < a.thresh_w) return 0.f;
-    if constexpr (BWD) return dyv * a.scale * act_derivative_c<ACT>(xv, a.act_param);
-    else return act_forward_c<ACT>(xv, a.act_param) * a.scale;
+    if constexpr (BWD) return dyv * a.scale * act_derivative_c<ACT>(xv, a.act_param, a.act);
+    else return act_forward_c<ACT>(xv, a.act_param, a.act) * a.scale;
 }
 
 // One element by scalar accesses (tails and unaligned tensors).
@@ -178,6 +179,7 @@ nrm_status act_dropout(const void* x, const void* dy, void* out, int64_t count, 
                        uint32_t seed, nrm_dtype dt, bool bwd, bool vec, cudaStream_t s) {
     DropArgs a{};
     a.act_param = act_param;
+    a.act = act;
     a.x = x;
     a.dy = dy;
     a.y = bwd ? nullptr : out;

@@ -28,10 +28,11 @@ from normalization_layernorm_rmsnorm_gb300 import synth
 
 TOL = {"f32": (1e-5, 1e-5), "f16": (2e-2, 1e-2), "bf16": (2e-2, 1e-2)}
 # the parameter the parameterised activations are tested with (slope, alpha)
-ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3}
+ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3, "celu": 0.7}
+SELU_L, SELU_A = 1.0507009873554805, 1.6732632423543772
 # activations with a kink at 0 whose branch the kernel (fp32) and the oracle
 # (double) may decide differently within RELU_BAND
-KINKED = ("relu", "leaky_relu", "elu")
+KINKED = ("relu", "leaky_relu", "elu", "selu")
 STAT_TOL = (1e-5, 1e-5)
 RELU_BAND = 1e-4
 TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
@@ -191,7 +192,8 @@ def oracle_bn(orc, inp, eps, momentum, training, act, with_res, with_affine=True
     import oracle as oracle_mod
     a = {"none": oracle_mod.ACT_NONE, "relu": oracle_mod.ACT_RELU, "gelu": oracle_mod.ACT_GELU,
          "silu": oracle_mod.ACT_SILU, "mish": oracle_mod.ACT_MISH, "leaky_relu": oracle_mod.ACT_LEAKY_RELU,
-         "elu": oracle_mod.ACT_ELU}[act]
+         "elu": oracle_mod.ACT_ELU, "sigmoid": oracle_mod.ACT_SIGMOID, "celu": oracle_mod.ACT_CELU,
+         "selu": oracle_mod.ACT_SELU}[act]
     prm = ACT_PARAM.get(act, 0.0)
     x = inp["x"].f64()
     res = inp["res"].f64() if with_res else None
@@ -209,8 +211,10 @@ def oracle_bn(orc, inp, eps, momentum, training, act, with_res, with_affine=True
         amb = np.abs(z) < RELU_BAND
         out["amb"] = amb
         # the other branch's output at the kink: relu 0 | z, leaky a*z | z, elu a*(e^z - 1) | z
-        neg = {"relu": 0.0 * z, "leaky_relu": prm * z, "elu": prm * np.expm1(z)}[act]
-        out["y_alt"] = np.where(z > 0, neg, z)
+        neg = {"relu": 0.0 * z, "leaky_relu": prm * z, "elu": prm * np.expm1(z),
+               "selu": SELU_L * SELU_A * np.expm1(z)}[act]
+        pos = SELU_L * z if act == "selu" else z
+        out["y_alt"] = np.where(z > 0, neg, pos)
         if act == "relu" and amb.any():
             bits = unpack_mask(f["mask"], *x.shape)
             out["bwd_flipped"] = orc.batchnorm_bwd(dy, x, res, w, b, rm0, rv0, eps, training, a,

@@ -98,7 +98,7 @@ P = 1 << 20  # a fake, aligned, non-null address: never dereferenced (validation
                                    4, 1e-5, 0.1, 1, 2, 0.0, 0, None, 0, None), 1),
     # unknown activation
     (lambda L: L.nrm_batchnorm_bwd(P, P * 2, None, None, None, P * 3, P * 4, None, P * 5, None, None,
-                                   None, 2, 3, 4, 1, 9, 0.0, 0, None, 0, None), 1),
+                                   None, 2, 3, 4, 1, 12, 0.0, 0, None, 0, None), 1),
     # a channel with 2^31 elements
     (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, None, None, None, None, None,
                                    1 << 16, 1, 1 << 15, 1e-5, 0.1, 1, 0, 0.0, 0, None, 0, None), 2),
@@ -108,12 +108,15 @@ P = 1 << 20  # a fake, aligned, non-null address: never dereferenced (validation
     (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 2, 0.0, 1.5, 7, 1, None), 1),
     (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 2, 0.0, float("nan"), 7, 1, None), 1),
     (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, -1, 2, 0.0, 0.5, 7, 1, None), 1),
-    (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, 16, 9, 0.0, 0.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, 16, 11, 0.0, 0.5, 7, 1, None), 1),
     (lambda L: L.nrm_act_dropout_fwd(P, None, 16, 2, 0.0, 0.5, 7, 1, None), 1),
     # a non-finite activation parameter (BatchNorm and dropout)
     (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, None, None, None, None, None, 2, 3,
                                    4, 1e-5, 0.1, 1, 5, float("inf"), 0, None, 0, None), 1),
     (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 6, float("nan"), 0.5, 7, 1, None), 1),
+    # CELU with alpha 0, an activation past the last one
+    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 8, 0.0, 0.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 10, 0.0, 0.5, 7, 1, None), 1),
     # element-misaligned fp16 pointer
     (lambda L: L.nrm_act_dropout_fwd(P + 1, P * 2, 16, 2, 0.0, 0.5, 7, 1, None), 1),
 ])

@@ -177,10 +177,11 @@ LEAKY_ELU = [
 ]
 
 
-@pytest.mark.parametrize("act", ["leaky_relu", "elu"])
+@pytest.mark.parametrize("act", ["leaky_relu", "elu", "sigmoid", "celu", "selu"])
 @pytest.mark.parametrize("case", LEAKY_ELU, ids=[f"{d}-{n}x{c}x{l}" for d, n, c, l in LEAKY_ELU])
 def test_bn_leaky_relu_elu(orc, act, case):
-    # the activations with a parameter (slope 0.05, alpha 1.3), z recomputed in the backward
+    # the activations with a parameter (slope 0.05, alpha 1.3 / 0.7) and the
+    # run-time dispatched ones (sigmoid, CELU, SELU), z recomputed in the backward
     dtype, n, c, l = case
     for training in (True, False):
         for with_res in (False, True):

@@ -13,9 +13,9 @@ from parity_util import TOL, assert_close, host
 
 pytestmark = pytest.mark.gpu
 
-ACTS = ["none", "relu", "gelu", "silu", "mish", "leaky_relu", "elu"]
-ACT_CODE = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "mish": 4, "leaky_relu": 5, "elu": 6}
-ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3}
+ACTS = ["none", "relu", "gelu", "silu", "mish", "leaky_relu", "elu", "sigmoid", "celu", "selu"]
+ACT_CODE = {a: i for i, a in enumerate(ACTS)}
+ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3, "celu": 0.7}
 
 
 @pytest.fixture(scope="module", autouse=True)
