@@ -138,6 +138,85 @@ def test_bn_guards_and_determinism(dtype, n, c, l, act, res, training, mask, off
         assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), f"{k} differs between runs"
 
 
+def _cf_run(dtype, n, c, l, offset, seed):
+    td = TORCH_DT[dtype]
+    x = synth.random_tensor(seed, 1, (n, c, l), dtype, mean=0.2, std=1.3).torch("cuda")
+    dy = synth.random_tensor(seed, 2, (n, c, l), dtype).torch("cuda")
+    w = synth.store(1 + 0.1 * synth.normal(seed, 3, c), dtype, (c,)).torch("cuda")
+    b = synth.store(0.1 * synth.normal(seed, 4, c), dtype, (c,)).torch("cuda")
+    outs = {k: Guarded(sh, t, offset) for k, sh, t in (
+        ("y", (n, c, l), td), ("dx", (n, c, l), td), ("dw", (c,), td), ("db", (c,), td),
+        ("mean", (n, l), torch.float32), ("rstd", (n, l), torch.float32))}
+    nws = nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_CF_BWD, n * l, c, DT_CODE[dtype])
+    ws = Guarded((nws // 4,), torch.float32)
+    o = {k: g.t for k, g in outs.items()}
+    nrm.nrm_layernorm_cf_fwd(x, w, b, o["y"], o["mean"], o["rstd"], 1e-6)
+    nrm.nrm_layernorm_cf_bwd(dy, x, w, o["mean"], o["rstd"], o["dx"], o["dw"], o["db"], ws.t)
+    nrm.nrm_sync_status()
+    for k, g in list(outs.items()) + [("ws", ws)]:
+        g.check(f"cf {dtype} [{n},{c},{l}] {k}")
+    return {k: g.t.clone() for k, g in outs.items()}
+
+
+@pytest.mark.parametrize("dtype,n,c,l,offset", [
+    ("f16", 4, 96, 3136, 0),   # TMA ring, ragged last tile
+    ("f32", 3, 300, 36, 0),    # two channel boxes
+    ("f16", 3, 257, 200, 0),   # second box past c
+    ("bf16", 4, 384, 196, 0),  # register kernel (unaligned planes)
+    ("f16", 2, 96, 784, 4),    # unaligned outputs: the register kernel
+])
+def test_cf_guards_and_determinism(dtype, n, c, l, offset):
+    a = _cf_run(dtype, n, c, l, offset, seed=n + c + l)
+    b = _cf_run(dtype, n, c, l, offset, seed=n + c + l)
+    for k in a:
+        assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), f"{k} differs between runs"
+
+
+@pytest.mark.parametrize("dtype,count,act,offset", [
+    ("f16", 100_003, "gelu", 0), ("f32", 4099, "selu", 4), ("bf16", 65_541, "leaky_relu", 2),
+    ("f16", 7, "mish", 0),
+])
+def test_dropout_guards_and_determinism(dtype, count, act, offset):
+    td = TORCH_DT[dtype]
+    x = synth.random_tensor(5, 1, (count,), dtype).torch("cuda")
+    dy = synth.random_tensor(5, 2, (count,), dtype).torch("cuda")
+    runs = []
+    for _ in range(2):
+        y = Guarded((count,), td, offset)
+        dx = Guarded((count,), td, offset)
+        nrm.nrm_act_dropout_fwd(x, y.t, act, 0.3, 12345, act_param=0.1)
+        nrm.nrm_act_dropout_bwd(dy, x, dx.t, act, 0.3, 12345, act_param=0.1)
+        nrm.nrm_sync_status()
+        y.check(f"dropout {dtype} {count} y")
+        dx.check(f"dropout {dtype} {count} dx")
+        runs.append((y.t.clone(), dx.t.clone()))
+    for (a, b) in zip(runs[0], runs[1]):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), "dropout differs between runs"
+
+
+def test_rmsnorm_bias_guards_and_determinism():
+    rows, cols = 300, 768
+    outs = []
+    for _ in range(2):
+        x = synth.random_tensor(9, 1, (rows, cols), "bf16").torch("cuda")
+        dy = synth.random_tensor(9, 2, (rows, cols), "bf16").torch("cuda")
+        w = synth.store(1 + 0.1 * synth.normal(9, 3, cols), "bf16", (cols,)).torch("cuda")
+        b = synth.store(0.1 * synth.normal(9, 4, cols), "bf16", (cols,)).torch("cuda")
+        g = {k: Guarded(sh, t) for k, sh, t in (
+            ("y", (rows, cols), torch.bfloat16), ("dx", (rows, cols), torch.bfloat16),
+            ("dw", (cols,), torch.bfloat16), ("db", (cols,), torch.bfloat16), ("rstd", (rows,), torch.float32))}
+        ws = Guarded((nrm.nrm_workspace_bytes(nrm.NRM_OP_RMSNORM_BWD, rows, cols, nrm.NRM_BF16) // 4,),
+                     torch.float32)
+        nrm.nrm_rmsnorm_fwd(x, w, g["y"].t, g["rstd"].t, 1e-6, b=b)
+        nrm.nrm_rmsnorm_bwd(dy, x, w, g["rstd"].t, g["dx"].t, g["dw"].t, ws.t, db=g["db"].t)
+        nrm.nrm_sync_status()
+        for k, v in list(g.items()) + [("ws", ws)]:
+            v.check(f"rms bias {k}")
+        outs.append({k: v.t.clone() for k, v in g.items()})
+    for k in outs[0]:
+        assert torch.equal(outs[0][k].view(torch.uint8), outs[1][k].view(torch.uint8)), f"{k} differs"
+
+
 def test_errors_leave_the_context_usable():
     lib = nrm.load()
     x = torch.randn(64, 256, device="cuda")
