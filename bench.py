@@ -15,8 +15,8 @@ bits) / summed device time, in GB/s.  Per-call times, GB/s and fraction of the
 measured HBM copy bandwidth are reported per workload.  Beside the step, and
 outside its value, extra_rows times the channels-first LayerNorm on fp16
 [128, 96, 56, 56] (ConvNeXt-T's 96 channels of 56x56) and GELU with fused
-dropout (p = 0.1) on fp16 [25216, 3072] (ViT-B MLP hidden activations) the same
-way.
+dropout (p = 0.1) on fp16 [25216, 3072] (ViT-B MLP hidden activations) and the
+ViT-B LayerNorm fp16 [25216, 768] with its output kept in fp32, the same way.
 
 --impl reference times the CPU oracle (plain double-precision C, one core) on a
 bounded sample of the same workloads (a quarter of the rows or channels of each).

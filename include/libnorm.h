@@ -239,6 +239,42 @@ NRM_API nrm_status nrm_rmsnorm_bwd(const void *dy, const void *x, const void *w,
                            size_t workspace_bytes, nrm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Output kept in float32 for a 16-bit input                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * nrm_layernorm_fwd_ex, nrm_rmsnorm_fwd_ex -- [NK] LayerNorm section, layer
+ * paragraph: the layer's autocast_to_fp32 flag chooses between keeping the
+ * input precision and PyTorch's mixed-precision behaviour of returning
+ * float32.  As nrm_layernorm_fwd / nrm_rmsnorm_fwd, with y stored in y_dt:
+ * y_dt == dt (the plain calls) or NRM_F32 for a float16/bfloat16 x (the
+ * arithmetic is float32 either way; only the output's rounding differs).
+ * Any other y_dt returns NRM_ERR_UNSUPPORTED.  y must be aligned to y_dt's
+ * size.
+ */
+NRM_API nrm_status nrm_layernorm_fwd_ex(const void *x, const void *w, const void *b, void *y,
+                                float *mean, float *rstd, int64_t rows, int64_t cols, float eps,
+                                nrm_dtype dt, nrm_dtype y_dt, nrm_stream_t stream);
+NRM_API nrm_status nrm_rmsnorm_fwd_ex(const void *x, const void *w, const void *b, void *y,
+                              float *rstd, int64_t rows, int64_t cols, float eps, nrm_dtype dt,
+                              nrm_dtype y_dt, nrm_stream_t stream);
+
+/*
+ * nrm_layernorm_bwd_ex, nrm_rmsnorm_bwd_ex -- the backward of the _ex
+ * forwards: dy is stored in dy_dt (the forward's y_dt); x, dx, w, dw, db in
+ * dt.  Otherwise as nrm_layernorm_bwd / nrm_rmsnorm_bwd (same workspace).
+ */
+NRM_API nrm_status nrm_layernorm_bwd_ex(const void *dy, const void *x, const void *w,
+                                const float *mean, const float *rstd, void *dx, void *dw,
+                                void *db, int64_t rows, int64_t cols, nrm_dtype dt,
+                                nrm_dtype dy_dt, void *workspace, size_t workspace_bytes,
+                                nrm_stream_t stream);
+NRM_API nrm_status nrm_rmsnorm_bwd_ex(const void *dy, const void *x, const void *w,
+                              const float *rstd, void *dx, void *dw, void *db, int64_t rows,
+                              int64_t cols, nrm_dtype dt, nrm_dtype dy_dt, void *workspace,
+                              size_t workspace_bytes, nrm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* BatchNorm over (batch, spatial) per channel, NCHW                         */
 /* ------------------------------------------------------------------------ */
 

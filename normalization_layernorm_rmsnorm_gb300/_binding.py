@@ -28,7 +28,8 @@ ACTS = {"none": NRM_ACT_NONE, "relu": NRM_ACT_RELU, "gelu": NRM_ACT_GELU, "silu"
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("nrm_layernorm_fwd", "nrm_layernorm_bwd", "nrm_layernorm_bwd_noalloc",
            "nrm_layernorm_cf_fwd", "nrm_layernorm_cf_bwd",
-           "nrm_rmsnorm_fwd", "nrm_rmsnorm_bwd",
+           "nrm_rmsnorm_fwd", "nrm_rmsnorm_bwd", "nrm_layernorm_fwd_ex", "nrm_layernorm_bwd_ex",
+           "nrm_rmsnorm_fwd_ex", "nrm_rmsnorm_bwd_ex",
            "nrm_batchnorm_fwd", "nrm_batchnorm_bwd", "nrm_act_dropout_fwd", "nrm_act_dropout_bwd",
            "nrm_workspace_bytes",
            "nrm_batchnorm_workspace_bytes",
@@ -67,6 +68,10 @@ def load(path: str | None = None):
         "nrm_layernorm_cf_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _P, ctypes.c_size_t,
                                  _P],
         "nrm_rmsnorm_fwd": [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P],
+        "nrm_layernorm_fwd_ex": [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P],
+        "nrm_layernorm_bwd_ex": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _I, _P, ctypes.c_size_t, _P],
+        "nrm_rmsnorm_fwd_ex": [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P],
+        "nrm_rmsnorm_bwd_ex": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _I, _P, ctypes.c_size_t, _P],
         "nrm_rmsnorm_bwd": [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, ctypes.c_size_t, _P],
         "nrm_batchnorm_fwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, _I,
                               _I, _F, _I, _P, ctypes.c_size_t, _P],
@@ -189,6 +194,40 @@ def nrm_rmsnorm_fwd(x, w, y, rstd, eps, stream=None, b=None):
     _check(load().nrm_rmsnorm_fwd(_ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(rstd), rows, cols, eps,
                                   _dtype_code(x), _stream(stream)),
            "nrm_rmsnorm_fwd")
+
+
+def nrm_layernorm_fwd_ex(x, w, b, y, mean, rstd, eps, stream=None):
+    """LayerNorm with y in its own dtype (x's, or float32 for a 16-bit x)."""
+    rows, cols = _rows_cols(x)
+    _check(load().nrm_layernorm_fwd_ex(_ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(mean), _ptr(rstd), rows,
+                                       cols, eps, _dtype_code(x), _dtype_code(y), _stream(stream)),
+           "nrm_layernorm_fwd_ex")
+
+
+def nrm_layernorm_bwd_ex(dy, x, w, mean, rstd, dx, dw, db, workspace, stream=None):
+    """LayerNorm backward with dy in its own dtype (the forward's y dtype)."""
+    rows, cols = _rows_cols(x)
+    _check(load().nrm_layernorm_bwd_ex(_ptr(dy), _ptr(x), _ptr(w), _ptr(mean), _ptr(rstd), _ptr(dx),
+                                       _ptr(dw), _ptr(db), rows, cols, _dtype_code(x), _dtype_code(dy),
+                                       _ptr(workspace), _ws(workspace), _stream(stream)),
+           "nrm_layernorm_bwd_ex")
+
+
+def nrm_rmsnorm_fwd_ex(x, w, y, rstd, eps, stream=None, b=None):
+    """RMSNorm with y in its own dtype (x's, or float32 for a 16-bit x)."""
+    rows, cols = _rows_cols(x)
+    _check(load().nrm_rmsnorm_fwd_ex(_ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(rstd), rows, cols, eps,
+                                     _dtype_code(x), _dtype_code(y), _stream(stream)),
+           "nrm_rmsnorm_fwd_ex")
+
+
+def nrm_rmsnorm_bwd_ex(dy, x, w, rstd, dx, dw, workspace, stream=None, db=None):
+    """RMSNorm backward with dy in its own dtype (the forward's y dtype)."""
+    rows, cols = _rows_cols(x)
+    _check(load().nrm_rmsnorm_bwd_ex(_ptr(dy), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw), _ptr(db),
+                                     rows, cols, _dtype_code(x), _dtype_code(dy), _ptr(workspace),
+                                     _ws(workspace), _stream(stream)),
+           "nrm_rmsnorm_bwd_ex")
 
 
 def nrm_rmsnorm_bwd(dy, x, w, rstd, dx, dw, workspace, stream=None, db=None):

@@ -257,16 +257,26 @@ size_t row_ws_bytes(bool layernorm, int64_t cols) {
     return size_t(row_bwd_max_partials(*d)) * size_t(cols) * sizeof(float) * (layernorm ? 2 : 1);
 }
 
+// The output's storage type: the input's, or fp32 for a 16-bit input.
+nrm_status check_out_dtype(nrm_dtype dt, nrm_dtype out_dt) {
+    if (!dtype_ok(out_dt)) return fail(NRM_ERR_INVALID_ARG, "unknown output dtype %d", int(out_dt));
+    if (out_dt != dt && out_dt != NRM_F32)
+        return fail(NRM_ERR_UNSUPPORTED, "the output dtype is the input's or float32");
+    return NRM_OK;
+}
+
 nrm_status row_fwd_common(bool ln, const void* x, const void* w, const void* b, void* y, float* mean,
                           float* rstd, int64_t rows, int64_t cols, float eps, nrm_dtype dt,
-                          nrm_stream_t stream) {
+                          nrm_stream_t stream, nrm_dtype y_dt) {
     t_msg[0] = 0;
     nrm_status st = check_rows(rows, cols, dt);
     if (st != NRM_OK) return st;
+    if ((st = check_out_dtype(dt, y_dt)) != NRM_OK) return st;
     if ((st = check_eps(eps)) != NRM_OK) return st;
     if (rows > 0 && (!x || !y)) return fail(NRM_ERR_INVALID_ARG, "x and y must not be NULL");
     const size_t es = dsize(dt);
-    if (!all_aligned({x, y, w, b}, es) || !all_aligned({mean, rstd}, 4))
+    const bool f32out = y_dt != dt;
+    if (!all_aligned({x, w, b}, es) || !all_aligned({y}, dsize(y_dt)) || !all_aligned({mean, rstd}, 4))
         return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
     if (rows > 0 && x == y) return fail(NRM_ERR_INVALID_ARG, "in-place (y == x) is not supported");
     const bool vec = (size_t(cols) * es) % 16 == 0 && all_aligned({x, y, w, b}, 16);
@@ -281,19 +291,22 @@ nrm_status row_fwd_common(bool ln, const void* x, const void* w, const void* b, 
     a.cols = int(cols);
     a.eps = eps;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (f32out) return by_dtype(dt, [&](auto tag) { return row_fwd_f32out<decltype(tag)>(a, ln, vec, s); });
     return by_dtype(dt, [&](auto tag) { return row_fwd<decltype(tag)>(a, ln, vec, s); });
 }
 
 nrm_status row_bwd_common(bool ln, const void* dy, const void* x, const void* w, const float* mean,
                           const float* rstd, void* dx, void* dw, void* db, int64_t rows, int64_t cols,
-                          nrm_dtype dt, void* ws, size_t ws_bytes, nrm_stream_t stream) {
+                          nrm_dtype dt, void* ws, size_t ws_bytes, nrm_stream_t stream, nrm_dtype dy_dt) {
     t_msg[0] = 0;
     nrm_status st = check_rows(rows, cols, dt);
     if (st != NRM_OK) return st;
+    if ((st = check_out_dtype(dt, dy_dt)) != NRM_OK) return st;
     if (rows > 0 && (!dy || !x || !dx || !rstd || (ln && !mean)))
         return fail(NRM_ERR_INVALID_ARG, "dy, x, dx and the saved statistics must not be NULL");
     const size_t es = dsize(dt);
-    if (!all_aligned({dy, x, dx, w, dw, db}, es) || !all_aligned({mean, rstd}, 4))
+    const bool f32dy = dy_dt != dt;
+    if (!all_aligned({x, dx, w, dw, db}, es) || !all_aligned({dy}, dsize(dy_dt)) || !all_aligned({mean, rstd}, 4))
         return fail(NRM_ERR_INVALID_ARG, "pointers must be aligned to their element size");
     if (rows > 0 && (dx == dy || dx == x))
         return fail(NRM_ERR_INVALID_ARG, "in-place (dx == dy or x) is not supported");
@@ -321,6 +334,7 @@ nrm_status row_bwd_common(bool ln, const void* dy, const void* x, const void* w,
     a.rows = rows;
     a.cols = int(cols);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (f32dy) return by_dtype(dt, [&](auto tag) { return row_bwd_f32dy<decltype(tag)>(a, ln, vec, s); });
     return by_dtype(dt, [&](auto tag) { return row_bwd<decltype(tag)>(a, ln, vec, s); });
 }
 
@@ -362,7 +376,7 @@ extern "C" {
 nrm_status nrm_layernorm_fwd(const void* x, const void* w, const void* b, void* y, float* mean,
                              float* rstd, int64_t rows, int64_t cols, float eps, nrm_dtype dt,
                              nrm_stream_t stream) {
-    return row_fwd_common(true, x, w, b, y, mean, rstd, rows, cols, eps, dt, stream);
+    return row_fwd_common(true, x, w, b, y, mean, rstd, rows, cols, eps, dt, stream, dt);
 }
 
 nrm_status nrm_layernorm_bwd(const void* dy, const void* x, const void* w, const float* mean,
@@ -370,7 +384,21 @@ nrm_status nrm_layernorm_bwd(const void* dy, const void* x, const void* w, const
                              int64_t cols, nrm_dtype dt, void* workspace, size_t workspace_bytes,
                              nrm_stream_t stream) {
     return row_bwd_common(true, dy, x, w, mean, rstd, dx, dw, db, rows, cols, dt, workspace,
-                          workspace_bytes, stream);
+                          workspace_bytes, stream, dt);
+}
+
+nrm_status nrm_layernorm_fwd_ex(const void* x, const void* w, const void* b, void* y, float* mean,
+                                float* rstd, int64_t rows, int64_t cols, float eps, nrm_dtype dt,
+                                nrm_dtype y_dt, nrm_stream_t stream) {
+    return row_fwd_common(true, x, w, b, y, mean, rstd, rows, cols, eps, dt, stream, y_dt);
+}
+
+nrm_status nrm_layernorm_bwd_ex(const void* dy, const void* x, const void* w, const float* mean,
+                                const float* rstd, void* dx, void* dw, void* db, int64_t rows,
+                                int64_t cols, nrm_dtype dt, nrm_dtype dy_dt, void* workspace,
+                                size_t workspace_bytes, nrm_stream_t stream) {
+    return row_bwd_common(true, dy, x, w, mean, rstd, dx, dw, db, rows, cols, dt, workspace,
+                          workspace_bytes, stream, dy_dt);
 }
 
 nrm_status nrm_layernorm_cf_fwd(const void* x, const void* w, const void* b, void* y, float* mean,
@@ -448,14 +476,27 @@ nrm_status nrm_layernorm_cf_bwd(const void* dy, const void* x, const void* w, co
 
 nrm_status nrm_rmsnorm_fwd(const void* x, const void* w, const void* b, void* y, float* rstd, int64_t rows,
                            int64_t cols, float eps, nrm_dtype dt, nrm_stream_t stream) {
-    return row_fwd_common(false, x, w, b, y, nullptr, rstd, rows, cols, eps, dt, stream);
+    return row_fwd_common(false, x, w, b, y, nullptr, rstd, rows, cols, eps, dt, stream, dt);
 }
 
 nrm_status nrm_rmsnorm_bwd(const void* dy, const void* x, const void* w, const float* rstd, void* dx,
                            void* dw, void* db, int64_t rows, int64_t cols, nrm_dtype dt, void* workspace,
                            size_t workspace_bytes, nrm_stream_t stream) {
     return row_bwd_common(false, dy, x, w, nullptr, rstd, dx, dw, db, rows, cols, dt, workspace,
-                          workspace_bytes, stream);
+                          workspace_bytes, stream, dt);
+}
+
+nrm_status nrm_rmsnorm_fwd_ex(const void* x, const void* w, const void* b, void* y, float* rstd,
+                              int64_t rows, int64_t cols, float eps, nrm_dtype dt, nrm_dtype y_dt,
+                              nrm_stream_t stream) {
+    return row_fwd_common(false, x, w, b, y, nullptr, rstd, rows, cols, eps, dt, stream, y_dt);
+}
+
+nrm_status nrm_rmsnorm_bwd_ex(const void* dy, const void* x, const void* w, const float* rstd, void* dx,
+                              void* dw, void* db, int64_t rows, int64_t cols, nrm_dtype dt, nrm_dtype dy_dt,
+                              void* workspace, size_t workspace_bytes, nrm_stream_t stream) {
+    return row_bwd_common(false, dy, x, w, nullptr, rstd, dx, dw, db, rows, cols, dt, workspace,
+                          workspace_bytes, stream, dy_dt);
 }
 
 nrm_status nrm_batchnorm_fwd(const void* x, const void* residual, const float* w, const float* b,

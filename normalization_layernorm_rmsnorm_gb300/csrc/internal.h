@@ -118,6 +118,10 @@ int row_bwd_max_partials(const DevInfo& d);
 template <typename T> nrm_status row_fwd(const RowArgs& a, bool layernorm, bool vec,
                                          cudaStream_t s);
 template <typename T> nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s);
+// The same with the forward's output, and so the backward's dy, held in fp32
+// for a 16-bit input (the autocast_to_fp32-style option).
+template <typename T> nrm_status row_fwd_f32out(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s);
+template <typename T> nrm_status row_bwd_f32dy(RowArgs a, bool layernorm, bool vec, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // BatchNorm

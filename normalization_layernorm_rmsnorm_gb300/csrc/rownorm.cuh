@@ -457,7 +457,46 @@ __device__ __forceinline__ void block_sum(float (&v)[NV], float* sm /* [32*NV] *
     __syncthreads();
 }
 
-template <typename T, bool LN, int VE>
+// VE fp32 values of type TD at p (fp32 values of a 16-bit VE-vector are two
+// 16-byte vectors; p is 16-byte aligned when VE > 1), and the stores of them.
+template <typename TD, int VE, bool STREAM = true>
+__device__ __forceinline__ void load_as(const TD* p, float (&out)[VE]) {
+    if constexpr (VE == 1 || VE == kVec<TD>) {
+        load_vec<TD, VE, STREAM>(p, out);
+    } else {
+        static_assert(VE == 2 * kVec<TD>, "fp32 values of a 16-bit vector");
+        constexpr int H = kVec<TD>;
+        float lo[H], hi[H];
+        load_vec<TD, H, STREAM>(p, lo);
+        load_vec<TD, H, STREAM>(p + H, hi);
+#pragma unroll
+        for (int k = 0; k < H; ++k) {
+            out[k] = lo[k];
+            out[H + k] = hi[k];
+        }
+    }
+}
+template <typename TO, int VE>
+__device__ __forceinline__ void store_as(TO* p, const float (&in)[VE]) {
+    if constexpr (VE == 1 || VE == kVec<TO>) {
+        store_vec<TO, VE>(p, in);
+    } else {
+        static_assert(VE == 2 * kVec<TO>, "fp32 values of a 16-bit vector");
+        constexpr int H = kVec<TO>;
+        float lo[H], hi[H];
+#pragma unroll
+        for (int k = 0; k < H; ++k) {
+            lo[k] = in[k];
+            hi[k] = in[H + k];
+        }
+        store_vec<TO, H>(p, lo);
+        store_vec<TO, H>(p + H, hi);
+    }
+}
+
+// TO: the output's storage type (T, or float for a 16-bit input whose output
+// is kept in fp32).
+template <typename T, bool LN, int VE, typename TO = T>
 __global__ void __launch_bounds__(kRowWideBlock)
 row_fwd_wide_kernel(const RowArgs a) {
     __shared__ Moments msm[33];
@@ -465,7 +504,7 @@ row_fwd_wide_kernel(const RowArgs a) {
     const int cols = a.cols;
     const int nvec = cols / VE;
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
-    T* __restrict__ y = reinterpret_cast<T*>(a.y);
+    TO* __restrict__ y = reinterpret_cast<TO*>(a.y);
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
         const T* xr = x + row * cols;
         float mu = 0.f, var;
@@ -502,7 +541,7 @@ row_fwd_wide_kernel(const RowArgs a) {
             if (LN && a.mean) a.mean[row] = mu;
             if (a.rstd) a.rstd[row] = rs;
         }
-        T* yr = y + row * cols;
+        TO* yr = y + row * cols;
         for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
             float v[VE], wv[VE], bv[VE], o[VE];
             load_vec<T, VE>(xr + int64_t(vi) * VE, v);
@@ -513,33 +552,42 @@ row_fwd_wide_kernel(const RowArgs a) {
                 const float xh = (v[k] - mu) * rs;
                 o[k] = fmaf(xh, wv[k], bv[k]);
             }
-            store_vec<T, VE>(yr + int64_t(vi) * VE, o);
+            store_as<TO, VE>(yr + int64_t(vi) * VE, o);
         }
     }
 }
 
-template <typename T, bool LN, int VE>
+// TD: the storage type of dy (T, or float when the forward's output was kept in fp32).
+template <typename T, bool LN, int VE, typename TD = T>
 __global__ void __launch_bounds__(kRowWideBlock)
 row_bwd_wide_kernel(const RowArgs a) {
     __shared__ float ssm[32 * 2];
     const int cols = a.cols;
     const int nvec = cols / VE;
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
-    const T* __restrict__ dy = reinterpret_cast<const T*>(a.dy);
+    const TD* __restrict__ dy = reinterpret_cast<const TD*>(a.dy);
     T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
     float* wsw = a.ws_dw ? a.ws_dw + int64_t(blockIdx.x) * cols : nullptr;
     float* wsb = a.ws_db ? a.ws_db + int64_t(blockIdx.x) * cols : nullptr;
-    // this CTA's partial rows; each column is always updated by the same thread
-    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+    // this CTA's partial rows; each column is always updated by the same thread.
+    // When the row has at most one vector per thread the sums stay in registers
+    // and are written once at the end; wider rows update the workspace row.
+    const bool in_regs = nvec <= int(blockDim.x);
+    float racc_w[VE], racc_b[VE];
 #pragma unroll
-        for (int k = 0; k < VE; ++k) {
-            if (wsw) wsw[vi * VE + k] = 0.f;
-            if (wsb) wsb[vi * VE + k] = 0.f;
+    for (int k = 0; k < VE; ++k) racc_w[k] = racc_b[k] = 0.f;
+    if (!in_regs) {
+        for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+#pragma unroll
+            for (int k = 0; k < VE; ++k) {
+                if (wsw) wsw[vi * VE + k] = 0.f;
+                if (wsb) wsb[vi * VE + k] = 0.f;
+            }
         }
     }
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
         const T* xr = x + row * cols;
-        const T* dyr = dy + row * cols;
+        const TD* dyr = dy + row * cols;
         const float rs = a.rstd_in[row];
         const float mu = LN ? a.mean_in[row] : 0.f;
         constexpr int NV = LN ? 2 : 1;
@@ -549,7 +597,7 @@ row_bwd_wide_kernel(const RowArgs a) {
         for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
             float xv[VE], dv[VE], wv[VE];
             load_vec<T, VE, false>(xr + int64_t(vi) * VE, xv);
-            load_vec<T, VE, false>(dyr + int64_t(vi) * VE, dv);
+            load_as<TD, VE, false>(dyr + int64_t(vi) * VE, dv);
             load_param<T, VE>(a.w, vi, wv, 1.f);
 #pragma unroll
             for (int k = 0; k < VE; ++k) {
@@ -569,23 +617,33 @@ row_bwd_wide_kernel(const RowArgs a) {
         for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
             float xv[VE], dv[VE], wv[VE], o[VE];
             load_vec<T, VE>(xr + int64_t(vi) * VE, xv);
-            load_vec<T, VE>(dyr + int64_t(vi) * VE, dv);
+            load_as<TD, VE>(dyr + int64_t(vi) * VE, dv);
             load_param<T, VE>(a.w, vi, wv, 1.f);
 #pragma unroll
             for (int k = 0; k < VE; ++k) {
                 const float g = dv[k] * wv[k];
+                const float xs = LN ? (xv[k] - mu) * rs : xv[k] * rs;  // xhat (LN) or x*inv_rms
                 if constexpr (LN) {
-                    const float xh = (xv[k] - mu) * rs;
-                    o[k] = rs * (g - c1 - xh * c2);
-                    if (wsw) wsw[vi * VE + k] = fmaf(dv[k], xh, wsw[vi * VE + k]);
-                    if (wsb) wsb[vi * VE + k] += dv[k];
+                    o[k] = rs * (g - c1 - xs * c2);
                 } else {
                     o[k] = rs * (g - xv[k] * (c1 * rs * rs));
-                    if (wsw) wsw[vi * VE + k] = fmaf(dv[k], xv[k] * rs, wsw[vi * VE + k]);
+                }
+                if (in_regs) {
+                    racc_w[k] = fmaf(dv[k], xs, racc_w[k]);
+                    racc_b[k] += dv[k];
+                } else {
+                    if (wsw) wsw[vi * VE + k] = fmaf(dv[k], xs, wsw[vi * VE + k]);
                     if (wsb) wsb[vi * VE + k] += dv[k];
                 }
             }
             store_vec<T, VE>(dxr + int64_t(vi) * VE, o);
+        }
+    }
+    if (in_regs && threadIdx.x < nvec) {
+#pragma unroll
+        for (int k = 0; k < VE; ++k) {
+            if (wsw) wsw[threadIdx.x * VE + k] = racc_w[k];
+            if (wsb) wsb[threadIdx.x * VE + k] = racc_b[k];
         }
     }
     pdl_trigger();
@@ -774,6 +832,73 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
                       cargs, s);
 }
 
+// Threads per CTA of a wide-row kernel used for rows of `nvec` vectors: a
+// warp multiple that covers the row, at most kRowWideBlock.
+inline int wide_block(int nvec) {
+    int b = (nvec + 31) / 32 * 32;
+    return b < 32 ? 32 : (b > kRowWideBlock ? kRowWideBlock : b);
+}
+
+// Forward with the output kept in fp32 for a 16-bit input (the wide-row
+// kernels with TO = float, one CTA per row sized to the row).
+template <typename T>
+nrm_status row_fwd_f32out(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s) {
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    if (a.rows == 0) return NRM_OK;
+    constexpr int V = kVec<T>;
+    const void* fn = layernorm ? (vec ? (const void*)&row_fwd_wide_kernel<T, true, V, float>
+                                      : (const void*)&row_fwd_wide_kernel<T, true, 1, float>)
+                               : (vec ? (const void*)&row_fwd_wide_kernel<T, false, V, float>
+                                      : (const void*)&row_fwd_wide_kernel<T, false, 1, float>);
+    const int block = wide_block(a.cols / (vec ? V : 1));
+    const int occ = cached_occupancy(fn, block, 0);
+    if (occ <= 0) return fail(NRM_ERR_CUDA, "row forward kernel cannot be resident");
+    const int64_t cap = int64_t(occ) * d->sms;
+    const int grid = int(a.rows < cap ? a.rows : cap);
+    RowArgs args = a;
+    void* kargs[] = {&args};
+    return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(block), kargs, 0, s), "row forward launch");
+}
+
+// Backward whose dy is fp32 (the forward kept its output in fp32) for a
+// 16-bit x: the wide-row kernels with TD = float, then the column sums.
+template <typename T>
+nrm_status row_bwd_f32dy(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
+    const DevInfo* d = dev_info();
+    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
+    const bool want = a.dw || a.db;
+    if (!want) a.ws_dw = a.ws_db = nullptr;
+    constexpr int V = kVec<T>;
+    const void* fn = layernorm ? (vec ? (const void*)&row_bwd_wide_kernel<T, true, V, float>
+                                      : (const void*)&row_bwd_wide_kernel<T, true, 1, float>)
+                               : (vec ? (const void*)&row_bwd_wide_kernel<T, false, V, float>
+                                      : (const void*)&row_bwd_wide_kernel<T, false, 1, float>);
+    const int block = wide_block(a.cols / (vec ? V : 1));
+    const int occ = cached_occupancy(fn, block, 0);
+    if (occ <= 0) return fail(NRM_ERR_CUDA, "row backward kernel cannot be resident");
+    int64_t p = int64_t(occ) * d->sms;
+    if (p > row_bwd_max_partials(*d)) p = row_bwd_max_partials(*d);
+    if (a.rows < p) p = a.rows;
+    const int P = int(p);
+    if (P > 0) {
+        RowArgs args = a;
+        void* kargs[] = {&args};
+        nrm_status st = cuda_status(cudaLaunchKernel(fn, dim3(P), dim3(block), kargs, 0, s), "row backward launch");
+        if (st != NRM_OK) return st;
+    }
+    if (!want) return NRM_OK;
+    const float* wsw = a.ws_dw;
+    const float* wsb = a.ws_db;
+    int P_ = P;
+    int cols = a.cols;
+    T* dw = reinterpret_cast<T*>(a.dw);
+    T* db = reinterpret_cast<T*>(a.db);
+    void* cargs[] = {&wsw, &wsb, &P_, &cols, &dw, &db};
+    return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((a.cols + 31) / 32, 2), dim3(kColsumWarps * 32),
+                      cargs, s);
+}
+
 // Plan of a channels-first ring kernel: positions per tile (the widest of 32,
 // 16, 8 vectors per channel row that the plane needs and that leaves at least
 // four slots, else three, else two), channel boxes of at most 256 rows, and
@@ -943,5 +1068,7 @@ nrm_status cf_bwd(CfArgs a, bool vec, cudaStream_t s) {
 #define NRM_INSTANTIATE_ROWNORM(T)                                                      \
     template nrm_status nrm::row_fwd<T>(const nrm::RowArgs&, bool, bool, cudaStream_t); \
     template nrm_status nrm::row_bwd<T>(nrm::RowArgs, bool, bool, cudaStream_t);        \
+    template nrm_status nrm::row_fwd_f32out<T>(const nrm::RowArgs&, bool, bool, cudaStream_t); \
+    template nrm_status nrm::row_bwd_f32dy<T>(nrm::RowArgs, bool, bool, cudaStream_t);  \
     template nrm_status nrm::cf_fwd<T>(const nrm::CfArgs&, bool, cudaStream_t);         \
     template nrm_status nrm::cf_bwd<T>(nrm::CfArgs, bool, cudaStream_t);

@@ -64,7 +64,9 @@ def build_calls(dev, names=None):
 DROPOUT_WORKLOAD = "act_dropout_gelu_f16_25216x3072"
 DROPOUT_P = 0.1
 DROPOUT_SEED = 2024
-EXTRA = ("ln_cf_f16_128x96x56x56", DROPOUT_WORKLOAD)
+# and the ViT-B LayerNorm with its output (and so dy) kept in float32
+F32OUT_WORKLOAD = "ln_f16_to_f32_25216x768"
+EXTRA = ("ln_cf_f16_128x96x56x56", DROPOUT_WORKLOAD, F32OUT_WORKLOAD)
 
 
 def build_extra_calls(dev, names=None):
@@ -79,6 +81,8 @@ def build_extra_calls(dev, names=None):
         calls += _ln_cf(EXTRA[0], 128, 96, 56 * 56, dev, f32)
     if names is None or DROPOUT_WORKLOAD in names:
         calls += _act_dropout(DROPOUT_WORKLOAD, 25216, 3072, dev)
+    if names is None or F32OUT_WORKLOAD in names:
+        calls += _ln_f32out(F32OUT_WORKLOAD, 25216, 768, dev, f32)
     return calls
 
 
@@ -227,4 +231,28 @@ def _act_dropout(name, rows, cols, dev):
              lambda: nrm.nrm_act_dropout_fwd(x, y, "gelu", p, s), nbytes(x, y), 1, [x], [y]),
         Call(name, "bwd", "act_dropout_vec_kernel<f16,gelu,bwd>",
              lambda: nrm.nrm_act_dropout_bwd(dy, x, dx, "gelu", p, s), nbytes(dy, x, dx), 1, [dy], [dx]),
+    ]
+
+
+def _ln_f32out(name, rows, cols, dev, f32):
+    import torch
+
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    seed = 41
+    x = synth.random_tensor(seed, 1, (rows, cols), "f16", mean=0.3, std=1.5).torch(dev)
+    w = synth.store(1 + 0.1 * synth.normal(seed, 2, cols), "f16", (cols,)).torch(dev)
+    b = synth.store(0.1 * synth.normal(seed, 3, cols), "f16", (cols,)).torch(dev)
+    dy = synth.random_tensor(seed, 4, (rows, cols), "f32").torch(dev)
+    y = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    dx, dw, db = x.new_empty(x.shape), w.new_empty(cols), b.new_empty(cols)
+    mean, rstd = f32(rows), f32(rows)
+    ws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_BWD, rows, cols, nrm.NRM_F16) // 4)
+    return [
+        Call(name, "fwd", "row_fwd_wide_kernel<f16,ln,f32 out>",
+             lambda: nrm.nrm_layernorm_fwd_ex(x, w, b, y, mean, rstd, 1e-6),
+             nbytes(x, w, b, y, mean, rstd), 1, [x, w, b], [y, mean, rstd]),
+        Call(name, "bwd", "row_bwd_wide_kernel<f16,ln,f32 dy>+colsum",
+             lambda: nrm.nrm_layernorm_bwd_ex(dy, x, w, mean, rstd, dx, dw, db, ws),
+             nbytes(dy, x, w, mean, rstd, dx, dw, db), 2, [dy], [dx, dw, db]),
     ]

@@ -117,6 +117,9 @@ P = 1 << 20  # a fake, aligned, non-null address: never dereferenced (validation
     # CELU with alpha 0, an activation past the last one
     (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 8, 0.0, 0.5, 7, 1, None), 1),
     (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 10, 0.0, 0.5, 7, 1, None), 1),
+    # an fp32 input with a 16-bit output (only 16-bit inputs may widen), an unknown output dtype
+    (lambda L: L.nrm_layernorm_fwd_ex(P, None, None, P * 2, None, None, 4, 8, 1e-5, 0, 1, None), 2),
+    (lambda L: L.nrm_rmsnorm_fwd_ex(P, None, None, P * 2, None, 4, 8, 1e-5, 1, 5, None), 1),
     # element-misaligned fp16 pointer
     (lambda L: L.nrm_act_dropout_fwd(P + 1, P * 2, 16, 2, 0.0, 0.5, 7, 1, None), 1),
 ])

@@ -9,8 +9,7 @@ import torch
 
 import normalization_layernorm_rmsnorm_gb300 as nrm
 from normalization_layernorm_rmsnorm_gb300 import synth
-from parity_util import (DT_CODE, TOL, compare_row, dev, empty, host, oracle_row, run_row,
-                         workspace)
+from parity_util import (DT_CODE, STAT_TOL, TOL, assert_close, compare_row, dev, empty, host, oracle_row, run_row, workspace)
 
 pytestmark = pytest.mark.gpu
 
@@ -165,3 +164,48 @@ def test_rmsnorm_with_bias(orc, dtype, shape):
     want = oracle_row(orc, "rmsnorm", inp, 1e-6)
     assert "db" in got
     compare_row(got, want, dtype, f"rms+bias {dtype} [{rows},{cols}]")
+
+
+F32OUT = [(300, 768), (97, 1023), (64, 4096), (5, 40000)]
+
+
+@pytest.mark.parametrize("kind", ["layernorm", "rmsnorm"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", F32OUT, ids=[f"{r}x{c}" for r, c in F32OUT])
+def test_row_f32_output(orc, kind, dtype, shape):
+    # the autocast_to_fp32-style option: a 16-bit x, y (and so dy) in float32;
+    # y meets the fp32 bound, dx/dw/db (stored 16-bit) the 16-bit one
+    rows, cols = shape
+    seed = 80 + cols % 91
+    x = synth.random_tensor(seed, 1, (rows, cols), dtype, mean=0.2, std=1.3)
+    w = synth.store(1 + 0.1 * synth.normal(seed, 2, cols), dtype, (cols,))
+    b = synth.store(0.1 * synth.normal(seed, 3, cols), dtype, (cols,))
+    dy = synth.random_tensor(seed, 4, (rows, cols), "f32")
+    xt, wt, bt, dyt = x.torch("cuda"), w.torch("cuda"), b.torch("cuda"), dy.torch("cuda")
+    y = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+    mean = torch.empty(rows, device="cuda")
+    rstd = torch.empty(rows, device="cuda")
+    dx = empty((rows, cols), dtype)
+    dw = empty((cols,), dtype)
+    db = empty((cols,), dtype)
+    if kind == "layernorm":
+        nrm.nrm_layernorm_fwd_ex(xt, wt, bt, y, mean, rstd, 1e-5)
+        ws = workspace(nrm.NRM_OP_LAYERNORM_BWD, rows, cols, DT_CODE[dtype])
+        nrm.nrm_layernorm_bwd_ex(dyt, xt, wt, mean, rstd, dx, dw, db, ws)
+        yo, mo, ro = orc.layernorm_fwd(x.f64(), w.f64(), b.f64(), 1e-5)
+        dxo, dwo, dbo = orc.layernorm_bwd(dy.f64(), x.f64(), w.f64(), 1e-5)
+    else:
+        nrm.nrm_rmsnorm_fwd_ex(xt, wt, y, rstd, 1e-5, b=bt)
+        ws = workspace(nrm.NRM_OP_RMSNORM_BWD, rows, cols, DT_CODE[dtype])
+        nrm.nrm_rmsnorm_bwd_ex(dyt, xt, wt, rstd, dx, dw, ws, db=db)
+        yo, ro = orc.rmsnorm_fwd(x.f64(), w.f64(), 1e-5, b=b.f64())
+        dxo, dwo, dbo = orc.rmsnorm_bwd(dy.f64(), x.f64(), w.f64(), 1e-5, with_db=True)
+    nrm.nrm_sync_status()
+    tag = f"{kind} {dtype}->f32 [{rows},{cols}]"
+    assert_close(host(y), yo, TOL["f32"], tag + " y")
+    assert_close(host(rstd), ro, STAT_TOL, tag + " rstd")
+    if kind == "layernorm":
+        assert_close(host(mean), mo, STAT_TOL, tag + " mean")
+    assert_close(host(dx), dxo, TOL[dtype], tag + " dx")
+    assert_close(host(dw), dwo, TOL[dtype], tag + " dw")
+    assert_close(host(db), dbo, TOL[dtype], tag + " db")
