@@ -34,9 +34,9 @@
 //     aligned to 16 bytes, with the same cooperative schedule and L2 staging.
 //   * Statistics: per-thread sums of (x - K) and (x - K)^2 about the thread's
 //     first value K, turned into (n, mean, M2) and merged with Chan's formula.
-//     Backward sums: sum(dz) and sum(dz*x) accumulated without rounding loss
-//     (error-free products and Kahan sums in fp32, combined in double);
-//     sum(dz*(x - mean)) = sum(dz*x) - mean*sum(dz) in double.
+//     Backward sums: sum(dz) and sum(dz*(x - mean)), centred on the saved
+//     mean (no cancellation), in fp32 per thread and float-float / double
+//     across threads, CTAs and slices.
 #pragma once
 
 #include "activation.cuh"
@@ -879,29 +879,27 @@ __device__ __forceinline__ void form_dz(const BnArgs& a, const BnGeom& g, const 
     }
 }
 
-// Sum of dz and of dz*x without rounding loss: each product's rounding error
-// is recovered exactly with an fma, the rounded products and dz are summed
-// with Kahan compensation, and the three parts are combined in double.
+// A thread's sums of dz and of dz*(x - mean), centred on the channel's saved
+// mean so that the mean does not cancel against the sum of dz (the mean is
+// known before the pass: it is part of z).  The thread's share of a slice is
+// short, so plain fp32 sums keep about fp32 precision; they are combined
+// across threads, CTAs and slices in float-float or double.
 struct GradSums {
-    Kahan dz, dzx;
-    float dzx_err = 0.f;
+    float dz = 0.f, dzc = 0.f;
+    float mu;
+    __device__ __forceinline__ explicit GradSums(float mean) : mu(mean) {}
     template <int VE>
     __device__ __forceinline__ void add(const float (&dzv)[VE], const float (&xv)[VE]) {
 #pragma unroll
         for (int k = 0; k < VE; ++k) {
-            const float p = dzv[k] * xv[k];
-            dzx_err += fmaf(dzv[k], xv[k], -p);
-            dzx.add(p);
-            dz.add(dzv[k]);
+            dz += dzv[k];
+            dzc = fmaf(dzv[k], xv[k] - mu, dzc);
         }
     }
-    __device__ __forceinline__ double sum_dz() const { return double(dz.s) - double(dz.c); }
-    __device__ __forceinline__ double sum_dzx() const {
-        return double(dzx.s) - double(dzx.c) + double(dzx_err);
-    }
-    // the same sums as float-float pairs (Kahan's s - c; plus the products' error term)
-    __device__ __forceinline__ FF ff_dz() const { return FF{dz.s, -dz.c}; }
-    __device__ __forceinline__ FF ff_dzx() const { return ff_add(FF{dzx.s, -dzx.c}, FF{dzx_err, 0.f}); }
+    __device__ __forceinline__ double sum_dz() const { return double(dz); }
+    __device__ __forceinline__ double sum_dzc() const { return double(dzc); }
+    __device__ __forceinline__ FF ff_dz() const { return FF{dz, 0.f}; }
+    __device__ __forceinline__ FF ff_dzc() const { return FF{dzc, 0.f}; }
 };
 
 // First pass of round r: dz from dy and x (both streamed from HBM and kept in
@@ -927,7 +925,7 @@ __device__ void bwd_pass1(const BnArgs& a, const Rounds& rd, int r, double (*war
     const float shift = bc - mu * scale;
 
     const bool use_mask = a.act == NRM_ACT_RELU && !need_z;
-    GradSums acc;
+    GradSums acc(mu);
     for (uint32_t base = b0 + warp; base < b1; base += kBnWarps * kBnUnroll2) {
         Pack<T, VE> pdy[kBnUnroll2], px[kBnUnroll2];
         uint32_t mbits[kBnUnroll2];
@@ -969,7 +967,7 @@ __device__ void bwd_pass1(const BnArgs& a, const Rounds& rd, int r, double (*war
             }
         }
     }
-    double d1 = acc.sum_dz(), d2 = acc.sum_dzx();
+    double d1 = acc.sum_dz(), d2 = acc.sum_dzc();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         d1 += __shfl_xor_sync(0xffffffffu, d1, o);
@@ -1056,8 +1054,7 @@ bn_bwd_kernel(const BnArgs a, const BnGeom g) {
                 t2 = l2;
             }
             if (lane == 0) {
-                // sum dz*(x - mean) = sum dz*x - mean*sum dz, in double
-                const double t2c = t2 - double(mu) * t1;
+                const double t2c = t2;  // sum dz*(x - mean): centred on the saved mean as summed
                 if (s == 0) {
                     if (a.db) a.db[ch] = float(t1);
                     if (a.dw) a.dw[ch] = float(t2c * double(rs));
@@ -1184,11 +1181,12 @@ __device__ __forceinline__ void merge_grad_partials(const BnGeom& g, int64_t ch,
     t2 = l2;
 }
 
-// dw, db of channel ch from its two sums: sum dz*(x - mean) = sum dz*x -
-// mean*sum dz, in double.  Returns sum dz*xhat.
+// dw, db of channel ch from its two sums, sum dz (t1) and sum dz*(x - mean)
+// (t2, centred on the saved mean as it was summed).  Returns sum dz*xhat.
 __device__ __forceinline__ double grad_center(const BnArgs& a, int64_t ch, float mu, float rs, double t1, double t2,
                                               bool write_grads) {
-    const double t2c = t2 - double(mu) * t1;
+    (void)mu;
+    const double t2c = t2;
     if (write_grads) {
         if (a.db) a.db[ch] = float(t1);
         if (a.dw) a.dw[ch] = float(t2c * double(rs));
@@ -1409,7 +1407,7 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
         auto publish = [&](int q, const GradSums& acc) {
             // float-float warp sums: no double-precision arithmetic on the consumers' path
             const FF d1 = ff_warp_sum(acc.ff_dz());
-            const FF d2 = ff_warp_sum(acc.ff_dzx());
+            const FF d2 = ff_warp_sum(acc.ff_dzc());
             if (lane == 0) {
                 if (q >= 2 && !mbar_wait_bounded(&sh.hs.sums_free[q & 1], ((q >> 1) - 1) & 1, kBnWaitLimitNs)) bad = true;
                 sh.warp_s[q & 1][warp] = make_float4(d1.hi, d1.lo, d2.hi, d2.lo);
@@ -1428,7 +1426,7 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
             uint32_t b0, b1;
             rd.range(q, ch, s, b0, b1);
             const float4 pr = params(q);
-            GradSums acc;
+            GradSums acc(pr.x);
             for (uint32_t cb = b0; cb < b1; cb += span) chunk1(ch, pr.z, pr.w, cb, min(span, b1 - cb), acc);
             publish(q, acc);
         };

@@ -278,7 +278,7 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     {
         const int j = warp % g.G;
         const int wpc = kGrpWarps / g.G;
-        GradSums acc;
+        GradSums acc(prm[j].x);
         for (int t = (warp / g.G) * 32 + lane; t < p.ns * g.l; t += wpc * 32) {
             const int s = int(fast_div(uint32_t(t), g.div_l));
             const int e = t - s * g.l;
@@ -290,7 +290,7 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
             acc.add(dz, xv);
         }
         const FF d1 = ff_warp_sum(acc.ff_dz());
-        const FF d2 = ff_warp_sum(acc.ff_dzx());
+        const FF d2 = ff_warp_sum(acc.ff_dzc());
         if (lane == 0) ws[warp] = make_double2(ff_to_double(d1), ff_to_double(d2));
     }
     __syncthreads();
@@ -312,8 +312,8 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
         }
         const int64_t ch = p.ch0 + threadIdx.x;
         const float4 pr = prm[threadIdx.x];
-        // sum dz*(x - mean) = sum dz*x - mean*sum dz, in double
-        const double t2c = t2 - double(pr.x) * t1;
+        // t2 is sum dz*(x - mean), centred on the saved mean as it was summed
+        const double t2c = t2;
         if (p.rank == 0) {
             if (a.db) a.db[ch] = float(t1);
             if (a.dw) a.dw[ch] = float(t2c * double(pr.y));
