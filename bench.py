@@ -156,7 +156,7 @@ class ClockSampler:
 
 def ncu_traffic(kernel: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the
-    kernel sources are unchanged since the capture (else None)."""
+    sources that kernel is built from are unchanged since the capture (else None)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(p) as f:
@@ -165,7 +165,7 @@ def ncu_traffic(kernel: str):
         return None
     from normalization_layernorm_rmsnorm_gb300.build import source_digest
     e = d.get(kernel)
-    if not e or e.get("source_digest") != source_digest():
+    if not e or e.get("source_digest") != source_digest(e.get("sources")):
         return None
     return e.get("dram_bytes_per_launch")
 

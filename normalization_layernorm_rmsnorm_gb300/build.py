@@ -71,12 +71,16 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     return LIB
 
 
-def source_digest() -> str:
-    """sha256 of the CUDA sources and the public header (names the kernel
-    version an ncu capture was taken on)."""
+def source_digest(files=None) -> str:
+    """sha256 of CUDA sources and the public header (names the kernel version
+    an ncu capture was taken on): all of them, or the named files of csrc/
+    (and "libnorm.h") that one kernel family is built from."""
     import hashlib
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(CSRC, "*"))) + [os.path.join(INCLUDE, "libnorm.h")]
+    if files is None:
+        files = sorted(glob.glob(os.path.join(CSRC, "*"))) + [os.path.join(INCLUDE, "libnorm.h")]
+    else:
+        files = [os.path.join(INCLUDE if f == "libnorm.h" else CSRC, f) for f in sorted(files)]
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:

@@ -1,7 +1,7 @@
 // common.cuh -- device helpers shared by the libnorm kernels: storage-type
 // traits, 128-bit global loads/stores, warp reductions, Chan's merge of
-// (count, mean, M2) triples, Kahan accumulation and division by a runtime
-// constant.
+// (count, mean, M2) triples, float-float sums, mbarrier and bulk-copy
+// wrappers, and division by a runtime constant.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -166,18 +166,6 @@ __device__ __forceinline__ FF ff_warp_sum(FF v) {
     return v;
 }
 __device__ __forceinline__ double ff_to_double(FF v) { return double(v.hi) + double(v.lo); }
-
-// Compensated (Kahan) float accumulation.
-struct Kahan {
-    float s = 0.f;
-    float c = 0.f;
-    __device__ __forceinline__ void add(float v) {
-        const float y = v - c;
-        const float t = s + y;
-        c = (t - s) - y;
-        s = t;
-    }
-};
 
 // ---------------------------------------------------------------------------
 // division of 32-bit unsigned integers by a runtime constant d < 2^32:
