@@ -700,15 +700,22 @@ inline bool rr_plan(RrGeom& g, int& tpr, size_t& smem, const RowArgs& a, size_t 
     return true;
 }
 
-template <typename T, bool LN, bool DB>
-const void* rr_fn(int tpr) {
+template <typename T, bool LN, bool DB, int VPT>
+const void* rr_fn_v(int tpr) {
     switch (tpr) {
-    case 32: return (const void*)&row_bwd_ring_kernel<T, LN, 32, DB>;
-    case 64: return (const void*)&row_bwd_ring_kernel<T, LN, 64, DB>;
-    case 128: return (const void*)&row_bwd_ring_kernel<T, LN, 128, DB>;
-    case 256: return (const void*)&row_bwd_ring_kernel<T, LN, 256, DB>;
-    default: return (const void*)&row_bwd_ring_kernel<T, LN, 512, DB>;
+    case 32: return (const void*)&row_bwd_ring_kernel<T, LN, 32, DB, VPT>;
+    case 64: return (const void*)&row_bwd_ring_kernel<T, LN, 64, DB, VPT>;
+    case 128: return (const void*)&row_bwd_ring_kernel<T, LN, 128, DB, VPT>;
+    case 256: return (const void*)&row_bwd_ring_kernel<T, LN, 256, DB, VPT>;
+    default: return (const void*)&row_bwd_ring_kernel<T, LN, 512, DB, VPT>;
     }
+}
+
+// The ring kernel for rows of `nvec` vectors at TPR threads per row: 3
+// vectors per thread when that covers the row, else 4.
+template <typename T, bool LN, bool DB>
+const void* rr_fn(int tpr, int nvec) {
+    return nvec <= 3 * tpr ? rr_fn_v<T, LN, DB, 3>(tpr) : rr_fn_v<T, LN, DB, kRrVpt>(tpr);
 }
 
 // Launches a ring kernel on `grid` CTAs (one per SM at most).
@@ -792,8 +799,9 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     int64_t groups, p;
     int block = kRrThreads;
     if (ring) {
-        fn = layernorm ? rr_fn<T, true, true>(rtpr)
-                       : (a.ws_db ? rr_fn<T, false, true>(rtpr) : rr_fn<T, false, false>(rtpr));
+        const int nv = a.cols / kVec<T>;
+        fn = layernorm ? rr_fn<T, true, true>(rtpr, nv)
+                       : (a.ws_db ? rr_fn<T, false, true>(rtpr, nv) : rr_fn<T, false, false>(rtpr, nv));
         groups = rg.chunks;
         p = d->sms;
     } else {

@@ -131,12 +131,15 @@ __device__ __forceinline__ void rr_partial_row(const float (&acc)[VPT][VE], floa
 }
 
 // DB: accumulate db = sum dy (LayerNorm, or RMSNorm with a bias); a template
-// parameter so that RMSNorm without one keeps those registers free.
-template <typename T, bool LN, int TPR, bool DB>
+// parameter so that RMSNorm without one keeps those registers free.  VPT: the
+// row's vectors per thread (3 or 4): the dw/db accumulators are VPT*VE floats
+// each, and at 544 threads a CTA has 96 registers per thread, so rows that
+// need 3 vectors per thread do not carry a fourth's accumulators (they spilled).
+template <typename T, bool LN, int TPR, bool DB, int VPT>
 __global__ void __launch_bounds__(kRrThreads, 1)
 row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
     constexpr int VE = kVec<T>;
-    constexpr int VPT = kRrVpt;
+    static_assert(VPT <= kRrVpt, "at most kRrVpt vectors per thread");
     constexpr int RPC = kRrConsumers / TPR;
     constexpr int NW = TPR / 32;
     constexpr int NV = LN ? 2 : 1;
