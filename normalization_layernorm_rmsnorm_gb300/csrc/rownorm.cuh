@@ -244,7 +244,8 @@ __device__ __forceinline__ void write_partial_row(const float (&acc)[VPT][VE], f
 // ---------------------------------------------------------------------------
 // backward, rows held in registers, next row prefetched; dw/db partials per CTA
 // ---------------------------------------------------------------------------
-template <typename T, bool LN, int TPR, int VE>
+// DB: accumulate db = sum dy (LayerNorm, or RMSNorm with a bias).
+template <typename T, bool LN, int TPR, int VE, bool DB = LN>
 __global__ void __launch_bounds__(kRowBwdBlock)
 row_bwd_kernel(const RowArgs a) {
     constexpr int VPT = kRowBwdVpt;
@@ -263,7 +264,6 @@ row_bwd_kernel(const RowArgs a) {
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
     const T* __restrict__ dy = reinterpret_cast<const T*>(a.dy);
     T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
-    const bool want_db = LN || a.ws_db != nullptr;  // RMSNorm: the optional bias
     int phase = 0;
 
     float accw[VPT][VE];
@@ -344,7 +344,7 @@ row_bwd_kernel(const RowArgs a) {
                     } else {
                         o[k] = rs * (g - xv * c2);
                         accw[j][k] = fmaf(dv, xv * rs, accw[j][k]);
-                        if (want_db) accb[j][k] += dv;
+                        if constexpr (DB) accb[j][k] += dv;
                     }
                 }
                 store_vec<T, VE>(dxr + int64_t(vi) * VE, o);
@@ -364,9 +364,11 @@ row_bwd_kernel(const RowArgs a) {
     if (a.ws_dw)
         write_partial_row<TPR, VPT, VE, RPC>(accw, a.ws_dw + int64_t(blockIdx.x) * cols, &part[0][0],
                                              group, t, cols);
-    if (a.ws_db)
-        write_partial_row<TPR, VPT, VE, RPC>(accb, a.ws_db + int64_t(blockIdx.x) * cols, &part[0][0],
-                                             group, t, cols);
+    if constexpr (DB) {
+        if (a.ws_db)
+            write_partial_row<TPR, VPT, VE, RPC>(accb, a.ws_db + int64_t(blockIdx.x) * cols, &part[0][0],
+                                                 group, t, cols);
+    }
 }
 
 // Compensated fp32 sum (Neumaier's variant of Kahan's): exact to about two
@@ -744,7 +746,17 @@ const void* row_fwd_fn(int tpr) {
 }
 
 template <typename T, bool LN, int VE>
-const void* row_bwd_fn(int tpr) {
+const void* row_bwd_fn(int tpr, bool db) {
+    if (!LN && db) {
+        switch (tpr) {  // RMSNorm with a bias
+        case 32: return (const void*)&row_bwd_kernel<T, LN, 32, VE, true>;
+        case 64: return (const void*)&row_bwd_kernel<T, LN, 64, VE, true>;
+        case 128: return (const void*)&row_bwd_kernel<T, LN, 128, VE, true>;
+        case 256: return (const void*)&row_bwd_kernel<T, LN, 256, VE, true>;
+        case 512: return (const void*)&row_bwd_kernel<T, LN, 512, VE, true>;
+        default: return (const void*)&row_bwd_wide_kernel<T, LN, VE>;
+        }
+    }
     switch (tpr) {
     case 32: return (const void*)&row_bwd_kernel<T, LN, 32, VE>;
     case 64: return (const void*)&row_bwd_kernel<T, LN, 64, VE>;
@@ -805,8 +817,9 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
         groups = rg.chunks;
         p = d->sms;
     } else {
-        fn = layernorm ? (vec ? row_bwd_fn<T, true, kVec<T>>(tpr) : row_bwd_fn<T, true, 1>(tpr))
-                       : (vec ? row_bwd_fn<T, false, kVec<T>>(tpr) : row_bwd_fn<T, false, 1>(tpr));
+        const bool db = a.ws_db != nullptr;
+        fn = layernorm ? (vec ? row_bwd_fn<T, true, kVec<T>>(tpr, db) : row_bwd_fn<T, true, 1>(tpr, db))
+                       : (vec ? row_bwd_fn<T, false, kVec<T>>(tpr, db) : row_bwd_fn<T, false, 1>(tpr, db));
         block = tpr ? kRowBwdBlock : kRowWideBlock;
         const int rpc = tpr ? block / tpr : 1;
         const int occ = cached_occupancy(fn, block, 0);
