@@ -8,8 +8,10 @@ on the full-size synthetic workloads:
   * BatchNorm2d fp32 [256, 64, 56, 56] + residual + ReLU, training (ResNet)
   * BatchNorm2d fp16 [128, 512, 7, 7] + GELU(erf), training
   * BatchNorm2d fp32 [256, 64, 56, 56] + residual + ReLU, eval (running statistics)
-L2 is flushed (a 512 MB write) before every call; each call is timed with CUDA
-events on the stream it is launched on.  value = algorithmic bytes of the step
+L2 is flushed before every call: a 512 MB write, then a read of another 512 MB
+buffer, so the call starts with none of its data in L2 and without the flush's
+dirty lines (whose write-back would otherwise land inside the timed call); each
+call is timed with CUDA events on the stream it is launched on.  value = algorithmic bytes of the step
 (every input read once, every output written once, saved statistics, ReLU mask
 bits) / summed device time, in GB/s.  Per-call times, GB/s and fraction of the
 measured HBM copy bandwidth are reported per workload.  Beside the step, and
@@ -186,11 +188,14 @@ def run_gpu(args, world, rank, local):
     calls = workloads.build_calls(dev)
     extra = workloads.build_extra_calls(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sum = torch.empty(1, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     def one_step(record, which=calls):
         for c in which:
             flush.fill_(1.0)
+            torch.sum(flush_rd, dim=0, keepdim=True, out=flush_sum)  # L2 left clean
             s = torch.cuda.Event(enable_timing=True)
             e = torch.cuda.Event(enable_timing=True)
             s.record(stream)
@@ -252,7 +257,7 @@ def run_gpu(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded counter-based generator; shapes of the articles' models)",
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
-                   "l2": "flushed (512 MB write) before every call",
+                   "l2": "flushed before every call (512 MB write, then 512 MB read: no call data, no dirty lines)",
                    "timing": "CUDA events around each call on its stream; step = sum of calls"},
         "roofline": roofline,
         "gpu_launches": sum(c.launches for c in calls) * args.steps,

@@ -62,58 +62,17 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// The element loops work on pairs of fp32 values with Blackwell's packed FP32
-// instructions (add/mul/fma.rn.f32x2): two elements per instruction, each
-// rounded as the scalar instruction would.
-template <typename T> constexpr int kPairs = kVec<T> / 2;
-
-template <typename T> __device__ __forceinline__ float2 cfr_cvt2(uint32_t w);
-template <> __device__ __forceinline__ float2 cfr_cvt2<__half>(uint32_t w) {
-    return __half22float2(*reinterpret_cast<const __half2*>(&w));
-}
-template <> __device__ __forceinline__ float2 cfr_cvt2<__nv_bfloat16>(uint32_t w) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-}
-template <typename T> __device__ __forceinline__ uint32_t cfr_pack2(float2 v);
-template <> __device__ __forceinline__ uint32_t cfr_pack2<__half>(float2 v) {
-    const __half2 h = __float22half2_rn(v);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-template <> __device__ __forceinline__ uint32_t cfr_pack2<__nv_bfloat16>(float2 v) {
-    const __nv_bfloat162 h = __float22bfloat162_rn(v);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 // 16 bytes of shared memory as fp32 pairs.
 template <typename T>
 __device__ __forceinline__ void cfr_load2(const unsigned char* p, float2 (&v)[kPairs<T>]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    if constexpr (sizeof(T) == 4) {
-        v[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
-        v[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
-    } else {
-        v[0] = cfr_cvt2<T>(u.x);
-        v[1] = cfr_cvt2<T>(u.y);
-        v[2] = cfr_cvt2<T>(u.z);
-        v[3] = cfr_cvt2<T>(u.w);
-    }
+    unpack2<T>(*reinterpret_cast<const uint4*>(p), v);
 }
 
 // fp32 pairs rounded to T and stored as one 16-byte global store.
 template <typename T>
 __device__ __forceinline__ void cfr_store2(T* p, const float2 (&o)[kPairs<T>]) {
-    uint4 u;
-    if constexpr (sizeof(T) == 4) {
-        u = make_uint4(__float_as_uint(o[0].x), __float_as_uint(o[0].y), __float_as_uint(o[1].x),
-                       __float_as_uint(o[1].y));
-    } else {
-        u = make_uint4(cfr_pack2<T>(o[0]), cfr_pack2<T>(o[1]), cfr_pack2<T>(o[2]), cfr_pack2<T>(o[3]));
-    }
-    st_v4(p, u);
+    st_v4(p, pack2x<T>(o));
 }
-
-__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
-__device__ __forceinline__ float2 f2neg(float2 v) { return make_float2(-v.x, -v.y); }
 
 // Producer (whole warp, lane 0 issues): the CTA's tiles into the ring, in
 // order.  `map_a` is x (forward) or dy (backward); `map_b` is x (backward).

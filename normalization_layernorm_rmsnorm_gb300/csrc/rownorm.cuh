@@ -124,13 +124,61 @@ __device__ __forceinline__ void load_row(const T* base, int64_t row, int cols, i
     }
 }
 
+// The element loops of the 16-byte vector paths work on pairs of fp32 values
+// with Blackwell's packed FP32 instructions (add/mul/fma.rn.f32x2): two
+// elements per instruction, each rounded as the scalar instruction would.
+template <typename T> constexpr int kPairs = kVec<T> / 2;
+
+template <typename T> __device__ __forceinline__ float2 cvt2(uint32_t w);
+template <> __device__ __forceinline__ float2 cvt2<__half>(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+template <> __device__ __forceinline__ float2 cvt2<__nv_bfloat16>(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+template <typename T> __device__ __forceinline__ uint32_t pack2(float2 v);
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float2 v) {
+    const __half2 h = __float22half2_rn(v);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float2 v) {
+    const __nv_bfloat162 h = __float22bfloat162_rn(v);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 16 raw bytes as fp32 pairs.
+template <typename T>
+__device__ __forceinline__ void unpack2(const uint4 u, float2 (&v)[kPairs<T>]) {
+    if constexpr (sizeof(T) == 4) {
+        v[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+        v[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+    } else {
+        v[0] = cvt2<T>(u.x);
+        v[1] = cvt2<T>(u.y);
+        v[2] = cvt2<T>(u.z);
+        v[3] = cvt2<T>(u.w);
+    }
+}
+
+// fp32 pairs rounded to T, as 16 raw bytes.
+template <typename T>
+__device__ __forceinline__ uint4 pack2x(const float2 (&o)[kPairs<T>]) {
+    if constexpr (sizeof(T) == 4)
+        return make_uint4(__float_as_uint(o[0].x), __float_as_uint(o[0].y), __float_as_uint(o[1].x),
+                          __float_as_uint(o[1].y));
+    else
+        return make_uint4(pack2<T>(o[0]), pack2<T>(o[1]), pack2<T>(o[2]), pack2<T>(o[3]));
+}
+
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 f2neg(float2 v) { return make_float2(-v.x, -v.y); }
+
 // ---------------------------------------------------------------------------
 // forward, rows held in registers
 // ---------------------------------------------------------------------------
-template <typename T, bool LN, int TPR, int VE>
+template <typename T, bool LN, int TPR, int VE, int VPT = kRowFwdVpt>
 __global__ void __launch_bounds__(row_fwd_block(TPR))
 row_fwd_kernel(const RowArgs a) {
-    constexpr int VPT = kRowFwdVpt;
     constexpr int BLOCK = row_fwd_block(TPR);
     constexpr int RPC = BLOCK / TPR;
     constexpr int NW = TPR / 32;
@@ -145,59 +193,122 @@ row_fwd_kernel(const RowArgs a) {
     T* __restrict__ y = reinterpret_cast<T*>(a.y);
     int phase = 0;
 
-    for (int64_t row = int64_t(blockIdx.x) * RPC + group; row < a.rows;
-         row += int64_t(gridDim.x) * RPC) {
+    const int64_t stride = int64_t(gridDim.x) * RPC;
+    int64_t row = int64_t(blockIdx.x) * RPC + group;
+    if constexpr (VE > 1) {
+        // 16-byte vectors: the element arithmetic on fp32 pairs, and the next
+        // row of the group loaded while this one is normalised
+        constexpr int H = VE / 2;
         Pack<T, VE> xp[VPT];
-        load_row<T, TPR, VPT, VE>(x, row, cols, t, xp);
-
-        float mu = 0.f;
-        float q[1] = {0.f};
-        if constexpr (LN) {
-            float s[1] = {0.f};
+        if (row < a.rows) load_row<T, TPR, VPT, VE>(x, row, cols, t, xp);
+        for (; row < a.rows; row += stride) {
+            Pack<T, VE> xn[VPT];
+            if (row + stride < a.rows) load_row<T, TPR, VPT, VE>(x, row + stride, cols, t, xn);
+            T* yr = y + row * cols;
+            float2 xv[VPT][H];
 #pragma unroll
-            for (int j = 0; j < VPT; ++j)
+            for (int j = 0; j < VPT; ++j) unpack2<T>(xp[j].u, xv[j]);
+            float mu = 0.f;
+            float2 q2 = f2(0.f);
+            if constexpr (LN) {
+                float2 s2 = f2(0.f);
 #pragma unroll
-                for (int k = 0; k < VE; ++k) s[0] += elem(xp[j], k);
-            group_sum<TPR, 1>(s, &red[group][0], phase, group);
-            mu = s[0] / fcols;
+                for (int j = 0; j < VPT; ++j)
+#pragma unroll
+                    for (int h = 0; h < H; ++h) s2 = __fadd2_rn(s2, xv[j][h]);
+                float s[1] = {s2.x + s2.y};
+                group_sum<TPR, 1>(s, &red[group][0], phase, group);
+                mu = s[0] / fcols;
+                const float2 nmu = f2(-mu);
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    if (j * TPR + t < nvec) {  // the zero padding past the row is not centred
+#pragma unroll
+                        for (int h = 0; h < H; ++h) {
+                            xv[j][h] = __fadd2_rn(xv[j][h], nmu);
+                            q2 = __ffma2_rn(xv[j][h], xv[j][h], q2);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < VPT; ++j)
+#pragma unroll
+                    for (int h = 0; h < H; ++h) q2 = __ffma2_rn(xv[j][h], xv[j][h], q2);
+            }
+            float q[1] = {q2.x + q2.y};
+            group_sum<TPR, 1>(q, &red[group][0], phase, group);
+            const float rs = rsqrtf(q[0] / fcols + a.eps);
+            if (t == 0) {
+                if (LN && a.mean) a.mean[row] = mu;
+                if (a.rstd) a.rstd[row] = rs;
+            }
+            const float2 rs2 = f2(rs);
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
-                if (j * TPR + t < nvec) {
+                const int vi = j * TPR + t;
+                if (vi < nvec) {
+                    float2 wv[H], bv[H], o[H];
+                    if (a.w) {
+                        unpack2<T>(ld_cached_v4(reinterpret_cast<const T*>(a.w) + int64_t(vi) * VE), wv);
+                    } else {
 #pragma unroll
-                    for (int k = 0; k < VE; ++k) {
-                        const float d = elem(xp[j], k) - mu;
+                        for (int h = 0; h < H; ++h) wv[h] = f2(1.f);
+                    }
+                    if (a.b) {  // LayerNorm's bias, or RMSNorm's optional one
+                        unpack2<T>(ld_cached_v4(reinterpret_cast<const T*>(a.b) + int64_t(vi) * VE), bv);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < H; ++h) bv[h] = f2(0.f);
+                    }
+#pragma unroll
+                    for (int h = 0; h < H; ++h) o[h] = __ffma2_rn(__fmul2_rn(xv[j][h], rs2), wv[h], bv[h]);
+                    st_v4(yr + int64_t(vi) * VE, pack2x<T>(o));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) xp[j] = xn[j];
+        }
+    } else {
+        for (; row < a.rows; row += stride) {
+            Pack<T, VE> xp[VPT];
+            load_row<T, TPR, VPT, VE>(x, row, cols, t, xp);
+            T* yr = y + row * cols;
+            float mu = 0.f;
+            float q[1] = {0.f};
+            if constexpr (LN) {
+                float s[1] = {0.f};
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) s[0] += elem(xp[j], 0);
+                group_sum<TPR, 1>(s, &red[group][0], phase, group);
+                mu = s[0] / fcols;
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    if (j * TPR + t < nvec) {
+                        const float d = elem(xp[j], 0) - mu;
                         q[0] = fmaf(d, d, q[0]);
                     }
                 }
+            } else {
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) q[0] = fmaf(elem(xp[j], 0), elem(xp[j], 0), q[0]);
             }
-        } else {
+            group_sum<TPR, 1>(q, &red[group][0], phase, group);
+            const float rs = rsqrtf(q[0] / fcols + a.eps);
+            if (t == 0) {
+                if (LN && a.mean) a.mean[row] = mu;
+                if (a.rstd) a.rstd[row] = rs;
+            }
 #pragma unroll
-            for (int j = 0; j < VPT; ++j)
-#pragma unroll
-                for (int k = 0; k < VE; ++k) q[0] = fmaf(elem(xp[j], k), elem(xp[j], k), q[0]);
-        }
-        group_sum<TPR, 1>(q, &red[group][0], phase, group);
-        const float rs = rsqrtf(q[0] / fcols + a.eps);
-
-        if (t == 0) {
-            if (LN && a.mean) a.mean[row] = mu;
-            if (a.rstd) a.rstd[row] = rs;
-        }
-
-        T* yr = y + row * cols;
-#pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int vi = j * TPR + t;
-            if (vi < nvec) {
-                float wv[VE], bv[VE], o[VE];
-                load_param<T, VE>(a.w, vi, wv, 1.f);
-                load_param<T, VE>(a.b, vi, bv, 0.f);  // LayerNorm's bias, or RMSNorm's optional one
-#pragma unroll
-                for (int k = 0; k < VE; ++k) {
-                    const float xh = (elem(xp[j], k) - mu) * rs;
-                    o[k] = fmaf(xh, wv[k], bv[k]);
+            for (int j = 0; j < VPT; ++j) {
+                const int vi = j * TPR + t;
+                if (vi < nvec) {
+                    float wv[1], bv[1], o[1];
+                    load_param<T, 1>(a.w, vi, wv, 1.f);
+                    load_param<T, 1>(a.b, vi, bv, 0.f);
+                    o[0] = fmaf((elem(xp[j], 0) - mu) * rs, wv[0], bv[0]);
+                    store_vec<T, 1>(yr + vi, o);
                 }
-                store_vec<T, VE>(yr + int64_t(vi) * VE, o);
             }
         }
     }
@@ -732,17 +843,28 @@ inline nrm_status rr_launch(const void* fn, const RowArgs& a, const RrGeom& g, s
     return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(kRrThreads), kargs, smem, s), "row ring launch");
 }
 
-template <typename T, bool LN, int VE>
-const void* row_fwd_fn(int tpr) {
+template <typename T, bool LN, int VE, int VPT>
+const void* row_fwd_fn_v(int tpr) {
     switch (tpr) {
-    case 32: return (const void*)&row_fwd_kernel<T, LN, 32, VE>;
-    case 64: return (const void*)&row_fwd_kernel<T, LN, 64, VE>;
-    case 128: return (const void*)&row_fwd_kernel<T, LN, 128, VE>;
-    case 256: return (const void*)&row_fwd_kernel<T, LN, 256, VE>;
-    case 512: return (const void*)&row_fwd_kernel<T, LN, 512, VE>;
-    case 1024: return (const void*)&row_fwd_kernel<T, LN, 1024, VE>;
+    case 32: return (const void*)&row_fwd_kernel<T, LN, 32, VE, VPT>;
+    case 64: return (const void*)&row_fwd_kernel<T, LN, 64, VE, VPT>;
+    case 128: return (const void*)&row_fwd_kernel<T, LN, 128, VE, VPT>;
+    case 256: return (const void*)&row_fwd_kernel<T, LN, 256, VE, VPT>;
+    case 512: return (const void*)&row_fwd_kernel<T, LN, 512, VE, VPT>;
+    case 1024: return (const void*)&row_fwd_kernel<T, LN, 1024, VE, VPT>;
     default: return (const void*)&row_fwd_wide_kernel<T, LN, VE>;
     }
+}
+
+// The forward for rows of `nvec` vectors at TPR threads per row (0: the wide
+// kernel): on the 16-byte path 3 vectors per thread when that covers the row
+// (no idle fourth vector, e.g. 768 fp16 columns at 32 threads), else 4.
+template <typename T, bool LN, int VE>
+const void* row_fwd_fn(int tpr, int nvec) {
+    if constexpr (VE > 1) {
+        if (tpr && nvec <= 3 * tpr) return row_fwd_fn_v<T, LN, VE, 3>(tpr);
+    }
+    return row_fwd_fn_v<T, LN, VE, kRowFwdVpt>(tpr);
 }
 
 template <typename T, bool LN, int VE>
@@ -782,8 +904,10 @@ nrm_status row_fwd(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s) {
     if (a.rows == 0) return NRM_OK;
     const int ve = vec ? kVec<T> : 1;
     const int tpr = row_tpr(a.cols / ve, kRowFwdVpt, kRowMaxFwdTpr);
-    const void* fn = layernorm ? (vec ? row_fwd_fn<T, true, kVec<T>>(tpr) : row_fwd_fn<T, true, 1>(tpr))
-                               : (vec ? row_fwd_fn<T, false, kVec<T>>(tpr) : row_fwd_fn<T, false, 1>(tpr));
+    const int nvec = a.cols / ve;
+    const void* fn = layernorm
+                         ? (vec ? row_fwd_fn<T, true, kVec<T>>(tpr, nvec) : row_fwd_fn<T, true, 1>(tpr, nvec))
+                         : (vec ? row_fwd_fn<T, false, kVec<T>>(tpr, nvec) : row_fwd_fn<T, false, 1>(tpr, nvec));
     const int block = tpr ? row_fwd_block(tpr) : kRowWideBlock;
     const int rpc = tpr ? block / tpr : 1;
     const int occ = cached_occupancy(fn, block, 0);

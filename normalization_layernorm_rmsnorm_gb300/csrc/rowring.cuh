@@ -9,7 +9,8 @@
 // warps process the rows in groups of TPR threads (vector j*TPR + t of a row
 // belongs to thread t of its group): the row sums from the slot, then dx from
 // a second read of the slot, stored with 16-byte stores, and dw/db
-// accumulated per thread in fp32.  The weight is converted to fp32 once per
+// accumulated per thread in fp32; the element arithmetic runs on fp32 pairs
+// with the packed FP32 instructions.  The weight is converted to fp32 once per
 // CTA and kept in shared memory.  Memory parallelism comes from the ring
 // (several chunks in flight per SM), not from registers.  (The forward keeps
 // the register kernel: its rows need one read, and many resident CTAs hide
@@ -64,38 +65,48 @@ __device__ void rr_produce(const RowArgs& a, const RrGeom& g, unsigned char* rin
     }
 }
 
-template <typename T>
-__device__ __forceinline__ void rr_unpack(const unsigned char* p, float (&v)[kVec<T>]) {
-    Pack<T, kVec<T>> pk;
-    pk.u = *reinterpret_cast<const uint4*>(p);
-#pragma unroll
-    for (int k = 0; k < kVec<T>; ++k) v[k] = Io<T>::load(pk.b[k]);
-}
-
-// VE consecutive fp32 values from shared memory (16-byte aligned), as float4s.
+// The fp32 weight in shared memory is laid out [VE/4][nvec][4]: quarter h of
+// vector vi at float4 index h*nvec + vi, so a warp's 16-byte reads of one
+// quarter for consecutive vectors are contiguous (no bank conflicts).
 template <int VE>
-__device__ __forceinline__ void rr_params(const float* p, float (&v)[VE]) {
+__device__ __forceinline__ void rr_params2(const float* wsm, int vi, int nvec, float2 (&v)[VE / 2]) {
 #pragma unroll
     for (int h = 0; h < VE / 4; ++h) {
-        const float4 f = reinterpret_cast<const float4*>(p)[h];
-        v[4 * h] = f.x;
-        v[4 * h + 1] = f.y;
-        v[4 * h + 2] = f.z;
-        v[4 * h + 3] = f.w;
+        const float4 f = reinterpret_cast<const float4*>(wsm)[h * nvec + vi];
+        v[2 * h] = make_float2(f.x, f.y);
+        v[2 * h + 1] = make_float2(f.z, f.w);
     }
 }
 
-// The weight of the row as fp32 in shared memory (consumer threads).
+// Pair accumulators back to per-element form.
+template <int VPT, int VE>
+__device__ __forceinline__ void unpair(const float2 (&in)[VPT][VE / 2], float (&out)[VPT][VE]) {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+        for (int h = 0; h < VE / 2; ++h) {
+            out[j][2 * h] = in[j][h].x;
+            out[j][2 * h + 1] = in[j][h].y;
+        }
+}
+
+// The weight of the row as fp32 in shared memory, in rr_params2's layout
+// (consumer threads).
 template <typename T>
 __device__ __forceinline__ void rr_stage_weight(const RowArgs& a, float* wsm) {
     using bits = typename Io<T>::bits_t;
-    for (int i = threadIdx.x; i < a.cols; i += kRrConsumers)
-        wsm[i] = a.w ? Io<T>::load(reinterpret_cast<const bits*>(a.w)[i]) : 1.f;
+    constexpr int VE = kVec<T>;
+    const int nvec = a.cols / VE;
+    for (int i = threadIdx.x; i < a.cols; i += kRrConsumers) {
+        const int vi = i / VE, k = i - vi * VE;
+        wsm[((k >> 2) * nvec + vi) * 4 + (k & 3)] = a.w ? Io<T>::load(reinterpret_cast<const bits*>(a.w)[i]) : 1.f;
+    }
 }
 
 // The CTA's dw (or db) partial row: each thread's per-column sums, summed over
 // the row groups in group order.  Consumer threads only; `part` is scratch
-// shared memory of RPC*TPR*VE floats (the drained ring).
+// shared memory of RPC*TPR*VE floats (the drained ring), staged element-major
+// (element k of thread t at k*TPR + t) so that the stores do not conflict.
 template <int TPR, int VPT, int VE, int RPC>
 __device__ __forceinline__ void rr_partial_row(const float (&acc)[VPT][VE], float* ws, float* part, int group,
                                                int t, int cols) {
@@ -114,10 +125,11 @@ __device__ __forceinline__ void rr_partial_row(const float (&acc)[VPT][VE], floa
         for (int j = 0; j < VPT; ++j) {
             if (j * TPR * VE >= cols) break;
 #pragma unroll
-            for (int k = 0; k < VE; ++k) part[group * TPR * VE + t * VE + k] = acc[j][k];
+            for (int k = 0; k < VE; ++k) part[group * TPR * VE + k * TPR + t] = acc[j][k];
             named_barrier(kRrBarConsumers, kRrConsumers);
             for (int i = threadIdx.x; i < TPR * VE; i += kRrConsumers) {
-                const int col = j * TPR * VE + i;
+                const int k = i / TPR;
+                const int col = j * TPR * VE + (i - k * TPR) * VE + k;
                 if (col < cols) {
                     float sum = 0.f;
 #pragma unroll
@@ -177,12 +189,14 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
         const size_t row_bytes = size_t(cols) * sizeof(T);
         T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
         int phase = 0;
-        float accw[VPT][VE];
-        float accb[VPT][VE];
+        // the element arithmetic runs on fp32 pairs (packed FP32 instructions)
+        constexpr int H = VE / 2;
+        float2 accw[VPT][H];
+        float2 accb[VPT][H];
 #pragma unroll
         for (int j = 0; j < VPT; ++j)
 #pragma unroll
-            for (int k = 0; k < VE; ++k) accw[j][k] = accb[j][k] = 0.f;
+            for (int h = 0; h < H; ++h) accw[j][h] = accb[j][h] = f2(0.f);
 
         int q = 0;
         for (int64_t c = blockIdx.x; c < g.chunks; c += gridDim.x, ++q) {
@@ -197,58 +211,67 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
                 const unsigned char* xr = base + size_t(g.R + r) * row_bytes;
                 const float rs = st[r];
                 const float mu = LN ? st[g.R + r] : 0.f;
+                const float2 rs2 = f2(rs);
+                const float2 nmu = f2(-mu);
                 // the row sums: sum(dy*w) and sum(dy*w*xhat) (LN) / sum(dy*w*x) (RMS)
-                float s[NV];
+                float2 s2[NV];
 #pragma unroll
-                for (int i = 0; i < NV; ++i) s[i] = 0.f;
+                for (int i = 0; i < NV; ++i) s2[i] = f2(0.f);
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
                     const int vi = j * TPR + t;
                     if (vi < nvec) {
-                        float dv[VE], xv[VE], wv[VE];
-                        rr_unpack<T>(dr + size_t(vi) * 16, dv);
-                        rr_unpack<T>(xr + size_t(vi) * 16, xv);
-                        rr_params<VE>(wsm + vi * VE, wv);
+                        float2 dv[H], xv[H], wv[H];
+                        unpack2<T>(*reinterpret_cast<const uint4*>(dr + size_t(vi) * 16), dv);
+                        unpack2<T>(*reinterpret_cast<const uint4*>(xr + size_t(vi) * 16), xv);
+                        rr_params2<VE>(wsm, vi, nvec, wv);
 #pragma unroll
-                        for (int k = 0; k < VE; ++k) {
-                            const float gw = dv[k] * wv[k];
+                        for (int h = 0; h < H; ++h) {
+                            const float2 gw = __fmul2_rn(dv[h], wv[h]);
                             if constexpr (LN) {
-                                const float xh = (xv[k] - mu) * rs;
-                                s[0] += gw;
-                                s[NV - 1] = fmaf(gw, xh, s[NV - 1]);
+                                const float2 xh = __fmul2_rn(__fadd2_rn(xv[h], nmu), rs2);
+                                s2[0] = __fadd2_rn(s2[0], gw);
+                                s2[NV - 1] = __ffma2_rn(gw, xh, s2[NV - 1]);
                             } else {
-                                s[0] = fmaf(gw, xv[k], s[0]);
+                                s2[0] = __ffma2_rn(gw, xv[h], s2[0]);
                             }
                         }
                     }
                 }
+                float s[NV];
+#pragma unroll
+                for (int i = 0; i < NV; ++i) s[i] = s2[i].x + s2[i].y;
                 group_sum<TPR, NV>(s, &red[group][0], phase, group);
                 const float c1 = s[0] / fcols;
                 const float c2 = LN ? s[NV - 1] / fcols : c1 * rs * rs;
+                const float2 nc1 = f2(-c1);
+                const float2 nc2 = f2(-c2);
                 T* dxr = dx + (r0 + r) * cols;
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
                     const int vi = j * TPR + t;
                     if (vi < nvec) {
-                        float dv[VE], xv[VE], wv[VE], o[VE];
-                        rr_unpack<T>(dr + size_t(vi) * 16, dv);
-                        rr_unpack<T>(xr + size_t(vi) * 16, xv);
-                        rr_params<VE>(wsm + vi * VE, wv);
+                        float2 dv[H], xv[H], wv[H], o[H];
+                        unpack2<T>(*reinterpret_cast<const uint4*>(dr + size_t(vi) * 16), dv);
+                        unpack2<T>(*reinterpret_cast<const uint4*>(xr + size_t(vi) * 16), xv);
+                        rr_params2<VE>(wsm, vi, nvec, wv);
 #pragma unroll
-                        for (int k = 0; k < VE; ++k) {
-                            const float gw = dv[k] * wv[k];
+                        for (int h = 0; h < H; ++h) {
+                            const float2 gw = __fmul2_rn(dv[h], wv[h]);
                             if constexpr (LN) {
-                                const float xh = (xv[k] - mu) * rs;
-                                o[k] = rs * (gw - c1 - xh * c2);
-                                accw[j][k] = fmaf(dv[k], xh, accw[j][k]);
-                                accb[j][k] += dv[k];
+                                // dx = rs * (dy*w - c1 - xhat*c2)
+                                const float2 xh = __fmul2_rn(__fadd2_rn(xv[h], nmu), rs2);
+                                o[h] = __fmul2_rn(rs2, __ffma2_rn(xh, nc2, __fadd2_rn(gw, nc1)));
+                                accw[j][h] = __ffma2_rn(dv[h], xh, accw[j][h]);
+                                accb[j][h] = __fadd2_rn(accb[j][h], dv[h]);
                             } else {
-                                o[k] = rs * (gw - xv[k] * c2);
-                                accw[j][k] = fmaf(dv[k], xv[k] * rs, accw[j][k]);
-                                if constexpr (DB) accb[j][k] += dv[k];
+                                // dx = rs * (dy*w - x*c2)
+                                o[h] = __fmul2_rn(rs2, __ffma2_rn(xv[h], nc2, gw));
+                                accw[j][h] = __ffma2_rn(dv[h], __fmul2_rn(xv[h], rs2), accw[j][h]);
+                                if constexpr (DB) accb[j][h] = __fadd2_rn(accb[j][h], dv[h]);
                             }
                         }
-                        store_vec<T, VE>(dxr + int64_t(vi) * VE, o);
+                        st_v4(dxr + int64_t(vi) * VE, pack2x<T>(o));
                     }
                 }
             }
@@ -261,11 +284,16 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
         // every chunk has been consumed (and its copies have landed): the ring is scratch now
         named_barrier(kRrBarConsumers, kRrConsumers);
         float* part = reinterpret_cast<float*>(ring);
-        if (a.ws_dw)
-            rr_partial_row<TPR, VPT, VE, RPC>(accw, a.ws_dw + int64_t(blockIdx.x) * cols, part, group, t, cols);
+        float acc[VPT][VE];
+        if (a.ws_dw) {
+            unpair<VPT, VE>(accw, acc);
+            rr_partial_row<TPR, VPT, VE, RPC>(acc, a.ws_dw + int64_t(blockIdx.x) * cols, part, group, t, cols);
+        }
         if constexpr (DB) {
-            if (a.ws_db)
-                rr_partial_row<TPR, VPT, VE, RPC>(accb, a.ws_db + int64_t(blockIdx.x) * cols, part, group, t, cols);
+            if (a.ws_db) {
+                unpair<VPT, VE>(accb, acc);
+                rr_partial_row<TPR, VPT, VE, RPC>(acc, a.ws_db + int64_t(blockIdx.x) * cols, part, group, t, cols);
+            }
         }
     }
     if (bad) s_bad = 1;
