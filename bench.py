@@ -101,7 +101,7 @@ def hbm_peak():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -109,13 +109,14 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.lines: list[str] = []
+        self.first = 0  # samples before this index were taken before the load began
         self.proc = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -126,6 +127,14 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def wait_live(self, timeout_s: float = 3.0):
+        """Returns once the first sample has arrived (or after `timeout_s`) and
+        marks the samples so far as taken before the load."""
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout_s:
+            time.sleep(0.01)
+        self.first = len(self.lines)
 
     def stop(self):
         if self.proc is None:
@@ -138,7 +147,9 @@ class ClockSampler:
         self.thread.join(timeout=5)
         sms, maxs, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        # the samples taken under load; all of them if none landed in that window
+        window = self.lines[self.first:] or self.lines
+        for ln in window:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -204,13 +215,15 @@ def run_gpu(args, world, rank, local):
             if record is not None:
                 record.append((c, s, e))
 
+    # clocks are sampled from the first warm-up step to the end of the timed steps
+    clocks = ClockSampler(local)
+    clocks.start()
+    clocks.wait_live()
     for _ in range(args.warmup):
         one_step(None)
     nrm.nrm_sync_status()
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
-    clocks.start()
     barrier()
     torch.cuda.synchronize()
     recs = []
