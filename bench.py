@@ -3,6 +3,7 @@
 
 One step = every row of the hot path, forward then backward, through the C ABI,
 on the full-size synthetic workloads:
+  * LayerNorm fp32 [64, 256]     (the small case: latency-bound, a few µs per call)
   * RMSNorm   bf16 [16384, 4096] (LLaMA-style, 8 outlier columns x20)
   * LayerNorm fp16 [25216, 768]  (ViT-B tokens)
   * BatchNorm2d fp32 [256, 64, 56, 56] + residual + ReLU, training (ResNet)
@@ -20,8 +21,11 @@ outside its value, extra_rows times the channels-first LayerNorm on fp16
 dropout (p = 0.1) on fp16 [25216, 3072] (ViT-B MLP hidden activations) and the
 ViT-B LayerNorm fp16 [25216, 768] with its output kept in fp32, the same way.
 
---impl reference times the CPU oracle (plain double-precision C, one core) on a
-bounded sample of the same workloads (a quarter of the rows or channels of each).
+--impl reference times the CPU oracle (plain double-precision C) on a bounded
+sample of the same workloads (a quarter of the rows or channels of each), on all
+host cores: each thread runs the unchanged oracle on its own share of the rows
+or channels.  The GPU run's cpu_baseline reports the same on all cores and on
+one core.
 
 Multi-GPU: one process per GPU (torchrun); each rank runs the same step on its
 own GPU (independent replicas, no collective on the data path); value sums
@@ -44,7 +48,7 @@ if ROOT not in sys.path:
 
 METRIC = "fwd+bwd achieved HBM GB/s and % of GB300 peak per norm config; µs per call"
 UNIT = "GB/s"
-WORKLOAD = ("norm suite fwd+bwd: RMSNorm bf16 [16384,4096] + LayerNorm f16 [25216,768] + "
+WORKLOAD = ("norm suite fwd+bwd: LayerNorm f32 [64,256] + RMSNorm bf16 [16384,4096] + LayerNorm f16 [25216,768] + "
             "BatchNorm2d f32 [256,64,56,56]+res+ReLU train + BatchNorm2d f16 [128,512,7,7]+GELU "
             "train + BatchNorm2d f32 [256,64,56,56]+res+ReLU eval")
 FALLBACK_HBM_GBS = 6800.0
@@ -280,7 +284,7 @@ def run_gpu(args, world, rank, local):
         "extra_rows": extra_rows,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(reps=24)
+        line["cpu_baseline"] = cpu_baseline()
     return line
 
 
@@ -396,7 +400,7 @@ def oracle_sample():
     algorithmic bytes the same calls would move at the workload's dtypes."""
     from normalization_layernorm_rmsnorm_gb300 import synth
     items = []
-    for name in ("rms_bf16_16384x4096", "ln_f16_25216x768"):
+    for name in ("ln_f32_64x256", "rms_bf16_16384x4096", "ln_f16_25216x768"):
         cfg = synth.CONFIGS[name]
         rows = cfg.rows // SAMPLE_FRACTION
         inp = synth.row_inputs(cfg, rows=rows)
@@ -449,18 +453,73 @@ def oracle_step(orc, items):
                               a["running_var"], cfg.eps, training, acts[cfg.act], mask=f["mask"])
 
 
-def cpu_baseline(reps=1):
+def host_cores() -> int:
+    """Cores this process may run on (the host's hardware concurrency unless
+    an affinity mask narrows it)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_parts(items, parts):
+    """Splits each sampled workload into `parts` pieces along its rows (row
+    norms) or channels (BatchNorm), as contiguous float64 arrays: the oracle's
+    results for the pieces are its results for the whole, row by row or channel
+    by channel, and each thread runs the unchanged oracle on its own pieces."""
+    import numpy as np
+    out = [[] for _ in range(parts)]
+    for tag, cfg, a, b, desc in items:
+        row_norm = hasattr(cfg, "kind")
+        extent = a["x"].shape[0] if row_norm else a["x"].shape[1]
+        for i in range(parts):
+            lo, hi = extent * i // parts, extent * (i + 1) // parts
+            if hi <= lo:
+                continue
+            piece = {}
+            for k, v in a.items():
+                if row_norm:
+                    piece[k] = np.ascontiguousarray(v[lo:hi]) if v.ndim == 2 else v
+                else:
+                    piece[k] = np.ascontiguousarray(v[:, lo:hi, :] if v.ndim == 3 else v[lo:hi])
+            out[i].append((tag, cfg, piece, 0, desc))
+    return [p for p in out if p]
+
+
+def oracle_parallel(orc, parts):
+    """One oracle step over all pieces, one thread per piece list (the oracle
+    is a C library called through ctypes, which releases the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        for f in [ex.submit(oracle_step, orc, p) for p in parts]:
+            f.result()
+
+
+def cpu_baseline(reps_one=8, reps_all=48):
+    """The oracle on the bounded sample: on one core (`reps_one` steps), then on
+    every host core (`reps_all` steps); value = the all-cores figure."""
     import oracle
     orc = oracle.get()
     items = oracle_sample()
     total = sum(i[3] for i in items)
     t0 = time.perf_counter()
-    for _ in range(reps):
+    for _ in range(reps_one):
         oracle_step(orc, items)
-    dt = time.perf_counter() - t0
-    return {"value": round(total * reps / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "seconds": round(dt, 2),
-            "sample": "; ".join(f"{i[0]}: {i[4]}" for i in items) + " (fwd+bwd each, single-threaded C, fp64)"}
+    dt1 = time.perf_counter() - t0
+    cores = host_cores()
+    parts = oracle_parts(items, cores)
+    oracle_parallel(orc, parts)  # warm-up: page the pieces in
+    t0 = time.perf_counter()
+    for _ in range(reps_all):
+        oracle_parallel(orc, parts)
+    dtn = time.perf_counter() - t0
+    sample = "; ".join(f"{i[0]}: {i[4]}" for i in items) + " (fwd+bwd each, C, fp64)"
+    return {"value": round(total * reps_all / dtn / 1e9, 4), "unit": UNIT, "cores": len(parts),
+            "kind": "oracle", "host_cores": cores, "seconds": round(dtn, 2),
+            "threads": f"{len(parts)} threads, each running the oracle on its share of the rows or channels",
+            "single_core": {"value": round(total * reps_one / dt1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                            "seconds": round(dt1, 2)},
+            "sample": sample}
 
 
 def run_reference(args, world, rank):
@@ -470,24 +529,27 @@ def run_reference(args, world, rank):
     orc = oracle.get()
     items = oracle_sample()
     total = sum(i[3] for i in items)
+    cores = host_cores()
+    parts = oracle_parts(items, cores)
     for _ in range(args.warmup):
-        oracle_step(orc, items)
+        oracle_parallel(orc, parts)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_step(orc, items)
+        oracle_parallel(orc, parts)
         times.append(time.perf_counter() - t0)
     ms = statistics.mean(times) * 1e3
     value = total / (ms * 1e-3) / 1e9
-    sample = "; ".join(f"{i[0]}: {i[4]}" for i in items) + " (fwd+bwd each, single-threaded C, fp64)"
+    sample = ("; ".join(f"{i[0]}: {i[4]}" for i in items)
+              + f" (fwd+bwd each, C, fp64, {len(parts)} threads on {cores} host cores)")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded counter-based generator; shapes of the articles' models)",
         "config": {"workload": WORKLOAD, "sample": f"1/{SAMPLE_FRACTION} of each workload"},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": len(parts), "kind": "oracle",
+                         "host_cores": cores, "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -161,8 +161,11 @@ NRM_API nrm_status nrm_layernorm_bwd(const void *dy, const void *x, const void *
  * any stream capture.  All calls share the one array, so calls that overlap on
  * the GPU (unordered streams) race on it; calls ordered on one stream are safe.
  * Its contents need no initialisation: every call writes each partial value it
- * reads.  Arguments, results and errors are otherwise those of
- * nrm_layernorm_bwd.
+ * reads.  The looked-up address is kept for the life of the process: do not
+ * reset a device (cudaDeviceReset) or destroy its primary context while the
+ * library is loaded and this call is in use, since the kept address would then
+ * point into a released module.  Arguments, results and errors are otherwise
+ * those of nrm_layernorm_bwd.
  */
 NRM_API nrm_status nrm_layernorm_bwd_noalloc(const void *dy, const void *x, const void *w,
                                      const float *mean, const float *rstd, void *dx,

@@ -40,6 +40,10 @@ def build_calls(dev, names=None):
     def want(name):
         return names is None or name in names
 
+    # ---- LayerNorm f32 [64, 256]: the small case (latency-bound, a few µs) ----
+    cfg = synth.CONFIGS["ln_f32_64x256"]
+    if want(cfg.name):
+        calls += _ln(cfg, dev, f32)
     # ---- RMSNorm bf16 [16384, 4096] ----
     cfg = synth.CONFIGS["rms_bf16_16384x4096"]
     if want(cfg.name):
@@ -117,11 +121,13 @@ def _ln(cfg, dev, f32):
     lx, lw, lb, ldy = (inp[k].torch(dev) for k in ("x", "w", "b", "dy"))
     ly, ldx, ldw, ldb = torch.empty_like(lx), torch.empty_like(lx), torch.empty_like(lw), torch.empty_like(lb)
     lmean, lrstd = f32(cfg.rows), f32(cfg.rows)
-    lws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_BWD, cfg.rows, cfg.cols, nrm.NRM_F16) // 4)
-    calls.append(Call(cfg.name, "fwd", "row_fwd_kernel<f16,ln>",
+    code = {"f32": nrm.NRM_F32, "f16": nrm.NRM_F16, "bf16": nrm.NRM_BF16}[cfg.dtype]
+    lws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_BWD, cfg.rows, cfg.cols, code) // 4)
+    dt = cfg.dtype
+    calls.append(Call(cfg.name, "fwd", f"row_fwd_kernel<{dt},ln>",
                       lambda e=cfg.eps: nrm.nrm_layernorm_fwd(lx, lw, lb, ly, lmean, lrstd, e),
                       nbytes(lx, lw, lb, ly, lmean, lrstd), 1, [lx, lw, lb], [ly, lmean, lrstd]))
-    calls.append(Call(cfg.name, "bwd", "row_bwd_ring_kernel<f16,ln>+colsum",
+    calls.append(Call(cfg.name, "bwd", f"row_bwd_ring_kernel<{dt},ln>+colsum",
                       lambda: nrm.nrm_layernorm_bwd(ldy, lx, lw, lmean, lrstd, ldx, ldw, ldb, lws),
                       nbytes(ldy, lx, lw, lmean, lrstd, ldx, ldw, ldb), 2, [ldy], [ldx, ldw, ldb]))
 

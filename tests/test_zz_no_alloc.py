@@ -4,11 +4,12 @@ loops that must never enter cudaMalloc after start-up, C callers holding only
 device pointers).  It keeps the dw/db partial rows in the library's own static
 device array instead of a caller workspace.
 
-Checked through the C ABI against nrm_layernorm_bwd (the entry point with a
-workspace), with the parity tolerances, on two calls in a row (the second call
-finds the previous call's partial sums still in the shared array).  This file
-sorts last so that a run stopping at the first failure has already run every
-other test; it also passes on its own in a fresh process."""
+Checked through the C ABI against the CPU oracle and against nrm_layernorm_bwd
+(the entry point with a workspace), with the parity tolerances, on two calls in
+a row (the second call finds the previous call's partial sums still in the
+shared array).  This file sorts last so that a run stopping at the first
+failure has already run every other test; it also passes on its own in a fresh
+process."""
 import pytest
 import torch
 
@@ -34,7 +35,7 @@ def _inputs(rows, cols, dtype, seed):
     mean = torch.empty(rows, device="cuda")
     rstd = torch.empty(rows, device="cuda")
     nrm.nrm_layernorm_fwd(x, w, b, y, mean, rstd, cfg.eps)
-    return x, w, dy, mean, rstd
+    return x, w, dy, mean, rstd, inp, cfg.eps
 
 
 @pytest.mark.parametrize("dtype,rows,cols", [
@@ -44,8 +45,9 @@ def _inputs(rows, cols, dtype, seed):
     ("bf16", 64, 12000),     # wide-row kernel
     ("f16", 37, 1025),       # unaligned scalar path
 ])
-def test_noalloc_matches_workspace_entry_point_twice(dtype, rows, cols):
-    x, w, dy, mean, rstd = _inputs(rows, cols, dtype, seed=rows + cols)
+def test_noalloc_matches_oracle_and_workspace_entry_point_twice(orc, dtype, rows, cols):
+    x, w, dy, mean, rstd, inp, eps = _inputs(rows, cols, dtype, seed=rows + cols)
+    dx_o, dw_o, db_o = orc.layernorm_bwd(inp["dy"].f64(), inp["x"].f64(), inp["w"].f64(), eps)
     dx_ref = torch.empty_like(x)
     dw_ref = torch.empty_like(w)
     db_ref = torch.empty_like(w)
@@ -60,6 +62,9 @@ def test_noalloc_matches_workspace_entry_point_twice(dtype, rows, cols):
         nrm.nrm_layernorm_bwd_noalloc(dy, x, w, mean, rstd, dx, dw, db)
         nrm.nrm_sync_status()
         tag = f"noalloc call {call + 1} {dtype} [{rows},{cols}]"
+        assert_close(host(dx), dx_o, tol, tag + " dx vs oracle")
+        assert_close(host(dw), dw_o, tol, tag + " dw vs oracle")
+        assert_close(host(db), db_o, tol, tag + " db vs oracle")
         assert_close(host(dx), host(dx_ref), tol, tag + " dx")
         assert_close(host(dw), host(dw_ref), tol, tag + " dw")
         assert_close(host(db), host(db_ref), tol, tag + " db")
