@@ -35,7 +35,8 @@
  *           NRM_ERR_WORKSPACE when workspace_bytes is too small;
  *           NRM_ERR_CUDA when a CUDA runtime call or launch fails;
  *           NRM_ERR_TIMEOUT (from nrm_sync_status) when a kernel's bounded wait
- *           on its own asynchronous copies gave up.  nrm_last_error_message()
+ *           gave up: on its own asynchronous copies, on another warp of its
+ *           CTA, or on the other CTAs of a BatchNorm channel.  nrm_last_error_message()
  *           gives a human-readable reason for the last failure on this thread.
  * Limits.   rows, n*c*l < 2^40; cols < 2^31; a BatchNorm channel holds fewer
  *           than 2^31 elements (n*l).
@@ -420,6 +421,25 @@ NRM_API const char *nrm_last_error_message(void);
 
 /* Library version, major*10000 + minor*100 + patch. */
 NRM_API int nrm_version(void);
+
+/*
+ * nrm_test_expire_peer_waits -- a test hook for the failure path of the
+ * BatchNorm kernels whose channels span several CTAs.  The articles have no
+ * counterpart: it exercises this library's own failure detection.
+ * Those kernels wait, bounded, for every CTA of a channel to publish its
+ * partial sums; a CTA that gives up records NRM_ERR_TIMEOUT (reported by the
+ * next nrm_sync_status), finishes its own part of the call with the partial
+ * sums it found and waits for its own copies before it exits.  This call arms,
+ * for the next nrm_batchnorm_fwd or nrm_batchnorm_bwd in training mode on the
+ * calling thread that runs such a kernel (16-byte aligned tensors, or the
+ * scalar path, with a channel cut into more than one slice), a wait for one
+ * CTA more than the launch has and a limit of `limit_ns` nanoseconds instead
+ * of 2 s: every waiting CTA then gives up after `limit_ns`, and that call's
+ * outputs are undefined.  Calls that do not wait for other CTAs leave it armed.
+ * limit_ns must be in [1, 10^9] (else NRM_ERR_INVALID_ARG).  No GPU fault is
+ * involved: the kernel ends normally and the device stays usable.
+ */
+NRM_API nrm_status nrm_test_expire_peer_waits(uint64_t limit_ns);
 
 #ifdef __cplusplus
 }

@@ -15,5 +15,5 @@ from ._binding import (  # noqa: F401
     NRM_F32, NRM_OK, NRM_OP_LAYERNORM_BWD, NRM_OP_LAYERNORM_CF_BWD, NRM_OP_RMSNORM_BWD, NrmError, batchnorm_workspace, load,
     nrm_act_dropout_bwd, nrm_act_dropout_fwd, nrm_act_mask_words, nrm_batchnorm_bwd, nrm_batchnorm_fwd, nrm_batchnorm_workspace_bytes, nrm_last_error_message,
     nrm_layernorm_bwd, nrm_layernorm_bwd_ex, nrm_layernorm_bwd_noalloc, nrm_layernorm_fwd_ex, nrm_rmsnorm_bwd_ex, nrm_rmsnorm_fwd_ex, nrm_layernorm_cf_bwd, nrm_layernorm_cf_fwd, nrm_layernorm_fwd, nrm_rmsnorm_bwd, nrm_rmsnorm_fwd, nrm_status_str,
-    nrm_sync_status, nrm_version, nrm_workspace_bytes,
+    nrm_sync_status, nrm_test_expire_peer_waits, nrm_version, nrm_workspace_bytes,
 )

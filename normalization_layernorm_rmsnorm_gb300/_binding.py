@@ -34,7 +34,7 @@ EXPORTS = ("nrm_layernorm_fwd", "nrm_layernorm_bwd", "nrm_layernorm_bwd_noalloc"
            "nrm_workspace_bytes",
            "nrm_batchnorm_workspace_bytes",
            "nrm_act_mask_words", "nrm_sync_status", "nrm_status_str",
-           "nrm_last_error_message", "nrm_version")
+           "nrm_last_error_message", "nrm_version", "nrm_test_expire_peer_waits")
 
 
 class NrmError(RuntimeError):
@@ -86,6 +86,7 @@ def load(path: str | None = None):
         "nrm_status_str": [_I],
         "nrm_last_error_message": [],
         "nrm_version": [],
+        "nrm_test_expire_peer_waits": [ctypes.c_uint64],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -325,3 +326,11 @@ def nrm_version() -> int:
 
 def nrm_last_error_message() -> str:
     return load().nrm_last_error_message().decode()
+
+
+def nrm_test_expire_peer_waits(limit_ns: int):
+    """Test hook: the next training BatchNorm call on this thread whose kernel
+    waits for the other CTAs of a channel waits for one CTA too many and gives
+    up after limit_ns (its outputs are then undefined; nrm_sync_status reports
+    NRM_ERR_TIMEOUT)."""
+    _check(load().nrm_test_expire_peer_waits(int(limit_ns)), "nrm_test_expire_peer_waits")

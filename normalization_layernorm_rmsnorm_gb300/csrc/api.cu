@@ -36,6 +36,15 @@ constexpr int64_t kMaxElems = int64_t(1) << 40;
 
 void clear_error() { t_msg[0] = 0; }
 
+thread_local uint64_t t_peer_test_ns = 0;
+
+bool take_peer_wait_test(uint64_t* ns) {
+    if (t_peer_test_ns == 0) return false;
+    *ns = t_peer_test_ns;
+    t_peer_test_ns = 0;
+    return true;
+}
+
 nrm_status fail(nrm_status s, const char* fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -686,6 +695,14 @@ const char* nrm_status_str(nrm_status status) {
 }
 
 const char* nrm_last_error_message(void) { return t_msg; }
+
+nrm_status nrm_test_expire_peer_waits(uint64_t limit_ns) {
+    t_msg[0] = 0;
+    if (limit_ns == 0 || limit_ns > nrm::kPeerTestMaxNs)
+        return fail(NRM_ERR_INVALID_ARG, "limit_ns must be in [1, %llu]", (unsigned long long)nrm::kPeerTestMaxNs);
+    nrm::t_peer_test_ns = limit_ns;
+    return NRM_OK;
+}
 
 int nrm_version(void) { return 100; }
 

@@ -66,6 +66,8 @@ struct BnGeom {
     float inv_m1;          // 1 / (n*l - 1)
     uint32_t* counters;    // [c] arrivals per channel, zero at launch (S > 1)
     void* partials;        // [c][S]: float4 (n, mean, m2, 0) forward; double2 backward
+    uint32_t peer_extra;   // arrivals awaited beyond S (0; 1 under the failure-path test hook)
+    uint64_t peer_wait_ns; // how long a CTA waits for a channel's other slices before giving up
 };
 
 // Whether the backward recomputes z = x*scale + shift (+ residual) to take the
@@ -186,14 +188,21 @@ struct ShiftedSums {
     }
 };
 
-// Bounded wait until `count` CTAs have signalled `counter`; false on timeout.
-__device__ __forceinline__ bool wait_count(const uint32_t* counter, uint32_t count) {
-    if (ld_acquire_u32(counter) >= count) return true;
+// Bounded wait until a channel's S slices (plus g.peer_extra) have signalled
+// `counter`.  Gives up after g.peer_wait_ns and sets `lost`; once `lost` is
+// set, later waits of the thread return at once (the peers' partial sums are
+// then unusable, and the CTA only finishes its own work).
+__device__ __forceinline__ void wait_peers(const BnGeom& g, const uint32_t* counter, bool& lost) {
+    const uint32_t count = uint32_t(g.S) + g.peer_extra;
+    if (lost || ld_acquire_u32(counter) >= count) return;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
         __nanosleep(64);
-        if (ld_acquire_u32(counter) >= count) return true;
-        if (global_timer_ns() - t0 > kBnWaitLimitNs) return false;
+        if (ld_acquire_u32(counter) >= count) return;
+        if (global_timer_ns() - t0 > g.peer_wait_ns) {
+            lost = true;
+            return;
+        }
     }
 }
 
@@ -314,7 +323,7 @@ bn_fwd_kernel(const BnArgs a, const BnGeom g) {
                 Moments tot = keep[r & 1];
                 if (g.S > 1) {
                     const float4* part = reinterpret_cast<const float4*>(g.partials) + ch * g.S;
-                    if (!wait_count(g.counters + ch, uint32_t(g.S))) bad = true;
+                    wait_peers(g, g.counters + ch, bad);
                     Moments lm{0.f, 0.f, 0.f};
                     for (int i = lane; i < g.S; i += 32) {
                         const float4 pv = ld_cg_f4(part + i);
@@ -1038,7 +1047,7 @@ bn_bwd_kernel(const BnArgs a, const BnGeom g) {
             double t1 = keep[r & 1].x, t2 = keep[r & 1].y;
             if (g.S > 1) {
                 const double2* part = reinterpret_cast<const double2*>(g.partials) + ch * g.S;
-                if (!wait_count(g.counters + ch, uint32_t(g.S))) bad = true;
+                wait_peers(g, g.counters + ch, bad);
                 double l1 = 0.0, l2 = 0.0;
                 for (int i = lane; i < g.S; i += 32) {
                     const double2 pv = ld_cg_d2(part + i);
@@ -1488,6 +1497,7 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
 
 }  // namespace nrm
 
+#include "batchnorm_train.cuh"
 #include "batchnorm_group.cuh"
 
 namespace nrm {
@@ -1498,11 +1508,14 @@ namespace nrm {
 
 // Upper bound of slices per channel (sizes the workspace).
 inline int bn_max_slices(const DevInfo& d) { return 4 * d.sms; }
+// Bytes of one (channel, slice) partial in the workspace: float4 (n, mean,
+// M2, -) forward, double2 (sum dz, sum dz*(x - mean)) backward.
+constexpr size_t kBnPartialBytes = 16;
 
 // Workspace bytes: per-channel counters, then per-(channel, slice) partials.
 inline size_t bn_workspace_bytes(const DevInfo& d, int64_t c) {
     const size_t counters = (size_t(c) * 4 + 255) / 256 * 256;
-    return counters + size_t(c) * size_t(bn_max_slices(d)) * 16;
+    return counters + size_t(c) * size_t(bn_max_slices(d)) * kBnPartialBytes;
 }
 
 struct BnPlan {
@@ -1525,6 +1538,8 @@ inline void bn_geometry(BnGeom& g, const BnArgs& a, int ve) {
     g.inv_m1 = m > 1 ? float(1.0 / (m - 1.0)) : 0.f;
     g.counters = nullptr;
     g.partials = nullptr;
+    g.peer_extra = 0;
+    g.peer_wait_ns = kBnWaitLimitNs;
 }
 
 // L2 held by the kept data of the rounds in flight (the first pass of round
@@ -1533,6 +1548,15 @@ inline void bn_geometry(BnGeom& g, const BnArgs& a, int ve) {
 // a larger share.
 constexpr double kBnL2Budget = 48.0 * 1024 * 1024;
 constexpr double kBnL2BudgetRingFwd = 64.0 * 1024 * 1024;
+// The training kernels keep up to lag + 1 rounds of first-pass data in L2.
+#ifndef NRM_BN_TRAIN_L2_MB_FWD
+#define NRM_BN_TRAIN_L2_MB_FWD 128
+#endif
+#ifndef NRM_BN_TRAIN_L2_MB_BWD
+#define NRM_BN_TRAIN_L2_MB_BWD 96
+#endif
+constexpr double kBnL2BudgetTrainFwd = double(NRM_BN_TRAIN_L2_MB_FWD) * 1024 * 1024;
+constexpr double kBnL2BudgetTrainBwd = double(NRM_BN_TRAIN_L2_MB_BWD) * 1024 * 1024;
 #ifndef NRM_BN_ROUND_OVERHEAD
 #define NRM_BN_ROUND_OVERHEAD 32
 #endif
@@ -1642,10 +1666,19 @@ inline nrm_status bn_plan_ring(BnPlan& pl, const BnArgs& a, const void* fn, size
     return NRM_OK;
 }
 
+// `peer_waits`: the kernel waits for a channel's other slices (training with
+// S > 1); only such a launch takes the failure-path test hook.
 inline nrm_status launch_bn(const void* fn, const BnArgs& a, BnPlan& pl, void* ws, size_t ws_bytes,
-                            cudaStream_t s, int threads = kBnThreads) {
+                            cudaStream_t s, int threads, bool peer_waits) {
     if (a.c == 0) return NRM_OK;
     const DevInfo* d = dev_info();
+    pl.g.peer_extra = 0;
+    pl.g.peer_wait_ns = kBnWaitLimitNs;
+    uint64_t test_ns = 0;
+    if (peer_waits && pl.g.S > 1 && take_peer_wait_test(&test_ns)) {
+        pl.g.peer_extra = 1;  // one arrival more than the grid makes: every such wait runs out
+        pl.g.peer_wait_ns = test_ns;
+    }
     if (pl.g.S > 1) {
         if (!ws || ws_bytes < bn_workspace_bytes(*d, a.c))
             return fail(NRM_ERR_WORKSPACE, "batchnorm needs a workspace of %zu bytes for this shape",
@@ -1678,24 +1711,34 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
         nrm_status st = NRM_OK;
         if (bn_fwd_group<T>(a, training, s, st)) return st;
     }
-    if (vec && a.c > 0 && a.n * a.l > 0) {
+    if (vec && a.c > 0 && a.n * a.l > 0 && training) {
         const void* fn = with_act(a.act, [&](auto act) {
-            return training ? (const void*)&bn_fwd_ring_kernel<T, true, decltype(act)::value>
-                            : (const void*)&bn_fwd_ring_kernel<T, false, decltype(act)::value>;
+            return (const void*)&bn_fwd_train_kernel<T, decltype(act)::value>;
         });
         BnPlan pl;
         bn_geometry(pl.g, a, kVec<T>);
-        nrm_status st = bn_plan_ring(pl, a, fn, size_t(kRingSlotsFwd) * kSlotBytes, training ? 1 : 0, 2,
+        nrm_status st = bn_plan_ring(pl, a, fn, size_t(kTfSlotsS + kTfSlotsA) * kSlotBytes, 1, kTfLag + 1,
+                                      kTrThreads, kBnL2BudgetTrainFwd);
+        if (st != NRM_OK) return st;
+        return launch_bn(fn, a, pl, ws, ws_bytes, s, kTrThreads, true);
+    }
+    if (vec && a.c > 0 && a.n * a.l > 0) {
+        const void* fn = with_act(a.act, [&](auto act) {
+            return (const void*)&bn_fwd_ring_kernel<T, false, decltype(act)::value>;
+        });
+        BnPlan pl;
+        bn_geometry(pl.g, a, kVec<T>);
+        nrm_status st = bn_plan_ring(pl, a, fn, size_t(kRingSlotsFwd) * kSlotBytes, 0, 2,
                                       kRingThreads, kBnL2BudgetRingFwd);
         if (st != NRM_OK) return st;
-        return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads);
+        return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads, false);
     }
     // unaligned tensors, channel counts the group path cannot tile, empty channels
     const void* fn = training ? (const void*)&bn_fwd_kernel<T, 1, true> : (const void*)&bn_fwd_kernel<T, 1, false>;
     BnPlan pl;
     nrm_status st = bn_plan(pl, a, 1, sizeof(T), fn);
     if (st != NRM_OK) return st;
-    return launch_bn(fn, a, pl, ws, ws_bytes, s);
+    return launch_bn(fn, a, pl, ws, ws_bytes, s, kBnThreads, training);
 }
 
 template <typename T>
@@ -1704,27 +1747,35 @@ nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
         nrm_status st = NRM_OK;
         if (bn_bwd_group<T>(a, training, s, st)) return st;
     }
-    if (vec && a.c > 0 && a.n * a.l > 0) {
+    if (vec && a.c > 0 && a.n * a.l > 0 && training) {
+        const bool need_z = bn_need_z(a.act, a.mask_in);
+        const int nt = (need_z && a.res) ? 3 : 2;
         const void* fn = with_act(a.act, [&](auto act) {
-            return training ? (const void*)&bn_bwd_ring_kernel<T, true, decltype(act)::value>
-                            : (const void*)&bn_bwd_ring_kernel<T, false, decltype(act)::value>;
+            return (const void*)&bn_bwd_train_kernel<T, decltype(act)::value>;
         });
         BnPlan pl;
         bn_geometry(pl.g, a, kVec<T>);
-        const bool need_z = bn_need_z(a.act, a.mask_in);
-        const int nt = (need_z && a.res) ? 3 : 2;
-        const int slots = training ? kRingSlotsBwdHbm + kRingSlotsBwdL2 : kRingSlotsBwd;
-        const int threads = training ? kRingThreadsBwdTrain : kRingThreads;
-        const size_t smem = size_t(slots) * (kSlotBytes + kSlotMaskWords * sizeof(uint32_t));
-        nrm_status st = bn_plan_ring(pl, a, fn, smem, training ? nt : 0, 2, threads, kBnL2Budget);
+        const size_t smem = size_t(kTbSlots1 + kTbSlots2) * (kSlotBytes + kSlotMaskWords * sizeof(uint32_t));
+        nrm_status st = bn_plan_ring(pl, a, fn, smem, nt, kTbLag + 1, kTrThreads, kBnL2BudgetTrainBwd);
         if (st != NRM_OK) return st;
-        return launch_bn(fn, a, pl, ws, ws_bytes, s, threads);
+        return launch_bn(fn, a, pl, ws, ws_bytes, s, kTrThreads, true);
+    }
+    if (vec && a.c > 0 && a.n * a.l > 0) {
+        const void* fn = with_act(a.act, [&](auto act) {
+            return (const void*)&bn_bwd_ring_kernel<T, false, decltype(act)::value>;
+        });
+        BnPlan pl;
+        bn_geometry(pl.g, a, kVec<T>);
+        const size_t smem = size_t(kRingSlotsBwd) * (kSlotBytes + kSlotMaskWords * sizeof(uint32_t));
+        nrm_status st = bn_plan_ring(pl, a, fn, smem, 0, 2, kRingThreads, kBnL2Budget);
+        if (st != NRM_OK) return st;
+        return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads, false);
     }
     const void* fn = training ? (const void*)&bn_bwd_kernel<T, 1, true> : (const void*)&bn_bwd_kernel<T, 1, false>;
     BnPlan pl;
     nrm_status st = bn_plan(pl, a, 1, 2 * sizeof(T), fn);
     if (st != NRM_OK) return st;
-    return launch_bn(fn, a, pl, ws, ws_bytes, s);
+    return launch_bn(fn, a, pl, ws, ws_bytes, s, kBnThreads, training);
 }
 
 }  // namespace nrm

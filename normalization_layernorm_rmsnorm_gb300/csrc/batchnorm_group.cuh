@@ -211,7 +211,11 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
             }
         }
     }
-    if (bad) atomicOr(a.err, kErrTimeoutStage);
+    if (bad) {
+        // the tile's copy may still be landing: wait once more (bounded) before exit
+        mbar_wait_bounded(&bar, 0, kBnWaitLimitNs);
+        atomicOr(a.err, kErrTimeoutStage);
+    }
 }
 
 template <typename T, bool TRAIN, int ACT>
@@ -362,7 +366,11 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
         if (dres) store_vec_pol<T, VE>(dres + off, dzv, pol);
         store_vec_pol<T, VE>(dx + off, ov, pol);
     }
-    if (bad) atomicOr(a.err, kErrTimeoutStage);
+    if (bad) {
+        // the tile's copy may still be landing: wait once more (bounded) before exit
+        mbar_wait_bounded(&bar, 0, kBnWaitLimitNs);
+        atomicOr(a.err, kErrTimeoutStage);
+    }
 }
 
 // ---------------------------------------------------------------------------

@@ -23,8 +23,8 @@
 // concurrently, each fed by its own producer warp and ring of shared-memory
 // slots (bulk copies, mbarrier completion), so that HBM keeps streaming the
 // next round while the previous one is finished from L2.  Team 1 starts round
-// q only after team 2 has finished round q - kTrLag, which bounds the L2 held
-// by kept data to about kTrLag + 1 rounds.  A bookkeeper warp merges team 1's
+// q only after team 2 has finished round q - lag (kTfLag, kTbLag), which bounds
+// the L2 held by kept data to about lag + 1 rounds.  A bookkeeper warp merges team 1's
 // per-warp sums, publishes the CTA's partial to the workspace, merges a
 // channel's S partials in slice order once its counter is complete and hands
 // team 2 the channel's coefficients.
@@ -41,11 +41,16 @@
 namespace nrm {
 
 constexpr int kTrThreads = 19 * 32;
-#ifndef NRM_BN_TRAIN_LAG
-#define NRM_BN_TRAIN_LAG 2
+// Team 1 runs at most this many rounds ahead of team 2 (forward, backward).
+#ifndef NRM_BN_TRAIN_LAG_FWD
+#define NRM_BN_TRAIN_LAG_FWD 3
 #endif
-constexpr int kTrLag = NRM_BN_TRAIN_LAG;  // team 1 runs at most this many rounds ahead of team 2
-static_assert(kTrLag >= 1 && kTrLag <= 3, "the round handoffs are four deep");
+#ifndef NRM_BN_TRAIN_LAG_BWD
+#define NRM_BN_TRAIN_LAG_BWD 3
+#endif
+constexpr int kTfLag = NRM_BN_TRAIN_LAG_FWD;
+constexpr int kTbLag = NRM_BN_TRAIN_LAG_BWD;
+static_assert(kTfLag >= 1 && kTfLag <= 3 && kTbLag >= 1 && kTbLag <= 3, "the round handoffs are four deep");
 
 // forward roles: warps [0, 4) statistics, [4, 16) apply, then two producers and the bookkeeper
 constexpr int kTfStatsWarps = 4;
@@ -202,7 +207,7 @@ struct TfShared {
 };
 
 // Bookkeeper of the training forward (one warp).
-__device__ void tf_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& rd, int nr, TfShared& sh, int lane) {
+static __device__ void tf_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& rd, int nr, TfShared& sh, int lane) {
     volatile int* abort = &sh.abort;
     int q_pub = 0, r_mrg = 0;
     int pre_r = -1;
@@ -343,7 +348,7 @@ bn_fwd_train_kernel(const BnArgs a, const BnGeom g) {
         // ---------------- statistics of round q: x from HBM, kept in L2 ----------------
         const uint32_t span = chunk_span(1);
         for (int q = 0; q < nr; ++q) {
-            const int qd = q - kTrLag;
+            const int qd = q - kTfLag;
             if (qd >= 0 && !tr_wait(&sh.apply_done[qd & 3], uint32_t(qd >> 2) & 1u, peer_limit, abort)) break;
             int64_t ch;
             int s;
@@ -478,7 +483,7 @@ struct TbShared {
 };
 
 // Bookkeeper of the training backward (one warp).
-__device__ void tb_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& rd, int nr, TbShared& sh, int lane) {
+static __device__ void tb_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& rd, int nr, TbShared& sh, int lane) {
     volatile int* abort = &sh.abort;
     int q_par = 0, q_pub = 0, r_mrg = 0;
     bool lost = false, peer_wait = false;
@@ -648,7 +653,7 @@ bn_bwd_train_kernel(const BnArgs a, const BnGeom g) {
         // ---------------- pass 1 of round q: dz, dres, the two channel sums ----------------
         const uint64_t pol_stream = l2_evict_first();
         for (int q = 0; q < nr; ++q) {
-            const int qd = q - kTrLag;
+            const int qd = q - kTbLag;
             if (qd >= 0 && !tr_wait(&sh.p2_done[qd & 3], uint32_t(qd >> 2) & 1u, peer_limit, abort)) break;
             if (!tr_wait(&sh.par_ready[q & 3], uint32_t(q >> 2) & 1u, kBnWaitLimitNs, abort)) break;
             const float4 pr = sh.par[q & 3];

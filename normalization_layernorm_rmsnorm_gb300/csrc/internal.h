@@ -27,6 +27,13 @@ nrm_status fail(nrm_status s, const char* fmt, ...);
 // Maps a CUDA error to NRM_ERR_CUDA with its message (NRM_OK for cudaSuccess).
 nrm_status cuda_status(cudaError_t e, const char* what);
 
+// Failure-path test hook (nrm_test_expire_peer_waits): the wait limit armed on
+// this thread for the next BatchNorm launch that waits for other CTAs, if any;
+// taking it disarms it.
+constexpr uint64_t kPeerTestMaxNs = 1000000000ull;  // 1 s
+extern thread_local uint64_t t_peer_test_ns;
+bool take_peer_wait_test(uint64_t* ns);
+
 // Resident CTAs per SM of kernel `fn` (cached per device and kernel).
 int cached_occupancy(const void* fn, int block, size_t smem);
 // Opts `fn` into `dyn_smem` bytes of dynamic shared memory and, if asked, into

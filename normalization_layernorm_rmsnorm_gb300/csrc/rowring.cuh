@@ -35,7 +35,9 @@ struct RrGeom {
 };
 
 // Producer (whole warp): the CTA's chunks of dy and x (and the rows' rstd,
-// mean) into the ring, in order.
+// mean) into the ring, in order.  If a wait for a free slot gives up, it
+// issues nothing more; either way it then waits (bounded) until the last copy
+// issued into each slot has landed, so that none is in flight at exit.
 template <typename T, bool LN>
 __device__ void rr_produce(const RowArgs& a, const RrGeom& g, unsigned char* ring, uint64_t* full,
                            uint64_t* empty, int lane, bool& bad) {
@@ -45,7 +47,10 @@ __device__ void rr_produce(const RowArgs& a, const RrGeom& g, unsigned char* rin
     for (int64_t c = blockIdx.x; c < g.chunks; c += gridDim.x, ++q) {
         const int slot = q % g.slots;
         const uint32_t use = uint32_t(q / g.slots);
-        if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1u, kRowWaitLimitNs)) bad = true;
+        if (use > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(&empty[slot], (use - 1) & 1u, kRowWaitLimitNs))) {
+            bad = true;
+            break;
+        }
         const int64_t r0 = c * g.R;
         const int ra = int(a.rows - r0 < g.R ? a.rows - r0 : g.R);
         unsigned char* base = ring + size_t(slot) * g.slot_bytes;
@@ -62,6 +67,10 @@ __device__ void rr_produce(const RowArgs& a, const RrGeom& g, unsigned char* rin
             if (LN) cp_async_4(st + g.R + i, a.mean_in + r0 + i);
         }
         cp_async_mbar_arrive_noinc(&full[slot]);
+    }
+    for (int s = 0; s < g.slots && s < q; ++s) {
+        const int last = s + ((q - 1 - s) / g.slots) * g.slots;  // last chunk index that used slot s
+        if (!mbar_wait_bounded(&full[s], uint32_t(last / g.slots) & 1u, kRowWaitLimitNs)) bad = true;
     }
 }
 

@@ -148,12 +148,12 @@ def _bn_res_relu(cfg, dev, f32):
     bsm, bsr, bdw, bdb = f32(c), f32(c), f32(c), f32(c)
     bmask = torch.empty(nrm.nrm_act_mask_words(n, c, l), dtype=torch.int32, device=dev)
     bws = nrm.batchnorm_workspace(bx)
-    calls.append(Call(cfg.name, "fwd", "bn_fwd_ring_kernel<f32,train>",
+    calls.append(Call(cfg.name, "fwd", "bn_fwd_train_kernel<f32,relu>",
                       lambda: nrm.nrm_batchnorm_fwd(bx, bres, bw, bb, by, brm, brv, bsm, bsr, bmask,
                                                     cfg.eps, cfg.momentum, True, "relu", bws),
                       nbytes(bx, bres, by, bmask, bw, bb, bsm, bsr) + 2 * nbytes(brm, brv), 1,
                       [bx, bres, bw, bb, brm, brv], [by, bmask, bsm, bsr, brm, brv]))
-    calls.append(Call(cfg.name, "bwd", "bn_bwd_ring_kernel<f32,train>",
+    calls.append(Call(cfg.name, "bwd", "bn_bwd_train_kernel<f32,relu>",
                       lambda: nrm.nrm_batchnorm_bwd(bdy, bx, bres, bw, bb, bsm, bsr, bmask, bdx, bdres,
                                                     bdw, bdb, True, "relu", bws),
                       nbytes(bdy, bx, bmask, bw, bb, bsm, bsr, bdx, bdres, bdw, bdb), 1,
