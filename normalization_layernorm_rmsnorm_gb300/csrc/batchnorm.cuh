@@ -13,21 +13,21 @@
 // of the math-helper article ("如何用attorch.math快速开发自定义GPU算子：面向进阶
 // 开发者的算子融合实战指南", section "实战二 Welford EMA 组合手写 BatchNorm 融合统计").
 //
-// GB300 design (three kernel families, chosen per call):
-//   * Ring kernels (16-byte vectors): a persistent cooperative grid, one CTA
-//     per SM.  A channel is cut into S slices, one per CTA; the grid holds a
-//     whole number k of channels, so the S slices of a channel run in the same
-//     round on different CTAs.  Inside a CTA, warps specialise: a producer
-//     warp streams the passes through a ring of shared-memory slots with bulk
-//     copies, 16 consumer warps compute, and a bookkeeper warp publishes the
-//     CTA's partial sums to the caller's workspace (release counter per
-//     channel), merges the channel's S partials in one fixed order once they
-//     have all arrived (acquire, bounded by 2 s) and hands the consumers the
-//     channel's coefficients.  The statistics pass of round r+1 runs ahead of
-//     the apply pass of round r; every CTA publishes round r+1 before it needs
-//     round r, so the waits cannot form a cycle.  L2 holds x (dy and x in the
-//     backward) between the two passes of a round: loads carry evict-last on
-//     the first pass and evict-first on the second.
+// GB300 design (kernel families, chosen per call):
+//   * Training, 16-byte vectors (batchnorm_train.cuh): a persistent
+//     cooperative grid, one CTA per SM.  A channel is cut into S slices, one
+//     per CTA; the grid holds a whole number k of channels, so the S slices of
+//     a channel run in the same round on different CTAs.  Inside a CTA one
+//     team of warps makes the first pass of round q (statistics, or the
+//     gradient sums; data from HBM, kept in L2) while another makes the
+//     second pass of an earlier round (apply, or dx; data re-read from L2),
+//     each team fed by its own producer warp and ring of shared-memory slots;
+//     a bookkeeper warp publishes the CTA's partial sums (release counter per
+//     channel), merges a channel's S partials in one fixed order once they
+//     have all arrived and hands the second team the coefficients.
+//   * Eval, 16-byte vectors (bn_fwd_eval_kernel / bn_bwd_eval_kernel below):
+//     the same rings with one pass per round, coefficients from the running
+//     statistics.
 //   * Channel-group kernels (batchnorm_group.cuh): short segments, staged
 //     whole in shared memory by a thread-block cluster per channel group.
 //   * Scalar kernels (bn_fwd_kernel / bn_bwd_kernel with VE = 1): tensors not
@@ -406,34 +406,19 @@ bn_fwd_kernel(const BnArgs a, const BnGeom g) {
 }
 
 // ---------------------------------------------------------------------------
-// 16-byte vectors: warp-specialised ring kernels
+// 16-byte vectors: rings of shared-memory slots fed by bulk copies
 // ---------------------------------------------------------------------------
-// Three roles per CTA.  The producer warp streams the CTA's passes in chunks
-// through a ring of 32 KB shared-memory slots (the bulk copy engine moves the
-// tensors, the warp's lanes move ReLU-mask words with 4-byte async copies); a
-// chunk of a pass over nt tensors holds 64/nt blocks of each.  16 consumer
-// warps compute from the slots and release them.  The bookkeeper warp does
-// everything that waits on memory latency or on other CTAs -- per-round
-// channel parameters, publishing the CTA's partial sums, merging a channel's
-// slices -- and trades results with the consumers through mbarrier
-// handoffs in shared memory, so the consumers never stop for it unless the
-// channel itself is late.  Every handoff is a ready/free barrier pair, every
-// wait is bounded.
-constexpr int kRingConsumerWarps = 16;
-constexpr int kProducerWarp = kRingConsumerWarps;
-constexpr int kBookkeeperWarp = kRingConsumerWarps + 1;
-constexpr int kRingThreads = (kRingConsumerWarps + 2) * 32;
+// A producer warp streams a CTA's passes in chunks through a ring of 32 KB
+// shared-memory slots (the bulk copy engine moves the tensors, the warp's
+// lanes move ReLU-mask words with 4-byte async copies); a chunk of a pass over
+// nt tensors holds 64/nt blocks of each.  Consumer warps compute from the
+// slots and release them.  Every wait is bounded: a wait that runs out sets
+// the CTA's abort word, which ends every other wait of the CTA at once; the
+// producers then stop issuing copies and wait, bounded, until each copy they
+// issued has landed, so none is in flight when the CTA exits.
 constexpr int kSlotBlocks = 64;                    // 512-byte blocks per slot
 constexpr int kSlotBytes = kSlotBlocks * 512;
 constexpr int kSlotMaskWords = 32 * 8;             // mask words of a chunk of >= 2 tensors
-constexpr int kRingSlotsFwd = 7;
-constexpr int kRingSlotsBwd = 6;
-// training backward: pass 1 (HBM) and pass 2 (L2 re-reads) on separate rings
-// with one producer each, so pass 2 never holds up the HBM stream
-constexpr int kRingSlotsBwdHbm = 4;
-constexpr int kRingSlotsBwdL2 = 2;
-constexpr int kProducer2Warp = kRingConsumerWarps + 2;
-constexpr int kRingThreadsBwdTrain = kRingThreads + 32;
 
 __host__ __device__ constexpr uint32_t chunk_span(int nt) { return uint32_t(kSlotBlocks / nt); }
 
@@ -472,11 +457,35 @@ struct Ring {
     __device__ uint32_t use() const { return uint32_t(seq / SLOTS); }
 };
 
-// Producer (whole warp): one chunk, blocks [cb, ce) of round r's slice, of
-// pass `ps`.
+// Waits for phase `parity` of `bar` for at most `limit_ns`; gives up at once
+// when another thread of the CTA has given up (*abort != 0), and sets *abort
+// when this wait runs out.  Called by every lane of a warp; the result is
+// warp-uniform.
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, volatile int* abort) {
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+            if (mbar_try_wait(bar, parity)) {
+                ok = true;
+                break;
+            }
+            if (*abort) break;
+            if (global_timer_ns() - t0 > limit_ns) {
+                *abort = 1;
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Producer (whole warp): one chunk of pass `ps`, blocks [cb, ce) of round r's
+// slice, into the next slot of `rg` once its consumers have released it.
+// False (nothing issued) when the wait for the slot gave up.
 template <typename T, int VE, int SLOTS>
-__device__ void ring_produce_chunk(Ring<SLOTS>& rg, const Rounds& rd, int r, const RingPass<T>& ps, uint32_t cb,
-                                   uint32_t ce, int lane, bool& bad) {
+__device__ bool ring_produce_chunk(Ring<SLOTS>& rg, const Rounds& rd, int r, const RingPass<T>& ps, uint32_t cb,
+                                   uint32_t ce, int lane, volatile int* abort) {
     const BnGeom& g = rd.g;
     int64_t ch;
     int s;
@@ -485,7 +494,7 @@ __device__ void ring_produce_chunk(Ring<SLOTS>& rg, const Rounds& rd, int r, con
     const uint32_t span = chunk_span(ps.nt);
     const int slot = rg.slot();
     const uint32_t use = rg.use();
-    if (use > 0 && !mbar_wait_bounded(&rg.empty[slot], (use - 1) & 1u, kBnWaitLimitNs)) bad = true;
+    if (use > 0 && !ring_wait(&rg.empty[slot], (use - 1) & 1u, kBnWaitLimitNs, abort)) return false;
     unsigned char* base = rg.data + size_t(slot) * kSlotBytes;
     if (lane == 0) {
         uint32_t bytes = 0;
@@ -517,27 +526,41 @@ __device__ void ring_produce_chunk(Ring<SLOTS>& rg, const Rounds& rd, int r, con
         cp_async_mbar_arrive_noinc(&rg.full[slot]);
     }
     ++rg.seq;
+    return true;
 }
 
-// Producer (whole warp): all chunks of round r's slice for pass `ps`.
+// Producer (whole warp): every chunk of round r's slice for pass `ps`.
 template <typename T, int VE, int SLOTS>
-__device__ void ring_produce(Ring<SLOTS>& rg, const Rounds& rd, int r, const RingPass<T>& ps, int lane,
-                             bool& bad) {
+__device__ bool ring_produce(Ring<SLOTS>& rg, const Rounds& rd, int r, const RingPass<T>& ps, int lane,
+                             volatile int* abort) {
     int64_t ch;
     int s;
     uint32_t b0, b1;
     rd.range(r, ch, s, b0, b1);
     const uint32_t span = chunk_span(ps.nt);
     for (uint32_t cb = b0; cb < b1; cb += span)
-        ring_produce_chunk<T, VE>(rg, rd, r, ps, cb, b1 - cb < span ? b1 : cb + span, lane, bad);
+        if (!ring_produce_chunk<T, VE>(rg, rd, r, ps, cb, b1 - cb < span ? b1 : cb + span, lane, abort)) return false;
+    return true;
 }
 
-// Consumer side of one chunk: wait until it has landed / hand the slot back.
+// Producer, at the end: waits (bounded, whatever *abort says) until the last
+// copies issued into every slot have landed.  A slot's copies are issued only
+// after its previous phase completed, so its last phase completing covers all
+// of them.
 template <int SLOTS>
-__device__ __forceinline__ int ring_take(Ring<SLOTS>& rg, bool& bad) {
+__device__ void ring_drain(Ring<SLOTS>& rg, bool& bad) {
+    for (int s = 0; s < SLOTS && s < rg.seq; ++s) {
+        const int last = s + ((rg.seq - 1 - s) / SLOTS) * SLOTS;  // last sequence number that used slot s
+        if (!mbar_wait_bounded(&rg.full[s], uint32_t(last / SLOTS) & 1u, kBnWaitLimitNs)) bad = true;
+    }
+}
+
+// Consumer (whole warp): the slot of the next chunk once it has landed, or -1
+// when the wait gave up.
+template <int SLOTS>
+__device__ __forceinline__ int ring_take(Ring<SLOTS>& rg, volatile int* abort) {
     const int slot = rg.slot();
-    if (!mbar_wait_bounded(&rg.full[slot], rg.use() & 1u, kBnWaitLimitNs)) bad = true;
-    return slot;
+    return ring_wait(&rg.full[slot], rg.use() & 1u, kBnWaitLimitNs, abort) ? slot : -1;
 }
 template <int SLOTS>
 __device__ __forceinline__ void ring_give(Ring<SLOTS>& rg, int slot, int lane) {
@@ -547,56 +570,12 @@ __device__ __forceinline__ void ring_give(Ring<SLOTS>& rg, int slot, int lane) {
 }
 
 template <int SLOTS>
-__device__ __forceinline__ void ring_init(Ring<SLOTS>& rg, uint32_t full_count) {
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < SLOTS; ++i) {
-            mbar_init(&rg.full[i], full_count);
-            mbar_init(&rg.empty[i], kRingConsumerWarps);
-        }
-        mbar_init_fence();
+__device__ __forceinline__ void ring_init(Ring<SLOTS>& rg, uint32_t full_count, uint32_t empty_count) {
+    for (int i = 0; i < SLOTS; ++i) {
+        mbar_init(&rg.full[i], full_count);
+        mbar_init(&rg.empty[i], empty_count);
     }
 }
-
-// Bookkeeper <-> consumer handoffs: per-warp partial sums (by pass parity),
-// a round's coefficients (by round parity), a round's channel parameters (by
-// round mod 4).  "ready" completes when the writer side has arrived, "free"
-// when the reader side has.
-struct Handoffs {
-    uint64_t sums_ready[2], sums_free[2];
-    uint64_t coef_ready[2], coef_free[2];
-    uint64_t par_ready[4], par_free[4];
-};
-
-__device__ __forceinline__ void handoffs_init(Handoffs& h) {
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&h.sums_ready[i], kRingConsumerWarps);
-            mbar_init(&h.sums_free[i], 1);
-            mbar_init(&h.coef_ready[i], 1);
-            mbar_init(&h.coef_free[i], kRingConsumerWarps);
-        }
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(&h.par_ready[i], 1);
-            mbar_init(&h.par_free[i], kRingConsumerWarps);
-        }
-        mbar_init_fence();
-    }
-}
-
-// Shared state of the consumer warps and the bookkeeper.
-struct BnFwdShared {
-    Handoffs hs;
-    Moments warp_m[2][kRingConsumerWarps];  // per-warp statistics by pass parity
-    float2 coef[2];                         // (scale, shift) by round parity
-    Moments keep[4];                        // S == 1: a round's statistics by round mod 4
-};
-struct BnBwdShared {
-    Handoffs hs;
-    float4 warp_s[2][kRingConsumerWarps];   // per-warp (sum dz, sum dz*x) as float-float pairs, by pass parity
-    float4 par[4];                          // (mean, rstd, scale, shift) by round mod 4
-    float2 coef[2];                         // dx coefficients (c1, c2) by round parity
-    double2 keep[4];                        // S == 1: a round's sums by round mod 4
-};
 
 // The VE mask bits of `lane`'s vector of chunk block i, from the slot's words.
 template <int VE>
@@ -605,133 +584,42 @@ __device__ __forceinline__ uint32_t slot_mask_bits(const uint32_t* mw, uint32_t 
     return (mw[i * VE + (e >> 5)] >> (e & 31)) & ((1u << VE) - 1u);
 }
 
-// Bookkeeper of a forward kernel (one warp): merges each statistics pass
-// over the consumer warps and publishes it, merges a complete channel into
-// (scale, shift) for the consumers (training; eval reads the running
-// statistics), and writes the saved and running statistics from slice 0.
-// Polls every handoff without blocking; gives up (sets `bad`) after 2 s
-// without progress.
-template <bool TRAIN>
-__device__ void fwd_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& rd, int nr, BnFwdShared& sh,
-                               int lane, bool& bad) {
-    int q_pub = TRAIN ? 0 : nr, r_mrg = 0;
-    int pre_r = -1;  // round whose weight and bias are in pre_w, pre_b
-    float pre_w = 1.f, pre_b = 0.f;
-    bool aborted = false;
-    uint64_t t_last = global_timer_ns();
-    while (q_pub < nr || r_mrg < nr) {
-        bool moved = false;
-        if (q_pub < nr && (aborted || mbar_test_wait(&sh.hs.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
-            Moments m = lane < kRingConsumerWarps ? sh.warp_m[q_pub & 1][lane] : Moments{0.f, 0.f, 0.f};
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.hs.sums_free[q_pub & 1]);
-            warp_merge(m);
-            int64_t ch;
-            int s;
-            uint32_t b0, b1;
-            rd.range(q_pub, ch, s, b0, b1);
-            if (g.S > 1) {
-                if (lane == 0) {
-                    float4* part = reinterpret_cast<float4*>(g.partials) + ch * g.S;
-                    part[s] = make_float4(m.n, m.mean, m.m2, 0.f);
-                    red_release_add_u32(g.counters + ch, 1u);
-                }
-            } else if (lane == 0) {
-                sh.keep[q_pub & 3] = m;
-            }
-            ++q_pub;
-            moved = true;
-        }
-        if (r_mrg < nr && (!TRAIN || r_mrg < q_pub)) {
-            const uint32_t u = uint32_t(r_mrg) >> 1;
-            bool ok = u == 0 || aborted || mbar_test_wait(&sh.hs.coef_free[r_mrg & 1], (u - 1) & 1);
-            int64_t ch;
-            int s;
-            uint32_t b0, b1;
-            rd.range(r_mrg, ch, s, b0, b1);
-            if (pre_r != r_mrg) {
-                // issued now, used once the channel is complete
-                pre_w = a.w ? a.w[ch] : 1.f;
-                pre_b = a.b ? a.b[ch] : 0.f;
-                pre_r = r_mrg;
-            }
-            if (TRAIN && ok && g.S > 1 && !aborted) {
-                // every lane acquires: the partials may then be read directly
-                ok = __all_sync(0xffffffffu, ld_acquire_u32(g.counters + ch) >= uint32_t(g.S));
-            }
-            if (ok) {
-                const float wc = pre_w;
-                const float bc = pre_b;
-                if constexpr (TRAIN) {
-                    Moments tot = sh.keep[r_mrg & 3];  // lane 0's copy is the one used when S == 1
-                    if (g.S > 1) {
-                        const float4* part = reinterpret_cast<const float4*>(g.partials) + ch * g.S;
-                        Moments lm{0.f, 0.f, 0.f};
-                        for (int i = lane; i < g.S; i += 32) {
-                            const float4 pv = ld_cg_f4(part + i);
-                            chan_merge(lm, pv.x, pv.y, pv.z);
-                        }
-                        warp_merge(lm);
-                        tot = lm;
-                    }
-                    if (lane == 0) {
-                        const float var = tot.m2 * g.inv_m;
-                        const float rs = rsqrtf(var + a.eps);
-                        sh.coef[r_mrg & 1] = make_float2(wc * rs, bc - tot.mean * wc * rs);
-                        mbar_arrive(&sh.hs.coef_ready[r_mrg & 1]);
-                        if (s == 0) {
-                            if (a.save_mean) a.save_mean[ch] = tot.mean;
-                            if (a.save_rstd) a.save_rstd[ch] = rs;
-                            if (a.rm) a.rm[ch] = fmaf(a.momentum, tot.mean, (1.f - a.momentum) * a.rm[ch]);
-                            if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * a.rv[ch]);
-                        }
-                    }
-                } else {
-                    if (lane == 0) {
-                        const float rs = rsqrtf(a.rv[ch] + a.eps);
-                        const float mu = a.rm[ch];
-                        sh.coef[r_mrg & 1] = make_float2(wc * rs, bc - mu * wc * rs);
-                        mbar_arrive(&sh.hs.coef_ready[r_mrg & 1]);
-                        if (s == 0) {
-                            if (a.save_mean) a.save_mean[ch] = mu;
-                            if (a.save_rstd) a.save_rstd[ch] = rs;
-                        }
-                    }
-                }
-                ++r_mrg;
-                moved = true;
-            }
-        }
-        if (moved) {
-            t_last = global_timer_ns();
-        } else {
-            __nanosleep(32);
-            if (global_timer_ns() - t_last > kBnWaitLimitNs) {
-                aborted = true;
-                bad = true;
-            }
-        }
-    }
+// Warp-uniform %globaltimer.
+__device__ __forceinline__ uint64_t warp_now() {
+    return __shfl_sync(0xffffffffu, (unsigned long long)global_timer_ns(), 0);
 }
 
 // ---------------------------------------------------------------------------
-// forward on the ring
+// eval mode on the ring: one pass per round, coefficients from the running
+// statistics (no channel depends on another CTA)
 // ---------------------------------------------------------------------------
-// Consumers: statistics of round r+1 (x, kept in L2) ahead of the apply pass
-// of round r (x from L2 and the residual, both read for the last time).  The
-// bookkeeper merges each statistics pass over the 16 consumer warps and
-// publishes it, merges a channel's S slices once they have all arrived, and
-// hands the consumers the channel's scale and shift.
-template <typename T, bool TRAIN, int ACT>
-__global__ void __launch_bounds__(kRingThreads, 1)
-bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
+// Roles: 16 consumer warps, a producer warp, and a bookkeeper warp that stages
+// each round's channel parameters ahead of the consumers (and, backward,
+// publishes the CTA's sums; the last slice of a channel to publish merges
+// dw, db).
+constexpr int kEvConsumerWarps = 16;
+constexpr int kEvThreads = (kEvConsumerWarps + 2) * 32;
+constexpr int kEvSlotsFwd = 7;
+constexpr int kEvSlotsBwd = 6;
+
+struct EvFwdShared {
+    uint64_t coef_ready[2], coef_free[2];   // bookkeeper -> consumers, by round parity
+    float2 coef[2];                         // (scale, shift)
+    int abort;
+};
+
+// y = act(x*scale + shift (+ residual)) with scale, shift from the running
+// statistics; saved statistics mean = running_mean, rstd = (running_var +
+// eps)^-1/2 from slice 0.
+template <typename T, int ACT>
+__global__ void __launch_bounds__(kEvThreads, 1)
+bn_fwd_eval_kernel(const BnArgs a, const BnGeom g) {
     constexpr int VE = kVec<T>;
-    constexpr int SLOTS = kRingSlotsFwd;
+    constexpr int SLOTS = kEvSlotsFwd;
     extern __shared__ __align__(128) unsigned char ring_data[];
     __shared__ __align__(8) uint64_t full[SLOTS];
     __shared__ __align__(8) uint64_t empty[SLOTS];
-    __shared__ BnFwdShared sh;
-    __shared__ int s_bad;
+    __shared__ EvFwdShared sh;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -741,85 +629,72 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
     const Rounds rd(g);
     const int nr = rd.count();
     Ring<SLOTS> rg{ring_data, nullptr, full, empty};
+    volatile int* abort = &sh.abort;
     bool bad = false;
 
-    if (threadIdx.x == 0) s_bad = 0;
-    ring_init(rg, 1);
-    handoffs_init(sh.hs);
+    if (threadIdx.x == 0) {
+        ring_init(rg, 1, kEvConsumerWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh.coef_ready[i], 1);
+            mbar_init(&sh.coef_free[i], kEvConsumerWarps);
+        }
+        sh.abort = 0;
+        mbar_init_fence();
+    }
     __syncthreads();
 
-    if (warp == kProducerWarp) {
+    if (warp == kEvConsumerWarps) {
         // ---------------- producer ----------------
-        const uint64_t pol_keep = TRAIN ? l2_evict_last() : l2_evict_first();
-        const uint64_t pol_stream = l2_evict_first();
-        const RingPass<T> stats{{x, nullptr, nullptr}, {pol_keep, 0, 0}, 1, nullptr};
-        const RingPass<T> apply{{x, res, nullptr}, {pol_stream, pol_stream, 0}, res ? 2 : 1, nullptr};
-        if (TRAIN && nr > 0) ring_produce<T, VE>(rg, rd, 0, stats, lane, bad);
+        const uint64_t pol = l2_evict_first();
+        const RingPass<T> apply{{x, res, nullptr}, {pol, pol, 0}, res ? 2 : 1, nullptr};
+        for (int r = 0; r < nr; ++r)
+            if (!ring_produce<T, VE>(rg, rd, r, apply, lane, abort)) break;
+        ring_drain(rg, bad);
+    } else if (warp == kEvConsumerWarps + 1) {
+        // ---------------- bookkeeper: (scale, shift) of round r ----------------
         for (int r = 0; r < nr; ++r) {
-            if (TRAIN && r + 1 < nr) ring_produce<T, VE>(rg, rd, r + 1, stats, lane, bad);
-            ring_produce<T, VE>(rg, rd, r, apply, lane, bad);
+            if (r >= 2 && !ring_wait(&sh.coef_free[r & 1], uint32_t((r >> 1) - 1) & 1u, kBnWaitLimitNs, abort)) break;
+            if (lane == 0) {
+                int64_t ch;
+                int s;
+                uint32_t b0, b1;
+                rd.range(r, ch, s, b0, b1);
+                const float wc = a.w ? a.w[ch] : 1.f;
+                const float bc = a.b ? a.b[ch] : 0.f;
+                const float rs = rsqrtf(a.rv[ch] + a.eps);
+                const float mu = a.rm[ch];
+                sh.coef[r & 1] = make_float2(wc * rs, bc - mu * wc * rs);
+                mbar_arrive(&sh.coef_ready[r & 1]);
+                if (s == 0) {
+                    if (a.save_mean) a.save_mean[ch] = mu;
+                    if (a.save_rstd) a.save_rstd[ch] = rs;
+                }
+            }
         }
-    } else if (warp == kBookkeeperWarp) {
-        // ---------------- bookkeeper ----------------
-        fwd_bookkeeper<TRAIN>(a, g, rd, nr, sh, lane, bad);
     } else {
         // ---------------- consumers ----------------
         const uint64_t pol_stream = l2_evict_first();
-        // statistics of round q's slice -> this warp's moments -> bookkeeper
-        auto stats = [&](int q) {
-            int64_t ch;
-            int s;
-            uint32_t b0, b1;
-            rd.range(q, ch, s, b0, b1);
-            ShiftedSums acc;
-            const uint32_t span = chunk_span(1);
-            for (uint32_t cb = b0; cb < b1; cb += span) {
-                const uint32_t n = b1 - cb < span ? b1 - cb : span;
-                const int slot = ring_take(rg, bad);
-                const uint4* sx = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
-                for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
-                    const BlockPos p = block_pos(g, cb + i, lane, ch);
-                    if (p.v < g.lv) {
-                        Pack<T, VE> pk;
-                        pk.u = sx[i * 32 + lane];
-                        float v[VE];
-                        unpack<T, VE>(pk, v);
-                        acc.add(v);
-                    }
-                }
-                ring_give(rg, slot, lane);
-            }
-            Moments m = acc.moments();
-            warp_merge(m);
-            if (lane == 0) {
-                if (q >= 2 && !mbar_wait_bounded(&sh.hs.sums_free[q & 1], ((q >> 1) - 1) & 1, kBnWaitLimitNs)) bad = true;
-                sh.warp_m[q & 1][warp] = m;
-                mbar_arrive(&sh.hs.sums_ready[q & 1]);
-            }
-        };
-
-        if (TRAIN && nr > 0) stats(0);
+        const uint32_t span = chunk_span(res ? 2 : 1);
         for (int r = 0; r < nr; ++r) {
+            if (!ring_wait(&sh.coef_ready[r & 1], uint32_t(r >> 1) & 1u, kBnWaitLimitNs, abort)) break;
+            const float2 sc = sh.coef[r & 1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.coef_free[r & 1]);
             int64_t ch;
             int s;
             uint32_t b0, b1;
             rd.range(r, ch, s, b0, b1);
-            if (TRAIN && r + 1 < nr) stats(r + 1);
-            if (!mbar_wait_bounded(&sh.hs.coef_ready[r & 1], (r >> 1) & 1, kBnWaitLimitNs)) bad = true;
-            const float2 sc = sh.coef[r & 1];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.hs.coef_free[r & 1]);
-            const float scale = sc.x;
-            const float shift = sc.y;
-
-            // ---- y = act(x*scale + shift (+ residual)) (+ ReLU mask) ----
-            const uint32_t span = chunk_span(res ? 2 : 1);
+            bool ok = true;
             for (uint32_t cb = b0; cb < b1; cb += span) {
                 const uint32_t n = b1 - cb < span ? b1 - cb : span;
-                const int slot = ring_take(rg, bad);
+                const int slot = ring_take(rg, abort);
+                if (slot < 0) {
+                    ok = false;
+                    break;
+                }
                 const uint4* sx = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
                 const uint4* sr = sx + span * 32;
-                for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
+                for (uint32_t i = warp; i < n; i += kEvConsumerWarps) {
                     const BlockPos p = block_pos(g, cb + i, lane, ch);
                     uint32_t nib = 0;
                     if (p.v < g.lv) {
@@ -833,7 +708,7 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
                         }
 #pragma unroll
                         for (int k = 0; k < VE; ++k) {
-                            float z = fmaf(v[k], scale, shift);
+                            float z = fmaf(v[k], sc.x, sc.y);
                             if (res) z += rr[k];
                             nib |= uint32_t(z > 0.f) << k;
                             o[k] = act_forward_c<ACT>(z, a.act_param, a.act);
@@ -844,12 +719,13 @@ bn_fwd_ring_kernel(const BnArgs a, const BnGeom g) {
                 }
                 ring_give(rg, slot, lane);
             }
+            if (!ok) break;
         }
     }
 
-    if (bad) s_bad = 1;
     __syncthreads();
-    if (threadIdx.x == 0 && s_bad) atomicOr(a.err, kErrTimeoutStage | kErrTimeoutPeers);
+    if (threadIdx.x == 0 && sh.abort) atomicOr(a.err, kErrTimeoutStage);
+    if (bad && lane == 0) atomicOr(a.err, kErrTimeoutStage);
 }
 
 // ---------------------------------------------------------------------------
@@ -1127,18 +1003,8 @@ bn_bwd_kernel(const BnArgs a, const BnGeom g) {
 }
 
 // ---------------------------------------------------------------------------
-// backward on the ring
+// backward on the ring: helpers shared by the eval and training kernels
 // ---------------------------------------------------------------------------
-// Tensors of a pass: dy, x, and the residual when z must be recomputed with
-// it; the ReLU mask words ride along in the slot.  Training: pass 1 of round
-// r+1 (dz, dres, channel sums; dy and x kept in L2) ahead of pass 2 of round
-// r (dx).  Pass 1 streams from HBM through one ring, pass 2 re-reads L2
-// through a second ring with its own producer warp, so the HBM ring keeps
-// prefetching the next rounds while pass 2 and the channel waits run.  Eval:
-// one pass per round (dx = dz*scale).
-// The bookkeeper stages each round's channel parameters, publishes the sums,
-// merges a channel's S slices (training: into the dx coefficients; eval: in
-// the last slice to finish, into dw and db) and writes dw, db.
 
 // dz of one lane's vector from the slot: dy passed through the activation's
 // derivative at z (mask bits, or z recomputed from x and the residual).
@@ -1203,140 +1069,27 @@ __device__ __forceinline__ double grad_center(const BnArgs& a, int64_t ch, float
     return t2c * double(rs);
 }
 
-// Bookkeeper of a backward kernel (one warp): stages each round's channel
-// parameters, publishes the CTA's pass-1 sums, and (training) turns a
-// complete channel into the dx coefficients; dw, db come from slice 0
-// (training) or from the last slice to publish (eval).  Polls every handoff
-// without blocking; gives up (sets `bad`) after 2 s without progress.
-template <bool TRAIN>
-__device__ void bwd_bookkeeper(const BnArgs& a, const BnGeom& g, const Rounds& rd, int nr, BnBwdShared& sh,
-                               int lane, bool& bad) {
-    int q_par = 0, q_pub = 0, r_mrg = TRAIN ? 0 : nr;
-    bool aborted = false;
-    uint64_t t_last = global_timer_ns();
-    while (q_par < nr || q_pub < nr || r_mrg < nr) {
-        bool moved = false;
-        // channel parameters of round q_par
-        if (q_par < nr) {
-            const uint32_t u = uint32_t(q_par) >> 2;
-            if (u == 0 || aborted || mbar_test_wait(&sh.hs.par_free[q_par & 3], (u - 1) & 1)) {
-                if (lane == 0) {
-                    int64_t ch;
-                    int s;
-                    uint32_t b0, b1;
-                    rd.range(q_par, ch, s, b0, b1);
-                    const float mu = a.mean_in[ch];
-                    const float rs = a.rstd_in[ch];
-                    const float wc = a.w ? a.w[ch] : 1.f;
-                    const float bc = a.b ? a.b[ch] : 0.f;
-                    const float scale = wc * rs;
-                    sh.par[q_par & 3] = make_float4(mu, rs, scale, bc - mu * scale);
-                    mbar_arrive(&sh.hs.par_ready[q_par & 3]);
-                }
-                ++q_par;
-                moved = true;
-            }
-        }
-        // pass-1 sums of round q_pub
-        if (q_pub < nr && (aborted || mbar_test_wait(&sh.hs.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
-            double2 v = make_double2(0.0, 0.0);
-            if (lane < kRingConsumerWarps) {
-                const float4 f = sh.warp_s[q_pub & 1][lane];
-                v = make_double2(ff_to_double(FF{f.x, f.y}), ff_to_double(FF{f.z, f.w}));
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.hs.sums_free[q_pub & 1]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-                v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-            }
-            int64_t ch;
-            int s;
-            uint32_t b0, b1;
-            rd.range(q_pub, ch, s, b0, b1);
-            if (g.S == 1) {
-                if (TRAIN) {
-                    if (lane == 0) sh.keep[q_pub & 3] = v;
-                } else if (lane == 0) {
-                    grad_center(a, ch, a.mean_in[ch], a.rstd_in[ch], v.x, v.y, true);
-                }
-            } else {
-                uint32_t last = 0;
-                if (lane == 0) {
-                    double2* part = reinterpret_cast<double2*>(g.partials) + ch * g.S;
-                    part[s] = v;
-                    if (TRAIN) red_release_add_u32(g.counters + ch, 1u);
-                    else last = atom_acq_rel_add_u32(g.counters + ch, 1u) == uint32_t(g.S - 1);
-                }
-                if (!TRAIN && __shfl_sync(0xffffffffu, last, 0)) {
-                    // every other slice has published: merge into dw, db
-                    if (ld_acquire_u32(g.counters + ch) < uint32_t(g.S)) bad = true;
-                    double t1, t2;
-                    merge_grad_partials(g, ch, lane, t1, t2);
-                    if (lane == 0) grad_center(a, ch, a.mean_in[ch], a.rstd_in[ch], t1, t2, true);
-                }
-            }
-            ++q_pub;
-            moved = true;
-        }
-        // training: the dx coefficients of round r_mrg once its channel is complete
-        if (TRAIN && r_mrg < nr && r_mrg < q_pub) {
-            const uint32_t u = uint32_t(r_mrg) >> 1;
-            bool ok = u == 0 || aborted || mbar_test_wait(&sh.hs.coef_free[r_mrg & 1], (u - 1) & 1);
-            int64_t ch;
-            int s;
-            uint32_t b0, b1;
-            rd.range(r_mrg, ch, s, b0, b1);
-            if (ok && g.S > 1 && !aborted) {
-                // every lane acquires: the partials may then be read directly
-                ok = __all_sync(0xffffffffu, ld_acquire_u32(g.counters + ch) >= uint32_t(g.S));
-            }
-            if (ok) {
-                double t1, t2;
-                if (g.S > 1) {
-                    merge_grad_partials(g, ch, lane, t1, t2);
-                } else {
-                    const double2 k = sh.keep[r_mrg & 3];  // used by lane 0 only
-                    t1 = k.x;
-                    t2 = k.y;
-                }
-                if (lane == 0) {
-                    // this round's parameters are still staged: its consumers free them after pass 2
-                    const float4 pr = sh.par[r_mrg & 3];
-                    const double t2r = grad_center(a, ch, pr.x, pr.y, t1, t2, s == 0);
-                    sh.coef[r_mrg & 1] = make_float2(float(t1 * double(g.inv_m)), float(t2r * double(g.inv_m)));
-                    mbar_arrive(&sh.hs.coef_ready[r_mrg & 1]);
-                }
-                ++r_mrg;
-                moved = true;
-            }
-        }
-        if (moved) {
-            t_last = global_timer_ns();
-        } else {
-            __nanosleep(32);
-            if (global_timer_ns() - t_last > kBnWaitLimitNs) {
-                aborted = true;
-                bad = true;
-            }
-        }
-    }
-}
+struct EvBwdShared {
+    uint64_t sums_ready[2], sums_free[2];   // consumers -> bookkeeper, by round parity
+    uint64_t par_ready[4], par_free[4];     // a round's channel parameters, by round mod 4
+    float4 warp_s[2][kEvConsumerWarps];     // per-warp (sum dz, sum dz*(x - mean)) as float-float pairs
+    float4 par[4];                          // (mean, rstd, scale, shift)
+    int abort;
+};
 
-template <typename T, bool TRAIN, int ACT>
-__global__ void __launch_bounds__(TRAIN ? kRingThreadsBwdTrain : kRingThreads, 1)
-bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
+// Eval backward: dz = dy*act'(z), dres = dz, dx = dz*w*rstd in one pass per
+// round; the CTA's two channel sums are published to the workspace and the
+// last slice of a channel to publish (acquire-release arrival count) merges
+// them in slice order into dw = sum dz*xhat and db = sum dz.
+template <typename T, int ACT>
+__global__ void __launch_bounds__(kEvThreads, 1)
+bn_bwd_eval_kernel(const BnArgs a, const BnGeom g) {
     constexpr int VE = kVec<T>;
-    constexpr int SLOTS = TRAIN ? kRingSlotsBwdHbm : kRingSlotsBwd;
-    constexpr int SLOTS2 = TRAIN ? kRingSlotsBwdL2 : 1;
+    constexpr int SLOTS = kEvSlotsBwd;
     extern __shared__ __align__(128) unsigned char ring_data[];
     __shared__ __align__(8) uint64_t full[SLOTS];
     __shared__ __align__(8) uint64_t empty[SLOTS];
-    __shared__ __align__(8) uint64_t full2[SLOTS2];
-    __shared__ __align__(8) uint64_t empty2[SLOTS2];
-    __shared__ BnBwdShared sh;
-    __shared__ int s_bad;
+    __shared__ EvBwdShared sh;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -1350,149 +1103,159 @@ bn_bwd_ring_kernel(const BnArgs a, const BnGeom g) {
     const int nt = (need_z && res) ? 3 : 2;
     const Rounds rd(g);
     const int nr = rd.count();
-    // [ring: SLOTS data | SLOTS mask words][ring 2 (training): SLOTS2 data | SLOTS2 mask words]
-    constexpr size_t kRingBytes = size_t(SLOTS) * (kSlotBytes + kSlotMaskWords * 4);
     Ring<SLOTS> rg{ring_data, reinterpret_cast<uint32_t*>(ring_data + size_t(SLOTS) * kSlotBytes), full, empty};
-    Ring<SLOTS2> rg2{ring_data + kRingBytes,
-                     reinterpret_cast<uint32_t*>(ring_data + kRingBytes + size_t(SLOTS2) * kSlotBytes), full2, empty2};
+    volatile int* abort = &sh.abort;
     bool bad = false;
 
-    if (threadIdx.x == 0) s_bad = 0;
-    ring_init(rg, use_mask ? 33u : 1u);
-    if (TRAIN) ring_init(rg2, use_mask ? 33u : 1u);
-    handoffs_init(sh.hs);
+    if (threadIdx.x == 0) {
+        ring_init(rg, use_mask ? 33u : 1u, kEvConsumerWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh.sums_ready[i], kEvConsumerWarps);
+            mbar_init(&sh.sums_free[i], 1);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&sh.par_ready[i], 1);
+            mbar_init(&sh.par_free[i], kEvConsumerWarps);
+        }
+        sh.abort = 0;
+        mbar_init_fence();
+    }
     __syncthreads();
 
-    if (warp == kProducerWarp) {
+    if (warp == kEvConsumerWarps) {
         // ---------------- producer ----------------
-        const uint64_t pol_keep = TRAIN ? l2_evict_last() : l2_evict_first();
-        const uint32_t* mk = use_mask ? a.mask_in : nullptr;
-        const RingPass<T> first{{dy, x, res}, {pol_keep, pol_keep, pol_keep}, nt, mk};
-        for (int q = 0; q < nr; ++q) ring_produce<T, VE>(rg, rd, q, first, lane, bad);
-    } else if (warp == kProducer2Warp) {
-        // ---------------- producer of pass 2 (training): L2 re-reads ----------------
-        const uint64_t pol_stream = l2_evict_first();
-        const RingPass<T> second{{dy, x, res}, {pol_stream, pol_stream, pol_stream}, nt,
-                                 use_mask ? a.mask_in : nullptr};
-        for (int r = 0; r < nr; ++r) ring_produce<T, VE>(rg2, rd, r, second, lane, bad);
-    } else if (warp == kBookkeeperWarp) {
-        // ---------------- bookkeeper ----------------
-        bwd_bookkeeper<TRAIN>(a, g, rd, nr, sh, lane, bad);
+        const uint64_t pol = l2_evict_first();
+        const RingPass<T> pass{{dy, x, res}, {pol, pol, pol}, nt, use_mask ? a.mask_in : nullptr};
+        for (int q = 0; q < nr; ++q)
+            if (!ring_produce<T, VE>(rg, rd, q, pass, lane, abort)) break;
+        ring_drain(rg, bad);
+    } else if (warp == kEvConsumerWarps + 1) {
+        // ---------------- bookkeeper: parameters ahead, sums published, dw/db merged ----------------
+        int q_par = 0, q_pub = 0;
+        uint64_t t_last = warp_now();
+        while ((q_par < nr || q_pub < nr) && !*abort) {
+            bool moved = false;
+            if (q_par < nr && (q_par < 4 || __all_sync(0xffffffffu, mbar_test_wait(&sh.par_free[q_par & 3],
+                                                                                   ((q_par >> 2) - 1) & 1)))) {
+                if (lane == 0) {
+                    int64_t ch;
+                    int s;
+                    uint32_t b0, b1;
+                    rd.range(q_par, ch, s, b0, b1);
+                    const float mu = a.mean_in[ch];
+                    const float rs = a.rstd_in[ch];
+                    const float wc = a.w ? a.w[ch] : 1.f;
+                    const float bc = a.b ? a.b[ch] : 0.f;
+                    const float scale = wc * rs;
+                    sh.par[q_par & 3] = make_float4(mu, rs, scale, bc - mu * scale);
+                    mbar_arrive(&sh.par_ready[q_par & 3]);
+                }
+                ++q_par;
+                moved = true;
+            }
+            if (q_pub < nr && __all_sync(0xffffffffu, mbar_test_wait(&sh.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
+                double2 v = make_double2(0.0, 0.0);
+                if (lane < kEvConsumerWarps) {
+                    const float4 f = sh.warp_s[q_pub & 1][lane];
+                    v = make_double2(ff_to_double(FF{f.x, f.y}), ff_to_double(FF{f.z, f.w}));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.sums_free[q_pub & 1]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+                    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+                }
+                int64_t ch;
+                int s;
+                uint32_t b0, b1;
+                rd.range(q_pub, ch, s, b0, b1);
+                if (g.S == 1) {
+                    if (lane == 0) grad_center(a, ch, a.mean_in[ch], a.rstd_in[ch], v.x, v.y, true);
+                } else {
+                    uint32_t last = 0;
+                    if (lane == 0) {
+                        double2* part = reinterpret_cast<double2*>(g.partials) + ch * g.S;
+                        part[s] = v;
+                        last = atom_acq_rel_add_u32(g.counters + ch, 1u) == uint32_t(g.S - 1);
+                    }
+                    if (__shfl_sync(0xffffffffu, last, 0)) {
+                        // every other slice has published: merge into dw, db
+                        double t1, t2;
+                        merge_grad_partials(g, ch, lane, t1, t2);
+                        if (lane == 0) grad_center(a, ch, a.mean_in[ch], a.rstd_in[ch], t1, t2, true);
+                    }
+                }
+                ++q_pub;
+                moved = true;
+            }
+            const uint64_t now = warp_now();
+            if (moved) {
+                t_last = now;
+            } else if (now - t_last > kBnWaitLimitNs) {
+                if (lane == 0) *abort = 1;
+                break;
+            }
+        }
     } else {
         // ---------------- consumers ----------------
         const uint64_t pol_stream = l2_evict_first();
         const uint32_t span = chunk_span(nt);
-
-        // one chunk of pass 1: dz, dres (and dx in eval), the two channel sums
-        auto chunk1 = [&](int64_t ch, float scale, float shift, uint32_t cb, uint32_t n, GradSums& acc) {
-            const int slot = ring_take(rg, bad);
-            const uint4* sd = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
-            const uint4* sx = sd + span * 32;
-            const uint4* sr = sx + span * 32;
-            const uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
-            for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
-                const BlockPos p = block_pos(g, cb + i, lane, ch);
-                if (p.v >= g.lv) continue;
-                Pack<T, VE> pdy, px;
-                pdy.u = sd[i * 32 + lane];
-                px.u = sx[i * 32 + lane];
-                float dyv[VE], xv[VE], dz[VE];
-                unpack<T, VE>(pdy, dyv);
-                unpack<T, VE>(px, xv);
-                ring_dz<T, VE, ACT>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
-                const int64_t e = (p.seg * g.lv + p.v) * VE;
-                if (dres) store_vec_pol<T, VE>(dres + e, dz, pol_stream);
-                acc.add(dz, xv);
-                if constexpr (!TRAIN) {
-                    float o[VE];
-#pragma unroll
-                    for (int k = 0; k < VE; ++k) o[k] = dz[k] * scale;
-                    store_vec_pol<T, VE>(dx + e, o, pol_stream);
-                }
-            }
-            ring_give(rg, slot, lane);
-        };
-        // this warp's pass-1 sums of round q -> bookkeeper
-        auto publish = [&](int q, const GradSums& acc) {
-            // float-float warp sums: no double-precision arithmetic on the consumers' path
-            const FF d1 = ff_warp_sum(acc.ff_dz());
-            const FF d2 = ff_warp_sum(acc.ff_dzc());
-            if (lane == 0) {
-                if (q >= 2 && !mbar_wait_bounded(&sh.hs.sums_free[q & 1], ((q >> 1) - 1) & 1, kBnWaitLimitNs)) bad = true;
-                sh.warp_s[q & 1][warp] = make_float4(d1.hi, d1.lo, d2.hi, d2.lo);
-                mbar_arrive(&sh.hs.sums_ready[q & 1]);
-                if (!TRAIN) mbar_arrive(&sh.hs.par_free[q & 3]);
-            }
-        };
-        // channel parameters (mean, rstd, scale, shift) of round q
-        auto params = [&](int q) {
-            if (!mbar_wait_bounded(&sh.hs.par_ready[q & 3], (q >> 2) & 1, kBnWaitLimitNs)) bad = true;
-            return sh.par[q & 3];
-        };
-        auto pass1 = [&](int q) {
+        for (int q = 0; q < nr; ++q) {
+            if (!ring_wait(&sh.par_ready[q & 3], uint32_t(q >> 2) & 1u, kBnWaitLimitNs, abort)) break;
+            const float4 pr = sh.par[q & 3];
             int64_t ch;
             int s;
             uint32_t b0, b1;
             rd.range(q, ch, s, b0, b1);
-            const float4 pr = params(q);
             GradSums acc(pr.x);
-            for (uint32_t cb = b0; cb < b1; cb += span) chunk1(ch, pr.z, pr.w, cb, min(span, b1 - cb), acc);
-            publish(q, acc);
-        };
-
-        if constexpr (!TRAIN) {
-            for (int q = 0; q < nr; ++q) pass1(q);
-        } else {
-            if (nr > 0) pass1(0);
-            for (int r = 0; r < nr; ++r) {
-                int64_t ch;
-                int s;
-                uint32_t b0, b1;
-                rd.range(r, ch, s, b0, b1);
-                if (r + 1 < nr) pass1(r + 1);
-                const float4 pr = sh.par[r & 3];  // waited for in pass 1 of round r; freed below
-                const float mu = pr.x, rs = pr.y, scale = pr.z, shift = pr.w;
-                if (!mbar_wait_bounded(&sh.hs.coef_ready[r & 1], (r >> 1) & 1, kBnWaitLimitNs)) bad = true;
-                const float2 cc = sh.coef[r & 1];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.hs.coef_free[r & 1]);
-                const float c1 = cc.x, c2 = cc.y;
-                // ---- pass 2: dx = w*rstd*(dz - sum(dz)/M - xhat*sum(dz*xhat)/M), from ring 2 ----
-                for (uint32_t cb = b0; cb < b1; cb += span) {
-                    const uint32_t n = min(span, b1 - cb);
-                    const int slot = ring_take(rg2, bad);
-                    const uint4* sd = reinterpret_cast<const uint4*>(rg2.data + size_t(slot) * kSlotBytes);
-                    const uint4* sx = sd + span * 32;
-                    const uint4* sr = sx + span * 32;
-                    const uint32_t* mw = rg2.mask + size_t(slot) * kSlotMaskWords;
-                    for (uint32_t i = warp; i < n; i += kRingConsumerWarps) {
-                        const BlockPos p = block_pos(g, cb + i, lane, ch);
-                        if (p.v >= g.lv) continue;
-                        Pack<T, VE> pdy, px;
-                        pdy.u = sd[i * 32 + lane];
-                        px.u = sx[i * 32 + lane];
-                        float dyv[VE], xv[VE], dz[VE], o[VE];
-                        unpack<T, VE>(pdy, dyv);
-                        unpack<T, VE>(px, xv);
-                        ring_dz<T, VE, ACT>(a, use_mask, need_z, mw, sr, i, lane, scale, shift, dyv, xv, dz);
-#pragma unroll
-                        for (int k = 0; k < VE; ++k) {
-                            const float xh = (xv[k] - mu) * rs;
-                            o[k] = scale * (dz[k] - c1 - xh * c2);
-                        }
-                        store_vec_pol<T, VE>(dx + (p.seg * g.lv + p.v) * VE, o, pol_stream);
-                    }
-                    ring_give(rg2, slot, lane);
+            bool ok = true;
+            for (uint32_t cb = b0; cb < b1; cb += span) {
+                const uint32_t n = min(span, b1 - cb);
+                const int slot = ring_take(rg, abort);
+                if (slot < 0) {
+                    ok = false;
+                    break;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.hs.par_free[r & 3]);
+                const uint4* sd = reinterpret_cast<const uint4*>(ring_data + size_t(slot) * kSlotBytes);
+                const uint4* sx = sd + span * 32;
+                const uint4* sr = sx + span * 32;
+                const uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
+                for (uint32_t i = warp; i < n; i += kEvConsumerWarps) {
+                    const BlockPos p = block_pos(g, cb + i, lane, ch);
+                    if (p.v >= g.lv) continue;
+                    Pack<T, VE> pdy, px;
+                    pdy.u = sd[i * 32 + lane];
+                    px.u = sx[i * 32 + lane];
+                    float dyv[VE], xv[VE], dz[VE], o[VE];
+                    unpack<T, VE>(pdy, dyv);
+                    unpack<T, VE>(px, xv);
+                    ring_dz<T, VE, ACT>(a, use_mask, need_z, mw, sr, i, lane, pr.z, pr.w, dyv, xv, dz);
+                    const int64_t e = (p.seg * g.lv + p.v) * VE;
+                    if (dres) store_vec_pol<T, VE>(dres + e, dz, pol_stream);
+                    acc.add(dz, xv);
+#pragma unroll
+                    for (int k = 0; k < VE; ++k) o[k] = dz[k] * pr.z;
+                    store_vec_pol<T, VE>(dx + e, o, pol_stream);
+                }
+                ring_give(rg, slot, lane);
+            }
+            if (!ok) break;
+            // float-float warp sums: no double-precision arithmetic on the consumers' path
+            const FF d1 = ff_warp_sum(acc.ff_dz());
+            const FF d2 = ff_warp_sum(acc.ff_dzc());
+            if (q >= 2 && !ring_wait(&sh.sums_free[q & 1], uint32_t((q >> 1) - 1) & 1u, kBnWaitLimitNs, abort)) break;
+            if (lane == 0) {
+                sh.warp_s[q & 1][warp] = make_float4(d1.hi, d1.lo, d2.hi, d2.lo);
+                mbar_arrive(&sh.sums_ready[q & 1]);
+                mbar_arrive(&sh.par_free[q & 3]);
             }
         }
     }
 
-    if (bad) s_bad = 1;
     __syncthreads();
-    if (threadIdx.x == 0 && s_bad) atomicOr(a.err, kErrTimeoutStage | kErrTimeoutPeers);
+    if (threadIdx.x == 0 && sh.abort) atomicOr(a.err, kErrTimeoutStage);
+    if (bad && lane == 0) atomicOr(a.err, kErrTimeoutStage);
 }
 
 }  // namespace nrm
@@ -1546,8 +1309,8 @@ inline void bn_geometry(BnGeom& g, const BnArgs& a, int ve) {
 // r+1 overlaps the second pass of round r).  The ring forward keeps one tensor
 // and prefers fewer, longer rounds (measured on the ResNet shape), so it gets
 // a larger share.
+// L2 held between the two passes of the scalar kernels' rounds.
 constexpr double kBnL2Budget = 48.0 * 1024 * 1024;
-constexpr double kBnL2BudgetRingFwd = 64.0 * 1024 * 1024;
 // The training kernels keep up to lag + 1 rounds of first-pass data in L2.
 #ifndef NRM_BN_TRAIN_L2_MB_FWD
 #define NRM_BN_TRAIN_L2_MB_FWD 128
@@ -1724,14 +1487,13 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
     }
     if (vec && a.c > 0 && a.n * a.l > 0) {
         const void* fn = with_act(a.act, [&](auto act) {
-            return (const void*)&bn_fwd_ring_kernel<T, false, decltype(act)::value>;
+            return (const void*)&bn_fwd_eval_kernel<T, decltype(act)::value>;
         });
         BnPlan pl;
         bn_geometry(pl.g, a, kVec<T>);
-        nrm_status st = bn_plan_ring(pl, a, fn, size_t(kRingSlotsFwd) * kSlotBytes, 0, 2,
-                                      kRingThreads, kBnL2BudgetRingFwd);
+        nrm_status st = bn_plan_ring(pl, a, fn, size_t(kEvSlotsFwd) * kSlotBytes, 0, 2, kEvThreads, 0.0);
         if (st != NRM_OK) return st;
-        return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads, false);
+        return launch_bn(fn, a, pl, ws, ws_bytes, s, kEvThreads, false);
     }
     // unaligned tensors, channel counts the group path cannot tile, empty channels
     const void* fn = training ? (const void*)&bn_fwd_kernel<T, 1, true> : (const void*)&bn_fwd_kernel<T, 1, false>;
@@ -1762,14 +1524,14 @@ nrm_status bn_bwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
     }
     if (vec && a.c > 0 && a.n * a.l > 0) {
         const void* fn = with_act(a.act, [&](auto act) {
-            return (const void*)&bn_bwd_ring_kernel<T, false, decltype(act)::value>;
+            return (const void*)&bn_bwd_eval_kernel<T, decltype(act)::value>;
         });
         BnPlan pl;
         bn_geometry(pl.g, a, kVec<T>);
-        const size_t smem = size_t(kRingSlotsBwd) * (kSlotBytes + kSlotMaskWords * sizeof(uint32_t));
-        nrm_status st = bn_plan_ring(pl, a, fn, smem, 0, 2, kRingThreads, kBnL2Budget);
+        const size_t smem = size_t(kEvSlotsBwd) * (kSlotBytes + kSlotMaskWords * sizeof(uint32_t));
+        nrm_status st = bn_plan_ring(pl, a, fn, smem, 0, 2, kEvThreads, 0.0);
         if (st != NRM_OK) return st;
-        return launch_bn(fn, a, pl, ws, ws_bytes, s, kRingThreads, false);
+        return launch_bn(fn, a, pl, ws, ws_bytes, s, kEvThreads, false);
     }
     const void* fn = training ? (const void*)&bn_bwd_kernel<T, 1, true> : (const void*)&bn_bwd_kernel<T, 1, false>;
     BnPlan pl;

@@ -66,129 +66,10 @@ constexpr int kTrProducer1 = 16;
 constexpr int kTrProducer2 = 17;
 constexpr int kTrBookkeeper = 18;
 
-// Waits for phase `parity` of `bar` for at most `limit_ns`; gives up at once
-// when another thread of the CTA has given up (*abort != 0), and sets *abort
-// when this wait runs out.  Called by every lane of a warp; the result is
-// warp-uniform.
-__device__ __forceinline__ bool tr_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, volatile int* abort) {
-    bool ok = mbar_try_wait(bar, parity);
-    if (!ok) {
-        const uint64_t t0 = global_timer_ns();
-        for (;;) {
-            if (mbar_try_wait(bar, parity)) {
-                ok = true;
-                break;
-            }
-            if (*abort) break;
-            if (global_timer_ns() - t0 > limit_ns) {
-                *abort = 1;
-                break;
-            }
-        }
-    }
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Producer (whole warp): one chunk of pass `ps`, blocks [cb, ce) of round r's
-// slice, into the next slot of `rg` once its consumers have released it.
-// False (nothing issued) when the wait for the slot gave up.
-template <typename T, int VE, int SLOTS>
-__device__ bool tr_produce_chunk(Ring<SLOTS>& rg, const Rounds& rd, int r, const RingPass<T>& ps, uint32_t cb,
-                                 uint32_t ce, int lane, volatile int* abort) {
-    const BnGeom& g = rd.g;
-    int64_t ch;
-    int s;
-    uint32_t b0, b1;
-    rd.range(r, ch, s, b0, b1);
-    const uint32_t span = chunk_span(ps.nt);
-    const int slot = rg.slot();
-    const uint32_t use = rg.use();
-    if (use > 0 && !tr_wait(&rg.empty[slot], (use - 1) & 1u, kBnWaitLimitNs, abort)) return false;
-    unsigned char* base = rg.data + size_t(slot) * kSlotBytes;
-    if (lane == 0) {
-        uint32_t bytes = 0;
-        for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
-            const uint32_t v_lo = (lo - n * g.nbs) * 32;
-            const uint32_t v_hi = min((hi - n * g.nbs) * 32, uint32_t(g.lv));
-            bytes += (v_hi - v_lo) * 16;
-        });
-        mbar_arrive_expect_tx(&rg.full[slot], bytes * uint32_t(ps.nt));
-        for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
-            const uint32_t v_lo = (lo - n * g.nbs) * 32;
-            const uint32_t v_hi = min((hi - n * g.nbs) * 32, uint32_t(g.lv));
-            const int64_t e = ((int64_t(n) * g.c + ch) * g.lv + v_lo) * VE;
-            const size_t off = size_t(lo - cb) * 512;
-            for (int t = 0; t < ps.nt; ++t)
-                bulk_g2s(base + size_t(t) * span * 512 + off, ps.t[t] + e, (v_hi - v_lo) * 16, &rg.full[slot],
-                         ps.pol[t]);
-        });
-    }
-    if (ps.mask) {
-        uint32_t* mw = rg.mask + size_t(slot) * kSlotMaskWords;
-        for_segments(g, cb, ce, [&](uint32_t n, uint32_t lo, uint32_t hi) {
-            const uint32_t w_lo = (lo - n * g.nbs) * VE;
-            const uint32_t w_hi = min((hi - n * g.nbs) * VE, uint32_t(g.words));
-            const uint32_t* src = ps.mask + (int64_t(n) * g.c + ch) * g.words;
-            uint32_t* dst = mw + (lo - cb) * VE;
-            for (uint32_t w = w_lo + lane; w < w_hi; w += 32) cp_async_4(dst + (w - w_lo), src + w);
-        });
-        cp_async_mbar_arrive_noinc(&rg.full[slot]);
-    }
-    ++rg.seq;
-    return true;
-}
-
-// Producer (whole warp): every chunk of round r's slice for pass `ps`.
-template <typename T, int VE, int SLOTS>
-__device__ bool tr_produce(Ring<SLOTS>& rg, const Rounds& rd, int r, const RingPass<T>& ps, int lane,
-                           volatile int* abort) {
-    int64_t ch;
-    int s;
-    uint32_t b0, b1;
-    rd.range(r, ch, s, b0, b1);
-    const uint32_t span = chunk_span(ps.nt);
-    for (uint32_t cb = b0; cb < b1; cb += span)
-        if (!tr_produce_chunk<T, VE>(rg, rd, r, ps, cb, b1 - cb < span ? b1 : cb + span, lane, abort)) return false;
-    return true;
-}
-
-// Producer, at the end: waits (bounded, whatever *abort says) until the last
-// copies issued into every slot have landed, so that no copy is in flight
-// when the CTA exits.  A slot's copies are issued only after its previous
-// phase completed, so its last phase completing covers all of them.
-template <int SLOTS>
-__device__ void tr_drain(Ring<SLOTS>& rg, bool& bad) {
-    for (int s = 0; s < SLOTS && s < rg.seq; ++s) {
-        const int last = s + ((rg.seq - 1 - s) / SLOTS) * SLOTS;  // last sequence number that used slot s
-        if (!mbar_wait_bounded(&rg.full[s], uint32_t(last / SLOTS) & 1u, kBnWaitLimitNs)) bad = true;
-    }
-}
-
-// Consumer (whole warp): the slot of the next chunk once it has landed, or -1
-// when the wait gave up.
-template <int SLOTS>
-__device__ __forceinline__ int tr_take(Ring<SLOTS>& rg, volatile int* abort) {
-    const int slot = rg.slot();
-    return tr_wait(&rg.full[slot], rg.use() & 1u, kBnWaitLimitNs, abort) ? slot : -1;
-}
-
-template <int SLOTS>
-__device__ __forceinline__ void tr_ring_init(Ring<SLOTS>& rg, uint32_t full_count, uint32_t empty_count) {
-    for (int i = 0; i < SLOTS; ++i) {
-        mbar_init(&rg.full[i], full_count);
-        mbar_init(&rg.empty[i], empty_count);
-    }
-}
-
 // Whether channel ch is complete (all S slices published), for a whole warp.
 // Once this CTA has given up on its peers (*lost) it no longer waits.
-__device__ __forceinline__ bool tr_channel_complete(const BnGeom& g, int64_t ch, bool lost) {
+__device__ __forceinline__ bool channel_complete(const BnGeom& g, int64_t ch, bool lost) {
     return __all_sync(0xffffffffu, lost || ld_acquire_u32(g.counters + ch) >= uint32_t(g.S) + g.peer_extra);
-}
-
-// Warp-uniform %globaltimer.
-__device__ __forceinline__ uint64_t tr_now() {
-    return __shfl_sync(0xffffffffu, (unsigned long long)global_timer_ns(), 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -213,10 +94,10 @@ static __device__ void tf_bookkeeper(const BnArgs& a, const BnGeom& g, const Rou
     int pre_r = -1;
     float pre_w = 1.f, pre_b = 0.f;
     bool lost = false, peer_wait = false;
-    uint64_t t_last = tr_now(), t_peer = 0;
+    uint64_t t_last = warp_now(), t_peer = 0;
     while ((q_pub < nr || r_mrg < nr) && !*abort) {
         bool moved = false;
-        const uint64_t now = tr_now();
+        const uint64_t now = warp_now();
         // a statistics pass: merge the team's warps, publish the CTA's partial
         if (q_pub < nr && __all_sync(0xffffffffu, mbar_test_wait(&sh.sums_ready[q_pub & 1], (q_pub >> 1) & 1))) {
             Moments m = lane < kTfStatsWarps ? sh.warp_m[q_pub & 1][lane] : Moments{0.f, 0.f, 0.f};
@@ -252,7 +133,7 @@ static __device__ void tf_bookkeeper(const BnArgs& a, const BnGeom& g, const Rou
                 pre_b = a.b ? a.b[ch] : 0.f;
                 pre_r = r_mrg;
             }
-            if (ok && g.S > 1 && !tr_channel_complete(g, ch, lost)) {
+            if (ok && g.S > 1 && !channel_complete(g, ch, lost)) {
                 ok = false;
                 if (!peer_wait) {
                     peer_wait = true;
@@ -329,8 +210,8 @@ bn_fwd_train_kernel(const BnArgs a, const BnGeom g) {
     bool bad = false;
 
     if (threadIdx.x == 0) {
-        tr_ring_init(rs, 1, kTfStatsWarps);
-        tr_ring_init(ra, 1, kTfApplyWarps);
+        ring_init(rs, 1, kTfStatsWarps);
+        ring_init(ra, 1, kTfApplyWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.sums_ready[i], kTfStatsWarps);
             mbar_init(&sh.sums_free[i], 1);
@@ -349,7 +230,7 @@ bn_fwd_train_kernel(const BnArgs a, const BnGeom g) {
         const uint32_t span = chunk_span(1);
         for (int q = 0; q < nr; ++q) {
             const int qd = q - kTfLag;
-            if (qd >= 0 && !tr_wait(&sh.apply_done[qd & 3], uint32_t(qd >> 2) & 1u, peer_limit, abort)) break;
+            if (qd >= 0 && !ring_wait(&sh.apply_done[qd & 3], uint32_t(qd >> 2) & 1u, peer_limit, abort)) break;
             int64_t ch;
             int s;
             uint32_t b0, b1;
@@ -358,7 +239,7 @@ bn_fwd_train_kernel(const BnArgs a, const BnGeom g) {
             bool ok = true;
             for (uint32_t cb = b0; cb < b1 && ok; cb += span) {
                 const uint32_t n = min(span, b1 - cb);
-                const int slot = tr_take(rs, abort);
+                const int slot = ring_take(rs, abort);
                 if (slot < 0) {
                     ok = false;
                     break;
@@ -379,7 +260,7 @@ bn_fwd_train_kernel(const BnArgs a, const BnGeom g) {
             if (!ok) break;
             Moments m = acc.moments();
             warp_merge(m);
-            if (q >= 2 && !tr_wait(&sh.sums_free[q & 1], uint32_t((q >> 1) - 1) & 1u, kBnWaitLimitNs, abort)) break;
+            if (q >= 2 && !ring_wait(&sh.sums_free[q & 1], uint32_t((q >> 1) - 1) & 1u, kBnWaitLimitNs, abort)) break;
             if (lane == 0) {
                 sh.warp_m[q & 1][warp] = m;
                 mbar_arrive(&sh.sums_ready[q & 1]);
@@ -391,7 +272,7 @@ bn_fwd_train_kernel(const BnArgs a, const BnGeom g) {
         const uint64_t pol_stream = l2_evict_first();
         const uint32_t span = chunk_span(res ? 2 : 1);
         for (int r = 0; r < nr; ++r) {
-            if (!tr_wait(&sh.coef_ready[r & 1], uint32_t(r >> 1) & 1u, peer_limit, abort)) break;
+            if (!ring_wait(&sh.coef_ready[r & 1], uint32_t(r >> 1) & 1u, peer_limit, abort)) break;
             const float2 sc = sh.coef[r & 1];
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.coef_free[r & 1]);
@@ -402,7 +283,7 @@ bn_fwd_train_kernel(const BnArgs a, const BnGeom g) {
             bool ok = true;
             for (uint32_t cb = b0; cb < b1; cb += span) {
                 const uint32_t n = min(span, b1 - cb);
-                const int slot = tr_take(ra, abort);
+                const int slot = ring_take(ra, abort);
                 if (slot < 0) {
                     ok = false;
                     break;
@@ -442,15 +323,15 @@ bn_fwd_train_kernel(const BnArgs a, const BnGeom g) {
         // ---------------- producer of the statistics pass ----------------
         const RingPass<T> stats{{x, nullptr, nullptr}, {l2_evict_last(), 0, 0}, 1, nullptr};
         for (int q = 0; q < nr; ++q)
-            if (!tr_produce<T, VE>(rs, rd, q, stats, lane, abort)) break;
-        tr_drain(rs, bad);
+            if (!ring_produce<T, VE>(rs, rd, q, stats, lane, abort)) break;
+        ring_drain(rs, bad);
     } else if (warp == kTrProducer2) {
         // ---------------- producer of the apply pass: x (L2) and the residual (HBM) ----------------
         const uint64_t pol = l2_evict_first();
         const RingPass<T> apply{{x, res, nullptr}, {pol, pol, 0}, res ? 2 : 1, nullptr};
         for (int r = 0; r < nr; ++r)
-            if (!tr_produce<T, VE>(ra, rd, r, apply, lane, abort)) break;
-        tr_drain(ra, bad);
+            if (!ring_produce<T, VE>(ra, rd, r, apply, lane, abort)) break;
+        ring_drain(ra, bad);
     } else {
         tf_bookkeeper(a, g, rd, nr, sh, lane);
     }
@@ -487,10 +368,10 @@ static __device__ void tb_bookkeeper(const BnArgs& a, const BnGeom& g, const Rou
     volatile int* abort = &sh.abort;
     int q_par = 0, q_pub = 0, r_mrg = 0;
     bool lost = false, peer_wait = false;
-    uint64_t t_last = tr_now(), t_peer = 0;
+    uint64_t t_last = warp_now(), t_peer = 0;
     while ((q_par < nr || q_pub < nr || r_mrg < nr) && !*abort) {
         bool moved = false;
-        const uint64_t now = tr_now();
+        const uint64_t now = warp_now();
         // channel parameters of round q_par
         if (q_par < nr) {
             const uint32_t u = uint32_t(q_par) >> 2;
@@ -550,7 +431,7 @@ static __device__ void tb_bookkeeper(const BnArgs& a, const BnGeom& g, const Rou
             int s;
             uint32_t b0, b1;
             rd.range(r_mrg, ch, s, b0, b1);
-            if (ok && g.S > 1 && !tr_channel_complete(g, ch, lost)) {
+            if (ok && g.S > 1 && !channel_complete(g, ch, lost)) {
                 ok = false;
                 if (!peer_wait) {
                     peer_wait = true;
@@ -629,8 +510,8 @@ bn_bwd_train_kernel(const BnArgs a, const BnGeom g) {
     bool bad = false;
 
     if (threadIdx.x == 0) {
-        tr_ring_init(r1, use_mask ? 33u : 1u, kTbP1Warps);
-        tr_ring_init(r2, use_mask ? 33u : 1u, kTbP2Warps);
+        ring_init(r1, use_mask ? 33u : 1u, kTbP1Warps);
+        ring_init(r2, use_mask ? 33u : 1u, kTbP2Warps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.sums_ready[i], kTbP1Warps);
             mbar_init(&sh.sums_free[i], 1);
@@ -654,8 +535,8 @@ bn_bwd_train_kernel(const BnArgs a, const BnGeom g) {
         const uint64_t pol_stream = l2_evict_first();
         for (int q = 0; q < nr; ++q) {
             const int qd = q - kTbLag;
-            if (qd >= 0 && !tr_wait(&sh.p2_done[qd & 3], uint32_t(qd >> 2) & 1u, peer_limit, abort)) break;
-            if (!tr_wait(&sh.par_ready[q & 3], uint32_t(q >> 2) & 1u, kBnWaitLimitNs, abort)) break;
+            if (qd >= 0 && !ring_wait(&sh.p2_done[qd & 3], uint32_t(qd >> 2) & 1u, peer_limit, abort)) break;
+            if (!ring_wait(&sh.par_ready[q & 3], uint32_t(q >> 2) & 1u, kBnWaitLimitNs, abort)) break;
             const float4 pr = sh.par[q & 3];
             int64_t ch;
             int s;
@@ -665,7 +546,7 @@ bn_bwd_train_kernel(const BnArgs a, const BnGeom g) {
             bool ok = true;
             for (uint32_t cb = b0; cb < b1; cb += span) {
                 const uint32_t n = min(span, b1 - cb);
-                const int slot = tr_take(r1, abort);
+                const int slot = ring_take(r1, abort);
                 if (slot < 0) {
                     ok = false;
                     break;
@@ -692,7 +573,7 @@ bn_bwd_train_kernel(const BnArgs a, const BnGeom g) {
             if (!ok) break;
             const FF d1 = ff_warp_sum(acc.ff_dz());
             const FF d2 = ff_warp_sum(acc.ff_dzc());
-            if (q >= 2 && !tr_wait(&sh.sums_free[q & 1], uint32_t((q >> 1) - 1) & 1u, kBnWaitLimitNs, abort)) break;
+            if (q >= 2 && !ring_wait(&sh.sums_free[q & 1], uint32_t((q >> 1) - 1) & 1u, kBnWaitLimitNs, abort)) break;
             if (lane == 0) {
                 sh.warp_s[q & 1][warp] = make_float4(d1.hi, d1.lo, d2.hi, d2.lo);
                 mbar_arrive(&sh.sums_ready[q & 1]);
@@ -703,10 +584,10 @@ bn_bwd_train_kernel(const BnArgs a, const BnGeom g) {
         const int pw = warp - kTbP1Warps;
         const uint64_t pol_stream = l2_evict_first();
         for (int r = 0; r < nr; ++r) {
-            if (!tr_wait(&sh.par_ready[r & 3], uint32_t(r >> 2) & 1u, peer_limit, abort)) break;
+            if (!ring_wait(&sh.par_ready[r & 3], uint32_t(r >> 2) & 1u, peer_limit, abort)) break;
             const float4 pr = sh.par[r & 3];
             const float mu = pr.x, rs = pr.y, scale = pr.z, shift = pr.w;
-            if (!tr_wait(&sh.coef_ready[r & 1], uint32_t(r >> 1) & 1u, peer_limit, abort)) break;
+            if (!ring_wait(&sh.coef_ready[r & 1], uint32_t(r >> 1) & 1u, peer_limit, abort)) break;
             const float2 cc = sh.coef[r & 1];
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.coef_free[r & 1]);
@@ -717,7 +598,7 @@ bn_bwd_train_kernel(const BnArgs a, const BnGeom g) {
             bool ok = true;
             for (uint32_t cb = b0; cb < b1; cb += span) {
                 const uint32_t n = min(span, b1 - cb);
-                const int slot = tr_take(r2, abort);
+                const int slot = ring_take(r2, abort);
                 if (slot < 0) {
                     ok = false;
                     break;
@@ -757,15 +638,15 @@ bn_bwd_train_kernel(const BnArgs a, const BnGeom g) {
         const uint64_t pol = l2_evict_last();
         const RingPass<T> first{{dy, x, res}, {pol, pol, pol}, nt, use_mask ? a.mask_in : nullptr};
         for (int q = 0; q < nr; ++q)
-            if (!tr_produce<T, VE>(r1, rd, q, first, lane, abort)) break;
-        tr_drain(r1, bad);
+            if (!ring_produce<T, VE>(r1, rd, q, first, lane, abort)) break;
+        ring_drain(r1, bad);
     } else if (warp == kTrProducer2) {
         // ---------------- producer of pass 2 (L2 re-reads) ----------------
         const uint64_t pol = l2_evict_first();
         const RingPass<T> second{{dy, x, res}, {pol, pol, pol}, nt, use_mask ? a.mask_in : nullptr};
         for (int r = 0; r < nr; ++r)
-            if (!tr_produce<T, VE>(r2, rd, r, second, lane, abort)) break;
-        tr_drain(r2, bad);
+            if (!ring_produce<T, VE>(r2, rd, r, second, lane, abort)) break;
+        ring_drain(r2, bad);
     } else {
         tb_bookkeeper(a, g, rd, nr, sh, lane);
     }
