@@ -8,16 +8,19 @@
 // form a span of G*l elements that starts and ends on a 16-byte boundary, so a
 // channel group is n such spans at a fixed stride.  A thread-block cluster of
 // Q CTAs owns a group: each CTA bulk-copies its n/Q samples' spans into
-// shared memory, reduces its per-channel partials, the cluster merges the Q
-// partials through distributed shared memory in rank order (every CTA gets
-// the same bits), and each CTA writes its outputs from shared memory with
-// 16-byte stores.  Every input byte is read once.
+// shared memory, reduces its per-channel partials and pushes them into every
+// cluster CTA's shared memory (distributed shared memory stores, after a
+// split cluster barrier that every CTA arrived on at start), one cluster
+// barrier later each CTA merges the Q partials in rank order (every CTA gets
+// the same bits), and writes its outputs from shared memory with 16-byte
+// stores.  Every input byte is read once.
 #pragma once
 
 namespace nrm {
 
 constexpr int kGrpThreads = 256;
 constexpr int kGrpWarps = kGrpThreads / 32;
+constexpr int kGrpMaxQ = 8;  // CTAs per cluster, at most
 
 struct GrpGeom {
     int64_t c;
@@ -85,15 +88,37 @@ __device__ __forceinline__ void grp_vec(const unsigned char* tile, int e, float 
     unpack<T, kVec<T>>(pk, v);
 }
 
+// Element walk of one channel's part of a CTA's tile: element t of the
+// channel's ns*l elements (sample-major) is element e of sample s, and the
+// walk advances t by a fixed step with one integer division at the start.
+struct GrpWalk {
+    int s, e, s_step, e_step;
+    __device__ __forceinline__ GrpWalk(int t0, int step, int l) {
+        s = t0 / l;
+        e = t0 - s * l;
+        s_step = step / l;
+        e_step = step - s_step * l;
+    }
+    __device__ __forceinline__ void next(int l) {
+        e += e_step;
+        s += s_step;
+        if (e >= l) {
+            e -= l;
+            ++s;
+        }
+    }
+};
+
 template <typename T, bool TRAIN, int ACT>
 __global__ void __launch_bounds__(kGrpThreads)
 bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
     constexpr int VE = kVec<T>;
+    using bits = typename Io<T>::bits_t;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bar;
     __shared__ Moments wm[kGrpWarps];
-    __shared__ float4 part[kGrpWarps];  // this CTA's (n, mean, m2) per channel, read by the cluster
-    __shared__ float2 coef[kGrpWarps];  // (scale, shift) per channel
+    __shared__ float4 allp[kGrpMaxQ][kGrpWarps];  // (n, mean, m2) per channel of every cluster CTA, pushed by it
+    __shared__ float2 coef[kGrpWarps];            // (scale, shift) per channel
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
@@ -103,6 +128,7 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
     const unsigned char* tx = smem;
     const unsigned char* tr = smem + g.tile;
 
+    if constexpr (TRAIN) cluster_arrive_relaxed();  // this CTA has started
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
         mbar_init_fence();
@@ -118,26 +144,30 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
         // short even when l is 1
         const int j = warp % g.G;
         const int wpc = kGrpWarps / g.G;  // warps per channel
+        const bits* tb = reinterpret_cast<const bits*>(tx) + j * g.l;
         ShiftedSums acc;
+        GrpWalk wk((warp / g.G) * 32 + lane, wpc * 32, g.l);
         for (int t = (warp / g.G) * 32 + lane; t < p.ns * g.l; t += wpc * 32) {
-            const int s = int(fast_div(uint32_t(t), g.div_l));
-            const float v[1] = {grp_elem<T>(tx, s * g.span + j * g.l + (t - s * g.l))};
+            const float v[1] = {Io<T>::load(tb[wk.s * g.span + wk.e])};
             acc.add(v);
+            wk.next(g.l);
         }
         Moments m = acc.moments();
         warp_merge(m);
         if (lane == 0) wm[warp] = m;
         __syncthreads();
+        cluster_wait();  // every CTA of the cluster has started: its shared memory may be written
         if (threadIdx.x < g.G) {
             Moments t = wm[threadIdx.x];
             for (int w = threadIdx.x + g.G; w < kGrpWarps; w += g.G) chan_merge(t, wm[w].n, wm[w].mean, wm[w].m2);
-            part[threadIdx.x] = make_float4(t.n, t.mean, t.m2, 0.f);
+            const float4 pv = make_float4(t.n, t.mean, t.m2, 0.f);
+            for (int r = 0; r < g.Q; ++r) st_dsmem_f4(dsmem_addr(&allp[p.rank][threadIdx.x], uint32_t(r)), pv);
         }
-        cluster_sync_all();
+        cluster_sync_all();  // every CTA's partials have landed in every CTA
         if (threadIdx.x < g.G) {
             Moments tot{0.f, 0.f, 0.f};
             for (int r = 0; r < g.Q; ++r) {
-                const float4 pv = ld_dsmem_f4(dsmem_addr(&part[threadIdx.x], uint32_t(r)));
+                const float4 pv = allp[r][threadIdx.x];
                 chan_merge(tot, pv.x, pv.y, pv.z);
             }
             const int64_t ch = p.ch0 + threadIdx.x;
@@ -152,7 +182,6 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
                 if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * a.rv[ch]);
             }
         }
-        cluster_sync_all();  // every CTA has read the partials before any moves on
     } else {
         if (threadIdx.x < g.G) {
             const int64_t ch = p.ch0 + threadIdx.x;
@@ -180,13 +209,15 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
         if (res) grp_vec<T>(tr, s * g.span + o, rv);
         int j = int(fast_div(uint32_t(o), g.div_l));
         int next = (j + 1) * g.l;
+        float2 cs = coef[j];  // the vector may cross into the next channel(s): reloaded there
 #pragma unroll
         for (int k = 0; k < VE; ++k) {
             if (o + k == next) {
                 ++j;
                 next += g.l;
+                cs = coef[j];
             }
-            float z = fmaf(xv[k], coef[j].x, coef[j].y);
+            float z = fmaf(xv[k], cs.x, cs.y);
             if (res) z += rv[k];
             ov[k] = act_forward_c<ACT>(z, a.act_param, a.act);
         }
@@ -197,12 +228,13 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
         for (int sg = warp; sg < p.ns * g.G; sg += kGrpWarps) {
             const int s = sg / g.G;
             const int j = sg - s * g.G;
+            const float2 cs = coef[j];
             uint32_t* mw = a.mask + (int64_t(p.n0 + s) * g.c + p.ch0 + j) * g.words;
             for (int wi = 0; wi < g.words; ++wi) {
                 const int e = wi * 32 + lane;
                 bool pos = false;
                 if (e < g.l) {
-                    float z = fmaf(grp_elem<T>(tx, s * g.span + j * g.l + e), coef[j].x, coef[j].y);
+                    float z = fmaf(grp_elem<T>(tx, s * g.span + j * g.l + e), cs.x, cs.y);
                     if (res) z += grp_elem<T>(tr, s * g.span + j * g.l + e);
                     pos = z > 0.f;
                 }
@@ -222,12 +254,13 @@ template <typename T, bool TRAIN, int ACT>
 __global__ void __launch_bounds__(kGrpThreads)
 bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     constexpr int VE = kVec<T>;
+    using bits = typename Io<T>::bits_t;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bar;
     __shared__ double2 ws[kGrpWarps];
-    __shared__ double2 part[kGrpWarps];  // this CTA's (sum dz, sum dz*x) per channel, read by the cluster
-    __shared__ float4 prm[kGrpWarps];    // (mean, rstd, scale, shift) per channel
-    __shared__ float2 coef[kGrpWarps];   // dx coefficients (c1, c2) per channel
+    __shared__ double2 allp[kGrpMaxQ][kGrpWarps];  // (sum dz, sum dz*(x - mean)) per channel of every cluster CTA
+    __shared__ float4 prm[kGrpWarps];              // (mean, rstd, scale, shift) per channel
+    __shared__ float2 coef[kGrpWarps];             // dx coefficients (c1, c2) per channel
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
@@ -245,6 +278,7 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     float* tz = reinterpret_cast<float*>(smem + (with_res ? 3 : 2) * size_t(g.tile));  // dz, fp32
     uint32_t* tm = reinterpret_cast<uint32_t*>(tz + size_t(g.spc) * g.span);            // mask words
 
+    cluster_arrive_relaxed();  // this CTA has started
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
         mbar_init_fence();
@@ -271,60 +305,67 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     if (p.ns > 0 && !mbar_wait_bounded(&bar, 0, kBnWaitLimitNs)) bad = true;
     __syncthreads();
 
-    // dz of element e of segment (s, j)
-    auto dz_of = [&](int s, int j, int e, float dyv, float xv, float rv) {
-        if (use_mask) return ((tm[(s * g.G + j) * g.words + (e >> 5)] >> (e & 31)) & 1u) ? dyv : 0.f;
-        if (need_z) return dyv * act_derivative_c<ACT>(fmaf(xv, prm[j].z, prm[j].w) + rv, a.act_param, a.act);
-        return dyv;
-    };
-
-    // ---- the two channel sums: warp w takes channel w % G ----
+    // ---- dz (kept in shared memory) and the two channel sums: warp w takes channel w % G ----
     {
         const int j = warp % g.G;
         const int wpc = kGrpWarps / g.G;
-        GradSums acc(prm[j].x);
+        const float4 pr = prm[j];
+        const bits* bdy = reinterpret_cast<const bits*>(tdy) + j * g.l;
+        const bits* bx = reinterpret_cast<const bits*>(tx) + j * g.l;
+        const bits* br = reinterpret_cast<const bits*>(tr) + j * g.l;
+        float* zj = tz + j * g.l;
+        const uint32_t* mj = tm + j * g.words;
+        GradSums acc(pr.x);
+        GrpWalk wk((warp / g.G) * 32 + lane, wpc * 32, g.l);
         for (int t = (warp / g.G) * 32 + lane; t < p.ns * g.l; t += wpc * 32) {
-            const int s = int(fast_div(uint32_t(t), g.div_l));
-            const int e = t - s * g.l;
-            const int idx = s * g.span + j * g.l + e;
-            const float xv[1] = {grp_elem<T>(tx, idx)};
-            const float rv = with_res ? grp_elem<T>(tr, idx) : 0.f;
-            const float dz[1] = {dz_of(s, j, e, grp_elem<T>(tdy, idx), xv[0], rv)};
-            tz[idx] = dz[0];
+            const int idx = wk.s * g.span + wk.e;
+            const float dyv = Io<T>::load(bdy[idx]);
+            const float xv[1] = {Io<T>::load(bx[idx])};
+            float dz[1];
+            if (use_mask) {
+                dz[0] = ((mj[wk.s * g.G * g.words + (wk.e >> 5)] >> (wk.e & 31)) & 1u) ? dyv : 0.f;
+            } else if (need_z) {
+                const float rv = with_res ? Io<T>::load(br[idx]) : 0.f;
+                dz[0] = dyv * act_derivative_c<ACT>(fmaf(xv[0], pr.z, pr.w) + rv, a.act_param, a.act);
+            } else {
+                dz[0] = dyv;
+            }
+            zj[idx] = dz[0];
             acc.add(dz, xv);
+            wk.next(g.l);
         }
         const FF d1 = ff_warp_sum(acc.ff_dz());
         const FF d2 = ff_warp_sum(acc.ff_dzc());
         if (lane == 0) ws[warp] = make_double2(ff_to_double(d1), ff_to_double(d2));
     }
     __syncthreads();
+    cluster_wait();  // every CTA of the cluster has started: its shared memory may be written
     if (threadIdx.x < g.G) {
         double2 t = ws[threadIdx.x];
         for (int w = threadIdx.x + g.G; w < kGrpWarps; w += g.G) {
             t.x += ws[w].x;
             t.y += ws[w].y;
         }
-        part[threadIdx.x] = t;
+        for (int r = 0; r < g.Q; ++r) st_dsmem_d2(dsmem_addr(&allp[p.rank][threadIdx.x], uint32_t(r)), t);
     }
-    cluster_sync_all();
+    cluster_sync_all();  // every CTA's partials have landed in every CTA
     if (threadIdx.x < g.G) {
         double t1 = 0.0, t2 = 0.0;
         for (int r = 0; r < g.Q; ++r) {
-            const double2 pv = ld_dsmem_d2(dsmem_addr(&part[threadIdx.x], uint32_t(r)));
+            const double2 pv = allp[r][threadIdx.x];
             t1 += pv.x;
             t2 += pv.y;
         }
         const int64_t ch = p.ch0 + threadIdx.x;
         const float4 pr = prm[threadIdx.x];
         // t2 is sum dz*(x - mean), centred on the saved mean as it was summed
-        const double t2c = t2;
         if (p.rank == 0) {
             if (a.db) a.db[ch] = float(t1);
-            if (a.dw) a.dw[ch] = float(t2c * double(pr.y));
+            if (a.dw) a.dw[ch] = float(t2 * double(pr.y));
         }
-        coef[threadIdx.x] = make_float2(float(t1 * double(g.inv_m)), float(t2c * double(pr.y) * double(g.inv_m)));
+        coef[threadIdx.x] = make_float2(float(t1 * double(g.inv_m)), float(t2 * double(pr.y) * double(g.inv_m)));
     }
-    cluster_sync_all();  // every CTA has read the partials before any moves on
+    __syncthreads();
 
     // ---- dres, dx: 16 bytes per thread and step ----
     const uint64_t pol = l2_evict_first();
@@ -348,16 +389,19 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
         }
         int j = int(fast_div(uint32_t(o), g.div_l));
         int next = (j + 1) * g.l;
+        float4 pr = prm[j];  // the vector may cross into the next channel(s): reloaded there
+        float2 cc = coef[j];
 #pragma unroll
         for (int k = 0; k < VE; ++k) {
             if (o + k == next) {
                 ++j;
                 next += g.l;
+                pr = prm[j];
+                cc = coef[j];
             }
-            const float4 pr = prm[j];
             if (TRAIN) {
                 const float xh = (xv[k] - pr.x) * pr.y;
-                ov[k] = pr.z * (dzv[k] - coef[j].x - xh * coef[j].y);
+                ov[k] = pr.z * (dzv[k] - cc.x - xh * cc.y);
             } else {
                 ov[k] = dzv[k] * pr.z;
             }
@@ -416,7 +460,7 @@ inline bool bn_plan_group(GrpPlan& pl, const BnArgs& a, size_t es, int nt, bool 
     const size_t span_bytes = size_t(g.span) * es;
     const size_t cap = size_t(d->max_smem_optin) - 4096;  // room for the static shared memory
     int chosen = 0;
-    for (int Q = 1; Q <= 8; Q *= 2) {
+    for (int Q = 1; Q <= kGrpMaxQ; Q *= 2) {
         if (Q > a.n) break;
         const int64_t spc = (a.n + Q - 1) / Q;
         const size_t tile = (size_t(spc) * span_bytes + 127) / 128 * 128;

@@ -347,6 +347,21 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
     return a;
 }
+// Split cluster barrier: arrive (relaxed: orders nothing) now, wait later.
+// A CTA may write a peer's shared memory only once every CTA of the cluster
+// has started, which the arrive at kernel start / wait before the first remote
+// write establishes.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+__device__ __forceinline__ void st_dsmem_f4(uint32_t a, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" :: "r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_dsmem_d2(uint32_t a, double2 v) {
+    asm volatile("st.shared::cluster.v2.f64 [%0], {%1,%2};" :: "r"(a), "d"(v.x), "d"(v.y) : "memory");
+}
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t a) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
