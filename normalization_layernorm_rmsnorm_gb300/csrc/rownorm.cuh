@@ -51,7 +51,9 @@ constexpr int kRowWideBlock = 1024;   // threads per CTA of the wide-row kernels
 constexpr int kRowMaxFwdTpr = 1024;
 constexpr int kRowMaxBwdTpr = 512;
 
-__host__ __device__ constexpr int row_fwd_block(int tpr) { return tpr > 256 ? tpr : 256; }
+// Threads per forward CTA: 128 for rows of up to 128 threads (finer occupancy
+// steps: measured faster than 256 on the ViT-B LayerNorm and LLaMA RMSNorm rows).
+__host__ __device__ constexpr int row_fwd_block(int tpr) { return tpr > 128 ? (tpr > 256 ? tpr : 256) : 128; }
 
 // Sum of NV values over the TPR threads of row group `group`.  For TPR > 32
 // the per-warp sums meet in shared memory `buf` ([2][TPR/32][NV] floats for
@@ -195,10 +197,34 @@ row_fwd_kernel(const RowArgs a) {
 
     const int64_t stride = int64_t(gridDim.x) * RPC;
     int64_t row = int64_t(blockIdx.x) * RPC + group;
+    const float inv_cols = 1.f / fcols;  // mean = sum * (1/cols): one division per thread
     if constexpr (VE > 1) {
         // 16-byte vectors: the element arithmetic on fp32 pairs, and the next
         // row of the group loaded while this one is normalised
         constexpr int H = VE / 2;
+        // this thread's columns of w and b, the same for every row: for one-warp
+        // rows (short rows, where per-row work is small) loaded once and kept
+        // packed; wider rows reload them per row (registers for occupancy)
+        constexpr bool kHoist = TPR == 32;
+        Pack<T, VE> wpk[kHoist ? VPT : 1], bpk[kHoist ? VPT : 1];
+        if constexpr (kHoist) {
+            Pack<T, VE> one, zero;
+#pragma unroll
+            for (int k = 0; k < VE; ++k) {
+                one.b[k] = Io<T>::store(1.f);
+                zero.b[k] = Io<T>::store(0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int vi = j * TPR + t;
+                wpk[j] = one;
+                bpk[j] = zero;
+                if (vi < nvec) {
+                    if (a.w) wpk[j].u = ld_cached_v4(reinterpret_cast<const T*>(a.w) + int64_t(vi) * VE);
+                    if (a.b) bpk[j].u = ld_cached_v4(reinterpret_cast<const T*>(a.b) + int64_t(vi) * VE);
+                }
+            }
+        }
         Pack<T, VE> xp[VPT];
         if (row < a.rows) load_row<T, TPR, VPT, VE>(x, row, cols, t, xp);
         for (; row < a.rows; row += stride) {
@@ -218,7 +244,7 @@ row_fwd_kernel(const RowArgs a) {
                     for (int h = 0; h < H; ++h) s2 = __fadd2_rn(s2, xv[j][h]);
                 float s[1] = {s2.x + s2.y};
                 group_sum<TPR, 1>(s, &red[group][0], phase, group);
-                mu = s[0] / fcols;
+                mu = s[0] * inv_cols;
                 const float2 nmu = f2(-mu);
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
@@ -238,7 +264,7 @@ row_fwd_kernel(const RowArgs a) {
             }
             float q[1] = {q2.x + q2.y};
             group_sum<TPR, 1>(q, &red[group][0], phase, group);
-            const float rs = rsqrtf(q[0] / fcols + a.eps);
+            const float rs = rsqrtf(q[0] * inv_cols + a.eps);
             if (t == 0) {
                 if (LN && a.mean) a.mean[row] = mu;
                 if (a.rstd) a.rstd[row] = rs;
@@ -249,17 +275,22 @@ row_fwd_kernel(const RowArgs a) {
                 const int vi = j * TPR + t;
                 if (vi < nvec) {
                     float2 wv[H], bv[H], o[H];
-                    if (a.w) {
-                        unpack2<T>(ld_cached_v4(reinterpret_cast<const T*>(a.w) + int64_t(vi) * VE), wv);
+                    if constexpr (kHoist) {
+                        unpack2<T>(wpk[j].u, wv);
+                        unpack2<T>(bpk[j].u, bv);  // LayerNorm's bias, or RMSNorm's optional one (else 0)
                     } else {
+                        if (a.w) {
+                            unpack2<T>(ld_cached_v4(reinterpret_cast<const T*>(a.w) + int64_t(vi) * VE), wv);
+                        } else {
 #pragma unroll
-                        for (int h = 0; h < H; ++h) wv[h] = f2(1.f);
-                    }
-                    if (a.b) {  // LayerNorm's bias, or RMSNorm's optional one
-                        unpack2<T>(ld_cached_v4(reinterpret_cast<const T*>(a.b) + int64_t(vi) * VE), bv);
-                    } else {
+                            for (int h = 0; h < H; ++h) wv[h] = f2(1.f);
+                        }
+                        if (a.b) {  // LayerNorm's bias, or RMSNorm's optional one
+                            unpack2<T>(ld_cached_v4(reinterpret_cast<const T*>(a.b) + int64_t(vi) * VE), bv);
+                        } else {
 #pragma unroll
-                        for (int h = 0; h < H; ++h) bv[h] = f2(0.f);
+                            for (int h = 0; h < H; ++h) bv[h] = f2(0.f);
+                        }
                     }
 #pragma unroll
                     for (int h = 0; h < H; ++h) o[h] = __ffma2_rn(__fmul2_rn(xv[j][h], rs2), wv[h], bv[h]);
@@ -281,7 +312,7 @@ row_fwd_kernel(const RowArgs a) {
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) s[0] += elem(xp[j], 0);
                 group_sum<TPR, 1>(s, &red[group][0], phase, group);
-                mu = s[0] / fcols;
+                mu = s[0] * inv_cols;
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
                     if (j * TPR + t < nvec) {
@@ -294,7 +325,7 @@ row_fwd_kernel(const RowArgs a) {
                 for (int j = 0; j < VPT; ++j) q[0] = fmaf(elem(xp[j], 0), elem(xp[j], 0), q[0]);
             }
             group_sum<TPR, 1>(q, &red[group][0], phase, group);
-            const float rs = rsqrtf(q[0] / fcols + a.eps);
+            const float rs = rsqrtf(q[0] * inv_cols + a.eps);
             if (t == 0) {
                 if (LN && a.mean) a.mean[row] = mu;
                 if (a.rstd) a.rstd[row] = rs;

@@ -195,6 +195,7 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
         const int cols = a.cols;
         const int nvec = cols / VE;
         const float fcols = float(cols);
+        const float inv_cols = 1.f / fcols;
         const size_t row_bytes = size_t(cols) * sizeof(T);
         T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
         int phase = 0;
@@ -251,8 +252,8 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
 #pragma unroll
                 for (int i = 0; i < NV; ++i) s[i] = s2[i].x + s2[i].y;
                 group_sum<TPR, NV>(s, &red[group][0], phase, group);
-                const float c1 = s[0] / fcols;
-                const float c2 = LN ? s[NV - 1] / fcols : c1 * rs * rs;
+                const float c1 = s[0] * inv_cols;
+                const float c2 = LN ? s[NV - 1] * inv_cols : c1 * rs * rs;
                 const float2 nc1 = f2(-c1);
                 const float2 nc2 = f2(-c2);
                 T* dxr = dx + (r0 + r) * cols;
