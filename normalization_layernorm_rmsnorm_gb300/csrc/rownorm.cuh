@@ -178,7 +178,9 @@ __device__ __forceinline__ float2 f2neg(float2 v) { return make_float2(-v.x, -v.
 // ---------------------------------------------------------------------------
 // forward, rows held in registers
 // ---------------------------------------------------------------------------
-template <typename T, bool LN, int TPR, int VE, int VPT = kRowFwdVpt>
+// TO: the output's storage type (T, or float for a 16-bit input whose output
+// is kept in float32).
+template <typename T, bool LN, int TPR, int VE, int VPT = kRowFwdVpt, typename TO = T>
 __global__ void __launch_bounds__(row_fwd_block(TPR))
 row_fwd_kernel(const RowArgs a) {
     constexpr int BLOCK = row_fwd_block(TPR);
@@ -192,7 +194,7 @@ row_fwd_kernel(const RowArgs a) {
     const int nvec = cols / VE;
     const float fcols = float(cols);
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
-    T* __restrict__ y = reinterpret_cast<T*>(a.y);
+    TO* __restrict__ y = reinterpret_cast<TO*>(a.y);
     int phase = 0;
 
     const int64_t stride = int64_t(gridDim.x) * RPC;
@@ -230,7 +232,7 @@ row_fwd_kernel(const RowArgs a) {
         for (; row < a.rows; row += stride) {
             Pack<T, VE> xn[VPT];
             if (row + stride < a.rows) load_row<T, TPR, VPT, VE>(x, row + stride, cols, t, xn);
-            T* yr = y + row * cols;
+            TO* yr = y + row * cols;
             float2 xv[VPT][H];
 #pragma unroll
             for (int j = 0; j < VPT; ++j) unpack2<T>(xp[j].u, xv[j]);
@@ -294,7 +296,15 @@ row_fwd_kernel(const RowArgs a) {
                     }
 #pragma unroll
                     for (int h = 0; h < H; ++h) o[h] = __ffma2_rn(__fmul2_rn(xv[j][h], rs2), wv[h], bv[h]);
-                    st_v4(yr + int64_t(vi) * VE, pack2x<T>(o));
+                    if constexpr (sizeof(TO) == sizeof(T)) {
+                        st_v4(yr + int64_t(vi) * VE, pack2x<T>(o));
+                    } else {  // float32 output of a 16-bit input: two 16-byte stores
+                        st_v4(yr + int64_t(vi) * VE, make_uint4(__float_as_uint(o[0].x), __float_as_uint(o[0].y),
+                                                                __float_as_uint(o[1].x), __float_as_uint(o[1].y)));
+                        st_v4(yr + int64_t(vi) * VE + 4,
+                              make_uint4(__float_as_uint(o[2].x), __float_as_uint(o[2].y), __float_as_uint(o[3].x),
+                                         __float_as_uint(o[3].y)));
+                    }
                 }
             }
 #pragma unroll
@@ -304,7 +314,7 @@ row_fwd_kernel(const RowArgs a) {
         for (; row < a.rows; row += stride) {
             Pack<T, VE> xp[VPT];
             load_row<T, TPR, VPT, VE>(x, row, cols, t, xp);
-            T* yr = y + row * cols;
+            TO* yr = y + row * cols;
             float mu = 0.f;
             float q[1] = {0.f};
             if constexpr (LN) {
@@ -338,7 +348,7 @@ row_fwd_kernel(const RowArgs a) {
                     load_param<T, 1>(a.w, vi, wv, 1.f);
                     load_param<T, 1>(a.b, vi, bv, 0.f);
                     o[0] = fmaf((elem(xp[j], 0) - mu) * rs, wv[0], bv[0]);
-                    store_vec<T, 1>(yr + vi, o);
+                    store_vec<TO, 1>(yr + vi, o);
                 }
             }
         }
@@ -810,7 +820,7 @@ namespace nrm {
 // Plan of a backward ring kernel: TPR (rows of at most kRrVpt*512 vectors), R rows per
 // chunk (a multiple of the row groups per CTA, about 48 KB per slot) and at
 // least three slots where they fit.  False when the row does not suit.
-inline bool rr_plan(RrGeom& g, int& tpr, size_t& smem, const RowArgs& a, size_t es, bool ln) {
+inline bool rr_plan(RrGeom& g, int& tpr, size_t& smem, const RowArgs& a, size_t es, bool ln, size_t es_dy) {
     const DevInfo* d = dev_info();
     if (!d || a.rows <= 0) return false;
     const int nvec = int(size_t(a.cols) * es / 16);
@@ -818,19 +828,18 @@ inline bool rr_plan(RrGeom& g, int& tpr, size_t& smem, const RowArgs& a, size_t 
     while (tpr * kRrVpt < nvec && tpr < kRrConsumers) tpr *= 2;
     if (tpr * kRrVpt < nvec) return false;
     const int rpc = kRrConsumers / tpr;
-    const size_t row_bytes = size_t(a.cols) * es;
-    const int nt = 2;  // dy, x
+    const size_t row_bytes = size_t(a.cols) * (es + es_dy);  // a row of dy and a row of x
     const size_t param = (size_t(a.cols) * 4 + 127) / 128 * 128;
     const size_t cap = size_t(d->max_smem_optin) - 4096;  // room for the static shared memory
     if (param >= cap) return false;
     const size_t avail = cap - param;
-    int m = int(49152 / (size_t(nt) * rpc * row_bytes));
+    int m = int(49152 / (size_t(rpc) * row_bytes));
     if (m < 1) m = 1;
     size_t slot = 0;
     int slots = 0;
     for (;; --m) {
         const size_t R = size_t(m) * rpc;
-        slot = (size_t(nt) * R * row_bytes + R * 4 * (ln ? 2 : 1) + 127) / 128 * 128;
+        slot = (R * row_bytes + R * 4 * (ln ? 2 : 1) + 127) / 128 * 128;
         slots = int(avail / slot < size_t(kRrMaxSlots) ? avail / slot : size_t(kRrMaxSlots));
         if (slots >= 3 || m == 1) break;
     }
@@ -844,22 +853,22 @@ inline bool rr_plan(RrGeom& g, int& tpr, size_t& smem, const RowArgs& a, size_t 
     return true;
 }
 
-template <typename T, bool LN, bool DB, int VPT>
+template <typename T, bool LN, bool DB, int VPT, typename TD>
 const void* rr_fn_v(int tpr) {
     switch (tpr) {
-    case 32: return (const void*)&row_bwd_ring_kernel<T, LN, 32, DB, VPT>;
-    case 64: return (const void*)&row_bwd_ring_kernel<T, LN, 64, DB, VPT>;
-    case 128: return (const void*)&row_bwd_ring_kernel<T, LN, 128, DB, VPT>;
-    case 256: return (const void*)&row_bwd_ring_kernel<T, LN, 256, DB, VPT>;
-    default: return (const void*)&row_bwd_ring_kernel<T, LN, 512, DB, VPT>;
+    case 32: return (const void*)&row_bwd_ring_kernel<T, LN, 32, DB, VPT, TD>;
+    case 64: return (const void*)&row_bwd_ring_kernel<T, LN, 64, DB, VPT, TD>;
+    case 128: return (const void*)&row_bwd_ring_kernel<T, LN, 128, DB, VPT, TD>;
+    case 256: return (const void*)&row_bwd_ring_kernel<T, LN, 256, DB, VPT, TD>;
+    default: return (const void*)&row_bwd_ring_kernel<T, LN, 512, DB, VPT, TD>;
     }
 }
 
 // The ring kernel for rows of `nvec` vectors at TPR threads per row: 3
 // vectors per thread when that covers the row, else 4.
-template <typename T, bool LN, bool DB>
+template <typename T, bool LN, bool DB, typename TD = T>
 const void* rr_fn(int tpr, int nvec) {
-    return nvec <= 3 * tpr ? rr_fn_v<T, LN, DB, 3>(tpr) : rr_fn_v<T, LN, DB, kRrVpt>(tpr);
+    return nvec <= 3 * tpr ? rr_fn_v<T, LN, DB, 3, TD>(tpr) : rr_fn_v<T, LN, DB, kRrVpt, TD>(tpr);
 }
 
 // Launches a ring kernel on `grid` CTAs (one per SM at most).
@@ -874,28 +883,28 @@ inline nrm_status rr_launch(const void* fn, const RowArgs& a, const RrGeom& g, s
     return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(kRrThreads), kargs, smem, s), "row ring launch");
 }
 
-template <typename T, bool LN, int VE, int VPT>
+template <typename T, bool LN, int VE, int VPT, typename TO>
 const void* row_fwd_fn_v(int tpr) {
     switch (tpr) {
-    case 32: return (const void*)&row_fwd_kernel<T, LN, 32, VE, VPT>;
-    case 64: return (const void*)&row_fwd_kernel<T, LN, 64, VE, VPT>;
-    case 128: return (const void*)&row_fwd_kernel<T, LN, 128, VE, VPT>;
-    case 256: return (const void*)&row_fwd_kernel<T, LN, 256, VE, VPT>;
-    case 512: return (const void*)&row_fwd_kernel<T, LN, 512, VE, VPT>;
-    case 1024: return (const void*)&row_fwd_kernel<T, LN, 1024, VE, VPT>;
-    default: return (const void*)&row_fwd_wide_kernel<T, LN, VE>;
+    case 32: return (const void*)&row_fwd_kernel<T, LN, 32, VE, VPT, TO>;
+    case 64: return (const void*)&row_fwd_kernel<T, LN, 64, VE, VPT, TO>;
+    case 128: return (const void*)&row_fwd_kernel<T, LN, 128, VE, VPT, TO>;
+    case 256: return (const void*)&row_fwd_kernel<T, LN, 256, VE, VPT, TO>;
+    case 512: return (const void*)&row_fwd_kernel<T, LN, 512, VE, VPT, TO>;
+    case 1024: return (const void*)&row_fwd_kernel<T, LN, 1024, VE, VPT, TO>;
+    default: return (const void*)&row_fwd_wide_kernel<T, LN, VE, TO>;
     }
 }
 
 // The forward for rows of `nvec` vectors at TPR threads per row (0: the wide
 // kernel): on the 16-byte path 3 vectors per thread when that covers the row
 // (no idle fourth vector, e.g. 768 fp16 columns at 32 threads), else 4.
-template <typename T, bool LN, int VE>
+template <typename T, bool LN, int VE, typename TO = T>
 const void* row_fwd_fn(int tpr, int nvec) {
     if constexpr (VE > 1) {
-        if (tpr && nvec <= 3 * tpr) return row_fwd_fn_v<T, LN, VE, 3>(tpr);
+        if (tpr && nvec <= 3 * tpr) return row_fwd_fn_v<T, LN, VE, 3, TO>(tpr);
     }
-    return row_fwd_fn_v<T, LN, VE, kRowFwdVpt>(tpr);
+    return row_fwd_fn_v<T, LN, VE, kRowFwdVpt, TO>(tpr);
 }
 
 template <typename T, bool LN, int VE>
@@ -928,17 +937,19 @@ inline int row_tpr(int nvec, int vpt, int max_tpr) {
     return tpr * vpt < nvec ? 0 : tpr;
 }
 
-template <typename T>
-nrm_status row_fwd(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s) {
+// The forward with output storage type TO (T, or float for a 16-bit T).
+template <typename T, typename TO>
+nrm_status row_fwd_to(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     if (a.rows == 0) return NRM_OK;
     const int ve = vec ? kVec<T> : 1;
     const int tpr = row_tpr(a.cols / ve, kRowFwdVpt, kRowMaxFwdTpr);
     const int nvec = a.cols / ve;
-    const void* fn = layernorm
-                         ? (vec ? row_fwd_fn<T, true, kVec<T>>(tpr, nvec) : row_fwd_fn<T, true, 1>(tpr, nvec))
-                         : (vec ? row_fwd_fn<T, false, kVec<T>>(tpr, nvec) : row_fwd_fn<T, false, 1>(tpr, nvec));
+    const void* fn = layernorm ? (vec ? row_fwd_fn<T, true, kVec<T>, TO>(tpr, nvec)
+                                      : row_fwd_fn<T, true, 1, TO>(tpr, nvec))
+                               : (vec ? row_fwd_fn<T, false, kVec<T>, TO>(tpr, nvec)
+                                      : row_fwd_fn<T, false, 1, TO>(tpr, nvec));
     const int block = tpr ? row_fwd_block(tpr) : kRowWideBlock;
     const int rpc = tpr ? block / tpr : 1;
     const int occ = cached_occupancy(fn, block, 0);
@@ -951,6 +962,11 @@ nrm_status row_fwd(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s) {
 }
 
 template <typename T>
+nrm_status row_fwd(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s) {
+    return row_fwd_to<T, T>(a, layernorm, vec, s);
+}
+
+template <typename T>
 nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
@@ -960,7 +976,7 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     RrGeom rg;
     int rtpr = 0;
     size_t rsmem = 0;
-    const bool ring = vec && rr_plan(rg, rtpr, rsmem, a, sizeof(T), layernorm);
+    const bool ring = vec && rr_plan(rg, rtpr, rsmem, a, sizeof(T), layernorm, sizeof(T));
     const int tpr = ring ? 0 : row_tpr(a.cols / ve, kRowBwdVpt, kRowMaxBwdTpr);
     const void* fn;
     int64_t groups, p;
@@ -1015,26 +1031,11 @@ inline int wide_block(int nvec) {
     return b < 32 ? 32 : (b > kRowWideBlock ? kRowWideBlock : b);
 }
 
-// Forward with the output kept in fp32 for a 16-bit input (the wide-row
-// kernels with TO = float, one CTA per row sized to the row).
+// Forward with the output kept in fp32 for a 16-bit input: the same kernels
+// as the plain forward, storing float32 (two 16-byte stores per input vector).
 template <typename T>
 nrm_status row_fwd_f32out(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s) {
-    const DevInfo* d = dev_info();
-    if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
-    if (a.rows == 0) return NRM_OK;
-    constexpr int V = kVec<T>;
-    const void* fn = layernorm ? (vec ? (const void*)&row_fwd_wide_kernel<T, true, V, float>
-                                      : (const void*)&row_fwd_wide_kernel<T, true, 1, float>)
-                               : (vec ? (const void*)&row_fwd_wide_kernel<T, false, V, float>
-                                      : (const void*)&row_fwd_wide_kernel<T, false, 1, float>);
-    const int block = wide_block(a.cols / (vec ? V : 1));
-    const int occ = cached_occupancy(fn, block, 0);
-    if (occ <= 0) return fail(NRM_ERR_CUDA, "row forward kernel cannot be resident");
-    const int64_t cap = int64_t(occ) * d->sms;
-    const int grid = int(a.rows < cap ? a.rows : cap);
-    RowArgs args = a;
-    void* kargs[] = {&args};
-    return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(block), kargs, 0, s), "row forward launch");
+    return row_fwd_to<T, float>(a, layernorm, vec, s);
 }
 
 // Backward whose dy is fp32 (the forward kept its output in fp32) for a
@@ -1046,22 +1047,47 @@ nrm_status row_bwd_f32dy(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     const bool want = a.dw || a.db;
     if (!want) a.ws_dw = a.ws_db = nullptr;
     constexpr int V = kVec<T>;
-    const void* fn = layernorm ? (vec ? (const void*)&row_bwd_wide_kernel<T, true, V, float>
-                                      : (const void*)&row_bwd_wide_kernel<T, true, 1, float>)
-                               : (vec ? (const void*)&row_bwd_wide_kernel<T, false, V, float>
-                                      : (const void*)&row_bwd_wide_kernel<T, false, 1, float>);
-    const int block = wide_block(a.cols / (vec ? V : 1));
-    const int occ = cached_occupancy(fn, block, 0);
-    if (occ <= 0) return fail(NRM_ERR_CUDA, "row backward kernel cannot be resident");
-    int64_t p = int64_t(occ) * d->sms;
-    if (p > row_bwd_max_partials(*d)) p = row_bwd_max_partials(*d);
-    if (a.rows < p) p = a.rows;
-    const int P = int(p);
-    if (P > 0) {
-        RowArgs args = a;
-        void* kargs[] = {&args};
-        nrm_status st = cuda_status(cudaLaunchKernel(fn, dim3(P), dim3(block), kargs, 0, s), "row backward launch");
-        if (st != NRM_OK) return st;
+    RrGeom rg;
+    int rtpr = 0;
+    size_t rsmem = 0;
+    int P = 0;
+    bool ring = false;
+    if constexpr (sizeof(T) == 2) {
+        // dy rows as float32 in the ring slots beside x
+        ring = vec && rr_plan(rg, rtpr, rsmem, a, sizeof(T), layernorm, sizeof(float));
+        if (ring) {
+            const int nv = a.cols / V;
+            const void* fn = layernorm ? rr_fn<T, true, true, float>(rtpr, nv)
+                                       : (a.ws_db ? rr_fn<T, false, true, float>(rtpr, nv)
+                                                  : rr_fn<T, false, false, float>(rtpr, nv));
+            int64_t p = d->sms;
+            if (p > row_bwd_max_partials(*d)) p = row_bwd_max_partials(*d);
+            if (rg.chunks < p) p = rg.chunks;
+            P = int(p);
+            if (P > 0) {
+                nrm_status st = rr_launch(fn, a, rg, rsmem, P, s);
+                if (st != NRM_OK) return st;
+            }
+        }
+    }
+    if (!ring) {
+        const void* fn = layernorm ? (vec ? (const void*)&row_bwd_wide_kernel<T, true, V, float>
+                                          : (const void*)&row_bwd_wide_kernel<T, true, 1, float>)
+                                   : (vec ? (const void*)&row_bwd_wide_kernel<T, false, V, float>
+                                          : (const void*)&row_bwd_wide_kernel<T, false, 1, float>);
+        const int block = wide_block(a.cols / (vec ? V : 1));
+        const int occ = cached_occupancy(fn, block, 0);
+        if (occ <= 0) return fail(NRM_ERR_CUDA, "row backward kernel cannot be resident");
+        int64_t p = int64_t(occ) * d->sms;
+        if (p > row_bwd_max_partials(*d)) p = row_bwd_max_partials(*d);
+        if (a.rows < p) p = a.rows;
+        P = int(p);
+        if (P > 0) {
+            RowArgs args = a;
+            void* kargs[] = {&args};
+            nrm_status st = cuda_status(cudaLaunchKernel(fn, dim3(P), dim3(block), kargs, 0, s), "row backward launch");
+            if (st != NRM_OK) return st;
+        }
     }
     if (!want) return NRM_OK;
     const float* wsw = a.ws_dw;

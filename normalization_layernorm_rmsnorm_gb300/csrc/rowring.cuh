@@ -29,19 +29,21 @@ constexpr int kRrBarConsumers = 15;            // named barrier over the consume
 struct RrGeom {
     int R;                 // rows per chunk
     int slots;             // ring slots
-    uint32_t slot_bytes;   // bytes of a slot: nt*R rows (+ R floats of rstd and of mean, backward)
+    uint32_t slot_bytes;   // bytes of a slot: R rows of dy, R rows of x, R floats of rstd (and of mean)
     uint32_t param_bytes;  // fp32 weight (and bias) at the front of dynamic shared memory
     int64_t chunks;        // ceil(rows / R)
 };
 
-// Producer (whole warp): the CTA's chunks of dy and x (and the rows' rstd,
-// mean) into the ring, in order.  If a wait for a free slot gives up, it
-// issues nothing more; either way it then waits (bounded) until the last copy
-// issued into each slot has landed, so that none is in flight at exit.
-template <typename T, bool LN>
+// Producer (whole warp): the CTA's chunks of dy (storage type TD) and x (T)
+// (and the rows' rstd, mean) into the ring, in order.  If a wait for a free
+// slot gives up, it issues nothing more; either way it then waits (bounded)
+// until the last copy issued into each slot has landed, so that none is in
+// flight at exit.
+template <typename T, bool LN, typename TD>
 __device__ void rr_produce(const RowArgs& a, const RrGeom& g, unsigned char* ring, uint64_t* full,
                            uint64_t* empty, int lane, bool& bad) {
     const size_t row_bytes = size_t(a.cols) * sizeof(T);
+    const size_t dy_row_bytes = size_t(a.cols) * sizeof(TD);
     const uint64_t pol = l2_evict_first();
     int q = 0;
     for (int64_t c = blockIdx.x; c < g.chunks; c += gridDim.x, ++q) {
@@ -55,13 +57,14 @@ __device__ void rr_produce(const RowArgs& a, const RrGeom& g, unsigned char* rin
         const int ra = int(a.rows - r0 < g.R ? a.rows - r0 : g.R);
         unsigned char* base = ring + size_t(slot) * g.slot_bytes;
         const uint32_t bytes = uint32_t(size_t(ra) * row_bytes);
+        const uint32_t dy_bytes = uint32_t(size_t(ra) * dy_row_bytes);
         if (lane == 0) {
-            mbar_arrive_expect_tx(&full[slot], 2 * bytes);
-            bulk_g2s(base, reinterpret_cast<const T*>(a.dy) + r0 * a.cols, bytes, &full[slot], pol);
-            bulk_g2s(base + size_t(g.R) * row_bytes, reinterpret_cast<const T*>(a.x) + r0 * a.cols, bytes,
+            mbar_arrive_expect_tx(&full[slot], dy_bytes + bytes);
+            bulk_g2s(base, reinterpret_cast<const TD*>(a.dy) + r0 * a.cols, dy_bytes, &full[slot], pol);
+            bulk_g2s(base + size_t(g.R) * dy_row_bytes, reinterpret_cast<const T*>(a.x) + r0 * a.cols, bytes,
                      &full[slot], pol);
         }
-        float* st = reinterpret_cast<float*>(base + 2 * size_t(g.R) * row_bytes);
+        float* st = reinterpret_cast<float*>(base + size_t(g.R) * (dy_row_bytes + row_bytes));
         for (int i = lane; i < ra; i += 32) {
             cp_async_4(st + i, a.rstd_in + r0 + i);
             if (LN) cp_async_4(st + g.R + i, a.mean_in + r0 + i);
@@ -156,7 +159,25 @@ __device__ __forceinline__ void rr_partial_row(const float (&acc)[VPT][VE], floa
 // row's vectors per thread (3 or 4): the dw/db accumulators are VPT*VE floats
 // each, and at 544 threads a CTA has 96 registers per thread, so rows that
 // need 3 vectors per thread do not carry a fourth's accumulators (they spilled).
-template <typename T, bool LN, int TPR, bool DB, int VPT>
+// Vector vi (VE elements of a row of T) of a dy row stored as TD in the slot:
+// one 16-byte read when TD is T, two when dy is float32 for a 16-bit x.
+template <typename T, typename TD>
+__device__ __forceinline__ void rr_load_dy(const unsigned char* dr, int vi, float2 (&dv)[kPairs<T>]) {
+    if constexpr (sizeof(TD) == sizeof(T)) {
+        unpack2<T>(*reinterpret_cast<const uint4*>(dr + size_t(vi) * 16), dv);
+    } else {
+        const uint4* p = reinterpret_cast<const uint4*>(dr + size_t(vi) * 32);
+        const uint4 u0 = p[0], u1 = p[1];
+        dv[0] = make_float2(__uint_as_float(u0.x), __uint_as_float(u0.y));
+        dv[1] = make_float2(__uint_as_float(u0.z), __uint_as_float(u0.w));
+        dv[2] = make_float2(__uint_as_float(u1.x), __uint_as_float(u1.y));
+        dv[3] = make_float2(__uint_as_float(u1.z), __uint_as_float(u1.w));
+    }
+}
+
+// TD: dy's storage type (T, or float32 when the forward kept its output in
+// float32 for a 16-bit x).
+template <typename T, bool LN, int TPR, bool DB, int VPT, typename TD = T>
 __global__ void __launch_bounds__(kRrThreads, 1)
 row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
     constexpr int VE = kVec<T>;
@@ -188,7 +209,7 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
     __syncthreads();
 
     if (warp == kRrConsumerWarps) {
-        rr_produce<T, LN>(a, g, ring, full, empty, lane, bad);
+        rr_produce<T, LN, TD>(a, g, ring, full, empty, lane, bad);
     } else {
         const int group = threadIdx.x / TPR;
         const int t = threadIdx.x % TPR;
@@ -197,6 +218,7 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
         const float fcols = float(cols);
         const float inv_cols = 1.f / fcols;
         const size_t row_bytes = size_t(cols) * sizeof(T);
+        const size_t dy_row_bytes = size_t(cols) * sizeof(TD);
         T* __restrict__ dx = reinterpret_cast<T*>(a.dx);
         int phase = 0;
         // the element arithmetic runs on fp32 pairs (packed FP32 instructions)
@@ -215,10 +237,10 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
             const int64_t r0 = c * g.R;
             const int ra = int(a.rows - r0 < g.R ? a.rows - r0 : g.R);
             const unsigned char* base = ring + size_t(slot) * g.slot_bytes;
-            const float* st = reinterpret_cast<const float*>(base + 2 * size_t(g.R) * row_bytes);
+            const float* st = reinterpret_cast<const float*>(base + size_t(g.R) * (dy_row_bytes + row_bytes));
             for (int r = group; r < ra; r += RPC) {
-                const unsigned char* dr = base + size_t(r) * row_bytes;
-                const unsigned char* xr = base + size_t(g.R + r) * row_bytes;
+                const unsigned char* dr = base + size_t(r) * dy_row_bytes;
+                const unsigned char* xr = base + size_t(g.R) * dy_row_bytes + size_t(r) * row_bytes;
                 const float rs = st[r];
                 const float mu = LN ? st[g.R + r] : 0.f;
                 const float2 rs2 = f2(rs);
@@ -232,7 +254,7 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
                     const int vi = j * TPR + t;
                     if (vi < nvec) {
                         float2 dv[H], xv[H], wv[H];
-                        unpack2<T>(*reinterpret_cast<const uint4*>(dr + size_t(vi) * 16), dv);
+                        rr_load_dy<T, TD>(dr, vi, dv);
                         unpack2<T>(*reinterpret_cast<const uint4*>(xr + size_t(vi) * 16), xv);
                         rr_params2<VE>(wsm, vi, nvec, wv);
 #pragma unroll
@@ -262,7 +284,7 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
                     const int vi = j * TPR + t;
                     if (vi < nvec) {
                         float2 dv[H], xv[H], wv[H], o[H];
-                        unpack2<T>(*reinterpret_cast<const uint4*>(dr + size_t(vi) * 16), dv);
+                        rr_load_dy<T, TD>(dr, vi, dv);
                         unpack2<T>(*reinterpret_cast<const uint4*>(xr + size_t(vi) * 16), xv);
                         rr_params2<VE>(wsm, vi, nvec, wv);
 #pragma unroll
