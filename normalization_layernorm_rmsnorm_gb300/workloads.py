@@ -162,12 +162,12 @@ def _bn_res_relu(cfg, dev, f32):
     erv = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,)).torch(dev)
     esm, esr = f32(c), f32(c)
     eval_name = cfg.name + "_eval"
-    calls.append(Call(eval_name, "fwd", "bn_fwd_ring_kernel<f32,eval>",
+    calls.append(Call(eval_name, "fwd", "bn_fwd_eval_kernel<f32,relu>",
                       lambda: nrm.nrm_batchnorm_fwd(bx, bres, bw, bb, by, erm, erv, esm, esr, bmask,
                                                     cfg.eps, cfg.momentum, False, "relu", bws),
                       nbytes(bx, bres, by, bmask, bw, bb, erm, erv, esm, esr), 1,
                       [erm, erv], [by, bmask]))
-    calls.append(Call(eval_name, "bwd", "bn_bwd_ring_kernel<f32,eval>",
+    calls.append(Call(eval_name, "bwd", "bn_bwd_eval_kernel<f32,relu>",
                       lambda: nrm.nrm_batchnorm_bwd(bdy, bx, bres, bw, bb, esm, esr, bmask, bdx, bdres,
                                                     bdw, bdb, False, "relu", bws),
                       nbytes(bdy, bx, bmask, bw, bb, esm, esr, bdx, bdres, bdw, bdb), 1,
@@ -255,10 +255,10 @@ def _ln_f32out(name, rows, cols, dev, f32):
     mean, rstd = f32(rows), f32(rows)
     ws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_BWD, rows, cols, nrm.NRM_F16) // 4)
     return [
-        Call(name, "fwd", "row_fwd_wide_kernel<f16,ln,f32 out>",
+        Call(name, "fwd", "row_fwd_kernel<f16,ln,f32 out>",
              lambda: nrm.nrm_layernorm_fwd_ex(x, w, b, y, mean, rstd, 1e-6),
              nbytes(x, w, b, y, mean, rstd), 1, [x, w, b], [y, mean, rstd]),
-        Call(name, "bwd", "row_bwd_wide_kernel<f16,ln,f32 dy>+colsum",
+        Call(name, "bwd", "row_bwd_ring_kernel<f16,ln,f32 dy>+colsum",
              lambda: nrm.nrm_layernorm_bwd_ex(dy, x, w, mean, rstd, dx, dw, db, ws),
              nbytes(dy, x, w, mean, rstd, dx, dw, db), 2, [dy], [dx, dw, db]),
     ]
