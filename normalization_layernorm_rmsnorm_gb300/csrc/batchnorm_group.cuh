@@ -8,32 +8,38 @@
 // form a span of G*l elements that starts and ends on a 16-byte boundary, so a
 // channel group is n such spans at a fixed stride.  A thread-block cluster of
 // Q CTAs owns a group: each CTA bulk-copies its n/Q samples' spans into
-// shared memory, reduces its per-channel partials and pushes them into every
-// cluster CTA's shared memory (distributed shared memory stores, after a
+// shared memory.  Each thread owns one 16-byte position of the span across a
+// share of the samples, so the channel of every element it touches is fixed:
+// it keeps per-element partial sums and per-element coefficients in
+// registers, with no per-element index arithmetic.  One warp per channel adds
+// the partials in a fixed order; each CTA pushes its per-channel result into
+// every cluster CTA's shared memory (distributed shared memory stores, after a
 // split cluster barrier that every CTA arrived on at start), one cluster
-// barrier later each CTA merges the Q partials in rank order (every CTA gets
-// the same bits), and writes its outputs from shared memory with 16-byte
-// stores.  Every input byte is read once.
+// barrier later each CTA merges the Q results in rank order (every CTA gets
+// the same bits), and writes its outputs with 16-byte stores.  Every input
+// byte is read once.
 #pragma once
 
 namespace nrm {
 
-constexpr int kGrpThreads = 256;
-constexpr int kGrpWarps = kGrpThreads / 32;
-constexpr int kGrpMaxQ = 8;  // CTAs per cluster, at most
+constexpr int kGrpMinThreads = 256;   // one warp per channel of a group (G <= 8), at least
+constexpr int kGrpMaxThreads = 1024;  // spans of up to 1024 vectors
+constexpr int kGrpMaxG = 8;           // channels per group, at most
+constexpr int kGrpMaxQ = 8;           // CTAs per cluster, at most
 
 struct GrpGeom {
     int64_t c;
     int n;
     int l;             // elements per (sample, channel)
-    int G;             // channels per group (divides kGrpWarps)
+    int G;             // channels per group
     int span;          // G*l elements: a sample's run of the group
+    int vps;           // 16-byte vectors per span
+    int P;             // sample phases: P*vps threads take the tile
     int Q;             // CTAs per group (the cluster)
     int spc;           // samples per CTA
     int words;         // ReLU-mask words per segment
     uint32_t tile;     // bytes of one tensor's tile in shared memory
-    FastDiv div_vps;   // division by the 16-byte vectors of a span
-    FastDiv div_l;     // division by l
+    uint32_t part;     // byte offset of the per-element partial sums (2*P*span floats)
     float inv_m;       // 1 / (n*l)
     float inv_m1;      // 1 / (n*l - 1)
 };
@@ -80,51 +86,110 @@ __device__ __forceinline__ float grp_elem(const unsigned char* tile, int idx) {
     return Io<T>::load(reinterpret_cast<const typename Io<T>::bits_t*>(tile)[idx]);
 }
 
-// One 16-byte vector of a tile (element offset `e`, a multiple of kVec<T>).
-template <typename T>
-__device__ __forceinline__ void grp_vec(const unsigned char* tile, int e, float (&v)[kVec<T>]) {
-    Pack<T, kVec<T>> pk;
-    pk.u = *reinterpret_cast<const uint4*>(tile + size_t(e) * sizeof(T));
-    unpack<T, kVec<T>>(pk, v);
+// NE elements of T in 8 or 16 bytes.
+template <typename T, int NE>
+union GrpPack {
+    static_assert(NE * sizeof(T) == 16 || NE * sizeof(T) == 8, "8 or 16 bytes");
+    typename std::conditional<NE * sizeof(T) == 16, uint4, uint2>::type u;
+    typename Io<T>::bits_t b[NE];
+};
+
+// NE elements at byte offset `off` of a shared-memory tile, as fp32 pairs.
+template <typename T, int NE>
+__device__ __forceinline__ void grp_ld(const unsigned char* tile, uint32_t off, float2 (&v)[NE / 2]) {
+    GrpPack<T, NE> pk;
+    pk.u = *reinterpret_cast<const decltype(pk.u)*>(tile + off);
+#pragma unroll
+    for (int h = 0; h < NE / 2; ++h) v[h] = make_float2(Io<T>::load(pk.b[2 * h]), Io<T>::load(pk.b[2 * h + 1]));
 }
 
-// Element walk of one channel's part of a CTA's tile: element t of the
-// channel's ns*l elements (sample-major) is element e of sample s, and the
-// walk advances t by a fixed step with one integer division at the start.
-struct GrpWalk {
-    int s, e, s_step, e_step;
-    __device__ __forceinline__ GrpWalk(int t0, int step, int l) {
-        s = t0 / l;
-        e = t0 - s * l;
-        s_step = step / l;
-        e_step = step - s_step * l;
+// NE elements rounded to T, stored to global memory with L2 policy `pol`.
+template <typename T, int NE>
+__device__ __forceinline__ void grp_st(T* p, const float2 (&v)[NE / 2], uint64_t pol) {
+    GrpPack<T, NE> pk;
+#pragma unroll
+    for (int h = 0; h < NE / 2; ++h) {
+        pk.b[2 * h] = Io<T>::store(v[h].x);
+        pk.b[2 * h + 1] = Io<T>::store(v[h].y);
     }
-    __device__ __forceinline__ void next(int l) {
-        e += e_step;
-        s += s_step;
-        if (e >= l) {
-            e -= l;
-            ++s;
+    if constexpr (NE * sizeof(T) == 16) {
+        st_v4_policy(p, pk.u, pol);
+    } else {
+        st_v2_policy(p, pk.u, pol);
+    }
+}
+
+// NE fp32 values to / from shared memory (8-byte aligned).
+template <int NE>
+__device__ __forceinline__ void grp_put_f32(float* d, const float2 (&v)[NE / 2]) {
+#pragma unroll
+    for (int h = 0; h < NE / 2; ++h) reinterpret_cast<float2*>(d)[h] = v[h];
+}
+template <int NE>
+__device__ __forceinline__ void grp_get_f32(const float* d, float2 (&v)[NE / 2]) {
+#pragma unroll
+    for (int h = 0; h < NE / 2; ++h) v[h] = reinterpret_cast<const float2*>(d)[h];
+}
+
+// The thread's place in the tile.  A span is vps positions of NE elements
+// (8 or 16 bytes); thread t < P*vps owns position vp = t % vps of every span
+// and takes the CTA's samples ph, ph + P, ... (ph = t / vps), so the channel
+// of each of its elements (and with it every per-channel coefficient) is the
+// same sample after sample: found once here, with ch[k] the group-relative
+// channel of element k and pos[k] its index within that (sample, channel)
+// segment.
+template <int NE>
+struct GrpSlot {
+    int vp, ph;
+    bool on;
+    int ch[NE], pos[NE];
+    __device__ __forceinline__ explicit GrpSlot(const GrpGeom& g) {
+        vp = int(threadIdx.x) % g.vps;
+        ph = int(threadIdx.x) / g.vps;
+        on = ph < g.P;
+        const int e0 = vp * NE;
+        int j = e0 / g.l, r = e0 - j * g.l;
+#pragma unroll
+        for (int k = 0; k < NE; ++k) {
+            ch[k] = j;
+            pos[k] = r;
+            if (++r == g.l) {
+                r = 0;
+                ++j;
+            }
         }
+    }
+    // element offset of the thread's position in sample s of a tile
+    __device__ __forceinline__ uint32_t at(const GrpGeom& g, int s) const {
+        return uint32_t(s) * uint32_t(g.span) + uint32_t(vp * NE);
     }
 };
 
+// Element k of this thread's position, summed over its samples, goes to
+// part[ph][vp*NE + k]: a [P][span] array of per-(phase, element) partials.
+template <int NE>
+__device__ __forceinline__ void grp_put_partial(float* part, const GrpGeom& g, const GrpSlot<NE>& sl,
+                                                const float2 (&v)[NE / 2]) {
+    grp_put_f32<NE>(part + size_t(sl.ph) * g.span + sl.vp * NE, v);
+}
+
 template <typename T, bool TRAIN, int ACT>
-__global__ void __launch_bounds__(kGrpThreads)
+__global__ void __launch_bounds__(kGrpMaxThreads)
 bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
-    constexpr int VE = kVec<T>;
-    using bits = typename Io<T>::bits_t;
+    constexpr int NE = kVec<T>;  // 16-byte positions
+    constexpr int H = NE / 2;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bar;
-    __shared__ Moments wm[kGrpWarps];
-    __shared__ float4 allp[kGrpMaxQ][kGrpWarps];  // (n, mean, m2) per channel of every cluster CTA, pushed by it
-    __shared__ float2 coef[kGrpWarps];            // (scale, shift) per channel
+    __shared__ float4 allp[kGrpMaxQ][kGrpMaxG];  // (n, mean, m2) per channel of every cluster CTA, pushed by it
+    __shared__ float2 coef[kGrpMaxG];            // (scale, shift) per channel
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
     const T* __restrict__ res = reinterpret_cast<const T*>(a.res);
     T* __restrict__ y = reinterpret_cast<T*>(a.y);
     const GrpPos p = grp_pos(g);
+    const GrpSlot<NE> sl(g);
     const unsigned char* tx = smem;
     const unsigned char* tr = smem + g.tile;
 
@@ -135,33 +200,71 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
     }
     __syncthreads();
     grp_load<T>(g, p, smem, &bar, x, res, nullptr);
+    // the channel's parameters (and running statistics), read while the tile lands
+    float wc = 1.f, bc = 0.f, rm = 0.f, rv = 1.f;
+    if (threadIdx.x < g.G) {
+        const int64_t ch = p.ch0 + threadIdx.x;
+        if (a.w) wc = a.w[ch];
+        if (a.b) bc = a.b[ch];
+        if (!TRAIN || p.rank == 0) {
+            if (a.rm) rm = a.rm[ch];
+            if (a.rv) rv = a.rv[ch];
+        }
+    }
     bool bad = false;
     if (p.ns > 0 && !mbar_wait_bounded(&bar, 0, kBnWaitLimitNs)) bad = true;
 
     if constexpr (TRAIN) {
-        // the warps w with w % G == j share channel j: its ns*l elements
-        // (sample-major) are dealt to their lanes, so every lane's chain is
-        // short even when l is 1
-        const int j = warp % g.G;
-        const int wpc = kGrpWarps / g.G;  // warps per channel
-        const bits* tb = reinterpret_cast<const bits*>(tx) + j * g.l;
-        ShiftedSums acc;
-        GrpWalk wk((warp / g.G) * 32 + lane, wpc * 32, g.l);
-        for (int t = (warp / g.G) * 32 + lane; t < p.ns * g.l; t += wpc * 32) {
-            const float v[1] = {Io<T>::load(tb[wk.s * g.span + wk.e])};
-            acc.add(v);
-            wk.next(g.l);
+        // per element of the thread's vectors: sums of (x - K) and (x - K)^2
+        // over its samples, K the channel's first value in the tile; with one
+        // K per channel these add across the CTA's threads
+        float* ps = reinterpret_cast<float*>(smem + g.part);
+        float* pq = ps + size_t(g.P) * g.span;
+        if (sl.on) {
+            float2 nk[H], s2[H], q2[H];
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                nk[h] = p.ns > 0 ? make_float2(-grp_elem<T>(tx, sl.ch[2 * h] * g.l),
+                                               -grp_elem<T>(tx, sl.ch[2 * h + 1] * g.l))
+                                 : make_float2(0.f, 0.f);
+                s2[h] = q2[h] = make_float2(0.f, 0.f);
+            }
+            for (int s = sl.ph; s < p.ns; s += g.P) {
+                float2 xv[H];
+                grp_ld<T, NE>(tx, sl.at(g, s) * sizeof(T), xv);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float2 d = __fadd2_rn(xv[h], nk[h]);
+                    s2[h] = __fadd2_rn(s2[h], d);
+                    q2[h] = __ffma2_rn(d, d, q2[h]);
+                }
+            }
+            grp_put_partial<NE>(ps, g, sl, s2);
+            grp_put_partial<NE>(pq, g, sl, q2);
         }
-        Moments m = acc.moments();
-        warp_merge(m);
-        if (lane == 0) wm[warp] = m;
         __syncthreads();
         cluster_wait();  // every CTA of the cluster has started: its shared memory may be written
-        if (threadIdx.x < g.G) {
-            Moments t = wm[threadIdx.x];
-            for (int w = threadIdx.x + g.G; w < kGrpWarps; w += g.G) chan_merge(t, wm[w].n, wm[w].mean, wm[w].m2);
-            const float4 pv = make_float4(t.n, t.mean, t.m2, 0.f);
-            for (int r = 0; r < g.Q; ++r) st_dsmem_f4(dsmem_addr(&allp[p.rank][threadIdx.x], uint32_t(r)), pv);
+        if (warp < g.G) {
+            // channel `warp`: its l elements of every phase's partials, in a fixed order
+            const int j = warp;
+            float sum = 0.f, sq = 0.f;
+            for (int i = lane; i < g.P * g.l; i += 32) {
+                const int q = i / g.l;
+                const int idx = q * g.span + j * g.l + (i - q * g.l);
+                sum += ps[idx];
+                sq += pq[idx];
+            }
+            sum = warp_sum(sum);
+            sq = warp_sum(sq);
+            if (lane == 0) {
+                float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.ns > 0) {
+                    const float n = float(p.ns) * float(g.l);
+                    const float sn = sum / n;
+                    pv = make_float4(n, grp_elem<T>(tx, j * g.l) + sn, fmaxf(sq - sum * sn, 0.f), 0.f);
+                }
+                for (int r = 0; r < g.Q; ++r) st_dsmem_f4(dsmem_addr(&allp[p.rank][j], uint32_t(r)), pv);
+            }
         }
         cluster_sync_all();  // every CTA's partials have landed in every CTA
         if (threadIdx.x < g.G) {
@@ -171,24 +274,20 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
                 chan_merge(tot, pv.x, pv.y, pv.z);
             }
             const int64_t ch = p.ch0 + threadIdx.x;
-            const float wc = a.w ? a.w[ch] : 1.f;
-            const float bc = a.b ? a.b[ch] : 0.f;
             const float rs = rsqrtf(tot.m2 * g.inv_m + a.eps);
             coef[threadIdx.x] = make_float2(wc * rs, bc - tot.mean * wc * rs);
             if (p.rank == 0) {
                 if (a.save_mean) a.save_mean[ch] = tot.mean;
                 if (a.save_rstd) a.save_rstd[ch] = rs;
-                if (a.rm) a.rm[ch] = fmaf(a.momentum, tot.mean, (1.f - a.momentum) * a.rm[ch]);
-                if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * a.rv[ch]);
+                if (a.rm) a.rm[ch] = fmaf(a.momentum, tot.mean, (1.f - a.momentum) * rm);
+                if (a.rv) a.rv[ch] = fmaf(a.momentum, tot.m2 * g.inv_m1, (1.f - a.momentum) * rv);
             }
         }
     } else {
         if (threadIdx.x < g.G) {
             const int64_t ch = p.ch0 + threadIdx.x;
-            const float wc = a.w ? a.w[ch] : 1.f;
-            const float bc = a.b ? a.b[ch] : 0.f;
-            const float rs = rsqrtf(a.rv[ch] + a.eps);
-            const float mu = a.rm[ch];
+            const float rs = rsqrtf(rv + a.eps);
+            const float mu = rm;
             coef[threadIdx.x] = make_float2(wc * rs, bc - mu * wc * rs);
             if (p.rank == 0) {
                 if (a.save_mean) a.save_mean[ch] = mu;
@@ -198,34 +297,34 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
     }
     __syncthreads();
 
-    // ---- y = act(x*scale + shift (+ residual)), 16 bytes per thread and step ----
+    // ---- y = act(x*scale + shift (+ residual)), the thread's vector of each of its samples ----
     const uint64_t pol = l2_evict_first();
-    const int vps = g.span / VE;
-    for (int v = threadIdx.x; v < p.ns * vps; v += kGrpThreads) {
-        const int s = int(fast_div(uint32_t(v), g.div_vps));
-        const int o = (v - s * vps) * VE;
-        float xv[VE], rv[VE], ov[VE];
-        grp_vec<T>(tx, s * g.span + o, xv);
-        if (res) grp_vec<T>(tr, s * g.span + o, rv);
-        int j = int(fast_div(uint32_t(o), g.div_l));
-        int next = (j + 1) * g.l;
-        float2 cs = coef[j];  // the vector may cross into the next channel(s): reloaded there
+    if (sl.on) {
+        float2 sc[H], sh[H];
 #pragma unroll
-        for (int k = 0; k < VE; ++k) {
-            if (o + k == next) {
-                ++j;
-                next += g.l;
-                cs = coef[j];
-            }
-            float z = fmaf(xv[k], cs.x, cs.y);
-            if (res) z += rv[k];
-            ov[k] = act_forward_c<ACT>(z, a.act_param, a.act);
+        for (int h = 0; h < H; ++h) {
+            const float2 c0 = coef[sl.ch[2 * h]], c1 = coef[sl.ch[2 * h + 1]];
+            sc[h] = make_float2(c0.x, c1.x);
+            sh[h] = make_float2(c0.y, c1.y);
         }
-        store_vec_pol<T, VE>(y + (int64_t(p.n0 + s) * g.c + p.ch0) * g.l + o, ov, pol);
+        for (int s = sl.ph; s < p.ns; s += g.P) {
+            float2 xv[H], rv[H];
+            grp_ld<T, NE>(tx, sl.at(g, s) * sizeof(T), xv);
+            if (res) grp_ld<T, NE>(tr, sl.at(g, s) * sizeof(T), rv);
+            float2 ov[H];
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                float2 z = __ffma2_rn(xv[h], sc[h], sh[h]);
+                if (res) z = __fadd2_rn(z, rv[h]);
+                ov[h] = make_float2(act_forward_c<ACT>(z.x, a.act_param, a.act),
+                                    act_forward_c<ACT>(z.y, a.act_param, a.act));
+            }
+            grp_st<T, NE>(y + (int64_t(p.n0 + s) * g.c + p.ch0) * g.l + sl.vp * NE, ov, pol);
+        }
     }
     // ---- ReLU mask: one warp per (sample, channel) segment, a ballot per word ----
     if (a.mask) {
-        for (int sg = warp; sg < p.ns * g.G; sg += kGrpWarps) {
+        for (int sg = warp; sg < p.ns * g.G; sg += nwarps) {
             const int s = sg / g.G;
             const int j = sg - s * g.G;
             const float2 cs = coef[j];
@@ -251,16 +350,15 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
 }
 
 template <typename T, bool TRAIN, int ACT>
-__global__ void __launch_bounds__(kGrpThreads)
+__global__ void __launch_bounds__(kGrpMaxThreads)
 bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
-    constexpr int VE = kVec<T>;
-    using bits = typename Io<T>::bits_t;
+    constexpr int NE = kVec<T> / 2;  // 8-byte positions: half the per-element registers
+    constexpr int H = NE / 2;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bar;
-    __shared__ double2 ws[kGrpWarps];
-    __shared__ double2 allp[kGrpMaxQ][kGrpWarps];  // (sum dz, sum dz*(x - mean)) per channel of every cluster CTA
-    __shared__ float4 prm[kGrpWarps];              // (mean, rstd, scale, shift) per channel
-    __shared__ float2 coef[kGrpWarps];             // dx coefficients (c1, c2) per channel
+    __shared__ double2 allp[kGrpMaxQ][kGrpMaxG];  // (sum dz, sum dz*(x - mean)) per channel of every cluster CTA
+    __shared__ float4 prm[kGrpMaxG];              // (mean, rstd, scale, shift) per channel
+    __shared__ float4 dxc[kGrpMaxG];              // dx = A*dz - B - C*(x - mean): (A, B, C, mean) per channel
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
@@ -272,11 +370,15 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     const bool use_mask = ACT == NRM_ACT_RELU && a.mask_in != nullptr;
     const bool with_res = need_z && res != nullptr;
     const GrpPos p = grp_pos(g);
+    const GrpSlot<NE> sl(g);
     const unsigned char* tdy = smem;
     const unsigned char* tx = smem + g.tile;
     const unsigned char* tr = smem + 2 * size_t(g.tile);
     float* tz = reinterpret_cast<float*>(smem + (with_res ? 3 : 2) * size_t(g.tile));  // dz, fp32
     uint32_t* tm = reinterpret_cast<uint32_t*>(tz + size_t(g.spc) * g.span);            // mask words
+    // the partial sums (2*P*span floats), over the dy tile when it is large enough
+    float* pd = reinterpret_cast<float*>(smem + g.part);
+    float* pc = pd + size_t(g.P) * g.span;
 
     cluster_arrive_relaxed();  // this CTA has started
     if (threadIdx.x == 0) {
@@ -296,7 +398,7 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     if (use_mask) {
         // the mask words of the CTA's segments: per sample, G*words consecutive words
         const int per = g.G * g.words;
-        for (int i = threadIdx.x; i < p.ns * per; i += kGrpThreads) {
+        for (int i = threadIdx.x; i < p.ns * per; i += blockDim.x) {
             const int s = i / per;
             tm[i] = a.mask_in[(int64_t(p.n0 + s) * g.c + p.ch0) * g.words + (i - s * per)];
         }
@@ -305,48 +407,81 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
     if (p.ns > 0 && !mbar_wait_bounded(&bar, 0, kBnWaitLimitNs)) bad = true;
     __syncthreads();
 
-    // ---- dz (kept in shared memory) and the two channel sums: warp w takes channel w % G ----
-    {
-        const int j = warp % g.G;
-        const int wpc = kGrpWarps / g.G;
-        const float4 pr = prm[j];
-        const bits* bdy = reinterpret_cast<const bits*>(tdy) + j * g.l;
-        const bits* bx = reinterpret_cast<const bits*>(tx) + j * g.l;
-        const bits* br = reinterpret_cast<const bits*>(tr) + j * g.l;
-        float* zj = tz + j * g.l;
-        const uint32_t* mj = tm + j * g.words;
-        GradSums acc(pr.x);
-        GrpWalk wk((warp / g.G) * 32 + lane, wpc * 32, g.l);
-        for (int t = (warp / g.G) * 32 + lane; t < p.ns * g.l; t += wpc * 32) {
-            const int idx = wk.s * g.span + wk.e;
-            const float dyv = Io<T>::load(bdy[idx]);
-            const float xv[1] = {Io<T>::load(bx[idx])};
-            float dz[1];
-            if (use_mask) {
-                dz[0] = ((mj[wk.s * g.G * g.words + (wk.e >> 5)] >> (wk.e & 31)) & 1u) ? dyv : 0.f;
-            } else if (need_z) {
-                const float rv = with_res ? Io<T>::load(br[idx]) : 0.f;
-                dz[0] = dyv * act_derivative_c<ACT>(fmaf(xv[0], pr.z, pr.w) + rv, a.act_param, a.act);
-            } else {
-                dz[0] = dyv;
-            }
-            zj[idx] = dz[0];
-            acc.add(dz, xv);
-            wk.next(g.l);
+    // ---- dz (kept in shared memory) and, per element of the thread's vectors, sums of dz and dz*(x - mean) ----
+    float2 sdz[H], sdc[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) sdz[h] = sdc[h] = make_float2(0.f, 0.f);
+    if (sl.on) {
+        float2 nmu[H], sc[H], sh[H];
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const float4 p0 = prm[sl.ch[2 * h]], p1 = prm[sl.ch[2 * h + 1]];
+            nmu[h] = make_float2(-p0.x, -p1.x);
+            sc[h] = make_float2(p0.z, p1.z);
+            sh[h] = make_float2(p0.w, p1.w);
         }
-        const FF d1 = ff_warp_sum(acc.ff_dz());
-        const FF d2 = ff_warp_sum(acc.ff_dzc());
-        if (lane == 0) ws[warp] = make_double2(ff_to_double(d1), ff_to_double(d2));
+        const int wps = g.G * g.words;  // mask words per sample
+        for (int s = sl.ph; s < p.ns; s += g.P) {
+            float2 dyv[H], xv[H], dz[H];
+            grp_ld<T, NE>(tdy, sl.at(g, s) * sizeof(T), dyv);
+            grp_ld<T, NE>(tx, sl.at(g, s) * sizeof(T), xv);
+            if (use_mask) {
+                const uint32_t* mw = tm + s * wps;
+                float m[NE];
+#pragma unroll
+                for (int k = 0; k < NE; ++k)
+                    m[k] = ((mw[sl.ch[k] * g.words + (sl.pos[k] >> 5)] >> (sl.pos[k] & 31)) & 1u) ? 1.f : 0.f;
+#pragma unroll
+                for (int h = 0; h < H; ++h) dz[h] = __fmul2_rn(dyv[h], make_float2(m[2 * h], m[2 * h + 1]));
+            } else if (need_z) {
+                float2 rv[H];
+                if (with_res) {
+                    grp_ld<T, NE>(tr, sl.at(g, s) * sizeof(T), rv);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < H; ++h) rv[h] = make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float2 z = __fadd2_rn(__ffma2_rn(xv[h], sc[h], sh[h]), rv[h]);
+                    dz[h] = __fmul2_rn(dyv[h], make_float2(act_derivative_c<ACT>(z.x, a.act_param, a.act),
+                                                           act_derivative_c<ACT>(z.y, a.act_param, a.act)));
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < H; ++h) dz[h] = dyv[h];
+            }
+            grp_put_f32<NE>(tz + sl.at(g, s), dz);
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                sdz[h] = __fadd2_rn(sdz[h], dz[h]);
+                sdc[h] = __ffma2_rn(dz[h], __fadd2_rn(xv[h], nmu[h]), sdc[h]);
+            }
+        }
+    }
+    __syncthreads();  // the dy tile is read: the partials may go over it
+    if (sl.on) {
+        grp_put_partial<NE>(pd, g, sl, sdz);
+        grp_put_partial<NE>(pc, g, sl, sdc);
     }
     __syncthreads();
     cluster_wait();  // every CTA of the cluster has started: its shared memory may be written
-    if (threadIdx.x < g.G) {
-        double2 t = ws[threadIdx.x];
-        for (int w = threadIdx.x + g.G; w < kGrpWarps; w += g.G) {
-            t.x += ws[w].x;
-            t.y += ws[w].y;
+    if (warp < g.G) {
+        // channel `warp`: its l elements of every phase's partials, in a fixed order, in float-float
+        const int j = warp;
+        FF d1{0.f, 0.f}, d2{0.f, 0.f};
+        for (int i = lane; i < g.P * g.l; i += 32) {
+            const int q = i / g.l;
+            const int idx = q * g.span + j * g.l + (i - q * g.l);
+            d1 = ff_add(d1, FF{pd[idx], 0.f});
+            d2 = ff_add(d2, FF{pc[idx], 0.f});
         }
-        for (int r = 0; r < g.Q; ++r) st_dsmem_d2(dsmem_addr(&allp[p.rank][threadIdx.x], uint32_t(r)), t);
+        d1 = ff_warp_sum(d1);
+        d2 = ff_warp_sum(d2);
+        if (lane == 0) {
+            const double2 t = make_double2(ff_to_double(d1), ff_to_double(d2));
+            for (int r = 0; r < g.Q; ++r) st_dsmem_d2(dsmem_addr(&allp[p.rank][j], uint32_t(r)), t);
+        }
     }
     cluster_sync_all();  // every CTA's partials have landed in every CTA
     if (threadIdx.x < g.G) {
@@ -363,52 +498,43 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
             if (a.db) a.db[ch] = float(t1);
             if (a.dw) a.dw[ch] = float(t2 * double(pr.y));
         }
-        coef[threadIdx.x] = make_float2(float(t1 * double(g.inv_m)), float(t2 * double(pr.y) * double(g.inv_m)));
+        // dx = scale*(dz - c1 - xhat*c2) with c1 = mean(dz), c2 = mean(dz*xhat)
+        const double c1 = t1 * double(g.inv_m);
+        const double c2 = t2 * double(pr.y) * double(g.inv_m);
+        dxc[threadIdx.x] = TRAIN ? make_float4(pr.z, float(double(pr.z) * c1), float(double(pr.z) * c2 * double(pr.y)), pr.x)
+                                 : make_float4(pr.z, 0.f, 0.f, 0.f);
     }
     __syncthreads();
 
-    // ---- dres, dx: 16 bytes per thread and step ----
+    // ---- dres, dx: the thread's vector of each of its samples ----
     const uint64_t pol = l2_evict_first();
-    const int vps = g.span / VE;
-    for (int v = threadIdx.x; v < p.ns * vps; v += kGrpThreads) {
-        const int s = int(fast_div(uint32_t(v), g.div_vps));
-        const int o = (v - s * vps) * VE;
-        float xv[VE], dzv[VE], ov[VE];
-        grp_vec<T>(tx, s * g.span + o, xv);
-        {
-            // dz as the sums pass formed it (two 16-byte reads per 8 values)
-            const float4* zp = reinterpret_cast<const float4*>(tz + s * g.span + o);
+    if (sl.on) {
+        float2 ca[H], cb[H], cc[H], nmu[H];
 #pragma unroll
-            for (int q = 0; q < VE / 4; ++q) {
-                const float4 z4 = zp[q];
-                dzv[4 * q] = z4.x;
-                dzv[4 * q + 1] = z4.y;
-                dzv[4 * q + 2] = z4.z;
-                dzv[4 * q + 3] = z4.w;
-            }
+        for (int h = 0; h < H; ++h) {
+            const float4 q0 = dxc[sl.ch[2 * h]], q1 = dxc[sl.ch[2 * h + 1]];
+            ca[h] = make_float2(q0.x, q1.x);
+            cb[h] = make_float2(-q0.y, -q1.y);
+            cc[h] = make_float2(-q0.z, -q1.z);
+            nmu[h] = make_float2(-q0.w, -q1.w);
         }
-        int j = int(fast_div(uint32_t(o), g.div_l));
-        int next = (j + 1) * g.l;
-        float4 pr = prm[j];  // the vector may cross into the next channel(s): reloaded there
-        float2 cc = coef[j];
-#pragma unroll
-        for (int k = 0; k < VE; ++k) {
-            if (o + k == next) {
-                ++j;
-                next += g.l;
-                pr = prm[j];
-                cc = coef[j];
-            }
+        for (int s = sl.ph; s < p.ns; s += g.P) {
+            float2 dzv[H], ov[H];
+            grp_get_f32<NE>(tz + sl.at(g, s), dzv);
             if (TRAIN) {
-                const float xh = (xv[k] - pr.x) * pr.y;
-                ov[k] = pr.z * (dzv[k] - cc.x - xh * cc.y);
+                float2 xv[H];
+                grp_ld<T, NE>(tx, sl.at(g, s) * sizeof(T), xv);
+#pragma unroll
+                for (int h = 0; h < H; ++h)
+                    ov[h] = __ffma2_rn(cc[h], __fadd2_rn(xv[h], nmu[h]), __ffma2_rn(ca[h], dzv[h], cb[h]));
             } else {
-                ov[k] = dzv[k] * pr.z;
+#pragma unroll
+                for (int h = 0; h < H; ++h) ov[h] = __fmul2_rn(dzv[h], ca[h]);
             }
+            const int64_t off = (int64_t(p.n0 + s) * g.c + p.ch0) * g.l + sl.vp * NE;
+            if (dres) grp_st<T, NE>(dres + off, dzv, pol);
+            grp_st<T, NE>(dx + off, ov, pol);
         }
-        const int64_t off = (int64_t(p.n0 + s) * g.c + p.ch0) * g.l + o;
-        if (dres) store_vec_pol<T, VE>(dres + off, dzv, pol);
-        store_vec_pol<T, VE>(dx + off, ov, pol);
     }
     if (bad) {
         // the tile's copy may still be landing: wait once more (bounded) before exit
@@ -433,18 +559,24 @@ inline int64_t gcd64(int64_t u, int64_t v) {
 struct GrpPlan {
     GrpGeom g;
     int grid;
+    int threads;
     size_t smem;
 };
 
-// Chooses G and the cluster size Q (the smallest that fills the GPU while a
-// CTA's tiles fit in shared memory).  False when the shape does not suit
-// (then another path runs); `nt` tensors are staged, plus mask words if asked.
-inline bool bn_plan_group(GrpPlan& pl, const BnArgs& a, size_t es, int nt, bool dz_buffer, bool mask_words) {
+// Chooses G, the block size, the cluster size Q (the smallest that fills the
+// GPU while a CTA's tiles fit in shared memory) and the sample phases P for
+// threads that own `pos_bytes` (8 or 16) of a span each.  False when the
+// shape does not suit (then another path runs).  `nt` tensors are staged,
+// plus the backward's fp32 dz buffer and mask words if asked; `sums` reserves
+// the per-element partial sums (over the first tile when it is large enough
+// and `over_first_tile`).
+inline bool bn_plan_group(GrpPlan& pl, const BnArgs& a, size_t es, int pos_bytes, int nt, bool dz_buffer,
+                          bool mask_words, bool sums, bool over_first_tile) {
     const DevInfo* d = dev_info();
     if (!d || a.n <= 0 || a.l <= 0 || a.c <= 0) return false;
     const int64_t seg = a.l * int64_t(es);
     const int64_t G = 16 / gcd64(seg, 16);
-    if (G > kGrpWarps || a.c % G != 0) return false;
+    if (G > kGrpMaxG || a.c % G != 0) return false;
     if (a.n > (int64_t(1) << 30) || a.l > (int64_t(1) << 20)) return false;
     GrpGeom& g = pl.g;
     g.c = a.c;
@@ -452,6 +584,9 @@ inline bool bn_plan_group(GrpPlan& pl, const BnArgs& a, size_t es, int nt, bool 
     g.l = int(a.l);
     g.G = int(G);
     g.span = int(G * a.l);
+    g.vps = int(int64_t(g.span) * int64_t(es) / pos_bytes);
+    if (g.vps > kGrpMaxThreads) return false;
+    pl.threads = g.vps <= kGrpMinThreads ? kGrpMinThreads : (g.vps + 31) / 32 * 32;
     g.words = int((a.l + 31) / 32);
     const double m = double(a.n) * double(a.l);
     g.inv_m = float(1.0 / m);
@@ -459,18 +594,31 @@ inline bool bn_plan_group(GrpPlan& pl, const BnArgs& a, size_t es, int nt, bool 
     const int64_t groups = a.c / G;
     const size_t span_bytes = size_t(g.span) * es;
     const size_t cap = size_t(d->max_smem_optin) - 4096;  // room for the static shared memory
+    const int pmax = pl.threads / g.vps;
     int chosen = 0;
     for (int Q = 1; Q <= kGrpMaxQ; Q *= 2) {
         if (Q > a.n) break;
         const int64_t spc = (a.n + Q - 1) / Q;
         const size_t tile = (size_t(spc) * span_bytes + 127) / 128 * 128;
+        // samples per thread, then as few phases as give each thread that many
+        const int64_t per = (spc + pmax - 1) / pmax;
+        const int P = int((spc + per - 1) / per);
         size_t smem = size_t(nt) * tile;
         if (dz_buffer) smem += size_t(spc) * size_t(g.span) * 4;
         if (mask_words) smem += size_t(spc) * size_t(G) * size_t(g.words) * 4;
+        smem = (smem + 15) / 16 * 16;
+        const size_t part_bytes = sums ? 2 * size_t(P) * size_t(g.span) * 4 : 0;
+        uint32_t part = 0;
+        if (!(over_first_tile && part_bytes <= tile)) {
+            part = uint32_t(smem);
+            smem += part_bytes;
+        }
         if (smem > cap) continue;
         chosen = Q;
         g.spc = int(spc);
+        g.P = P;
         g.tile = uint32_t(tile);
+        g.part = part;
         pl.smem = smem;
         // enough CTAs for two per SM: the elementwise work is instruction-heavy
         if (groups * Q >= 2 * d->sms) break;
@@ -479,12 +627,6 @@ inline bool bn_plan_group(GrpPlan& pl, const BnArgs& a, size_t es, int nt, bool 
     if (groups * chosen > (int64_t(1) << 31) - 1) return false;
     g.Q = chosen;
     pl.grid = int(groups * chosen);
-    const FastDivHost fv = make_fast_div(uint32_t(g.span / (16 / es)));
-    const FastDivHost fl = make_fast_div(uint32_t(g.l));
-    g.div_vps.d = fv.d;
-    g.div_vps.m = fv.m;
-    g.div_l.d = fl.d;
-    g.div_l.m = fl.m;
     return true;
 }
 
@@ -496,7 +638,7 @@ inline nrm_status launch_group(const void* fn, const BnArgs& a, GrpPlan& pl, cud
     void* kargs[] = {&args, &geom};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(pl.grid));
-    cfg.blockDim = dim3(kGrpThreads);
+    cfg.blockDim = dim3(unsigned(pl.threads));
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -515,7 +657,7 @@ template <typename T>
 bool bn_fwd_group(const BnArgs& a, bool training, cudaStream_t s, nrm_status& st) {
     if (!aligned16(a.x) || !aligned16(a.res) || !aligned16(a.y)) return false;
     GrpPlan pl;
-    if (!bn_plan_group(pl, a, sizeof(T), a.res ? 2 : 1, false, false)) return false;
+    if (!bn_plan_group(pl, a, sizeof(T), 16, a.res ? 2 : 1, false, false, training, false)) return false;
     const void* fn = with_act(a.act, [&](auto act) {
         return training ? (const void*)&bn_fwd_group_kernel<T, true, decltype(act)::value>
                         : (const void*)&bn_fwd_group_kernel<T, false, decltype(act)::value>;
@@ -531,7 +673,8 @@ bool bn_bwd_group(const BnArgs& a, bool training, cudaStream_t s, nrm_status& st
     const bool need_z = bn_need_z(a.act, a.mask_in);
     const bool use_mask = a.act == NRM_ACT_RELU && a.mask_in != nullptr;
     GrpPlan pl;
-    if (!bn_plan_group(pl, a, sizeof(T), (need_z && a.res) ? 3 : 2, true, use_mask)) return false;
+    if (!bn_plan_group(pl, a, sizeof(T), 8, (need_z && a.res) ? 3 : 2, true, use_mask, true, true))
+        return false;
     const void* fn = with_act(a.act, [&](auto act) {
         return training ? (const void*)&bn_bwd_group_kernel<T, true, decltype(act)::value>
                         : (const void*)&bn_bwd_group_kernel<T, false, decltype(act)::value>;

@@ -214,6 +214,11 @@ __device__ __forceinline__ void st_v4_policy(void* p, uint4 v, uint64_t pol) {
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol) : "memory");
 }
 
+__device__ __forceinline__ void st_v2_policy(void* p, uint2 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "l"(pol) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // mbarriers and 1-D bulk copies (TMA) into shared memory
 // ---------------------------------------------------------------------------

@@ -76,6 +76,27 @@ def test_dropout_mask_bit_exact(orc):
         assert ((y != 0) == keep).all(), f"keep flags differ for p={p}, seed={seed}"
 
 
+def test_gelu_dense_grid_fp32(orc):
+    # GELU and GELU' in fp32 on a dense grid of z in [-12, 12] (p = 0: y = GELU(z),
+    # dx = GELU'(z) for dy = 1) against the oracle's exact values.  The kernels
+    # take Phi from the erfc approximation of Abramowitz and Stegun 7.1.26 (erf
+    # within 1.5e-7): the bound below is that, times |z|, plus fp32 rounding of
+    # the reciprocal, exponential and products, and is 10x tighter than the
+    # fp32 parity tolerance.
+    z = np.concatenate([np.linspace(-12.0, 12.0, 1_200_001), [0.0, 1e-30, -1e-30, 1e-6, -1e-6, 40.0, -40.0]])
+    x = synth.store(z, "f32", z.shape)
+    dy = synth.store(np.ones_like(z), "f32", z.shape)
+    y, dx = _run(x, dy, "gelu", 0.0, 1)
+    zf = x.f64()
+    yo = orc.act_dropout_fwd(zf, ACT_CODE["gelu"], 0.0, 1)
+    dxo = orc.act_dropout_bwd(dy.f64(), zf, ACT_CODE["gelu"], 0.0, 1)
+    bound = 1e-6 * np.maximum(1.0, np.abs(zf))
+    ey = np.abs(y - yo)
+    edx = np.abs(dx - dxo)
+    assert (ey <= bound).all(), f"GELU: max error {ey.max():.3g} at z = {zf[ey.argmax()]}"
+    assert (edx <= bound).all(), f"GELU': max error {edx.max():.3g} at z = {zf[edx.argmax()]}"
+
+
 @pytest.mark.parametrize("p", [0.0, 1.0])
 def test_dropout_extremes(orc, p):
     n = 4099
