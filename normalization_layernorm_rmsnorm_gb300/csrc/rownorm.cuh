@@ -825,9 +825,9 @@ inline bool rr_plan(RrGeom& g, int& tpr, size_t& smem, const RowArgs& a, size_t 
     if (!d || a.rows <= 0) return false;
     const int nvec = int(size_t(a.cols) * es / 16);
     tpr = 32;
-    while (tpr * kRrVpt < nvec && tpr < kRrConsumers) tpr *= 2;
+    while (tpr * kRrVpt < nvec && tpr < kRrMaxConsumers) tpr *= 2;
     if (tpr * kRrVpt < nvec) return false;
-    const int rpc = kRrConsumers / tpr;
+    const int rpc = rr_consumers(tpr) / tpr;
     const size_t row_bytes = size_t(a.cols) * (es + es_dy);  // a row of dy and a row of x
     const size_t param = (size_t(a.cols) * 4 + 127) / 128 * 128;
     const size_t cap = size_t(d->max_smem_optin) - 4096;  // room for the static shared memory
@@ -871,8 +871,8 @@ const void* rr_fn(int tpr, int nvec) {
     return nvec <= 3 * tpr ? rr_fn_v<T, LN, DB, 3, TD>(tpr) : rr_fn_v<T, LN, DB, kRrVpt, TD>(tpr);
 }
 
-// Launches a ring kernel on `grid` CTAs (one per SM at most).
-inline nrm_status rr_launch(const void* fn, const RowArgs& a, const RrGeom& g, size_t smem, int grid,
+// Launches a ring kernel (row groups of `tpr` threads) on `grid` CTAs (one per SM at most).
+inline nrm_status rr_launch(const void* fn, const RowArgs& a, const RrGeom& g, int tpr, size_t smem, int grid,
                             cudaStream_t s) {
     nrm_status st = prepare_kernel(fn, smem, false);
     if (st != NRM_OK) return st;
@@ -880,7 +880,7 @@ inline nrm_status rr_launch(const void* fn, const RowArgs& a, const RrGeom& g, s
     args.err = dev_info()->err;
     RrGeom geom = g;
     void* kargs[] = {&args, &geom};
-    return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(kRrThreads), kargs, smem, s), "row ring launch");
+    return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(rr_threads(tpr)), kargs, smem, s), "row ring launch");
 }
 
 template <typename T, bool LN, int VE, int VPT, typename TO>
@@ -980,7 +980,7 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     const int tpr = ring ? 0 : row_tpr(a.cols / ve, kRowBwdVpt, kRowMaxBwdTpr);
     const void* fn;
     int64_t groups, p;
-    int block = kRrThreads;
+    int block = 0;
     if (ring) {
         const int nv = a.cols / kVec<T>;
         fn = layernorm ? rr_fn<T, true, true>(rtpr, nv)
@@ -1003,7 +1003,7 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     if (groups < p) p = groups;
     const int P = int(p);
     if (ring && P > 0) {
-        nrm_status st = rr_launch(fn, a, rg, rsmem, P, s);
+        nrm_status st = rr_launch(fn, a, rg, rtpr, rsmem, P, s);
         if (st != NRM_OK) return st;
     } else if (P > 0) {
         RowArgs args = a;
@@ -1065,7 +1065,7 @@ nrm_status row_bwd_f32dy(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
             if (rg.chunks < p) p = rg.chunks;
             P = int(p);
             if (P > 0) {
-                nrm_status st = rr_launch(fn, a, rg, rsmem, P, s);
+                nrm_status st = rr_launch(fn, a, rg, rtpr, rsmem, P, s);
                 if (st != NRM_OK) return st;
             }
         }

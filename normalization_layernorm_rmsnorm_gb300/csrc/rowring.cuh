@@ -19,9 +19,15 @@
 
 namespace nrm {
 
-constexpr int kRrConsumerWarps = 16;
-constexpr int kRrConsumers = kRrConsumerWarps * 32;
-constexpr int kRrThreads = kRrConsumers + 32;  // + the producer warp
+// Consumer warps per CTA.  One-warp rows (TPR 32) take 15, so that the CTA
+// with its producer warp has 16 warps: 4 per SM sub-partition, and 128
+// registers per thread, enough to keep the thread's columns of the weight in
+// registers (a 17th warp would leave 96).  Wider rows take 16, a multiple of
+// their row groups.
+__host__ __device__ constexpr int rr_consumer_warps(int tpr) { return tpr == 32 ? 15 : 16; }
+__host__ __device__ constexpr int rr_consumers(int tpr) { return rr_consumer_warps(tpr) * 32; }
+__host__ __device__ constexpr int rr_threads(int tpr) { return rr_consumers(tpr) + 32; }  // + the producer warp
+constexpr int kRrMaxConsumers = 16 * 32;
 constexpr int kRrVpt = 4;                      // 16-byte vectors per thread and row, at most
 constexpr int kRrMaxSlots = 8;
 constexpr int kRrBarConsumers = 15;            // named barrier over the consumer warps
@@ -105,11 +111,11 @@ __device__ __forceinline__ void unpair(const float2 (&in)[VPT][VE / 2], float (&
 // The weight of the row as fp32 in shared memory, in rr_params2's layout
 // (consumer threads).
 template <typename T>
-__device__ __forceinline__ void rr_stage_weight(const RowArgs& a, float* wsm) {
+__device__ __forceinline__ void rr_stage_weight(const RowArgs& a, float* wsm, int consumers) {
     using bits = typename Io<T>::bits_t;
     constexpr int VE = kVec<T>;
     const int nvec = a.cols / VE;
-    for (int i = threadIdx.x; i < a.cols; i += kRrConsumers) {
+    for (int i = threadIdx.x; i < a.cols; i += consumers) {
         const int vi = i / VE, k = i - vi * VE;
         wsm[((k >> 2) * nvec + vi) * 4 + (k & 3)] = a.w ? Io<T>::load(reinterpret_cast<const bits*>(a.w)[i]) : 1.f;
     }
@@ -119,7 +125,7 @@ __device__ __forceinline__ void rr_stage_weight(const RowArgs& a, float* wsm) {
 // the row groups in group order.  Consumer threads only; `part` is scratch
 // shared memory of RPC*TPR*VE floats (the drained ring), staged element-major
 // (element k of thread t at k*TPR + t) so that the stores do not conflict.
-template <int TPR, int VPT, int VE, int RPC>
+template <int TPR, int VPT, int VE, int RPC, int NC = RPC * TPR>
 __device__ __forceinline__ void rr_partial_row(const float (&acc)[VPT][VE], float* ws, float* part, int group,
                                                int t, int cols) {
     const int nvec = cols / VE;
@@ -138,8 +144,8 @@ __device__ __forceinline__ void rr_partial_row(const float (&acc)[VPT][VE], floa
             if (j * TPR * VE >= cols) break;
 #pragma unroll
             for (int k = 0; k < VE; ++k) part[group * TPR * VE + k * TPR + t] = acc[j][k];
-            named_barrier(kRrBarConsumers, kRrConsumers);
-            for (int i = threadIdx.x; i < TPR * VE; i += kRrConsumers) {
+            named_barrier(kRrBarConsumers, NC);
+            for (int i = threadIdx.x; i < TPR * VE; i += NC) {
                 const int k = i / TPR;
                 const int col = j * TPR * VE + (i - k * TPR) * VE + k;
                 if (col < cols) {
@@ -149,7 +155,7 @@ __device__ __forceinline__ void rr_partial_row(const float (&acc)[VPT][VE], floa
                     ws[col] = sum;
                 }
             }
-            named_barrier(kRrBarConsumers, kRrConsumers);
+            named_barrier(kRrBarConsumers, NC);
         }
     }
 }
@@ -178,11 +184,16 @@ __device__ __forceinline__ void rr_load_dy(const unsigned char* dr, int vi, floa
 // TD: dy's storage type (T, or float32 when the forward kept its output in
 // float32 for a 16-bit x).
 template <typename T, bool LN, int TPR, bool DB, int VPT, typename TD = T>
-__global__ void __launch_bounds__(kRrThreads, 1)
+__global__ void __launch_bounds__(rr_threads(TPR), 1)
 row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
     constexpr int VE = kVec<T>;
     static_assert(VPT <= kRrVpt, "at most kRrVpt vectors per thread");
-    constexpr int RPC = kRrConsumers / TPR;
+    constexpr int CW = rr_consumer_warps(TPR);
+    constexpr int NC = CW * 32;
+    constexpr int RPC = NC / TPR;
+    // one-warp rows of up to 3 vectors per thread keep the thread's columns of
+    // the weight in registers (with a fourth vector's accumulators they would spill)
+    constexpr bool kRegW = TPR == 32 && VPT <= 3;
     constexpr int NW = TPR / 32;
     constexpr int NV = LN ? 2 : 1;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -201,14 +212,14 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
         s_bad = 0;
         for (int i = 0; i < g.slots; ++i) {
             mbar_init(&full[i], 33);  // the bulk copies' arrival + one per producer lane (mean/rstd)
-            mbar_init(&empty[i], kRrConsumerWarps);
+            mbar_init(&empty[i], CW);
         }
         mbar_init_fence();
     }
-    if (warp < kRrConsumerWarps) rr_stage_weight<T>(a, wsm);
+    if (warp < CW) rr_stage_weight<T>(a, wsm, NC);
     __syncthreads();
 
-    if (warp == kRrConsumerWarps) {
+    if (warp == CW) {
         rr_produce<T, LN, TD>(a, g, ring, full, empty, lane, bad);
     } else {
         const int group = threadIdx.x / TPR;
@@ -225,10 +236,23 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
         constexpr int H = VE / 2;
         float2 accw[VPT][H];
         float2 accb[VPT][H];
+        float2 wreg[kRegW ? VPT : 1][H];
 #pragma unroll
         for (int j = 0; j < VPT; ++j)
 #pragma unroll
             for (int h = 0; h < H; ++h) accw[j][h] = accb[j][h] = f2(0.f);
+        if constexpr (kRegW) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int vi = j * TPR + t;
+                if (vi < nvec) {
+                    rr_params2<VE>(wsm, vi, nvec, wreg[j]);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < H; ++h) wreg[j][h] = f2(0.f);
+                }
+            }
+        }
 
         int q = 0;
         for (int64_t c = blockIdx.x; c < g.chunks; c += gridDim.x, ++q) {
@@ -245,10 +269,13 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
                 const float mu = LN ? st[g.R + r] : 0.f;
                 const float2 rs2 = f2(rs);
                 const float2 nmu = f2(-mu);
-                // the row sums: sum(dy*w) and sum(dy*w*xhat) (LN) / sum(dy*w*x) (RMS)
-                float2 s2[NV];
+                // the row sums: sum(dy*w) and sum(dy*w*xhat) (LN) / sum(dy*w*x) (RMS),
+                // one accumulator per vector (short dependency chains)
+                float2 s2[VPT][NV];
 #pragma unroll
-                for (int i = 0; i < NV; ++i) s2[i] = f2(0.f);
+                for (int j = 0; j < VPT; ++j)
+#pragma unroll
+                    for (int i = 0; i < NV; ++i) s2[j][i] = f2(0.f);
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
                     const int vi = j * TPR + t;
@@ -256,23 +283,33 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
                         float2 dv[H], xv[H], wv[H];
                         rr_load_dy<T, TD>(dr, vi, dv);
                         unpack2<T>(*reinterpret_cast<const uint4*>(xr + size_t(vi) * 16), xv);
-                        rr_params2<VE>(wsm, vi, nvec, wv);
+                        if constexpr (kRegW) {
+#pragma unroll
+                            for (int h = 0; h < H; ++h) wv[h] = wreg[j][h];
+                        } else {
+                            rr_params2<VE>(wsm, vi, nvec, wv);
+                        }
 #pragma unroll
                         for (int h = 0; h < H; ++h) {
                             const float2 gw = __fmul2_rn(dv[h], wv[h]);
                             if constexpr (LN) {
                                 const float2 xh = __fmul2_rn(__fadd2_rn(xv[h], nmu), rs2);
-                                s2[0] = __fadd2_rn(s2[0], gw);
-                                s2[NV - 1] = __ffma2_rn(gw, xh, s2[NV - 1]);
+                                s2[j][0] = __fadd2_rn(s2[j][0], gw);
+                                s2[j][NV - 1] = __ffma2_rn(gw, xh, s2[j][NV - 1]);
                             } else {
-                                s2[0] = __ffma2_rn(gw, xv[h], s2[0]);
+                                s2[j][0] = __ffma2_rn(gw, xv[h], s2[j][0]);
                             }
                         }
                     }
                 }
                 float s[NV];
 #pragma unroll
-                for (int i = 0; i < NV; ++i) s[i] = s2[i].x + s2[i].y;
+                for (int i = 0; i < NV; ++i) {
+                    float2 acc = s2[0][i];
+#pragma unroll
+                    for (int j = 1; j < VPT; ++j) acc = __fadd2_rn(acc, s2[j][i]);
+                    s[i] = acc.x + acc.y;
+                }
                 group_sum<TPR, NV>(s, &red[group][0], phase, group);
                 const float c1 = s[0] * inv_cols;
                 const float c2 = LN ? s[NV - 1] * inv_cols : c1 * rs * rs;
@@ -286,7 +323,12 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
                         float2 dv[H], xv[H], wv[H], o[H];
                         rr_load_dy<T, TD>(dr, vi, dv);
                         unpack2<T>(*reinterpret_cast<const uint4*>(xr + size_t(vi) * 16), xv);
-                        rr_params2<VE>(wsm, vi, nvec, wv);
+                        if constexpr (kRegW) {
+#pragma unroll
+                            for (int h = 0; h < H; ++h) wv[h] = wreg[j][h];
+                        } else {
+                            rr_params2<VE>(wsm, vi, nvec, wv);
+                        }
 #pragma unroll
                         for (int h = 0; h < H; ++h) {
                             const float2 gw = __fmul2_rn(dv[h], wv[h]);
@@ -314,17 +356,18 @@ row_bwd_ring_kernel(const RowArgs a, const RrGeom g) {
         // the column-sum kernel may be scheduled now; it waits for this grid
         pdl_trigger();
         // every chunk has been consumed (and its copies have landed): the ring is scratch now
-        named_barrier(kRrBarConsumers, kRrConsumers);
+        named_barrier(kRrBarConsumers, NC);
         float* part = reinterpret_cast<float*>(ring);
         float acc[VPT][VE];
         if (a.ws_dw) {
             unpair<VPT, VE>(accw, acc);
-            rr_partial_row<TPR, VPT, VE, RPC>(acc, a.ws_dw + int64_t(blockIdx.x) * cols, part, group, t, cols);
+            rr_partial_row<TPR, VPT, VE, RPC, NC>(acc, a.ws_dw + int64_t(blockIdx.x) * cols, part, group, t, cols);
         }
         if constexpr (DB) {
             if (a.ws_db) {
                 unpair<VPT, VE>(accb, acc);
-                rr_partial_row<TPR, VPT, VE, RPC>(acc, a.ws_db + int64_t(blockIdx.x) * cols, part, group, t, cols);
+                rr_partial_row<TPR, VPT, VE, RPC, NC>(acc, a.ws_db + int64_t(blockIdx.x) * cols, part, group, t,
+                                                      cols);
             }
         }
     }
