@@ -205,25 +205,34 @@ row_fwd_kernel(const RowArgs a) {
         // row of the group loaded while this one is normalised
         constexpr int H = VE / 2;
         // this thread's columns of w and b, the same for every row: for one-warp
-        // rows (short rows, where per-row work is small) loaded once and kept
-        // packed; wider rows reload them per row (registers for occupancy)
+        // rows (short rows, where per-row work is small) loaded once, as fp32
+        // pairs for up to 3 vectors per thread and as packed T for 4 (fp32
+        // pairs would take 32 more registers there); wider rows reload them
+        // per row (registers for occupancy)
         constexpr bool kHoist = TPR == 32;
-        Pack<T, VE> wpk[kHoist ? VPT : 1], bpk[kHoist ? VPT : 1];
+        constexpr bool kHoistF = kHoist && VPT <= 3;
+        float2 wf[kHoistF ? VPT : 1][H], bf[kHoistF ? VPT : 1][H];
+        Pack<T, VE> wpk[kHoist && !kHoistF ? VPT : 1], bpk[kHoist && !kHoistF ? VPT : 1];
         if constexpr (kHoist) {
-            Pack<T, VE> one, zero;
-#pragma unroll
-            for (int k = 0; k < VE; ++k) {
-                one.b[k] = Io<T>::store(1.f);
-                zero.b[k] = Io<T>::store(0.f);
-            }
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
                 const int vi = j * TPR + t;
-                wpk[j] = one;
-                bpk[j] = zero;
+                Pack<T, VE> pw, pb;
+#pragma unroll
+                for (int k = 0; k < VE; ++k) {
+                    pw.b[k] = Io<T>::store(1.f);
+                    pb.b[k] = Io<T>::store(0.f);
+                }
                 if (vi < nvec) {
-                    if (a.w) wpk[j].u = ld_cached_v4(reinterpret_cast<const T*>(a.w) + int64_t(vi) * VE);
-                    if (a.b) bpk[j].u = ld_cached_v4(reinterpret_cast<const T*>(a.b) + int64_t(vi) * VE);
+                    if (a.w) pw.u = ld_cached_v4(reinterpret_cast<const T*>(a.w) + int64_t(vi) * VE);
+                    if (a.b) pb.u = ld_cached_v4(reinterpret_cast<const T*>(a.b) + int64_t(vi) * VE);
+                }
+                if constexpr (kHoistF) {
+                    unpack2<T>(pw.u, wf[j]);
+                    unpack2<T>(pb.u, bf[j]);
+                } else {
+                    wpk[j] = pw;
+                    bpk[j] = pb;
                 }
             }
         }
@@ -277,9 +286,15 @@ row_fwd_kernel(const RowArgs a) {
                 const int vi = j * TPR + t;
                 if (vi < nvec) {
                     float2 wv[H], bv[H], o[H];
-                    if constexpr (kHoist) {
+                    if constexpr (kHoistF) {
+#pragma unroll
+                        for (int h = 0; h < H; ++h) {
+                            wv[h] = wf[j][h];
+                            bv[h] = bf[j][h];  // LayerNorm's bias, or RMSNorm's optional one (else 0)
+                        }
+                    } else if constexpr (kHoist) {
                         unpack2<T>(wpk[j].u, wv);
-                        unpack2<T>(bpk[j].u, bv);  // LayerNorm's bias, or RMSNorm's optional one (else 0)
+                        unpack2<T>(bpk[j].u, bv);
                     } else {
                         if (a.w) {
                             unpack2<T>(ld_cached_v4(reinterpret_cast<const T*>(a.w) + int64_t(vi) * VE), wv);
