@@ -25,9 +25,14 @@
 //     a bookkeeper warp publishes the CTA's partial sums (release counter per
 //     channel), merges a channel's S partials in one fixed order once they
 //     have all arrived and hands the second team the coefficients.
-//   * Eval, 16-byte vectors (bn_fwd_eval_kernel / bn_bwd_eval_kernel below):
-//     the same rings with one pass per round, coefficients from the running
-//     statistics.
+//   * Eval forward, 16-byte vectors (bn_fwd_eval_stream_kernel below): the
+//     output is elementwise once the running statistics fix the coefficients,
+//     so warps stream blocks of vectors through registers with a per-CTA table
+//     of (scale, shift); more than kEsMaxChannels channels take the ring
+//     kernel below.
+//   * Eval backward, 16-byte vectors (bn_bwd_eval_kernel below), and the eval
+//     forward for very many channels (bn_fwd_eval_kernel): the same rings with
+//     one pass per round, coefficients from the running statistics.
 //   * Channel-group kernels (batchnorm_group.cuh): short segments, staged
 //     whole in shared memory by a thread-block cluster per channel group.
 //   * Scalar kernels (bn_fwd_kernel / bn_bwd_kernel with VE = 1): tensors not
@@ -726,6 +731,85 @@ bn_fwd_eval_kernel(const BnArgs a, const BnGeom g) {
     __syncthreads();
     if (threadIdx.x == 0 && sh.abort) atomicOr(a.err, kErrTimeoutStage);
     if (bad && lane == 0) atomicOr(a.err, kErrTimeoutStage);
+}
+
+// ---------------------------------------------------------------------------
+// eval forward, streamed through registers
+// ---------------------------------------------------------------------------
+// y = act(x*scale[c] + shift[c] (+ residual)) is elementwise once the running
+// statistics fix the coefficients, so the eval forward needs no rounds: every
+// warp takes kEsUnroll consecutive blocks of 32 vectors (loads first, then the
+// arithmetic), and a per-CTA table in shared memory holds (scale, shift) of
+// every channel.
+constexpr int kEsThreads = 256;
+constexpr int kEsWarps = kEsThreads / 32;
+constexpr int kEsUnroll = 4;
+constexpr int kEsMaxChannels = 4096;
+
+template <typename T, int ACT>
+__global__ void __launch_bounds__(kEsThreads)
+bn_fwd_eval_stream_kernel(const BnArgs a, const BnGeom g, const FastDiv div_c, const uint32_t nblocks) {
+    constexpr int VE = kVec<T>;
+    constexpr int U = kEsUnroll;
+    __shared__ float2 coef[kEsMaxChannels];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    for (int ch = threadIdx.x; ch < int(g.c); ch += kEsThreads) {
+        const float wc = a.w ? a.w[ch] : 1.f;
+        const float bc = a.b ? a.b[ch] : 0.f;
+        const float rs = rsqrtf(a.rv[ch] + a.eps);
+        const float mu = a.rm[ch];
+        coef[ch] = make_float2(wc * rs, bc - mu * wc * rs);
+        if (blockIdx.x == 0) {
+            if (a.save_mean) a.save_mean[ch] = mu;
+            if (a.save_rstd) a.save_rstd[ch] = rs;
+        }
+    }
+    __syncthreads();
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    const T* __restrict__ res = reinterpret_cast<const T*>(a.res);
+    T* __restrict__ y = reinterpret_cast<T*>(a.y);
+    const uint64_t pol = l2_evict_first();
+    const uint32_t step = gridDim.x * kEsWarps * U;
+    for (uint32_t b0 = (blockIdx.x * kEsWarps + warp) * U; b0 < nblocks; b0 += step) {
+        Pack<T, VE> px[U], pr[U];
+        BlockPos p[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t b = b0 + u;
+            const uint32_t seg = fast_div(b < nblocks ? b : 0u, g.div_nbs);
+            p[u].ni = 0;
+            p[u].bs = b - seg * uint32_t(g.nbs);
+            p[u].v = int(p[u].bs) * 32 + lane;
+            p[u].seg = int64_t(seg);
+            if (b < nblocks && p[u].v < g.lv) {
+                raw_load_pol<T, VE>(x, p[u].seg * g.lv + p[u].v, px[u], pol);
+                if (res) raw_load_pol<T, VE>(res, p[u].seg * g.lv + p[u].v, pr[u], pol);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (b0 + u >= nblocks) break;  // the same for the whole warp
+            const uint32_t seg = uint32_t(p[u].seg);
+            const uint32_t ch = seg - fast_div(seg, div_c) * uint32_t(g.c);
+            const float2 sc = coef[ch];
+            uint32_t nib = 0;
+            if (p[u].v < g.lv) {
+                float v[VE], rr[VE], o[VE];
+                unpack<T, VE>(px[u], v);
+                if (res) unpack<T, VE>(pr[u], rr);
+#pragma unroll
+                for (int k = 0; k < VE; ++k) {
+                    float z = fmaf(v[k], sc.x, sc.y);
+                    if (res) z += rr[k];
+                    nib |= uint32_t(z > 0.f) << k;
+                    o[k] = act_forward_c<ACT>(z, a.act_param, a.act);
+                }
+                store_vec_pol<T, VE>(y + (p[u].seg * g.lv + p[u].v) * VE, o, pol);
+            }
+            if (a.mask) store_mask_bits<VE>(a.mask, g, p[u], lane, nib);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1484,6 +1568,31 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
                                       kTrThreads, kBnL2BudgetTrainFwd);
         if (st != NRM_OK) return st;
         return launch_bn(fn, a, pl, ws, ws_bytes, s, kTrThreads, true);
+    }
+    if (vec && a.c > 0 && a.n * a.l > 0 && a.c <= kEsMaxChannels) {
+        BnGeom g;
+        bn_geometry(g, a, kVec<T>);
+        const uint64_t nblocks = uint64_t(a.n) * uint64_t(a.c) * uint64_t(g.nbs);
+        if (nblocks < (uint64_t(1) << 31)) {
+            const void* fn = with_act(a.act, [&](auto act) {
+                return (const void*)&bn_fwd_eval_stream_kernel<T, decltype(act)::value>;
+            });
+            const DevInfo* d = dev_info();
+            const int occ = cached_occupancy(fn, kEsThreads, 0);
+            if (occ < 1) return fail(NRM_ERR_CUDA, "batchnorm eval kernel cannot be resident");
+            const uint64_t per_cta = uint64_t(kEsWarps) * kEsUnroll;
+            uint64_t grid = (nblocks + per_cta - 1) / per_cta;
+            if (grid > uint64_t(occ) * d->sms) grid = uint64_t(occ) * d->sms;
+            const FastDivHost fc = make_fast_div(uint32_t(a.c));
+            FastDiv div_c;
+            div_c.d = fc.d;
+            div_c.m = fc.m;
+            BnArgs args = a;
+            uint32_t nb = uint32_t(nblocks);
+            void* kargs[] = {&args, &g, &div_c, &nb};
+            return cuda_status(cudaLaunchKernel(fn, dim3(unsigned(grid)), dim3(kEsThreads), kargs, 0, s),
+                               "batchnorm eval launch");
+        }
     }
     if (vec && a.c > 0 && a.n * a.l > 0) {
         const void* fn = with_act(a.act, [&](auto act) {
