@@ -162,7 +162,7 @@ def _bn_res_relu(cfg, dev, f32):
     erv = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,)).torch(dev)
     esm, esr = f32(c), f32(c)
     eval_name = cfg.name + "_eval"
-    calls.append(Call(eval_name, "fwd", "bn_fwd_eval_kernel<f32,relu>",
+    calls.append(Call(eval_name, "fwd", "bn_fwd_eval_stream_kernel<f32,relu>",
                       lambda: nrm.nrm_batchnorm_fwd(bx, bres, bw, bb, by, erm, erv, esm, esr, bmask,
                                                     cfg.eps, cfg.momentum, False, "relu", bws),
                       nbytes(bx, bres, by, bmask, bw, bb, erm, erv, esm, esr), 1,
