@@ -74,6 +74,22 @@ def test_bn_odd_shapes(orc, dtype, shape):
                    f"bn {dtype} {shape} training={training} act={act} res={with_res} mask={use_mask}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bn_eval_forward_both_paths(orc, dtype):
+    # the eval forward streams through registers with a per-CTA table of up to
+    # 4096 channels' coefficients; more channels take the ring kernel.  Both,
+    # with the ReLU mask and a residual, with a ragged last block per segment
+    for n, c, l in ((3, 4096, 40), (2, 4104, 24)):
+        cfg = synth.BnConfig("evc", n, c, l, dtype, 1e-5, 0.1, seed=640 + c % 97, act="relu",
+                             residual=True, x_kind="offset_scale", w_std=0.2, b_std=0.2)
+        inp = synth.bn_inputs(cfg)
+        inp["running_mean"] = synth.store(0.2 * synth.normal(cfg.seed, 20, c), "f32", (c,))
+        inp["running_var"] = synth.store(0.5 + synth.uniform(cfg.seed, 21, c), "f32", (c,))
+        got = run_bn(inp, dtype, cfg.eps, cfg.momentum, False, "relu", True, True)
+        want = oracle_bn(orc, inp, cfg.eps, cfg.momentum, False, "relu", True)
+        compare_bn(got, want, dtype, False, "relu", f"bn eval {dtype} [{n},{c},{l}]")
+
+
 @pytest.mark.parametrize("act", ["none", "relu", "gelu"])
 def test_bn_without_affine_or_running_stats(orc, act):
     n, c, l = 6, 5, 200
