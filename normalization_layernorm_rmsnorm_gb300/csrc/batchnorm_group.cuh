@@ -22,7 +22,7 @@
 
 namespace nrm {
 
-constexpr int kGrpMinThreads = 256;   // one warp per channel of a group (G <= 8), at least
+constexpr int kGrpMinThreads = 512;   // threads per CTA, at least (one warp per channel of a group needs 256)
 constexpr int kGrpMaxThreads = 1024;  // spans of up to 1024 vectors
 constexpr int kGrpMaxG = 8;           // channels per group, at most
 constexpr int kGrpMaxQ = 8;           // CTAs per cluster, at most
@@ -620,8 +620,9 @@ inline bool bn_plan_group(GrpPlan& pl, const BnArgs& a, size_t es, int pos_bytes
         g.tile = uint32_t(tile);
         g.part = part;
         pl.smem = smem;
-        // enough CTAs for two per SM: the elementwise work is instruction-heavy
-        if (groups * Q >= 2 * d->sms) break;
+        // enough CTAs for 1.5 per SM (512-thread CTAs, two fit an SM): measured on the fp16
+        // [128,512,7,7] workload against 256-thread CTAs at two to four per SM
+        if (2 * groups * Q >= 3 * d->sms) break;
     }
     if (chosen == 0) return false;
     if (groups * chosen > (int64_t(1) << 31) - 1) return false;
