@@ -60,8 +60,8 @@ constexpr int kTfSlotsA = 4;     // x (L2) and the residual (HBM) of the apply p
 // backward roles: warps [0, 8) pass 1, [8, 16) pass 2, then two producers and the bookkeeper
 constexpr int kTbP1Warps = 8;
 constexpr int kTbP2Warps = 8;
-constexpr int kTbSlots1 = 4;     // dy, x (+ residual), mask words of pass 1 (HBM)
-constexpr int kTbSlots2 = 2;     // the same, re-read for pass 2 (L2)
+constexpr int kTbSlots1 = 3;     // dy, x (+ residual), mask words of pass 1 (HBM)
+constexpr int kTbSlots2 = 3;     // the same, re-read for pass 2 (L2)
 constexpr int kTrProducer1 = 16;
 constexpr int kTrProducer2 = 17;
 constexpr int kTrBookkeeper = 18;
