@@ -598,11 +598,11 @@ __device__ __forceinline__ uint64_t warp_now() {
 // eval mode on the ring: one pass per round, coefficients from the running
 // statistics (no channel depends on another CTA)
 // ---------------------------------------------------------------------------
-// Roles: 16 consumer warps, a producer warp, and a bookkeeper warp that stages
+// Roles: 12 consumer warps, a producer warp, and a bookkeeper warp that stages
 // each round's channel parameters ahead of the consumers (and, backward,
 // publishes the CTA's sums; the last slice of a channel to publish merges
 // dw, db).
-constexpr int kEvConsumerWarps = 16;
+constexpr int kEvConsumerWarps = 12;
 constexpr int kEvThreads = (kEvConsumerWarps + 2) * 32;
 constexpr int kEvSlotsFwd = 7;
 constexpr int kEvSlotsBwd = 6;
