@@ -159,8 +159,8 @@ NRM_API nrm_status nrm_layernorm_bwd(const void *dy, const void *x, const void *
  * exits.  cols must be <= 65536 (else NRM_ERR_UNSUPPORTED); the call allocates
  * nothing.  The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current.  All calls share the one
- * array, so calls that overlap on
- * the GPU (unordered streams) race on it; calls ordered on one stream are safe.
+ * array, so calls that overlap on the GPU (unordered streams) race on it;
+ * calls ordered on one stream are safe.
  * Its contents need no initialisation: every call writes each partial value it
  * reads.  The looked-up address is kept for the life of the process: do not
  * reset a device (cudaDeviceReset) or destroy its primary context while the
