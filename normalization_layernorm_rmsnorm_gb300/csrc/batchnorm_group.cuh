@@ -316,8 +316,7 @@ bn_fwd_group_kernel(const BnArgs a, const GrpGeom g) {
             for (int h = 0; h < H; ++h) {
                 float2 z = __ffma2_rn(xv[h], sc[h], sh[h]);
                 if (res) z = __fadd2_rn(z, rv[h]);
-                ov[h] = make_float2(act_forward_c<ACT>(z.x, a.act_param, a.act),
-                                    act_forward_c<ACT>(z.y, a.act_param, a.act));
+                ov[h] = act_forward2_c<ACT>(z, a.act_param, a.act);
             }
             grp_st<T, NE>(y + (int64_t(p.n0 + s) * g.c + p.ch0) * g.l + sl.vp * NE, ov, pol);
         }
@@ -444,8 +443,7 @@ bn_bwd_group_kernel(const BnArgs a, const GrpGeom g) {
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
                     const float2 z = __fadd2_rn(__ffma2_rn(xv[h], sc[h], sh[h]), rv[h]);
-                    dz[h] = __fmul2_rn(dyv[h], make_float2(act_derivative_c<ACT>(z.x, a.act_param, a.act),
-                                                           act_derivative_c<ACT>(z.y, a.act_param, a.act)));
+                    dz[h] = __fmul2_rn(dyv[h], act_derivative2_c<ACT>(z, a.act_param, a.act));
                 }
             } else {
 #pragma unroll

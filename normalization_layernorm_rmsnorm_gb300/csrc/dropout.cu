@@ -79,6 +79,16 @@ __device__ __forceinline__ float drop_elem(float xv, float dyv, uint32_t word, c
     else return act_forward_c<ACT>(xv, a.act_param, a.act) * a.scale;
 }
 
+// drop_elem for GELU on two elements at once: the same products in the same
+// order (GELU(x)*scale, dy*scale*GELU'(x)), each lane bitwise drop_elem's.
+template <bool BWD>
+__device__ __forceinline__ float2 drop_pair_gelu(float2 xv, float2 dyv, uint32_t w0, uint32_t w1, const DropArgs& a) {
+    float2 o;
+    if constexpr (BWD) o = __fmul2_rn(__fmul2_rn(dyv, act_pair(a.scale)), gelu_grad2_f(xv));
+    else o = __fmul2_rn(gelu2_f(xv), act_pair(a.scale));
+    return make_float2(w0 < a.thresh_w ? 0.f : o.x, w1 < a.thresh_w ? 0.f : o.y);
+}
+
 // One element by scalar accesses (tails and unaligned tensors).
 template <typename T, int ACT, bool BWD>
 __device__ __forceinline__ void drop_scalar(const DropArgs& a, int64_t e, uint32_t word) {
@@ -119,10 +129,23 @@ act_dropout_vec_kernel(const DropArgs a) {
 #pragma unroll
                 for (int q = 0; q < V / 4; ++q) {
                     const uint4 r = drop_words(uint64_t(v) * (V / 4) + q, a);
+                    if constexpr (ACT == NRM_ACT_GELU) {
+                        // pairs of elements on packed fp32
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        o[4 * q + k] = drop_elem<ACT, BWD>(xv[u][4 * q + k], BWD ? dv[u][4 * q + k] : 0.f,
-                                                           word_of(r, k), a);
+                        for (int k = 0; k < 4; k += 2) {
+                            const float2 o2 = drop_pair_gelu<BWD>(
+                                make_float2(xv[u][4 * q + k], xv[u][4 * q + k + 1]),
+                                BWD ? make_float2(dv[u][4 * q + k], dv[u][4 * q + k + 1]) : make_float2(0.f, 0.f),
+                                word_of(r, k), word_of(r, k + 1), a);
+                            o[4 * q + k] = o2.x;
+                            o[4 * q + k + 1] = o2.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            o[4 * q + k] = drop_elem<ACT, BWD>(xv[u][4 * q + k], BWD ? dv[u][4 * q + k] : 0.f,
+                                                               word_of(r, k), a);
+                    }
                 }
                 store_vec<T, V>(out + v * V, o);
             }
