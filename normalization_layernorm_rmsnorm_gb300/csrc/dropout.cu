@@ -28,8 +28,7 @@
 
 namespace nrm {
 
-constexpr int kDropThreads = 256;
-constexpr int kDropUnroll = 1;  // 16-byte vectors per thread and iteration (2 and 4 measured slower)
+constexpr int kDropThreads = 512;  // 128 / 256 / 512 measured 99.5 / 98.3 / 96.3 us (GELU forward, fp16 [25216,3072])
 
 constexpr int kPhiloxRounds = 10;
 
@@ -100,56 +99,41 @@ __device__ __forceinline__ void drop_scalar(const DropArgs& a, int64_t e, uint32
 }
 
 // 16-byte vectors (every pointer 16-byte aligned); the count % V tail elements
-// by scalar accesses.
+// by scalar accesses.  The element arithmetic runs on fp32 pairs, converted
+// from and to T two elements per instruction.  (Loading a thread's next
+// vector before computing the current one was measured slower: the kernel is
+// bound by instruction issue, not by load latency.)
 template <typename T, int ACT, bool BWD>
 __global__ void __launch_bounds__(kDropThreads)
 act_dropout_vec_kernel(const DropArgs a) {
     constexpr int V = kVec<T>;  // elements per vector: 4 (fp32) or 8 (16-bit)
+    constexpr int H = V / 2;
     const int64_t nvec = a.count / V;
     const int64_t stride = int64_t(gridDim.x) * kDropThreads;
     const int64_t t0 = int64_t(blockIdx.x) * kDropThreads + threadIdx.x;
     const T* x = reinterpret_cast<const T*>(a.x);
     const T* dy = reinterpret_cast<const T*>(a.dy);
     T* out = reinterpret_cast<T*>(BWD ? a.dx : a.y);
-    for (int64_t v0 = t0; v0 < nvec; v0 += kDropUnroll * stride) {
-        float xv[kDropUnroll][V], dv[kDropUnroll][V];
+    for (int64_t v = t0; v < nvec; v += stride) {
+        float2 xv[H], dv[H], o[H];
+        unpack2<T>(ld_stream_v4(x + v * V), xv);
+        if (BWD) unpack2<T>(ld_stream_v4(dy + v * V), dv);
 #pragma unroll
-        for (int u = 0; u < kDropUnroll; ++u) {
-            const int64_t v = v0 + u * stride;
-            if (v < nvec) {
-                load_vec<T, V>(x + v * V, xv[u]);
-                if (BWD) load_vec<T, V>(dy + v * V, dv[u]);
-            }
-        }
+        for (int q = 0; q < V / 4; ++q) {
+            const uint4 r = drop_words(uint64_t(v) * (V / 4) + q, a);
 #pragma unroll
-        for (int u = 0; u < kDropUnroll; ++u) {
-            const int64_t v = v0 + u * stride;
-            if (v < nvec) {
-                float o[V];
-#pragma unroll
-                for (int q = 0; q < V / 4; ++q) {
-                    const uint4 r = drop_words(uint64_t(v) * (V / 4) + q, a);
-                    if constexpr (ACT == NRM_ACT_GELU) {
-                        // pairs of elements on packed fp32
-#pragma unroll
-                        for (int k = 0; k < 4; k += 2) {
-                            const float2 o2 = drop_pair_gelu<BWD>(
-                                make_float2(xv[u][4 * q + k], xv[u][4 * q + k + 1]),
-                                BWD ? make_float2(dv[u][4 * q + k], dv[u][4 * q + k + 1]) : make_float2(0.f, 0.f),
-                                word_of(r, k), word_of(r, k + 1), a);
-                            o[4 * q + k] = o2.x;
-                            o[4 * q + k + 1] = o2.y;
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            o[4 * q + k] = drop_elem<ACT, BWD>(xv[u][4 * q + k], BWD ? dv[u][4 * q + k] : 0.f,
-                                                               word_of(r, k), a);
-                    }
+            for (int k = 0; k < 4; k += 2) {
+                const int h = 2 * q + k / 2;
+                const float2 d = BWD ? dv[h] : make_float2(0.f, 0.f);
+                if constexpr (ACT == NRM_ACT_GELU) {  // both elements on packed fp32
+                    o[h] = drop_pair_gelu<BWD>(xv[h], d, word_of(r, k), word_of(r, k + 1), a);
+                } else {
+                    o[h] = make_float2(drop_elem<ACT, BWD>(xv[h].x, d.x, word_of(r, k), a),
+                                       drop_elem<ACT, BWD>(xv[h].y, d.y, word_of(r, k + 1), a));
                 }
-                store_vec<T, V>(out + v * V, o);
             }
         }
+        st_v4(out + v * V, pack2x<T>(o));
     }
     // the tail: fewer than V elements after the last whole vector
     const int64_t e = nvec * V + t0;
@@ -185,7 +169,7 @@ nrm_status act_dropout_launch(const DropArgs& a, int act, bool vec, cudaStream_t
         return vec ? (const void*)&act_dropout_vec_kernel<T, A, BWD>
                    : (const void*)&act_dropout_scalar_kernel<T, A, BWD>;
     });
-    const int64_t items = vec ? (a.count / kVec<T> + kDropUnroll - 1) / kDropUnroll : (a.count + 3) / 4;
+    const int64_t items = vec ? a.count / kVec<T> : (a.count + 3) / 4;
     int64_t blocks = (items + kDropThreads - 1) / kDropThreads;
     const int occ = cached_occupancy(fn, kDropThreads, 0);
     if (occ <= 0) return fail(NRM_ERR_CUDA, "activation-dropout kernel cannot be resident");

@@ -126,55 +126,6 @@ __device__ __forceinline__ void load_row(const T* base, int64_t row, int cols, i
     }
 }
 
-// The element loops of the 16-byte vector paths work on pairs of fp32 values
-// with Blackwell's packed FP32 instructions (add/mul/fma.rn.f32x2): two
-// elements per instruction, each rounded as the scalar instruction would.
-template <typename T> constexpr int kPairs = kVec<T> / 2;
-
-template <typename T> __device__ __forceinline__ float2 cvt2(uint32_t w);
-template <> __device__ __forceinline__ float2 cvt2<__half>(uint32_t w) {
-    return __half22float2(*reinterpret_cast<const __half2*>(&w));
-}
-template <> __device__ __forceinline__ float2 cvt2<__nv_bfloat16>(uint32_t w) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-}
-template <typename T> __device__ __forceinline__ uint32_t pack2(float2 v);
-template <> __device__ __forceinline__ uint32_t pack2<__half>(float2 v) {
-    const __half2 h = __float22half2_rn(v);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float2 v) {
-    const __nv_bfloat162 h = __float22bfloat162_rn(v);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// 16 raw bytes as fp32 pairs.
-template <typename T>
-__device__ __forceinline__ void unpack2(const uint4 u, float2 (&v)[kPairs<T>]) {
-    if constexpr (sizeof(T) == 4) {
-        v[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
-        v[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
-    } else {
-        v[0] = cvt2<T>(u.x);
-        v[1] = cvt2<T>(u.y);
-        v[2] = cvt2<T>(u.z);
-        v[3] = cvt2<T>(u.w);
-    }
-}
-
-// fp32 pairs rounded to T, as 16 raw bytes.
-template <typename T>
-__device__ __forceinline__ uint4 pack2x(const float2 (&o)[kPairs<T>]) {
-    if constexpr (sizeof(T) == 4)
-        return make_uint4(__float_as_uint(o[0].x), __float_as_uint(o[0].y), __float_as_uint(o[1].x),
-                          __float_as_uint(o[1].y));
-    else
-        return make_uint4(pack2<T>(o[0]), pack2<T>(o[1]), pack2<T>(o[2]), pack2<T>(o[3]));
-}
-
-__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
-__device__ __forceinline__ float2 f2neg(float2 v) { return make_float2(-v.x, -v.y); }
-
 // ---------------------------------------------------------------------------
 // forward, rows held in registers
 // ---------------------------------------------------------------------------
