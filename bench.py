@@ -267,7 +267,7 @@ def run_gpu(args, world, rank, local):
                 "bytes_per_launch": dom.bytes, "launch_us": round(dom_t * 1e3, 2),
                 "peak_source": peak_src}
 
-    e2e = run_e2e(calls, args, stream, step_bytes, world)
+    e2e = run_e2e([calls, workloads.build_calls(dev)], args, stream, step_bytes, world)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
@@ -310,43 +310,65 @@ def per_workload(calls, peak):
     return per
 
 
-def run_e2e(calls, args, stream, step_bytes, world):
+def run_e2e(call_sets, args, stream, step_bytes, world):
     """Same step through host buffers, inside the timed region: every input
     uploaded from pinned host memory before the call that first reads it,
     every output downloaded after the call that last writes it.  Uploads and
     downloads run on their own streams, so they overlap each other and the
-    other calls' kernels; a step's uploads wait for the previous step's
-    kernels (which read those inputs) and its kernels for the previous step's
-    downloads (which read their outputs)."""
+    other calls' kernels.  Two sets of device buffers alternate between steps:
+    a step's uploads wait only for the kernels of the step two before (which
+    read the same buffers) and its kernels only for that step's downloads, so
+    the host link carries both directions at once throughout.  The pinned
+    host buffers are shared by the two sets (uploads only read them; the
+    downloads into them are ordered on one stream)."""
     import collections
 
     import torch
-    first_read, last_write = {}, {}
-    for i, c in enumerate(calls):
-        for t in c.inputs:
-            first_read.setdefault(id(t), (i, t))
-        for t in c.outputs:
-            last_write[id(t)] = (i, t)
-    up = collections.defaultdict(list)
-    down = collections.defaultdict(list)
-    for i, t in first_read.values():
-        up[i].append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())))
-    for i, t in last_write.values():
-        down[i].append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)))
-    h2d = sum(t.numel() * t.element_size() for lst in up.values() for t, _ in lst)
-    d2h = sum(t.numel() * t.element_size() for lst in down.values() for t, _ in lst)
-    steps = max(1, min(args.steps, 5))
+
+    def plan(calls):
+        # inputs that no earlier call of the step writes come from the host;
+        # what a call writes (saved statistics, the ReLU mask) stays on the
+        # device for the calls that read it later
+        first_read, last_write, written = {}, {}, set()
+        for i, c in enumerate(calls):
+            for t in c.inputs:
+                if id(t) not in written:
+                    first_read.setdefault(id(t), (i, t))
+            for t in c.outputs:
+                written.add(id(t))
+                last_write[id(t)] = (i, t)
+        up = collections.defaultdict(list)
+        down = collections.defaultdict(list)
+        for i, t in first_read.values():
+            up[i].append(t)
+        for i, t in last_write.values():
+            down[i].append(t)
+        return up, down
+
+    plans = [plan(calls) for calls in call_sets]
+    up0, down0 = plans[0]
+    host_up = {i: [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for t in lst]
+               for i, lst in up0.items()}
+    host_down = {i: [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in lst] for i, lst in down0.items()}
+    for up, down in plans[1:]:  # the sets are built alike: the same tensors in the same order
+        assert {i: [t.shape for t in l] for i, l in up.items()} == {i: [t.shape for t in l] for i, l in up0.items()}
+        assert {i: [t.shape for t in l] for i, l in down.items()} == {i: [t.shape for t in l] for i, l in down0.items()}
+    h2d = sum(t.numel() * t.element_size() for lst in host_up.values() for t in lst)
+    d2h = sum(t.numel() * t.element_size() for lst in host_down.values() for t in lst)
+    steps = max(2, min(args.steps, 10))
     h2d_s = torch.cuda.Stream()
     d2h_s = torch.cuda.Stream()
 
-    def step(prev):
-        if prev is not None:
+    def step(k, prev):
+        calls = call_sets[k % len(call_sets)]
+        up, down = plans[k % len(call_sets)]
+        if prev is not None:  # the last step on the same device buffers
             h2d_s.wait_event(prev[0])
             stream.wait_event(prev[1])
         up_done = []
         with torch.cuda.stream(h2d_s):
             for i in range(len(calls)):
-                for d, h in up[i]:
+                for d, h in zip(up[i], host_up.get(i, [])):
                     d.copy_(h, non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(h2d_s)
@@ -360,7 +382,7 @@ def run_e2e(calls, args, stream, step_bytes, world):
                 ev.record(stream)
                 d2h_s.wait_event(ev)
                 with torch.cuda.stream(d2h_s):
-                    for d, h in down[i]:
+                    for d, h in zip(down[i], host_down[i]):
                         h.copy_(d, non_blocking=True)
         kernels_done = torch.cuda.Event()
         kernels_done.record(stream)
@@ -369,7 +391,8 @@ def run_e2e(calls, args, stream, step_bytes, world):
         return kernels_done, copies_done
 
     torch.cuda.synchronize()
-    step(None)
+    for k in range(len(call_sets)):
+        step(k, None)
     torch.cuda.synchronize()
     barrier()
     s = torch.cuda.Event(enable_timing=True)
@@ -377,17 +400,19 @@ def run_e2e(calls, args, stream, step_bytes, world):
     s.record(stream)
     h2d_s.wait_event(s)
     d2h_s.wait_event(s)
-    prev = None
-    for _ in range(steps):
-        prev = step(prev)
-    stream.wait_event(prev[1])  # the last downloads are inside the timed region
+    prev = [None] * len(call_sets)
+    last = None
+    for k in range(steps):
+        last = prev[k % len(call_sets)] = step(k, prev[k % len(call_sets)])
+    stream.wait_event(last[1])  # the last downloads are inside the timed region
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
     ms, gbs = aggregate(ms, step_bytes, world)
     return {"value": round(gbs, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": steps,
-            "overlap": "uploads, kernels and downloads on three streams, ordered per tensor"}
+            "overlap": "uploads, kernels and downloads on three streams, ordered per tensor; "
+                       "two sets of device buffers alternate between steps"}
 
 
 # ---------------------------------------------------------------------------
