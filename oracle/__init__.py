@@ -26,7 +26,7 @@ _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
 ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU, ACT_MISH, ACT_LEAKY_RELU, ACT_ELU = 0, 1, 2, 3, 4, 5, 6
-ACT_SIGMOID, ACT_CELU, ACT_SELU = 7, 8, 9
+ACT_SIGMOID, ACT_CELU, ACT_SELU, ACT_RELU6, ACT_HARDTANH = 7, 8, 9, 10, 11
 
 # -ffp-contract=off keeps a*b+c as two roundings on every host (gcc fuses them by
 # default on aarch64), so the oracle gives the same bits here and on the GPU machine.

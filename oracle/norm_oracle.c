@@ -35,6 +35,10 @@
  *   - sigmoid(z) = 1/(1 + e^-z); selu(z) = L*z for z > 0, else L*A*(e^z - 1),
  *     with the constants L, A of Klambauer et al., "Self-Normalizing Neural
  *     Networks" (2017).
+ *   - The clamping activations the activation article names beside ReLU
+ *     (section 七): relu6(z) = min(max(z, 0), 6) and hardtanh(z) =
+ *     min(max(z, -1), 1); each has derivative 1 strictly inside its range and
+ *     0 outside it and at its ends.
  *   - Dropout draws Philox4x32-10 with key (seed, 0) and counter (e / 4, 0, 0) for
  *     element e, which takes output word e % 4 as the uniform (word >> 8) * 2^-24;
  *     the element is dropped when that value is below drop_p (single precision).
@@ -300,6 +304,8 @@ static double act_forward(int act, double param, double z)
     case ORACLE_ACT_GELU: return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
     case ORACLE_ACT_SILU: return z * sigmoid(z);
     case ORACLE_ACT_MISH: return z * tanh(softplus(z));
+    case ORACLE_ACT_RELU6: return z < 0.0 ? 0.0 : (z > 6.0 ? 6.0 : z);
+    case ORACLE_ACT_HARDTANH: return z < -1.0 ? -1.0 : (z > 1.0 ? 1.0 : z);
     default:              return z;
     }
 }
@@ -331,6 +337,8 @@ static double act_derivative(int act, double param, double z)
         double t = tanh(softplus(z));
         return t + z * (1.0 - t * t) * sigmoid(z);
     }
+    case ORACLE_ACT_RELU6: return (z > 0.0 && z < 6.0) ? 1.0 : 0.0;
+    case ORACLE_ACT_HARDTANH: return (z > -1.0 && z < 1.0) ? 1.0 : 0.0;
     default: return 1.0;
     }
 }

@@ -14,7 +14,7 @@ extern "C" {
 
 enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_RELU = 1, ORACLE_ACT_GELU = 2, ORACLE_ACT_SILU = 3, ORACLE_ACT_MISH = 4,
        ORACLE_ACT_LEAKY_RELU = 5, ORACLE_ACT_ELU = 6, ORACLE_ACT_SIGMOID = 7, ORACLE_ACT_CELU = 8,
-       ORACLE_ACT_SELU = 9 };
+       ORACLE_ACT_SELU = 9, ORACLE_ACT_RELU6 = 10, ORACLE_ACT_HARDTANH = 11 };
 
 void oracle_layernorm_fwd(int64_t rows, int64_t cols, const double *x,
                           const double *w, const double *b, double eps,

@@ -29,7 +29,9 @@ import numpy as np
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 ACT = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "mish": 4, "leaky_relu": 5, "elu": 6,
-       "sigmoid": 7, "celu": 8, "selu": 9}
+       "sigmoid": 7, "celu": 8, "selu": 9, "relu6": 10, "hardtanh": 11}
+# where each kinked activation's derivative jumps (finite differences keep clear of them)
+KINKS = {"relu": (0.0,), "leaky_relu": (0.0,), "relu6": (0.0, 6.0), "hardtanh": (-1.0, 1.0)}
 # the parameter the activations that take one are exercised with (slope, alpha)
 ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3, "celu": 0.7}
 ALL_ACTS = tuple(ACT)
@@ -323,6 +325,10 @@ def _torch_bn_forward(x, res, w, b, rm, rv, eps, momentum, training, act):
         return F.celu(z, ACT_PARAM[act])
     if act == "selu":
         return F.selu(z)
+    if act == "relu6":
+        return F.relu6(z)
+    if act == "hardtanh":
+        return F.hardtanh(z)
     return z
 
 
@@ -430,6 +436,32 @@ def pin_sigmoid_celu_selu_values(o):
     _close(dx, [lam, lam * alp / 2.0], 1e-15, 1e-16, "selu derivative")
 
 
+def pin_relu6_hardtanh_values(o):
+    # z = x as above; closed forms from the definitions: relu6 clamps to [0, 6]
+    # and hardtanh to [-1, 1]; each derivative is 1 strictly inside the range and
+    # 0 outside it and at both ends
+    rm, rv = np.zeros(1), np.array([0.75])
+
+    def run(act, zs):
+        z = np.array(zs).reshape(1, 1, len(zs))
+        y = o.batchnorm_fwd(z, eps=0.25, training=False, act=ACT[act], running_mean=rm,
+                            running_var=rv)["y"].ravel()
+        dx = o.batchnorm_bwd(np.ones_like(z), z, None, np.ones(1), np.zeros(1), rm, rv, eps=0.25,
+                             training=False, act=ACT[act])[0].ravel()
+        return y, dx
+    y, dx = run("relu6", [-2.5, 0.0, 0.75, 6.0, 7.5])
+    _close(y, [0.0, 0.0, 0.75, 6.0, 6.0], 0, 0, "relu6 values")
+    _close(dx, [0.0, 0.0, 1.0, 0.0, 0.0], 0, 0, "relu6 derivative")
+    y, dx = run("hardtanh", [-3.0, -1.0, -0.25, 0.5, 1.0, 2.0])
+    _close(y, [-1.0, -1.0, -0.25, 0.5, 1.0, 1.0], 0, 0, "hardtanh values")
+    _close(dx, [0.0, 0.0, 1.0, 1.0, 0.0, 0.0], 0, 0, "hardtanh derivative")
+    # the two are one clamp shifted and scaled: hardtanh(z) = relu6(3z + 3)/3 - 1
+    zs = np.linspace(-2.0, 2.0, 41)
+    ya = o.act_dropout_fwd(zs, ACT["hardtanh"], 0.0, 1)
+    yb = o.act_dropout_fwd(3.0 * zs + 3.0, ACT["relu6"], 0.0, 1) / 3.0 - 1.0
+    _close(ya, yb, 0, 1e-15, "hardtanh(z) = relu6(3z + 3)/3 - 1")
+
+
 def pin_batchnorm_mask_layout(o):
     # eval mode, z = x: mask bit (i, ch, j) must be x > 0 with the documented layout
     n, c, l = 2, 3, 70
@@ -449,20 +481,21 @@ def pin_batchnorm_mask_layout(o):
 
 
 def _bn_inputs_away_from_kinks(r, n, c, l, act, with_res):
-    """Tiny BatchNorm inputs whose pre-activation stays 1e-3 away from 0 for
-    ReLU, so finite differences do not cross the kink."""
+    """Tiny BatchNorm inputs whose pre-activation stays 1e-3 away from every
+    kink of the activation (0 for ReLU, 0 and 6 for ReLU6, -1 and 1 for
+    hardtanh), so finite differences do not cross one."""
     for _ in range(1000):
         x = r.normal(size=(n, c, l)) * 1.3 + 0.2
         res = r.normal(size=(n, c, l)) if with_res else None
         w = 1 + 0.3 * r.normal(size=c)
         b = 0.3 * r.normal(size=c)
-        if act not in ("relu", "leaky_relu"):
+        if act not in KINKS:
             return x, res, w, b
         xc = x.transpose(1, 0, 2).reshape(c, -1)
         mu = xc.mean(1)[None, :, None]
         rs = (1 / np.sqrt(xc.var(1) + 1e-3))[None, :, None]
         z = (x - mu) * rs * w[None, :, None] + b[None, :, None] + (res if with_res else 0)
-        if np.abs(z).min() > 1e-3:
+        if min(np.abs(z - k).min() for k in KINKS[act]) > 1e-3:
             return x, res, w, b
     raise RuntimeError("no input away from the ReLU kink")
 
@@ -525,7 +558,8 @@ def pin_batchnorm_bwd_vs_torch(o):
     n, c, l = 3, 4, 6
     acts = {"none": lambda z: z, "gelu": lambda z: F.gelu(z, approximate="none"), "silu": F.silu,
             "mish": F.mish, "elu": lambda z: F.elu(z, ACT_PARAM["elu"]), "sigmoid": torch.sigmoid,
-            "celu": lambda z: F.celu(z, ACT_PARAM["celu"]), "selu": F.selu}
+            "celu": lambda z: F.celu(z, ACT_PARAM["celu"]), "selu": F.selu, "relu6": F.relu6,
+            "hardtanh": F.hardtanh}
     for training in (True, False):
         for act in acts:
             x = torch.tensor(r.normal(size=(n, c, l)) * 1.5, requires_grad=True)
@@ -694,7 +728,8 @@ def _act_torch():
     lk, al, ca = ACT_PARAM["leaky_relu"], ACT_PARAM["elu"], ACT_PARAM["celu"]
     return {0: (lambda t: t, 0.0), 1: (torch.relu, 0.0), 2: (F.gelu, 0.0), 3: (F.silu, 0.0),
             4: (F.mish, 0.0), 5: (lambda t: F.leaky_relu(t, lk), lk), 6: (lambda t: F.elu(t, al), al),
-            7: (torch.sigmoid, 0.0), 8: (lambda t: F.celu(t, ca), ca), 9: (F.selu, 0.0)}
+            7: (torch.sigmoid, 0.0), 8: (lambda t: F.celu(t, ca), ca), 9: (F.selu, 0.0),
+            10: (F.relu6, 0.0), 11: (F.hardtanh, 0.0)}
 
 
 def pin_act_dropout_no_drop_is_activation(o):
@@ -728,7 +763,9 @@ def pin_act_dropout_bwd_fd(o):
     """Backward = derivative of sum(dy * forward) with the seed held fixed."""
     r = _rng(43)
     x = r.normal(size=64) * 2
-    x = np.where(np.abs(x) < 0.05, 0.3, x)  # keep ReLU's kink out of the stencil
+    # keep the kinks (0, and ReLU6's 6 and hardtanh's -1, 1) out of the stencil
+    near = np.min([np.abs(x - k) for k in (-1.0, 0.0, 1.0, 6.0)], axis=0) < 0.05
+    x = np.where(near, x + 0.3, x)
     dy = r.normal(size=64)
     for act, (_, prm) in _act_torch().items():
         for p in (0.0, 0.3):

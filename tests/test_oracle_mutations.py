@@ -53,6 +53,14 @@ MUTATIONS = {
     "elu_grad_drops_exp": ("case ORACLE_ACT_ELU: return z > 0.0 ? 1.0 : param * exp(z);",
                            "case ORACLE_ACT_ELU: return z > 0.0 ? 1.0 : param;"),
     "bn_gelu_grad_drops_pdf_term": ("return cdf + z * pdf;", "return cdf;"),
+    "relu6_no_upper_clamp": ("case ORACLE_ACT_RELU6: return z < 0.0 ? 0.0 : (z > 6.0 ? 6.0 : z);",
+                             "case ORACLE_ACT_RELU6: return z < 0.0 ? 0.0 : z;"),
+    "relu6_grad_at_upper_end": ("case ORACLE_ACT_RELU6: return (z > 0.0 && z < 6.0) ? 1.0 : 0.0;",
+                                "case ORACLE_ACT_RELU6: return (z > 0.0 && z <= 6.0) ? 1.0 : 0.0;"),
+    "hardtanh_lower_bound_zero": ("case ORACLE_ACT_HARDTANH: return z < -1.0 ? -1.0 : (z > 1.0 ? 1.0 : z);",
+                                  "case ORACLE_ACT_HARDTANH: return z < 0.0 ? 0.0 : (z > 1.0 ? 1.0 : z);"),
+    "hardtanh_grad_ignores_range": ("case ORACLE_ACT_HARDTANH: return (z > -1.0 && z < 1.0) ? 1.0 : 0.0;",
+                                    "case ORACLE_ACT_HARDTANH: return 1.0;"),
     "bn_relu_grad_at_zero": ("case ORACLE_ACT_RELU: return z > 0.0 ? 1.0 : 0.0;",
                              "case ORACLE_ACT_RELU: return z >= 0.0 ? 1.0 : 0.0;"),
     "bn_mask_bit_order": ("|= (uint32_t)1u << (j % 32);", "|= (uint32_t)1u << (31 - j % 32);"),
