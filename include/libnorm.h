@@ -84,7 +84,10 @@ typedef enum nrm_dtype { NRM_F32 = 0, NRM_F16 = 1, NRM_BF16 = 2 } nrm_dtype;
  * 1, else act_param*e^z); CELU is z for z > 0, else act_param*(e^(z/act_param)
  * - 1) (derivative 1, else e^(z/act_param); act_param != 0).  SIGMOID is
  * 1/(1 + e^-z).  SELU is L*z for z > 0, else L*A*(e^z - 1), L and A the
- * constants of Klambauer et al. (2017).  act_param is ignored by the others. */
+ * constants of Klambauer et al. (2017).  RELU6 and HARDTANH are the clamps the
+ * [AF] article names beside ReLU (section 七): min(max(z, 0), 6) and
+ * min(max(z, -1), 1), each with derivative 1 strictly inside its range and 0
+ * outside it and at both ends.  act_param is ignored by the others. */
 typedef enum nrm_act {
     NRM_ACT_NONE = 0,
     NRM_ACT_RELU = 1,
@@ -95,7 +98,9 @@ typedef enum nrm_act {
     NRM_ACT_ELU = 6,
     NRM_ACT_SIGMOID = 7,
     NRM_ACT_CELU = 8,
-    NRM_ACT_SELU = 9
+    NRM_ACT_SELU = 9,
+    NRM_ACT_RELU6 = 10,
+    NRM_ACT_HARDTANH = 11
 } nrm_act;
 
 /* Operations that need a workspace (for nrm_workspace_bytes). */

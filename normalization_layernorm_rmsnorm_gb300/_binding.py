@@ -19,11 +19,13 @@ NRM_OK, NRM_ERR_INVALID_ARG, NRM_ERR_UNSUPPORTED, NRM_ERR_WORKSPACE, NRM_ERR_CUD
 NRM_F32, NRM_F16, NRM_BF16 = 0, 1, 2
 NRM_ACT_NONE, NRM_ACT_RELU, NRM_ACT_GELU, NRM_ACT_SILU, NRM_ACT_MISH = 0, 1, 2, 3, 4
 NRM_ACT_LEAKY_RELU, NRM_ACT_ELU, NRM_ACT_SIGMOID, NRM_ACT_CELU, NRM_ACT_SELU = 5, 6, 7, 8, 9
+NRM_ACT_RELU6, NRM_ACT_HARDTANH = 10, 11
 NRM_OP_LAYERNORM_BWD, NRM_OP_RMSNORM_BWD, NRM_OP_LAYERNORM_CF_BWD = 1, 2, 3
 
 ACTS = {"none": NRM_ACT_NONE, "relu": NRM_ACT_RELU, "gelu": NRM_ACT_GELU, "silu": NRM_ACT_SILU,
         "mish": NRM_ACT_MISH, "leaky_relu": NRM_ACT_LEAKY_RELU, "elu": NRM_ACT_ELU,
-        "sigmoid": NRM_ACT_SIGMOID, "celu": NRM_ACT_CELU, "selu": NRM_ACT_SELU}
+        "sigmoid": NRM_ACT_SIGMOID, "celu": NRM_ACT_CELU, "selu": NRM_ACT_SELU,
+        "relu6": NRM_ACT_RELU6, "hardtanh": NRM_ACT_HARDTANH}
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("nrm_layernorm_fwd", "nrm_layernorm_bwd", "nrm_layernorm_bwd_noalloc",

@@ -124,6 +124,8 @@ __device__ __forceinline__ float act_forward(int act, float z, float prm) {
     if (act == NRM_ACT_SIGMOID) return 1.f / (1.f + expf(-z));
     if (act == NRM_ACT_CELU) return z > 0.f ? z : prm * expm1f(z / prm);
     if (act == NRM_ACT_SELU) return z > 0.f ? kSeluLambda * z : (kSeluLambda * kSeluAlpha) * expm1f(z);
+    if (act == NRM_ACT_RELU6) return z < 0.f ? 0.f : (z > 6.f ? 6.f : z);
+    if (act == NRM_ACT_HARDTANH) return z < -1.f ? -1.f : (z > 1.f ? 1.f : z);
     if (act == NRM_ACT_GELU) return gelu_f(z);
     if (act == NRM_ACT_SILU) return z / (1.f + expf(-z));
     if (act == NRM_ACT_MISH) return z * tanhf(softplus_f(z));
@@ -141,6 +143,8 @@ __device__ __forceinline__ float act_derivative(int act, float z, float prm) {
     }
     if (act == NRM_ACT_CELU) return z > 0.f ? 1.f : expf(z / prm);
     if (act == NRM_ACT_SELU) return z > 0.f ? kSeluLambda : (kSeluLambda * kSeluAlpha) * expf(z);
+    if (act == NRM_ACT_RELU6) return (z > 0.f && z < 6.f) ? 1.f : 0.f;
+    if (act == NRM_ACT_HARDTANH) return (z > -1.f && z < 1.f) ? 1.f : 0.f;
     if (act == NRM_ACT_GELU) return gelu_grad_f(z);
     if (act == NRM_ACT_SILU) {
         const float sg = 1.f / (1.f + expf(-z));
@@ -199,7 +203,9 @@ auto with_act(int act, F&& f) {
     case NRM_ACT_ELU: return f(ActTag<NRM_ACT_ELU>{});
     case NRM_ACT_SIGMOID:
     case NRM_ACT_CELU:
-    case NRM_ACT_SELU: return f(ActTag<kActGeneric>{});
+    case NRM_ACT_SELU:
+    case NRM_ACT_RELU6:
+    case NRM_ACT_HARDTANH: return f(ActTag<kActGeneric>{});
     default: return f(ActTag<NRM_ACT_NONE>{});
     }
 }

@@ -357,7 +357,7 @@ nrm_status check_cf_shape(int64_t n, int64_t c, int64_t l, nrm_dtype dt) {
 }
 
 nrm_status check_act(nrm_act act, float act_param) {
-    if (int(act) < int(NRM_ACT_NONE) || int(act) > int(NRM_ACT_SELU))
+    if (int(act) < int(NRM_ACT_NONE) || int(act) > int(NRM_ACT_HARDTANH))
         return fail(NRM_ERR_INVALID_ARG, "unknown activation %d", int(act));
     if (!std::isfinite(act_param)) return fail(NRM_ERR_INVALID_ARG, "act_param must be finite");
     if (act == NRM_ACT_CELU && act_param == 0.f) return fail(NRM_ERR_INVALID_ARG, "CELU needs act_param != 0");

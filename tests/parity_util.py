@@ -36,6 +36,9 @@ SELU_L, SELU_A = 1.0507009873554805, 1.6732632423543772
 # activations with a kink at 0 whose branch the kernel (fp32) and the oracle
 # (double) may decide differently within RELU_BAND
 KINKED = ("relu", "leaky_relu", "elu", "selu")
+# the clamping activations: their two ends, where either branch (z passed
+# through, or the bound) is accepted within RELU_BAND
+CLAMPS = {"relu6": (0.0, 6.0), "hardtanh": (-1.0, 1.0)}
 STAT_TOL = (1e-5, 1e-5)
 # rounding term of the BatchNorm channel sums of 16-bit workloads, in units of
 # 2^-24 * sum|term| (derivation beside the tolerances in the design notes)
@@ -202,7 +205,8 @@ def oracle_bn(orc, inp, eps, momentum, training, act, with_res, with_affine=True
     a = {"none": oracle_mod.ACT_NONE, "relu": oracle_mod.ACT_RELU, "gelu": oracle_mod.ACT_GELU,
          "silu": oracle_mod.ACT_SILU, "mish": oracle_mod.ACT_MISH, "leaky_relu": oracle_mod.ACT_LEAKY_RELU,
          "elu": oracle_mod.ACT_ELU, "sigmoid": oracle_mod.ACT_SIGMOID, "celu": oracle_mod.ACT_CELU,
-         "selu": oracle_mod.ACT_SELU}[act]
+         "selu": oracle_mod.ACT_SELU, "relu6": oracle_mod.ACT_RELU6,
+         "hardtanh": oracle_mod.ACT_HARDTANH}[act]
     prm = ACT_PARAM.get(act, 0.0)
     x = inp["x"].f64()
     res = inp["res"].f64() if with_res else None
@@ -228,6 +232,14 @@ def oracle_bn(orc, inp, eps, momentum, training, act, with_res, with_affine=True
             bits = unpack_mask(f["mask"], *x.shape)
             out["bwd_flipped"] = orc.batchnorm_bwd(dy, x, res, w, b, rm0, rv0, eps, training, a,
                                                    mask=pack_mask(bits ^ amb))
+    elif act in CLAMPS:
+        lo, hi = CLAMPS[act]
+        z = f["z"]
+        near_lo = np.abs(z - lo) < RELU_BAND
+        amb = near_lo | (np.abs(z - hi) < RELU_BAND)
+        out["amb"] = amb
+        # the other branch: the bound where the oracle passed z through, z where it clamped
+        out["y_alt"] = np.where(f["y"] == z, np.where(near_lo, lo, hi), z)
     return out
 
 

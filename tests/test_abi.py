@@ -108,7 +108,7 @@ P = 1 << 20  # a fake, aligned, non-null address: never dereferenced (validation
     (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 2, 0.0, 1.5, 7, 1, None), 1),
     (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 2, 0.0, float("nan"), 7, 1, None), 1),
     (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, -1, 2, 0.0, 0.5, 7, 1, None), 1),
-    (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, 16, 11, 0.0, 0.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_bwd(P, P * 2, P * 3, 16, 12, 0.0, 0.5, 7, 1, None), 1),
     (lambda L: L.nrm_act_dropout_fwd(P, None, 16, 2, 0.0, 0.5, 7, 1, None), 1),
     # a non-finite activation parameter (BatchNorm and dropout)
     (lambda L: L.nrm_batchnorm_fwd(P, None, None, None, P * 2, None, None, None, None, None, 2, 3,
@@ -116,7 +116,7 @@ P = 1 << 20  # a fake, aligned, non-null address: never dereferenced (validation
     (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 6, float("nan"), 0.5, 7, 1, None), 1),
     # CELU with alpha 0, an activation past the last one
     (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 8, 0.0, 0.5, 7, 1, None), 1),
-    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 10, 0.0, 0.5, 7, 1, None), 1),
+    (lambda L: L.nrm_act_dropout_fwd(P, P * 2, 16, 12, 0.0, 0.5, 7, 1, None), 1),
     # an fp32 input with a 16-bit output (only 16-bit inputs may widen), an unknown output dtype
     (lambda L: L.nrm_layernorm_fwd_ex(P, None, None, P * 2, None, None, 4, 8, 1e-5, 0, 1, None), 2),
     (lambda L: L.nrm_rmsnorm_fwd_ex(P, None, None, P * 2, None, 4, 8, 1e-5, 1, 5, None), 1),

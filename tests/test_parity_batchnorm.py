@@ -193,7 +193,7 @@ LEAKY_ELU = [
 ]
 
 
-@pytest.mark.parametrize("act", ["leaky_relu", "elu", "sigmoid", "celu", "selu"])
+@pytest.mark.parametrize("act", ["leaky_relu", "elu", "sigmoid", "celu", "selu", "relu6", "hardtanh"])
 @pytest.mark.parametrize("case", LEAKY_ELU, ids=[f"{d}-{n}x{c}x{l}" for d, n, c, l in LEAKY_ELU])
 def test_bn_leaky_relu_elu(orc, act, case):
     # the activations with a parameter (slope 0.05, alpha 1.3 / 0.7) and the

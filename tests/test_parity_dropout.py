@@ -13,7 +13,8 @@ from parity_util import TOL, assert_close, host
 
 pytestmark = pytest.mark.gpu
 
-ACTS = ["none", "relu", "gelu", "silu", "mish", "leaky_relu", "elu", "sigmoid", "celu", "selu"]
+ACTS = ["none", "relu", "gelu", "silu", "mish", "leaky_relu", "elu", "sigmoid", "celu", "selu", "relu6",
+        "hardtanh"]
 ACT_CODE = {a: i for i, a in enumerate(ACTS)}
 ACT_PARAM = {"leaky_relu": 0.05, "elu": 1.3, "celu": 0.7}
 
@@ -95,6 +96,25 @@ def test_gelu_dense_grid_fp32(orc):
     edx = np.abs(dx - dxo)
     assert (ey <= bound).all(), f"GELU: max error {ey.max():.3g} at z = {zf[ey.argmax()]}"
     assert (edx <= bound).all(), f"GELU': max error {edx.max():.3g} at z = {zf[edx.argmax()]}"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("act", ["relu6", "hardtanh"])
+def test_clamp_activations_at_their_ends(orc, dtype, act):
+    # values across both clamps with every end present exactly (0, 6, -1, 1 and
+    # the 1/256 grid on [-8, 8] are exact in fp16): y and dx against the oracle,
+    # the derivative exactly 0 at the ends and nonzero strictly inside
+    lo, hi = {"relu6": (0.0, 6.0), "hardtanh": (-1.0, 1.0)}[act]
+    z = np.concatenate([np.linspace(-8.0, 8.0, 4097), np.repeat([lo, hi], 64)])
+    x = synth.store(z, dtype, z.shape)
+    dy = synth.store(np.ones_like(z), dtype, z.shape)
+    keep, y = _check(orc, x, dy, act, 0.2, 31, dtype, f"{act} {dtype}")
+    _, dx = _run(x, dy, act, 0.2, 31)
+    xv = x.f64()
+    assert not dx[(xv == lo) | (xv == hi)].any(), f"{act}: derivative at the ends must be 0"
+    inside = (xv > lo) & (xv < hi)
+    assert (dx[inside & keep] != 0).all() and not dx[~inside].any(), f"{act}: derivative support"
+    assert (y[keep & (xv >= hi)] == y[keep & (xv >= hi)].max()).all(), f"{act}: upper clamp"
 
 
 @pytest.mark.parametrize("p", [0.0, 1.0])
