@@ -166,7 +166,7 @@ def test_rmsnorm_with_bias(orc, dtype, shape):
     compare_row(got, want, dtype, f"rms+bias {dtype} [{rows},{cols}]")
 
 
-F32OUT = [(300, 768), (97, 1023), (64, 4096), (5, 40000)]
+F32OUT = [(300, 768), (97, 1023), (64, 4096), (5, 40000), (25216, 768)]  # the last: the bench workload's size
 
 
 @pytest.mark.parametrize("kind", ["layernorm", "rmsnorm"])
