@@ -735,25 +735,55 @@ row_bwd_wide_kernel(const RowArgs a) {
         const float c2 = s[NV - 1] / float(cols);
         T* dxr = dx + row * cols;
         for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
-            float xv[VE], dv[VE], wv[VE], o[VE];
+            float xv[VE], dv[VE], wv[VE], o[VE], xs[VE];
             load_vec<T, VE>(xr + int64_t(vi) * VE, xv);
             load_as<TD, VE>(dyr + int64_t(vi) * VE, dv);
             load_param<T, VE>(a.w, vi, wv, 1.f);
 #pragma unroll
             for (int k = 0; k < VE; ++k) {
                 const float g = dv[k] * wv[k];
-                const float xs = LN ? (xv[k] - mu) * rs : xv[k] * rs;  // xhat (LN) or x*inv_rms
+                xs[k] = LN ? (xv[k] - mu) * rs : xv[k] * rs;  // xhat (LN) or x*inv_rms
                 if constexpr (LN) {
-                    o[k] = rs * (g - c1 - xs * c2);
+                    o[k] = rs * (g - c1 - xs[k] * c2);
                 } else {
                     o[k] = rs * (g - xv[k] * (c1 * rs * rs));
                 }
                 if (in_regs) {
-                    racc_w[k] = fmaf(dv[k], xs, racc_w[k]);
+                    racc_w[k] = fmaf(dv[k], xs[k], racc_w[k]);
                     racc_b[k] += dv[k];
+                }
+            }
+            if (!in_regs) {
+                if constexpr (VE >= 4) {
+                    // the partial rows by 16-byte accesses (the workspace and every
+                    // CTA's row in it are 16-byte aligned; cols is a multiple of VE)
+#pragma unroll
+                    for (int h = 0; h < VE; h += 4) {
+                        if (wsw) {
+                            float4* p = reinterpret_cast<float4*>(wsw + vi * VE + h);
+                            float4 u = *p;
+                            u.x = fmaf(dv[h], xs[h], u.x);
+                            u.y = fmaf(dv[h + 1], xs[h + 1], u.y);
+                            u.z = fmaf(dv[h + 2], xs[h + 2], u.z);
+                            u.w = fmaf(dv[h + 3], xs[h + 3], u.w);
+                            *p = u;
+                        }
+                        if (wsb) {
+                            float4* p = reinterpret_cast<float4*>(wsb + vi * VE + h);
+                            float4 u = *p;
+                            u.x += dv[h];
+                            u.y += dv[h + 1];
+                            u.z += dv[h + 2];
+                            u.w += dv[h + 3];
+                            *p = u;
+                        }
+                    }
                 } else {
-                    if (wsw) wsw[vi * VE + k] = fmaf(dv[k], xs, wsw[vi * VE + k]);
-                    if (wsb) wsb[vi * VE + k] += dv[k];
+#pragma unroll
+                    for (int k = 0; k < VE; ++k) {
+                        if (wsw) wsw[vi * VE + k] = fmaf(dv[k], xs[k], wsw[vi * VE + k]);
+                        if (wsb) wsb[vi * VE + k] += dv[k];
+                    }
                 }
             }
             store_vec<T, VE>(dxr + int64_t(vi) * VE, o);

@@ -70,7 +70,10 @@ DROPOUT_P = 0.1
 DROPOUT_SEED = 2024
 # and the ViT-B LayerNorm with its output (and so dy) kept in float32
 F32OUT_WORKLOAD = "ln_f16_to_f32_25216x768"
-EXTRA = ("ln_cf_f16_128x96x56x56", DROPOUT_WORKLOAD, F32OUT_WORKLOAD)
+# and rows too wide for the register and ring kernels (above 32768 fp16 values
+# forward, 16384 backward), which take one 1024-thread CTA per row
+WIDE_WORKLOAD = "ln_f16_2048x65536"
+EXTRA = ("ln_cf_f16_128x96x56x56", DROPOUT_WORKLOAD, F32OUT_WORKLOAD, WIDE_WORKLOAD)
 
 
 def build_extra_calls(dev, names=None):
@@ -87,6 +90,8 @@ def build_extra_calls(dev, names=None):
         calls += _act_dropout(DROPOUT_WORKLOAD, 25216, 3072, dev)
     if names is None or F32OUT_WORKLOAD in names:
         calls += _ln_f32out(F32OUT_WORKLOAD, 25216, 768, dev, f32)
+    if names is None or WIDE_WORKLOAD in names:
+        calls += _ln_wide(WIDE_WORKLOAD, 2048, 65536, dev, f32)
     return calls
 
 
@@ -260,5 +265,26 @@ def _ln_f32out(name, rows, cols, dev, f32):
              nbytes(x, w, b, y, mean, rstd), 1, [x, w, b], [y, mean, rstd]),
         Call(name, "bwd", "row_bwd_ring_kernel<f16,ln,f32 dy>+colsum",
              lambda: nrm.nrm_layernorm_bwd_ex(dy, x, w, mean, rstd, dx, dw, db, ws),
+             nbytes(dy, x, w, mean, rstd, dx, dw, db), 2, [dy], [dx, dw, db]),
+    ]
+
+
+def _ln_wide(name, rows, cols, dev, f32):
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    seed = 43
+    x = synth.random_tensor(seed, 1, (rows, cols), "f16", mean=0.3, std=1.5).torch(dev)
+    w = synth.store(1 + 0.1 * synth.normal(seed, 2, cols), "f16", (cols,)).torch(dev)
+    b = synth.store(0.1 * synth.normal(seed, 3, cols), "f16", (cols,)).torch(dev)
+    dy = synth.random_tensor(seed, 4, (rows, cols), "f16").torch(dev)
+    y, dx, dw, db = x.new_empty(x.shape), x.new_empty(x.shape), w.new_empty(cols), b.new_empty(cols)
+    mean, rstd = f32(rows), f32(rows)
+    ws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_BWD, rows, cols, nrm.NRM_F16) // 4)
+    return [
+        Call(name, "fwd", "row_fwd_wide_kernel<f16,ln>",
+             lambda: nrm.nrm_layernorm_fwd(x, w, b, y, mean, rstd, 1e-5),
+             nbytes(x, w, b, y, mean, rstd), 1, [x, w, b], [y, mean, rstd]),
+        Call(name, "bwd", "row_bwd_wide_kernel<f16,ln>+colsum",
+             lambda: nrm.nrm_layernorm_bwd(dy, x, w, mean, rstd, dx, dw, db, ws),
              nbytes(dy, x, w, mean, rstd, dx, dw, db), 2, [dy], [dx, dw, db]),
     ]

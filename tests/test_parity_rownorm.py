@@ -30,6 +30,16 @@ def test_row_workloads_full_size(orc, name):
     compare_row(got, want, cfg.dtype, name)
 
 
+def test_row_wide_workload_full_size(orc):
+    # the wide-row workload timed beside the step, LayerNorm fp16 [2048, 65536]:
+    # rows above the register and ring kernels' widths, one 1024-thread CTA each
+    cfg = synth.RowConfig("wide", "layernorm", 2048, 65536, "f16", 1e-5, seed=43, x_mean=0.3, x_std=1.5)
+    inp = synth.row_inputs(cfg)
+    got = run_row(cfg.kind, inp, cfg.dtype, cfg.eps)
+    want = oracle_row(orc, cfg.kind, inp, cfg.eps)
+    compare_row(got, want, cfg.dtype, "ln f16 [2048,65536]")
+
+
 ODD_COLS = [1, 7, 8, 33, 64, 100, 256, 768, 1023, 1025, 2048, 4097, 8200, 40000]
 
 
