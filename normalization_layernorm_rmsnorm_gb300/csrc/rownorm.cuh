@@ -614,6 +614,30 @@ __device__ __forceinline__ void store_as(TO* p, const float (&in)[VE]) {
     }
 }
 
+// 16-byte raw loads of VE elements of T (one or two 16-byte accesses), kept
+// packed until they are used, so that several can be in flight per thread.
+template <typename T, int VE>
+struct RawVec {
+    static constexpr int N = int(sizeof(T)) * VE / 16;
+    uint4 u[N];
+    __device__ __forceinline__ void load(const T* p) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) u[i] = ld_stream_v4(p + i * (16 / int(sizeof(T))));
+    }
+    __device__ __forceinline__ void unpack(float (&out)[VE]) const {
+        constexpr int E = 16 / int(sizeof(T));
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            Pack<T, E> pk;
+            pk.u = u[i];
+#pragma unroll
+            for (int k = 0; k < E; ++k) out[i * E + k] = Io<T>::load(pk.b[k]);
+        }
+    }
+};
+constexpr int kWideBatch = 4;  // 16-byte vectors per thread whose loads the wide kernels issue together
+constexpr int kWideFwdBlock = 512;  // threads per CTA of the wide forward: 512 / 1024 measured 143 / 174 us (fp16 [2048,65536])
+
 // TO: the output's storage type (T, or float for a 16-bit input whose output
 // is kept in fp32).
 template <typename T, bool LN, int VE, typename TO = T>
@@ -630,9 +654,7 @@ row_fwd_wide_kernel(const RowArgs a) {
         float mu = 0.f, var;
         if constexpr (LN) {
             Moments m{0.f, 0.f, 0.f};
-            for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
-                float v[VE];
-                load_vec<T, VE, false>(xr + int64_t(vi) * VE, v);
+            auto add = [&](const float (&v)[VE]) {
                 float s = 0.f;
 #pragma unroll
                 for (int k = 0; k < VE; ++k) s += v[k];
@@ -641,6 +663,29 @@ row_fwd_wide_kernel(const RowArgs a) {
 #pragma unroll
                 for (int k = 0; k < VE; ++k) q = fmaf(v[k] - vm, v[k] - vm, q);
                 chan_merge(m, float(VE), vm, q);
+            };
+            if constexpr (VE == kVec<T>) {
+                // kWideBatch vectors' loads in flight per thread
+                for (int v0 = threadIdx.x; v0 < nvec; v0 += kWideBatch * int(blockDim.x)) {
+                    RawVec<T, VE> r[kWideBatch];
+#pragma unroll
+                    for (int u = 0; u < kWideBatch; ++u)
+                        if (v0 + u * int(blockDim.x) < nvec) r[u].load(xr + int64_t(v0 + u * int(blockDim.x)) * VE);
+#pragma unroll
+                    for (int u = 0; u < kWideBatch; ++u) {
+                        if (v0 + u * int(blockDim.x) < nvec) {
+                            float v[VE];
+                            r[u].unpack(v);
+                            add(v);
+                        }
+                    }
+                }
+            } else {
+                for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+                    float v[VE];
+                    load_vec<T, VE, false>(xr + int64_t(vi) * VE, v);
+                    add(v);
+                }
             }
             const Moments tot = block_merge(m, msm);
             mu = tot.mean;
@@ -662,9 +707,8 @@ row_fwd_wide_kernel(const RowArgs a) {
             if (a.rstd) a.rstd[row] = rs;
         }
         TO* yr = y + row * cols;
-        for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
-            float v[VE], wv[VE], bv[VE], o[VE];
-            load_vec<T, VE>(xr + int64_t(vi) * VE, v);
+        auto out = [&](int vi, const float (&v)[VE]) {
+            float wv[VE], bv[VE], o[VE];
             load_param<T, VE>(a.w, vi, wv, 1.f);
             load_param<T, VE>(a.b, vi, bv, 0.f);
 #pragma unroll
@@ -673,6 +717,28 @@ row_fwd_wide_kernel(const RowArgs a) {
                 o[k] = fmaf(xh, wv[k], bv[k]);
             }
             store_as<TO, VE>(yr + int64_t(vi) * VE, o);
+        };
+        if constexpr (VE == kVec<T>) {
+            for (int v0 = threadIdx.x; v0 < nvec; v0 += kWideBatch * int(blockDim.x)) {
+                RawVec<T, VE> r[kWideBatch];
+#pragma unroll
+                for (int u = 0; u < kWideBatch; ++u)
+                    if (v0 + u * int(blockDim.x) < nvec) r[u].load(xr + int64_t(v0 + u * int(blockDim.x)) * VE);
+#pragma unroll
+                for (int u = 0; u < kWideBatch; ++u) {
+                    if (v0 + u * int(blockDim.x) < nvec) {
+                        float v[VE];
+                        r[u].unpack(v);
+                        out(v0 + u * int(blockDim.x), v);
+                    }
+                }
+            }
+        } else {
+            for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+                float v[VE];
+                load_vec<T, VE>(xr + int64_t(vi) * VE, v);
+                out(vi, v);
+            }
         }
     }
 }
@@ -794,6 +860,137 @@ row_bwd_wide_kernel(const RowArgs a) {
         for (int k = 0; k < VE; ++k) {
             if (wsw) wsw[threadIdx.x * VE + k] = racc_w[k];
             if (wsb) wsb[threadIdx.x * VE + k] = racc_b[k];
+        }
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------
+// backward of rows too wide for the ring, in two kernels: the per-row sums,
+// then a column pass in which each thread keeps its columns' dw/db sums in
+// registers over a chunk of rows (one partial row per chunk, no
+// read-modify-write of a workspace row per row)
+// ---------------------------------------------------------------------------
+constexpr int kWideColsBlock = 256;  // threads per CTA of the column pass
+constexpr int kWideColsRows = 4;     // rows whose loads the column pass issues together
+
+constexpr int kWideSumsBlock = 512;  // threads per CTA of the per-row sums (two CTAs share an SM)
+
+// c[row] = (sum(g)/cols, sum(g*xhat)/cols) for LayerNorm, (sum(g*x)/cols, the
+// same) for RMSNorm, g = dy*w: one CTA per row.
+template <typename T, bool LN, int VE, typename TD = T>
+__global__ void __launch_bounds__(kWideSumsBlock)
+row_bwd_wide_sums_kernel(const RowArgs a, float2* __restrict__ c) {
+    __shared__ float ssm[32 * 2];
+    constexpr int NV = LN ? 2 : 1;
+    constexpr int U = kWideBatch;
+    const int cols = a.cols;
+    const int nvec = cols / VE;
+    const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
+    const TD* __restrict__ dy = reinterpret_cast<const TD*>(a.dy);
+    const int bd = blockDim.x;
+    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+        const T* xr = x + row * cols;
+        const TD* dyr = dy + row * cols;
+        const float rs = a.rstd_in[row];
+        const float mu = LN ? a.mean_in[row] : 0.f;
+        float s[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) s[i] = 0.f;
+        for (int v0 = threadIdx.x; v0 < nvec; v0 += U * bd) {
+            RawVec<T, VE> rx[U];
+            RawVec<TD, VE> rd[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int vi = v0 + u * bd;
+                if (vi < nvec) {
+                    rx[u].load(xr + int64_t(vi) * VE);
+                    rd[u].load(dyr + int64_t(vi) * VE);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int vi = v0 + u * bd;
+                if (vi < nvec) {
+                    float xv[VE], dv[VE], wv[VE];
+                    rx[u].unpack(xv);
+                    rd[u].unpack(dv);
+                    load_param<T, VE>(a.w, vi, wv, 1.f);
+#pragma unroll
+                    for (int k = 0; k < VE; ++k) {
+                        const float g = dv[k] * wv[k];
+                        if constexpr (LN) {
+                            s[0] += g;
+                            s[NV - 1] = fmaf(g, (xv[k] - mu) * rs, s[NV - 1]);
+                        } else {
+                            s[0] = fmaf(g, xv[k], s[0]);
+                        }
+                    }
+                }
+            }
+        }
+        block_sum<NV>(s, ssm);
+        if (threadIdx.x == 0) c[row] = make_float2(s[0] / float(cols), s[NV - 1] / float(cols));
+    }
+}
+
+// dx for rows [blockIdx.y*rpc, +rpc) and this thread's column vector, and the
+// chunk's partial dw/db row.
+template <typename T, bool LN, int VE, typename TD = T>
+__global__ void __launch_bounds__(kWideColsBlock)
+row_bwd_wide_cols_kernel(const RowArgs a, const float2* __restrict__ c, int rpc) {
+    const int cols = a.cols;
+    const int nvec = cols / VE;
+    const int vi = blockIdx.x * kWideColsBlock + threadIdx.x;
+    if (vi < nvec) {
+        const int64_t r0 = int64_t(blockIdx.y) * rpc;
+        const int64_t r1 = a.rows - r0 < rpc ? a.rows : r0 + rpc;
+        const T* __restrict__ x = reinterpret_cast<const T*>(a.x) + int64_t(vi) * VE;
+        const TD* __restrict__ dy = reinterpret_cast<const TD*>(a.dy) + int64_t(vi) * VE;
+        T* __restrict__ dx = reinterpret_cast<T*>(a.dx) + int64_t(vi) * VE;
+        float wv[VE], accw[VE], accb[VE];
+        load_param<T, VE>(a.w, vi, wv, 1.f);
+#pragma unroll
+        for (int k = 0; k < VE; ++k) accw[k] = accb[k] = 0.f;
+        for (int64_t rb = r0; rb < r1; rb += kWideColsRows) {
+            const int nr = r1 - rb < kWideColsRows ? int(r1 - rb) : kWideColsRows;
+            float xv[kWideColsRows][VE], dv[kWideColsRows][VE];
+#pragma unroll
+            for (int u = 0; u < kWideColsRows; ++u) {
+                if (u < nr) {
+                    load_vec<T, VE>(x + (rb + u) * cols, xv[u]);
+                    load_as<TD, VE>(dy + (rb + u) * cols, dv[u]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kWideColsRows; ++u) {
+                if (u < nr) {
+                    const int64_t r = rb + u;
+                    const float rs = a.rstd_in[r];
+                    const float mu = LN ? a.mean_in[r] : 0.f;
+                    const float2 cc = c[r];
+                    float o[VE];
+#pragma unroll
+                    for (int k = 0; k < VE; ++k) {
+                        const float g = dv[u][k] * wv[k];
+                        const float xs = LN ? (xv[u][k] - mu) * rs : xv[u][k] * rs;  // xhat or x*inv_rms
+                        if constexpr (LN) {
+                            o[k] = rs * (g - cc.x - xs * cc.y);
+                        } else {
+                            o[k] = rs * (g - xv[u][k] * (cc.x * rs * rs));
+                        }
+                        accw[k] = fmaf(dv[u][k], xs, accw[k]);
+                        accb[k] += dv[u][k];
+                    }
+                    store_vec<T, VE>(dx + r * cols, o);
+                }
+            }
+        }
+        const int64_t off = int64_t(blockIdx.y) * cols + int64_t(vi) * VE;
+#pragma unroll
+        for (int k = 0; k < VE; ++k) {
+            if (a.ws_dw) a.ws_dw[off + k] = accw[k];
+            if (a.ws_db) a.ws_db[off + k] = accb[k];
         }
     }
     pdl_trigger();
@@ -946,7 +1143,7 @@ nrm_status row_fwd_to(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s
                                       : row_fwd_fn<T, true, 1, TO>(tpr, nvec))
                                : (vec ? row_fwd_fn<T, false, kVec<T>, TO>(tpr, nvec)
                                       : row_fwd_fn<T, false, 1, TO>(tpr, nvec));
-    const int block = tpr ? row_fwd_block(tpr) : kRowWideBlock;
+    const int block = tpr ? row_fwd_block(tpr) : kWideFwdBlock;
     const int rpc = tpr ? block / tpr : 1;
     const int occ = cached_occupancy(fn, block, 0);
     if (occ <= 0) return fail(NRM_ERR_CUDA, "row forward kernel cannot be resident");
@@ -962,11 +1159,80 @@ nrm_status row_fwd(const RowArgs& a, bool layernorm, bool vec, cudaStream_t s) {
     return row_fwd_to<T, T>(a, layernorm, vec, s);
 }
 
+// The fixed-order column sums of P partial dw/db rows (programmatic dependent
+// launch after the kernel that wrote them).
+template <typename T>
+nrm_status row_colsum_launch(const RowArgs& a, int P, cudaStream_t s) {
+    const float* wsw = a.ws_dw;
+    const float* wsb = a.ws_db;
+    int P_ = P;
+    int cols = a.cols;
+    T* dw = reinterpret_cast<T*>(a.dw);
+    T* db = reinterpret_cast<T*>(a.db);
+    void* cargs[] = {&wsw, &wsb, &P_, &cols, &dw, &db};
+    return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((a.cols + 31) / 32, 2), dim3(kColsumWarps * 32),
+                      cargs, s);
+}
+
+// Threads per CTA of a wide-row kernel used for rows of `nvec` vectors: a
+// warp multiple that covers the row, at most kRowWideBlock.
+inline int wide_block(int nvec) {
+    int b = (nvec + 31) / 32 * 32;
+    return b < 32 ? 32 : (b > kRowWideBlock ? kRowWideBlock : b);
+}
+
+// The wide-row backward in two kernels (per-row sums, then the column pass)
+// for 16-byte vectors.  The per-row sums take 2*rows floats of the dw
+// workspace after the chunks' partial rows; returns the chunk count (the
+// partial rows for the column sums), or 0 when the workspace has no room for
+// them (the one-kernel wide path runs instead).
+template <typename T, typename TD>
+int row_bwd_wide_split(const RowArgs& a, float* ws0, bool layernorm, cudaStream_t s, nrm_status& st) {
+    constexpr int VE = kVec<T>;
+    const DevInfo* d = dev_info();
+    st = NRM_OK;
+    if (!d || !ws0 || a.rows <= 0) return 0;
+    const int nvec = a.cols / VE;
+    const int slabs = (nvec + kWideColsBlock - 1) / kWideColsBlock;
+    int64_t cap = row_bwd_max_partials(*d);
+    if (a.max_partials > 0 && cap > a.max_partials) cap = a.max_partials;
+    const int64_t c_rows = (2 * a.rows + a.cols - 1) / a.cols;  // workspace rows the sums take
+    int64_t rc = (int64_t(4) * d->sms + slabs - 1) / slabs;   // about four CTAs per SM
+    if (rc > a.rows) rc = a.rows;
+    if (rc > cap - c_rows) rc = cap - c_rows;
+    if (rc < 1) return 0;
+    const int rpc = int((a.rows + rc - 1) / rc);
+    rc = (a.rows + rpc - 1) / rpc;
+    float2* c = reinterpret_cast<float2*>(ws0 + size_t(rc) * size_t(a.cols));
+    const void* sums = layernorm ? (const void*)&row_bwd_wide_sums_kernel<T, true, VE, TD>
+                                 : (const void*)&row_bwd_wide_sums_kernel<T, false, VE, TD>;
+    const void* colk = layernorm ? (const void*)&row_bwd_wide_cols_kernel<T, true, VE, TD>
+                                 : (const void*)&row_bwd_wide_cols_kernel<T, false, VE, TD>;
+    const int block = kWideSumsBlock;
+    const int occ = cached_occupancy(sums, block, 0);
+    if (occ <= 0) {
+        st = fail(NRM_ERR_CUDA, "row backward (sums) kernel cannot be resident");
+        return 0;
+    }
+    const int64_t g1 = a.rows < int64_t(occ) * d->sms ? a.rows : int64_t(occ) * d->sms;
+    RowArgs args = a;
+    void* k1[] = {&args, &c};
+    st = cuda_status(cudaLaunchKernel(sums, dim3(unsigned(g1)), dim3(block), k1, 0, s), "row backward (sums) launch");
+    if (st != NRM_OK) return 0;
+    const float2* cc = c;
+    int rpc_ = rpc;
+    void* k2[] = {&args, &cc, &rpc_};
+    st = cuda_status(cudaLaunchKernel(colk, dim3(unsigned(slabs), unsigned(rc)), dim3(kWideColsBlock), k2, 0, s),
+                     "row backward (columns) launch");
+    return st == NRM_OK ? int(rc) : 0;
+}
+
 template <typename T>
 nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     const bool want = a.dw || a.db;
+    float* const ws0 = a.ws_dw;
     if (!want) a.ws_dw = a.ws_db = nullptr;
     const int ve = vec ? kVec<T> : 1;
     RrGeom rg;
@@ -984,6 +1250,12 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
         groups = rg.chunks;
         p = d->sms;
     } else {
+        if (tpr == 0 && vec) {
+            nrm_status st = NRM_OK;
+            const int rc = row_bwd_wide_split<T, T>(a, ws0, layernorm, s, st);
+            if (st != NRM_OK) return st;
+            if (rc > 0) return want ? row_colsum_launch<T>(a, rc, s) : NRM_OK;
+        }
         const bool db = a.ws_db != nullptr;
         fn = layernorm ? (vec ? row_bwd_fn<T, true, kVec<T>>(tpr, db) : row_bwd_fn<T, true, 1>(tpr, db))
                        : (vec ? row_bwd_fn<T, false, kVec<T>>(tpr, db) : row_bwd_fn<T, false, 1>(tpr, db));
@@ -1020,12 +1292,6 @@ nrm_status row_bwd(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
                       cargs, s);
 }
 
-// Threads per CTA of a wide-row kernel used for rows of `nvec` vectors: a
-// warp multiple that covers the row, at most kRowWideBlock.
-inline int wide_block(int nvec) {
-    int b = (nvec + 31) / 32 * 32;
-    return b < 32 ? 32 : (b > kRowWideBlock ? kRowWideBlock : b);
-}
 
 // Forward with the output kept in fp32 for a 16-bit input: the same kernels
 // as the plain forward, storing float32 (two 16-byte stores per input vector).
@@ -1041,6 +1307,7 @@ nrm_status row_bwd_f32dy(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
     const DevInfo* d = dev_info();
     if (!d) return fail(NRM_ERR_CUDA, "no usable CUDA device");
     const bool want = a.dw || a.db;
+    float* const ws0 = a.ws_dw;
     if (!want) a.ws_dw = a.ws_db = nullptr;
     constexpr int V = kVec<T>;
     RrGeom rg;
@@ -1065,6 +1332,12 @@ nrm_status row_bwd_f32dy(RowArgs a, bool layernorm, bool vec, cudaStream_t s) {
                 if (st != NRM_OK) return st;
             }
         }
+    }
+    if (!ring && vec && sizeof(T) == 2) {
+        nrm_status st = NRM_OK;
+        const int rc = row_bwd_wide_split<T, float>(a, ws0, layernorm, s, st);
+        if (st != NRM_OK) return st;
+        if (rc > 0) return want ? row_colsum_launch<T>(a, rc, s) : NRM_OK;
     }
     if (!ring) {
         const void* fn = layernorm ? (vec ? (const void*)&row_bwd_wide_kernel<T, true, V, float>
