@@ -624,6 +624,11 @@ struct RawVec {
 #pragma unroll
         for (int i = 0; i < N; ++i) u[i] = ld_stream_v4(p + i * (16 / int(sizeof(T))));
     }
+    // with an L2 eviction policy
+    __device__ __forceinline__ void load(const T* p, uint64_t pol) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) u[i] = ld_v4_policy(p + i * (16 / int(sizeof(T))), pol);
+    }
     __device__ __forceinline__ void unpack(float (&out)[VE]) const {
         constexpr int E = 16 / int(sizeof(T));
 #pragma unroll
@@ -665,12 +670,15 @@ row_fwd_wide_kernel(const RowArgs a) {
                 chan_merge(m, float(VE), vm, q);
             };
             if constexpr (VE == kVec<T>) {
-                // kWideBatch vectors' loads in flight per thread
+                // kWideBatch vectors' loads in flight per thread; the row stays in
+                // L2 (evict_last) for the normalising pass
+                const uint64_t keep = l2_evict_last();
                 for (int v0 = threadIdx.x; v0 < nvec; v0 += kWideBatch * int(blockDim.x)) {
                     RawVec<T, VE> r[kWideBatch];
 #pragma unroll
                     for (int u = 0; u < kWideBatch; ++u)
-                        if (v0 + u * int(blockDim.x) < nvec) r[u].load(xr + int64_t(v0 + u * int(blockDim.x)) * VE);
+                        if (v0 + u * int(blockDim.x) < nvec)
+                            r[u].load(xr + int64_t(v0 + u * int(blockDim.x)) * VE, keep);
 #pragma unroll
                     for (int u = 0; u < kWideBatch; ++u) {
                         if (v0 + u * int(blockDim.x) < nvec) {
@@ -719,11 +727,13 @@ row_fwd_wide_kernel(const RowArgs a) {
             store_as<TO, VE>(yr + int64_t(vi) * VE, o);
         };
         if constexpr (VE == kVec<T>) {
+            const uint64_t drop = l2_evict_first();  // the row's last read
             for (int v0 = threadIdx.x; v0 < nvec; v0 += kWideBatch * int(blockDim.x)) {
                 RawVec<T, VE> r[kWideBatch];
 #pragma unroll
                 for (int u = 0; u < kWideBatch; ++u)
-                    if (v0 + u * int(blockDim.x) < nvec) r[u].load(xr + int64_t(v0 + u * int(blockDim.x)) * VE);
+                    if (v0 + u * int(blockDim.x) < nvec)
+                        r[u].load(xr + int64_t(v0 + u * int(blockDim.x)) * VE, drop);
 #pragma unroll
                 for (int u = 0; u < kWideBatch; ++u) {
                     if (v0 + u * int(blockDim.x) < nvec) {
@@ -872,7 +882,7 @@ row_bwd_wide_kernel(const RowArgs a) {
 // read-modify-write of a workspace row per row)
 // ---------------------------------------------------------------------------
 constexpr int kWideColsBlock = 256;  // threads per CTA of the column pass
-constexpr int kWideColsRows = 4;     // rows whose loads the column pass issues together
+constexpr int kWideColsRows = 8;     // rows whose loads the column pass issues together
 
 constexpr int kWideSumsBlock = 512;  // threads per CTA of the per-row sums (two CTAs share an SM)
 
@@ -939,6 +949,8 @@ row_bwd_wide_sums_kernel(const RowArgs a, float2* __restrict__ c) {
 template <typename T, bool LN, int VE, typename TD = T>
 __global__ void __launch_bounds__(kWideColsBlock)
 row_bwd_wide_cols_kernel(const RowArgs a, const float2* __restrict__ c, int rpc) {
+    // rows in flight: 8, or 4 when dy is fp32 (twice the raw bytes per row)
+    constexpr int R = sizeof(TD) == sizeof(T) ? kWideColsRows : kWideColsRows / 2;
     const int cols = a.cols;
     const int nvec = cols / VE;
     const int vi = blockIdx.x * kWideColsBlock + threadIdx.x;
@@ -952,35 +964,39 @@ row_bwd_wide_cols_kernel(const RowArgs a, const float2* __restrict__ c, int rpc)
         load_param<T, VE>(a.w, vi, wv, 1.f);
 #pragma unroll
         for (int k = 0; k < VE; ++k) accw[k] = accb[k] = 0.f;
-        for (int64_t rb = r0; rb < r1; rb += kWideColsRows) {
-            const int nr = r1 - rb < kWideColsRows ? int(r1 - rb) : kWideColsRows;
-            float xv[kWideColsRows][VE], dv[kWideColsRows][VE];
+        for (int64_t rb = r0; rb < r1; rb += R) {
+            const int nr = r1 - rb < R ? int(r1 - rb) : R;
+            // the rows' raw bytes, all loads in flight before the arithmetic
+            RawVec<T, VE> rx[R];
+            RawVec<TD, VE> rd[R];
 #pragma unroll
-            for (int u = 0; u < kWideColsRows; ++u) {
+            for (int u = 0; u < R; ++u) {
                 if (u < nr) {
-                    load_vec<T, VE>(x + (rb + u) * cols, xv[u]);
-                    load_as<TD, VE>(dy + (rb + u) * cols, dv[u]);
+                    rx[u].load(x + (rb + u) * cols);
+                    rd[u].load(dy + (rb + u) * cols);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kWideColsRows; ++u) {
+            for (int u = 0; u < R; ++u) {
                 if (u < nr) {
                     const int64_t r = rb + u;
                     const float rs = a.rstd_in[r];
                     const float mu = LN ? a.mean_in[r] : 0.f;
                     const float2 cc = c[r];
-                    float o[VE];
+                    float xv[VE], dv[VE], o[VE];
+                    rx[u].unpack(xv);
+                    rd[u].unpack(dv);
 #pragma unroll
                     for (int k = 0; k < VE; ++k) {
-                        const float g = dv[u][k] * wv[k];
-                        const float xs = LN ? (xv[u][k] - mu) * rs : xv[u][k] * rs;  // xhat or x*inv_rms
+                        const float g = dv[k] * wv[k];
+                        const float xs = LN ? (xv[k] - mu) * rs : xv[k] * rs;  // xhat or x*inv_rms
                         if constexpr (LN) {
                             o[k] = rs * (g - cc.x - xs * cc.y);
                         } else {
-                            o[k] = rs * (g - xv[u][k] * (cc.x * rs * rs));
+                            o[k] = rs * (g - xv[k] * (cc.x * rs * rs));
                         }
-                        accw[k] = fmaf(dv[u][k], xs, accw[k]);
-                        accb[k] += dv[u][k];
+                        accw[k] = fmaf(dv[k], xs, accw[k]);
+                        accb[k] += dv[k];
                     }
                     store_vec<T, VE>(dx + r * cols, o);
                 }

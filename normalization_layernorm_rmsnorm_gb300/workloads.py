@@ -284,7 +284,7 @@ def _ln_wide(name, rows, cols, dev, f32):
         Call(name, "fwd", "row_fwd_wide_kernel<f16,ln>",
              lambda: nrm.nrm_layernorm_fwd(x, w, b, y, mean, rstd, 1e-5),
              nbytes(x, w, b, y, mean, rstd), 1, [x, w, b], [y, mean, rstd]),
-        Call(name, "bwd", "row_bwd_wide_kernel<f16,ln>+colsum",
+        Call(name, "bwd", "row_bwd_wide_sums+cols_kernel<f16,ln>+colsum",
              lambda: nrm.nrm_layernorm_bwd(dy, x, w, mean, rstd, dx, dw, db, ws),
-             nbytes(dy, x, w, mean, rstd, dx, dw, db), 2, [dy], [dx, dw, db]),
+             nbytes(dy, x, w, mean, rstd, dx, dw, db), 3, [dy], [dx, dw, db]),
     ]
