@@ -537,6 +537,25 @@ row_colsum_kernel(const float* __restrict__ ws_dw, const float* __restrict__ ws_
     }
 }
 
+// The same for a few partial rows (at most kColsumSerialMax): one thread per
+// column adds its P values in order (Neumaier-compensated), 256 columns per CTA.
+constexpr int kColsumSerialMax = 64;
+constexpr int kColsumSerialBlock = 256;
+template <typename T>
+__global__ void __launch_bounds__(kColsumSerialBlock)
+row_colsum_serial_kernel(const float* __restrict__ ws_dw, const float* __restrict__ ws_db, int P, int cols, T* dw,
+                         T* db) {
+    pdl_wait();
+    const float* ws = blockIdx.y == 0 ? ws_dw : ws_db;
+    T* out = blockIdx.y == 0 ? dw : db;
+    const int col = blockIdx.x * kColsumSerialBlock + threadIdx.x;
+    if (out == nullptr || col >= cols) return;
+    NeumaierSum s;
+#pragma unroll 8
+    for (int p = 0; p < P; ++p) s.add(ws[int64_t(p) * cols + col]);
+    reinterpret_cast<typename Io<T>::bits_t*>(out)[col] = Io<T>::store(s.value());
+}
+
 // ---------------------------------------------------------------------------
 // wide rows: one CTA per row, two passes over global memory
 // ---------------------------------------------------------------------------
@@ -1186,6 +1205,10 @@ nrm_status row_colsum_launch(const RowArgs& a, int P, cudaStream_t s) {
     T* dw = reinterpret_cast<T*>(a.dw);
     T* db = reinterpret_cast<T*>(a.db);
     void* cargs[] = {&wsw, &wsb, &P_, &cols, &dw, &db};
+    if (P <= kColsumSerialMax)
+        return launch_pdl((const void*)&row_colsum_serial_kernel<T>,
+                          dim3((a.cols + kColsumSerialBlock - 1) / kColsumSerialBlock, 2), dim3(kColsumSerialBlock),
+                          cargs, s);
     return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((a.cols + 31) / 32, 2), dim3(kColsumWarps * 32),
                       cargs, s);
 }
