@@ -310,6 +310,30 @@ def per_workload(calls, peak):
     return per
 
 
+def e2e_plan(calls):
+    """The copies of one end-to-end step: {call index: tensors to upload before
+    it} and {call index: tensors to download after it}.  An input is uploaded
+    before the call that first reads it unless an earlier call of the step
+    writes it (saved statistics, the ReLU mask stay on the device); an output
+    is downloaded after the call that last writes it."""
+    import collections
+    first_read, last_write, written = {}, {}, set()
+    for i, c in enumerate(calls):
+        for t in c.inputs:
+            if id(t) not in written:
+                first_read.setdefault(id(t), (i, t))
+        for t in c.outputs:
+            written.add(id(t))
+            last_write[id(t)] = (i, t)
+    up = collections.defaultdict(list)
+    down = collections.defaultdict(list)
+    for i, t in first_read.values():
+        up[i].append(t)
+    for i, t in last_write.values():
+        down[i].append(t)
+    return up, down
+
+
 def run_e2e(call_sets, args, stream, step_bytes, world):
     """Same step through host buffers, inside the timed region: every input
     uploaded from pinned host memory before the call that first reads it,
@@ -321,31 +345,9 @@ def run_e2e(call_sets, args, stream, step_bytes, world):
     the host link carries both directions at once throughout.  The pinned
     host buffers are shared by the two sets (uploads only read them; the
     downloads into them are ordered on one stream)."""
-    import collections
-
     import torch
 
-    def plan(calls):
-        # inputs that no earlier call of the step writes come from the host;
-        # what a call writes (saved statistics, the ReLU mask) stays on the
-        # device for the calls that read it later
-        first_read, last_write, written = {}, {}, set()
-        for i, c in enumerate(calls):
-            for t in c.inputs:
-                if id(t) not in written:
-                    first_read.setdefault(id(t), (i, t))
-            for t in c.outputs:
-                written.add(id(t))
-                last_write[id(t)] = (i, t)
-        up = collections.defaultdict(list)
-        down = collections.defaultdict(list)
-        for i, t in first_read.values():
-            up[i].append(t)
-        for i, t in last_write.values():
-            down[i].append(t)
-        return up, down
-
-    plans = [plan(calls) for calls in call_sets]
+    plans = [e2e_plan(calls) for calls in call_sets]
     up0, down0 = plans[0]
     host_up = {i: [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for t in lst]
                for i, lst in up0.items()}

@@ -79,3 +79,29 @@ def test_traffic_reported_only_for_matching_sources(tmp_path, monkeypatch):
     assert bench.ncu_traffic("k_stale") is None
     assert bench.ncu_traffic("k_nodigest") is None
     assert bench.ncu_traffic("missing") is None
+
+
+def test_e2e_plan_uploads_first_reads_and_downloads_last_writes():
+    # a forward writing y and the saved mean, then a backward reading them with
+    # dy: x, w and dy come from the host before the call that first reads them,
+    # the saved mean (written by the forward) is not uploaded again; y and mean
+    # are downloaded after the forward, dx and dw after the backward
+    import types
+    x, w, y, mean, dy, dx, dw = (object() for _ in range(7))
+    fwd = types.SimpleNamespace(inputs=[x, w], outputs=[y, mean])
+    bwd = types.SimpleNamespace(inputs=[dy, x, w, mean], outputs=[dx, dw])
+    up, down = bench.e2e_plan([fwd, bwd])
+    assert up[0] == [x, w] and up[1] == [dy]
+    assert down[0] == [y, mean] and down[1] == [dx, dw]
+
+
+def test_e2e_plan_rewritten_tensor_moves_once_each_way():
+    # running statistics read and updated by two calls: uploaded before the
+    # first, downloaded after the last
+    import types
+    rm = object()
+    a = types.SimpleNamespace(inputs=[rm], outputs=[rm])
+    b = types.SimpleNamespace(inputs=[rm], outputs=[rm])
+    up, down = bench.e2e_plan([a, b])
+    assert up[0] == [rm] and 1 not in up
+    assert down[1] == [rm] and 0 not in down
