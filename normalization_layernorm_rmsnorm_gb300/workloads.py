@@ -207,7 +207,7 @@ def _bn_gelu(cfg, dev, f32):
     return calls
 
 
-def _ln_cf(name, n, c, l, dev, f32):
+def _ln_cf(name, n, c, l, dev, f32, kernels=("lncf_fwd_ring_kernel<f16>", "lncf_bwd_ring_kernel<f16>+colsum")):
     import normalization_layernorm_rmsnorm_gb300 as nrm
     from normalization_layernorm_rmsnorm_gb300 import synth
     seed = 31
@@ -220,10 +220,10 @@ def _ln_cf(name, n, c, l, dev, f32):
     mean, rstd = f32(n * l), f32(n * l)
     ws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_CF_BWD, n * l, c, nrm.NRM_F16) // 4)
     return [
-        Call(name, "fwd", "lncf_fwd_ring_kernel<f16>",
+        Call(name, "fwd", kernels[0],
              lambda: nrm.nrm_layernorm_cf_fwd(x, w, b, y, mean, rstd, 1e-6),
              nbytes(x, w, b, y, mean, rstd), 1, [x, w, b], [y, mean, rstd]),
-        Call(name, "bwd", "lncf_bwd_ring_kernel<f16>+colsum",
+        Call(name, "bwd", kernels[1],
              lambda: nrm.nrm_layernorm_cf_bwd(dy, x, w, mean, rstd, dx, dw, db, ws),
              nbytes(dy, x, w, mean, rstd, dx, dw, db), 2, [dy], [dx, dw, db]),
     ]
@@ -287,4 +287,103 @@ def _ln_wide(name, rows, cols, dev, f32):
         Call(name, "bwd", "row_bwd_wide_sums+cols_kernel<f16,ln>+colsum",
              lambda: nrm.nrm_layernorm_bwd(dy, x, w, mean, rstd, dx, dw, db, ws),
              nbytes(dy, x, w, mean, rstd, dx, dw, db), 3, [dy], [dx, dw, db]),
+    ]
+
+
+# Shapes that take the paths no bench workload reaches, run only by
+# profile_case for their ncu captures: rows that are not 16-byte multiples (the
+# scalar register kernels), BatchNorm eval above 4096 channels (the ring eval
+# forward), channels-first planes that are not 16-byte multiples (the register
+# kernels), an unaligned activation-dropout tensor (the scalar kernel) and
+# unaligned rows too wide for the register kernels (the one-kernel wide
+# backward).
+PROFILE_ONLY = ("ln_f16_65536x1023", "bn_f32_64x8192x8x8_eval", "ln_cf_f16_2048x768x7x7",
+                "act_dropout_gelu_f16_unaligned_67108863", "ln_f16_2048x65537")
+
+
+def build_profile_calls(dev, names):
+    import torch
+
+    def f32(n):
+        return torch.empty(n, dtype=torch.float32, device=dev)
+
+    calls = []
+    if "ln_f16_65536x1023" in names:
+        calls += _ln_plain("ln_f16_65536x1023", 65536, 1023, dev, f32,
+                           ("row_fwd_kernel<f16,ln,scalar>", "row_bwd_kernel<f16,ln,scalar>+colsum"))
+    if "bn_f32_64x8192x8x8_eval" in names:
+        calls += _bn_eval_plain("bn_f32_64x8192x8x8_eval", 64, 8192, 64, dev, f32)
+    if "ln_cf_f16_2048x768x7x7" in names:
+        calls += _ln_cf("ln_cf_f16_2048x768x7x7", 2048, 768, 49, dev, f32,
+                        ("lncf_fwd_kernel<f16>", "lncf_bwd_kernel<f16>+colsum"))
+    if "act_dropout_gelu_f16_unaligned_67108863" in names:
+        calls += _act_dropout_unaligned("act_dropout_gelu_f16_unaligned_67108863", 67108863, dev)
+    if "ln_f16_2048x65537" in names:
+        calls += _ln_plain("ln_f16_2048x65537", 2048, 65537, dev, f32,
+                           ("row_fwd_wide_kernel<f16,ln,scalar>", "row_bwd_wide_kernel<f16,ln,scalar>+colsum"))
+    return calls
+
+
+def _ln_plain(name, rows, cols, dev, f32, kernels):
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    seed = 47
+    x = synth.random_tensor(seed, 1, (rows, cols), "f16", mean=0.3, std=1.5).torch(dev)
+    w = synth.store(1 + 0.1 * synth.normal(seed, 2, cols), "f16", (cols,)).torch(dev)
+    b = synth.store(0.1 * synth.normal(seed, 3, cols), "f16", (cols,)).torch(dev)
+    dy = synth.random_tensor(seed, 4, (rows, cols), "f16").torch(dev)
+    y, dx, dw, db = x.new_empty(x.shape), x.new_empty(x.shape), w.new_empty(cols), b.new_empty(cols)
+    mean, rstd = f32(rows), f32(rows)
+    ws = f32(nrm.nrm_workspace_bytes(nrm.NRM_OP_LAYERNORM_BWD, rows, cols, nrm.NRM_F16) // 4)
+    return [
+        Call(name, "fwd", kernels[0], lambda: nrm.nrm_layernorm_fwd(x, w, b, y, mean, rstd, 1e-5),
+             nbytes(x, w, b, y, mean, rstd), 1, [x, w, b], [y, mean, rstd]),
+        Call(name, "bwd", kernels[1], lambda: nrm.nrm_layernorm_bwd(dy, x, w, mean, rstd, dx, dw, db, ws),
+             nbytes(dy, x, w, mean, rstd, dx, dw, db), 2, [dy], [dx, dw, db]),
+    ]
+
+
+def _bn_eval_plain(name, n, c, l, dev, f32):
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    seed = 53
+    x = synth.random_tensor(seed, 1, (n, c, l), "f32", mean=0.2, std=1.4).torch(dev)
+    dy = synth.random_tensor(seed, 2, (n, c, l), "f32").torch(dev)
+    w = synth.store(1 + 0.2 * synth.normal(seed, 3, c), "f32", (c,)).torch(dev)
+    b = synth.store(0.2 * synth.normal(seed, 4, c), "f32", (c,)).torch(dev)
+    rm = synth.store(0.3 * synth.normal(seed, 5, c), "f32", (c,)).torch(dev)
+    rv = synth.store(0.5 + synth.uniform(seed, 6, c), "f32", (c,)).torch(dev)
+    y, dx = x.new_empty(x.shape), x.new_empty(x.shape)
+    sm, sr, dw, db = f32(c), f32(c), f32(c), f32(c)
+    ws = nrm.batchnorm_workspace(x)
+    return [
+        Call(name, "fwd", "bn_fwd_eval_kernel<f32,none>",
+             lambda: nrm.nrm_batchnorm_fwd(x, None, w, b, y, rm, rv, sm, sr, None, 1e-5, 0.1, False, "none", ws),
+             nbytes(x, y, w, b, rm, rv, sm, sr), 1, [x, w, b, rm, rv], [y, sm, sr]),
+        Call(name, "bwd", "bn_bwd_eval_kernel<f32,none>",
+             lambda: nrm.nrm_batchnorm_bwd(dy, x, None, w, b, sm, sr, None, dx, None, dw, db, False, "none", ws),
+             nbytes(dy, x, w, b, sm, sr, dx, dw, db), 1, [dy], [dx, dw, db]),
+    ]
+
+
+def _act_dropout_unaligned(name, count, dev):
+    import torch
+
+    import normalization_layernorm_rmsnorm_gb300 as nrm
+    from normalization_layernorm_rmsnorm_gb300 import synth
+    seed = 59
+    # views one element into their buffers: not 16-byte aligned
+    xb = torch.empty(count + 1, dtype=torch.float16, device=dev)
+    dyb = torch.empty(count + 1, dtype=torch.float16, device=dev)
+    xb[1:] = synth.random_tensor(seed, 1, (count,), "f16").torch(dev)
+    dyb[1:] = synth.random_tensor(seed, 2, (count,), "f16").torch(dev)
+    x, dy = xb[1:], dyb[1:]
+    y = torch.empty(count + 1, dtype=torch.float16, device=dev)[1:]
+    dx = torch.empty(count + 1, dtype=torch.float16, device=dev)[1:]
+    p, s = DROPOUT_P, DROPOUT_SEED
+    return [
+        Call(name, "fwd", "act_dropout_scalar_kernel<f16,gelu>",
+             lambda: nrm.nrm_act_dropout_fwd(x, y, "gelu", p, s), nbytes(x, y), 1, [x], [y]),
+        Call(name, "bwd", "act_dropout_scalar_kernel<f16,gelu,bwd>",
+             lambda: nrm.nrm_act_dropout_bwd(dy, x, dx, "gelu", p, s), nbytes(dy, x, dx), 1, [dy], [dx]),
     ]
