@@ -62,10 +62,13 @@ __device__ __forceinline__ CfTile cf_tile(int64_t t, int64_t tiles_per_sample, i
     return r;
 }
 
-template <typename T, int V>
+// K groups of V positions per lane, strided by 32*V: a tile of PW = 32*V*K
+// positions.  K > 1 serves planes that are not 16-byte multiples (V = 1), so
+// that a 7x7 or 14x14 plane is one tile rather than two to seven of 32.
+template <typename T, int V, int K = 1>
 __global__ void __launch_bounds__(kCfThreads)
 lncf_fwd_kernel(const CfArgs a) {
-    constexpr int PW = 32 * V;  // positions per tile
+    constexpr int PW = 32 * V * K;  // positions per tile
     __shared__ float part[kCfWarps][3][PW];  // per warp and position: n, mean, m2
     __shared__ float stat[2][PW];            // mean, rstd per position
     const int lane = threadIdx.x & 31;
@@ -78,38 +81,62 @@ lncf_fwd_kernel(const CfArgs a) {
 
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const CfTile tl = cf_tile(t, tps, PW);
-        const int64_t p0 = tl.p_base + lane * V;
-        const bool on = p0 < l;  // V divides l on the vector path
-        const T* xb = x + tl.i * c * l + p0;
+        int64_t p0[K];
+        bool on[K];
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            p0[j] = tl.p_base + (j * 32 + lane) * V;
+            on[j] = p0[j] < l;  // V divides l on the vector path
+            any |= on[j];
+        }
+        const T* xs = x + tl.i * c * l;
         // ---- pass 1: shifted sums over this warp's channels ----
-        float kk[V], s[V], q[V];
+        float kk[K][V], s[K][V], q[K][V];
         int cnt = 0;
 #pragma unroll
-        for (int k = 0; k < V; ++k) kk[k] = s[k] = q[k] = 0.f;
-        if (on) {
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int k = 0; k < V; ++k) kk[j][k] = s[j][k] = q[j][k] = 0.f;
+        if (any) {
             for (int64_t ch = warp; ch < c; ch += kCfWarps) {
-                float v[V];
-                cf_load<T, V>(xb + ch * l, v);
+                float v[K][V];
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    if (on[j]) {
+                        cf_load<T, V>(xs + ch * l + p0[j], v[j]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < V; ++k) v[j][k] = 0.f;
+                    }
+                }
                 if (cnt == 0) {
 #pragma unroll
-                    for (int k = 0; k < V; ++k) kk[k] = v[k];
+                    for (int j = 0; j < K; ++j)
+#pragma unroll
+                        for (int k = 0; k < V; ++k) kk[j][k] = v[j][k];
                 }
 #pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    const float d = v[k] - kk[k];
-                    s[k] += d;
-                    q[k] = fmaf(d, d, q[k]);
-                }
+                for (int j = 0; j < K; ++j)
+#pragma unroll
+                    for (int k = 0; k < V; ++k) {
+                        const float d = v[j][k] - kk[j][k];
+                        s[j][k] += d;
+                        q[j][k] = fmaf(d, d, q[j][k]);
+                    }
                 ++cnt;
             }
         }
 #pragma unroll
-        for (int k = 0; k < V; ++k) {
-            const float fn = float(cnt);
-            part[warp][0][lane * V + k] = fn;
-            part[warp][1][lane * V + k] = cnt ? kk[k] + s[k] / fn : 0.f;
-            part[warp][2][lane * V + k] = cnt ? fmaxf(q[k] - s[k] * (s[k] / fn), 0.f) : 0.f;
-        }
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const int pi = (j * 32 + lane) * V + k;
+                const float fn = on[j] ? float(cnt) : 0.f;
+                part[warp][0][pi] = fn;
+                part[warp][1][pi] = fn > 0.f ? kk[j][k] + s[j][k] / fn : 0.f;
+                part[warp][2][pi] = fn > 0.f ? fmaxf(q[j][k] - s[j][k] * (s[j][k] / fn), 0.f) : 0.f;
+            }
         __syncthreads();
         // ---- merge the 8 warps per position (fixed order) ----
         for (int pi = threadIdx.x; pi < PW; pi += kCfThreads) {
@@ -127,32 +154,42 @@ lncf_fwd_kernel(const CfArgs a) {
         }
         __syncthreads();
         // ---- pass 2: y = (x - mean)*rstd*w + b ----
-        if (on) {
-            float mu[V], rs[V];
+        if (any) {
+            float mu[K][V], rs[K][V];
 #pragma unroll
-            for (int k = 0; k < V; ++k) {
-                mu[k] = stat[0][lane * V + k];
-                rs[k] = stat[1][lane * V + k];
-            }
-            T* yb = y + tl.i * c * l + p0;
+            for (int j = 0; j < K; ++j)
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    mu[j][k] = stat[0][(j * 32 + lane) * V + k];
+                    rs[j][k] = stat[1][(j * 32 + lane) * V + k];
+                }
+            T* ys = y + tl.i * c * l;
             for (int64_t ch = warp; ch < c; ch += kCfWarps) {
-                float v[V], o[V];
-                cf_load<T, V>(xb + ch * l, v);
                 const float wc = cf_wb<T>(a.w, ch, 1.f);
                 const float bc = cf_wb<T>(a.b, ch, 0.f);
+                float v[K][V];
 #pragma unroll
-                for (int k = 0; k < V; ++k) o[k] = fmaf((v[k] - mu[k]) * rs[k], wc, bc);
-                cf_store<T, V>(yb + ch * l, o);
+                for (int j = 0; j < K; ++j)
+                    if (on[j]) cf_load<T, V>(xs + ch * l + p0[j], v[j]);
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    if (on[j]) {
+                        float o[V];
+#pragma unroll
+                        for (int k = 0; k < V; ++k) o[k] = fmaf((v[j][k] - mu[j][k]) * rs[j][k], wc, bc);
+                        cf_store<T, V>(ys + ch * l + p0[j], o);
+                    }
+                }
             }
         }
         __syncthreads();  // part / stat are rewritten by the next tile
     }
 }
 
-template <typename T, int V>
+template <typename T, int V, int K = 1>
 __global__ void __launch_bounds__(kCfThreads)
 lncf_bwd_kernel(const CfArgs a) {
-    constexpr int PW = 32 * V;
+    constexpr int PW = 32 * V * K;
     __shared__ float part[kCfWarps][2][PW];  // per warp and position: sum g, sum g*xhat
     __shared__ float coef[2][PW];            // c1, c2 per position
     extern __shared__ float acc[];           // [2][c]: this CTA's dw, db partial row
@@ -171,38 +208,61 @@ lncf_bwd_kernel(const CfArgs a) {
 
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const CfTile tl = cf_tile(t, tps, PW);
-        const int64_t p0 = tl.p_base + lane * V;
-        const bool on = p0 < l;
-        const int64_t off = tl.i * c * l + p0;
-        float mu[V], rs[V];
+        int64_t p0[K];
+        bool on[K];
+        bool any = false;
 #pragma unroll
-        for (int k = 0; k < V; ++k) {
-            mu[k] = on ? a.mean_in[tl.i * l + p0 + k] : 0.f;
-            rs[k] = on ? a.rstd_in[tl.i * l + p0 + k] : 0.f;
+        for (int j = 0; j < K; ++j) {
+            p0[j] = tl.p_base + (j * 32 + lane) * V;
+            on[j] = p0[j] < l;
+            any |= on[j];
         }
-        // ---- pass 1: sum g and sum g*xhat over this warp's channels, g = dy*w ----
-        float s1[V], s2[V];
+        const int64_t base = tl.i * c * l;
+        float mu[K][V], rs[K][V];
 #pragma unroll
-        for (int k = 0; k < V; ++k) s1[k] = s2[k] = 0.f;
-        if (on) {
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                mu[j][k] = on[j] ? a.mean_in[tl.i * l + p0[j] + k] : 0.f;
+                rs[j][k] = on[j] ? a.rstd_in[tl.i * l + p0[j] + k] : 0.f;
+            }
+        // ---- pass 1: sum g and sum g*xhat over this warp's channels, g = dy*w ----
+        float s1[K][V], s2[K][V];
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int k = 0; k < V; ++k) s1[j][k] = s2[j][k] = 0.f;
+        if (any) {
             for (int64_t ch = warp; ch < c; ch += kCfWarps) {
-                float dv[V], xv[V];
-                cf_load<T, V>(dy + off + ch * l, dv);
-                cf_load<T, V>(x + off + ch * l, xv);
+                float dv[K][V], xv[K][V];
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    if (on[j]) {
+                        cf_load<T, V>(dy + base + ch * l + p0[j], dv[j]);
+                        cf_load<T, V>(x + base + ch * l + p0[j], xv[j]);
+                    }
+                }
                 const float wc = cf_wb<T>(a.w, ch, 1.f);
 #pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    const float g = dv[k] * wc;
-                    s1[k] += g;
-                    s2[k] = fmaf(g, (xv[k] - mu[k]) * rs[k], s2[k]);
+                for (int j = 0; j < K; ++j) {
+                    if (on[j]) {
+#pragma unroll
+                        for (int k = 0; k < V; ++k) {
+                            const float g = dv[j][k] * wc;
+                            s1[j][k] += g;
+                            s2[j][k] = fmaf(g, (xv[j][k] - mu[j][k]) * rs[j][k], s2[j][k]);
+                        }
+                    }
                 }
             }
         }
 #pragma unroll
-        for (int k = 0; k < V; ++k) {
-            part[warp][0][lane * V + k] = s1[k];
-            part[warp][1][lane * V + k] = s2[k];
-        }
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                part[warp][0][(j * 32 + lane) * V + k] = s1[j][k];
+                part[warp][1][(j * 32 + lane) * V + k] = s2[j][k];
+            }
         __syncthreads();
         for (int pi = threadIdx.x; pi < PW; pi += kCfThreads) {
             float t1 = 0.f, t2 = 0.f;
@@ -216,27 +276,40 @@ lncf_bwd_kernel(const CfArgs a) {
         }
         __syncthreads();
         // ---- pass 2: dx; this tile's dw, db per channel ----
-        float c1[V], c2[V];
+        float c1[K][V], c2[K][V];
 #pragma unroll
-        for (int k = 0; k < V; ++k) {
-            c1[k] = coef[0][lane * V + k];
-            c2[k] = coef[1][lane * V + k];
-        }
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                c1[j][k] = coef[0][(j * 32 + lane) * V + k];
+                c2[j][k] = coef[1][(j * 32 + lane) * V + k];
+            }
         for (int64_t ch = warp; ch < c; ch += kCfWarps) {
             float pw = 0.f, pb = 0.f;
-            if (on) {
-                float dv[V], xv[V], o[V];
-                cf_load<T, V>(dy + off + ch * l, dv);
-                cf_load<T, V>(x + off + ch * l, xv);
+            if (any) {
+                float dv[K][V], xv[K][V];
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    if (on[j]) {
+                        cf_load<T, V>(dy + base + ch * l + p0[j], dv[j]);
+                        cf_load<T, V>(x + base + ch * l + p0[j], xv[j]);
+                    }
+                }
                 const float wc = cf_wb<T>(a.w, ch, 1.f);
 #pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    const float xh = (xv[k] - mu[k]) * rs[k];
-                    o[k] = rs[k] * (dv[k] * wc - c1[k] - xh * c2[k]);
-                    pw = fmaf(dv[k], xh, pw);
-                    pb += dv[k];
+                for (int j = 0; j < K; ++j) {
+                    if (on[j]) {
+                        float o[V];
+#pragma unroll
+                        for (int k = 0; k < V; ++k) {
+                            const float xh = (xv[j][k] - mu[j][k]) * rs[j][k];
+                            o[k] = rs[j][k] * (dv[j][k] * wc - c1[j][k] - xh * c2[j][k]);
+                            pw = fmaf(dv[j][k], xh, pw);
+                            pb += dv[j][k];
+                        }
+                        cf_store<T, V>(dx + base + ch * l + p0[j], o);
+                    }
                 }
-                cf_store<T, V>(dx + off + ch * l, o);
             }
             if (grads) {
                 pw = warp_sum(pw);

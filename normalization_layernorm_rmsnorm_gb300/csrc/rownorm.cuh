@@ -1465,6 +1465,19 @@ inline bool cfr_plan(CfrGeom& g, size_t& smem, const CfArgs& a, size_t es, bool 
     return true;
 }
 
+// Position groups per lane of the scalar register kernels: the fewest of 1, 2,
+// 4, 8 (32 positions each) that cover a plane of l positions.
+inline int cf_scalar_groups(int64_t l) { return l <= 32 ? 1 : (l <= 64 ? 2 : (l <= 128 ? 4 : 8)); }
+template <typename T, bool BWD>
+const void* cf_scalar_fn(int K) {
+    switch (K) {
+    case 1: return BWD ? (const void*)&lncf_bwd_kernel<T, 1, 1> : (const void*)&lncf_fwd_kernel<T, 1, 1>;
+    case 2: return BWD ? (const void*)&lncf_bwd_kernel<T, 1, 2> : (const void*)&lncf_fwd_kernel<T, 1, 2>;
+    case 4: return BWD ? (const void*)&lncf_bwd_kernel<T, 1, 4> : (const void*)&lncf_fwd_kernel<T, 1, 4>;
+    default: return BWD ? (const void*)&lncf_bwd_kernel<T, 1, 8> : (const void*)&lncf_fwd_kernel<T, 1, 8>;
+    }
+}
+
 template <typename T>
 nrm_status cf_fwd(const CfArgs& a, bool vec, cudaStream_t s) {
     const DevInfo* d = dev_info();
@@ -1485,8 +1498,13 @@ nrm_status cf_fwd(const CfArgs& a, bool vec, cudaStream_t s) {
         return cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(kCfrThreads), kargs, smem, s),
                            "channels-first LayerNorm forward launch");
     }
-    const void* fn = vec ? (const void*)&lncf_fwd_kernel<T, kVec<T>> : (const void*)&lncf_fwd_kernel<T, 1>;
-    const int pw = 32 * (vec ? kVec<T> : 1);
+    // groups only where they fold a mostly idle second tile into the first
+    // (planes of up to 64 positions): the forward has no per-channel warp
+    // reductions to save, and fewer tiles are fewer CTAs (fp16 [256,384,14,14]:
+    // 51 us with 32-position tiles, 62 with one 256-position tile per plane)
+    const int K = vec ? 1 : (a.l <= 64 ? cf_scalar_groups(a.l) : 1);
+    const void* fn = vec ? (const void*)&lncf_fwd_kernel<T, kVec<T>> : cf_scalar_fn<T, false>(K);
+    const int pw = 32 * (vec ? kVec<T> : K);
     const int64_t tiles = a.n * ((a.l + pw - 1) / pw);
     const int occ = cached_occupancy(fn, kCfThreads, 0);
     if (occ <= 0) return fail(NRM_ERR_CUDA, "channels-first LayerNorm forward cannot be resident");
@@ -1544,8 +1562,12 @@ nrm_status cf_bwd(CfArgs a, bool vec, cudaStream_t s) {
         return launch_pdl((const void*)&row_colsum_kernel<T>, dim3((cols + 31) / 32, 2),
                           dim3(kColsumWarps * 32), cargs, s);
     }
-    const void* fn = vec ? (const void*)&lncf_bwd_kernel<T, kVec<T>> : (const void*)&lncf_bwd_kernel<T, 1>;
-    const int pw = 32 * (vec ? kVec<T> : 1);
+    // one dw/db warp reduction per channel and tile: a plane in one tile where
+    // it fits 256 positions (fp16 [256,384,14,14] 158 -> 127 us, [2048,768,7,7]
+    // 676 -> 545 us)
+    const int K = vec ? 1 : cf_scalar_groups(a.l);
+    const void* fn = vec ? (const void*)&lncf_bwd_kernel<T, kVec<T>> : cf_scalar_fn<T, true>(K);
+    const int pw = 32 * (vec ? kVec<T> : K);
     const int64_t tiles = a.n * ((a.l + pw - 1) / pw);
     // the CTA's dw, db partial row
     const size_t smem = size_t(a.c) * 2 * sizeof(float);
