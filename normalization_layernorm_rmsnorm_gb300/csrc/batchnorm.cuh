@@ -28,8 +28,8 @@
 //   * Eval forward, 16-byte vectors (bn_fwd_eval_stream_kernel below): the
 //     output is elementwise once the running statistics fix the coefficients,
 //     so warps stream blocks of vectors through registers with a per-CTA table
-//     of (scale, shift); more than kEsMaxChannels channels take the ring
-//     kernel below.
+//     of (scale, shift) in dynamic shared memory; more than kEsMaxChannels
+//     channels take the ring kernel below.
 //   * Eval backward, 16-byte vectors (bn_bwd_eval_kernel below), and the eval
 //     forward for very many channels (bn_fwd_eval_kernel): the same rings with
 //     one pass per round, coefficients from the running statistics.
@@ -739,19 +739,20 @@ bn_fwd_eval_kernel(const BnArgs a, const BnGeom g) {
 // y = act(x*scale[c] + shift[c] (+ residual)) is elementwise once the running
 // statistics fix the coefficients, so the eval forward needs no rounds: every
 // warp takes kEsUnroll consecutive blocks of 32 vectors (loads first, then the
-// arithmetic), and a per-CTA table in shared memory holds (scale, shift) of
-// every channel.
+// arithmetic), and a per-CTA table in dynamic shared memory holds (scale,
+// shift) of every channel (8 bytes each: 128 KB at kEsMaxChannels; 64 KB for
+// 8192 channels still leaves three CTAs per SM).
 constexpr int kEsThreads = 256;
 constexpr int kEsWarps = kEsThreads / 32;
 constexpr int kEsUnroll = 4;
-constexpr int kEsMaxChannels = 4096;
+constexpr int kEsMaxChannels = 16384;
 
 template <typename T, int ACT>
 __global__ void __launch_bounds__(kEsThreads)
 bn_fwd_eval_stream_kernel(const BnArgs a, const BnGeom g, const FastDiv div_c, const uint32_t nblocks) {
     constexpr int VE = kVec<T>;
     constexpr int U = kEsUnroll;
-    __shared__ float2 coef[kEsMaxChannels];
+    extern __shared__ float2 coef[];  // [c]
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     for (int ch = threadIdx.x; ch < int(g.c); ch += kEsThreads) {
@@ -1578,7 +1579,10 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
                 return (const void*)&bn_fwd_eval_stream_kernel<T, decltype(act)::value>;
             });
             const DevInfo* d = dev_info();
-            const int occ = cached_occupancy(fn, kEsThreads, 0);
+            const size_t smem = size_t(a.c) * sizeof(float2);
+            nrm_status pst = prepare_kernel(fn, smem, false);
+            if (pst != NRM_OK) return pst;
+            const int occ = cached_occupancy(fn, kEsThreads, smem);
             if (occ < 1) return fail(NRM_ERR_CUDA, "batchnorm eval kernel cannot be resident");
             const uint64_t per_cta = uint64_t(kEsWarps) * kEsUnroll;
             uint64_t grid = (nblocks + per_cta - 1) / per_cta;
@@ -1590,7 +1594,7 @@ nrm_status bn_fwd(const BnArgs& a, bool training, bool vec, void* ws, size_t ws_
             BnArgs args = a;
             uint32_t nb = uint32_t(nblocks);
             void* kargs[] = {&args, &g, &div_c, &nb};
-            return cuda_status(cudaLaunchKernel(fn, dim3(unsigned(grid)), dim3(kEsThreads), kargs, 0, s),
+            return cuda_status(cudaLaunchKernel(fn, dim3(unsigned(grid)), dim3(kEsThreads), kargs, smem, s),
                                "batchnorm eval launch");
         }
     }

@@ -292,8 +292,8 @@ def _ln_wide(name, rows, cols, dev, f32):
 
 # Shapes that take the paths no bench workload reaches, run only by
 # profile_case for their ncu captures: rows that are not 16-byte multiples (the
-# scalar register kernels), BatchNorm eval above 4096 channels (the ring eval
-# forward), channels-first planes that are not 16-byte multiples (the register
+# scalar register kernels), BatchNorm eval with 8192 channels (a 64 KB
+# coefficient table in the streamed eval forward; the ring eval backward), channels-first planes that are not 16-byte multiples (the register
 # kernels), an unaligned activation-dropout tensor (the scalar kernel) and
 # unaligned rows too wide for the register kernels (the one-kernel wide
 # backward).
@@ -357,7 +357,7 @@ def _bn_eval_plain(name, n, c, l, dev, f32):
     sm, sr, dw, db = f32(c), f32(c), f32(c), f32(c)
     ws = nrm.batchnorm_workspace(x)
     return [
-        Call(name, "fwd", "bn_fwd_eval_kernel<f32,none>",
+        Call(name, "fwd", "bn_fwd_eval_stream_kernel<f32,none>",
              lambda: nrm.nrm_batchnorm_fwd(x, None, w, b, y, rm, rv, sm, sr, None, 1e-5, 0.1, False, "none", ws),
              nbytes(x, y, w, b, rm, rv, sm, sr), 1, [x, w, b, rm, rv], [y, sm, sr]),
         Call(name, "bwd", "bn_bwd_eval_kernel<f32,none>",

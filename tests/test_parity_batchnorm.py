@@ -77,9 +77,10 @@ def test_bn_odd_shapes(orc, dtype, shape):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_bn_eval_forward_both_paths(orc, dtype):
     # the eval forward streams through registers with a per-CTA table of up to
-    # 4096 channels' coefficients; more channels take the ring kernel.  Both,
-    # with the ReLU mask and a residual, with a ragged last block per segment
-    for n, c, l in ((3, 4096, 40), (2, 4104, 24)):
+    # 16384 channels' coefficients in dynamic shared memory (above 48 KB, 6144
+    # channels, with the opt-in size); more channels take the ring kernel.  All
+    # three, with the ReLU mask and a residual, with a ragged last block per segment
+    for n, c, l in ((3, 4096, 40), (2, 8200, 24), (2, 16400, 8)):
         cfg = synth.BnConfig("evc", n, c, l, dtype, 1e-5, 0.1, seed=640 + c % 97, act="relu",
                              residual=True, x_kind="offset_scale", w_std=0.2, b_std=0.2)
         inp = synth.bn_inputs(cfg)
