@@ -9,9 +9,10 @@
 // over its c channels, as ConvNeXt -- which the article's application
 // paragraph lists as a LayerNorm user -- normalises channels.
 //
-// Design: a CTA of 8 warps owns a tile of 32*V consecutive positions of one
-// sample (V = 16/sizeof(T) positions per thread when rows are 16-byte aligned,
-// else 1), so every load is a coalesced run of the tile in one channel plane.
+// Design: a CTA of 8 warps owns a tile of 32*V*K positions of one sample: each
+// lane K groups of V consecutive positions, 32*V apart (V = 16/sizeof(T) when
+// rows are 16-byte aligned, else 1; K > 1 only for those scalar planes), so
+// every load is a coalesced run of the tile in one channel plane.
 // Warp w takes channels w, w+8, ...; per-position statistics are merged across
 // the 8 warps in shared memory in a fixed order.  The second pass re-reads the
 // tile (L2: a CTA's tile is c*32*V elements).  The backward keeps the per-CTA
