@@ -15,7 +15,7 @@
 // every load is a coalesced run of the tile in one channel plane.
 // Warp w takes channels w, w+8, ...; per-position statistics are merged across
 // the 8 warps in shared memory in a fixed order.  The second pass re-reads the
-// tile (L2: a CTA's tile is c*32*V elements).  The backward keeps the per-CTA
+// tile (L2: a CTA's tile is c*32*V*K elements).  The backward keeps the per-CTA
 // dw/db partial row in shared memory (channel ch belongs to warp ch % 8, so
 // no atomics) and writes it to the workspace for the fixed-order column sum.
 #pragma once
