@@ -12,6 +12,8 @@ What pins what:
     to 0 and sum(dx*xhat) = rstd*sum(g*xhat)*eps/(var+eps); the RMSNorm gradient satisfies
     sum(x*dx) = inv_rms*sum(g*x)*eps/(ms+eps); the running statistics follow
     the EMA with the unbiased batch variance (numpy var with ddof=1);
+  * brute force on the smallest sizes, worked by hand: rows of one and two
+    columns, BatchNorm channels of two elements (training and eval);
   * central finite differences of L = sum(dy * y) for every backward output;
   * independent library routines: torch.nn.functional layer_norm / rms_norm /
     batch_norm / gelu / silu / mish and torch autograd, all in float64 on the CPU;
@@ -789,6 +791,123 @@ def pin_act_dropout_bwd_vs_torch(o):
         (fn(x) * keep / (1 - p)).backward(torch.from_numpy(dy))
         dx = o.act_dropout_bwd(dy, x.detach().numpy(), act, p, 999, act_param=prm)
         _close(dx, x.grad.numpy(), _torch_rtol(act, 1e-14), 1e-13, f"act {act} dx vs torch")
+
+
+def _two_point(x1, x2, eps):
+    """Standardising two values by hand: with u = (x1 - x2)/2 their biased
+    variance is u^2, so xhat1 = u/sqrt(u^2 + eps) = -xhat2, and
+    d xhat1 / d x1 = -d xhat1 / d x2 = eps / (2 (u^2 + eps)^(3/2))."""
+    u = (x1 - x2) / 2
+    return u / np.sqrt(u * u + eps), eps / (2 * (u * u + eps) ** 1.5), u
+
+
+def pin_row_norms_one_and_two_columns(o):
+    """Rows of one and two columns, worked by hand.  One column: LayerNorm's
+    xhat is 0, so y = b, dx = 0, dw = 0, db = sum(dy), rstd = 1/sqrt(eps);
+    RMSNorm's rstd is 1/sqrt(x^2 + eps) and dy/dx = w eps/(x^2 + eps)^(3/2).
+    Two columns: the two-point standardisation of _two_point, whose
+    derivative gives dx1 = -dx2 = (g1 - g2) eps/(2 (u^2 + eps)^(3/2)).
+    The gaps u are taken below, near and above sqrt(eps), so that an eps
+    placed outside the root, or a variance divided by N - 1, fails."""
+    r = _rng(45)
+    eps = 1e-2
+    rows = 5
+    # one column
+    x = r.normal(size=(rows, 1)) * 3
+    w = 1 + 0.4 * r.normal(size=1)
+    b = 0.7 * r.normal(size=1)
+    dy = r.normal(size=(rows, 1))
+    y, mean, rstd = o.layernorm_fwd(x, w, b, eps=eps)
+    _close(y, np.broadcast_to(b, (rows, 1)), 0, 1e-15, "one-column LayerNorm y = b")
+    _close(mean, x[:, 0], 0, 0, "one-column LayerNorm mean")
+    _close(rstd, np.full(rows, 1 / math.sqrt(eps)), 1e-15, 0, "one-column LayerNorm rstd")
+    dx, dw, db = o.layernorm_bwd(dy, x, w, eps=eps)
+    _close(dx, np.zeros_like(x), 0, 1e-15, "one-column LayerNorm dx = 0")
+    _close(dw, np.zeros(1), 0, 1e-15, "one-column LayerNorm dw = 0")
+    _close(db, dy.sum(0), 1e-14, 1e-15, "one-column LayerNorm db = sum dy")
+    y, rstd = o.rmsnorm_fwd(x, w, eps=eps)
+    _close(rstd, 1 / np.sqrt(x[:, 0] ** 2 + eps), 1e-14, 0, "one-column RMSNorm rstd")
+    _close(y, x * w / np.sqrt(x * x + eps), 1e-14, 0, "one-column RMSNorm y")
+    dx, dw = o.rmsnorm_bwd(dy, x, w, eps=eps)
+    _close(dx, dy * w * eps / (x * x + eps) ** 1.5, 1e-13, 1e-16, "one-column RMSNorm dx")
+    _close(dw, (dy * x / np.sqrt(x * x + eps)).sum(0), 1e-13, 1e-15, "one-column RMSNorm dw")
+    # two columns: rows of centre m and half-gap u, in both orders
+    m = r.uniform(-4, 4, size=rows)
+    u = np.array([0.03, -0.08, 0.1, 0.4, -2.5])
+    x = np.stack([m + u, m - u], axis=1)
+    w = 1 + 0.4 * r.normal(size=2)
+    b = 0.7 * r.normal(size=2)
+    dy = r.normal(size=(rows, 2))
+    xh1, dxh, _ = _two_point(x[:, 0], x[:, 1], eps)
+    xh = np.stack([xh1, -xh1], axis=1)
+    y, mean, rstd = o.layernorm_fwd(x, w, b, eps=eps)
+    _close(y, xh * w + b, 1e-13, 1e-15, "two-column LayerNorm y")
+    _close(mean, x.mean(1), 1e-15, 1e-15, "two-column LayerNorm mean")
+    dx, dw, db = o.layernorm_bwd(dy, x, w, eps=eps)
+    g = dy * w
+    d1 = (g[:, 0] - g[:, 1]) * dxh
+    _close(dx, np.stack([d1, -d1], axis=1), 1e-12, 1e-15, "two-column LayerNorm dx")
+    _close(dw, (dy * xh).sum(0), 1e-13, 1e-15, "two-column LayerNorm dw")
+    _close(db, dy.sum(0), 1e-14, 1e-15, "two-column LayerNorm db")
+
+
+def pin_batchnorm_two_element_channels(o):
+    """Channels of two elements (n = 2, l = 1 and n = 1, l = 2), worked by
+    hand.  Training: the mean is the midpoint, xhat = +-u/sqrt(u^2 + eps),
+    the running variance takes the unbiased 2u^2, and with no activation
+    dx1 = -dx2 = w (dy1 - dy2) eps/(2 (u^2 + eps)^(3/2)), dw = (dy1 - dy2) xhat1,
+    db = dy1 + dy2, dres = dy.  Eval: the running statistics replace the
+    batch ones and dx = dy w / sqrt(rv + eps)."""
+    r = _rng(46)
+    eps, mom = 1e-2, 0.2
+    c = 4
+    u = np.array([0.05, -0.1, 0.3, 1.7])
+    m = r.uniform(-3, 3, size=c)
+    w = 1 + 0.3 * r.normal(size=c)
+    b = 0.5 * r.normal(size=c)
+    rm = r.normal(size=c)
+    rv = r.uniform(0.5, 2, size=c)
+    for n, l in ((2, 1), (1, 2)):
+        pair = np.stack([m + u, m - u], axis=0)  # [2, c]: element k of each channel
+        x = pair[:, :, None] if l == 1 else pair.T[None, :, :]
+        res = r.normal(size=x.shape)
+        dy = r.normal(size=x.shape)
+        def el(t, k):  # element k of every channel of t
+            return t[k, :, 0] if l == 1 else t[0, :, k]
+        xh1, dxh, uu = _two_point(el(x, 0), el(x, 1), eps)
+        f = o.batchnorm_fwd(x, res=res, w=w, b=b, eps=eps, momentum=mom, training=True,
+                            running_mean=rm, running_var=rv)
+        xh = np.stack([xh1, -xh1], axis=0)
+        want_y = (xh * w + b)
+        want_y = want_y[:, :, None] if l == 1 else want_y.T[None, :, :]
+        _close(f["y"], want_y + res, 1e-13, 1e-15, f"BatchNorm [{n},{c},{l}] y")
+        _close(f["save_mean"], m, 1e-15, 1e-15, f"BatchNorm [{n},{c},{l}] mean")
+        _close(f["save_rstd"], 1 / np.sqrt(uu * uu + eps), 1e-14, 0, f"BatchNorm [{n},{c},{l}] rstd")
+        _close(f["running_mean"], (1 - mom) * rm + mom * m, 1e-15, 1e-15, "running mean")
+        _close(f["running_var"], (1 - mom) * rv + mom * 2 * uu * uu, 1e-14, 1e-16, "running var")
+        dx, dres, dw, db = o.batchnorm_bwd(dy, x, res=res, w=w, b=b, eps=eps, training=True)
+        dy1, dy2 = el(dy, 0), el(dy, 1)
+        d1 = w * (dy1 - dy2) * dxh
+        want_dx = np.stack([d1, -d1], axis=0)
+        want_dx = want_dx[:, :, None] if l == 1 else want_dx.T[None, :, :]
+        _close(dx, want_dx, 1e-12, 1e-15, f"BatchNorm [{n},{c},{l}] dx")
+        _close(dres, dy, 0, 0, f"BatchNorm [{n},{c},{l}] dres = dy")
+        _close(dw, (dy1 - dy2) * xh1, 1e-13, 1e-15, f"BatchNorm [{n},{c},{l}] dw")
+        _close(db, dy1 + dy2, 1e-14, 1e-15, f"BatchNorm [{n},{c},{l}] db")
+        # eval: the running statistics, untouched
+        f = o.batchnorm_fwd(x, w=w, b=b, eps=eps, momentum=mom, training=False,
+                            running_mean=rm, running_var=rv)
+        k = 1 / np.sqrt(rv + eps)
+        _close(f["y"], (x - rm[None, :, None]) * (k * w)[None, :, None] + b[None, :, None], 1e-14, 1e-15,
+               f"BatchNorm [{n},{c},{l}] eval y")
+        _close(f["running_mean"], rm, 0, 0, "eval leaves running mean")
+        _close(f["running_var"], rv, 0, 0, "eval leaves running var")
+        dx, _, dw, db = o.batchnorm_bwd(dy, x, w=w, b=b, running_mean=rm, running_var=rv, eps=eps,
+                                        training=False)
+        _close(dx, dy * (k * w)[None, :, None], 1e-14, 1e-16, f"BatchNorm [{n},{c},{l}] eval dx")
+        _close(dw, (dy * (x - rm[None, :, None]) * k[None, :, None]).sum(axis=(0, 2)), 1e-13, 1e-15,
+               f"BatchNorm [{n},{c},{l}] eval dw")
+        _close(db, dy.sum(axis=(0, 2)), 1e-14, 1e-15, f"BatchNorm [{n},{c},{l}] eval db")
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
