@@ -16,6 +16,20 @@ MUTATIONS = {
                              "double var = ssd / (double)(cols - 1);"),
     "ln_eps_outside_root": ("double rs = 1.0 / sqrt(var + eps);",
                             "double rs = 1.0 / (sqrt(var) + eps);"),
+    "ln_bwd_eps_outside_root": ("double rs = 1.0 / sqrt(ssd / (double)cols + eps);",
+                                "double rs = 1.0 / (sqrt(ssd / (double)cols) + eps);"),
+    "ln_bwd_unbiased_variance": ("double rs = 1.0 / sqrt(ssd / (double)cols + eps);",
+                                 "double rs = 1.0 / sqrt(ssd / (double)(cols - 1) + eps);"),
+    "rms_fwd_eps_outside_root": (
+        "double rr = 1.0 / sqrt(ss / (double)cols + eps);\n        for (int64_t j = 0; j < cols; ++j)\n            y[",
+        "double rr = 1.0 / (sqrt(ss / (double)cols) + eps);\n        for (int64_t j = 0; j < cols; ++j)\n            y["),
+    "rms_bwd_eps_outside_root": ("double rr = 1.0 / sqrt(ss / (double)cols + eps);\n\n        double s = 0.0;",
+                                 "double rr = 1.0 / (sqrt(ss / (double)cols) + eps);\n\n        double s = 0.0;"),
+    "bn_fwd_eps_outside_root": ("rs = 1.0 / sqrt(var_biased + eps);", "rs = 1.0 / (sqrt(var_biased) + eps);"),
+    "bn_bwd_eps_outside_root": ("rs = 1.0 / sqrt(ssd / (double)m + eps);",
+                                "rs = 1.0 / (sqrt(ssd / (double)m) + eps);"),
+    "bn_eval_fwd_drops_eps": ("rs = 1.0 / sqrt(running_var[ch] + eps);\n        }\n        if (save_mean)",
+                              "rs = 1.0 / sqrt(running_var[ch]);\n        }\n        if (save_mean)"),
     "ln_bwd_drops_xhat_term": ("- xhat * sum_gxhat / (double)cols);", ");"),
     "ln_bwd_mean_term_divisor": ("rs * (g - sum_g / (double)cols",
                                  "rs * (g - sum_g / (double)(cols - 1)"),
