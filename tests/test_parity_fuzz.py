@@ -1,9 +1,10 @@
 """Seeded random shapes through libnorm's C ABI against the CPU oracle, element
 by element, beside the hand-picked shapes of the other parity tests: row norms
 with widths from 1 to 70000 (every kernel family: register, ring, wide,
-scalar), BatchNorm with every activation, residual and mask choice in both
-modes, channels-first LayerNorm, and the activation with fused dropout at any
-length, probability and pointer offset.  Each case draws its parameters from
+scalar), also with float32 output and RMSNorm with a bias; BatchNorm with
+every activation, residual and mask choice in both modes; channels-first
+LayerNorm; and the activation with fused dropout at any length, probability
+and pointer offset.  Each case draws its parameters from
 its own seed, so a failure names a reproducible case; the comparisons and
 their tolerances are those of the other parity tests."""
 import math
@@ -17,6 +18,7 @@ from normalization_layernorm_rmsnorm_gb300 import synth
 from parity_util import compare_bn, compare_row, oracle_bn, oracle_row, run_bn, run_row
 import test_parity_dropout as drop
 import test_parity_layernorm_cf as cf
+import test_parity_rownorm as rn
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +56,26 @@ def test_fuzz_row_norms(orc, case):
     got = run_row(kind, inp, dtype, eps, with_w=affine, with_b=affine, want_dw=affine, want_db=affine)
     want = oracle_row(orc, kind, inp, eps, with_w=affine, with_b=affine)
     compare_row(got, want, dtype, f"fuzz {case}: {kind} {dtype} [{rows},{cols}] affine={affine} eps={eps}")
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_fuzz_row_f32_output(orc, case):
+    # a 16-bit x with y and dy in float32 (the _ex entry points)
+    r = np.random.default_rng(7500 + case)
+    kind = ("layernorm", "rmsnorm")[case % 2]
+    dtype = ("f16", "bf16")[(case // 2) % 2]
+    cols = _log_uniform(r, 1, 70000)
+    rows = _log_uniform(r, 1, max(1, min(20000, MAX_ELEMS // cols)))
+    rn.check_f32_output(orc, kind, dtype, rows, cols, 7500 + case)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_fuzz_rmsnorm_bias(orc, case):
+    r = np.random.default_rng(7600 + case)
+    dtype = DTYPES[case % 3]
+    cols = _log_uniform(r, 1, 70000)
+    rows = _log_uniform(r, 1, max(1, min(20000, MAX_ELEMS // cols)))
+    rn.check_rmsnorm_bias(orc, dtype, rows, cols, 7600 + case)
 
 
 @pytest.mark.parametrize("case", range(48))

@@ -163,7 +163,11 @@ def test_rmsnorm_with_bias(orc, dtype, shape):
     # the ring backward (aligned rows), the register kernels (1023 columns are
     # not 16-byte rows), the wide-row kernels (40000 columns)
     rows, cols = shape
-    seed = 60 + cols % 97
+    check_rmsnorm_bias(orc, dtype, rows, cols, 60 + cols % 97)
+
+
+def check_rmsnorm_bias(orc, dtype, rows, cols, seed):
+    """RMSNorm with its optional bias, forward and backward (db), against the oracle."""
     inp = {
         "x": synth.random_tensor(seed, 1, (rows, cols), dtype, std=1.3),
         "w": synth.store(1 + 0.1 * synth.normal(seed, 2, cols), dtype, (cols,)),
@@ -183,10 +187,13 @@ F32OUT = [(300, 768), (97, 1023), (64, 4096), (5, 40000), (25216, 768)]  # the l
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("shape", F32OUT, ids=[f"{r}x{c}" for r, c in F32OUT])
 def test_row_f32_output(orc, kind, dtype, shape):
-    # the autocast_to_fp32-style option: a 16-bit x, y (and so dy) in float32;
-    # y meets the fp32 bound, dx/dw/db (stored 16-bit) the 16-bit one
     rows, cols = shape
-    seed = 80 + cols % 91
+    check_f32_output(orc, kind, dtype, rows, cols, 80 + cols % 91)
+
+
+def check_f32_output(orc, kind, dtype, rows, cols, seed):
+    """The autocast_to_fp32-style option: a 16-bit x, y (and so dy) in float32;
+    y meets the fp32 bound, dx/dw/db (stored 16-bit) the 16-bit one."""
     x = synth.random_tensor(seed, 1, (rows, cols), dtype, mean=0.2, std=1.3)
     w = synth.store(1 + 0.1 * synth.normal(seed, 2, cols), dtype, (cols,))
     b = synth.store(0.1 * synth.normal(seed, 3, cols), dtype, (cols,))
